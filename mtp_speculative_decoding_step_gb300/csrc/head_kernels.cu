@@ -1,0 +1,515 @@
+// MTP drafter head kernels for sm_103a: the batch-1..8 GEMV family (fc, QKV,
+// o_proj, gate/up, down, lm_head) with fused RMSNorm prologues and residual /
+// SwiGLU / logits+argmax epilogues, the per-head q/k norm + RoPE + KV append,
+// and split-slot decode attention.
+//
+// The head's forward is the one given on the "support the qwen3_5_mtp
+// drafter" issue page, section "Upstream contract to port":
+//   h = fc(concat(pre_fc_norm_embedding(embed(tok)), pre_fc_norm_hidden(hidden)))
+// followed by one full-attention decoder layer and the final norm, with the
+// target's tied lm_head borrowed for the logits.
+//
+// All of it is HBM-bound at these batch widths: every kernel streams its
+// weight matrix exactly once with 16-byte L1-bypassing loads, keeps the
+// activations (fp32) in shared memory and accumulates in fp32.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtp {
+
+// ---------------------------------------------------------------- GEMV
+
+template <typename WT>
+struct Vec;
+template <>
+struct Vec<uint16_t> {  // 8 bf16 per 16-byte vector
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& w, float* f) {
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
+    f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
+    f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+  }
+};
+template <>
+struct Vec<float> {  // 4 fp32 per 16-byte vector
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& w, float* f) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+  }
+};
+
+template <typename WT, int MT, int RPW>
+__device__ __forceinline__ void gemv_fma(float (&acc)[RPW][MT], const uint4 (&w)[RPW], const float* xs,
+                                         int KS, int kb) {
+  constexpr int VN = Vec<WT>::N;
+  float xv[MT][VN];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const float4* p = reinterpret_cast<const float4*>(xs + m * KS + kb);
+#pragma unroll
+    for (int j = 0; j < VN / 4; ++j) {
+      float4 t = p[j];
+      xv[m][4 * j] = t.x; xv[m][4 * j + 1] = t.y; xv[m][4 * j + 2] = t.z; xv[m][4 * j + 3] = t.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    float wf[VN];
+    Vec<WT>::unpack(w[i], wf);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float a = acc[i][m];
+#pragma unroll
+      for (int j = 0; j < VN; ++j) a = fmaf(wf[j], xv[m][j], a);
+      acc[i][m] = a;
+    }
+  }
+}
+
+// Stage x[m][k0 .. k0+KS) (fp32) into shared memory, applying the prologue.
+template <int MT>
+__device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, float* red) {
+  const int tid = threadIdx.x;
+  if (a.pro == PRO_DUAL) {
+    // x = [norm_e(E[tok]) ; norm_h(hidden)]; this block's slice lies in one half.
+    const int H = a.K / 2;
+    const bool emb = k0 < H;
+    const float* nw = emb ? a.nw : a.nw2;
+    const int kk0 = emb ? k0 : k0 - H;
+    for (int m = 0; m < a.M; ++m) {
+      const void* src = emb ? a.E : a.hid;
+      const int dt = emb ? a.wdt : a.hid_dt;
+      int t = emb ? a.tok[a.tok_idx[m]] : 0;
+      if (t < 0 || t >= a.vocab) {  // a bad token id reads row 0 and raises the status word
+        if (tid == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+        t = 0;
+      }
+      const size_t base = emb ? (size_t)t * (size_t)H : (size_t)a.hid_off[m];
+      float ss = 0.f;
+      for (int k = tid; k < H; k += blockDim.x) {
+        float v = load_elem(src, dt, base + k);
+        ss = fmaf(v, v, ss);
+      }
+      ss = block_sum(ss, red);
+      const float inv = rsqrtf(ss / (float)H + a.eps);
+      for (int k = tid; k < KS; k += blockDim.x)
+        xs[m * KS + k] = load_elem(src, dt, base + kk0 + k) * inv * nw[kk0 + k];
+    }
+  } else {
+    for (int m = 0; m < a.M; ++m) {
+      const float* xm = a.x + (size_t)m * a.ldx;
+      float inv = 1.f;
+      if (a.pro == PRO_NORM) {
+        float ss = 0.f;
+        for (int k = tid; k < a.K; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
+        ss = block_sum(ss, red);
+        inv = rsqrtf(ss / (float)a.K + a.eps);
+        for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = xm[k0 + k] * inv * a.nw[k0 + k];
+      } else {
+        for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = xm[k0 + k];
+      }
+    }
+  }
+  for (int m = a.M; m < MT; ++m)
+    for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
+}
+
+template <typename WT, int MT>
+__global__ void __launch_bounds__(256) k_gemv(const __grid_constant__ GemvArgs a) {
+  constexpr int VN = Vec<WT>::N;
+  constexpr int RPW = MT <= 2 ? 8 : (MT == 4 ? 4 : 2);
+  constexpr int ROWS = 8 * RPW;
+  extern __shared__ __align__(16) float xs[];
+  __shared__ float s_out[MT][ROWS];
+  __shared__ float s_red[32];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = blockIdx.x / a.S, split = blockIdx.x - group * a.S;
+  const int KS = a.K / a.S, k0 = split * KS;
+
+  gemv_prologue<MT>(a, xs, k0, KS, s_red);
+  __syncthreads();
+
+  // This warp's RPW consecutive physical rows.
+  const int l0 = warp * RPW;
+  const WT* W;
+  if (a.epi == EPI_SWIGLU) {
+    constexpr int HALF = ROWS / 2;
+    const int prow = group * HALF + (l0 % HALF);
+    W = reinterpret_cast<const WT*>(a.w[l0 < HALF ? 0 : 1]) + (size_t)prow * a.K;
+  } else {
+    const int v = group * ROWS + l0;
+    int s = 0, start = 0;
+    while (v >= a.seg_end[s]) { start = a.seg_end[s]; ++s; }
+    W = reinterpret_cast<const WT*>(a.w[s]) + (size_t)(v - start) * a.K;
+  }
+  W += k0;
+
+  float acc[RPW][MT];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
+
+  const int nvec = KS / VN;
+  for (int v0 = lane; v0 < nvec; v0 += 64) {
+    const bool has1 = v0 + 32 < nvec;
+    uint4 w0[RPW], w1[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
+    if (has1) {
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) w1[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
+    }
+    gemv_fma<WT, MT, RPW>(acc, w0, xs, KS, v0 * VN);
+    if (has1) gemv_fma<WT, MT, RPW>(acc, w1, xs, KS, (v0 + 32) * VN);
+  }
+
+#pragma unroll
+  for (int i = 0; i < RPW; ++i)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[i][m] = warp_sum(acc[i][m]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) s_out[m][l0 + i] = acc[i][m];
+  }
+  __syncthreads();
+
+  // Deterministic split-K: every split stores its partial; the last block of
+  // the group sums them in split order.
+  if (a.S > 1) {
+    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+      const int m = t / ROWS, l = t - m * ROWS;
+      a.part[((size_t)split * MT + m) * a.N + (size_t)group * ROWS + l] = s_out[m][l];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&a.counters[group], 1) == a.S - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+      const int m = t / ROWS, l = t - m * ROWS;
+      float sum = 0.f;
+      for (int s = 0; s < a.S; ++s) sum += __ldcg(&a.part[((size_t)s * MT + m) * a.N + (size_t)group * ROWS + l]);
+      s_out[m][l] = sum;
+    }
+    if (tid == 0) a.counters[group] = 0;
+    __syncthreads();
+  }
+
+  if (a.epi == EPI_SWIGLU) {
+    constexpr int HALF = ROWS / 2;
+    for (int t = tid; t < a.M * HALF; t += blockDim.x) {
+      const int m = t / HALF, l = t - m * HALF;
+      const float g = s_out[m][l], u = s_out[m][l + HALF];
+      a.y[(size_t)m * a.ldy + (size_t)group * HALF + l] = g / (1.f + expf(-g)) * u;
+    }
+    return;
+  }
+  for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+    const int m = t / ROWS, l = t - m * ROWS;
+    const size_t n = (size_t)group * ROWS + l;
+    float v = s_out[m][l];
+    if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + n];
+    a.y[(size_t)m * a.ldy + n] = v;
+    if (a.epi == EPI_LOGITS && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
+  }
+  if (a.epi != EPI_LOGITS) return;
+
+  // Group argmax (value desc, id asc) per item, then the last group block
+  // reduces all groups into the token.
+  if (warp < a.M) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int l = lane; l < ROWS; l += 32) {
+      const float v = s_out[warp][l];
+      const int i = group * ROWS + l;
+      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      a.gmax[(size_t)warp * a.ngroups + group] = bv;
+      a.gidx[(size_t)warp * a.ngroups + group] = bi;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.done, 1) == a.ngroups - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < a.M) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int g = lane; g < a.ngroups; g += 32) {
+      const float v = __ldcg(&a.gmax[(size_t)warp * a.ngroups + g]);
+      const int i = __ldcg(&a.gidx[(size_t)warp * a.ngroups + g]);
+      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[warp]] = bi;
+  }
+  if (tid == 0) *a.done = 0;
+}
+
+template <typename WT, int MT>
+static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
+  auto k = k_gemv<WT, MT>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  k<<<a.ngroups * a.S, 256, smem, s>>>(a);
+}
+
+void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
+  const bool bf = a.wdt == MTP_DTYPE_BF16;
+  switch (mt) {
+    case 1: bf ? launch_gemv_t<uint16_t, 1>(a, smem, s) : launch_gemv_t<float, 1>(a, smem, s); break;
+    case 2: bf ? launch_gemv_t<uint16_t, 2>(a, smem, s) : launch_gemv_t<float, 2>(a, smem, s); break;
+    case 4: bf ? launch_gemv_t<uint16_t, 4>(a, smem, s) : launch_gemv_t<float, 4>(a, smem, s); break;
+    default: bf ? launch_gemv_t<uint16_t, 8>(a, smem, s) : launch_gemv_t<float, 8>(a, smem, s); break;
+  }
+}
+
+// ------------------------------------------------- q/k norm, RoPE, KV append
+
+// Rotate the pair (x0 at i, x1 at i + dh/2) to position `pos`:
+// angle = pos * theta^(-2i/dh), evaluated in double.
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int dh, int pos, float theta) {
+  const double inv = pow((double)theta, -2.0 * (double)i / (double)dh);
+  double sn, cs;
+  sincos((double)pos * inv, &sn, &cs);
+  const float c = (float)cs, s = (float)sn;
+  const float y0 = x0 * c - x1 * s;
+  const float y1 = x1 * c + x0 * s;
+  x0 = y0;
+  x1 = y1;
+}
+
+// grid (M, nq + nkv), block dh/2 threads: thread i owns the pair (i, i + dh/2).
+__global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
+  __shared__ float red[32];
+  const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.dh / 2;
+  const int qw = a.nq * a.dh, kw = a.nkv * a.dh;
+  const float* src = a.qkv + (size_t)m * (qw + 2 * kw);
+  const int slot = a.slot[m], row = a.row[m];
+  if (h < a.nq) {
+    const int qd = a.qdst[m];
+    if (qd < 0) return;  // uniform across the block
+    float x0 = src[h * a.dh + i], x1 = src[h * a.dh + i + half];
+    const float ss = block_sum(x0 * x0 + x1 * x1, red);
+    const float inv = rsqrtf(ss / (float)a.dh + a.eps);
+    x0 = x0 * inv * a.wq[i];
+    x1 = x1 * inv * a.wq[i + half];
+    rope_pair(x0, x1, i, a.dh, slot, a.theta);
+    float* dst = a.q_out + (size_t)qd * qw + h * a.dh;
+    dst[i] = x0;
+    dst[i + half] = x1;
+  } else {
+    const int g = h - a.nq;
+    float x0 = src[qw + g * a.dh + i], x1 = src[qw + g * a.dh + i + half];
+    const float ss = block_sum(x0 * x0 + x1 * x1, red);
+    const float inv = rsqrtf(ss / (float)a.dh + a.eps);
+    x0 = x0 * inv * a.wk[i];
+    x1 = x1 * inv * a.wk[i + half];
+    rope_pair(x0, x1, i, a.dh, slot, a.theta);
+    const size_t off = (((size_t)row * a.nkv + g) * a.cap + slot) * a.dh;
+    store_elem(a.kc, a.wdt, off + i, x0);
+    store_elem(a.kc, a.wdt, off + i + half, x1);
+    const float* vs = src + qw + kw + g * a.dh;
+    store_elem(a.vc, a.wdt, off + i, vs[i]);
+    store_elem(a.vc, a.wdt, off + i + half, vs[i + half]);
+  }
+}
+
+void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
+  dim3 grid(a.M, a.nq + a.nkv);
+  k_qkv_post<<<grid, a.dh / 2, 0, s>>>(a);
+}
+
+// ------------------------------------------------------- decode attention
+
+// One block per (chunk of kAttnChunk slots, kv head, head item). The G query
+// heads of the group share each key/value row read. Partials (o, max, sum)
+// are merged by k_attn_merge.
+template <int DH, int G>
+__global__ void __launch_bounds__(128) k_attn_chunk(const __grid_constant__ AttnArgs a) {
+  constexpr int EPL = DH / 32;  // elements per lane of one key row
+  __shared__ __align__(16) float qs[G][DH];
+  __shared__ float sc[G][kAttnChunk];
+  const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
+  const int L = a.slot[m] + 1;
+  const int t0 = c * kAttnChunk;
+  if (t0 >= L) return;
+  const int n = min(kAttnChunk, L - t0);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* qg = a.q + (size_t)m * a.nq * DH + (size_t)g * G * DH;
+  for (int t = tid; t < G * DH; t += 128) qs[t / DH][t % DH] = qg[t];
+  __syncthreads();
+
+  const size_t base = (((size_t)a.row[m] * a.nkv + g) * a.cap + t0) * DH;
+  for (int j = warp; j < n; j += 4) {
+    float kv[EPL];
+    const size_t off = base + (size_t)j * DH + lane * EPL;
+    if (a.wdt == MTP_DTYPE_BF16) {
+      const uint16_t* kp = reinterpret_cast<const uint16_t*>(a.kc) + off;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) kv[e] = bf16_to_f(kp[e]);
+    } else {
+      const float* kp = reinterpret_cast<const float*>(a.kc) + off;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) kv[e] = kp[e];
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float d = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) d = fmaf(qs[h][lane * EPL + e], kv[e], d);
+      d = warp_sum(d);
+      if (lane == 0) sc[h][j] = d * a.scale;
+    }
+  }
+  __syncthreads();
+  // chunk softmax statistics per head
+  __shared__ float smax[G], ssum[G];
+  for (int h = warp; h < G; h += 4) {
+    float mx = -INFINITY;
+    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[h][j]);
+    mx = warp_max(mx);
+    float sum = 0.f;
+    for (int j = lane; j < n; j += 32) {
+      const float e = expf(sc[h][j] - mx);
+      sc[h][j] = e;
+      sum += e;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) { smax[h] = mx; ssum[h] = sum; }
+  }
+  __syncthreads();
+  for (int d = tid; d < DH; d += 128) {
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const float v = load_elem(a.vc, a.wdt, base + (size_t)j * DH + d);
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(sc[h][j], v, acc[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const size_t hq = (size_t)m * a.nq + g * G + h;
+      a.po[(hq * a.max_chunks + c) * DH + d] = acc[h];
+    }
+  }
+  if (tid < G) {
+    const size_t hq = (size_t)m * a.nq + g * G + tid;
+    a.pml[(hq * a.max_chunks + c) * 2 + 0] = smax[tid];
+    a.pml[(hq * a.max_chunks + c) * 2 + 1] = ssum[tid];
+  }
+}
+
+// grid (nq, Mh), block DH threads: merge the chunk partials of one query head.
+template <int DH>
+__global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
+  const int h = blockIdx.x, m = blockIdx.y, d = threadIdx.x;
+  const int L = a.slot[m] + 1;
+  const int nch = (L + kAttnChunk - 1) / kAttnChunk;
+  const size_t hq = (size_t)m * a.nq + h;
+  const float* ml = a.pml + hq * a.max_chunks * 2;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[2 * c]);
+  float den = 0.f, num = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float w = expf(ml[2 * c] - M);
+    den = fmaf(ml[2 * c + 1], w, den);
+    num = fmaf(a.po[(hq * a.max_chunks + c) * DH + d], w, num);
+  }
+  a.o[(size_t)m * a.nq * DH + (size_t)h * DH + d] = num / den;
+}
+
+template <int DH, int G>
+static void attn_t(const AttnArgs& a, int nch, cudaStream_t s) {
+  k_attn_chunk<DH, G><<<dim3(nch, a.nkv, a.Mh), 128, 0, s>>>(a);
+  k_attn_merge<DH><<<dim3(a.nq, a.Mh), DH, 0, s>>>(a);
+}
+
+void launch_attention(const AttnArgs& a, cudaStream_t s) {
+  int maxL = 0;
+  for (int m = 0; m < a.Mh; ++m) maxL = a.slot[m] + 1 > maxL ? a.slot[m] + 1 : maxL;
+  const int nch = (maxL + kAttnChunk - 1) / kAttnChunk;
+  const int G = a.nq / a.nkv;
+#define MTP_ATTN_CASE(DHV, GV) \
+  if (a.dh == DHV && G == GV) { attn_t<DHV, GV>(a, nch, s); return; }
+  MTP_ATTN_CASE(256, 6)
+  MTP_ATTN_CASE(256, 1)
+  MTP_ATTN_CASE(256, 2)
+  MTP_ATTN_CASE(256, 4)
+  MTP_ATTN_CASE(256, 8)
+  MTP_ATTN_CASE(128, 1)
+  MTP_ATTN_CASE(128, 2)
+  MTP_ATTN_CASE(128, 4)
+  MTP_ATTN_CASE(128, 6)
+  MTP_ATTN_CASE(128, 8)
+  MTP_ATTN_CASE(64, 1)
+  MTP_ATTN_CASE(64, 2)
+  MTP_ATTN_CASE(64, 4)
+  MTP_ATTN_CASE(64, 8)
+#undef MTP_ATTN_CASE
+}
+
+// ------------------------------------------------------------ small kernels
+
+__global__ void k_norm_copy(const void* src, int dt, int n, float shift, float* dst) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = load_elem(src, dt, i) + shift;
+}
+
+void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, cudaStream_t s) {
+  k_norm_copy<<<(n + 255) / 256, 256, 0, s>>>(src, dt, n, shift, dst);
+}
+
+// grid (rows, nkv): set lengths, trim target lengths, zero dropped slots.
+__global__ void k_rollback(const __grid_constant__ RollbackArgs a) {
+  const int r = blockIdx.x, g = blockIdx.y;
+  if (a.keep[r] < 0) return;
+  if (g == 0 && threadIdx.x == 0) {
+    a.len[r] = a.keep[r];
+    if (a.target_len && a.n_acc) a.target_len[r] -= a.block - (a.n_acc[r] + 1);
+  }
+  if (!a.zero_tail || a.old_len[r] <= a.keep[r]) return;
+  const size_t off = (((size_t)r * a.nkv + g) * a.cap + a.keep[r]) * a.dh * a.esize;
+  const size_t bytes = (size_t)(a.old_len[r] - a.keep[r]) * a.dh * a.esize;
+  unsigned char* kp = reinterpret_cast<unsigned char*>(a.kc) + off;
+  unsigned char* vp = reinterpret_cast<unsigned char*>(a.vc) + off;
+  for (size_t b = threadIdx.x; b < bytes; b += blockDim.x) { kp[b] = 0; vp[b] = 0; }
+}
+
+void launch_rollback(const RollbackArgs& a, cudaStream_t s) {
+  k_rollback<<<dim3(a.rows, a.nkv), 256, 0, s>>>(a);
+}
+
+struct LenArgs {
+  int32_t* len;
+  int rows;
+  int v[kMaxRows];
+};
+__global__ void k_set_len(const __grid_constant__ LenArgs a) {
+  const int r = threadIdx.x;
+  if (r < a.rows) a.len[r] = a.v[r];
+}
+
+void launch_set_len(int32_t* len, int rows, const int* h_len, cudaStream_t s) {
+  LenArgs a;
+  a.len = len;
+  a.rows = rows;
+  for (int r = 0; r < rows; ++r) a.v[r] = h_len[r];
+  k_set_len<<<1, kMaxRows, 0, s>>>(a);
+}
+
+}  // namespace mtp

@@ -1,0 +1,158 @@
+// Internal launch interface between the C ABI (mtp_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtp.h"
+
+namespace mtp {
+
+constexpr int kMaxItems = 256;   // pairs per head call (the pages' flush cap)
+constexpr int kMaxRows = 64;
+constexpr int kAttnChunk = 64;   // KV slots per decode-attention block
+constexpr int kClusterCTAs = 8;  // CTAs per sampling cluster
+
+enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_DUAL = 2 };
+enum { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+// y[m][n] = sum_k W[n][k] x[m][k] over a virtual row space (several weight
+// segments, or gate/up halves), batch of M <= MT items, fp32 accumulate.
+struct GemvArgs {
+  const void* w[3];
+  int seg_end[3];
+  int N, K, S, ngroups;
+  int pro, epi, M, wdt;
+  const float* x;
+  long long ldx;
+  const float* nw;
+  const float* nw2;
+  float eps;
+  const void* E;
+  int vocab;
+  const int32_t* tok;
+  int tok_idx[8];
+  const void* hid;
+  long long hid_off[8];
+  int hid_dt;
+  float* y;
+  long long ldy;
+  const float* resid;
+  long long ldr;
+  float* part;
+  int* counters;
+  float* gmax;
+  int* gidx;
+  int* done;
+  int32_t* amax_out;
+  int amax_idx[8];
+  int32_t* status;
+};
+
+// rows per block group for a batch width MT
+inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 2 ? 8 : (mt == 4 ? 4 : 2)); }
+void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
+
+// Per-item per-head q_norm / k_norm + RoPE + KV append.
+struct QkvPostArgs {
+  const float* qkv;      // [M][qw + 2 kw]
+  int M, nq, nkv, dh, wdt;
+  float eps, theta;
+  const float* wq;
+  const float* wk;
+  float* q_out;          // [n_head][qw] for items with qdst >= 0
+  void* kc;
+  void* vc;
+  long long cap;
+  int row[kMaxItems];
+  int slot[kMaxItems];
+  short qdst[kMaxItems];
+};
+void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s);
+
+// Decode attention of the head items over slots 0..slot (split over chunks).
+struct AttnArgs {
+  const float* q;        // [Mh][nq*dh]
+  const void* kc;
+  const void* vc;
+  long long cap;
+  int Mh, nq, nkv, dh, wdt, max_chunks;
+  float scale;
+  float* po;             // [Mh][nq][max_chunks][dh]
+  float* pml;            // [Mh][nq][max_chunks][2]
+  float* o;              // [Mh][nq*dh]
+  int row[kMaxRows];
+  int slot[kMaxRows];
+};
+void launch_attention(const AttnArgs& a, cudaStream_t s);
+
+// Copy a norm vector to fp32 adding `shift`.
+void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, cudaStream_t s);
+
+// Set device lengths, trim target lengths, zero dropped draft slots.
+struct RollbackArgs {
+  int32_t* len;
+  int rows;
+  int keep[kMaxRows];
+  int old_len[kMaxRows];
+  int zero_tail;
+  void* kc;
+  void* vc;
+  long long cap;
+  int nkv, dh, esize;
+  const int32_t* n_acc;
+  int32_t* target_len;
+  int block;
+};
+void launch_rollback(const RollbackArgs& a, cudaStream_t s);
+void launch_set_len(int32_t* len, int rows, const int* h_len, cudaStream_t s);
+
+// ---------------------------------------------------------------- sampling
+struct RowParams {
+  float temperature, rep_penalty, top_p, min_p;
+  int top_k, greedy;
+};
+
+// Transform descriptor of one (row, position): enough to evaluate p(v) at any v.
+struct TDesc {
+  float m;          // max transformed logit
+  float S;          // normaliser of the kept set
+  uint32_t k_key;   // top-k prefix bound on the descending key
+  int k_cut;        // id bound among keys equal to k_key
+  uint32_t p_key;   // top-p prefix bound
+  int p_cut;
+  int argmax;       // argmax of the penalised logits
+  int kept;         // support size
+};
+
+struct SampleArgs {
+  int mode;                  // 0 = draft step, 1 = verify descriptors
+  int rows, V, W, depth, pos;  // pos: draft step index k-1 (draft mode)
+  const float* logits;       // draft: [rows][ld] ; verify: [rows][depth+1][V]
+  long long ld;
+  const int32_t* hist;       // [rows][W]
+  const int32_t* drafts;     // [rows][depth]
+  const float* u;            // draft: [rows][depth]
+  float* q;                  // draft: [rows][depth][V]
+  int32_t* draft_out;        // draft: [rows][depth]
+  TDesc* desc;               // verify: [rows][depth+1]
+  int32_t* status;
+  RowParams p[kMaxRows];
+};
+void launch_sample(const SampleArgs& a, cudaStream_t s);
+
+struct VerifyArgs {
+  int rows, V, W, depth;
+  const float* logits;
+  const int32_t* drafts;
+  const float* q;
+  const int32_t* hist;
+  const float* u;
+  const TDesc* desc;
+  int32_t* n_acc;
+  int32_t* out_tok;
+  int32_t* stats;
+  RowParams p[kMaxRows];
+};
+void launch_verify(const VerifyArgs& a, cudaStream_t s);
+
+}  // namespace mtp

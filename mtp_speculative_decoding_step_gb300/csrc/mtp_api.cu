@@ -1,0 +1,802 @@
+// C ABI of the MTP speculative-decoding step: validation, the head handle,
+// and the launch sequence of one head call. See include/mtp.h for the
+// contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mtp.h"
+#include "kernels.h"
+
+using namespace mtp;
+
+namespace {
+
+// The fifteen tensors of the published head ("support the qwen3_5_mtp
+// drafter" issue, "Where the MTP weights actually live").
+enum TensorId {
+  T_FC, T_NORM, T_PRE_E, T_PRE_H, T_IN, T_POST, T_GATE, T_UP, T_DOWN, T_Q, T_K, T_V, T_O, T_QN, T_KN, T_COUNT
+};
+const char* kNames[T_COUNT] = {
+    "fc.weight",
+    "norm.weight",
+    "pre_fc_norm_embedding.weight",
+    "pre_fc_norm_hidden.weight",
+    "layers.0.input_layernorm.weight",
+    "layers.0.post_attention_layernorm.weight",
+    "layers.0.mlp.gate_proj.weight",
+    "layers.0.mlp.up_proj.weight",
+    "layers.0.mlp.down_proj.weight",
+    "layers.0.self_attn.q_proj.weight",
+    "layers.0.self_attn.k_proj.weight",
+    "layers.0.self_attn.v_proj.weight",
+    "layers.0.self_attn.o_proj.weight",
+    "layers.0.self_attn.q_norm.weight",
+    "layers.0.self_attn.k_norm.weight",
+};
+
+// Norm weights that take +1.0 in the raw-HF layout ("Upstream contract to
+// port", sanitize paragraph: seven suffixes).
+const char* kShiftSuffixes[7] = {
+    ".input_layernorm.weight", ".post_attention_layernorm.weight", ".q_norm.weight", ".k_norm.weight",
+    "norm.weight",             "pre_fc_norm_embedding.weight",    "pre_fc_norm_hidden.weight",
+};
+
+bool ends_with(const std::string& s, const char* suf) {
+  const size_t n = std::strlen(suf);
+  return s.size() >= n && s.compare(s.size() - n, n, suf) == 0;
+}
+
+enum ProfKind {
+  PK_FC, PK_QKV, PK_QKV_POST, PK_ATTN, PK_O, PK_GATEUP, PK_DOWN, PK_LMHEAD, PK_SAMPLE, PK_FLUSH_FC, PK_FLUSH_KV,
+  PK_ROLLBACK, PK_COUNT
+};
+const char* kProfNames[PK_COUNT] = {"fc",      "qkv",    "qkv_post", "attention", "o_proj",   "gate_up",
+                                    "down",    "lm_head", "sample",  "flush_fc",  "flush_kv", "rollback"};
+
+struct GemvPlan {
+  int mt, S, ngroups, smem;
+};
+
+}  // namespace
+
+struct mtp_handle {
+  mtp_config cfg;
+  std::string arch;
+  int sms = 0;
+  const void* w[T_COUNT] = {};
+  const void* embed = nullptr;
+  const void* lm = nullptr;
+  mtp_kv kv{};
+  float* norms = nullptr;
+  float* nrm[T_COUNT] = {};
+  // scratch
+  float *h0 = nullptr, *qkv = nullptr, *qrot = nullptr, *o = nullptr, *h1 = nullptr, *mlp = nullptr,
+        *h2 = nullptr, *logits = nullptr, *po = nullptr, *pml = nullptr, *part = nullptr, *gmax = nullptr;
+  int *gidx = nullptr, *counters = nullptr, *done = nullptr;
+  int32_t* status = nullptr;
+  size_t part_floats = 0;
+  int max_chunks = 0, lm_groups_max = 0, counters_n = 0;
+  std::vector<void*> allocs;
+  // host mirror of the row lengths
+  std::vector<int> len, keep, drafted_len;
+  // profiling
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  struct Rec { int kind; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  size_t ev_next = 0;
+};
+
+namespace {
+
+mtp_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA; }
+
+template <typename T>
+mtp_status alloc(mtp_handle* h, T** p, size_t n) {
+  void* q = nullptr;
+  if (n == 0) n = 1;
+  if (cudaMalloc(&q, n * sizeof(T)) != cudaSuccess) return MTP_ERR_CUDA;
+  h->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return MTP_OK;
+}
+
+void free_all(mtp_handle* h) {
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+  for (auto e : h->ev_pool) cudaEventDestroy(e);
+  h->ev_pool.clear();
+}
+
+int esize(int dt) { return dt == MTP_DTYPE_BF16 ? 2 : 4; }
+
+GemvPlan plan_gemv(int N, int K, int M, bool dual, int sms) {
+  GemvPlan p;
+  p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+  const int rows = gemv_rows_per_group(p.mt);
+  p.ngroups = N / rows;
+  p.S = dual ? 2 : 1;
+  while (p.S < 8 && (long long)p.ngroups * p.S < 4LL * sms) p.S *= 2;
+  while (p.S < 8 && (long long)p.mt * (K / p.S) * 4 > 96 * 1024) p.S *= 2;
+  p.smem = p.mt * (K / p.S) * 4;
+  return p;
+}
+
+// Profiling brackets around a launch group.
+struct ProfScope {
+  mtp_handle* h;
+  cudaStream_t s;
+  int kind;
+  cudaEvent_t b = nullptr;
+  ProfScope(mtp_handle* hh, cudaStream_t ss, int k) : h(hh), s(ss), kind(k) {
+    if (!h->prof) return;
+    cudaEvent_t a = next();
+    b = next();
+    cudaEventRecord(a, s);
+    h->recs.push_back({kind, a, b});
+  }
+  ~ProfScope() {
+    if (h->prof && b) cudaEventRecord(b, s);
+  }
+  cudaEvent_t next() {
+    if (h->ev_next >= h->ev_pool.size()) {
+      cudaEvent_t e;
+      cudaEventCreate(&e);
+      h->ev_pool.push_back(e);
+    }
+    return h->ev_pool[h->ev_next++];
+  }
+};
+
+// One GEMV over a list of items, in passes of at most 8.
+struct GemvJob {
+  const void* w[3];
+  int seg_end[3];
+  int N, K, pro, epi;
+  bool dual;
+  // item-indexed operands (row stride in elements)
+  const float* x;
+  long long ldx;
+  const float* nw;
+  const float* nw2;
+  float* y;
+  long long ldy;
+  const float* resid;
+  long long ldr;
+  // dual prologue sources
+  const int32_t* tok;
+  const int* tok_idx;        // per item
+  const void* hid;
+  const long long* hid_off;  // per item, elements
+  int hid_dt;
+  int32_t* amax_out;
+  const int* amax_idx;
+};
+
+void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
+  for (int m0 = 0; m0 < M; m0 += 8) {
+    const int mp = std::min(8, M - m0);
+    const GemvPlan pl = plan_gemv(j.N, j.K, mp, j.dual, h->sms);
+    GemvArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int i = 0; i < 3; ++i) { a.w[i] = j.w[i]; a.seg_end[i] = j.seg_end[i]; }
+    a.N = j.N; a.K = j.K; a.S = pl.S; a.ngroups = pl.ngroups;
+    a.pro = j.pro; a.epi = j.epi; a.M = mp; a.wdt = h->cfg.dtype;
+    a.x = j.x ? j.x + (size_t)m0 * j.ldx : nullptr;
+    a.ldx = j.ldx;
+    a.nw = j.nw; a.nw2 = j.nw2; a.eps = h->cfg.eps;
+    a.E = h->embed;
+    a.vocab = h->cfg.vocab;
+    a.tok = j.tok;
+    a.hid = j.hid;
+    a.hid_dt = j.hid_dt;
+    for (int m = 0; m < mp; ++m) {
+      if (j.tok_idx) a.tok_idx[m] = j.tok_idx[m0 + m];
+      if (j.hid_off) a.hid_off[m] = j.hid_off[m0 + m];
+      if (j.amax_idx) a.amax_idx[m] = j.amax_idx[m0 + m];
+    }
+    a.y = j.y + (size_t)m0 * j.ldy;
+    a.ldy = j.ldy;
+    a.resid = j.resid ? j.resid + (size_t)m0 * j.ldr : nullptr;
+    a.ldr = j.ldr;
+    a.part = h->part;
+    a.counters = h->counters;
+    a.gmax = h->gmax;
+    a.gidx = h->gidx;
+    a.done = h->done;
+    a.amax_out = j.amax_out;
+    a.status = h->status;
+    launch_gemv(pl.mt, a, pl.smem, s);
+  }
+}
+
+bool fast_greedy(const mtp_sampling& p) { return (p.temperature <= 0.f || p.top_k == 1) && p.rep_penalty == 1.f; }
+
+mtp_status check_params(const mtp_sampling* hp, int rows) {
+  if (!hp) return MTP_ERR_BAD_ARG;
+  for (int r = 0; r < rows; ++r) {
+    const mtp_sampling& p = hp[r];
+    if (!(p.temperature >= 0.f) || !(p.rep_penalty > 0.f) || !(p.top_p > 0.f && p.top_p <= 1.f) ||
+        !(p.min_p >= 0.f && p.min_p < 1.f) || p.top_k < 0 || p.top_k > 1024 || p.reserved != 0)
+      return MTP_ERR_BAD_ARG;
+  }
+  return MTP_OK;
+}
+
+RowParams row_params(const mtp_sampling& p) {
+  RowParams r;
+  r.temperature = p.temperature;
+  r.rep_penalty = p.rep_penalty;
+  r.top_p = p.top_p;
+  r.min_p = p.min_p;
+  r.top_k = p.top_k;
+  r.greedy = (p.temperature <= 0.f || p.top_k == 1) ? 1 : 0;
+  return r;
+}
+
+// Items of one head call. Head items (one per row, the row's newest pair)
+// come first so that per-row activations stay contiguous.
+struct Items {
+  int n = 0, n_head = 0;
+  std::vector<int> row, slot, tok_idx, head_of_row;
+  std::vector<long long> hid_off;
+};
+
+// fc -> input norm -> q/k/v -> q/k norm + RoPE + KV append for every item;
+// q is kept for head items.
+mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const void* hid, int hid_dt,
+                     bool need_q, cudaStream_t s, int pk_fc, int pk_kv) {
+  const mtp_config& c = h->cfg;
+  const int H = c.hidden, qw = c.n_q * c.head_dim, kw = c.n_kv * c.head_dim;
+  const long long ldq = qw + 2 * kw;
+  {
+    ProfScope ps(h, s, pk_fc);
+    GemvJob j;
+    std::memset(&j, 0, sizeof(j));
+    j.w[0] = h->w[T_FC];
+    j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
+    j.N = H; j.K = 2 * H; j.pro = PRO_DUAL; j.epi = EPI_STORE; j.dual = true;
+    j.nw = h->nrm[T_PRE_E]; j.nw2 = h->nrm[T_PRE_H];
+    j.y = h->h0; j.ldy = H;
+    j.tok = tok; j.tok_idx = it.tok_idx.data();
+    j.hid = hid; j.hid_off = it.hid_off.data(); j.hid_dt = hid_dt;
+    run_gemv(h, j, it.n, s);
+  }
+  {
+    ProfScope ps(h, s, pk_kv);
+    GemvJob j;
+    std::memset(&j, 0, sizeof(j));
+    if (need_q) {
+      j.w[0] = h->w[T_Q]; j.w[1] = h->w[T_K]; j.w[2] = h->w[T_V];
+      j.seg_end[0] = qw; j.seg_end[1] = qw + kw; j.seg_end[2] = qw + 2 * kw;
+      j.N = qw + 2 * kw;
+      j.y = h->qkv;
+    } else {
+      j.w[0] = h->w[T_K]; j.w[1] = h->w[T_V]; j.w[2] = h->w[T_V];
+      j.seg_end[0] = kw; j.seg_end[1] = 2 * kw; j.seg_end[2] = 2 * kw;
+      j.N = 2 * kw;
+      j.y = h->qkv + qw;
+    }
+    j.ldy = ldq;
+    j.K = H; j.pro = PRO_NORM; j.epi = EPI_STORE;
+    j.x = h->h0; j.ldx = H; j.nw = h->nrm[T_IN];
+    run_gemv(h, j, it.n, s);
+  }
+  {
+    ProfScope ps(h, s, PK_QKV_POST);
+    for (int m0 = 0; m0 < it.n; m0 += kMaxItems) {
+      const int mp = std::min(kMaxItems, it.n - m0);
+      QkvPostArgs a;
+      std::memset(&a, 0, sizeof(a));
+      a.qkv = h->qkv + (size_t)m0 * ldq;
+      a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
+      a.eps = c.eps; a.theta = c.rope_theta;
+      a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN];
+      a.q_out = h->qrot;
+      a.kc = h->kv.k; a.vc = h->kv.v; a.cap = c.kv_capacity;
+      for (int m = 0; m < mp; ++m) {
+        a.row[m] = it.row[m0 + m];
+        a.slot[m] = it.slot[m0 + m];
+        a.qdst[m] = (short)((need_q && m0 + m < it.n_head) ? m0 + m : -1);
+      }
+      launch_qkv_post(a, s);
+    }
+  }
+  return cuda_ok(cudaGetLastError());
+}
+
+// attention -> o_proj + residual -> post norm -> gate/up SwiGLU -> down +
+// residual -> final norm -> lm_head (+ argmax) for the head items.
+mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_logits, int32_t* amax_out,
+                    const std::vector<int>& amax_idx, cudaStream_t s) {
+  const mtp_config& c = h->cfg;
+  const int H = c.hidden, qw = c.n_q * c.head_dim, I = c.inter;
+  const int R = it.n_head;
+  {
+    ProfScope ps(h, s, PK_ATTN);
+    for (int m0 = 0; m0 < R; m0 += kMaxRows) {
+      AttnArgs a;
+      std::memset(&a, 0, sizeof(a));
+      const int mp = std::min(kMaxRows, R - m0);
+      a.q = h->qrot + (size_t)m0 * qw;
+      a.kc = h->kv.k; a.vc = h->kv.v; a.cap = c.kv_capacity;
+      a.Mh = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
+      a.max_chunks = h->max_chunks;
+      a.scale = 1.0f / std::sqrt((float)c.head_dim);
+      a.po = h->po; a.pml = h->pml; a.o = h->o + (size_t)m0 * qw;
+      for (int m = 0; m < mp; ++m) { a.row[m] = it.row[m0 + m]; a.slot[m] = it.slot[m0 + m]; }
+      launch_attention(a, s);
+    }
+  }
+  GemvJob j;
+  {
+    ProfScope ps(h, s, PK_O);
+    std::memset(&j, 0, sizeof(j));
+    j.w[0] = h->w[T_O]; j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
+    j.N = H; j.K = qw; j.pro = PRO_PLAIN; j.epi = EPI_RESID;
+    j.x = h->o; j.ldx = qw; j.y = h->h1; j.ldy = H; j.resid = h->h0; j.ldr = H;
+    run_gemv(h, j, R, s);
+  }
+  {
+    ProfScope ps(h, s, PK_GATEUP);
+    std::memset(&j, 0, sizeof(j));
+    j.w[0] = h->w[T_GATE]; j.w[1] = h->w[T_UP];
+    j.N = 2 * I; j.K = H; j.pro = PRO_NORM; j.epi = EPI_SWIGLU;
+    j.x = h->h1; j.ldx = H; j.nw = h->nrm[T_POST]; j.y = h->mlp; j.ldy = I;
+    run_gemv(h, j, R, s);
+  }
+  {
+    ProfScope ps(h, s, PK_DOWN);
+    std::memset(&j, 0, sizeof(j));
+    j.w[0] = h->w[T_DOWN]; j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
+    j.N = H; j.K = I; j.pro = PRO_PLAIN; j.epi = EPI_RESID;
+    j.x = h->mlp; j.ldx = I; j.y = h->h2; j.ldy = H; j.resid = h->h1; j.ldr = H;
+    run_gemv(h, j, R, s);
+  }
+  {
+    ProfScope ps(h, s, PK_LMHEAD);
+    std::memset(&j, 0, sizeof(j));
+    j.w[0] = h->lm; j.seg_end[0] = c.vocab; j.seg_end[1] = c.vocab; j.seg_end[2] = c.vocab;
+    j.N = c.vocab; j.K = H; j.pro = PRO_NORM; j.epi = EPI_LOGITS;
+    j.x = h->h2; j.ldx = H; j.nw = h->nrm[T_NORM]; j.y = logits; j.ldy = ld_logits;
+    j.amax_out = amax_out; j.amax_idx = amax_out ? amax_idx.data() : nullptr;
+    run_gemv(h, j, R, s);
+  }
+  return cuda_ok(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mtp_default_block_size(const mtp_config* cfg) { return cfg ? cfg->mtp_layers + 2 : -1; }
+
+const char* mtp_status_str(mtp_status s) {
+  switch (s) {
+    case MTP_OK: return "ok";
+    case MTP_ERR_UNSUPPORTED_ARCH: return "unsupported draft architecture";
+    case MTP_ERR_MISSING_TENSOR: return "missing head tensor";
+    case MTP_ERR_DUP_TENSOR: return "duplicate head tensor";
+    case MTP_ERR_UNKNOWN_TENSOR: return "unknown head tensor";
+    case MTP_ERR_SHAPE: return "tensor shape or dtype mismatch";
+    case MTP_ERR_CONFIG_BOUNDS: return "config scalar out of bounds";
+    case MTP_ERR_NOT_BOUND: return "drafter not bound to a target embedding";
+    case MTP_ERR_KV_CAPACITY: return "draft KV capacity exceeded";
+    case MTP_ERR_BAD_ARG: return "bad argument";
+    case MTP_ERR_NONFINITE: return "non-finite logits";
+    case MTP_ERR_TIMEOUT: return "timeout";
+    case MTP_ERR_CUDA: return "CUDA error";
+    case MTP_ERR_LAYOUT: return "mixed raw-HF and split tensor layouts";
+  }
+  return "unknown status";
+}
+
+mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_tensors, const void* d_embed,
+                    const void* d_lm_head, mtp_kv kv, const int32_t* h_len, mtp_stream stream, mtp_t* out) {
+  if (!out) return MTP_ERR_BAD_ARG;
+  *out = nullptr;
+  if (!cfg || !tensors || n_tensors < 0) return MTP_ERR_BAD_ARG;
+  const mtp_config& c = *cfg;
+  if (!c.architecture || std::strcmp(c.architecture, "qwen3_5_mtp") != 0) return MTP_ERR_UNSUPPORTED_ARCH;
+  // config scalar bounds
+  const bool dims_ok = c.hidden >= 256 && c.hidden <= 16384 && c.hidden % 256 == 0 && c.n_q >= 1 &&
+                       c.n_kv >= 1 && c.n_q % c.n_kv == 0 && c.n_q / c.n_kv <= 8 && c.n_q <= 128 &&
+                       (c.head_dim == 64 || c.head_dim == 128 || c.head_dim == 256) && c.inter >= 256 &&
+                       c.inter % 256 == 0 && c.inter <= 65536 && c.vocab >= 64 && c.vocab % 64 == 0 &&
+                       c.vocab <= (1 << 20) && c.mtp_layers == 1 && c.max_rows >= 1 && c.max_rows <= kMaxRows &&
+                       c.kv_capacity >= 64 && c.kv_capacity % 64 == 0 && c.kv_capacity <= (1 << 20) &&
+                       c.max_depth >= 1 && c.max_depth <= 16 && c.eps > 0.f && c.eps < 1.f &&
+                       c.rope_theta > 1.f && (c.dtype == MTP_DTYPE_F32 || c.dtype == MTP_DTYPE_BF16) &&
+                       ((c.n_q * c.head_dim) % 256 == 0);
+  if (!dims_ok) return MTP_ERR_CONFIG_BOUNDS;
+  if (!d_embed) return MTP_ERR_NOT_BOUND;
+  if (!kv.k || !kv.v || !kv.len) return MTP_ERR_BAD_ARG;
+
+  // tensor table: layout, inventory, duplicates, shapes
+  int raw = -1;
+  const void* ptr[T_COUNT] = {};
+  bool seen[T_COUNT] = {};
+  for (int i = 0; i < n_tensors; ++i) {
+    if (!tensors[i].name) return MTP_ERR_BAD_ARG;
+    std::string nm = tensors[i].name;
+    const int is_raw = nm.rfind("mtp.", 0) == 0 ? 1 : 0;
+    if (raw < 0) raw = is_raw;
+    if (raw != is_raw) return MTP_ERR_LAYOUT;
+    const std::string base = is_raw ? nm.substr(4) : nm;
+    int id = -1;
+    for (int t = 0; t < T_COUNT; ++t)
+      if (base == kNames[t]) id = t;
+    if (id < 0) return MTP_ERR_UNKNOWN_TENSOR;
+    if (seen[id]) return MTP_ERR_DUP_TENSOR;
+    seen[id] = true;
+  }
+  for (int t = 0; t < T_COUNT; ++t)
+    if (!seen[t]) return MTP_ERR_MISSING_TENSOR;
+  const int H = c.hidden, qw = c.n_q * c.head_dim, kw = c.n_kv * c.head_dim, I = c.inter, dh = c.head_dim;
+  const long long want[T_COUNT][2] = {{H, 2 * H}, {H, 0},  {H, 0},  {H, 0},  {H, 0},  {H, 0},  {I, H}, {I, H},
+                                      {H, I},     {qw, H}, {kw, H}, {kw, H}, {H, qw}, {dh, 0}, {dh, 0}};
+  bool shifted[T_COUNT] = {};
+  for (int i = 0; i < n_tensors; ++i) {
+    const mtp_tensor& t = tensors[i];
+    std::string nm = t.name;
+    const std::string base = raw ? nm.substr(4) : nm;
+    int id = 0;
+    for (int k = 0; k < T_COUNT; ++k)
+      if (base == kNames[k]) id = k;
+    const bool vec = want[id][1] == 0;
+    if (!t.data || t.dtype != c.dtype || t.ndim != (vec ? 1 : 2) || t.shape[0] != want[id][0] ||
+        (!vec && t.shape[1] != want[id][1]))
+      return MTP_ERR_SHAPE;
+    ptr[id] = t.data;
+    if (raw)
+      for (auto suf : kShiftSuffixes)
+        if (ends_with(nm, suf)) shifted[id] = true;
+  }
+
+  mtp_handle* h = new mtp_handle();
+  h->cfg = c;
+  h->arch = c.architecture;
+  h->cfg.architecture = h->arch.c_str();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev);
+  if (h->sms <= 0) h->sms = 152;
+  for (int t = 0; t < T_COUNT; ++t) h->w[t] = ptr[t];
+  h->embed = d_embed;
+  h->lm = d_lm_head ? d_lm_head : d_embed;
+  h->kv = kv;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  mtp_status st = MTP_OK;
+  const int R = c.max_rows;
+  // norm copies (fp32, shifted once for the raw-HF layout)
+  const int norm_ids[7] = {T_NORM, T_PRE_E, T_PRE_H, T_IN, T_POST, T_QN, T_KN};
+  size_t norm_total = 0;
+  for (int id : norm_ids) norm_total += want[id][0];
+  st = alloc(h, &h->norms, norm_total);
+  size_t off = 0;
+  for (int id : norm_ids) {
+    if (st != MTP_OK) break;
+    h->nrm[id] = h->norms + off;
+    launch_norm_copy(ptr[id], c.dtype, (int)want[id][0], shifted[id] ? 1.0f : 0.0f, h->nrm[id], s);
+    off += want[id][0];
+  }
+  // scratch
+  h->max_chunks = c.kv_capacity / kAttnChunk;
+  if (st == MTP_OK) st = alloc(h, &h->h0, (size_t)kMaxItems * H);
+  if (st == MTP_OK) st = alloc(h, &h->qkv, (size_t)kMaxItems * (qw + 2 * kw));
+  if (st == MTP_OK) st = alloc(h, &h->qrot, (size_t)R * qw);
+  if (st == MTP_OK) st = alloc(h, &h->o, (size_t)R * qw);
+  if (st == MTP_OK) st = alloc(h, &h->h1, (size_t)R * H);
+  if (st == MTP_OK) st = alloc(h, &h->mlp, (size_t)R * I);
+  if (st == MTP_OK) st = alloc(h, &h->h2, (size_t)R * H);
+  if (st == MTP_OK) st = alloc(h, &h->logits, (size_t)R * c.vocab);
+  if (st == MTP_OK) st = alloc(h, &h->po, (size_t)std::min(R, kMaxRows) * c.n_q * h->max_chunks * dh);
+  if (st == MTP_OK) st = alloc(h, &h->pml, (size_t)std::min(R, kMaxRows) * c.n_q * h->max_chunks * 2);
+  // split-K partials and counters: worst case over every GEMV shape and width
+  size_t part = 0;
+  int groups = 0;
+  const int shapes[7][3] = {{H, 2 * H, 1}, {qw + 2 * kw, H, 0}, {2 * kw, H, 0}, {H, qw, 0},
+                            {2 * I, H, 0}, {H, I, 0},          {c.vocab, H, 0}};
+  for (int mt : {1, 2, 4, 8})
+    for (auto& sh : shapes) {
+      GemvPlan pl = plan_gemv(sh[0], sh[1], mt, sh[2] != 0, h->sms);
+      if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * sh[0]);
+      groups = std::max(groups, pl.ngroups);
+    }
+  h->part_floats = part;
+  h->lm_groups_max = c.vocab / gemv_rows_per_group(8);
+  h->lm_groups_max = std::max(h->lm_groups_max, c.vocab / gemv_rows_per_group(1));
+  h->counters_n = groups;
+  if (st == MTP_OK) st = alloc(h, &h->part, part);
+  if (st == MTP_OK) st = alloc(h, &h->gmax, (size_t)8 * h->lm_groups_max);
+  if (st == MTP_OK) st = alloc(h, &h->gidx, (size_t)8 * h->lm_groups_max);
+  if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
+  if (st == MTP_OK) st = alloc(h, &h->done, 1);
+  if (st == MTP_OK) st = alloc(h, &h->status, 1);
+  if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->counters, 0, sizeof(int) * groups, s));
+  if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->done, 0, sizeof(int), s));
+  if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->status, 0, sizeof(int32_t), s));
+  h->len.assign(R, 0);
+  h->keep.assign(R, -1);
+  h->drafted_len.assign(R, 0);
+  if (h_len)
+    for (int r = 0; r < R; ++r) {
+      if (h_len[r] < 0 || h_len[r] > c.kv_capacity) st = MTP_ERR_BAD_ARG;
+      h->len[r] = h_len[r];
+    }
+  if (st == MTP_OK) launch_set_len(h->kv.len, R, h->len.data(), s);
+  if (st == MTP_OK) st = cuda_ok(cudaGetLastError());
+  if (st == MTP_OK) st = cuda_ok(cudaStreamSynchronize(s));
+  if (st != MTP_OK) {
+    free_all(h);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return MTP_OK;
+}
+
+mtp_status mtp_free(mtp_t h) {
+  if (!h) return MTP_ERR_BAD_ARG;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return MTP_OK;
+}
+
+mtp_status mtp_get_lengths(mtp_t h, int32_t* h_len) {
+  if (!h || !h_len) return MTP_ERR_BAD_ARG;
+  for (int r = 0; r < h->cfg.max_rows; ++r) h_len[r] = h->len[r];
+  return MTP_OK;
+}
+
+mtp_status mtp_set_lengths(mtp_t h, mtp_stream stream, const int32_t* h_len) {
+  if (!h || !h_len) return MTP_ERR_BAD_ARG;
+  for (int r = 0; r < h->cfg.max_rows; ++r)
+    if (h_len[r] < 0 || h_len[r] > h->cfg.kv_capacity) return MTP_ERR_BAD_ARG;
+  for (int r = 0; r < h->cfg.max_rows; ++r) { h->len[r] = h_len[r]; h->keep[r] = -1; }
+  launch_set_len(h->kv.len, h->cfg.max_rows, h->len.data(), reinterpret_cast<cudaStream_t>(stream));
+  return cuda_ok(cudaGetLastError());
+}
+
+int32_t* mtp_device_status(mtp_t h) { return h ? h->status : nullptr; }
+
+mtp_status mtp_flush(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* h_pairs, int32_t pmax,
+                     const int32_t* d_tok, const void* d_hid, int32_t hid_dtype) {
+  if (!h || !h_pairs || rows < 1 || rows > h->cfg.max_rows || pmax < 1 || !d_tok || !d_hid ||
+      (hid_dtype != MTP_DTYPE_F32 && hid_dtype != MTP_DTYPE_BF16))
+    return MTP_ERR_BAD_ARG;
+  const mtp_config& c = h->cfg;
+  for (int r = 0; r < rows; ++r) {
+    if (h_pairs[r] < 0 || h_pairs[r] > pmax) return MTP_ERR_BAD_ARG;
+    if ((long long)h->len[r] + h_pairs[r] > c.kv_capacity) return MTP_ERR_KV_CAPACITY;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Items all;
+  for (int r = 0; r < rows; ++r)
+    for (int j = 0; j < h_pairs[r]; ++j) {
+      all.row.push_back(r);
+      all.slot.push_back(h->len[r] + j);
+      all.tok_idx.push_back(r * pmax + j);
+      all.hid_off.push_back(((long long)r * pmax + j) * c.hidden);
+    }
+  all.n = (int)all.row.size();
+  for (int m0 = 0; m0 < all.n; m0 += kMaxItems) {
+    Items it;
+    const int mp = std::min(kMaxItems, all.n - m0);
+    it.n = mp;
+    it.n_head = 0;
+    it.row.assign(all.row.begin() + m0, all.row.begin() + m0 + mp);
+    it.slot.assign(all.slot.begin() + m0, all.slot.begin() + m0 + mp);
+    it.tok_idx.assign(all.tok_idx.begin() + m0, all.tok_idx.begin() + m0 + mp);
+    it.hid_off.assign(all.hid_off.begin() + m0, all.hid_off.begin() + m0 + mp);
+    mtp_status st = run_front(h, it, d_tok, d_hid, hid_dtype, false, s, PK_FLUSH_FC, PK_FLUSH_KV);
+    if (st != MTP_OK) return st;
+  }
+  for (int r = 0; r < rows; ++r) { h->len[r] += h_pairs[r]; h->keep[r] = -1; }
+  launch_set_len(h->kv.len, c.max_rows, h->len.data(), s);
+  return cuda_ok(cudaGetLastError());
+}
+
+mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, const int32_t* h_pairs,
+                     int32_t pmax, const int32_t* d_tok, const void* d_hid, int32_t hid_dtype,
+                     const mtp_sampling* h_params, const int32_t* d_hist, int32_t hist_w, const float* d_u,
+                     int32_t* d_draft, float* d_q, float* d_logits, float* d_hidden) {
+  if (!h || rows < 1 || rows > h->cfg.max_rows || depth < 1 || depth > h->cfg.max_depth || !h_pairs ||
+      pmax < 1 || !d_tok || !d_hid || !d_draft || hist_w < 0 || hist_w > 128 || (hist_w > 0 && !d_hist) ||
+      (hid_dtype != MTP_DTYPE_F32 && hid_dtype != MTP_DTYPE_BF16))
+    return MTP_ERR_BAD_ARG;
+  mtp_status st = check_params(h_params, rows);
+  if (st != MTP_OK) return st;
+  const mtp_config& c = h->cfg;
+  bool all_fast = true, any_sampled = false;
+  for (int r = 0; r < rows; ++r) {
+    all_fast &= fast_greedy(h_params[r]);
+    any_sampled |= !row_params(h_params[r]).greedy;
+  }
+  if (any_sampled && (!d_q || !d_u)) return MTP_ERR_BAD_ARG;
+  int total = 0;
+  for (int r = 0; r < rows; ++r) {
+    if (h_pairs[r] < 1 || h_pairs[r] > pmax) return MTP_ERR_BAD_ARG;
+    if ((long long)h->len[r] + h_pairs[r] + depth - 1 > c.kv_capacity) return MTP_ERR_KV_CAPACITY;
+    total += h_pairs[r];
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int H = c.hidden, V = c.vocab;
+
+  // step-1 items: head items first, then the pending pairs
+  Items it1;
+  it1.n_head = rows;
+  for (int r = 0; r < rows; ++r) {
+    const int j = h_pairs[r] - 1;
+    it1.row.push_back(r);
+    it1.slot.push_back(h->len[r] + j);
+    it1.tok_idx.push_back(r * pmax + j);
+    it1.hid_off.push_back(((long long)r * pmax + j) * H);
+  }
+  for (int r = 0; r < rows; ++r)
+    for (int j = 0; j + 1 < h_pairs[r]; ++j) {
+      it1.row.push_back(r);
+      it1.slot.push_back(h->len[r] + j);
+      it1.tok_idx.push_back(r * pmax + j);
+      it1.hid_off.push_back(((long long)r * pmax + j) * H);
+    }
+  it1.n = (int)it1.row.size();
+  if (it1.n > kMaxItems) return MTP_ERR_BAD_ARG;
+
+  std::vector<int> amax_idx(rows);
+  SampleArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  sa.mode = 0; sa.rows = rows; sa.V = V; sa.W = hist_w; sa.depth = depth;
+  sa.hist = d_hist; sa.drafts = d_draft; sa.u = d_u; sa.q = d_q; sa.draft_out = d_draft;
+  sa.status = h->status;
+  for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
+
+  for (int k = 1; k <= depth; ++k) {
+    Items itk;
+    const Items* it = &it1;
+    const int32_t* tok = d_tok;
+    const void* hid = d_hid;
+    int hdt = hid_dtype;
+    if (k > 1) {
+      itk.n = rows;
+      itk.n_head = rows;
+      for (int r = 0; r < rows; ++r) {
+        itk.row.push_back(r);
+        itk.slot.push_back(h->len[r] + h_pairs[r] + k - 2);
+        itk.tok_idx.push_back(r * depth + (k - 2));
+        itk.hid_off.push_back((long long)r * H);
+      }
+      it = &itk;
+      tok = d_draft;
+      hid = h->h2;
+      hdt = MTP_DTYPE_F32;
+    }
+    st = run_front(h, *it, tok, hid, hdt, true, s, PK_FC, PK_QKV);
+    if (st != MTP_OK) return st;
+    float* lg = d_logits ? d_logits + (size_t)(k - 1) * V : h->logits;
+    const long long ldl = d_logits ? (long long)depth * V : V;
+    for (int r = 0; r < rows; ++r) amax_idx[r] = r * depth + (k - 1);
+    st = run_back(h, *it, lg, ldl, all_fast ? d_draft : nullptr, amax_idx, s);
+    if (st != MTP_OK) return st;
+    if (!all_fast) {
+      ProfScope ps(h, s, PK_SAMPLE);
+      sa.pos = k - 1;
+      sa.logits = lg;
+      sa.ld = ldl;
+      launch_sample(sa, s);
+    }
+    if (d_hidden) {
+      st = cuda_ok(cudaMemcpy2DAsync(d_hidden + (size_t)(k - 1) * H, sizeof(float) * depth * H, h->h2,
+                                     sizeof(float) * H, sizeof(float) * H, rows, cudaMemcpyDeviceToDevice, s));
+      if (st != MTP_OK) return st;
+    }
+  }
+  for (int r = 0; r < rows; ++r) {
+    h->keep[r] = h->len[r] + h_pairs[r];
+    h->len[r] += h_pairs[r] + depth - 1;
+  }
+  for (int r = rows; r < c.max_rows; ++r) h->keep[r] = -1;
+  launch_set_len(h->kv.len, c.max_rows, h->len.data(), s);
+  return cuda_ok(cudaGetLastError());
+}
+
+size_t spec_verify_workspace_bytes(int32_t rows, int32_t depth, int32_t vocab) {
+  (void)vocab;
+  if (rows < 1 || depth < 1) return 0;
+  return sizeof(TDesc) * (size_t)rows * (depth + 1);
+}
+
+mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
+                       const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
+                       const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
+                       int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace) {
+  if (rows < 1 || rows > kMaxRows || depth < 1 || depth > 16 || vocab < 1 || !d_logits || !d_draft ||
+      hist_w < 0 || hist_w > 128 || (hist_w > 0 && !d_hist) || !d_u || !d_n_acc || !d_out_tok || !d_workspace)
+    return MTP_ERR_BAD_ARG;
+  mtp_status st = check_params(h_params, rows);
+  if (st != MTP_OK) return st;
+  bool any_sampled = false;
+  for (int r = 0; r < rows; ++r) any_sampled |= !row_params(h_params[r]).greedy;
+  if (any_sampled && !d_q) return MTP_ERR_BAD_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TDesc* desc = static_cast<TDesc*>(d_workspace);
+  SampleArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  sa.mode = 1; sa.rows = rows; sa.V = vocab; sa.W = hist_w; sa.depth = depth;
+  sa.logits = d_logits; sa.hist = d_hist; sa.drafts = d_draft; sa.desc = desc;
+  for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
+  launch_sample(sa, s);
+  VerifyArgs va;
+  std::memset(&va, 0, sizeof(va));
+  va.rows = rows; va.V = vocab; va.W = hist_w; va.depth = depth;
+  va.logits = d_logits; va.drafts = d_draft; va.q = d_q; va.hist = d_hist; va.u = d_u; va.desc = desc;
+  va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
+  for (int r = 0; r < rows; ++r) va.p[r] = sa.p[r];
+  launch_verify(va, s);
+  st = cuda_ok(cudaGetLastError());
+  if (st != MTP_OK) return st;
+  if (h_out) {
+    const size_t pitch = sizeof(int32_t) * (depth + 2);
+    st = cuda_ok(cudaMemcpy2DAsync(h_out, pitch, d_n_acc, sizeof(int32_t), sizeof(int32_t), rows,
+                                   cudaMemcpyDeviceToHost, s));
+    if (st == MTP_OK)
+      st = cuda_ok(cudaMemcpy2DAsync(h_out + 1, pitch, d_out_tok, sizeof(int32_t) * (depth + 1),
+                                     sizeof(int32_t) * (depth + 1), rows, cudaMemcpyDeviceToHost, s));
+  }
+  return st;
+}
+
+mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* d_n_acc, int32_t* d_target_len,
+                       int32_t depth, int32_t zero_tail) {
+  if (!h || rows < 1 || rows > h->cfg.max_rows || depth < 1 || (d_target_len && !d_n_acc)) return MTP_ERR_BAD_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ProfScope ps(h, s, PK_ROLLBACK);
+  RollbackArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.len = h->kv.len; a.rows = rows; a.zero_tail = zero_tail ? 1 : 0;
+  a.kc = h->kv.k; a.vc = h->kv.v; a.cap = h->cfg.kv_capacity;
+  a.nkv = h->cfg.n_kv; a.dh = h->cfg.head_dim; a.esize = esize(h->cfg.dtype);
+  a.n_acc = d_n_acc; a.target_len = d_target_len; a.block = depth + 1;
+  for (int r = 0; r < rows; ++r) {
+    a.keep[r] = h->keep[r];
+    a.old_len[r] = h->len[r];
+  }
+  launch_rollback(a, s);
+  for (int r = 0; r < rows; ++r)
+    if (h->keep[r] >= 0) { h->len[r] = h->keep[r]; h->keep[r] = -1; }
+  return cuda_ok(cudaGetLastError());
+}
+
+mtp_status mtp_profile_enable(mtp_t h, int32_t on) {
+  if (!h) return MTP_ERR_BAD_ARG;
+  h->prof = on != 0;
+  return MTP_OK;
+}
+
+int32_t mtp_profile_kinds(void) { return PK_COUNT; }
+
+const char* mtp_profile_kind_name(int32_t kind) { return kind >= 0 && kind < PK_COUNT ? kProfNames[kind] : ""; }
+
+mtp_status mtp_profile_read(mtp_t h, float* h_ms, int32_t* h_launches) {
+  if (!h || !h_ms || !h_launches) return MTP_ERR_BAD_ARG;
+  for (int k = 0; k < PK_COUNT; ++k) { h_ms[k] = 0.f; h_launches[k] = 0; }
+  for (auto& r : h->recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return MTP_ERR_CUDA;
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    h_ms[r.kind] += ms;
+    h_launches[r.kind] += 1;
+  }
+  h->recs.clear();
+  h->ev_next = 0;
+  return MTP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,611 @@
+// Sampling transforms and rejection-sampling verify for sm_103a.
+//
+// The sampler chain (temperature, repetition penalty over a ring history,
+// top-k, top-p, min-p) and the unified greedy/sampled verify follow the
+// Ollama MLX-runner commit log ("greedy is a special case of sampled decoding
+// -- at temperature 0 the sampler yields a point mass, so rejection-sampling
+// acceptance reduces to argmax-match"; sampler transforms commit). Readings
+// where the pages are silent:
+//   * penalty applies once per distinct window token: z/r if z > 0 else z*r;
+//   * tokens are ordered by (transformed logit desc, id asc); top-k keeps the
+//     first k, top-p the shortest prefix whose cumulative exp(z - zmax)
+//     reaches top_p of the top-k total, min-p keeps exp(z - zmax) >= min_p;
+//     the kept set is their intersection, renormalised;
+//   * draws are inverse-CDF in ascending id order with a pre-drawn uniform.
+//
+// One thread-block cluster of 8 CTAs works on one (row, position): each CTA
+// holds a contiguous slice of the vocabulary in shared memory, and the CTAs
+// combine histograms, sums and arg-maxima through distributed shared memory.
+// Sums that decide a threshold are exact integers (values scaled by 2^40), so
+// every result is independent of thread scheduling.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace mtp {
+
+constexpr int kST = 512;  // threads per sampling CTA
+constexpr double kFix = 1099511627776.0;  // 2^40
+
+__device__ __forceinline__ uint32_t desc_key(float z) {
+  uint32_t u = __float_as_uint(z);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending in z
+  return ~u;                                        // ascending in -z
+}
+
+__device__ __forceinline__ uint64_t to_fix(float w) {
+  return w > 0.f ? (uint64_t)__float2ull_rn(w * 1099511627776.0f) : 0ull;
+}
+
+__device__ __forceinline__ float penalize(float z, float r) { return z > 0.f ? z / r : z * r; }
+
+struct Mail {
+  unsigned long long u[4];
+  float f[4];
+  int i[4];
+};
+
+struct SampleSmem {
+  Mail mail[2];
+  unsigned long long hist[2][256];
+  unsigned long long tot[256];
+  unsigned long long wsum[kST / 32];
+  int wtok[160];
+  int nwin;
+  int sel_bin;
+  unsigned long long sel_rem;
+  int found;
+};
+
+// Cluster context for one task.
+struct Clu {
+  cg::cluster_group cl;
+  SampleSmem* sm;
+  int ph;
+  int rank;
+  __device__ Clu(SampleSmem* s) : cl(cg::this_cluster()), sm(s), ph(0), rank((int)cg::this_cluster().block_rank()) {}
+
+  // Publish (f, i, u) scalars from thread 0 and return every CTA's values.
+  __device__ Mail* publish() {
+    cl.sync();
+    Mail* m = &sm->mail[ph];
+    ph ^= 1;
+    return m;
+  }
+  __device__ Mail* remote(Mail* local, int r) { return cl.map_shared_rank(local, r); }
+};
+
+// Argmax (value desc, id asc) over the block, result to all threads.
+__device__ void block_argmax(float& v, int& i, float* sv, int* si) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  warp_argmax(v, i);
+  __syncthreads();
+  if (lane == 0) { sv[w] = v; si[w] = i; }
+  __syncthreads();
+  if (w == 0) {
+    v = lane < kST / 32 ? sv[lane] : -INFINITY;
+    i = lane < kST / 32 ? si[lane] : 0x7FFFFFFF;
+    warp_argmax(v, i);
+    if (lane == 0) { sv[0] = v; si[0] = i; }
+  }
+  __syncthreads();
+  v = sv[0];
+  i = si[0];
+}
+
+__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if (lane == 0) sh[w] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int k = 0; k < kST / 32; ++k) t += sh[k];  // fixed order
+  __syncthreads();
+  return t;
+}
+
+// Sum a per-CTA u64 over the cluster (rank order).
+__device__ unsigned long long cluster_sum_u64(Clu& c, unsigned long long local) {
+  if (threadIdx.x == 0) c.sm->mail[c.ph].u[0] = local;
+  Mail* m = c.publish();
+  unsigned long long t = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) t += c.remote(m, r)->u[0];
+  return t;
+}
+
+// Radix selection over the cluster: among active elements ordered by
+// (key asc, id asc) with integer weights, find the key K* of the element at
+// which the running weight first reaches `target`, and how much of the
+// target remains within the elements whose key is K*.
+template <class Act, class Wt>
+__device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, Wt weight,
+                             unsigned long long target, uint32_t& key_out, unsigned long long& rem_out) {
+  SampleSmem* sm = c.sm;
+  uint32_t prefix = 0, mask = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    unsigned long long* h = sm->hist[c.ph];
+    for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n_local; j += kST) {
+      if (!active(j)) continue;
+      const uint32_t k = desc_key(zs[j]);
+      if ((k & mask) != prefix) continue;
+      atomicAdd(&h[(k >> shift) & 255u], weight(j));
+    }
+    c.cl.sync();
+    for (int b = threadIdx.x; b < 256; b += kST) {
+      unsigned long long t = 0;
+      for (int r = 0; r < kClusterCTAs; ++r) t += c.cl.map_shared_rank(h, r)[b];
+      sm->tot[b] = t;
+    }
+    c.ph ^= 1;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      unsigned long long s8 = 0;
+      for (int b = 0; b < 8; ++b) s8 += sm->tot[lane * 8 + b];
+      unsigned long long incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      unsigned long long cum = incl - s8;
+      const bool mine = cum < target && target <= incl;
+      if (mine) {
+        for (int b = 0; b < 8; ++b) {
+          const unsigned long long t = sm->tot[lane * 8 + b];
+          if (cum < target && target <= cum + t) {
+            sm->sel_bin = lane * 8 + b;
+            sm->sel_rem = target - cum;
+            break;
+          }
+          cum += t;
+        }
+      }
+      const unsigned any = __ballot_sync(0xFFFFFFFFu, mine);
+      if (!any && lane == 0) {  // target above the total: keep everything
+        sm->sel_bin = 255;
+        sm->sel_rem = target;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm->sel_bin << shift;
+    mask |= 255u << shift;
+    target = sm->sel_rem;
+    __syncthreads();
+  }
+  key_out = prefix;
+  rem_out = target;
+}
+
+// Among active elements with key == K* (ids ascending over the cluster),
+// return the id of the n-th (1-based), or INT_MAX if n covers all of them.
+template <class Act>
+__device__ int tie_cut(Clu& c, const float* zs, int n_local, int v0, Act active, uint32_t K,
+                       unsigned long long n) {
+  SampleSmem* sm = c.sm;
+  unsigned long long cnt = 0;
+  for (int j = threadIdx.x; j < n_local; j += kST)
+    if (active(j) && desc_key(zs[j]) == K) ++cnt;
+  cnt = block_sum_u64(cnt, sm->wsum);
+  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = cnt;
+  Mail* m = c.publish();
+  unsigned long long before = 0, total = 0;
+  int owner = -1;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    const unsigned long long t = c.remote(m, r)->u[0];
+    if (owner < 0 && before + t >= n) owner = r;
+    if (owner < 0) before += t;
+    total += t;
+  }
+  if (n >= total) return 0x7FFFFFFF;
+  int cut = -1;
+  if (c.rank == owner) {
+    // scan this slice in id order, 512 elements at a time
+    unsigned long long need = n - before;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) sm->found = -1;
+    __syncthreads();
+    for (int base = 0; base < n_local; base += kST) {
+      const int j = base + threadIdx.x;
+      const unsigned flag = (j < n_local && active(j) && desc_key(zs[j]) == K) ? 1u : 0u;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, flag);
+      __syncthreads();
+      if (lane == 0) sm->wsum[w] = __popc(bal);
+      __syncthreads();
+      unsigned long long wbefore = 0, chunk = 0;
+      for (int k = 0; k < kST / 32; ++k) {
+        if (k < w) wbefore += sm->wsum[k];
+        chunk += sm->wsum[k];
+      }
+      const unsigned long long incl = wbefore + __popc(bal & ((2u << lane) - 1u));
+      if (flag && incl == need) sm->found = v0 + j;
+      __syncthreads();
+      if (chunk >= need) break;
+      need -= chunk;
+    }
+    cut = sm->found;
+  }
+  if (threadIdx.x == 0) sm->mail[c.ph].i[0] = cut;
+  m = c.publish();
+  return c.remote(m, owner)->i[0];
+}
+
+// Inverse-CDF draw over the cluster with per-element integer weights:
+// smallest id whose cumulative weight exceeds u * total. Returns -1 if the
+// total is zero.
+template <class Wt>
+__device__ int cluster_draw(Clu& c, int n_local, int v0, Wt weight, float u) {
+  SampleSmem* sm = c.sm;
+  unsigned long long loc = 0;
+  for (int j = threadIdx.x; j < n_local; j += kST) loc += weight(j);
+  loc = block_sum_u64(loc, sm->wsum);
+  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = loc;
+  Mail* m = c.publish();
+  unsigned long long tot = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) tot += c.remote(m, r)->u[0];
+  if (tot == 0) return -1;
+  const unsigned long long target = (unsigned long long)floor((double)u * (double)tot) + 1ull;
+  unsigned long long before = 0;
+  int owner = kClusterCTAs - 1;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    const unsigned long long t = c.remote(m, r)->u[0];
+    if (before + t >= target) { owner = r; break; }
+    before += t;
+  }
+  int pick = -1;
+  if (c.rank == owner) {
+    unsigned long long need = target - before;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) sm->found = -1;
+    for (int base = 0; base < n_local; base += kST) {
+      const int j = base + threadIdx.x;
+      const unsigned long long x = j < n_local ? weight(j) : 0ull;
+      unsigned long long incl = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      __syncthreads();
+      if (lane == 31) sm->wsum[w] = incl;
+      __syncthreads();
+      unsigned long long wbefore = 0, chunk = 0;
+      for (int k = 0; k < kST / 32; ++k) {
+        if (k < w) wbefore += sm->wsum[k];
+        chunk += sm->wsum[k];
+      }
+      incl += wbefore;
+      if (x > 0 && incl >= need && incl - x < need) sm->found = v0 + j;
+      __syncthreads();
+      if (chunk >= need) break;
+      need -= chunk;
+    }
+    pick = sm->found;
+  }
+  if (threadIdx.x == 0) sm->mail[c.ph].i[0] = pick;
+  m = c.publish();
+  return c.remote(m, owner)->i[0];
+}
+
+// Load the penalty window of position i into shared memory.
+__device__ void load_window(SampleSmem* sm, const int32_t* hist, int W, const int32_t* drafts, int i) {
+  const int drop = i < W ? i : W;
+  const int nh = W - drop;
+  const int first = i > W ? i - W : 0;
+  const int nd = i - first;
+  for (int t = threadIdx.x; t < nh + nd; t += kST)
+    sm->wtok[t] = t < nh ? hist[drop + t] : drafts[first + t - nh];
+  if (threadIdx.x == 0) sm->nwin = nh + nd;
+  __syncthreads();
+}
+
+// Mark window tokens that fall in [v0, v0+n) in the bitmap (each once).
+__device__ void build_bitmap(SampleSmem* sm, uint32_t* bits, int v0, int n) {
+  for (int w = threadIdx.x; w < (n + 31) / 32; w += kST) bits[w] = 0u;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < sm->nwin; ++t) {
+      const int v = sm->wtok[t] - v0;
+      if (v >= 0 && v < n) bits[v >> 5] |= 1u << (v & 31);
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ bool bit(const uint32_t* bits, int j) { return (bits[j >> 5] >> (j & 31)) & 1u; }
+
+__device__ __forceinline__ bool in_prefix(uint32_t key, int v, uint32_t K, int cut) {
+  return key < K || (key == K && v <= cut);
+}
+
+// Transform one row of logits in the cluster. On return zs holds the
+// transformed logits (penalised, then / T) and `d` the descriptor; greedy rows
+// only get d.argmax.
+__device__ void transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
+                              const RowParams& p, TDesc& d, int32_t* status) {
+  SampleSmem* sm = c.sm;
+  for (int j = threadIdx.x; j < n; j += kST) zs[j] = lg[v0 + j];
+  build_bitmap(sm, bits, v0, n);
+  if (p.rep_penalty != 1.f)
+    for (int j = threadIdx.x; j < n; j += kST)
+      if (bit(bits, j)) zs[j] = penalize(zs[j], p.rep_penalty);
+  __syncthreads();
+  // argmax of the penalised logits
+  float bv = -INFINITY;
+  int bi = 0x7FFFFFFF;
+  bool bad = false;
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const float z = zs[j];
+    if (!isfinite(z)) bad = true;
+    if (better(z, v0 + j, bv, bi)) { bv = z; bi = v0 + j; }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, MTP_ERR_NONFINITE);
+  __shared__ float sv[kST / 32];
+  __shared__ int si[kST / 32];
+  block_argmax(bv, bi, sv, si);
+  if (threadIdx.x == 0) { sm->mail[c.ph].f[0] = bv; sm->mail[c.ph].i[0] = bi; }
+  Mail* m = c.publish();
+  float gv = -INFINITY;
+  int gi = 0x7FFFFFFF;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    Mail* x = c.remote(m, r);
+    if (better(x->f[0], x->i[0], gv, gi)) { gv = x->f[0]; gi = x->i[0]; }
+  }
+  d.argmax = gi;
+  d.k_key = 0xFFFFFFFFu;
+  d.k_cut = 0x7FFFFFFF;
+  d.p_key = 0xFFFFFFFFu;
+  d.p_cut = 0x7FFFFFFF;
+  d.m = 0.f;
+  d.S = 1.f;
+  d.kept = 1;
+  if (p.greedy) return;
+
+  for (int j = threadIdx.x; j < n; j += kST) zs[j] = zs[j] / p.temperature + 0.0f;
+  __syncthreads();
+  d.m = gv / p.temperature + 0.0f;
+  const float mx = d.m;
+
+  if (p.top_k > 0 && p.top_k < V) {
+    uint32_t K;
+    unsigned long long rem;
+    radix_select(c, zs, n, [](int) { return true; }, [](int) { return 1ull; },
+                 (unsigned long long)p.top_k, K, rem);
+    d.k_key = K;
+    d.k_cut = tie_cut(c, zs, n, v0, [](int) { return true; }, K, rem);
+  }
+  const uint32_t kK = d.k_key;
+  const int kC = d.k_cut;
+  auto in_k = [&](int j) { return in_prefix(desc_key(zs[j]), v0 + j, kK, kC); };
+  auto e_of = [&](int j) { return expf(zs[j] - mx); };
+
+  if (p.top_p > 0.f && p.top_p < 1.f) {
+    unsigned long long loc = 0;
+    for (int j = threadIdx.x; j < n; j += kST)
+      if (in_k(j)) loc += to_fix(e_of(j));
+    loc = block_sum_u64(loc, sm->wsum);
+    const unsigned long long SE = cluster_sum_u64(c, loc);
+    const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+    uint32_t K;
+    unsigned long long rem;
+    radix_select(c, zs, n, in_k, [&](int j) { return to_fix(e_of(j)); }, target, K, rem);
+    // every element tied at K carries the same weight
+    float zt = 0.f;
+    // find the weight of a tied element: any element with key K (zs value is determined by K)
+    {
+      uint32_t u = ~K;
+      u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+      zt = __uint_as_float(u);
+    }
+    const unsigned long long ew = to_fix(expf(zt - mx));
+    const unsigned long long need = ew > 0 ? (rem + ew - 1) / ew : 1ull;
+    d.p_key = K;
+    d.p_cut = tie_cut(c, zs, n, v0, in_k, K, need);
+  }
+  const uint32_t pK = d.p_key;
+  const int pC = d.p_cut;
+  auto kept = [&](int j) {
+    const uint32_t key = desc_key(zs[j]);
+    if (!in_prefix(key, v0 + j, kK, kC) || !in_prefix(key, v0 + j, pK, pC)) return false;
+    return !(p.min_p > 0.f) || expf(zs[j] - mx) >= p.min_p;
+  };
+  unsigned long long loc = 0, cnt = 0;
+  for (int j = threadIdx.x; j < n; j += kST)
+    if (kept(j)) { loc += to_fix(e_of(j)); ++cnt; }
+  loc = block_sum_u64(loc, sm->wsum);
+  cnt = block_sum_u64(cnt, sm->wsum);
+  if (threadIdx.x == 0) { sm->mail[c.ph].u[0] = loc; sm->mail[c.ph].u[1] = cnt; }
+  m = c.publish();
+  unsigned long long S = 0, K = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) { S += c.remote(m, r)->u[0]; K += c.remote(m, r)->u[1]; }
+  d.S = (float)((double)S / kFix);
+  d.kept = (int)K;
+}
+
+// Evaluate the transformed distribution at v from the raw logit.
+__device__ __forceinline__ float eval_p(const TDesc& d, const RowParams& p, float raw, bool pen, int v) {
+  float z = raw;
+  if (pen && p.rep_penalty != 1.f) z = penalize(z, p.rep_penalty);
+  if (p.greedy) return v == d.argmax ? 1.f : 0.f;
+  z = z / p.temperature + 0.0f;
+  const uint32_t key = desc_key(z);
+  if (!in_prefix(key, v, d.k_key, d.k_cut) || !in_prefix(key, v, d.p_key, d.p_cut)) return 0.f;
+  const float e = expf(z - d.m);
+  if (p.min_p > 0.f && !(e >= p.min_p)) return 0.f;
+  return e / d.S;
+}
+
+__device__ __forceinline__ void slice_of(int V, int rank, int& v0, int& n) {
+  const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
+  v0 = rank * per;
+  n = V - v0;
+  if (n > per) n = per;
+  if (n < 0) n = 0;
+}
+
+// Draft-side sampling (mode 0) or verify descriptors (mode 1).
+__global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ SampleArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  Clu c(sm);
+  const int task = blockIdx.x / kClusterCTAs;
+  int v0, n;
+  slice_of(a.V, c.rank, v0, n);
+  const int per = (a.V + kClusterCTAs - 1) / kClusterCTAs;
+  float* zs = reinterpret_cast<float*>(dyn + sizeof(SampleSmem));
+  uint32_t* bits = reinterpret_cast<uint32_t*>(zs + per);
+
+  int r, i;
+  const float* lg;
+  if (a.mode == 0) {
+    r = task;
+    i = a.pos;
+    lg = a.logits + (size_t)r * a.ld;
+  } else {
+    r = task / (a.depth + 1);
+    i = task - r * (a.depth + 1);
+    lg = a.logits + ((size_t)r * (a.depth + 1) + i) * a.V;
+  }
+  const RowParams p = a.p[r];
+  load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, i);
+  TDesc d;
+  transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status);
+
+  if (a.mode == 1) {
+    if (c.rank == 0 && threadIdx.x == 0) a.desc[task] = d;
+  } else if (p.greedy) {
+    if (c.rank == 0 && threadIdx.x == 0) a.draft_out[(size_t)r * a.depth + i] = d.argmax;
+  } else {
+    float* q = a.q + ((size_t)r * a.depth + i) * a.V;
+    const float mx = d.m, S = d.S;
+    for (int j = threadIdx.x; j < n; j += kST) {
+      const uint32_t key = desc_key(zs[j]);
+      float pv = 0.f;
+      if (in_prefix(key, v0 + j, d.k_key, d.k_cut) && in_prefix(key, v0 + j, d.p_key, d.p_cut)) {
+        const float e = expf(zs[j] - mx);
+        if (!(p.min_p > 0.f) || e >= p.min_p) pv = e / S;
+      }
+      zs[j] = pv;  // zs now holds q for this slice
+      q[v0 + j] = pv;
+    }
+    __syncthreads();
+    const float u = a.u[(size_t)r * a.depth + i];
+    const int x = cluster_draw(c, n, v0, [&](int j) { return to_fix(zs[j]); }, u);
+    if (c.rank == 0 && threadIdx.x == 0) a.draft_out[(size_t)r * a.depth + i] = x >= 0 ? x : d.argmax;
+  }
+  c.cl.sync();  // keep shared memory alive until every remote read is done
+}
+
+// Per-row accept chain and the one draw.
+__global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ VerifyArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  Clu c(sm);
+  const int r = blockIdx.x / kClusterCTAs;
+  const int d = a.depth;
+  int v0, n;
+  slice_of(a.V, c.rank, v0, n);
+  const int per = (a.V + kClusterCTAs - 1) / kClusterCTAs;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + sizeof(SampleSmem) + sizeof(float) * per);
+  const RowParams p = a.p[r];
+  const TDesc* desc = a.desc + (size_t)r * (d + 1);
+  const int32_t* dr = a.drafts + (size_t)r * d;
+  const float* lg = a.logits + (size_t)r * (d + 1) * a.V;
+  const float* uu = a.u + (size_t)r * (d + 1);
+
+  // accept chain (every CTA evaluates it identically)
+  int nacc = 0;
+  for (int i = 1; i <= d; ++i) {
+    const int x = dr[i - 1];
+    bool acc;
+    if (x < 0 || x >= a.V) {  // an out-of-range draft is rejected, never dereferenced
+      acc = false;
+    } else if (p.greedy) {
+      acc = x == desc[i - 1].argmax;
+    } else {
+      load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, i - 1);
+      bool pen = false;
+      for (int t = 0; t < sm->nwin; ++t) pen |= sm->wtok[t] == x;
+      const float pv = eval_p(desc[i - 1], p, lg[(size_t)(i - 1) * a.V + x], pen, x);
+      const float qv = a.q[((size_t)r * d + (i - 1)) * a.V + x];
+      acc = qv > 0.f && uu[i - 1] < pv / qv;
+      __syncthreads();
+    }
+    if (!acc) break;
+    nacc = i;
+  }
+  int y;
+  if (p.greedy) {
+    y = desc[nacc].argmax;
+  } else {
+    load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, nacc);
+    build_bitmap(sm, bits, v0, n);
+    const TDesc dn = desc[nacc];
+    const float* ln = lg + (size_t)nacc * a.V;
+    y = -1;
+    if (nacc < d) {
+      const float* qn = a.q + ((size_t)r * d + nacc) * a.V;
+      y = cluster_draw(c, n, v0, [&](int j) {
+        const float pv = eval_p(dn, p, ln[v0 + j], bit(bits, j), v0 + j);
+        const float rv = pv - qn[v0 + j];
+        return to_fix(rv > 0.f ? rv : 0.f);
+      }, uu[d]);
+    }
+    if (y < 0)
+      y = cluster_draw(c, n, v0, [&](int j) { return to_fix(eval_p(dn, p, ln[v0 + j], bit(bits, j), v0 + j)); },
+                       uu[d]);
+    if (y < 0) y = dn.argmax;
+  }
+  if (c.rank == 0 && threadIdx.x == 0) {
+    a.n_acc[r] = nacc;
+    int32_t* o = a.out_tok + (size_t)r * (d + 1);
+    for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
+    if (a.stats) {
+      int32_t* s = a.stats + (size_t)r * (d + 2);
+      s[0] += 1;
+      if (nacc < d) s[1] += 1;
+      for (int i = 1; i <= nacc; ++i) s[1 + i] += 1;
+    }
+  }
+  c.cl.sync();
+}
+
+static int sample_smem(int V) {
+  const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
+  return (int)(sizeof(SampleSmem) + sizeof(float) * per + sizeof(uint32_t) * ((per + 31) / 32) + 16);
+}
+
+template <class Args>
+static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cudaStream_t s) {
+  const int smem = sample_smem(V);
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tasks * kClusterCTAs);
+  cfg.blockDim = dim3(kST);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCTAs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k, a);
+}
+
+void launch_sample(const SampleArgs& a, cudaStream_t s) {
+  const int tasks = a.mode == 0 ? a.rows : a.rows * (a.depth + 1);
+  launch_cluster(k_sample, a, tasks, a.V, s);
+}
+
+void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verify, a, a.rows, a.V, s); }
+
+}  // namespace mtp
