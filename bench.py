@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the MTP self-speculative decoding step on one GB300.
+
+One step = one speculative round on the 27B-shaped Qwen3.5-family MTP head
+(bf16 weights, fp32 accumulation, batch 1, greedy, depth 2 = block 3, draft KV
+at 4096 positions):
+  mtp_draft   two head calls (the first also flushes the pending completed
+              pairs of the previous round into the draft KV)
+  target      synthetic stand-in for the caller's target forward: N(0,4)
+              logits for the 3 verify positions with the argmax planted on
+              each draft with probability 0.7
+  spec_verify rejection-sampling verify (greedy: argmax match)
+  kv_rollback drop the speculative draft-KV slots
+  one device->host read of the accepted count (the round's one sync)
+
+Reported value: drafted tokens per second over whole rounds.  The JSON line
+adds verify rounds/s, the roofline of the dominant kernel (the tied lm_head
+GEMV), an end-to-end figure with the target's outputs copied from pinned host
+memory each round, the CPU oracle's rate on a bounded sample, and the SM
+clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MTP draft tok/s + verify rounds/s at 1 GB300 (27B shape); HBM GB/s vs peak"
+DEPTH = 2
+KV_LEN = 4096
+POOL = 16
+WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064), bf16 weights, "
+            "batch 1, greedy, depth 2 (block 3), draft KV 4096")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 7:
+                    try:
+                        rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+                    except ValueError:
+                        pass
+        os.unlink(self.f.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[0] for r in rows]) if rows else None,
+                "sm_max_mhz": max(r[1] for r in rows) if rows else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def combine_ranks(local_ms: float, local_units: int, device=None):
+    """Replicas only: the job's time is the slowest rank's, its work the sum
+    over ranks.  Returns (max_ms, total_units); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(local_ms), int(local_units)
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
+def build_workload(seed: int, rank: int, vocab: int = 0):
+    import dataclasses
+    import synth
+    s = synth.QWEN27B
+    if vocab:
+        s = dataclasses.replace(s, vocab=vocab, name=f"{s.name}-V{vocab}")
+    model = synth.make_model(s, seed)
+    K, V = synth.kv_prefill(s, seed, 1, KV_LEN + 1024, [KV_LEN])
+    tag = f"r{rank}"
+    base = synth.normal(seed, tag + ":target_logits", (POOL, DEPTH + 1, s.vocab), std=4.0)
+    thid = synth.normal(seed, tag + ":target_hidden", (POOL, DEPTH + 1, s.hidden), dtype="bf16")
+    tok0 = int(synth.randint(seed, tag + ":tok0", (1,), s.vocab)[0])
+    return s, model, K, V, base, thid, tok0
+
+
+def plant_device(lg, draft, coins):
+    """Device-side planting (torch ops, no host sync): see synth.plant_logits."""
+    import torch
+    for i, c in enumerate(coins):
+        row = lg[0, i]
+        x = draft[0, i].long().view(1)
+        top = torch.topk(row, 2)
+        if c:
+            row.index_put_((x,), top.values[0:1] + 1.0)
+        else:
+            new = torch.where(top.indices[0:1] == x, top.values[1:2] - 1.0, row.index_select(0, x))
+            row.index_put_((x,), new)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    s, model, K, V, base, thid, tok0 = build_workload(args.seed, rank, args.vocab)
+    to = lambda a: (torch.from_numpy(a).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)).to(dev)
+    tensors = {n: to(a) for n, a in model.tensors.items()}
+    embed = to(model.embed)
+    kk, vv = to(K), to(V)
+    klen = torch.tensor([KV_LEN], dtype=torch.int32, device=dev)
+    cfg = m.make_config(s, 1, KV_LEN + 1024, DEPTH)
+    h = m.mtp_load(cfg, tensors, embed, None, kk, vv, klen, lengths=[KV_LEN])
+    params = m.sampling_array([dict(temperature=0.0)])
+    base_d = to(base)
+    thid_d = to(thid)
+    base_h = torch.from_numpy(base).pin_memory()
+    thid_h = torch.from_numpy(thid.view(np.int16)).pin_memory()
+    rounds = args.warmup + args.steps
+    coins = synth.uniform(args.seed, f"r{rank}:coins", (2 * rounds + 8, DEPTH)) < 0.7
+    draft = torch.zeros((1, DEPTH), dtype=torch.int32, device=dev)
+    lg = torch.zeros((1, DEPTH + 1, s.vocab), dtype=torch.float32, device=dev)
+    u = torch.zeros((1, DEPTH + 1), dtype=torch.float32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_tok = torch.zeros((1, DEPTH + 1), dtype=torch.int32, device=dev)
+    first_tok = torch.zeros((1, DEPTH + 1), dtype=torch.int32, device=dev)
+    first_tok[0, 0] = tok0
+    ws = torch.zeros(m.spec_verify_workspace_bytes(1, DEPTH, s.vocab), dtype=torch.uint8, device=dev)
+    h_out = torch.zeros(DEPTH + 2, dtype=torch.int32).pin_memory()
+    hid_in = torch.zeros((1, DEPTH + 1, s.hidden), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev_v0 = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
+    ev_v1 = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
+
+    state = {"P": 1, "tok": first_tok, "ncommit": 0, "nacc": 0}
+
+    def one_round(i, e2e=False, timed_verify=False):
+        P = state["P"]
+        if e2e:
+            hid_in.view(torch.int16).copy_(thid_h[i % POOL].view(1, DEPTH + 1, s.hidden), non_blocking=True)
+            hid = hid_in
+        else:
+            hid = thid_d[i % POOL].view(1, DEPTH + 1, s.hidden)
+        m.mtp_draft(h, DEPTH, [P], state["tok"], hid, params, draft)
+        if e2e:
+            lg.copy_(base_h[i % POOL].view(1, DEPTH + 1, s.vocab), non_blocking=True)
+        else:
+            lg.copy_(base_d[i % POOL].view(1, DEPTH + 1, s.vocab))
+        plant_device(lg, draft, coins[i])
+        if timed_verify:
+            ev_v0[i].record(stream)
+        m.spec_verify(lg, draft, params, u, n_acc, out_tok, ws, h_out=h_out)
+        if timed_verify:
+            ev_v1[i].record(stream)
+        m.kv_rollback(h, 1, DEPTH)
+        stream.synchronize()
+        n = int(h_out[0])
+        state["P"] = n + 1
+        state["tok"] = out_tok
+        state["ncommit"] += n + 1
+        state["nacc"] += n
+
+    # warmup
+    for i in range(args.warmup):
+        one_round(i)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    # timed region (device-resident inputs)
+    clocks = Clocks(local_rank)
+    m.mtp_profile_enable(h, True)
+    m.mtp_profile_read(h)
+    launches0 = m.mtp_kernel_launches()
+    state["ncommit"] = state["nacc"] = 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    wall0 = time.perf_counter()
+    for i in range(args.warmup, rounds):
+        one_round(i, timed_verify=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = m.mtp_kernel_launches() - launches0
+    clk = clocks.stop()
+    prof = m.mtp_profile_read(h)
+    m.mtp_profile_enable(h, False)
+    ms = t0.elapsed_time(t1)
+    ncommit, nacc = state["ncommit"], state["nacc"]
+    verify_ms = [ev_v0[i].elapsed_time(ev_v1[i]) for i in range(args.warmup, rounds)]
+    ms, drafted = combine_ranks(ms, args.steps * DEPTH, dev)
+
+    # end to end: target outputs copied from pinned host memory, result read back
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = time.perf_counter()
+    for i in range(rounds, rounds + (0 if args.quick else args.steps)):
+        one_round(i % (2 * rounds), e2e=True)
+    torch.cuda.synchronize()
+    e2e_s = max(time.perf_counter() - e0, 1e-9)
+    e2e_ms, e2e_units = combine_ranks(e2e_s * 1e3, (0 if args.quick else args.steps) * DEPTH, dev)
+    e2e_s = e2e_ms / 1e3
+
+    h.close()
+
+    H, V = s.hidden, s.vocab
+    lm_bytes = V * H * 2 + V * 4 + H * 4
+    lm_ms, lm_n = prof["lm_head"]
+    lm_avg_s = lm_ms / max(lm_n, 1) / 1e3
+    peak, src = peaks()
+    achieved = lm_bytes / lm_avg_s / 1e9
+    breakdown = {k: round(v[0] / max(v[1], 1) * 1e3, 2) for k, v in prof.items() if v[1]}
+    layer_bytes = 2 * (H * 2 * H + (24 * 256 + 2 * 4 * 256) * H + H * 24 * 256 + 3 * 17408 * H)
+    kv_bytes = 2 * 4 * 256 * 2 * KV_LEN
+    step_bytes = layer_bytes + lm_bytes + kv_bytes
+    draft_ms = sum(v[0] for k, v in prof.items() if k not in ("rollback",)) / args.steps
+    result = {
+        "metric": METRIC,
+        "value": round(drafted / (ms / 1e3), 2),
+        "unit": "draft tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Philox weights N(0,0.02), KV/hidden N(0,1), target logits N(0,4) planted)",
+        "config": {"workload": WORKLOAD if not args.vocab else WORKLOAD.replace("V=152064", f"V={args.vocab}"),
+                   "rows": 1, "depth": DEPTH, "kv_len": KV_LEN,
+                   "l2": "inputs larger than L2 (2.36 GB of weights streamed per draft step)",
+                   "parallelism": f"replicas x{world}"},
+        "verify_rounds_per_s": round(world * args.steps / (ms / 1e3), 2),
+        "committed_tok_per_s": round(world * ncommit / (ms / 1e3), 2),
+        "acceptance_per_draft": round(nacc / (args.steps * DEPTH), 4),
+        "verify_us_per_round": round(1e3 * float(np.mean(verify_ms)), 2),
+        "draft_step_us": round(1e3 * draft_ms / DEPTH, 1),
+        "draft_step_hbm_frac": round(step_bytes / (draft_ms / DEPTH / 1e3) / 1e9 / peak, 4),
+        "kernel_avg_us": breakdown,
+        "roofline": {"bound": "hbm", "kernel": "lm_head GEMV (tied head, fused final norm + argmax)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "bytes_per_launch": lm_bytes},
+        "gpu_launches": int(launches),
+        "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
+                "h2d_bytes_per_step": (DEPTH + 1) * V * 4 + (DEPTH + 1) * H * 2,
+                "d2h_bytes_per_step": 4 * (DEPTH + 2)},
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    return result, (s, model, K, V, base, thid, tok0, coins)
+
+
+def cpu_rounds(work, budget_s: float, max_rounds: int):
+    """The oracle, as it stands, on the same workload: whole rounds until the
+    time budget is spent.  Returns (rounds, seconds, threads)."""
+    import oracle
+    import synth
+    s, model, K, V, base, thid, tok0, coins = work
+    head = oracle.Head(s, model.tensors, model.embed)
+    Kc, Vc = K.copy(), V.copy()
+    slot = KV_LEN
+    p = oracle.make_params(0.0)
+    toks = [tok0]
+    hids = [thid[0, 0]]
+    t0 = time.perf_counter()
+    done = 0
+    while done < max_rounds:
+        d = head.draft(Kc[0], Vc[0], slot, toks, hids, DEPTH, p, np.zeros(0, np.int32), np.zeros(DEPTH, np.float32))
+        lg = synth.plant_logits(base[done % POOL], d["drafts"], coins[done])
+        n, out, _ = oracle.verify_row(lg, d["drafts"], None, p, np.zeros(0, np.int32),
+                                      np.zeros(DEPTH + 1, np.float32))
+        slot += len(toks)
+        toks = [int(t) for t in out[:n + 1]]
+        hids = [thid[done % POOL, j] for j in range(n + 1)]
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return done, time.perf_counter() - t0, int(os.environ.get("OMP_NUM_THREADS", os.cpu_count()))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=2)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (small profiling cases)")
+    ap.add_argument("--quick", action="store_true", help="skip the end-to-end and CPU-baseline legs")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle as it stands (rank 0 only).
+        if rank != 0:
+            return
+        import oracle
+        import synth
+        synth.build()
+        oracle.build()
+        s, model, K, V, base, thid, tok0 = build_workload(args.seed, 0)
+        coins = synth.uniform(args.seed, "r0:coins", (args.warmup + args.steps + 8, DEPTH)) < 0.7
+        work = (s, model, K, V, base, thid, tok0, coins)
+        per_step_budget = max(1.0, 150.0 / (args.steps + args.warmup))
+        n, sec, thr = cpu_rounds(work, per_step_budget * args.steps, args.steps)
+        val = n * DEPTH / sec
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "draft tok/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sec / max(n, 1), 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64-accumulate over bf16 weights", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows": 1, "depth": DEPTH, "kv_len": KV_LEN},
+            "cpu_baseline": {"value": round(val, 3), "unit": "draft tok/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{n} whole rounds (2 draft steps + verify) of the benchmark workload"},
+            "e2e": {"value": round(val, 3), "unit": "draft tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    from mtp_speculative_decoding_step_gb300 import _build
+    import oracle
+    import synth
+    if rank == 0:
+        _build.build()
+        synth.build()
+        oracle.build()
+    if world > 1:
+        torch.distributed.barrier()
+    result, work = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.quick:
+        n, sec, thr = cpu_rounds(work, args.cpu_budget, 8)
+        result["cpu_baseline"] = {"value": round(n * DEPTH / sec, 3), "unit": "draft tok/s", "cores": thr,
+                                  "kind": "oracle",
+                                  "sample": f"{n} whole rounds (2 draft steps + verify) of the same workload"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -229,6 +229,9 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
 mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* d_n_acc,
                        int32_t* d_target_len, int32_t depth, int32_t zero_tail);
 
+/* Number of kernels this library has launched in the process so far. */
+int64_t mtp_kernel_launches(void);
+
 /* Timing hook for the benchmark: when enabled, every kernel the handle
  * launches is bracketed by CUDA events on its stream; mtp_profile_read
  * synchronises those events and returns, per kernel kind, the summed

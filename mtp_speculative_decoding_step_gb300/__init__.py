@@ -31,7 +31,7 @@ EXPORTS = (
     "mtp_default_block_size", "mtp_status_str", "mtp_load", "mtp_free", "mtp_get_lengths",
     "mtp_set_lengths", "mtp_device_status", "mtp_flush", "mtp_draft", "spec_verify_workspace_bytes",
     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_kinds", "mtp_profile_kind_name",
-    "mtp_profile_read",
+    "mtp_profile_read", "mtp_kernel_launches",
 )
 
 
@@ -98,6 +98,7 @@ def lib():
         L.mtp_profile_kind_name.argtypes = [i32]
         L.mtp_profile_kind_name.restype = ctypes.c_char_p
         L.mtp_profile_read.argtypes = [vp, vp, vp]
+        L.mtp_kernel_launches.restype = ctypes.c_int64
         for name in ("mtp_load", "mtp_free", "mtp_get_lengths", "mtp_set_lengths", "mtp_flush", "mtp_draft",
                      "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_read"):
             getattr(L, name).restype = ctypes.c_int
@@ -269,3 +270,7 @@ def mtp_profile_read(h: Handle) -> dict:
     cnt = np.zeros(n, np.int32)
     _check(lib().mtp_profile_read(h.ptr, ms.ctypes.data, cnt.ctypes.data), "mtp_profile_read")
     return {lib().mtp_profile_kind_name(i).decode(): (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def mtp_kernel_launches() -> int:
+    return int(lib().mtp_kernel_launches())

@@ -1,0 +1,286 @@
+// Flush path on the 5th-generation tensor cores (sm_103a).
+//
+// A flush writes up to 256 completed pairs (token at S+1, target hidden at S,
+// "Ollama qwen3_5 MTP loader and SelfDraft path", Facts: pairing, 256-token
+// cap) into the draft KV. For a one-layer head the K/V of a slot depend only on
+// its pair, so a flush of M pairs is two dense contractions:
+//   h0[M, H]      = x[M, 2H] . W_fc^T          x = [norm_e(E[tok]) ; norm_h(hid)]
+//   kv[M, 2 kw]   = b[M, H] . [W_k ; W_v]^T    b = norm_in(h0)
+// followed by the per-head k_norm + RoPE + cache store.
+//
+// k_tc_gemm: D[M, N] (fp32) = A[M, K] . B[N, K]^T with A, B bf16 and K-major.
+// One CTA owns a 128 x BN tile of D for a K range:
+//   warp 0, one thread : TMA producer (128B-swizzled 64-wide K tiles of A, B)
+//   warp 1, one thread : tcgen05.mma issuer (M128 x N BN x K16 per instruction)
+//   warps 0-3          : epilogue, TMEM -> registers -> global (fp32)
+// The accumulator lives in tensor memory (BN columns). Split-K CTAs write
+// partial tiles [split][M][N] that the consumer kernel sums in split order.
+// Every mbarrier wait is bounded: on expiry the CTA raises the status word,
+// waits (bounded) for its own copies, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mtp {
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;  // bf16 elements: one 128-byte swizzle row
+constexpr unsigned kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false on expiry.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (unsigned i = 0; i < kWaitLimit; ++i)
+    if (mbar_try(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in 128B-swizzled 8-row x
+// 128-byte atoms (stride between 8-row groups 1024 bytes).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);        // start address
+  d |= (uint64_t)1 << 16;                        // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset
+  d |= (uint64_t)1 << 46;                        // descriptor version
+  d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulate, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace
+
+struct TcGemmArgs {
+  int M, N, K;
+  int n_split_b;     // columns [0, n_split_b) come from map b0, the rest from map b1
+  int ksplit;        // number of K splits (gridDim.z)
+  float* D;          // [ksplit][M][ldd]
+  long long ldd;
+  int32_t* status;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
+              const __grid_constant__ CUtensorMap tb1, const TcGemmArgs a) {
+  constexpr uint32_t kABytes = kTileM * kTileK * 2;
+  constexpr uint32_t kBBytes = BN * kTileK * 2;
+  constexpr uint32_t kStage = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * kStage);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kTileM, n0 = blockIdx.y * BN;
+  const int nk_total = a.K / kTileK;
+  const int per = (nk_total + a.ksplit - 1) / a.ksplit;
+  const int kb = blockIdx.z * per;
+  const int nk = min(per, nk_total - kb);
+  const CUtensorMap* tb = n0 < a.n_split_b ? &tb0 : &tb1;
+  const int nb = n0 < a.n_split_b ? n0 : n0 - a.n_split_b;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(accf), 1);
+    *s_fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES, r = i / STAGES;
+      if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1)) { *s_fail = 1; break; }
+      uint8_t* as = base + s * kStage;
+      mbar_expect_tx(smem_u32(&full[s]), kStage);
+      tma_load_2d(smem_u32(as), &ta, (kb + i) * kTileK, m0, smem_u32(&full[s]));
+      tma_load_2d(smem_u32(as + kABytes), tb, (kb + i) * kTileK, nb, smem_u32(&full[s]));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kTileM, BN);
+    bool ok = true;
+    for (int i = 0; i < nk && ok; ++i) {
+      const int s = i % STAGES, r = i / STAGES;
+      if (!mbar_wait(smem_u32(&full[s]), r & 1)) { ok = false; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t as = smem_u32(base + s * kStage), bs = as + kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kTileK / 16; ++kk)
+        mma_bf16(tmem, sdesc(as + kk * 32), sdesc(bs + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(smem_u32(&empty[s]));
+    }
+    if (!ok) *s_fail = 1;
+    mma_commit(smem_u32(accf));
+  }
+  __syncwarp();
+
+  // epilogue: TMEM lanes 32w..32w+31 hold rows m0 + 32w + lane
+  const bool got = mbar_wait(smem_u32(accf), 0);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const int row = m0 + warp * 32 + lane;
+  float* drow = a.D + ((size_t)blockIdx.z * a.M + row) * a.ldd + n0;
+  if (got) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+      if (row < a.M) {
+        float4* d4 = reinterpret_cast<float4*>(drow + c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && (!got || *s_fail)) {
+    flag_status(a.status, MTP_ERR_TIMEOUT);
+    // let any copy still in flight land before the shared memory is released
+    for (int s = 0; s < STAGES; ++s) mbar_wait(smem_u32(&full[s]), 0);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] as a 2-D map with a 64 x box_rows box.
+static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// D[split][M][N] = A[M][K] . [B0; B1]^T  (B0 rows [0, n0rows), B1 the rest).
+template <int BN>
+static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int ksplit,
+                      float* D, int32_t* status, cudaStream_t s) {
+  constexpr int STAGES = BN <= 128 ? 6 : 5;
+  if (M < 1 || K % kTileK != 0 || N % BN != 0 || n0rows % BN != 0 || ksplit < 1) return false;
+  CUtensorMap ta, tb0, tb1;
+  if (!make_map(&ta, A, M, K, kTileM)) return false;
+  if (!make_map(&tb0, B0, n0rows, K, BN)) return false;
+  if (!make_map(&tb1, B1 ? B1 : B0, B1 ? N - n0rows : n0rows, K, BN)) return false;
+  TcGemmArgs a;
+  a.M = M; a.N = N; a.K = K; a.n_split_b = n0rows; a.ksplit = ksplit; a.D = D; a.ldd = N; a.status = status;
+  const int smem = STAGES * (kTileM + BN) * kTileK * 2 + 1024 + 256;
+  auto k = k_tc_gemm<BN, STAGES>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  dim3 grid((M + kTileM - 1) / kTileM, N / BN, ksplit);
+  k<<<grid, 128, smem, s>>>(ta, tb0, tb1, a);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess;
+}
+
+bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
+                    int ksplit, float* D, int32_t* status, cudaStream_t s) {
+  if (bn == 160) return tc_gemm_t<160>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+  return tc_gemm_t<128>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+}
+
+}  // namespace mtp

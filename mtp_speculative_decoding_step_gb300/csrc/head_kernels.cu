@@ -19,6 +19,10 @@
 
 namespace mtp {
 
+static unsigned long long g_launches = 0;
+void count_launch(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
+unsigned long long launches_so_far() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
 // ---------------------------------------------------------------- GEMV
 
 template <typename WT>
@@ -265,6 +269,7 @@ static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
   auto k = k_gemv<WT, MT>;
   if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   k<<<a.ngroups * a.S, 256, smem, s>>>(a);
+  count_launch();
 }
 
 void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
@@ -293,27 +298,32 @@ __device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int dh, i
 }
 
 // grid (M, nq + nkv), block dh/2 threads: thread i owns the pair (i, i + dh/2).
+__device__ __forceinline__ float qkv_at(const QkvPostArgs& a, int m, int col) {
+  const float* p = a.qkv + (size_t)m * a.ld + col;
+  float v = p[0];
+  for (int s = 1; s < a.nsplit; ++s) v += p[(size_t)s * a.split_stride];
+  return v;
+}
+
 __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
   __shared__ float red[32];
   const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.dh / 2;
-  const int qw = a.nq * a.dh, kw = a.nkv * a.dh;
-  const float* src = a.qkv + (size_t)m * (qw + 2 * kw);
   const int slot = a.slot[m], row = a.row[m];
   if (h < a.nq) {
     const int qd = a.qdst[m];
-    if (qd < 0) return;  // uniform across the block
-    float x0 = src[h * a.dh + i], x1 = src[h * a.dh + i + half];
+    if (qd < 0 || a.q_off < 0) return;  // uniform across the block
+    float x0 = qkv_at(a, m, a.q_off + h * a.dh + i), x1 = qkv_at(a, m, a.q_off + h * a.dh + i + half);
     const float ss = block_sum(x0 * x0 + x1 * x1, red);
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
     x0 = x0 * inv * a.wq[i];
     x1 = x1 * inv * a.wq[i + half];
     rope_pair(x0, x1, i, a.dh, slot, a.theta);
-    float* dst = a.q_out + (size_t)qd * qw + h * a.dh;
+    float* dst = a.q_out + (size_t)qd * a.nq * a.dh + h * a.dh;
     dst[i] = x0;
     dst[i + half] = x1;
   } else {
     const int g = h - a.nq;
-    float x0 = src[qw + g * a.dh + i], x1 = src[qw + g * a.dh + i + half];
+    float x0 = qkv_at(a, m, a.k_off + g * a.dh + i), x1 = qkv_at(a, m, a.k_off + g * a.dh + i + half);
     const float ss = block_sum(x0 * x0 + x1 * x1, red);
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
     x0 = x0 * inv * a.wk[i];
@@ -322,15 +332,73 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
     const size_t off = (((size_t)row * a.nkv + g) * a.cap + slot) * a.dh;
     store_elem(a.kc, a.wdt, off + i, x0);
     store_elem(a.kc, a.wdt, off + i + half, x1);
-    const float* vs = src + qw + kw + g * a.dh;
-    store_elem(a.vc, a.wdt, off + i, vs[i]);
-    store_elem(a.vc, a.wdt, off + i + half, vs[i + half]);
+    store_elem(a.vc, a.wdt, off + i, qkv_at(a, m, a.v_off + g * a.dh + i));
+    store_elem(a.vc, a.wdt, off + i + half, qkv_at(a, m, a.v_off + g * a.dh + i + half));
   }
+}
+
+// grid (M), block 256: x[m] = [norm_e(E[tok]) ; norm_h(hid)] rounded to bf16.
+__global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
+  __shared__ float red[32];
+  const int m = blockIdx.x, H = a.H;
+  int t = a.tok[a.tok_idx[m]];
+  if (t < 0 || t >= a.vocab) {
+    if (threadIdx.x == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+    t = 0;
+  }
+  uint16_t* x = a.x + (size_t)m * 2 * H;
+  for (int half = 0; half < 2; ++half) {
+    const void* src = half == 0 ? a.E : a.hid;
+    const int dt = half == 0 ? a.wdt : a.hid_dt;
+    const size_t base = half == 0 ? (size_t)t * H : (size_t)a.hid_item[m] * H;
+    const float* w = half == 0 ? a.nw_e : a.nw_h;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+      const float v = load_elem(src, dt, base + k);
+      ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv = rsqrtf(ss / (float)H + a.eps);
+    for (int k = threadIdx.x; k < H; k += blockDim.x)
+      x[half * H + k] = f_to_bf16(load_elem(src, dt, base + k) * inv * w[k]);
+  }
+}
+
+void launch_flush_x(const FlushXArgs& a, int M, cudaStream_t s) {
+  k_flush_x<<<M, 256, 0, s>>>(a);
+  count_launch();
+}
+
+__global__ void k_flush_norm(const float* part, int nsplit, long long split_stride, int H, const float* w,
+                             float eps, uint16_t* b) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  const float* p = part + (size_t)m * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    float v = p[k];
+    for (int sidx = 1; sidx < nsplit; ++sidx) v += p[(size_t)sidx * split_stride + k];
+    ss = fmaf(v, v, ss);
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)H + eps);
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    float v = p[k];
+    for (int sidx = 1; sidx < nsplit; ++sidx) v += p[(size_t)sidx * split_stride + k];
+    b[(size_t)m * H + k] = f_to_bf16(v * inv * w[k]);
+  }
+}
+
+void launch_flush_norm(const float* part, int nsplit, long long split_stride, int M, int H, const float* w,
+                       float eps, uint16_t* b, cudaStream_t s) {
+  k_flush_norm<<<M, 256, 0, s>>>(part, nsplit, split_stride, H, w, eps, b);
+  count_launch();
 }
 
 void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
   dim3 grid(a.M, a.nq + a.nkv);
   k_qkv_post<<<grid, a.dh / 2, 0, s>>>(a);
+  count_launch();
 }
 
 // ------------------------------------------------------- decode attention
@@ -437,6 +505,7 @@ template <int DH, int G>
 static void attn_t(const AttnArgs& a, int nch, cudaStream_t s) {
   k_attn_chunk<DH, G><<<dim3(nch, a.nkv, a.Mh), 128, 0, s>>>(a);
   k_attn_merge<DH><<<dim3(a.nq, a.Mh), DH, 0, s>>>(a);
+  count_launch(2);
 }
 
 void launch_attention(const AttnArgs& a, cudaStream_t s) {
@@ -472,6 +541,7 @@ __global__ void k_norm_copy(const void* src, int dt, int n, float shift, float* 
 
 void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, cudaStream_t s) {
   k_norm_copy<<<(n + 255) / 256, 256, 0, s>>>(src, dt, n, shift, dst);
+  count_launch();
 }
 
 // grid (rows, nkv): set lengths, trim target lengths, zero dropped slots.
@@ -492,6 +562,7 @@ __global__ void k_rollback(const __grid_constant__ RollbackArgs a) {
 
 void launch_rollback(const RollbackArgs& a, cudaStream_t s) {
   k_rollback<<<dim3(a.rows, a.nkv), 256, 0, s>>>(a);
+  count_launch();
 }
 
 struct LenArgs {
@@ -510,6 +581,7 @@ void launch_set_len(int32_t* len, int rows, const int* h_len, cudaStream_t s) {
   a.rows = rows;
   for (int r = 0; r < rows; ++r) a.v[r] = h_len[r];
   k_set_len<<<1, kMaxRows, 0, s>>>(a);
+  count_launch();
 }
 
 }  // namespace mtp

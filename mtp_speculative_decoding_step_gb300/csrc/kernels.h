@@ -7,6 +7,9 @@
 
 namespace mtp {
 
+// Count of kernels launched by this library (for the benchmark's launch tally).
+void count_launch(int n = 1);
+
 constexpr int kMaxItems = 256;   // pairs per head call (the pages' flush cap)
 constexpr int kMaxRows = 64;
 constexpr int kAttnChunk = 64;   // KV slots per decode-attention block
@@ -54,7 +57,11 @@ void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.
 struct QkvPostArgs {
-  const float* qkv;      // [M][qw + 2 kw]
+  const float* qkv;      // item m's projections at qkv + m*ld (+ s*split_stride, summed over splits)
+  long long ld;
+  int q_off, k_off, v_off;  // column offsets; q_off < 0: no q
+  int nsplit;
+  long long split_stride;
   int M, nq, nkv, dh, wdt;
   float eps, theta;
   const float* wq;
@@ -68,6 +75,29 @@ struct QkvPostArgs {
   short qdst[kMaxItems];
 };
 void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s);
+
+// Flush on tensor cores: bf16 activations for the two contractions.
+struct FlushXArgs {
+  const void* E;
+  int wdt, H, vocab;
+  const int32_t* tok;
+  const void* hid;
+  int hid_dt;
+  const float* nw_e;
+  const float* nw_h;
+  float eps;
+  uint16_t* x;           // [M][2H] bf16
+  int32_t* status;
+  int tok_idx[kMaxItems];
+  int hid_item[kMaxItems];  // hidden of item m at hid + hid_item[m] * H
+};
+void launch_flush_x(const FlushXArgs& a, int M, cudaStream_t s);
+// b[m] = bf16(rmsnorm(sum_s part[s][m], w))
+void launch_flush_norm(const float* part, int nsplit, long long split_stride, int M, int H, const float* w,
+                       float eps, uint16_t* b, cudaStream_t s);
+// D[split][M][N] = A[M][K] . [B0; B1]^T on tcgen05 (bf16 in, fp32 out).
+bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
+                    int ksplit, float* D, int32_t* status, cudaStream_t s);
 
 // Decode attention of the head items over slots 0..slot (split over chunks).
 struct AttnArgs {

@@ -14,6 +14,12 @@
 
 using namespace mtp;
 
+constexpr int kTcFlushMinItems = 16;  // below this the flush stays on the GEMV path
+
+namespace mtp {
+unsigned long long launches_so_far();
+}
+
 namespace {
 
 // The fifteen tensors of the published head ("support the qwen3_5_mtp
@@ -78,6 +84,8 @@ struct mtp_handle {
   float *h0 = nullptr, *qkv = nullptr, *qrot = nullptr, *o = nullptr, *h1 = nullptr, *mlp = nullptr,
         *h2 = nullptr, *logits = nullptr, *po = nullptr, *pml = nullptr, *part = nullptr, *gmax = nullptr;
   int *gidx = nullptr, *counters = nullptr, *done = nullptr;
+  uint16_t *xb = nullptr, *bb = nullptr;  // bf16 activations of the tensor-core flush
+  float* tcpart = nullptr;                // split-K partial tiles of the tensor-core flush
   int32_t* status = nullptr;
   size_t part_floats = 0;
   int max_chunks = 0, lm_groups_max = 0, counters_n = 0;
@@ -294,6 +302,7 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
       QkvPostArgs a;
       std::memset(&a, 0, sizeof(a));
       a.qkv = h->qkv + (size_t)m0 * ldq;
+      a.ld = ldq; a.q_off = 0; a.k_off = qw; a.v_off = qw + kw; a.nsplit = 1; a.split_stride = 0;
       a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
       a.eps = c.eps; a.theta = c.rope_theta;
       a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN];
@@ -366,6 +375,61 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     j.x = h->h2; j.ldx = H; j.nw = h->nrm[T_NORM]; j.y = logits; j.ldy = ld_logits;
     j.amax_out = amax_out; j.amax_idx = amax_out ? amax_idx.data() : nullptr;
     run_gemv(h, j, R, s);
+  }
+  return cuda_ok(cudaGetLastError());
+}
+
+// K splits so that (M tiles) x (N tiles) x splits fills at most one wave.
+int tc_splits(int mtiles, int ntiles, int ktiles, int sms, int max_splits) {
+  int best = 1;
+  for (int k = 1; k <= max_splits; ++k)
+    if (mtiles * ntiles * k <= sms && ktiles / k >= 4) best = k;
+  return best;
+}
+
+// Flush of mp pairs on tcgen05: x -> fc -> input norm -> k/v -> k_norm + RoPE + store.
+mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, const int32_t* d_tok,
+                              const void* d_hid, int hid_dtype, cudaStream_t s) {
+  const mtp_config& c = h->cfg;
+  const int H = c.hidden, kw = c.n_kv * c.head_dim;
+  {
+    ProfScope ps(h, s, PK_FLUSH_FC);
+    FlushXArgs x;
+    std::memset(&x, 0, sizeof(x));
+    x.E = h->embed; x.wdt = c.dtype; x.H = H; x.vocab = c.vocab;
+    x.tok = d_tok; x.hid = d_hid; x.hid_dt = hid_dtype;
+    x.nw_e = h->nrm[T_PRE_E]; x.nw_h = h->nrm[T_PRE_H]; x.eps = c.eps;
+    x.x = h->xb; x.status = h->status;
+    for (int m = 0; m < mp; ++m) {
+      x.tok_idx[m] = all.tok_idx[m0 + m];
+      x.hid_item[m] = (int)(all.hid_off[m0 + m] / H);
+    }
+    launch_flush_x(x, mp, s);
+    const int bn = H % 160 == 0 ? 160 : 128;
+    const int ks = tc_splits((mp + 127) / 128, H / bn, 2 * H / 64, h->sms, 8);
+    if (!launch_tc_gemm(h->xb, mp, 2 * H, h->w[T_FC], H, nullptr, H, bn, ks, h->tcpart, h->status, s))
+      return MTP_ERR_CUDA;
+    launch_flush_norm(h->tcpart, ks, (long long)mp * H, mp, H, h->nrm[T_IN], c.eps, h->bb, s);
+  }
+  {
+    ProfScope ps(h, s, PK_FLUSH_KV);
+    const int ks = tc_splits((mp + 127) / 128, 2 * kw / 128, H / 64, h->sms, 8);
+    if (!launch_tc_gemm(h->bb, mp, H, h->w[T_K], kw, h->w[T_V], 2 * kw, 128, ks, h->tcpart, h->status, s))
+      return MTP_ERR_CUDA;
+    QkvPostArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.qkv = h->tcpart; a.ld = 2 * kw; a.q_off = -1; a.k_off = 0; a.v_off = kw;
+    a.nsplit = ks; a.split_stride = (long long)mp * 2 * kw;
+    a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
+    a.eps = c.eps; a.theta = c.rope_theta;
+    a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN]; a.q_out = h->qrot;
+    a.kc = h->kv.k; a.vc = h->kv.v; a.cap = c.kv_capacity;
+    for (int m = 0; m < mp; ++m) {
+      a.row[m] = all.row[m0 + m];
+      a.slot[m] = all.slot[m0 + m];
+      a.qdst[m] = -1;
+    }
+    launch_qkv_post(a, s);
   }
   return cuda_ok(cudaGetLastError());
 }
@@ -514,6 +578,11 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   h->lm_groups_max = std::max(h->lm_groups_max, c.vocab / gemv_rows_per_group(1));
   h->counters_n = groups;
   if (st == MTP_OK) st = alloc(h, &h->part, part);
+  if (c.dtype == MTP_DTYPE_BF16) {
+    if (st == MTP_OK) st = alloc(h, &h->xb, (size_t)kMaxItems * 2 * H);
+    if (st == MTP_OK) st = alloc(h, &h->bb, (size_t)kMaxItems * H);
+    if (st == MTP_OK) st = alloc(h, &h->tcpart, (size_t)kMaxItems * std::max(8 * H, 8 * 2 * kw));
+  }
   if (st == MTP_OK) st = alloc(h, &h->gmax, (size_t)8 * h->lm_groups_max);
   if (st == MTP_OK) st = alloc(h, &h->gidx, (size_t)8 * h->lm_groups_max);
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
@@ -587,6 +656,13 @@ mtp_status mtp_flush(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* h_
       all.hid_off.push_back(((long long)r * pmax + j) * c.hidden);
     }
   all.n = (int)all.row.size();
+  if (c.dtype == MTP_DTYPE_BF16 && all.n >= kTcFlushMinItems) {
+    for (int m0 = 0; m0 < all.n; m0 += kMaxItems) {
+      const int mp = std::min(kMaxItems, all.n - m0);
+      mtp_status st = flush_tensor_cores(h, all, m0, mp, d_tok, d_hid, hid_dtype, s);
+      if (st != MTP_OK) return st;
+    }
+  } else
   for (int m0 = 0; m0 < all.n; m0 += kMaxItems) {
     Items it;
     const int mp = std::min(kMaxItems, all.n - m0);
@@ -773,6 +849,8 @@ mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* 
     if (h->keep[r] >= 0) { h->len[r] = h->keep[r]; h->keep[r] = -1; }
   return cuda_ok(cudaGetLastError());
 }
+
+int64_t mtp_kernel_launches(void) { return (int64_t)launches_so_far(); }
 
 mtp_status mtp_profile_enable(mtp_t h, int32_t on) {
   if (!h) return MTP_ERR_BAD_ARG;

@@ -599,6 +599,7 @@ static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cud
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, k, a);
+  count_launch();
 }
 
 void launch_sample(const SampleArgs& a, cudaStream_t s) {

@@ -220,3 +220,19 @@ def kv_prefill(s: Shape, seed: int, rows: int, capacity: int, lengths, tag: str 
         k[r, :, lengths[r]:, :] = 0
         v[r, :, lengths[r]:, :] = 0
     return k, v
+
+
+def plant_logits(base: np.ndarray, drafts, coins) -> np.ndarray:
+    """Synthetic target rows for a verify block: row i (i < d) has its argmax
+    moved onto draft x_{i+1} when coins[i] (logit = max + 1), and otherwise
+    made to differ from it (logit = second - 1 when x_{i+1} was the argmax).
+    Row d (the bonus row) is left as drawn."""
+    out = np.array(base, dtype=np.float32, copy=True)
+    for i, x in enumerate(drafts):
+        row = out[i]
+        top = np.argsort(-row.astype(np.float64), kind="stable")[:2]
+        if coins[i]:
+            row[x] = row[top[0]] + np.float32(1.0)
+        elif top[0] == x:
+            row[x] = row[top[1]] - np.float32(1.0)
+    return out

@@ -19,3 +19,10 @@ def _build_host_libs():
     synth.build()
     oracle.build()
     yield
+
+
+@pytest.fixture(scope="session")
+def model27():
+    """The 27B-shaped synthetic head (host arrays), built once per session."""
+    import synth
+    return synth.make_model(synth.QWEN27B, 2)

@@ -51,6 +51,8 @@ class Rig:
 
     def close(self):
         self.h.close()
+        self.dev = self.embed = self.kk = self.vv = None
+        torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- inputs
     def pairs(self, toks, seed_tag="pairs"):

@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol include/mtp.h declares, and mtp_load / spec_verify reject bad
+arguments before touching the device (fail-closed named errors, "support the
+qwen3_5_mtp drafter" issue: unsupported architectures and incomplete heads
+fail closed; the loader never infers MTP from mtp_num_hidden_layers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mtp_speculative_decoding_step_gb300 as m
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mtp_speculative_decoding_step_gb300 import _build
+    _build.build()
+    return m.lib()
+
+
+def test_header_declares_exactly_the_exported_symbols(L):
+    hdr = open(os.path.join(ROOT, "include", "mtp.h")).read()
+    declared = set(re.findall(r"^[a-z_0-9 \*]*?\b((?:mtp|spec|kv)_[a-z_0-9]+)\(", hdr, re.M))
+    assert declared == set(m.EXPORTS)
+    for name in m.EXPORTS:
+        assert hasattr(L, name), name
+
+
+def test_block_size_and_status_strings(L):
+    cfg = m.make_config(synth.TINY, 1, 256, 2)
+    assert m.mtp_default_block_size(cfg) == 3
+    assert m.mtp_status_str(1) == "unsupported draft architecture"
+    for code in m.STATUS:
+        assert m.mtp_status_str(code)
+
+
+FAKE = 0x10000  # never dereferenced: every case below fails host validation
+
+
+def _table(shape, raw=True, drop=None, dup=None, extra=None, bad_shape=None, dtype=None):
+    shapes = synth.tensor_shapes(shape)
+    names = list(synth.INVENTORY)
+    if drop:
+        names.remove(drop)
+    if dup:
+        names.append(dup)
+    if extra:
+        names.append(extra)
+    arr = (m.Tensor * len(names))()
+    keep = []
+    for i, n in enumerate(names):
+        shp = shapes.get(n, (3,))
+        if bad_shape == n:
+            shp = (shp[0] + 64,) + tuple(shp[1:])
+        full = ("mtp." + n) if raw else n
+        if raw == "mixed" and i == 0:
+            full = n
+        b = full.encode()
+        keep.append(b)
+        dt = m.MTP_DTYPE_BF16 if shape.dtype == "bf16" else m.MTP_DTYPE_F32
+        arr[i] = m.Tensor(b, FAKE, dtype if dtype is not None else dt, len(shp),
+                          (ctypes.c_int64 * 2)(*(list(shp) + [0, 0])[:2]))
+    return arr, len(names), keep
+
+
+def _load(L, cfg, table, embed=FAKE):
+    arr, n, _ = table
+    out = ctypes.c_void_p()
+    kv = m.KV(FAKE, FAKE, FAKE)
+    return L.mtp_load(ctypes.byref(cfg), arr, n, embed, None, kv, None, None, ctypes.byref(out))
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(arch="qwen3_5_moe"), 1),
+    (dict(drop="layers.0.mlp.down_proj.weight"), 2),
+    (dict(dup="fc.weight"), 3),
+    (dict(extra="layers.0.linear_attn.in_proj.weight"), 4),
+    (dict(bad_shape="layers.0.self_attn.k_proj.weight"), 5),
+    (dict(dtype=m.MTP_DTYPE_F32), 5),
+    (dict(layers=2), 6),
+    (dict(vocab=2050), 6),
+    (dict(head_dim=96), 6),
+    (dict(embed=None), 7),
+    (dict(raw="mixed"), 13),
+])
+def test_mtp_load_fails_closed(L, case, code):
+    s = synth.Shape("t", 512, 8, 2, 128, 1536, case.get("vocab", 4096), dtype="bf16")
+    if "head_dim" in case:
+        s = synth.Shape("t", 512, 8, 2, case["head_dim"], 1536, 4096, dtype="bf16")
+    cfg = m.make_config(s, 1, 256, 2, architecture=case.get("arch", "qwen3_5_mtp"))
+    if "layers" in case:
+        cfg.mtp_layers = case["layers"]
+    table = _table(s, raw=case.get("raw", True), drop=case.get("drop"), dup=case.get("dup"),
+                   extra=case.get("extra"), bad_shape=case.get("bad_shape"), dtype=case.get("dtype"))
+    assert _load(L, cfg, table, embed=case.get("embed", FAKE)) == code
+
+
+def test_config_layer_count_does_not_stand_in_for_tensors(L):
+    # a config advertising one MTP layer with no mtp.* tensors is a missing head
+    s = synth.small_shape()
+    cfg = m.make_config(s, 1, 256, 2)
+    arr = (m.Tensor * 0)()
+    out = ctypes.c_void_p()
+    rc = L.mtp_load(ctypes.byref(cfg), arr, 0, FAKE, None, m.KV(FAKE, FAKE, FAKE), None, None, ctypes.byref(out))
+    assert rc == 2 and out.value is None
+
+
+def test_spec_verify_rejects_bad_arguments_without_launching(L):
+    sp = m.sampling_array([dict(temperature=0.0)])
+    args = [None, 1, 2, 64, FAKE, FAKE, None, sp, None, 0, FAKE, FAKE, FAKE, None, None, FAKE]
+    bad = list(args)
+    bad[1] = 0
+    assert L.spec_verify(*bad) == 9
+    bad = list(args)
+    bad[15] = None                      # no workspace
+    assert L.spec_verify(*bad) == 9
+    sp2 = m.sampling_array([dict(temperature=0.7, top_p=0.9)])
+    bad = list(args)
+    bad[7] = sp2                        # sampled row without q
+    assert L.spec_verify(*bad) == 9
+    sp3 = m.sampling_array([dict(temperature=0.7, top_p=1.5)])
+    bad = list(args)
+    bad[7] = sp3
+    bad[6] = FAKE
+    assert L.spec_verify(*bad) == 9
+    assert m.spec_verify_workspace_bytes(8, 3, 152064) >= 8 * 4 * 32

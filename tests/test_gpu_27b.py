@@ -1,0 +1,73 @@
+"""GPU parity at the 27B shape (H=5120, 24/4 heads x 256, SwiGLU 17408,
+vocab 152064, bf16 weights, fp32 accumulation): a greedy depth-2 draft with the
+draft KV at 4096 positions, the verify of planted target logits, and the flush
+of 256 pairs at starting offsets 0, 8192 and 32768.  Hidden states and logits
+within max relative error 1e-2; tokens exact unless the oracle reports a
+near-tie."""
+import numpy as np
+import pytest
+
+import mtp_speculative_decoding_step_gb300 as m
+import oracle
+import synth
+from tests import gpu_common as g
+
+pytestmark = pytest.mark.gpu
+S = synth.QWEN27B
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def model(model27):
+    return model27
+
+
+def test_greedy_round_parity(model):
+    rig = g.Rig(S, seed=2, rows=1, capacity=4096 + 256, prefill=[4096], max_depth=2, model=model)
+    toks = [1234, 77, 150000]
+    tok, hid = rig.pairs([toks])
+    out = rig.draft(2, [3], tok, hid, [dict(temperature=0.0)])
+    ref = rig.oracle_draft(0, 2, toks, g.to_f32(hid)[0], oracle.make_params(0.0))
+    assert g.max_rel(out["logits"][0, 0], ref["logits"][0]) < TOL
+    assert g.max_rel(out["hidden"][0, 0], ref["h2"][0]) < TOL
+    K, V = rig.kv_host()
+    for slot in range(4096, 4099):
+        assert g.max_rel(K[0, :, slot], g.to_f32(rig.oK[0, :, slot])) < TOL
+        assert g.max_rel(V[0, :, slot], g.to_f32(rig.oV[0, :, slot])) < TOL
+    if ref["margins"][0] > 1e-2:
+        assert out["draft"][0, 0] == ref["drafts"][0]
+        assert g.max_rel(out["logits"][0, 1], ref["logits"][1]) < TOL
+        if ref["margins"][1] > 1e-2:
+            assert out["draft"][0, 1] == ref["drafts"][1]
+    # verify of planted target logits (argmax moved onto each draft w.p. 0.7)
+    base = synth.normal(2, "t27:logits", (1, 3, S.vocab), std=4.0)
+    coins = synth.uniform(2, "t27:coins", (2,)) < 0.7
+    lg_g = synth.plant_logits(base[0], out["draft"][0], coins)[None]
+    lg_o = synth.plant_logits(base[0], ref["drafts"], coins)
+    got = rig.verify(lg_g, out["draft"], None, [dict(temperature=0.0)], np.zeros((1, 3), np.float32))
+    n, toks_ref, _ = oracle.verify_row(lg_o, ref["drafts"], None, oracle.make_params(0.0),
+                                       np.zeros(0, np.int32), np.zeros(3, np.float32))
+    if np.array_equal(out["draft"][0], ref["drafts"]):
+        assert got["n_acc"][0] == n and np.array_equal(got["out_tok"][0], toks_ref)
+    m.kv_rollback(rig.h, 1, 2)
+    assert list(m.mtp_get_lengths(rig.h)) == [4099]
+    rig.close()
+
+
+@pytest.mark.parametrize("offset", [0, 8192, 32768])
+def test_flush_256_pairs_at_offset(model, offset):
+    rig = g.Rig(S, seed=2, rows=1, capacity=offset + 256, prefill=[offset], max_depth=2, model=model)
+    toks = synth.randint(2, f"fl{offset}:tok", (256,), S.vocab)
+    tok, hid = rig.pairs([list(toks)], seed_tag=f"fl{offset}")
+    m.mtp_flush(rig.h, [256], tok, hid)
+    assert list(m.mtp_get_lengths(rig.h)) == [offset + 256]
+    K, V = rig.kv_host()
+    hh = g.to_f32(hid)[0]
+    # each slot's K/V depend only on its own pair: check a sample of slots one by one
+    for j in range(0, 256, 17):
+        rig.orc.step(int(toks[j]), hh[j], rig.oK[0], rig.oV[0], offset + j, kv_only=True)
+        assert g.max_rel(K[0, :, offset + j], g.to_f32(rig.oK[0, :, offset + j])) < TOL, j
+        assert g.max_rel(V[0, :, offset + j], g.to_f32(rig.oV[0, :, offset + j])) < TOL, j
+    if offset:
+        np.testing.assert_array_equal(K[0, :, :offset][:, ::997], g.to_f32(rig.oK[0, :, :offset][:, ::997]))
+    rig.close()
