@@ -109,3 +109,23 @@ class Rig:
     def oracle_flush(self, r, toks, hids):
         self.orc.flush(toks, hids, self.oK[r], self.oV[r], self.olen[r])
         self.olen[r] += len(toks)
+
+
+# Near-tie bands.  Accept tests: |p/q - u| < 1e-3 (the workload's stated band).
+# Inverse-CDF draws: the threshold within 1e-5 of a cumulative boundary (the two
+# sides' cumulative sums differ by ~1e-7 of the total).  Greedy argmax over
+# recomputed logits: top-2 gap below GAP.
+ACCEPT_BAND = 1e-3
+DRAW_BAND = 1e-5
+
+
+def verify_near_tie(mg, n, d, greedy, gap=0.0):
+    """Oracle margins of one verified row -> True if any decision was a near-tie."""
+    acc = mg[: min(n + 1, d)]
+    if greedy:
+        return bool(np.min(np.append(acc, mg[d])) <= gap)
+    return bool((acc.size and np.min(acc) < ACCEPT_BAND) or mg[d] < DRAW_BAND)
+
+
+def draft_near_tie(margin, greedy, gap):
+    return margin <= gap if greedy else margin < DRAW_BAND

@@ -78,8 +78,8 @@ def test_sampled_draft_q_and_tokens(params):
         if ref["q"] is not None:
             assert g.max_rel(out["q"][0, k], ref["q"][k]) < 1e-5
             assert np.array_equal(out["q"][0, k] > 0, ref["q"][k] > 0)
-        if ref["margins"][k] < 1e-3:
-            pytest.skip("near-tie in the oracle's draw")
+        if g.draft_near_tie(ref["margins"][k], oracle.is_greedy(p), 1e-4):
+            pytest.skip("near-tie in the oracle's draft decision")
         assert out["draft"][0, k] == ref["drafts"][k], k
     rig.close()
 
@@ -112,7 +112,7 @@ def test_verify_block_of_three(temperature):
     for r in range(rows):
         n, toks, mg = oracle.verify_row(lg[r], drafts[r], None if q is None else q[r], p,
                                         np.zeros(0, np.int32), u[r])
-        if np.min(mg[: min(n + 1, d)]) < 1e-3 or mg[d] < 1e-3:
+        if g.verify_near_tie(mg, n, d, temperature == 0.0):
             near += 1
             continue
         assert got["n_acc"][r] == n, r
