@@ -121,18 +121,24 @@ def build_workload(seed: int, rank: int, vocab: int = 0):
     return s, model, K, V, base, thid, tok0
 
 
-def plant_device(lg, draft, coins):
-    """Device-side planting (torch ops, no host sync): see synth.plant_logits."""
+def pool_top2(base):
+    """Per pool row i: (max, second, argmax) of the base target rows (host)."""
+    o = np.argsort(-base.astype(np.float64), axis=-1, kind="stable")[..., :2]
+    v = np.take_along_axis(base, o, axis=-1)
+    return v[..., 0].astype(np.float32), v[..., 1].astype(np.float32), o[..., 0].astype(np.int64)
+
+
+def plant_device(lg, draft, coins, top1, top2, arg1):
+    """Device-side planting (torch ops, no host sync), same rule as
+    synth.plant_logits: row i gets logit[x_{i+1}] = max + 1 when coins[i],
+    else logit[x_{i+1}] = second - 1 if x_{i+1} was the argmax.
+    coins/top1/top2/arg1: [DEPTH] device tensors for this round / pool row."""
     import torch
-    for i, c in enumerate(coins):
-        row = lg[0, i]
-        x = draft[0, i].long().view(1)
-        top = torch.topk(row, 2)
-        if c:
-            row.index_put_((x,), top.values[0:1] + 1.0)
-        else:
-            new = torch.where(top.indices[0:1] == x, top.values[1:2] - 1.0, row.index_select(0, x))
-            row.index_put_((x,), new)
+    x = draft[0].long()
+    rows = torch.arange(x.numel(), device=x.device)
+    cur = lg[0, rows, x]
+    new = torch.where(coins, top1 + 1.0, torch.where(arg1 == x, top2 - 1.0, cur))
+    lg[0].index_put_((rows, x), new)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -154,10 +160,13 @@ def run_ours(args, rank, world, local_rank):
     params = m.sampling_array([dict(temperature=0.0)])
     base_d = to(base)
     thid_d = to(thid)
+    t1, t2, a1 = pool_top2(base[:, :DEPTH])
+    top1_d, top2_d, arg1_d = to(t1), to(t2), torch.from_numpy(a1).to(dev)
     base_h = torch.from_numpy(base).pin_memory()
     thid_h = torch.from_numpy(thid.view(np.int16)).pin_memory()
     rounds = args.warmup + args.steps
     coins = synth.uniform(args.seed, f"r{rank}:coins", (2 * rounds + 8, DEPTH)) < 0.7
+    coins_d = torch.from_numpy(coins).to(dev)
     draft = torch.zeros((1, DEPTH), dtype=torch.int32, device=dev)
     lg = torch.zeros((1, DEPTH + 1, s.vocab), dtype=torch.float32, device=dev)
     u = torch.zeros((1, DEPTH + 1), dtype=torch.float32, device=dev)
@@ -186,7 +195,7 @@ def run_ours(args, rank, world, local_rank):
             lg.copy_(base_h[i % POOL].view(1, DEPTH + 1, s.vocab), non_blocking=True)
         else:
             lg.copy_(base_d[i % POOL].view(1, DEPTH + 1, s.vocab))
-        plant_device(lg, draft, coins[i])
+        plant_device(lg, draft, coins_d[i], top1_d[i % POOL], top2_d[i % POOL], arg1_d[i % POOL])
         if timed_verify:
             ev_v0[i].record(stream)
         m.spec_verify(lg, draft, params, u, n_acc, out_tok, ws, h_out=h_out)
@@ -244,8 +253,8 @@ def run_ours(args, rank, world, local_rank):
 
     h.close()
 
-    H, V = s.hidden, s.vocab
-    lm_bytes = V * H * 2 + V * 4 + H * 4
+    H, Vocab = s.hidden, s.vocab
+    lm_bytes = Vocab * H * 2 + Vocab * 4 + H * 4
     lm_ms, lm_n = prof["lm_head"]
     lm_avg_s = lm_ms / max(lm_n, 1) / 1e3
     peak, src = peaks()
@@ -285,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
                      "bytes_per_launch": lm_bytes},
         "gpu_launches": int(launches),
         "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
-                "h2d_bytes_per_step": (DEPTH + 1) * V * 4 + (DEPTH + 1) * H * 2,
+                "h2d_bytes_per_step": (DEPTH + 1) * Vocab * 4 + (DEPTH + 1) * H * 2,
                 "d2h_bytes_per_step": 4 * (DEPTH + 2)},
         "clocks": clk,
         "wall_s": round(wall, 3),
@@ -378,11 +387,12 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     result, work = run_ours(args, rank, world, local_rank)
-    if rank == 0 and not args.quick:
-        n, sec, thr = cpu_rounds(work, args.cpu_budget, 8)
-        result["cpu_baseline"] = {"value": round(n * DEPTH / sec, 3), "unit": "draft tok/s", "cores": thr,
-                                  "kind": "oracle",
-                                  "sample": f"{n} whole rounds (2 draft steps + verify) of the same workload"}
+    if rank == 0:
+        if not args.quick:
+            n, sec, thr = cpu_rounds(work, args.cpu_budget, 8)
+            result["cpu_baseline"] = {"value": round(n * DEPTH / sec, 3), "unit": "draft tok/s", "cores": thr,
+                                      "kind": "oracle",
+                                      "sample": f"{n} whole rounds (2 draft steps + verify) of the same workload"}
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -89,4 +89,120 @@ __device__ __forceinline__ float block_sum(float v, float* sh /*[32]*/) {
   return sh[0];
 }
 
+// Programmatic dependent launch: wait for the previous kernel in the stream
+// (a no-op when this grid was launched without the attribute), and let the
+// next kernel's blocks be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Sum of squares of n elements (n % 8 == 0, 16-byte aligned) of an fp32 or
+// bf16 row, block-wide, vector loads with independent iterations.
+__device__ __forceinline__ float row_sumsq(const void* src, int dt, size_t base, int n, float* red) {
+  float ss = 0.f;
+  if (dt == MTP_DTYPE_BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n / 8; i += blockDim.x) {
+      const uint4 w = __ldg(p + i);
+      const float f[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                          bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n / 4; i += blockDim.x) {
+      const float4 v = p[i];
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+  }
+  return block_sum(ss, red);
+}
+
+// dst[k] = src[base + k] * scale * w[k] for k < n (n % 8 == 0), to fp32 shared memory.
+__device__ __forceinline__ void row_stage(float* dst, const void* src, int dt, size_t base, int n, float scale,
+                                          const float* w) {
+  if (dt == MTP_DTYPE_BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base);
+#pragma unroll 2
+    for (int i = threadIdx.x; i < n / 8; i += blockDim.x) {
+      const uint4 v = __ldg(p + i);
+      const float f[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                          bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[8 * i + j] = f[j] * scale * (w ? w[8 * i + j] : 1.f);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base);
+    float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n / 4; i += blockDim.x) {
+      float4 v = p[i];
+      if (w) {
+        const float4 ww = reinterpret_cast<const float4*>(w)[i];
+        v = make_float4(v.x * scale * ww.x, v.y * scale * ww.y, v.z * scale * ww.z, v.w * scale * ww.w);
+      } else {
+        v = make_float4(v.x * scale, v.y * scale, v.z * scale, v.w * scale);
+      }
+      d4[i] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------ mbarrier / bulk copy
+constexpr unsigned kWaitLimit = 1u << 24;  // try_wait polls before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false when the poll budget runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (unsigned i = 0; i < kWaitLimit; ++i)
+    if (mbar_try(bar, parity)) return true;
+  return false;
+}
+
+// Bulk asynchronous copy global -> shared (16-byte aligned, size % 16 == 0),
+// completing on an mbarrier transaction count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<A&&>(args)...);
+}
+
 }  // namespace mtp

@@ -77,7 +77,6 @@ __device__ __forceinline__ void gemv_fma(float (&acc)[RPW][MT], const uint4 (&w)
 // Stage x[m][k0 .. k0+KS) (fp32) into shared memory, applying the prologue.
 template <int MT>
 __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, float* red) {
-  const int tid = threadIdx.x;
   if (a.pro == PRO_DUAL) {
     // x = [norm_e(E[tok]) ; norm_h(hidden)]; this block's slice lies in one half.
     const int H = a.K / 2;
@@ -89,41 +88,30 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
       const int dt = emb ? a.wdt : a.hid_dt;
       int t = emb ? a.tok[a.tok_idx[m]] : 0;
       if (t < 0 || t >= a.vocab) {  // a bad token id reads row 0 and raises the status word
-        if (tid == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+        if (threadIdx.x == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
         t = 0;
       }
       const size_t base = emb ? (size_t)t * (size_t)H : (size_t)a.hid_off[m];
-      float ss = 0.f;
-      for (int k = tid; k < H; k += blockDim.x) {
-        float v = load_elem(src, dt, base + k);
-        ss = fmaf(v, v, ss);
-      }
-      ss = block_sum(ss, red);
-      const float inv = rsqrtf(ss / (float)H + a.eps);
-      for (int k = tid; k < KS; k += blockDim.x)
-        xs[m * KS + k] = load_elem(src, dt, base + kk0 + k) * inv * nw[kk0 + k];
+      const float inv = rsqrtf(row_sumsq(src, dt, base, H, red) / (float)H + a.eps);
+      row_stage(xs + m * KS, src, dt, base + kk0, KS, inv, nw + kk0);
     }
   } else {
     for (int m = 0; m < a.M; ++m) {
       const float* xm = a.x + (size_t)m * a.ldx;
-      float inv = 1.f;
       if (a.pro == PRO_NORM) {
-        float ss = 0.f;
-        for (int k = tid; k < a.K; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
-        ss = block_sum(ss, red);
-        inv = rsqrtf(ss / (float)a.K + a.eps);
-        for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = xm[k0 + k] * inv * a.nw[k0 + k];
+        const float inv = rsqrtf(row_sumsq(xm, MTP_DTYPE_F32, 0, a.K, red) / (float)a.K + a.eps);
+        row_stage(xs + m * KS, xm, MTP_DTYPE_F32, k0, KS, inv, a.nw + k0);
       } else {
-        for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = xm[k0 + k];
+        row_stage(xs + m * KS, xm, MTP_DTYPE_F32, k0, KS, 1.f, nullptr);
       }
     }
   }
   for (int m = a.M; m < MT; ++m)
-    for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
+    for (int k = threadIdx.x; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
 }
 
 template <typename WT, int MT>
-__global__ void __launch_bounds__(256) k_gemv(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(256, (MT <= 2 ? 3 : 2)) k_gemv(const __grid_constant__ GemvArgs a) {
   constexpr int VN = Vec<WT>::N;
   constexpr int RPW = MT <= 2 ? 8 : (MT == 4 ? 4 : 2);
   constexpr int ROWS = 8 * RPW;
@@ -135,9 +123,6 @@ __global__ void __launch_bounds__(256) k_gemv(const __grid_constant__ GemvArgs a
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int group = blockIdx.x / a.S, split = blockIdx.x - group * a.S;
   const int KS = a.K / a.S, k0 = split * KS;
-
-  gemv_prologue<MT>(a, xs, k0, KS, s_red);
-  __syncthreads();
 
   // This warp's RPW consecutive physical rows.
   const int l0 = warp * RPW;
@@ -154,24 +139,37 @@ __global__ void __launch_bounds__(256) k_gemv(const __grid_constant__ GemvArgs a
   }
   W += k0;
 
+  // The weights do not depend on the previous kernel: issue this warp's first
+  // loads before waiting for it. Each lane keeps one 16-byte vector of each
+  // of its RPW rows in flight.
+  const int nvec = KS / VN;
+  int v0 = lane;
+  bool has0 = v0 < nvec;
+  uint4 w0[RPW];
+  if (has0) {
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  gemv_prologue<MT>(a, xs, k0, KS, s_red);
+  __syncthreads();
+
   float acc[RPW][MT];
 #pragma unroll
   for (int i = 0; i < RPW; ++i)
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
 
-  const int nvec = KS / VN;
-  for (int v0 = lane; v0 < nvec; v0 += 64) {
-    const bool has1 = v0 + 32 < nvec;
-    uint4 w0[RPW], w1[RPW];
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
-    if (has1) {
-#pragma unroll
-      for (int i = 0; i < RPW; ++i) w1[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
-    }
+  while (has0) {
     gemv_fma<WT, MT, RPW>(acc, w0, xs, KS, v0 * VN);
-    if (has1) gemv_fma<WT, MT, RPW>(acc, w1, xs, KS, (v0 + 32) * VN);
+    v0 += 32;
+    has0 = v0 < nvec;
+    if (has0) {
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
+    }
   }
 
 #pragma unroll
@@ -268,7 +266,7 @@ template <typename WT, int MT>
 static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
   auto k = k_gemv<WT, MT>;
   if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  k<<<a.ngroups * a.S, 256, smem, s>>>(a);
+  launch_pdl(k, dim3(a.ngroups * a.S), dim3(256), smem, s, a);
   count_launch();
 }
 
@@ -307,6 +305,8 @@ __device__ __forceinline__ float qkv_at(const QkvPostArgs& a, int m, int col) {
 
 __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.dh / 2;
   const int slot = a.slot[m], row = a.row[m];
   if (h < a.nq) {
@@ -396,115 +396,195 @@ void launch_flush_norm(const float* part, int nsplit, long long split_stride, in
 }
 
 void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
-  dim3 grid(a.M, a.nq + a.nkv);
-  k_qkv_post<<<grid, a.dh / 2, 0, s>>>(a);
+  launch_pdl(k_qkv_post, dim3(a.M, a.nq + a.nkv), dim3(a.dh / 2), 0, s, a);
   count_launch();
 }
 
 // ------------------------------------------------------- decode attention
 
-// One block per (chunk of kAttnChunk slots, kv head, head item). The G query
-// heads of the group share each key/value row read. Partials (o, max, sum)
-// are merged by k_attn_merge.
-template <int DH, int G>
-__global__ void __launch_bounds__(128) k_attn_chunk(const __grid_constant__ AttnArgs a) {
-  constexpr int EPL = DH / 32;  // elements per lane of one key row
-  __shared__ __align__(16) float qs[G][DH];
-  __shared__ float sc[G][kAttnChunk];
+// One block per (chunk of kAttnChunk slots, kv head, head item). Thread 0
+// copies the chunk's K and V rows (contiguous in the cache) into shared memory
+// as 64-slot tiles with bulk asynchronous copies; the block then computes the
+// scores of the G query heads of the group against each tile, keeps an online
+// softmax, and accumulates P.V with one thread per head dimension. Partials
+// (o, running max, running sum) are merged by k_attn_merge.
+template <int DH, int G, typename KT>
+__global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ AttnArgs a) {
+  constexpr int TS = 64;
+  constexpr int NT = kAttnChunk / TS;
+  constexpr int EPL = DH / 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  KT* ks = reinterpret_cast<KT*>(smem);
+  KT* vs = ks + NT * TS * DH;
+  float* qs = reinterpret_cast<float*>(vs + NT * TS * DH);
+  float* ps = qs + G * DH;          // [G][TS]
+  float* st = ps + G * TS;          // [G][4]: running max, alpha, running sum
+  uint64_t* bar = reinterpret_cast<uint64_t*>(st + 4 * 8);
+
   const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
   const int L = a.slot[m] + 1;
   const int t0 = c * kAttnChunk;
   if (t0 >= L) return;
   const int n = min(kAttnChunk, L - t0);
+  const int nt = (n + TS - 1) / TS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float* qg = a.q + (size_t)m * a.nq * DH + (size_t)g * G * DH;
-  for (int t = tid; t < G * DH; t += 128) qs[t / DH][t % DH] = qg[t];
-  __syncthreads();
 
+  if (tid == 0) {
+    for (int i = 0; i < NT; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < G) { st[4 * tid] = -INFINITY; st[4 * tid + 1] = 0.f; st[4 * tid + 2] = 0.f; }
+  __syncthreads();
+  pdl_wait();  // the cache rows of this call's new slots come from k_qkv_post
   const size_t base = (((size_t)a.row[m] * a.nkv + g) * a.cap + t0) * DH;
-  for (int j = warp; j < n; j += 4) {
-    float kv[EPL];
-    const size_t off = base + (size_t)j * DH + lane * EPL;
-    if (a.wdt == MTP_DTYPE_BF16) {
-      const uint16_t* kp = reinterpret_cast<const uint16_t*>(a.kc) + off;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = bf16_to_f(kp[e]);
-    } else {
-      const float* kp = reinterpret_cast<const float*>(a.kc) + off;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = kp[e];
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float d = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) d = fmaf(qs[h][lane * EPL + e], kv[e], d);
-      d = warp_sum(d);
-      if (lane == 0) sc[h][j] = d * a.scale;
+  if (tid == 0) {
+    for (int i = 0; i < nt; ++i) {
+      const int rows = min(TS, n - i * TS);
+      const uint32_t bytes = (uint32_t)(rows * DH * sizeof(KT));
+      mbar_expect_tx(smem_u32(&bar[i]), 2 * bytes);
+      bulk_g2s(smem_u32(ks + i * TS * DH), reinterpret_cast<const KT*>(a.kc) + base + (size_t)i * TS * DH, bytes,
+               smem_u32(&bar[i]));
+      bulk_g2s(smem_u32(vs + i * TS * DH), reinterpret_cast<const KT*>(a.vc) + base + (size_t)i * TS * DH, bytes,
+               smem_u32(&bar[i]));
     }
   }
-  __syncthreads();
-  // chunk softmax statistics per head
-  __shared__ float smax[G], ssum[G];
-  for (int h = warp; h < G; h += 4) {
-    float mx = -INFINITY;
-    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[h][j]);
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j < n; j += 32) {
-      const float e = expf(sc[h][j] - mx);
-      sc[h][j] = e;
-      sum += e;
+  pdl_trigger();
+  const float* qg = a.q + (size_t)m * a.nq * DH + (size_t)g * G * DH;
+  for (int t = tid; t < G * DH; t += blockDim.x) qs[t] = qg[t];
+
+  float o[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) o[h] = 0.f;
+  bool ok = true;
+  for (int i = 0; i < nt; ++i) {
+    const int rows = min(TS, n - i * TS);
+    const bool got = mbar_wait(smem_u32(&bar[i]), 0);
+    if (__syncthreads_or(!got)) { ok = false; break; }
+    // scores: warp w takes keys w, w+8, ...; lane owns EPL consecutive dims
+    for (int j = warp; j < rows; j += 8) {
+      const KT* kr = ks + (size_t)(i * TS + j) * DH + lane * EPL;
+      float kv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) kv[e] = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)kr)[e]) : ((const float*)kr)[e];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) d = fmaf(qs[h * DH + lane * EPL + e], kv[e], d);
+        d = warp_sum(d);
+        if (lane == 0) ps[h * TS + j] = d * a.scale;
+      }
     }
-    sum = warp_sum(sum);
-    if (lane == 0) { smax[h] = mx; ssum[h] = sum; }
+    __syncthreads();
+    // online softmax update: warp h owns query head h
+    if (warp < G) {
+      const int h = warp;
+      float mx = -INFINITY;
+      for (int j = lane; j < rows; j += 32) mx = fmaxf(mx, ps[h * TS + j]);
+      mx = warp_max(mx);
+      const float m_old = st[4 * h];
+      const float m_new = fmaxf(m_old, mx);
+      const float alpha = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
+      float sum = 0.f;
+      for (int j = lane; j < rows; j += 32) {
+        const float e = expf(ps[h * TS + j] - m_new);
+        ps[h * TS + j] = e;
+        sum += e;
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) {
+        st[4 * h] = m_new;
+        st[4 * h + 1] = alpha;
+        st[4 * h + 2] = st[4 * h + 2] * alpha + sum;
+      }
+    }
+    __syncthreads();
+    for (int d = tid; d < DH; d += blockDim.x) {
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = o[h] * st[4 * h + 1];
+      const KT* vr = vs + (size_t)i * TS * DH + d;
+      for (int j = 0; j < rows; ++j) {
+        const float v = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)vr)[(size_t)j * DH]) : ((const float*)vr)[(size_t)j * DH];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(ps[h * TS + j], v, acc[h]);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) o[h] = acc[h];
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int d = tid; d < DH; d += 128) {
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-    for (int j = 0; j < n; ++j) {
-      const float v = load_elem(a.vc, a.wdt, base + (size_t)j * DH + d);
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(sc[h][j], v, acc[h]);
+  if (!ok) {
+    if (tid == 0) {
+      flag_status(a.status, MTP_ERR_TIMEOUT);
+      for (int i = 0; i < nt; ++i) mbar_wait(smem_u32(&bar[i]), 0);  // let copies land before exit
     }
+    return;
+  }
+  for (int d = tid; d < DH; d += blockDim.x) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const size_t hq = (size_t)m * a.nq + g * G + h;
-      a.po[(hq * a.max_chunks + c) * DH + d] = acc[h];
+      a.po[(hq * a.max_chunks + c) * DH + d] = o[h];
     }
   }
   if (tid < G) {
     const size_t hq = (size_t)m * a.nq + g * G + tid;
-    a.pml[(hq * a.max_chunks + c) * 2 + 0] = smax[tid];
-    a.pml[(hq * a.max_chunks + c) * 2 + 1] = ssum[tid];
+    a.pml[(hq * a.max_chunks + c) * 2 + 0] = st[4 * tid];
+    a.pml[(hq * a.max_chunks + c) * 2 + 1] = st[4 * tid + 2];
   }
 }
 
 // grid (nq, Mh), block DH threads: merge the chunk partials of one query head.
 template <int DH>
 __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
+  extern __shared__ float wch[];  // per-chunk weight exp(m_c - M)
+  __shared__ float red[32];
   const int h = blockIdx.x, m = blockIdx.y, d = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const int L = a.slot[m] + 1;
   const int nch = (L + kAttnChunk - 1) / kAttnChunk;
   const size_t hq = (size_t)m * a.nq + h;
   const float* ml = a.pml + hq * a.max_chunks * 2;
+  float mx = -INFINITY;
+  for (int c = d; c < nch; c += DH) mx = fmaxf(mx, ml[2 * c]);
+  // block max through the sum helper's scratch: negate-free max reduction
+  mx = warp_max(mx);
+  if ((d & 31) == 0) red[d >> 5] = mx;
+  __syncthreads();
   float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[2 * c]);
-  float den = 0.f, num = 0.f;
-  for (int c = 0; c < nch; ++c) {
+  for (int w = 0; w < DH / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float den = 0.f;
+  for (int c = d; c < nch; c += DH) {
     const float w = expf(ml[2 * c] - M);
+    wch[c] = w;
     den = fmaf(ml[2 * c + 1], w, den);
-    num = fmaf(a.po[(hq * a.max_chunks + c) * DH + d], w, num);
   }
+  den = block_sum(den, red);
+  const float* po = a.po + hq * a.max_chunks * DH + d;
+  float num = 0.f;
+  int c = 0;
+  for (; c + 8 <= nch; c += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(c + u) * DH];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) num = fmaf(v[u], wch[c + u], num);
+  }
+  for (; c < nch; ++c) num = fmaf(po[(size_t)c * DH], wch[c], num);
   a.o[(size_t)m * a.nq * DH + (size_t)h * DH + d] = num / den;
 }
 
-template <int DH, int G>
+template <int DH, int G, typename KT>
 static void attn_t(const AttnArgs& a, int nch, cudaStream_t s) {
-  k_attn_chunk<DH, G><<<dim3(nch, a.nkv, a.Mh), 128, 0, s>>>(a);
-  k_attn_merge<DH><<<dim3(a.nq, a.Mh), DH, 0, s>>>(a);
+  constexpr int TS = 64, NT = kAttnChunk / TS;
+  const size_t smem = 2 * (size_t)NT * TS * DH * sizeof(KT) + (size_t)(G * DH + G * TS + 32) * sizeof(float) + 64;
+  auto k = k_attn_chunk<DH, G, KT>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_pdl(k, dim3(nch, a.nkv, a.Mh), dim3(256), smem, s, a);
+  launch_pdl(k_attn_merge<DH>, dim3(a.nq, a.Mh), dim3(DH), (size_t)a.max_chunks * sizeof(float), s, a);
   count_launch(2);
 }
 
@@ -513,8 +593,12 @@ void launch_attention(const AttnArgs& a, cudaStream_t s) {
   for (int m = 0; m < a.Mh; ++m) maxL = a.slot[m] + 1 > maxL ? a.slot[m] + 1 : maxL;
   const int nch = (maxL + kAttnChunk - 1) / kAttnChunk;
   const int G = a.nq / a.nkv;
-#define MTP_ATTN_CASE(DHV, GV) \
-  if (a.dh == DHV && G == GV) { attn_t<DHV, GV>(a, nch, s); return; }
+  const bool bf = a.wdt == MTP_DTYPE_BF16;
+#define MTP_ATTN_CASE(DHV, GV)                                                \
+  if (a.dh == DHV && G == GV) {                                               \
+    if (bf) attn_t<DHV, GV, uint16_t>(a, nch, s); else attn_t<DHV, GV, float>(a, nch, s); \
+    return;                                                                   \
+  }
   MTP_ATTN_CASE(256, 6)
   MTP_ATTN_CASE(256, 1)
   MTP_ATTN_CASE(256, 2)
@@ -546,6 +630,8 @@ void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, c
 
 // grid (rows, nkv): set lengths, trim target lengths, zero dropped slots.
 __global__ void k_rollback(const __grid_constant__ RollbackArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x, g = blockIdx.y;
   if (a.keep[r] < 0) return;
   if (g == 0 && threadIdx.x == 0) {
@@ -561,7 +647,7 @@ __global__ void k_rollback(const __grid_constant__ RollbackArgs a) {
 }
 
 void launch_rollback(const RollbackArgs& a, cudaStream_t s) {
-  k_rollback<<<dim3(a.rows, a.nkv), 256, 0, s>>>(a);
+  launch_pdl(k_rollback, dim3(a.rows, a.nkv), dim3(256), 0, s, a);
   count_launch();
 }
 
@@ -571,6 +657,8 @@ struct LenArgs {
   int v[kMaxRows];
 };
 __global__ void k_set_len(const __grid_constant__ LenArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = threadIdx.x;
   if (r < a.rows) a.len[r] = a.v[r];
 }
@@ -580,7 +668,7 @@ void launch_set_len(int32_t* len, int rows, const int* h_len, cudaStream_t s) {
   a.len = len;
   a.rows = rows;
   for (int r = 0; r < rows; ++r) a.v[r] = h_len[r];
-  k_set_len<<<1, kMaxRows, 0, s>>>(a);
+  launch_pdl(k_set_len, dim3(1), dim3(kMaxRows), 0, s, a);
   count_launch();
 }
 

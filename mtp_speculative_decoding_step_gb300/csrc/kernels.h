@@ -12,7 +12,7 @@ void count_launch(int n = 1);
 
 constexpr int kMaxItems = 256;   // pairs per head call (the pages' flush cap)
 constexpr int kMaxRows = 64;
-constexpr int kAttnChunk = 64;   // KV slots per decode-attention block
+constexpr int kAttnChunk = 128;  // KV slots per decode-attention block
 constexpr int kClusterCTAs = 8;  // CTAs per sampling cluster
 
 enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_DUAL = 2 };
@@ -110,6 +110,7 @@ struct AttnArgs {
   float* po;             // [Mh][nq][max_chunks][dh]
   float* pml;            // [Mh][nq][max_chunks][2]
   float* o;              // [Mh][nq*dh]
+  int32_t* status;
   int row[kMaxRows];
   int slot[kMaxRows];
 };

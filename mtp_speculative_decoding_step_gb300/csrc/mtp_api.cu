@@ -337,7 +337,7 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
       a.Mh = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
       a.max_chunks = h->max_chunks;
       a.scale = 1.0f / std::sqrt((float)c.head_dim);
-      a.po = h->po; a.pml = h->pml; a.o = h->o + (size_t)m0 * qw;
+      a.po = h->po; a.pml = h->pml; a.o = h->o + (size_t)m0 * qw; a.status = h->status;
       for (int m = 0; m < mp; ++m) { a.row[m] = it.row[m0 + m]; a.slot[m] = it.slot[m0 + m]; }
       launch_attention(a, s);
     }
@@ -551,7 +551,7 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     off += want[id][0];
   }
   // scratch
-  h->max_chunks = c.kv_capacity / kAttnChunk;
+  h->max_chunks = (c.kv_capacity + kAttnChunk - 1) / kAttnChunk;
   if (st == MTP_OK) st = alloc(h, &h->h0, (size_t)kMaxItems * H);
   if (st == MTP_OK) st = alloc(h, &h->qkv, (size_t)kMaxItems * (qw + 2 * kw));
   if (st == MTP_OK) st = alloc(h, &h->qrot, (size_t)R * qw);

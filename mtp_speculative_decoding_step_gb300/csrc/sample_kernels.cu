@@ -455,6 +455,8 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   Clu c(sm);
+  pdl_wait();
+  pdl_trigger();
   const int task = blockIdx.x / kClusterCTAs;
   int v0, n;
   slice_of(a.V, c.rank, v0, n);
@@ -508,6 +510,8 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   Clu c(sm);
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x / kClusterCTAs;
   const int d = a.depth;
   int v0, n;
@@ -591,13 +595,15 @@ static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cud
   cfg.blockDim = dim3(kST);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterCTAs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaLaunchKernelEx(&cfg, k, a);
   count_launch();
 }
