@@ -41,6 +41,11 @@ METRIC = "MTP draft tok/s + verify rounds/s at 1 GB300 (27B shape); HBM GB/s vs 
 DEPTH = 2
 KV_LEN = 4096
 POOL = 16
+# DRAM traffic (read + write) of one full lm_head launch, from the ncu capture
+# of the same kernel at V=32768 (profiles/lm_head_gemv_H5120_V32768.md),
+# scaled by the rows processed (152064 / 32768). Set to None when the kernel
+# changes until it is captured again.
+LM_TRAFFIC_BYTES = round((335.650048e6 + 5.9648e6) * 152064 / 32768)
 WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064), bf16 weights, "
             "batch 1, greedy, depth 2 (block 3), draft KV 4096")
 
@@ -290,7 +295,9 @@ def run_ours(args, rank, world, local_rank):
         "kernel_avg_us": breakdown,
         "roofline": {"bound": "hbm", "kernel": "lm_head GEMV (tied head, fused final norm + argmax)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": LM_TRAFFIC_BYTES if not args.vocab else None,
+                     "traffic_source": "ncu capture at V=32768 scaled by rows to V=152064",
                      "bytes_per_launch": lm_bytes},
         "gpu_launches": int(launches),
         "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
