@@ -217,6 +217,26 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
                        int32_t* d_stats, int32_t* h_out, void* d_workspace);
 
 /*
+ * spec_verify_noalloc — spec_verify without a caller-provided workspace, for
+ * callers that cannot allocate device memory (a host whose own pool owns all
+ * device memory, or code running where a cudaMalloc would stall the device or
+ * is forbidden). The pages have no counterpart; it exists for such hosts.
+ * Same arguments and results as spec_verify minus d_workspace. The scratch
+ * (one 32-byte descriptor per verified row and position) is a fixed array
+ * inside the library, 1088 descriptors (34,816 bytes) per device, held for
+ * the life of the process: rows * (depth + 1) above 1088 returns
+ * MTP_ERR_BAD_ARG. The first call on a device, with that device current, looks
+ * up the array's address; make it before capturing a stream into a graph.
+ * Every call shares the array, so calls that can run at the same time on the
+ * GPU (unordered streams) race on it. Allocates nothing.
+ */
+mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab,
+                               const float* d_logits, const int32_t* d_draft, const float* d_q,
+                               const mtp_sampling* h_params, const int32_t* d_hist, int32_t hist_w,
+                               const float* d_u, int32_t* d_n_acc, int32_t* d_out_tok,
+                               int32_t* d_stats, int32_t* h_out);
+
+/*
  * kv_rollback — drop speculative cache slots after a verify.
  * Draft KV: row r keeps only the slots of the last mtp_draft's first head call
  * (its length becomes the length before that call + h_pairs[r]); with

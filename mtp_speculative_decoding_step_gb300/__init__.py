@@ -31,7 +31,7 @@ EXPORTS = (
     "mtp_default_block_size", "mtp_status_str", "mtp_load", "mtp_free", "mtp_get_lengths",
     "mtp_set_lengths", "mtp_device_status", "mtp_flush", "mtp_draft", "spec_verify_workspace_bytes",
     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_kinds", "mtp_profile_kind_name",
-    "mtp_profile_read", "mtp_kernel_launches",
+    "mtp_profile_read", "mtp_kernel_launches", "spec_verify_noalloc",
 )
 
 
@@ -92,6 +92,8 @@ def lib():
         L.spec_verify_workspace_bytes.restype = sz
         L.spec_verify.argtypes = [vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(Sampling), vp, i32, vp, vp,
                                   vp, vp, vp, vp]
+        L.spec_verify_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(Sampling), vp, i32,
+                                          vp, vp, vp, vp, vp]
         L.kv_rollback.argtypes = [vp, vp, i32, vp, vp, i32, i32]
         L.mtp_profile_enable.argtypes = [vp, i32]
         L.mtp_profile_kinds.restype = i32
@@ -100,7 +102,8 @@ def lib():
         L.mtp_profile_read.argtypes = [vp, vp, vp]
         L.mtp_kernel_launches.restype = ctypes.c_int64
         for name in ("mtp_load", "mtp_free", "mtp_get_lengths", "mtp_set_lengths", "mtp_flush", "mtp_draft",
-                     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_read"):
+                     "spec_verify", "spec_verify_noalloc", "kv_rollback", "mtp_profile_enable",
+                     "mtp_profile_read"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -251,6 +254,19 @@ def spec_verify(logits, draft, params, u, n_acc, out_tok, workspace, q=None, his
                            _ptr(hist), hist_w, _ptr(u), _ptr(n_acc), _ptr(out_tok), _ptr(stats), _ptr(h_out),
                            _ptr(workspace))
     _check(rc, "spec_verify")
+
+
+def spec_verify_noalloc(logits, draft, params, u, n_acc, out_tok, q=None, hist=None, stats=None, h_out=None,
+                        stream=None):
+    """spec_verify with the library's fixed scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    rows, dp1, V = logits.shape
+    sp = params if isinstance(params, ctypes.Array) else sampling_array(params)
+    hist_w = 0 if hist is None else hist.shape[1]
+    rc = lib().spec_verify_noalloc(_stream(stream), rows, dp1 - 1, V, _ptr(logits), _ptr(draft), _ptr(q), sp,
+                                   _ptr(hist), hist_w, _ptr(u), _ptr(n_acc), _ptr(out_tok), _ptr(stats),
+                                   _ptr(h_out))
+    _check(rc, "spec_verify_noalloc")
 
 
 def kv_rollback(h: Handle, rows: int, depth: int, n_acc=None, target_len=None, zero_tail: bool = False,
