@@ -170,7 +170,7 @@ def run_ours(args, rank, world, local_rank):
     base_h = torch.from_numpy(base).pin_memory()
     thid_h = torch.from_numpy(thid.view(np.int16)).pin_memory()
     rounds = args.warmup + args.steps
-    coins = synth.uniform(args.seed, f"r{rank}:coins", (2 * rounds + 8, DEPTH)) < 0.7
+    coins = synth.uniform(args.seed, f"r{rank}:coins", (2 * rounds + 40, DEPTH)) < 0.7
     coins_d = torch.from_numpy(coins).to(dev)
     draft = torch.zeros((1, DEPTH), dtype=torch.int32, device=dev)
     lg = torch.zeros((1, DEPTH + 1, s.vocab), dtype=torch.float32, device=dev)
@@ -207,6 +207,8 @@ def run_ours(args, rank, world, local_rank):
         if timed_verify:
             ev_v1[i].record(stream)
         m.kv_rollback(h, 1, DEPTH)
+        if i % 64 == 63:  # keep the draft KV near 4096 positions over long runs
+            m.mtp_set_lengths(h, [KV_LEN])
         stream.synchronize()
         n = int(h_out[0])
         state["P"] = n + 1
@@ -221,9 +223,15 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     # timed region (device-resident inputs)
-    clocks = Clocks(local_rank)
+    # per-kernel breakdown: a separate, untimed pass with every kind bracketed
     m.mtp_profile_enable(h, True)
     m.mtp_profile_read(h)
+    for i in range(args.warmup, min(rounds, args.warmup + 20)):
+        one_round(i)
+    prof_all = m.mtp_profile_read(h)
+    # timed region: only the lm_head launches are bracketed (roofline of the dominant kernel)
+    clocks = Clocks(local_rank)
+    m.mtp_profile_enable(h, ["lm_head"])
     launches0 = m.mtp_kernel_launches()
     state["ncommit"] = state["nacc"] = 0
     t0 = torch.cuda.Event(enable_timing=True)
@@ -264,11 +272,12 @@ def run_ours(args, rank, world, local_rank):
     lm_avg_s = lm_ms / max(lm_n, 1) / 1e3
     peak, src = peaks()
     achieved = lm_bytes / lm_avg_s / 1e9
-    breakdown = {k: round(v[0] / max(v[1], 1) * 1e3, 2) for k, v in prof.items() if v[1]}
+    breakdown = {k: round(v[0] / max(v[1], 1) * 1e3, 2) for k, v in prof_all.items() if v[1]}
     layer_bytes = 2 * (H * 2 * H + (24 * 256 + 2 * 4 * 256) * H + H * 24 * 256 + 3 * 17408 * H)
     kv_bytes = 2 * 4 * 256 * 2 * KV_LEN
     step_bytes = layer_bytes + lm_bytes + kv_bytes
-    draft_ms = sum(v[0] for k, v in prof.items() if k not in ("rollback",)) / args.steps
+    n_prof = max(prof_all["lm_head"][1] // DEPTH, 1)
+    draft_ms = sum(v[0] for k, v in prof_all.items() if k not in ("rollback",)) / n_prof
     result = {
         "metric": METRIC,
         "value": round(drafted / (ms / 1e3), 2),
@@ -340,8 +349,8 @@ def cpu_rounds(work, budget_s: float, max_rounds: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -363,10 +372,11 @@ def main():
         synth.build()
         oracle.build()
         s, model, K, V, base, thid, tok0 = build_workload(args.seed, 0)
-        coins = synth.uniform(args.seed, "r0:coins", (args.warmup + args.steps + 8, DEPTH)) < 0.7
+        coins = synth.uniform(args.seed, "r0:coins", (args.warmup + args.steps + 40, DEPTH)) < 0.7
         work = (s, model, K, V, base, thid, tok0, coins)
-        per_step_budget = max(1.0, 150.0 / (args.steps + args.warmup))
-        n, sec, thr = cpu_rounds(work, per_step_budget * args.steps, args.steps)
+        # each step is one oracle round of the same workload; the whole run is
+        # bounded to ~2.5 minutes of host time
+        n, sec, thr = cpu_rounds(work, 150.0, args.steps)
         val = n * DEPTH / sec
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": "draft tok/s",
@@ -375,7 +385,8 @@ def main():
             "vs_baseline": None, "dtype": "f64-accumulate over bf16 weights", "data": "synthetic",
             "config": {"workload": WORKLOAD, "rows": 1, "depth": DEPTH, "kv_len": KV_LEN},
             "cpu_baseline": {"value": round(val, 3), "unit": "draft tok/s", "cores": thr, "kind": "oracle",
-                             "sample": f"{n} whole rounds (2 draft steps + verify) of the benchmark workload"},
+                             "sample": f"{n} whole rounds (2 draft steps + verify) of the benchmark workload, "
+                                       f"at most 150 s of host time"},
             "e2e": {"value": round(val, 3), "unit": "draft tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
         }), flush=True)

@@ -252,12 +252,13 @@ mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* 
 /* Number of kernels this library has launched in the process so far. */
 int64_t mtp_kernel_launches(void);
 
-/* Timing hook for the benchmark: when enabled, every kernel the handle
- * launches is bracketed by CUDA events on its stream; mtp_profile_read
- * synchronises those events and returns, per kernel kind, the summed
- * milliseconds and the launch count since the last read. Kinds are listed by
- * mtp_profile_kind_name(i) for i < mtp_profile_kinds(). */
-mtp_status mtp_profile_enable(mtp_t h, int32_t on);
+/* Timing hook for the benchmark: kernels of the kinds selected by `mask`
+ * (bit i = kind i, -1 = all, 0 = off) are bracketed by CUDA events on the
+ * launching stream; mtp_profile_read synchronises those events and returns,
+ * per kernel kind, the summed milliseconds and the launch count since the
+ * last read. Kinds are listed by mtp_profile_kind_name(i) for
+ * i < mtp_profile_kinds(). */
+mtp_status mtp_profile_enable(mtp_t h, int32_t mask);
 int32_t mtp_profile_kinds(void);
 const char* mtp_profile_kind_name(int32_t kind);
 mtp_status mtp_profile_read(mtp_t h, float* h_ms, int32_t* h_launches);

@@ -276,8 +276,21 @@ def kv_rollback(h: Handle, rows: int, depth: int, n_acc=None, target_len=None, z
     _check(rc, "kv_rollback")
 
 
-def mtp_profile_enable(h: Handle, on: bool = True):
-    _check(lib().mtp_profile_enable(h.ptr, 1 if on else 0), "mtp_profile_enable")
+PROFILE_KINDS = ("fc", "qkv", "qkv_post", "attention", "o_proj", "gate_up", "down", "lm_head", "sample",
+                 "flush_fc", "flush_kv", "rollback")
+
+
+def mtp_profile_enable(h: Handle, kinds=True):
+    """kinds: True (all), False (off), or an iterable of kind names."""
+    if kinds is True:
+        mask = -1
+    elif not kinds:
+        mask = 0
+    else:
+        mask = 0
+        for k in kinds:
+            mask |= 1 << PROFILE_KINDS.index(k)
+    _check(lib().mtp_profile_enable(h.ptr, mask), "mtp_profile_enable")
 
 
 def mtp_profile_read(h: Handle) -> dict:

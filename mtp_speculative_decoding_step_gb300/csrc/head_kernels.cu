@@ -111,9 +111,9 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
 }
 
 template <typename WT, int MT>
-__global__ void __launch_bounds__(256, (MT <= 2 ? 3 : 2)) k_gemv(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(256, (MT == 1 ? 3 : 2)) k_gemv(const __grid_constant__ GemvArgs a) {
   constexpr int VN = Vec<WT>::N;
-  constexpr int RPW = MT <= 2 ? 8 : (MT == 4 ? 4 : 2);
+  constexpr int RPW = MT <= 4 ? 8 : 2;
   constexpr int ROWS = 8 * RPW;
   extern __shared__ __align__(16) float xs[];
   __shared__ float s_out[MT][ROWS];
@@ -282,13 +282,16 @@ void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
 
 // ------------------------------------------------- q/k norm, RoPE, KV append
 
-// Rotate the pair (x0 at i, x1 at i + dh/2) to position `pos`:
-// angle = pos * theta^(-2i/dh), evaluated in double.
-__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int dh, int pos, float theta) {
-  const double inv = pow((double)theta, -2.0 * (double)i / (double)dh);
-  double sn, cs;
-  sincos((double)pos * inv, &sn, &cs);
-  const float c = (float)cs, s = (float)sn;
+// Rotate the pair (x0 at i, x1 at i + dh/2) to position `pos`: angle =
+// pos * theta^(-2i/dh). inv_freq[i] is that frequency in double (computed on
+// the host at load); the angle is formed and reduced modulo 2*pi in double and
+// its sine/cosine taken in fp32 (error ~2^-24 rad after reduction).
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int pos, const double* inv_freq) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double ang = (double)pos * inv_freq[i];
+  ang -= two_pi * floor(ang / two_pi);
+  float s, c;
+  sincosf((float)ang, &s, &c);
   const float y0 = x0 * c - x1 * s;
   const float y1 = x1 * c + x0 * s;
   x0 = y0;
@@ -317,7 +320,7 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
     x0 = x0 * inv * a.wq[i];
     x1 = x1 * inv * a.wq[i + half];
-    rope_pair(x0, x1, i, a.dh, slot, a.theta);
+    rope_pair(x0, x1, i, slot, a.inv_freq);
     float* dst = a.q_out + (size_t)qd * a.nq * a.dh + h * a.dh;
     dst[i] = x0;
     dst[i + half] = x1;
@@ -328,7 +331,7 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
     x0 = x0 * inv * a.wk[i];
     x1 = x1 * inv * a.wk[i + half];
-    rope_pair(x0, x1, i, a.dh, slot, a.theta);
+    rope_pair(x0, x1, i, slot, a.inv_freq);
     const size_t off = (((size_t)row * a.nkv + g) * a.cap + slot) * a.dh;
     store_elem(a.kc, a.wdt, off + i, x0);
     store_elem(a.kc, a.wdt, off + i + half, x1);
@@ -450,7 +453,11 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
   }
   pdl_trigger();
   const float* qg = a.q + (size_t)m * a.nq * DH + (size_t)g * G * DH;
-  for (int t = tid; t < G * DH; t += blockDim.x) qs[t] = qg[t];
+  float qr[G][EPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) qr[h][e] = qg[h * DH + lane * EPL + e];
 
   float o[G];
 #pragma unroll
@@ -460,19 +467,45 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
     const int rows = min(TS, n - i * TS);
     const bool got = mbar_wait(smem_u32(&bar[i]), 0);
     if (__syncthreads_or(!got)) { ok = false; break; }
-    // scores: warp w takes keys w, w+8, ...; lane owns EPL consecutive dims
-    for (int j = warp; j < rows; j += 8) {
-      const KT* kr = ks + (size_t)(i * TS + j) * DH + lane * EPL;
-      float kv[EPL];
+    // scores: warp w takes keys 8w..8w+7 of the tile; lane owns EPL dims of
+    // every key; the 8 keys x 8 head slots of partial dots are reduced across
+    // the warp by a halving butterfly (62 shuffles), leaving lane l with the
+    // sums of key l/4, head slots 2(l%4) and 2(l%4)+1.
+    {
+      float v[64];
+      const int kb = warp * 8;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)kr)[e]) : ((const float*)kr)[e];
+      for (int kk = 0; kk < 8; ++kk) {
+        float kv[EPL];
+        const int j = kb + kk < rows ? kb + kk : rows - 1;
+        const KT* kr = ks + (size_t)(i * TS + j) * DH + lane * EPL;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float d = 0.f;
+        for (int e = 0; e < EPL; ++e)
+          kv[e] = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)kr)[e]) : ((const float*)kr)[e];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) d = fmaf(qs[h * DH + lane * EPL + e], kv[e], d);
-        d = warp_sum(d);
-        if (lane == 0) ps[h * TS + j] = d * a.scale;
+        for (int h = 0; h < 8; ++h) {
+          float d = 0.f;
+          if (h < G) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) d = fmaf(qr[h][e], kv[e], d);
+          }
+          v[kk * 8 + h] = d;
+        }
+      }
+#pragma unroll
+      for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int t = 0; t < n / 2; ++t) {
+          const float send = up ? v[t] : v[t + n / 2];
+          const float keep = up ? v[t + n / 2] : v[t];
+          v[t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+      }
+      const int key = kb + lane / 4, h0 = 2 * (lane % 4);
+      if (key < rows) {
+        if (h0 < G) ps[h0 * TS + key] = v[0] * a.scale;
+        if (h0 + 1 < G) ps[(h0 + 1) * TS + key] = v[1] * a.scale;
       }
     }
     __syncthreads();
@@ -504,7 +537,20 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[h] = o[h] * st[4 * h + 1];
       const KT* vr = vs + (size_t)i * TS * DH + d;
-      for (int j = 0; j < rows; ++j) {
+      int j = 0;
+      for (; j + 4 <= rows; j += 4) {
+        float vv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          vv[u] = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)vr)[(size_t)(j + u) * DH])
+                                  : ((const float*)vr)[(size_t)(j + u) * DH];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 pp = *reinterpret_cast<const float4*>(ps + h * TS + j);
+          acc[h] = fmaf(pp.x, vv[0], fmaf(pp.y, vv[1], fmaf(pp.z, vv[2], fmaf(pp.w, vv[3], acc[h]))));
+        }
+      }
+      for (; j < rows; ++j) {
         const float v = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)vr)[(size_t)j * DH]) : ((const float*)vr)[(size_t)j * DH];
 #pragma unroll
         for (int h = 0; h < G; ++h) acc[h] = fmaf(ps[h * TS + j], v, acc[h]);
@@ -566,12 +612,12 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
   const float* po = a.po + hq * a.max_chunks * DH + d;
   float num = 0.f;
   int c = 0;
-  for (; c + 8 <= nch; c += 8) {
-    float v[8];
+  for (; c + 16 <= nch; c += 16) {
+    float v[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(c + u) * DH];
+    for (int u = 0; u < 16; ++u) v[u] = po[(size_t)(c + u) * DH];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) num = fmaf(v[u], wch[c + u], num);
+    for (int u = 0; u < 16; ++u) num = fmaf(v[u], wch[c + u], num);
   }
   for (; c < nch; ++c) num = fmaf(po[(size_t)c * DH], wch[c], num);
   a.o[(size_t)m * a.nq * DH + (size_t)h * DH + d] = num / den;

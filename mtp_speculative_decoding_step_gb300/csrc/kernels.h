@@ -52,7 +52,7 @@ struct GemvArgs {
 };
 
 // rows per block group for a batch width MT
-inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 2 ? 8 : (mt == 4 ? 4 : 2)); }
+inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 2); }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.
@@ -64,6 +64,7 @@ struct QkvPostArgs {
   long long split_stride;
   int M, nq, nkv, dh, wdt;
   float eps, theta;
+  const double* inv_freq;  // [dh/2] RoPE frequencies theta^(-2i/dh)
   const float* wq;
   const float* wk;
   float* q_out;          // [n_head][qw] for items with qdst >= 0

@@ -85,6 +85,7 @@ struct mtp_handle {
         *h2 = nullptr, *logits = nullptr, *po = nullptr, *pml = nullptr, *part = nullptr, *gmax = nullptr;
   int *gidx = nullptr, *counters = nullptr, *done = nullptr;
   uint16_t *xb = nullptr, *bb = nullptr;  // bf16 activations of the tensor-core flush
+  double* inv_freq = nullptr;             // RoPE frequencies theta^(-2i/dh), [dh/2]
   float* tcpart = nullptr;                // split-K partial tiles of the tensor-core flush
   int32_t* status = nullptr;
   size_t part_floats = 0;
@@ -93,7 +94,7 @@ struct mtp_handle {
   // host mirror of the row lengths
   std::vector<int> len, keep, drafted_len;
   // profiling
-  bool prof = false;
+  uint32_t prof = 0;  // bit mask of profiled kinds
   std::vector<cudaEvent_t> ev_pool;
   struct Rec { int kind; cudaEvent_t a, b; };
   std::vector<Rec> recs;
@@ -142,14 +143,14 @@ struct ProfScope {
   int kind;
   cudaEvent_t b = nullptr;
   ProfScope(mtp_handle* hh, cudaStream_t ss, int k) : h(hh), s(ss), kind(k) {
-    if (!h->prof) return;
+    if (!(h->prof >> kind & 1u)) return;
     cudaEvent_t a = next();
     b = next();
     cudaEventRecord(a, s);
     h->recs.push_back({kind, a, b});
   }
   ~ProfScope() {
-    if (h->prof && b) cudaEventRecord(b, s);
+    if (b) cudaEventRecord(b, s);
   }
   cudaEvent_t next() {
     if (h->ev_next >= h->ev_pool.size()) {
@@ -305,7 +306,7 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
       a.ld = ldq; a.q_off = 0; a.k_off = qw; a.v_off = qw + kw; a.nsplit = 1; a.split_stride = 0;
       a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
       a.eps = c.eps; a.theta = c.rope_theta;
-      a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN];
+      a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN]; a.inv_freq = h->inv_freq;
       a.q_out = h->qrot;
       a.kc = h->kv.k; a.vc = h->kv.v; a.cap = c.kv_capacity;
       for (int m = 0; m < mp; ++m) {
@@ -422,7 +423,7 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
     a.nsplit = ks; a.split_stride = (long long)mp * 2 * kw;
     a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
     a.eps = c.eps; a.theta = c.rope_theta;
-    a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN]; a.q_out = h->qrot;
+    a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN]; a.q_out = h->qrot; a.inv_freq = h->inv_freq;
     a.kc = h->kv.k; a.vc = h->kv.v; a.cap = c.kv_capacity;
     for (int m = 0; m < mp; ++m) {
       a.row[m] = all.row[m0 + m];
@@ -588,6 +589,12 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
   if (st == MTP_OK) st = alloc(h, &h->done, 1);
   if (st == MTP_OK) st = alloc(h, &h->status, 1);
+  if (st == MTP_OK) st = alloc(h, &h->inv_freq, (size_t)dh / 2);
+  if (st == MTP_OK) {
+    std::vector<double> f(dh / 2);
+    for (int i = 0; i < dh / 2; ++i) f[i] = std::pow((double)c.rope_theta, -2.0 * i / (double)dh);
+    st = cuda_ok(cudaMemcpy(h->inv_freq, f.data(), sizeof(double) * f.size(), cudaMemcpyHostToDevice));
+  }
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->counters, 0, sizeof(int) * groups, s));
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->done, 0, sizeof(int), s));
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->status, 0, sizeof(int32_t), s));
@@ -852,9 +859,9 @@ mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* 
 
 int64_t mtp_kernel_launches(void) { return (int64_t)launches_so_far(); }
 
-mtp_status mtp_profile_enable(mtp_t h, int32_t on) {
+mtp_status mtp_profile_enable(mtp_t h, int32_t mask) {
   if (!h) return MTP_ERR_BAD_ARG;
-  h->prof = on != 0;
+  h->prof = (uint32_t)mask;
   return MTP_OK;
 }
 
