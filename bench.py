@@ -59,6 +59,14 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -265,6 +273,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = e2e_ms / 1e3
 
     h.close()
+    flush, flush_flops, flush_bytes = ({}, 0.0, 0.0) if args.quick else measure_flush(tensors, embed, s, dev)
+    sampled = None if args.quick else measure_sampled(tensors, embed, s, dev)
+    batched = None if args.quick else measure_batched(tensors, embed, s, dev)
 
     H, Vocab = s.hidden, s.vocab
     lm_bytes = Vocab * H * 2 + Vocab * 4 + H * 4
@@ -309,6 +320,10 @@ def run_ours(args, rank, world, local_rank):
                      "traffic_source": "ncu capture at V=32768 scaled by rows to V=152064",
                      "bytes_per_launch": lm_bytes},
         "gpu_launches": int(launches),
+        "sampled_depth_sweep": sampled,
+        "batched_8_rows": batched,
+        "flush_256_pairs": {"by_offset": flush, "flops": flush_flops, "weight_bytes": flush_bytes,
+                            "bf16_peak_tflops": peak_bf16(), "bound": "tensor/hbm ridge"} if flush else None,
         "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
                 "h2d_bytes_per_step": (DEPTH + 1) * Vocab * 4 + (DEPTH + 1) * H * 2,
                 "d2h_bytes_per_step": 4 * (DEPTH + 2)},
@@ -316,6 +331,205 @@ def run_ours(args, rank, world, local_rank):
         "wall_s": round(wall, 3),
     }
     return result, (s, model, K, V, base, thid, tok0, coins)
+
+
+def measure_flush(tensors, embed, s, dev, reps: int = 20):
+    """Flush of 256 completed pairs into the draft KV at starting offsets 0,
+    8192 and 32768 (tensor-core path), timed with CUDA events; reported as
+    pairs/s and as tensor throughput against the measured bf16 peak."""
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+    npairs, cap = 256, 32768 + 256
+    kw = s.n_kv * s.head_dim
+    flops = 2.0 * npairs * (s.hidden * 2 * s.hidden + 2 * kw * s.hidden)
+    wbytes = 2.0 * (s.hidden * 2 * s.hidden + 2 * kw * s.hidden)
+    kk = torch.zeros((1, s.n_kv, cap, s.head_dim), dtype=torch.bfloat16, device=dev)
+    vv = torch.zeros_like(kk)
+    klen = torch.zeros(1, dtype=torch.int32, device=dev)
+    cfg = m.make_config(s, 1, cap, 2)
+    h = m.mtp_load(cfg, tensors, embed, None, kk, vv, klen, lengths=[0])
+    tok = torch.from_numpy(synth.randint(3, "flush:tok", (1, npairs), s.vocab)).to(dev)
+    hid = torch.from_numpy(synth.normal(3, "flush:hid", (1, npairs, s.hidden), dtype="bf16")).view(
+        torch.bfloat16).to(dev)
+    stream = torch.cuda.current_stream()
+    out = {}
+    for off in (0, 8192, 32768):
+        for i in range(3):
+            m.mtp_set_lengths(h, [off])
+            m.mtp_flush(h, [npairs], tok, hid)
+        m.mtp_profile_enable(h, ["flush_fc", "flush_kv"])
+        m.mtp_profile_read(h)
+        ms = 0.0
+        for i in range(reps):
+            m.mtp_set_lengths(h, [off])
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            m.mtp_flush(h, [npairs], tok, hid)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        prof = m.mtp_profile_read(h)
+        m.mtp_profile_enable(h, False)
+        t = ms / reps / 1e3
+        out[str(off)] = {"us": round(t * 1e6, 2), "pairs_per_s": round(npairs / t, 1),
+                         "tflops": round(flops / t / 1e12, 2), "weight_gbs": round(wbytes / t / 1e9, 1),
+                         "fc_us": round(1e3 * prof["flush_fc"][0] / max(prof["flush_fc"][1], 1), 2),
+                         "kv_us": round(1e3 * prof["flush_kv"][0] / max(prof["flush_kv"][1], 1), 2)}
+    h.close()
+    return out, flops, wbytes
+
+
+SAMPLED = dict(temperature=0.8, rep_penalty=1.1, top_k=40, top_p=0.95, min_p=0.05)
+
+
+def measure_sampled(tensors, embed, s, dev, rounds: int = 100):
+    """Sampled decoding on the 27B-shaped head: T 0.8, repetition penalty 1.1
+    over a 64-token history, top-k 40, top-p 0.95, min-p 0.05, depth 1..6.
+    Target row i = the drafter's logits at step i+1 plus N(0,1) noise (the
+    bonus row N(0,4)), so acceptance is partial. Reports per-position
+    acceptance, rollbacks, drafted tok/s and the verify / sampler times."""
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+    V, H, W = s.vocab, s.hidden, 64
+    cap = KV_LEN + 1024
+    out = {}
+    params = m.sampling_array([SAMPLED])
+    stream = torch.cuda.current_stream()
+    noise = torch.from_numpy(synth.normal(7, "smp:noise", (8, 6, V), std=1.0)).to(dev)
+    bonus = torch.from_numpy(synth.normal(7, "smp:bonus", (8, V), std=4.0)).to(dev)
+    thid = torch.from_numpy(synth.normal(7, "smp:hid", (8, 7, H), dtype="bf16")).view(torch.bfloat16).to(dev)
+    K, Vc = synth.kv_prefill(s, 7, 1, cap, [KV_LEN])
+    for depth in range(1, 7):
+        kk = torch.from_numpy(K).view(torch.bfloat16).to(dev)
+        vv = torch.from_numpy(Vc).view(torch.bfloat16).to(dev)
+        klen = torch.tensor([KV_LEN], dtype=torch.int32, device=dev)
+        h = m.mtp_load(m.make_config(s, 1, cap, 6), tensors, embed, None, kk, vv, klen, lengths=[KV_LEN])
+        hist = torch.from_numpy(synth.randint(7, "smp:hist", (1, W), V)).to(dev)
+        ud = torch.from_numpy(synth.uniform(7, f"smp:ud{depth}", (rounds + 4, 1, depth))).to(dev)
+        uv = torch.from_numpy(synth.uniform(7, f"smp:uv{depth}", (rounds + 4, 1, depth + 1))).to(dev)
+        draft = torch.zeros((1, depth), dtype=torch.int32, device=dev)
+        q = torch.zeros((1, depth, V), dtype=torch.float32, device=dev)
+        dl = torch.zeros((1, depth, V), dtype=torch.float32, device=dev)
+        tl = torch.zeros((1, depth + 1, V), dtype=torch.float32, device=dev)
+        n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+        out_tok = torch.zeros((1, depth + 1), dtype=torch.int32, device=dev)
+        out_tok[0, 0] = 11
+        stats = torch.zeros((1, depth + 2), dtype=torch.int32, device=dev)
+        ws = torch.zeros(m.spec_verify_workspace_bytes(1, depth, V), dtype=torch.uint8, device=dev)
+        h_out = torch.zeros(depth + 2, dtype=torch.int32).pin_memory()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        P, vt, committed = 1, 0.0, 0
+        m.mtp_profile_enable(h, ["sample"])
+        for r in range(rounds + 2):
+            if r == 2:
+                torch.cuda.synchronize()
+                m.mtp_profile_read(h)
+                stats.zero_()
+                ev[0].record(stream)
+                vt, committed = 0.0, 0
+            m.mtp_draft(h, depth, [P], out_tok, thid[r % 8].view(1, 7, H)[:, :depth + 1], params, draft,
+                        hist=hist, u=ud[r], q=q, logits=dl)
+            tl[0, :depth] = dl[0] + noise[r % 8, :depth]
+            tl[0, depth] = bonus[r % 8]
+            ev[1].record(stream)
+            m.spec_verify(tl, draft, params, uv[r], n_acc, out_tok, ws, q=q, hist=hist, stats=stats, h_out=h_out)
+            ev[2].record(stream)
+            m.kv_rollback(h, 1, depth)
+            if r % 64 == 63:
+                m.mtp_set_lengths(h, [KV_LEN])
+            stream.synchronize()
+            n = int(h_out[0])
+            if r >= 2:
+                vt += ev[1].elapsed_time(ev[2])
+                committed += n + 1
+            # the committed tokens enter the penalty history
+            hist = torch.cat([hist[:, n + 1:], out_tok[:, :n + 1]], dim=1)
+            P = n + 1
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[3])
+        st = stats.cpu().numpy()[0]
+        prof = m.mtp_profile_read(h)
+        m.mtp_profile_enable(h, False)
+        out[str(depth)] = {"rounds": int(st[0]), "rollbacks": int(st[1]),
+                           "accept_per_position": [round(int(x) / max(int(st[0]), 1), 4) for x in st[2:]],
+                           "draft_tok_per_s": round(rounds * depth / (ms / 1e3), 1),
+                           "committed_tok_per_s": round(committed / (ms / 1e3), 1),
+                           "verify_us": round(1e3 * vt / rounds, 2),
+                           "draft_sampler_us": round(1e3 * prof["sample"][0] / max(prof["sample"][1], 1), 2)}
+        h.close()
+    return out
+
+
+def measure_batched(tensors, embed, s, dev, reps: int = 20):
+    """8 independent rows on the 27B-shaped head, draft KV lengths drawn from
+    U[1024, 16384], depth 3, rows alternating greedy and (T 0.7, top-p 0.9):
+    one draft call over all rows, one verify over all rows, per-row rollback.
+    The verify is also reported against its algorithmic bytes (target logits
+    of every row and position, q of the sampled rows, read once)."""
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+    R, depth, V, H = 8, 3, s.vocab, s.hidden
+    lens = [int(x) for x in (1024 + synth.randint(40, "lens", (R,), 16384 - 1024 + 1))]
+    cap = (max(lens) + 256 + 63) // 64 * 64
+    K, Vc = synth.kv_prefill(s, 40, R, cap, lens)
+    kk = torch.from_numpy(K).view(torch.bfloat16).to(dev)
+    vv = torch.from_numpy(Vc).view(torch.bfloat16).to(dev)
+    del K, Vc
+    klen = torch.tensor(lens, dtype=torch.int32, device=dev)
+    h = m.mtp_load(m.make_config(s, R, cap, depth), tensors, embed, None, kk, vv, klen, lengths=lens)
+    rows = [dict(temperature=0.0) if r % 2 == 0 else dict(temperature=0.7, top_p=0.9) for r in range(R)]
+    params = m.sampling_array(rows)
+    tok = torch.from_numpy(synth.randint(40, "tok0", (R, 1), V)).to(dev)
+    hid = torch.from_numpy(synth.normal(40, "hid", (R, 1, H), dtype="bf16")).view(torch.bfloat16).to(dev)
+    hist = torch.from_numpy(synth.randint(40, "hist", (R, 64), V)).to(dev)
+    ud = torch.from_numpy(synth.uniform(40, "ud", (R, depth))).to(dev)
+    uv = torch.from_numpy(synth.uniform(40, "uv", (R, depth + 1))).to(dev)
+    draft = torch.zeros((R, depth), dtype=torch.int32, device=dev)
+    q = torch.zeros((R, depth, V), dtype=torch.float32, device=dev)
+    dl = torch.zeros((R, depth, V), dtype=torch.float32, device=dev)
+    tl = torch.from_numpy(synth.normal(40, "tl", (R, depth + 1, V), std=4.0)).to(dev)
+    n_acc = torch.zeros(R, dtype=torch.int32, device=dev)
+    out_tok = torch.zeros((R, depth + 1), dtype=torch.int32, device=dev)
+    ws = torch.zeros(m.spec_verify_workspace_bytes(R, depth, V), dtype=torch.uint8, device=dev)
+    flush = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)  # > L2: flush between timed verifies
+    stream = torch.cuda.current_stream()
+    dt = vt = 0.0
+    for i in range(reps + 2):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        m.mtp_set_lengths(h, lens)
+        e[0].record(stream)
+        m.mtp_draft(h, depth, [1] * R, tok, hid, params, draft, hist=hist, u=ud, q=q, logits=dl)
+        e[1].record(stream)
+        tl[:, :depth] = dl + 0.5
+        flush.add_(1)
+        flush.add_(1)
+        e[2].record(stream)
+        m.spec_verify(tl, draft, params, uv, n_acc, out_tok, ws, q=q, hist=hist)
+        e[3].record(stream)
+        m.kv_rollback(h, R, depth)
+        torch.cuda.synchronize()
+        if i >= 2:
+            dt += e[0].elapsed_time(e[1])
+            vt += e[2].elapsed_time(e[3])
+    h.close()
+    dt, vt = dt / reps / 1e3, vt / reps / 1e3
+    sampled_rows = sum(1 for r in rows if r["temperature"] > 0)
+    vbytes = R * (depth + 1) * V * 4 + sampled_rows * depth * V * 4
+    wbytes = 2 * (H * 2 * H + (24 * 256 + 2 * 4 * 256) * H + H * 24 * 256 + 3 * 17408 * H) + 2 * V * H
+    kvbytes = sum(2 * 4 * 256 * 2 * (L + 1) for L in lens)
+    return {"rows": R, "depth": depth, "kv_lens": lens,
+            "draft_tok_per_s": round(R * depth / dt, 1), "draft_step_us": round(1e6 * dt / depth, 1),
+            "draft_step_hbm_gbs": round((wbytes + kvbytes) / (dt / depth) / 1e9, 1),
+            "verify_us": round(1e6 * vt, 2), "verify_bytes": vbytes,
+            "verify_gbs": round(vbytes / vt / 1e9, 1), "verify_l2": "flushed (128 MiB write) before each verify"}
 
 
 def cpu_rounds(work, budget_s: float, max_rounds: int):

@@ -121,13 +121,53 @@ __device__ unsigned long long cluster_sum_u64(Clu& c, unsigned long long local) 
 // Radix selection over the cluster: among active elements ordered by
 // (key asc, id asc) with integer weights, find the key K* of the element at
 // which the running weight first reaches `target`, and how much of the
-// target remains within the elements whose key is K*.
+// target remains within the elements whose key is K*. The digits start at the
+// highest bit where the active keys differ (from their cluster-wide min and
+// max), so the bins spread over the keys actually present.
 template <class Act, class Wt>
 __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, Wt weight,
                              unsigned long long target, uint32_t& key_out, unsigned long long& rem_out) {
   SampleSmem* sm = c.sm;
-  uint32_t prefix = 0, mask = 0;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int j = threadIdx.x; j < n_local; j += kST)
+    if (active(j)) {
+      const uint32_t k = desc_key(zs[j]);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = 0xFFFFFFFFu, b = 0u;
+    for (int w = 0; w < kST / 32; ++w) {
+      a = min(a, (uint32_t)(sm->wsum[w] >> 32));
+      b = max(b, (uint32_t)sm->wsum[w]);
+    }
+    sm->mail[c.ph].u[0] = a;
+    sm->mail[c.ph].u[1] = b;
+  }
+  Mail* mm = c.publish();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    kmin = min(kmin, (uint32_t)c.remote(mm, r)->u[0]);
+    kmax = max(kmax, (uint32_t)c.remote(mm, r)->u[1]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
+  uint32_t prefix = kmin & mask;
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
     unsigned long long* h = sm->hist[c.ph];
     for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0;
     __syncthreads();
@@ -135,7 +175,7 @@ __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, W
       if (!active(j)) continue;
       const uint32_t k = desc_key(zs[j]);
       if ((k & mask) != prefix) continue;
-      atomicAdd(&h[(k >> shift) & 255u], weight(j));
+      atomicAdd(&h[(k >> lo) & dmask], weight(j));
     }
     c.cl.sync();
     for (int b = threadIdx.x; b < 256; b += kST) {
@@ -170,15 +210,16 @@ __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, W
       }
       const unsigned any = __ballot_sync(0xFFFFFFFFu, mine);
       if (!any && lane == 0) {  // target above the total: keep everything
-        sm->sel_bin = 255;
+        sm->sel_bin = (int)dmask;
         sm->sel_rem = target;
       }
     }
     __syncthreads();
-    prefix |= (uint32_t)sm->sel_bin << shift;
-    mask |= 255u << shift;
+    prefix |= (uint32_t)sm->sel_bin << lo;
+    mask |= dmask << lo;
     target = sm->sel_rem;
     __syncthreads();
+    hi = lo - 1;
   }
   key_out = prefix;
   rem_out = target;
