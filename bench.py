@@ -570,6 +570,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (small profiling cases)")
     ap.add_argument("--quick", action="store_true", help="skip the end-to-end and CPU-baseline legs")
+    ap.add_argument("--flush-only", action="store_true", help="time only the 256-pair flush (profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -618,6 +619,15 @@ def main():
         oracle.build()
     if world > 1:
         torch.distributed.barrier()
+    if args.flush_only:
+        import torch as _t
+        s, model, K, V, base, thid, tok0 = build_workload(args.seed, rank, args.vocab)
+        dev = _t.device("cuda", local_rank)
+        to = lambda a: (_t.from_numpy(a).view(_t.bfloat16) if a.dtype == np.uint16 else _t.from_numpy(a)).to(dev)
+        tensors = {n: to(a) for n, a in model.tensors.items()}
+        flush, flops, wbytes = measure_flush(tensors, to(model.embed), s, dev, reps=max(args.steps, 1))
+        print(json.dumps({"flush_256_pairs": flush, "flops": flops, "weight_bytes": wbytes}), flush=True)
+        return
     result, work = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.quick:

@@ -50,26 +50,51 @@ template <typename WT, int MT, int RPW>
 __device__ __forceinline__ void gemv_fma(float (&acc)[RPW][MT], const uint4 (&w)[RPW], const float* xs,
                                          int KS, int kb) {
   constexpr int VN = Vec<WT>::N;
-  float xv[MT][VN];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    const float4* p = reinterpret_cast<const float4*>(xs + m * KS + kb);
-#pragma unroll
-    for (int j = 0; j < VN / 4; ++j) {
-      float4 t = p[j];
-      xv[m][4 * j] = t.x; xv[m][4 * j + 1] = t.y; xv[m][4 * j + 2] = t.z; xv[m][4 * j + 3] = t.w;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) {
-    float wf[VN];
-    Vec<WT>::unpack(w[i], wf);
+  if constexpr (MT <= 4) {
+    // x of every item held in registers, reused across the RPW rows
+    float xv[MT][VN];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      float a = acc[i][m];
+      const float4* p = reinterpret_cast<const float4*>(xs + m * KS + kb);
 #pragma unroll
-      for (int j = 0; j < VN; ++j) a = fmaf(wf[j], xv[m][j], a);
-      acc[i][m] = a;
+      for (int j = 0; j < VN / 4; ++j) {
+        float4 t = p[j];
+        xv[m][4 * j] = t.x; xv[m][4 * j + 1] = t.y; xv[m][4 * j + 2] = t.z; xv[m][4 * j + 3] = t.w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      float wf[VN];
+      Vec<WT>::unpack(w[i], wf);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        float a = acc[i][m];
+#pragma unroll
+        for (int j = 0; j < VN; ++j) a = fmaf(wf[j], xv[m][j], a);
+        acc[i][m] = a;
+      }
+    }
+  } else {
+    // wide batches: rows unpacked once, x of one item at a time
+    float wf[RPW][VN];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) Vec<WT>::unpack(w[i], wf[i]);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float xv[VN];
+      const float4* p = reinterpret_cast<const float4*>(xs + m * KS + kb);
+#pragma unroll
+      for (int j = 0; j < VN / 4; ++j) {
+        float4 t = p[j];
+        xv[4 * j] = t.x; xv[4 * j + 1] = t.y; xv[4 * j + 2] = t.z; xv[4 * j + 3] = t.w;
+      }
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        float a = acc[i][m];
+#pragma unroll
+        for (int j = 0; j < VN; ++j) a = fmaf(wf[i][j], xv[j], a);
+        acc[i][m] = a;
+      }
     }
   }
 }
@@ -113,7 +138,7 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
 template <typename WT, int MT>
 __global__ void __launch_bounds__(256, (MT == 1 ? 3 : 2)) k_gemv(const __grid_constant__ GemvArgs a) {
   constexpr int VN = Vec<WT>::N;
-  constexpr int RPW = MT <= 4 ? 8 : 2;
+  constexpr int RPW = MT <= 4 ? 8 : 4;
   constexpr int ROWS = 8 * RPW;
   extern __shared__ __align__(16) float xs[];
   __shared__ float s_out[MT][ROWS];
@@ -355,15 +380,26 @@ __global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
     const int dt = half == 0 ? a.wdt : a.hid_dt;
     const size_t base = half == 0 ? (size_t)t * H : (size_t)a.hid_item[m] * H;
     const float* w = half == 0 ? a.nw_e : a.nw_h;
-    float ss = 0.f;
-    for (int k = threadIdx.x; k < H; k += blockDim.x) {
-      const float v = load_elem(src, dt, base + k);
-      ss = fmaf(v, v, ss);
+    const float inv = rsqrtf(row_sumsq(src, dt, base, H, red) / (float)H + a.eps);
+    // 8 elements per thread step: one 16-byte store of bf16
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+      float f[8];
+      if (dt == MTP_DTYPE_BF16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base) + i);
+        f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+        f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+      } else {
+        const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base) + 2 * i;
+        const float4 u0 = p4[0], u1 = p4[1];
+        f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w; f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = (uint32_t)f_to_bf16(f[2 * j] * inv * w[8 * i + 2 * j]) |
+               ((uint32_t)f_to_bf16(f[2 * j + 1] * inv * w[8 * i + 2 * j + 1]) << 16);
+      reinterpret_cast<uint4*>(x + half * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    ss = block_sum(ss, red);
-    const float inv = rsqrtf(ss / (float)H + a.eps);
-    for (int k = threadIdx.x; k < H; k += blockDim.x)
-      x[half * H + k] = f_to_bf16(load_elem(src, dt, base + k) * inv * w[k]);
   }
 }
 
@@ -377,18 +413,52 @@ __global__ void k_flush_norm(const float* part, int nsplit, long long split_stri
   __shared__ float red[32];
   const int m = blockIdx.x;
   const float* p = part + (size_t)m * H;
+  // sum the split-K partials of this row (4 elements per step)
+  float4 v[4];  // H <= 16384 -> at most 16 float4 per thread with 256 threads
+  const int n4 = H / 4;
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    float v = p[k];
-    for (int sidx = 1; sidx < nsplit; ++sidx) v += p[(size_t)sidx * split_stride + k];
-    ss = fmaf(v, v, ss);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < n4) {
+      for (int sidx = 0; sidx < nsplit; ++sidx) {
+        const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
+        acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+      }
+    }
+    v[u] = acc;
+    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+  }
+  for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {  // H > 4096
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sidx = 0; sidx < nsplit; ++sidx) {
+      const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
+      acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+    }
+    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)H + eps);
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    float v = p[k];
-    for (int sidx = 1; sidx < nsplit; ++sidx) v += p[(size_t)sidx * split_stride + k];
-    b[(size_t)m * H + k] = f_to_bf16(v * inv * w[k]);
+  uint2* out = reinterpret_cast<uint2*>(b + (size_t)m * H);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    if (i < n4) {
+      const float4 ww = reinterpret_cast<const float4*>(w)[i];
+      out[i] = make_uint2((uint32_t)f_to_bf16(v[u].x * inv * ww.x) | ((uint32_t)f_to_bf16(v[u].y * inv * ww.y) << 16),
+                          (uint32_t)f_to_bf16(v[u].z * inv * ww.z) | ((uint32_t)f_to_bf16(v[u].w * inv * ww.w) << 16));
+    }
+  }
+  for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sidx = 0; sidx < nsplit; ++sidx) {
+      const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
+      acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+    }
+    const float4 ww = reinterpret_cast<const float4*>(w)[i];
+    out[i] = make_uint2((uint32_t)f_to_bf16(acc.x * inv * ww.x) | ((uint32_t)f_to_bf16(acc.y * inv * ww.y) << 16),
+                        (uint32_t)f_to_bf16(acc.z * inv * ww.z) | ((uint32_t)f_to_bf16(acc.w * inv * ww.w) << 16));
   }
 }
 

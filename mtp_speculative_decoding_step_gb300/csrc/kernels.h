@@ -52,7 +52,7 @@ struct GemvArgs {
 };
 
 // rows per block group for a batch width MT
-inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 2); }
+inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.

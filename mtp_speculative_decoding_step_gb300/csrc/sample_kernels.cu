@@ -171,11 +171,20 @@ __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, W
     unsigned long long* h = sm->hist[c.ph];
     for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0;
     __syncthreads();
-    for (int j = threadIdx.x; j < n_local; j += kST) {
-      if (!active(j)) continue;
-      const uint32_t k = desc_key(zs[j]);
-      if ((k & mask) != prefix) continue;
-      atomicAdd(&h[(k >> lo) & dmask], weight(j));
+    // warp-aggregated: lanes with the same bin add their weights (split in
+    // 24-bit halves so the 32-bit warp sums stay exact), one atomic per bin
+    for (int base = 0; base < n_local; base += kST) {
+      const int j = base + threadIdx.x;
+      bool act = j < n_local && active(j);
+      const uint32_t k = act ? desc_key(zs[j]) : 0u;
+      act = act && (k & mask) == prefix;
+      const uint32_t bin = act ? ((k >> lo) & dmask) : 0xFFFFFFFFu;
+      const unsigned long long w = act ? weight(j) : 0ull;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
+      const unsigned sl = __reduce_add_sync(peers, (unsigned)(w & 0xFFFFFFull));
+      const unsigned sh = __reduce_add_sync(peers, (unsigned)(w >> 24));
+      if (act && (int)(threadIdx.x & 31) == __ffs(peers) - 1)
+        atomicAdd(&h[bin], ((unsigned long long)sh << 24) + (unsigned long long)sl);
     }
     c.cl.sync();
     for (int b = threadIdx.x; b < 256; b += kST) {
