@@ -385,7 +385,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
 SAMPLED = dict(temperature=0.8, rep_penalty=1.1, top_k=40, top_p=0.95, min_p=0.05)
 
 
-def measure_sampled(tensors, embed, s, dev, rounds: int = 100):
+def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 4, 5, 6)):
     """Sampled decoding on the 27B-shaped head: T 0.8, repetition penalty 1.1
     over a 64-token history, top-k 40, top-p 0.95, min-p 0.05, depth 1..6.
     Target row i = the drafter's logits at step i+1 plus N(0,1) noise (the
@@ -404,7 +404,7 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100):
     bonus = torch.from_numpy(synth.normal(7, "smp:bonus", (8, V), std=4.0)).to(dev)
     thid = torch.from_numpy(synth.normal(7, "smp:hid", (8, 7, H), dtype="bf16")).view(torch.bfloat16).to(dev)
     K, Vc = synth.kv_prefill(s, 7, 1, cap, [KV_LEN])
-    for depth in range(1, 7):
+    for depth in depths:
         kk = torch.from_numpy(K).view(torch.bfloat16).to(dev)
         vv = torch.from_numpy(Vc).view(torch.bfloat16).to(dev)
         klen = torch.tensor([KV_LEN], dtype=torch.int32, device=dev)
@@ -571,6 +571,8 @@ def main():
     ap.add_argument("--vocab", type=int, default=0, help="override the vocabulary (small profiling cases)")
     ap.add_argument("--quick", action="store_true", help="skip the end-to-end and CPU-baseline legs")
     ap.add_argument("--flush-only", action="store_true", help="time only the 256-pair flush (profiling case)")
+    ap.add_argument("--sampled-only", action="store_true",
+                    help="time only sampled rounds at depth 1 (profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -619,6 +621,15 @@ def main():
         oracle.build()
     if world > 1:
         torch.distributed.barrier()
+    if args.sampled_only:
+        import torch as _t
+        s, model, K, V, base, thid, tok0 = build_workload(args.seed, rank, args.vocab)
+        dev = _t.device("cuda", local_rank)
+        to = lambda a: (_t.from_numpy(a).view(_t.bfloat16) if a.dtype == np.uint16 else _t.from_numpy(a)).to(dev)
+        tensors = {n: to(a) for n, a in model.tensors.items()}
+        out = measure_sampled(tensors, to(model.embed), s, dev, rounds=max(args.steps, 1), depths=(1,))
+        print(json.dumps({"sampled": out}), flush=True)
+        return
     if args.flush_only:
         import torch as _t
         s, model, K, V, base, thid, tok0 = build_workload(args.seed, rank, args.vocab)

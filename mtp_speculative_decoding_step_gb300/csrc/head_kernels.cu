@@ -335,7 +335,7 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
-  const int m = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = a.dh / 2;
+  const int m = blockIdx.x, h = blockIdx.y + (a.q_off < 0 ? a.nq : 0), i = threadIdx.x, half = a.dh / 2;
   const int slot = a.slot[m], row = a.row[m];
   if (h < a.nq) {
     const int qd = a.qdst[m];
@@ -469,7 +469,8 @@ void launch_flush_norm(const float* part, int nsplit, long long split_stride, in
 }
 
 void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
-  launch_pdl(k_qkv_post, dim3(a.M, a.nq + a.nkv), dim3(a.dh / 2), 0, s, a);
+  // without q (flush) only the kv heads have work
+  launch_pdl(k_qkv_post, dim3(a.M, (a.q_off < 0 ? 0 : a.nq) + a.nkv), dim3(a.dh / 2), 0, s, a);
   count_launch();
 }
 

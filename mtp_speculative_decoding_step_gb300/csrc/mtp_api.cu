@@ -303,7 +303,7 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
       QkvPostArgs a;
       std::memset(&a, 0, sizeof(a));
       a.qkv = h->qkv + (size_t)m0 * ldq;
-      a.ld = ldq; a.q_off = 0; a.k_off = qw; a.v_off = qw + kw; a.nsplit = 1; a.split_stride = 0;
+      a.ld = ldq; a.q_off = need_q ? 0 : -1; a.k_off = qw; a.v_off = qw + kw; a.nsplit = 1; a.split_stride = 0;
       a.M = mp; a.nq = c.n_q; a.nkv = c.n_kv; a.dh = c.head_dim; a.wdt = c.dtype;
       a.eps = c.eps; a.theta = c.rope_theta;
       a.wq = h->nrm[T_QN]; a.wk = h->nrm[T_KN]; a.inv_freq = h->inv_freq;
