@@ -168,6 +168,8 @@ struct SampleArgs {
   int32_t* draft_out;        // draft: [rows][depth]
   TDesc* desc;               // verify: [rows][depth+1]
   int32_t* status;
+  int cand;                  // local candidates per CTA (set by launch_sample)
+  int merge;                 // merged candidate buffer (power of two)
   RowParams p[kMaxRows];
 };
 void launch_sample(const SampleArgs& a, cudaStream_t s);

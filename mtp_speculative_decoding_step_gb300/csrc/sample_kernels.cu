@@ -58,6 +58,11 @@ struct SampleSmem {
   int sel_bin;
   unsigned long long sel_rem;
   int found;
+  int ccount;
+  int fin_kf;
+  int fin_valid;
+  unsigned long long fin_sf;
+  int fin_draw;
 };
 
 // Cluster context for one task.
@@ -375,11 +380,339 @@ __device__ __forceinline__ bool in_prefix(uint32_t key, int v, uint32_t K, int c
   return key < K || (key == K && v <= cut);
 }
 
+// ------------------------------------------------------------ candidate path
+// Most rows keep a small support (top-k set, or a peaky top-p/min-p prefix).
+// Each CTA selects its local top-C keys with block-local passes, the cluster
+// exchanges them once, and every CTA sorts the union by (key, id) -- the
+// oracle's (transformed logit desc, id asc) order -- and cuts top-k, top-p and
+// min-p on that list. The first C entries of the sorted union are the global
+// top-C, so the cut is exact whenever it falls inside them (always with top-k
+// <= C); otherwise the full cluster radix path below is used.
+
+constexpr int kCandTopP = 128;  // local candidates per CTA when no top-k is set
+
+struct CandBufs {
+  uint32_t* ckey;  // [C] local candidates
+  int* cid;
+  uint32_t* mkey;  // [P] merged, sorted
+  int* mid;
+  unsigned long long* sw;  // [C] draw weights in id order
+  int* sid;
+  int C, P;
+};
+
+__device__ __forceinline__ float key_to_z(uint32_t K) {
+  uint32_t u = ~K;
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+// Exactly min(C, n) local elements satisfy in_prefix(key, v0 + j, K, cut).
+__device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int C, uint32_t& Kout, int& cut) {
+  if (n <= C) { Kout = 0xFFFFFFFFu; cut = 0x7FFFFFFF; return; }
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const uint32_t k = desc_key(zs[j]);
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+  __syncthreads();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int w = 0; w < kST / 32; ++w) {
+    kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
+    kmax = max(kmax, (uint32_t)sm->wsum[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
+  uint32_t prefix = kmin & mask;
+  unsigned long long target = (unsigned long long)C;
+  unsigned long long* h = sm->hist[0];
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kST) {
+      const int j = base + threadIdx.x;
+      const uint32_t k = j < n ? desc_key(zs[j]) : 0u;
+      const bool act = j < n && (k & mask) == prefix;
+      const uint32_t bin = act ? ((k >> lo) & dmask) : 0xFFFFFFFFu;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
+      if (act && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (unsigned long long)__popc(peers));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      unsigned long long s8 = 0;
+      for (int b = 0; b < 8; ++b) s8 += h[lane * 8 + b];
+      unsigned long long incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned long long cum = incl - s8;
+      if (cum < target && target <= incl) {
+        for (int b = 0; b < 8; ++b) {
+          const unsigned long long t = h[lane * 8 + b];
+          if (cum < target && target <= cum + t) {
+            sm->sel_bin = lane * 8 + b;
+            sm->sel_rem = target - cum;
+            break;
+          }
+          cum += t;
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm->sel_bin << lo;
+    mask |= dmask << lo;
+    target = sm->sel_rem;
+    hi = lo - 1;
+  }
+  Kout = prefix;
+  // ties at K: keep the first `target` of them in index order
+  unsigned long long ties = 0;
+  for (int j = threadIdx.x; j < n; j += kST)
+    if (desc_key(zs[j]) == prefix) ++ties;
+  ties = block_sum_u64(ties, sm->wsum);
+  if (target >= ties) { cut = 0x7FFFFFFF; return; }
+  unsigned long long need = target;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) sm->found = 0x7FFFFFFF;
+  __syncthreads();
+  for (int base = 0; base < n; base += kST) {
+    const int j = base + threadIdx.x;
+    const unsigned flag = (j < n && desc_key(zs[j]) == prefix) ? 1u : 0u;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, flag);
+    __syncthreads();
+    if (lane == 0) sm->wsum[w] = __popc(bal);
+    __syncthreads();
+    unsigned long long wbefore = 0, chunk = 0;
+    for (int k = 0; k < kST / 32; ++k) {
+      if (k < w) wbefore += sm->wsum[k];
+      chunk += sm->wsum[k];
+    }
+    const unsigned long long incl = wbefore + __popc(bal & ((2u << lane) - 1u));
+    if (flag && incl == need) sm->found = v0 + j;
+    __syncthreads();
+    if (chunk >= need) break;
+    need -= chunk;
+  }
+  cut = sm->found;
+  __syncthreads();
+}
+
+__device__ __forceinline__ bool pair_gt(uint32_t ka, int ia, uint32_t kb, int ib) {
+  return ka > kb || (ka == kb && ia > ib);
+}
+
+// Ascending (key, id) bitonic sort of P (power of two) entries in shared memory.
+__device__ void bitonic_sort(uint32_t* key, int* id, int P) {
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += kST) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool asc = (i & k) == 0;
+          const uint32_t ka = key[i], kb = key[ixj];
+          const int ia = id[i], ib = id[ixj];
+          if (pair_gt(ka, ia, kb, ib) == asc) {
+            key[i] = kb; key[ixj] = ka;
+            id[i] = ib; id[ixj] = ia;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Warp 0: first index j < L at which the running sum of w(j) reaches target
+// (L if never). w must be cheap and deterministic.
+template <class W>
+__device__ int warp_find_cross(int L, unsigned long long target, W w, unsigned long long* total_out) {
+  const int lane = threadIdx.x & 31;
+  const int chunk = (L + 31) / 32;
+  const int a = min(lane * chunk, L), b = min(a + chunk, L);
+  unsigned long long loc = 0;
+  for (int j = a; j < b; ++j) loc += w(j);
+  unsigned long long incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const unsigned long long total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (total_out) *total_out = total;
+  int found = L;
+  unsigned long long cum = incl - loc;
+  if (cum < target && target <= incl) {
+    for (int j = a; j < b; ++j) {
+      cum += w(j);
+      if (cum >= target) { found = j; break; }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) found = min(found, __shfl_xor_sync(0xFFFFFFFFu, found, o));
+  return found;
+}
+
+// Candidate path for a sampled row whose zs holds transformed logits and
+// whose global max is mx. Returns false (nothing decided) when the cut is not
+// guaranteed to lie inside the exact part of the union.
+__device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int V, const RowParams& p, float mx,
+                                    CandBufs& cb, TDesc& d) {
+  SampleSmem* sm = c.sm;
+  const int k = (p.top_k > 0 && p.top_k < V) ? p.top_k : 0;
+  if (k == 0 && !(p.top_p > 0.f && p.top_p < 1.f) && !(p.min_p > 0.f)) return false;  // nothing to cut
+  const int C = k > 0 ? k : kCandTopP;
+  uint32_t K;
+  int cut;
+  local_select(sm, zs, n, v0, C, K, cut);
+  if (threadIdx.x == 0) sm->ccount = 0;
+  __syncthreads();
+  unsigned long long sall = 0;
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const uint32_t key = desc_key(zs[j]);
+    if (in_prefix(key, v0 + j, K, cut)) {
+      const int pos = atomicAdd(&sm->ccount, 1);
+      cb.ckey[pos] = key;
+      cb.cid[pos] = v0 + j;
+    }
+    if (k == 0) sall += to_fix(expf(zs[j] - mx));
+  }
+  sall = block_sum_u64(sall, sm->wsum);
+  if (threadIdx.x == 0) {
+    sm->mail[c.ph].u[0] = (unsigned long long)sm->ccount;
+    sm->mail[c.ph].u[1] = sall;
+    sm->mail[c.ph].i[0] = n > C ? 1 : 0;
+  }
+  Mail* m = c.publish();
+  int off[kClusterCTAs + 1];
+  off[0] = 0;
+  unsigned long long S_all = 0;
+  bool truncated = false;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    Mail* x = c.remote(m, r);
+    off[r + 1] = off[r] + (int)x->u[0];
+    S_all += x->u[1];
+    truncated |= x->i[0] != 0;
+  }
+  const int L = off[kClusterCTAs];
+  for (int t = threadIdx.x; t < cb.P; t += kST) {
+    if (t < L) {
+      int r = 0;
+      while (t >= off[r + 1]) ++r;
+      cb.mkey[t] = c.cl.map_shared_rank(cb.ckey, r)[t - off[r]];
+      cb.mid[t] = c.cl.map_shared_rank(cb.cid, r)[t - off[r]];
+    } else {
+      cb.mkey[t] = 0xFFFFFFFFu;
+      cb.mid[t] = 0x7FFFFFFF;
+    }
+  }
+  __syncthreads();
+  bitonic_sort(cb.mkey, cb.mid, cb.P);
+  if (threadIdx.x < 32) {
+    auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
+    const int Kk = k > 0 ? min(k, L) : L;
+    unsigned long long SE = 0;
+    if (k > 0) {
+      warp_find_cross(Kk, ~0ull, fx, &SE);
+    } else {
+      SE = S_all;
+    }
+    int Kf = Kk;
+    bool reached = true;
+    if (p.top_p > 0.f && p.top_p < 1.f) {
+      const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+      const int j = warp_find_cross(Kk, target, fx, nullptr);
+      if (j < Kk) Kf = min(Kf, j + 1);
+      else reached = false;
+    }
+    if (p.min_p > 0.f) {
+      const int lane = threadIdx.x;
+      int first = Kk;
+      for (int j = lane; j < Kk; j += 32)
+        if (!(expf(key_to_z(cb.mkey[j]) - mx) >= p.min_p)) { first = j; break; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
+      if (first < Kf) { Kf = first; reached = true; }
+    }
+    if (Kf < 1) Kf = 1;
+    bool valid;
+    if (k > 0) valid = true;
+    else if (!truncated) valid = true;  // the union holds every element
+    else valid = reached && Kf < C;
+    unsigned long long Sf = 0;
+    warp_find_cross(Kf, ~0ull, fx, &Sf);
+    if (threadIdx.x == 0) {
+      sm->fin_kf = Kf;
+      sm->fin_valid = valid ? 1 : 0;
+      sm->fin_sf = Sf;
+    }
+  }
+  __syncthreads();
+  if (!sm->fin_valid) return false;
+  const int Kf = sm->fin_kf;
+  d.k_key = 0xFFFFFFFFu;
+  d.k_cut = 0x7FFFFFFF;
+  if (Kf >= L && !truncated) {  // nothing cut
+    d.p_key = 0xFFFFFFFFu;
+    d.p_cut = 0x7FFFFFFF;
+  } else {
+    d.p_key = cb.mkey[Kf - 1];
+    d.p_cut = cb.mid[Kf - 1];
+  }
+  d.m = mx;
+  d.S = (float)((double)sm->fin_sf / kFix);
+  d.kept = Kf;
+  __syncthreads();
+  return true;
+}
+
+// Inverse-CDF draw over the first Kf sorted candidates, in ascending id order,
+// with weights to_fix(exp(z - m) / S) -- the q values the draft writes.
+__device__ int candidate_draw(const TDesc& d, CandBufs& cb, float u, SampleSmem* sm) {
+  const int Kf = d.kept;
+  for (int j = threadIdx.x; j < Kf; j += kST) {
+    const int id = cb.mid[j];
+    int rank = 0;
+    for (int i = 0; i < Kf; ++i) rank += cb.mid[i] < id;
+    cb.sid[rank] = id;
+    cb.sw[rank] = to_fix(expf(key_to_z(cb.mkey[j]) - d.m) / d.S);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned long long tot = 0;
+    warp_find_cross(Kf, ~0ull, [&](int j) { return cb.sw[j]; }, &tot);
+    int pick = -1;
+    if (tot > 0) {
+      const unsigned long long target = (unsigned long long)floor((double)u * (double)tot) + 1ull;
+      const int j = warp_find_cross(Kf, target, [&](int j) { return cb.sw[j]; }, nullptr);
+      pick = j < Kf ? cb.sid[j] : cb.sid[Kf - 1];
+    }
+    if (threadIdx.x == 0) sm->fin_draw = pick;
+  }
+  __syncthreads();
+  return sm->fin_draw;
+}
+
 // Transform one row of logits in the cluster. On return zs holds the
 // transformed logits (penalised, then / T) and `d` the descriptor; greedy rows
 // only get d.argmax.
-__device__ void transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
-                              const RowParams& p, TDesc& d, int32_t* status) {
+__device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
+                              const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb) {
   SampleSmem* sm = c.sm;
   for (int j = threadIdx.x; j < n; j += kST) zs[j] = lg[v0 + j];
   build_bitmap(sm, bits, v0, n);
@@ -416,12 +749,13 @@ __device__ void transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   d.m = 0.f;
   d.S = 1.f;
   d.kept = 1;
-  if (p.greedy) return;
+  if (p.greedy) return false;
 
   for (int j = threadIdx.x; j < n; j += kST) zs[j] = zs[j] / p.temperature + 0.0f;
   __syncthreads();
   d.m = gv / p.temperature + 0.0f;
   const float mx = d.m;
+  if (candidate_transform(c, zs, v0, n, V, p, mx, cb, d)) return true;
 
   if (p.top_k > 0 && p.top_k < V) {
     uint32_t K;
@@ -477,6 +811,7 @@ __device__ void transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   for (int r = 0; r < kClusterCTAs; ++r) { S += c.remote(m, r)->u[0]; K += c.remote(m, r)->u[1]; }
   d.S = (float)((double)S / kFix);
   d.kept = (int)K;
+  return false;
 }
 
 // Evaluate the transformed distribution at v from the raw logit.
@@ -513,6 +848,15 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
   const int per = (a.V + kClusterCTAs - 1) / kClusterCTAs;
   float* zs = reinterpret_cast<float*>(dyn + sizeof(SampleSmem));
   uint32_t* bits = reinterpret_cast<uint32_t*>(zs + per);
+  CandBufs cb;
+  cb.C = a.cand;
+  cb.P = a.merge;
+  cb.ckey = reinterpret_cast<uint32_t*>((reinterpret_cast<uintptr_t>(bits + (per + 31) / 32) + 15) & ~uintptr_t(15));
+  cb.cid = reinterpret_cast<int*>(cb.ckey + cb.C);
+  cb.mkey = reinterpret_cast<uint32_t*>(cb.cid + cb.C);
+  cb.mid = reinterpret_cast<int*>(cb.mkey + cb.P);
+  cb.sid = cb.mid + cb.P;
+  cb.sw = reinterpret_cast<unsigned long long*>(cb.sid + cb.C + (cb.C & 1));
 
   int r, i;
   const float* lg;
@@ -528,7 +872,7 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
   const RowParams p = a.p[r];
   load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, i);
   TDesc d;
-  transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status);
+  const bool fast = transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status, cb);
 
   if (a.mode == 1) {
     if (c.rank == 0 && threadIdx.x == 0) a.desc[task] = d;
@@ -549,7 +893,7 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
     }
     __syncthreads();
     const float u = a.u[(size_t)r * a.depth + i];
-    const int x = cluster_draw(c, n, v0, [&](int j) { return to_fix(zs[j]); }, u);
+    const int x = fast ? candidate_draw(d, cb, u, sm) : cluster_draw(c, n, v0, [&](int j) { return to_fix(zs[j]); }, u);
     if (c.rank == 0 && threadIdx.x == 0) a.draft_out[(size_t)r * a.depth + i] = x >= 0 ? x : d.argmax;
   }
   c.cl.sync();  // keep shared memory alive until every remote read is done
@@ -631,14 +975,15 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
   c.cl.sync();
 }
 
-static int sample_smem(int V) {
+static int sample_smem(int V, int C = 0, int P = 0) {
   const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
-  return (int)(sizeof(SampleSmem) + sizeof(float) * per + sizeof(uint32_t) * ((per + 31) / 32) + 16);
+  const size_t cand = 16 + (size_t)C * 8 + (size_t)P * 8 + (size_t)C * 4 + 4 + (size_t)C * 8;
+  return (int)(sizeof(SampleSmem) + sizeof(float) * per + sizeof(uint32_t) * ((per + 31) / 32) + cand + 32);
 }
 
 template <class Args>
-static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cudaStream_t s) {
-  const int smem = sample_smem(V);
+static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cudaStream_t s, int C = 0, int P = 0) {
+  const int smem = sample_smem(V, C, P);
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tasks * kClusterCTAs);
@@ -658,9 +1003,20 @@ static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cud
   count_launch();
 }
 
-void launch_sample(const SampleArgs& a, cudaStream_t s) {
+void launch_sample(const SampleArgs& a0, cudaStream_t s) {
+  SampleArgs a = a0;
+  int C = 1;
+  for (int r = 0; r < a.rows; ++r) {
+    if (a.p[r].greedy) continue;
+    const int c = (a.p[r].top_k > 0 && a.p[r].top_k < a.V) ? a.p[r].top_k : kCandTopP;
+    C = c > C ? c : C;
+  }
+  int P = 1;
+  while (P < kClusterCTAs * C) P <<= 1;
+  a.cand = C;
+  a.merge = P;
   const int tasks = a.mode == 0 ? a.rows : a.rows * (a.depth + 1);
-  launch_cluster(k_sample, a, tasks, a.V, s);
+  launch_cluster(k_sample, a, tasks, a.V, s, C, P);
 }
 
 void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verify, a, a.rows, a.V, s); }
