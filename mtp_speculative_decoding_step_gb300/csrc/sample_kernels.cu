@@ -408,33 +408,16 @@ __device__ __forceinline__ float key_to_z(uint32_t K) {
 }
 
 // Exactly min(C, n) local elements satisfy in_prefix(key, v0 + j, K, cut).
-__device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int C, uint32_t& Kout, int& cut) {
+// kmin / kmax: the range of the block's keys (from the staging pass).
+__device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int C, uint32_t kmin, uint32_t kmax,
+                             uint32_t& Kout, int& cut) {
   if (n <= C) { Kout = 0xFFFFFFFFu; cut = 0x7FFFFFFF; return; }
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int j = threadIdx.x; j < n; j += kST) {
-    const uint32_t k = desc_key(zs[j]);
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
-  }
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
-  __syncthreads();
-  kmin = 0xFFFFFFFFu;
-  kmax = 0u;
-  for (int w = 0; w < kST / 32; ++w) {
-    kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
-    kmax = max(kmax, (uint32_t)sm->wsum[w]);
-  }
   const uint32_t diff = kmin ^ kmax;
   int hi = diff ? 31 - __clz(diff) : -1;
   uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
   uint32_t prefix = kmin & mask;
   unsigned long long target = (unsigned long long)C;
+  unsigned long long ties = (unsigned long long)n;  // all keys equal when hi < 0
   unsigned long long* h = sm->hist[0];
   while (hi >= 0) {
     const int lo = hi >= 7 ? hi - 7 : 0;
@@ -468,6 +451,7 @@ __device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int
           if (cum < target && target <= cum + t) {
             sm->sel_bin = lane * 8 + b;
             sm->sel_rem = target - cum;
+            sm->fin_sf = t;  // elements in the chosen bin
             break;
           }
           cum += t;
@@ -478,15 +462,12 @@ __device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int
     prefix |= (uint32_t)sm->sel_bin << lo;
     mask |= dmask << lo;
     target = sm->sel_rem;
+    if (lo == 0) ties = sm->fin_sf;  // the last digit resolves the key: its bin holds the ties
     hi = lo - 1;
   }
   Kout = prefix;
   // ties at K: keep the first `target` of them in index order
-  unsigned long long ties = 0;
-  for (int j = threadIdx.x; j < n; j += kST)
-    if (desc_key(zs[j]) == prefix) ++ties;
-  ties = block_sum_u64(ties, sm->wsum);
-  if (target >= ties) { cut = 0x7FFFFFFF; return; }
+  if (target >= ties) { cut = 0x7FFFFFFF; __syncthreads(); return; }
   unsigned long long need = target;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x == 0) sm->found = 0x7FFFFFFF;
@@ -572,14 +553,14 @@ __device__ int warp_find_cross(int L, unsigned long long target, W w, unsigned l
 // whose global max is mx. Returns false (nothing decided) when the cut is not
 // guaranteed to lie inside the exact part of the union.
 __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int V, const RowParams& p, float mx,
-                                    CandBufs& cb, TDesc& d) {
+                                    uint32_t kmin, uint32_t kmax, CandBufs& cb, TDesc& d) {
   SampleSmem* sm = c.sm;
   const int k = (p.top_k > 0 && p.top_k < V) ? p.top_k : 0;
   if (k == 0 && !(p.top_p > 0.f && p.top_p < 1.f) && !(p.min_p > 0.f)) return false;  // nothing to cut
   const int C = k > 0 ? k : kCandTopP;
   uint32_t K;
   int cut;
-  local_select(sm, zs, n, v0, C, K, cut);
+  local_select(sm, zs, n, v0, C, kmin, kmax, K, cut);
   if (threadIdx.x == 0) sm->ccount = 0;
   __syncthreads();
   unsigned long long sall = 0;
@@ -714,25 +695,60 @@ __device__ int candidate_draw(const TDesc& d, CandBufs& cb, float u, SampleSmem*
 __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
                               const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb) {
   SampleSmem* sm = c.sm;
-  for (int j = threadIdx.x; j < n; j += kST) zs[j] = lg[v0 + j];
   build_bitmap(sm, bits, v0, n);
-  if (p.rep_penalty != 1.f)
-    for (int j = threadIdx.x; j < n; j += kST)
-      if (bit(bits, j)) zs[j] = penalize(zs[j], p.rep_penalty);
-  __syncthreads();
-  // argmax of the penalised logits
+  // one pass: stage, repetition penalty, argmax of the penalised logits,
+  // temperature, and the range of the transformed keys
+  const bool pen = p.rep_penalty != 1.f;
+  const bool smp = !p.greedy;
   float bv = -INFINITY;
   int bi = 0x7FFFFFFF;
   bool bad = false;
-  for (int j = threadIdx.x; j < n; j += kST) {
-    const float z = zs[j];
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  auto one = [&](int j, float z) {
+    if (pen && bit(bits, j)) z = penalize(z, p.rep_penalty);
     if (!isfinite(z)) bad = true;
     if (better(z, v0 + j, bv, bi)) { bv = z; bi = v0 + j; }
+    if (smp) {
+      z = z / p.temperature + 0.0f;
+      const uint32_t k = desc_key(z);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+    zs[j] = z;
+  };
+  if ((v0 & 3) == 0 && (n & 3) == 0) {
+    const float4* l4 = reinterpret_cast<const float4*>(lg + v0);
+#pragma unroll 4
+    for (int j4 = threadIdx.x; j4 < n / 4; j4 += kST) {
+      const float4 x = __ldg(l4 + j4);
+      one(4 * j4, x.x);
+      one(4 * j4 + 1, x.y);
+      one(4 * j4 + 2, x.z);
+      one(4 * j4 + 3, x.w);
+    }
+  } else {
+    for (int j = threadIdx.x; j < n; j += kST) one(j, lg[v0 + j]);
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(status, MTP_ERR_NONFINITE);
   __shared__ float sv[kST / 32];
   __shared__ int si[kST / 32];
   block_argmax(bv, bi, sv, si);
+  if (smp) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+    }
+    if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+    __syncthreads();
+    kmin = 0xFFFFFFFFu;
+    kmax = 0u;
+    for (int w = 0; w < kST / 32; ++w) {
+      kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
+      kmax = max(kmax, (uint32_t)sm->wsum[w]);
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) { sm->mail[c.ph].f[0] = bv; sm->mail[c.ph].i[0] = bi; }
   Mail* m = c.publish();
   float gv = -INFINITY;
@@ -751,11 +767,9 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   d.kept = 1;
   if (p.greedy) return false;
 
-  for (int j = threadIdx.x; j < n; j += kST) zs[j] = zs[j] / p.temperature + 0.0f;
-  __syncthreads();
   d.m = gv / p.temperature + 0.0f;
   const float mx = d.m;
-  if (candidate_transform(c, zs, v0, n, V, p, mx, cb, d)) return true;
+  if (candidate_transform(c, zs, v0, n, V, p, mx, kmin, kmax, cb, d)) return true;
 
   if (p.top_k > 0 && p.top_k < V) {
     uint32_t K;
