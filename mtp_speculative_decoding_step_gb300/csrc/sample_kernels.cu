@@ -365,11 +365,9 @@ __device__ void load_window(SampleSmem* sm, const int32_t* hist, int W, const in
 __device__ void build_bitmap(SampleSmem* sm, uint32_t* bits, int v0, int n) {
   for (int w = threadIdx.x; w < (n + 31) / 32; w += kST) bits[w] = 0u;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int t = 0; t < sm->nwin; ++t) {
-      const int v = sm->wtok[t] - v0;
-      if (v >= 0 && v < n) bits[v >> 5] |= 1u << (v & 31);
-    }
+  for (int t = threadIdx.x; t < sm->nwin; t += kST) {
+    const int v = sm->wtok[t] - v0;
+    if (v >= 0 && v < n) atomicOr(&bits[v >> 5], 1u << (v & 31));
   }
   __syncthreads();
 }
@@ -429,6 +427,7 @@ __device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int
       const int j = base + threadIdx.x;
       const uint32_t k = j < n ? desc_key(zs[j]) : 0u;
       const bool act = j < n && (k & mask) == prefix;
+      if (!__any_sync(0xFFFFFFFFu, act)) continue;
       const uint32_t bin = act ? ((k >> lo) & dmask) : 0xFFFFFFFFu;
       const unsigned peers = __match_any_sync(0xFFFFFFFFu, bin);
       if (act && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (unsigned long long)__popc(peers));
@@ -492,6 +491,64 @@ __device__ void local_select(SampleSmem* sm, const float* zs, int n, int v0, int
   }
   cut = sm->found;
   __syncthreads();
+}
+
+// Local candidates in one histogram pass: bins are 256 equal slices of the
+// block's value range [zmin, zmax] (bin 0 holds the largest); bin index is
+// weakly monotone in z, so every bin is a contiguous range of the (key, id)
+// order. All elements of the bins up to and including the one holding the
+// C-th largest are written out -- a superset of the local top-C. Returns the
+// count, or -1 if it would exceed cap (the caller then selects exactly).
+__device__ int local_candidates(SampleSmem* sm, const float* zs, int n, int v0, int C, int cap, uint32_t kmin,
+                                uint32_t kmax, uint32_t* ckey, int* cid) {
+  const float zmax = key_to_z(kmin), zmin = key_to_z(kmax);
+  const float span = zmax - zmin;
+  const float scale = span > 0.f ? 255.99f / span : 0.f;
+  unsigned int* h = reinterpret_cast<unsigned int*>(sm->hist[0]);
+  for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0u;
+  if (threadIdx.x == 0) sm->ccount = 0;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const int b = min(255, (int)((zmax - zs[j]) * scale));
+    atomicAdd(&h[b], 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    unsigned int s8 = 0;
+    for (int b = 0; b < 8; ++b) s8 += h[lane * 8 + b];
+    unsigned int incl = s8;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned int cum = incl - s8;
+    if (cum < (unsigned)C && (unsigned)C <= incl) {
+      for (int b = 0; b < 8; ++b) {
+        cum += h[lane * 8 + b];
+        if (cum >= (unsigned)C) {
+          sm->sel_bin = lane * 8 + b;
+          sm->fin_draw = (int)cum;  // elements in bins <= sel_bin
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int B = sm->sel_bin, total = sm->fin_draw;
+  __syncthreads();
+  if (total > cap) return -1;
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const int b = min(255, (int)((zmax - zs[j]) * scale));
+    if (b <= B) {
+      const int pos = atomicAdd(&sm->ccount, 1);
+      ckey[pos] = desc_key(zs[j]);
+      cid[pos] = v0 + j;
+    }
+  }
+  __syncthreads();
+  return sm->ccount;
 }
 
 __device__ __forceinline__ bool pair_gt(uint32_t ka, int ia, uint32_t kb, int ib) {
@@ -558,26 +615,31 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
   const int k = (p.top_k > 0 && p.top_k < V) ? p.top_k : 0;
   if (k == 0 && !(p.top_p > 0.f && p.top_p < 1.f) && !(p.min_p > 0.f)) return false;  // nothing to cut
   const int C = k > 0 ? k : kCandTopP;
-  uint32_t K;
-  int cut;
-  local_select(sm, zs, n, v0, C, kmin, kmax, K, cut);
-  if (threadIdx.x == 0) sm->ccount = 0;
-  __syncthreads();
-  unsigned long long sall = 0;
-  for (int j = threadIdx.x; j < n; j += kST) {
-    const uint32_t key = desc_key(zs[j]);
-    if (in_prefix(key, v0 + j, K, cut)) {
-      const int pos = atomicAdd(&sm->ccount, 1);
-      cb.ckey[pos] = key;
-      cb.cid[pos] = v0 + j;
+  int got = n <= cb.C ? -1 : local_candidates(sm, zs, n, v0, C, cb.C, kmin, kmax, cb.ckey, cb.cid);
+  if (got < 0) {  // few elements, or a flat slice: select exactly min(C, n)
+    uint32_t K;
+    int cut;
+    local_select(sm, zs, n, v0, min(C, cb.C), kmin, kmax, K, cut);
+    if (threadIdx.x == 0) sm->ccount = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += kST) {
+      const uint32_t key = desc_key(zs[j]);
+      if (in_prefix(key, v0 + j, K, cut)) {
+        const int pos = atomicAdd(&sm->ccount, 1);
+        cb.ckey[pos] = key;
+        cb.cid[pos] = v0 + j;
+      }
     }
-    if (k == 0) sall += to_fix(expf(zs[j] - mx));
+    __syncthreads();
   }
+  unsigned long long sall = 0;
+  if (k == 0)
+    for (int j = threadIdx.x; j < n; j += kST) sall += to_fix(expf(zs[j] - mx));
   sall = block_sum_u64(sall, sm->wsum);
   if (threadIdx.x == 0) {
     sm->mail[c.ph].u[0] = (unsigned long long)sm->ccount;
     sm->mail[c.ph].u[1] = sall;
-    sm->mail[c.ph].i[0] = n > C ? 1 : 0;
+    sm->mail[c.ph].i[0] = sm->ccount < n ? 1 : 0;
   }
   Mail* m = c.publish();
   int off[kClusterCTAs + 1];
@@ -591,7 +653,9 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     truncated |= x->i[0] != 0;
   }
   const int L = off[kClusterCTAs];
-  for (int t = threadIdx.x; t < cb.P; t += kST) {
+  int Pd = 1;
+  while (Pd < L) Pd <<= 1;
+  for (int t = threadIdx.x; t < Pd; t += kST) {
     if (t < L) {
       int r = 0;
       while (t >= off[r + 1]) ++r;
@@ -603,7 +667,7 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
   }
   __syncthreads();
-  bitonic_sort(cb.mkey, cb.mid, cb.P);
+  bitonic_sort(cb.mkey, cb.mid, Pd);
   if (threadIdx.x < 32) {
     auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
     const int Kk = k > 0 ? min(k, L) : L;
@@ -1025,6 +1089,7 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
     const int c = (a.p[r].top_k > 0 && a.p[r].top_k < a.V) ? a.p[r].top_k : kCandTopP;
     C = c > C ? c : C;
   }
+  C = C * 4 < (C > 1024 ? C : 1024) ? C * 4 : (C > 1024 ? C : 1024);  // room for the value-binned superset
   int P = 1;
   while (P < kClusterCTAs * C) P <<= 1;
   a.cand = C;
