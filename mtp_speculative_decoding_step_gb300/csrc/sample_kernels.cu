@@ -316,32 +316,34 @@ __device__ int cluster_draw(Clu& c, int n_local, int v0, Wt weight, float u) {
   }
   int pick = -1;
   if (c.rank == owner) {
-    unsigned long long need = target - before;
+    const unsigned long long need = target - before;
+    const int per_t = (n_local + kST - 1) / kST;
+    const int a0 = min(threadIdx.x * per_t, n_local), a1 = min(a0 + per_t, n_local);
+    unsigned long long loc2 = 0;
+    for (int j = a0; j < a1; ++j) loc2 += weight(j);
+    // exclusive block scan of the per-thread sums
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    if (threadIdx.x == 0) sm->found = -1;
-    for (int base = 0; base < n_local; base += kST) {
-      const int j = base + threadIdx.x;
-      const unsigned long long x = j < n_local ? weight(j) : 0ull;
-      unsigned long long incl = x;
+    unsigned long long incl = loc2;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      __syncthreads();
-      if (lane == 31) sm->wsum[w] = incl;
-      __syncthreads();
-      unsigned long long wbefore = 0, chunk = 0;
-      for (int k = 0; k < kST / 32; ++k) {
-        if (k < w) wbefore += sm->wsum[k];
-        chunk += sm->wsum[k];
-      }
-      incl += wbefore;
-      if (x > 0 && incl >= need && incl - x < need) sm->found = v0 + j;
-      __syncthreads();
-      if (chunk >= need) break;
-      need -= chunk;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
     }
+    if (threadIdx.x == 0) sm->found = -1;
+    __syncthreads();
+    if (lane == 31) sm->wsum[w] = incl;
+    __syncthreads();
+    unsigned long long wbefore = 0;
+    for (int k = 0; k < w; ++k) wbefore += sm->wsum[k];
+    unsigned long long cum = wbefore + incl - loc2;
+    if (cum < need && need <= cum + loc2) {
+      for (int j = a0; j < a1; ++j) {
+        const unsigned long long x = weight(j);
+        cum += x;
+        if (x > 0 && cum >= need) { sm->found = v0 + j; break; }
+      }
+    }
+    __syncthreads();
     pick = sm->found;
   }
   if (threadIdx.x == 0) sm->mail[c.ph].i[0] = pick;
@@ -667,7 +669,31 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
   }
   __syncthreads();
-  bitonic_sort(cb.mkey, cb.mid, Pd);
+  if (L <= 1024) {
+    // rank sort: every entry's position is its count of smaller (key, id)
+    // pairs; ids are distinct, so positions are a permutation of 0..L-1
+    uint32_t rk[2];
+    int ri[2], pos[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = threadIdx.x + u * kST;
+      pos[u] = -1;
+      if (t < L) {
+        rk[u] = cb.mkey[t];
+        ri[u] = cb.mid[t];
+        int cnt = 0;
+        for (int q = 0; q < L; ++q) cnt += pair_gt(rk[u], ri[u], cb.mkey[q], cb.mid[q]);
+        pos[u] = cnt;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (pos[u] >= 0) { cb.mkey[pos[u]] = rk[u]; cb.mid[pos[u]] = ri[u]; }
+    __syncthreads();
+  } else {
+    bitonic_sort(cb.mkey, cb.mid, Pd);
+  }
   if (threadIdx.x < 32) {
     auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
     const int Kk = k > 0 ? min(k, L) : L;
@@ -782,13 +808,24 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   };
   if ((v0 & 3) == 0 && (n & 3) == 0) {
     const float4* l4 = reinterpret_cast<const float4*>(lg + v0);
-#pragma unroll 4
-    for (int j4 = threadIdx.x; j4 < n / 4; j4 += kST) {
-      const float4 x = __ldg(l4 + j4);
-      one(4 * j4, x.x);
-      one(4 * j4 + 1, x.y);
-      one(4 * j4 + 2, x.z);
-      one(4 * j4 + 3, x.w);
+    const int n4 = n / 4;
+    for (int b0 = 0; b0 < n4; b0 += 8 * kST) {  // all of a batch's loads in flight first
+      float4 xb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j4 = b0 + u * kST + threadIdx.x;
+        if (j4 < n4) xb[u] = __ldg(l4 + j4);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j4 = b0 + u * kST + threadIdx.x;
+        if (j4 < n4) {
+          one(4 * j4, xb[u].x);
+          one(4 * j4 + 1, xb[u].y);
+          one(4 * j4 + 2, xb[u].z);
+          one(4 * j4 + 3, xb[u].w);
+        }
+      }
     }
   } else {
     for (int j = threadIdx.x; j < n; j += kST) one(j, lg[v0 + j]);
@@ -1025,18 +1062,42 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
     build_bitmap(sm, bits, v0, n);
     const TDesc dn = desc[nacc];
     const float* ln = lg + (size_t)nacc * a.V;
+    const float* qn = nacc < d ? a.q + ((size_t)r * d + nacc) * a.V : nullptr;
+    float* ws = reinterpret_cast<float*>(dyn + sizeof(SampleSmem));
+    // draw weights of this slice, computed once: the residual max(p - q, 0)
+    // after a rejection, else p (the bonus row)
+    auto stage = [&](bool residual) {
+      for (int b0 = 0; b0 < n; b0 += 8 * kST) {
+        float lv[8], qv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = b0 + u * kST + threadIdx.x;
+          if (j < n) {
+            lv[u] = __ldg(ln + v0 + j);
+            qv[u] = residual ? __ldg(qn + v0 + j) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = b0 + u * kST + threadIdx.x;
+          if (j < n) {
+            const float pv = eval_p(dn, p, lv[u], bit(bits, j), v0 + j);
+            const float rv = residual ? pv - qv[u] : pv;
+            ws[j] = rv > 0.f ? rv : 0.f;
+          }
+        }
+      }
+      __syncthreads();
+    };
     y = -1;
     if (nacc < d) {
-      const float* qn = a.q + ((size_t)r * d + nacc) * a.V;
-      y = cluster_draw(c, n, v0, [&](int j) {
-        const float pv = eval_p(dn, p, ln[v0 + j], bit(bits, j), v0 + j);
-        const float rv = pv - qn[v0 + j];
-        return to_fix(rv > 0.f ? rv : 0.f);
-      }, uu[d]);
+      stage(true);
+      y = cluster_draw(c, n, v0, [&](int j) { return to_fix(ws[j]); }, uu[d]);
     }
-    if (y < 0)
-      y = cluster_draw(c, n, v0, [&](int j) { return to_fix(eval_p(dn, p, ln[v0 + j], bit(bits, j), v0 + j)); },
-                       uu[d]);
+    if (y < 0) {
+      stage(false);
+      y = cluster_draw(c, n, v0, [&](int j) { return to_fix(ws[j]); }, uu[d]);
+    }
     if (y < 0) y = dn.argmax;
   }
   if (c.rank == 0 && threadIdx.x == 0) {
