@@ -91,14 +91,17 @@ struct TcGemmArgs {
   int32_t* status;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int MH>
 __global__ void __launch_bounds__(128, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
               const __grid_constant__ CUtensorMap tb1, const TcGemmArgs a) {
-  constexpr uint32_t kABytes = kTileM * kTileK * 2;
+  // MH row halves of 128 per CTA share every B tile; accumulator h lives in
+  // TMEM columns [h*BN, (h+1)*BN).
+  constexpr uint32_t kABytes = MH * kTileM * kTileK * 2;
   constexpr uint32_t kBBytes = BN * kTileK * 2;
   constexpr uint32_t kStage = kABytes + kBBytes;
-  constexpr uint32_t kTmemCols = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  constexpr uint32_t kCols = MH * BN;
+  constexpr uint32_t kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base + STAGES * kStage);
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(128, 1)
   int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kTileM, n0 = blockIdx.y * BN;
+  const int m0 = blockIdx.x * kTileM * MH, n0 = blockIdx.y * BN;
   const int nk_total = a.K / kTileK;
   const int per = (nk_total + a.ksplit - 1) / a.ksplit;
   const int kb = blockIdx.z * per;
@@ -157,7 +160,10 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t as = smem_u32(base + s * kStage), bs = as + kABytes;
 #pragma unroll
       for (int kk = 0; kk < kTileK / 16; ++kk)
-        mma_bf16(tmem, sdesc(as + kk * 32), sdesc(bs + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+          mma_bf16(tmem + (uint32_t)(h * BN), sdesc(as + h * kTileM * kTileK * 2 + kk * 32), sdesc(bs + kk * 32),
+                   idesc, (i > 0 || kk > 0) ? 1u : 0u);
       mma_commit(smem_u32(&empty[s]));
     }
     if (!ok) *s_fail = 1;
@@ -168,17 +174,20 @@ __global__ void __launch_bounds__(128, 1)
   // epilogue: TMEM lanes 32w..32w+31 hold rows m0 + 32w + lane
   const bool got = mbar_wait(smem_u32(accf), 0);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const int row = m0 + warp * 32 + lane;
-  float* drow = a.D + ((size_t)blockIdx.z * a.M + row) * a.ldd + n0;
   if (got) {
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-      if (row < a.M) {
-        float4* d4 = reinterpret_cast<float4*>(drow + c);
+    for (int h = 0; h < MH; ++h) {
+      const int row = m0 + h * kTileM + warp * 32 + lane;
+      float* drow = a.D + ((size_t)blockIdx.z * a.M + row) * a.ldd + n0;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(h * BN + c), v);
+        if (row < a.M) {
+          float4* d4 = reinterpret_cast<float4*>(drow + c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
       }
     }
   }
@@ -226,30 +235,31 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
 }
 
 // D[split][M][N] = A[M][K] . [B0; B1]^T  (B0 rows [0, n0rows), B1 the rest).
-template <int BN>
+template <int BN, int STAGES, int MH>
 static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int ksplit,
                       float* D, int32_t* status, cudaStream_t s) {
-  constexpr int STAGES = BN <= 128 ? 6 : 5;
   if (M < 1 || K % kTileK != 0 || N % BN != 0 || n0rows % BN != 0 || ksplit < 1) return false;
   CUtensorMap ta, tb0, tb1;
-  if (!make_map(&ta, A, M, K, kTileM)) return false;
+  if (!make_map(&ta, A, M, K, kTileM * MH)) return false;
   if (!make_map(&tb0, B0, n0rows, K, BN)) return false;
   if (!make_map(&tb1, B1 ? B1 : B0, B1 ? N - n0rows : n0rows, K, BN)) return false;
   TcGemmArgs a;
   a.M = M; a.N = N; a.K = K; a.n_split_b = n0rows; a.ksplit = ksplit; a.D = D; a.ldd = N; a.status = status;
-  const int smem = STAGES * (kTileM + BN) * kTileK * 2 + 1024 + 256;
-  auto k = k_tc_gemm<BN, STAGES>;
+  const int smem = STAGES * (kTileM * MH + BN) * kTileK * 2 + 1024 + 256;
+  auto k = k_tc_gemm<BN, STAGES, MH>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  dim3 grid((M + kTileM - 1) / kTileM, N / BN, ksplit);
+  dim3 grid((M + kTileM * MH - 1) / (kTileM * MH), N / BN, ksplit);
   k<<<grid, 128, smem, s>>>(ta, tb0, tb1, a);
   count_launch();
   return cudaGetLastError() == cudaSuccess;
 }
 
+// mh: 128-row halves per CTA (1 or 2); bn: 128 or 160.
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
-                    int ksplit, float* D, int32_t* status, cudaStream_t s) {
-  if (bn == 160) return tc_gemm_t<160>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
-  return tc_gemm_t<128>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh) {
+  if (mh == 2) return tc_gemm_t<128, 4, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+  if (bn == 160) return tc_gemm_t<160, 5, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+  return tc_gemm_t<128, 6, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
 }
 
 }  // namespace mtp

@@ -98,7 +98,7 @@ void launch_flush_norm(const float* part, int nsplit, long long split_stride, in
                        float eps, uint16_t* b, cudaStream_t s);
 // D[split][M][N] = A[M][K] . [B0; B1]^T on tcgen05 (bf16 in, fp32 out).
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
-                    int ksplit, float* D, int32_t* status, cudaStream_t s);
+                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh = 1);
 
 // Decode attention of the head items over slots 0..slot (split over chunks).
 struct AttnArgs {
