@@ -326,8 +326,13 @@ __device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int pos, 
 // grid (M, nq + nkv), block dh/2 threads: thread i owns the pair (i, i + dh/2).
 __device__ __forceinline__ float qkv_at(const QkvPostArgs& a, int m, int col) {
   const float* p = a.qkv + (size_t)m * a.ld + col;
-  float v = p[0];
-  for (int s = 1; s < a.nsplit; ++s) v += p[(size_t)s * a.split_stride];
+  if (a.nsplit == 1) return p[0];
+  float t[8];  // split-K partials (at most 8): all loads in flight, summed in split order
+#pragma unroll
+  for (int s = 0; s < 8; ++s) t[s] = s < a.nsplit ? p[(size_t)s * a.split_stride] : 0.f;
+  float v = t[0];
+#pragma unroll
+  for (int s = 1; s < 8; ++s) v += t[s];
   return v;
 }
 

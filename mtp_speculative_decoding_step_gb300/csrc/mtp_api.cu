@@ -408,7 +408,7 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
     launch_flush_x(x, mp, s);
     // more than 128 pairs: 256-row tiles share each weight tile (half the weight traffic per FLOP)
     const int mh = mp > 128 ? 2 : 1;
-    const int bn = mh == 2 ? 128 : (H % 160 == 0 ? 160 : 128);
+    const int bn = mh == 2 ? (H % 256 == 0 ? 256 : 128) : (H % 160 == 0 ? 160 : 128);
     const int ks = tc_splits((mp + 128 * mh - 1) / (128 * mh), H / bn, 2 * H / 64, h->sms, 8);
     if (!launch_tc_gemm(h->xb, mp, 2 * H, h->w[T_FC], H, nullptr, H, bn, ks, h->tcpart, h->status, s, mh))
       return MTP_ERR_CUDA;
