@@ -406,9 +406,10 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
       x.hid_item[m] = (int)(all.hid_off[m0 + m] / H);
     }
     launch_flush_x(x, mp, s);
-    // more than 128 pairs: 256-row tiles share each weight tile (half the weight traffic per FLOP)
-    const int mh = mp > 128 ? 2 : 1;
-    const int bn = mh == 2 ? (H % 256 == 0 ? 256 : 128) : (H % 160 == 0 ? 160 : 128);
+    // 128 x 160 tiles measured fastest on the 256-pair flush (the 256-row
+    // variants hold fewer pipeline stages and expose more TMA latency)
+    const int mh = 1;
+    const int bn = H % 160 == 0 ? 160 : 128;
     const int ks = tc_splits((mp + 128 * mh - 1) / (128 * mh), H / bn, 2 * H / 64, h->sms, 8);
     if (!launch_tc_gemm(h->xb, mp, 2 * H, h->w[T_FC], H, nullptr, H, bn, ks, h->tcpart, h->status, s, mh))
       return MTP_ERR_CUDA;
@@ -416,7 +417,7 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
   }
   {
     ProfScope ps(h, s, PK_FLUSH_KV);
-    const int mh = mp > 128 ? 2 : 1;
+    const int mh = 1;
     const int ks = tc_splits((mp + 128 * mh - 1) / (128 * mh), 2 * kw / 128, H / 64, h->sms, 8);
     if (!launch_tc_gemm(h->bb, mp, H, h->w[T_K], kw, h->w[T_V], 2 * kw, 128, ks, h->tcpart, h->status, s, mh))
       return MTP_ERR_CUDA;
