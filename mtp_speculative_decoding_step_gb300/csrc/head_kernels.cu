@@ -136,7 +136,7 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
 }
 
 template <typename WT, int MT>
-__global__ void __launch_bounds__(256, (MT == 1 ? 3 : 2)) k_gemv(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArgs a) {
   constexpr int VN = Vec<WT>::N;
   constexpr int RPW = MT <= 4 ? 8 : 4;
   constexpr int ROWS = 8 * RPW;
@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(256, (MT == 1 ? 3 : 2)) k_gemv(const __grid_co
 
   // The weights do not depend on the previous kernel: issue this warp's first
   // loads before waiting for it. Each lane keeps one 16-byte vector of each
-  // of its RPW rows in flight.
+  // of its RPW rows in flight; with one item the next vector set is issued
+  // before the current one is consumed (two sets in flight).
   const int nvec = KS / VN;
   int v0 = lane;
   bool has0 = v0 < nvec;
@@ -187,13 +188,34 @@ __global__ void __launch_bounds__(256, (MT == 1 ? 3 : 2)) k_gemv(const __grid_co
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
 
-  while (has0) {
-    gemv_fma<WT, MT, RPW>(acc, w0, xs, KS, v0 * VN);
-    v0 += 32;
-    has0 = v0 < nvec;
-    if (has0) {
+  if constexpr (MT == 1) {
+    uint4 w1[RPW];
+    while (has0) {
+      const bool has1 = v0 + 32 < nvec;
+      if (has1) {
 #pragma unroll
-      for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
+        for (int i = 0; i < RPW; ++i) w1[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
+      }
+      gemv_fma<WT, MT, RPW>(acc, w0, xs, KS, v0 * VN);
+      if (!has1) break;
+      v0 += 32;
+      has0 = v0 + 32 < nvec;
+      if (has0) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
+      }
+      gemv_fma<WT, MT, RPW>(acc, w1, xs, KS, v0 * VN);
+      v0 += 32;
+    }
+  } else {
+    while (has0) {
+      gemv_fma<WT, MT, RPW>(acc, w0, xs, KS, v0 * VN);
+      v0 += 32;
+      has0 = v0 < nvec;
+      if (has0) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)v0 * VN);
+      }
     }
   }
 

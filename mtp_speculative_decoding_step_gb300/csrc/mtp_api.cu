@@ -129,10 +129,11 @@ GemvPlan plan_gemv(int N, int K, int M, bool dual, int sms) {
   p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   const int rows = gemv_rows_per_group(p.mt);
   p.ngroups = N / rows;
-  // enough blocks for two per SM: one wave of long, HBM-bound blocks beats
-  // several waves of short ones with split-K tails
+  // at least one block per SM: every block keeps enough loads in flight to
+  // draw its share of HBM, so long blocks in one wave beat many short ones
+  // with split-K tails
   p.S = dual ? 2 : 1;
-  while (p.S < 8 && (long long)p.ngroups * p.S < 2LL * sms) p.S *= 2;
+  while (p.S < 8 && (long long)p.ngroups * p.S < (long long)sms) p.S *= 2;
   while (p.S < 8 && (long long)p.mt * (K / p.S) * 4 > 96 * 1024) p.S *= 2;
   p.smem = p.mt * (K / p.S) * 4;
   return p;
