@@ -99,40 +99,110 @@ __device__ __forceinline__ void gemv_fma(float (&acc)[RPW][MT], const uint4 (&w)
   }
 }
 
+// Block-reduce MT partial sums at once (one barrier round; 256 threads);
+// every thread gets all MT totals, each summed in a fixed order.
+template <int MT>
+__device__ __forceinline__ void block_sum_n(float (&v)[MT], float* red /* >= 8 * MT */) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 0; m < MT; ++m) v[m] = warp_sum(v[m]);
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int m = 0; m < MT; ++m) red[m * 8 + w] = v[m];
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += red[m * 8 + k];
+    v[m] = t;
+  }
+  __syncthreads();
+}
+
 // Stage x[m][k0 .. k0+KS) (fp32) into shared memory, applying the prologue.
+// All items are handled together: one pass for their sums of squares, one
+// barrier round, one staging pass.
 template <int MT>
 __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, float* red) {
+  const int tid = threadIdx.x;
   if (a.pro == PRO_DUAL) {
     // x = [norm_e(E[tok]) ; norm_h(hidden)]; this block's slice lies in one half.
     const int H = a.K / 2;
     const bool emb = k0 < H;
     const float* nw = emb ? a.nw : a.nw2;
     const int kk0 = emb ? k0 : k0 - H;
-    for (int m = 0; m < a.M; ++m) {
-      const void* src = emb ? a.E : a.hid;
-      const int dt = emb ? a.wdt : a.hid_dt;
-      int t = emb ? a.tok[a.tok_idx[m]] : 0;
-      if (t < 0 || t >= a.vocab) {  // a bad token id reads row 0 and raises the status word
-        if (threadIdx.x == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
-        t = 0;
+    const void* src = emb ? a.E : a.hid;
+    const int dt = emb ? a.wdt : a.hid_dt;
+    size_t base[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      base[m] = 0;
+      if (m < a.M) {
+        int t = emb ? a.tok[a.tok_idx[m]] : 0;
+        if (t < 0 || t >= a.vocab) {  // a bad token id reads row 0 and raises the status word
+          if (tid == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+          t = 0;
+        }
+        base[m] = emb ? (size_t)t * (size_t)H : (size_t)a.hid_off[m];
       }
-      const size_t base = emb ? (size_t)t * (size_t)H : (size_t)a.hid_off[m];
-      const float inv = rsqrtf(row_sumsq(src, dt, base, H, red) / (float)H + a.eps);
-      row_stage(xs + m * KS, src, dt, base + kk0, KS, inv, nw + kk0);
     }
+    float ss[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) ss[m] = 0.f;
+    if (dt == MTP_DTYPE_BF16) {
+      for (int i = tid; i < H / 8; i += blockDim.x) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < a.M) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base[m]) + i);
+            const float f[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                                bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss[m] = fmaf(f[j], f[j], ss[m]);
+          }
+        }
+      }
+    } else {
+      for (int i = tid; i < H / 4; i += blockDim.x) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < a.M) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base[m]) + i);
+            ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+          }
+        }
+      }
+    }
+    block_sum_n<MT>(ss, red);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      if (m < a.M) row_stage(xs + m * KS, src, dt, base[m] + kk0, KS, rsqrtf(ss[m] / (float)H + a.eps), nw + kk0);
+  } else if (a.pro == PRO_NORM) {
+    float ss[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) ss[m] = 0.f;
+    for (int i = tid; i < a.K / 4; i += blockDim.x) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < a.M) {
+          const float4 v = reinterpret_cast<const float4*>(a.x + (size_t)m * a.ldx)[i];
+          ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+        }
+      }
+    }
+    block_sum_n<MT>(ss, red);
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      if (m < a.M)
+        row_stage(xs + m * KS, a.x + (size_t)m * a.ldx, MTP_DTYPE_F32, k0, KS, rsqrtf(ss[m] / (float)a.K + a.eps),
+                  a.nw + k0);
   } else {
-    for (int m = 0; m < a.M; ++m) {
-      const float* xm = a.x + (size_t)m * a.ldx;
-      if (a.pro == PRO_NORM) {
-        const float inv = rsqrtf(row_sumsq(xm, MTP_DTYPE_F32, 0, a.K, red) / (float)a.K + a.eps);
-        row_stage(xs + m * KS, xm, MTP_DTYPE_F32, k0, KS, inv, a.nw + k0);
-      } else {
-        row_stage(xs + m * KS, xm, MTP_DTYPE_F32, k0, KS, 1.f, nullptr);
-      }
-    }
+    for (int m = 0; m < a.M; ++m)
+      row_stage(xs + m * KS, a.x + (size_t)m * a.ldx, MTP_DTYPE_F32, k0, KS, 1.f, nullptr);
   }
   for (int m = a.M; m < MT; ++m)
-    for (int k = threadIdx.x; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
+    for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
 }
 
 template <typename WT, int MT>
@@ -142,7 +212,7 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   constexpr int ROWS = 8 * RPW;
   extern __shared__ __align__(16) float xs[];
   __shared__ float s_out[MT][ROWS];
-  __shared__ float s_red[32];
+  __shared__ float s_red[8 * MT > 32 ? 8 * MT : 32];
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -392,57 +462,89 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
   }
 }
 
-// grid (M), block 256: x[m] = [norm_e(E[tok]) ; norm_h(hid)] rounded to bf16.
+// One block per (pair, half): half 0 = RMSNorm_e(E[tok]), half 1 =
+// RMSNorm_h(hidden), written as bf16 into the pair's row of x. Each thread
+// keeps its (at most two) 8-element vectors in registers between the sum of
+// squares and the store, so the source row is read once.
 __global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
   __shared__ float red[32];
-  const int m = blockIdx.x, H = a.H;
-  int t = a.tok[a.tok_idx[m]];
-  if (t < 0 || t >= a.vocab) {
-    if (threadIdx.x == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
-    t = 0;
+  const int m = blockIdx.x, half = blockIdx.y, H = a.H, nv = H / 8;
+  pdl_wait();
+  pdl_trigger();
+  size_t base;
+  if (half == 0) {
+    int t = a.tok[a.tok_idx[m]];
+    if (t < 0 || t >= a.vocab) {
+      if (threadIdx.x == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+      t = 0;
+    }
+    base = (size_t)t * H;
+  } else {
+    base = (size_t)a.hid_item[m] * H;
   }
-  uint16_t* x = a.x + (size_t)m * 2 * H;
-  for (int half = 0; half < 2; ++half) {
-    const void* src = half == 0 ? a.E : a.hid;
-    const int dt = half == 0 ? a.wdt : a.hid_dt;
-    const size_t base = half == 0 ? (size_t)t * H : (size_t)a.hid_item[m] * H;
-    const float* w = half == 0 ? a.nw_e : a.nw_h;
-    const float inv = rsqrtf(row_sumsq(src, dt, base, H, red) / (float)H + a.eps);
-    // 8 elements per thread step: one 16-byte store of bf16
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
-      float f[8];
+  const void* src = half == 0 ? a.E : a.hid;
+  const int dt = half == 0 ? a.wdt : a.hid_dt;
+  const float* w = half == 0 ? a.nw_e : a.nw_h;
+  float f[2][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    if (i < nv) {
       if (dt == MTP_DTYPE_BF16) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base) + i);
-        f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-        f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+        f[u][0] = bf16lo(v.x); f[u][1] = bf16hi(v.x); f[u][2] = bf16lo(v.y); f[u][3] = bf16hi(v.y);
+        f[u][4] = bf16lo(v.z); f[u][5] = bf16hi(v.z); f[u][6] = bf16lo(v.w); f[u][7] = bf16hi(v.w);
       } else {
         const float4* p4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base) + 2 * i;
-        const float4 u0 = p4[0], u1 = p4[1];
-        f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w; f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
+        const float4 u0 = __ldg(p4), u1 = __ldg(p4 + 1);
+        f[u][0] = u0.x; f[u][1] = u0.y; f[u][2] = u0.z; f[u][3] = u0.w;
+        f[u][4] = u1.x; f[u][5] = u1.y; f[u][6] = u1.z; f[u][7] = u1.w;
       }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(f[u][j], f[u][j], ss);
+    }
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / (float)H + a.eps);
+  uint16_t* x = a.x + (size_t)m * 2 * H + (size_t)half * H;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    if (i < nv) {
+      const float4 w0 = reinterpret_cast<const float4*>(w)[2 * i], w1 = reinterpret_cast<const float4*>(w)[2 * i + 1];
+      const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        o[j] = (uint32_t)f_to_bf16(f[2 * j] * inv * w[8 * i + 2 * j]) |
-               ((uint32_t)f_to_bf16(f[2 * j + 1] * inv * w[8 * i + 2 * j + 1]) << 16);
-      reinterpret_cast<uint4*>(x + half * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        o[j] = (uint32_t)f_to_bf16(f[u][2 * j] * inv * ww[2 * j]) |
+               ((uint32_t)f_to_bf16(f[u][2 * j + 1] * inv * ww[2 * j + 1]) << 16);
+      reinterpret_cast<uint4*>(x)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
 
+// Threads for a row of n vectors with at most `per` vectors per thread.
+static int row_threads(int n, int per) {
+  int t = (n + per - 1) / per;
+  t = (t + 31) / 32 * 32;
+  return t < 32 ? 32 : (t > 1024 ? 1024 : t);
+}
+
 void launch_flush_x(const FlushXArgs& a, int M, cudaStream_t s) {
-  k_flush_x<<<M, 256, 0, s>>>(a);
+  launch_pdl(k_flush_x, dim3(M, 2), dim3(row_threads(a.H / 8, 2)), 0, s, a);
   count_launch();
 }
 
+// b[m] = bf16(RMSNorm(sum of the split-K partials of row m) * w): one block per
+// row, each thread holding at most four float4 of the summed row in registers.
 __global__ void k_flush_norm(const float* part, int nsplit, long long split_stride, int H, const float* w,
                              float eps, uint16_t* b) {
   __shared__ float red[32];
-  const int m = blockIdx.x;
+  const int m = blockIdx.x, n4 = H / 4;
+  pdl_wait();
+  pdl_trigger();
   const float* p = part + (size_t)m * H;
-  // sum the split-K partials of this row (4 elements per step)
-  float4 v[4];  // H <= 16384 -> at most 16 float4 per thread with 256 threads
-  const int n4 = H / 4;
+  float4 v[4];
   float ss = 0.f;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -450,23 +552,14 @@ __global__ void k_flush_norm(const float* part, int nsplit, long long split_stri
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (i < n4) {
       for (int sidx = 0; sidx < nsplit; ++sidx) {
-        const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
+        const float4 t = __ldg(reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride) + i);
         acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
       }
     }
     v[u] = acc;
     ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
   }
-  for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {  // H > 4096
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sidx = 0; sidx < nsplit; ++sidx) {
-      const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
-      acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
-    }
-    ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / (float)H + eps);
+  const float inv = rsqrtf(block_sum(ss, red) / (float)H + eps);
   uint2* out = reinterpret_cast<uint2*>(b + (size_t)m * H);
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -477,21 +570,11 @@ __global__ void k_flush_norm(const float* part, int nsplit, long long split_stri
                           (uint32_t)f_to_bf16(v[u].z * inv * ww.z) | ((uint32_t)f_to_bf16(v[u].w * inv * ww.w) << 16));
     }
   }
-  for (int i = threadIdx.x + 4 * blockDim.x; i < n4; i += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sidx = 0; sidx < nsplit; ++sidx) {
-      const float4 t = reinterpret_cast<const float4*>(p + (size_t)sidx * split_stride)[i];
-      acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
-    }
-    const float4 ww = reinterpret_cast<const float4*>(w)[i];
-    out[i] = make_uint2((uint32_t)f_to_bf16(acc.x * inv * ww.x) | ((uint32_t)f_to_bf16(acc.y * inv * ww.y) << 16),
-                        (uint32_t)f_to_bf16(acc.z * inv * ww.z) | ((uint32_t)f_to_bf16(acc.w * inv * ww.w) << 16));
-  }
 }
 
 void launch_flush_norm(const float* part, int nsplit, long long split_stride, int M, int H, const float* w,
                        float eps, uint16_t* b, cudaStream_t s) {
-  k_flush_norm<<<M, 256, 0, s>>>(part, nsplit, split_stride, H, w, eps, b);
+  launch_pdl(k_flush_norm, dim3(M), dim3(row_threads(H / 4, 4)), 0, s, part, nsplit, split_stride, H, w, eps, b);
   count_launch();
 }
 

@@ -578,6 +578,31 @@ __device__ void bitonic_sort(uint32_t* key, int* id, int P) {
   }
 }
 
+// Ascending (key, id) sort of L <= 2 * kST entries with distinct ids: every
+// entry's position is its count of smaller (key, id) pairs, so positions are a
+// permutation of 0..L-1.
+__device__ void rank_sort(uint32_t* key, int* id, int L) {
+  uint32_t rk[2];
+  int ri[2], pos[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int t = threadIdx.x + u * kST;
+    pos[u] = -1;
+    if (t < L) {
+      rk[u] = key[t];
+      ri[u] = id[t];
+      int cnt = 0;
+      for (int q = 0; q < L; ++q) cnt += pair_gt(rk[u], ri[u], key[q], id[q]);
+      pos[u] = cnt;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+    if (pos[u] >= 0) { key[pos[u]] = rk[u]; id[pos[u]] = ri[u]; }
+  __syncthreads();
+}
+
 // Warp 0: first index j < L at which the running sum of w(j) reaches target
 // (L if never). w must be cheap and deterministic.
 template <class W>
@@ -669,31 +694,8 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
   }
   __syncthreads();
-  if (L <= 1024) {
-    // rank sort: every entry's position is its count of smaller (key, id)
-    // pairs; ids are distinct, so positions are a permutation of 0..L-1
-    uint32_t rk[2];
-    int ri[2], pos[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int t = threadIdx.x + u * kST;
-      pos[u] = -1;
-      if (t < L) {
-        rk[u] = cb.mkey[t];
-        ri[u] = cb.mid[t];
-        int cnt = 0;
-        for (int q = 0; q < L; ++q) cnt += pair_gt(rk[u], ri[u], cb.mkey[q], cb.mid[q]);
-        pos[u] = cnt;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-      if (pos[u] >= 0) { cb.mkey[pos[u]] = rk[u]; cb.mid[pos[u]] = ri[u]; }
-    __syncthreads();
-  } else {
-    bitonic_sort(cb.mkey, cb.mid, Pd);
-  }
+  if (L <= 1024) rank_sort(cb.mkey, cb.mid, L);
+  else bitonic_sort(cb.mkey, cb.mid, Pd);
   if (threadIdx.x < 32) {
     auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
     const int Kk = k > 0 ? min(k, L) : L;
@@ -779,11 +781,150 @@ __device__ int candidate_draw(const TDesc& d, CandBufs& cb, float u, SampleSmem*
   return sm->fin_draw;
 }
 
+// Top-p cut without top-k, for a support too wide for the candidate union.
+// Transformed logits z <= mx fall into kFlatBins equal slices of
+// [mx - span, mx] (bin 0 holds the largest); the bin index is weakly monotone
+// in z, so every bin is a contiguous range of the (key, id) order. One pass
+// adds each element's fixed-point weight to its bin; each CTA then sums 256 of
+// the cluster's bins, the cluster finds the bin in which the running mass
+// reaches ceil(top_p * SE), and that bin's elements are gathered and sorted to
+// find the exact crossing element. Elements beyond the span weigh 0 and follow
+// every binned element, so they never hold the crossing. Sets the top-p fields
+// of d and returns true, or returns false (nothing decided) when the crossing
+// bin holds more than 2 * kST elements.
+constexpr int kFlatBins = 256 * kClusterCTAs;
+constexpr float kFlatSpan = 30.f;  // exp(-30) * 2^40 rounds to 0
+
+__device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowParams& p, float mx, float zmin,
+                           CandBufs& cb, TDesc& d) {
+  SampleSmem* sm = c.sm;
+  float span = mx - zmin;
+  if (!(span > 0.f)) return false;  // one distinct value, or non-finite input
+  if (span > kFlatSpan) span = kFlatSpan;
+  const float scale = ((float)kFlatBins - 0.01f) / span;
+  auto bin_of = [&](float z) {  // kFlatBins for elements beyond the span (and NaN)
+    const float t = (mx - z) * scale;
+    return t < (float)kFlatBins ? (int)t : kFlatBins;
+  };
+  unsigned long long* hw = reinterpret_cast<unsigned long long*>(cb.mkey);  // aliases the merge buffers
+  for (int b = threadIdx.x; b < kFlatBins; b += kST) hw[b] = 0ull;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const float z = zs[j];
+    const int b = bin_of(z);
+    if (b < kFlatBins) {
+      const unsigned long long w = to_fix(expf(z - mx));
+      if (w) atomicAdd(&hw[b], w);
+    }
+  }
+  c.cl.sync();
+  unsigned long long own = 0;
+  if (threadIdx.x < 256) {
+    const int b = c.rank * 256 + threadIdx.x;
+    for (int r = 0; r < kClusterCTAs; ++r) own += c.cl.map_shared_rank(hw, r)[b];
+    sm->tot[threadIdx.x] = own;
+  }
+  own = block_sum_u64(own, sm->wsum);
+  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = own;
+  Mail* m = c.publish();  // also ends every remote read of hw
+  unsigned long long SE = 0;
+  for (int r = 0; r < kClusterCTAs; ++r) SE += c.remote(m, r)->u[0];
+  if (SE == 0) return false;
+  const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+  unsigned long long before = 0;
+  int owner = kClusterCTAs - 1;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    const unsigned long long t = c.remote(m, r)->u[0];
+    if (before + t >= target) { owner = r; break; }
+    before += t;
+  }
+  if (c.rank == owner && threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const unsigned long long need = target - before;
+    unsigned long long s8 = 0;
+    for (int b = 0; b < 8; ++b) s8 += sm->tot[lane * 8 + b];
+    unsigned long long incl = s8;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    unsigned long long cum = incl - s8;
+    int fb = -1;
+    unsigned long long fr = 0;
+    if (cum < need && need <= incl) {
+      for (int b = 0; b < 8; ++b) {
+        const unsigned long long t = sm->tot[lane * 8 + b];
+        if (cum < need && need <= cum + t) {
+          fb = owner * 256 + lane * 8 + b;
+          fr = need - cum;
+          break;
+        }
+        cum += t;
+      }
+    }
+    const unsigned who = __ballot_sync(0xFFFFFFFFu, fb >= 0);
+    const int src = who ? __ffs(who) - 1 : 0;
+    fb = __shfl_sync(0xFFFFFFFFu, fb, src);
+    fr = __shfl_sync(0xFFFFFFFFu, fr, src);
+    if (lane == 0) {
+      sm->mail[c.ph].i[0] = fb;  // -1 only if the bins do not add up: nothing is gathered
+      sm->mail[c.ph].u[0] = fr;
+    }
+  }
+  m = c.publish();
+  const int bstar = c.remote(m, owner)->i[0];
+  const unsigned long long rem = c.remote(m, owner)->u[0];
+  // gather the crossing bin
+  if (threadIdx.x == 0) sm->ccount = 0;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const float z = zs[j];
+    if (bin_of(z) == bstar) {
+      const int pos = atomicAdd(&sm->ccount, 1);
+      if (pos < cb.C) {
+        cb.ckey[pos] = desc_key(z);
+        cb.cid[pos] = v0 + j;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = (unsigned long long)sm->ccount;
+  m = c.publish();
+  int off[kClusterCTAs + 1];
+  off[0] = 0;
+  bool over = false;
+  for (int r = 0; r < kClusterCTAs; ++r) {
+    const int cnt = (int)c.remote(m, r)->u[0];
+    over |= cnt > cb.C;
+    off[r + 1] = off[r] + cnt;
+  }
+  const int L = off[kClusterCTAs];
+  if (over || L == 0 || L > 2 * kST) return false;
+  for (int t = threadIdx.x; t < L; t += kST) {
+    int r = 0;
+    while (t >= off[r + 1]) ++r;
+    cb.mkey[t] = c.cl.map_shared_rank(cb.ckey, r)[t - off[r]];
+    cb.mid[t] = c.cl.map_shared_rank(cb.cid, r)[t - off[r]];
+  }
+  __syncthreads();
+  rank_sort(cb.mkey, cb.mid, L);
+  if (threadIdx.x < 32) {
+    const int j = warp_find_cross(L, rem, [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); }, nullptr);
+    if (threadIdx.x == 0) sm->found = j < L ? j : L - 1;
+  }
+  __syncthreads();
+  d.p_key = cb.mkey[sm->found];
+  d.p_cut = cb.mid[sm->found];
+  __syncthreads();
+  return true;
+}
+
 // Transform one row of logits in the cluster. On return zs holds the
 // transformed logits (penalised, then / T) and `d` the descriptor; greedy rows
 // only get d.argmax.
 __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
-                              const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb) {
+                              const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb, bool flat_first) {
   SampleSmem* sm = c.sm;
   build_bitmap(sm, bits, v0, n);
   // one pass: stage, repetition penalty, argmax of the penalised logits,
@@ -850,13 +991,18 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) { sm->mail[c.ph].f[0] = bv; sm->mail[c.ph].i[0] = bi; }
+  if (threadIdx.x == 0) {
+    sm->mail[c.ph].f[0] = bv;
+    sm->mail[c.ph].i[0] = bi;
+    sm->mail[c.ph].f[1] = smp ? key_to_z(kmax) : 0.f;  // smallest transformed logit of the slice
+  }
   Mail* m = c.publish();
-  float gv = -INFINITY;
+  float gv = -INFINITY, zmin = INFINITY;
   int gi = 0x7FFFFFFF;
   for (int r = 0; r < kClusterCTAs; ++r) {
     Mail* x = c.remote(m, r);
     if (better(x->f[0], x->i[0], gv, gi)) { gv = x->f[0]; gi = x->i[0]; }
+    zmin = fminf(zmin, x->f[1]);
   }
   d.argmax = gi;
   d.k_key = 0xFFFFFFFFu;
@@ -870,7 +1016,12 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
 
   d.m = gv / p.temperature + 0.0f;
   const float mx = d.m;
-  if (candidate_transform(c, zs, v0, n, V, p, mx, kmin, kmax, cb, d)) return true;
+  // verify descriptors try the binned top-p cut first (no draw follows);
+  // the draft step tries the candidate union first (its draw reuses the list)
+  const bool flat_ok = !(p.top_k > 0 && p.top_k < V) && p.top_p > 0.f && p.top_p < 1.f;
+  bool flat_done = flat_first && flat_ok && flat_top_p(c, zs, v0, n, p, mx, zmin, cb, d);
+  if (!flat_done && candidate_transform(c, zs, v0, n, V, p, mx, kmin, kmax, cb, d)) return true;
+  if (!flat_done && !flat_first && flat_ok) flat_done = flat_top_p(c, zs, v0, n, p, mx, zmin, cb, d);
 
   if (p.top_k > 0 && p.top_k < V) {
     uint32_t K;
@@ -885,7 +1036,7 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   auto in_k = [&](int j) { return in_prefix(desc_key(zs[j]), v0 + j, kK, kC); };
   auto e_of = [&](int j) { return expf(zs[j] - mx); };
 
-  if (p.top_p > 0.f && p.top_p < 1.f) {
+  if (p.top_p > 0.f && p.top_p < 1.f && !flat_done) {
     unsigned long long loc = 0;
     for (int j = threadIdx.x; j < n; j += kST)
       if (in_k(j)) loc += to_fix(e_of(j));
@@ -987,7 +1138,7 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
   const RowParams p = a.p[r];
   load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, i);
   TDesc d;
-  const bool fast = transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status, cb);
+  const bool fast = transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status, cb, a.mode == 1);
 
   if (a.mode == 1) {
     if (c.rank == 0 && threadIdx.x == 0) a.desc[task] = d;
