@@ -100,6 +100,66 @@ void launch_flush_norm(const float* part, int nsplit, long long split_stride, in
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
                     int ksplit, float* D, int32_t* status, cudaStream_t s, int mh = 1);
 
+// Batched GEMV on tcgen05 (bf16 weights, kTcGemvMaxItems items per pass).
+constexpr int kTcGemvMaxItems = 64;
+
+// X2[NI][K] bf16: rows m < MI hold bf16(x_m), rows MI + m hold the rounding
+// residue bf16(x_m - bf16(x_m)); x_m after the prologue; items M..MI-1 zero.
+struct TcxPrepArgs {
+  int pro, K, M, MI;
+  const float* x;
+  long long ldx;
+  const float* nw;
+  const float* nw2;
+  float eps;
+  const void* E;
+  int wdt, vocab;
+  const int32_t* tok;
+  const void* hid;
+  int hid_dt;
+  uint16_t* X2;
+  int32_t* status;
+  int tok_idx[kTcGemvMaxItems];
+  long long hid_off[kTcGemvMaxItems];
+};
+void launch_tcx_prep(const TcxPrepArgs& a, cudaStream_t s);
+
+// out[split][item][row] (strides ld_split, ld_item) = W[row] . x[item] over the
+// virtual row space: segments w[0..nmaps) ending at seg_end, or (swiglu) 128-row
+// tiles of 64 gate rows (w[0]) then the matching 64 up rows (w[1]).
+struct TcGemvLaunch {
+  const void* w[3];
+  int rows[3];
+  int nmaps;
+  int seg_end[3];
+  int swiglu;
+  int N, K, M, NI, ksplit;
+  const uint16_t* X2;
+  float* out;
+  long long ld_item, ld_split;
+  int32_t* status;
+};
+bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s);
+
+// Sum the split partials (split order) and apply the epilogue; outputs
+// o < nout (nout = N, or N/2 for SwiGLU).
+struct TcFinishArgs {
+  const float* part;
+  long long ld_item, ld_split;
+  int ksplit, M, epi, nout, write_y;
+  float* y;
+  long long ldy;
+  const float* resid;
+  long long ldr;
+  float* gmax;
+  int* gidx;
+  int* done;
+  int32_t* amax_out;
+  int32_t* status;
+  int amax_idx[kTcGemvMaxItems];
+};
+void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s);
+
 // Decode attention of the head items over slots 0..slot (split over chunks).
 struct AttnArgs {
   const float* q;        // [Mh][nq*dh]

@@ -87,6 +87,9 @@ struct mtp_handle {
   uint16_t *xb = nullptr, *bb = nullptr;  // bf16 activations of the tensor-core flush
   double* inv_freq = nullptr;             // RoPE frequencies theta^(-2i/dh), [dh/2]
   float* tcpart = nullptr;                // split-K partial tiles of the tensor-core flush
+  uint16_t* x2 = nullptr;                 // hi/lo bf16 activations of the tensor-core GEMV
+  float* tvpart = nullptr;                // its split-K partials
+  bool tc_gemv = false;                   // batched GEMVs on tcgen05 (bf16 weights)
   int32_t* status = nullptr;
   size_t part_floats = 0;
   int max_chunks = 0, lm_groups_max = 0, counters_n = 0;
@@ -190,7 +193,93 @@ struct GemvJob {
   const int* amax_idx;
 };
 
+// Batches of at least this many items run their GEMVs on the tensor cores:
+// below it the CUDA-core GEMV keeps up with HBM.
+constexpr int kTcGemvMinItems = 5;
+
+// K splits for the tensor-core GEMV: about two CTAs per SM, at least 8 K tiles each.
+int tcv_splits(int tiles, int ktiles, int sms) {
+  int ks = 1;
+  while (ks < 8 && tiles * ks < 2 * sms && ktiles / (2 * ks) >= 8) ks *= 2;
+  return ks;
+}
+
+// Weight maps of a GEMV job on the tensor-core path; false if the job's row
+// layout does not tile (segment boundaries off the 128-row grid).
+bool tc_layout(const GemvJob& j, TcGemvLaunch& L) {
+  std::memset(&L, 0, sizeof(L));
+  L.N = j.N; L.K = j.K;
+  if (j.K % 64 != 0) return false;
+  if (j.epi == EPI_SWIGLU) {
+    const int I = j.N / 2;
+    if (I % 64 != 0) return false;
+    L.swiglu = 1; L.nmaps = 2;
+    L.w[0] = j.w[0]; L.w[1] = j.w[1]; L.w[2] = j.w[1];
+    L.rows[0] = L.rows[1] = L.rows[2] = I;
+    L.seg_end[0] = L.seg_end[1] = L.seg_end[2] = j.N;
+    return true;
+  }
+  int start = 0;
+  for (int sg = 0; sg < 3; ++sg) {
+    L.seg_end[sg] = j.seg_end[sg];
+    if (j.seg_end[sg] <= start) continue;
+    if (j.seg_end[sg] < j.N && j.seg_end[sg] % 128 != 0) return false;
+    L.w[L.nmaps] = j.w[sg];
+    L.rows[L.nmaps] = j.seg_end[sg] - start;
+    ++L.nmaps;
+    start = j.seg_end[sg];
+  }
+  for (int i = L.nmaps; i < 3; ++i) { L.w[i] = L.w[L.nmaps - 1]; L.rows[i] = L.rows[L.nmaps - 1]; }
+  return L.nmaps > 0 && start == j.N;
+}
+
+// prologue + hi/lo split, tcgen05 contraction, split sum + epilogue; passes of
+// at most kTcGemvMaxItems items.
+bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
+  TcGemvLaunch L;
+  if (!tc_layout(j, L)) return false;
+  const int tiles = (j.N + 127) / 128;
+  const int ks = tcv_splits(tiles, j.K / 64, h->sms);
+  for (int m0 = 0; m0 < M; m0 += kTcGemvMaxItems) {
+    const int mp = std::min(kTcGemvMaxItems, M - m0);
+    const int NI = mp <= 8 ? 16 : (mp <= 16 ? 32 : (mp <= 32 ? 64 : 128));
+    TcxPrepArgs p;
+    std::memset(&p, 0, sizeof(p));
+    p.pro = j.pro; p.K = j.K; p.M = mp; p.MI = NI / 2;
+    p.x = j.x ? j.x + (size_t)m0 * j.ldx : nullptr;
+    p.ldx = j.ldx; p.nw = j.nw; p.nw2 = j.nw2; p.eps = h->cfg.eps;
+    p.E = h->embed; p.wdt = h->cfg.dtype; p.vocab = h->cfg.vocab;
+    p.tok = j.tok; p.hid = j.hid; p.hid_dt = j.hid_dt; p.X2 = h->x2; p.status = h->status;
+    for (int m = 0; m < mp; ++m) {
+      if (j.tok_idx) p.tok_idx[m] = j.tok_idx[m0 + m];
+      if (j.hid_off) p.hid_off[m] = j.hid_off[m0 + m];
+    }
+    launch_tcx_prep(p, s);
+    const bool direct = ks == 1 && (j.epi == EPI_STORE || j.epi == EPI_LOGITS);
+    float* y = j.y + (size_t)m0 * j.ldy;
+    L.M = mp; L.NI = NI; L.ksplit = ks; L.X2 = h->x2; L.status = h->status;
+    L.out = direct ? y : h->tvpart;
+    L.ld_item = direct ? j.ldy : j.N;
+    L.ld_split = (long long)mp * j.N;
+    if (!launch_tc_gemv(L, s)) return false;
+    if (direct && j.epi == EPI_STORE) continue;
+    TcFinishArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.part = L.out; f.ld_item = L.ld_item; f.ld_split = L.ld_split; f.ksplit = ks; f.M = mp; f.epi = j.epi;
+    f.nout = j.epi == EPI_SWIGLU ? j.N / 2 : j.N;
+    f.write_y = direct ? 0 : 1;
+    f.y = y; f.ldy = j.ldy;
+    f.resid = j.resid ? j.resid + (size_t)m0 * j.ldr : nullptr;
+    f.ldr = j.ldr;
+    f.gmax = h->gmax; f.gidx = h->gidx; f.done = h->done; f.amax_out = j.amax_out; f.status = h->status;
+    for (int m = 0; m < mp; ++m) f.amax_idx[m] = j.amax_idx ? j.amax_idx[m0 + m] : 0;
+    launch_tcv_finish(f, s);
+  }
+  return true;
+}
+
 void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
+  if (h->tc_gemv && M >= kTcGemvMinItems && run_gemv_tc(h, j, M, s)) return;
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mp = std::min(8, M - m0);
     const GemvPlan pl = plan_gemv(j.N, j.K, mp, j.dual, h->sms);
@@ -590,9 +679,21 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     if (st == MTP_OK) st = alloc(h, &h->xb, (size_t)kMaxItems * 2 * H);
     if (st == MTP_OK) st = alloc(h, &h->bb, (size_t)kMaxItems * H);
     if (st == MTP_OK) st = alloc(h, &h->tcpart, (size_t)kMaxItems * std::max(8 * H, 8 * 2 * kw));
+    // tensor-core GEMV: hi/lo activations [2 * kTcGemvMaxItems][K] and the
+    // split partials of the widest shape
+    const int kmax = std::max(std::max(2 * H, I), qw);
+    size_t tvp = 0;
+    for (auto& sh : shapes) {
+      const int ks = tcv_splits((sh[0] + 127) / 128, sh[1] / 64, h->sms);
+      tvp = std::max(tvp, (size_t)ks * kTcGemvMaxItems * sh[0]);
+    }
+    if (st == MTP_OK) st = alloc(h, &h->x2, (size_t)2 * kTcGemvMaxItems * kmax);
+    if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
+    h->tc_gemv = st == MTP_OK;
   }
-  if (st == MTP_OK) st = alloc(h, &h->gmax, (size_t)8 * h->lm_groups_max);
-  if (st == MTP_OK) st = alloc(h, &h->gidx, (size_t)8 * h->lm_groups_max);
+  const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 1023) / 1024));
+  if (st == MTP_OK) st = alloc(h, &h->gmax, gslots);
+  if (st == MTP_OK) st = alloc(h, &h->gidx, gslots);
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
   if (st == MTP_OK) st = alloc(h, &h->done, 1);
   if (st == MTP_OK) st = alloc(h, &h->status, 1);

@@ -32,14 +32,18 @@ def _desc_key(z: np.ndarray) -> np.ndarray:
     return (~asc).astype(np.uint32)
 
 
-def _kept_from_desc(lg, d, params, window):
+def _transformed(lg, params, window):
+    """Penalised, temperature-scaled logits in fp32 (the order the keys follow)."""
     z = lg.astype(np.float32).copy()
     r = np.float32(params.get("rep_penalty", 1.0))
     if r != 1.0 and window.size:
         ids = np.unique(window)
         z[ids] = np.where(z[ids] > 0, z[ids] / r, z[ids] * r)
-    z = (z / np.float32(params["temperature"])).astype(np.float32)
-    key = _desc_key(z)
+    return (z / np.float32(params["temperature"])).astype(np.float32)
+
+
+def _kept_from_desc(lg, d, params, window):
+    key = _desc_key(_transformed(lg, params, window))
     ids = np.arange(V)
     keep = (key < d["k_key"]) | ((key == d["k_key"]) & (ids <= d["k_cut"]))
     keep &= (key < d["p_key"]) | ((key == d["p_key"]) & (ids <= d["p_cut"]))
@@ -96,8 +100,8 @@ def test_wide_top_p_descriptors():
                 assert abs(int(got.sum()) - int(want.sum())) <= 1, (r, i)
                 near += 1
                 continue
-            ez = np.exp(np.float64(lg[r, i][want].astype(np.float32) / np.float32(rows[r]["temperature"]))
-                        - np.float64(desc[r, i]["m"]))
+            z = _transformed(lg[r, i], rows[r], window)
+            ez = np.exp(z[want].astype(np.float64) - np.float64(desc[r, i]["m"]))
             assert abs(float(desc[r, i]["S"]) - ez.sum()) <= 1e-5 * ez.sum(), (r, i)
             assert desc[r, i]["kept"] == want.sum(), (r, i)
     assert near <= 1
