@@ -39,7 +39,8 @@ def _transformed(lg, params, window):
     if r != 1.0 and window.size:
         ids = np.unique(window)
         z[ids] = np.where(z[ids] > 0, z[ids] / r, z[ids] * r)
-    return (z / np.float32(params["temperature"])).astype(np.float32)
+    # + 0.0 turns -0.0 into +0.0: equal values share one key, as in the kernels
+    return ((z / np.float32(params["temperature"])).astype(np.float32) + np.float32(0.0)).astype(np.float32)
 
 
 def _kept_from_desc(lg, d, params, window):
