@@ -583,6 +583,8 @@ def main():
     ap.add_argument("--flush-only", action="store_true", help="time only the 256-pair flush (profiling case)")
     ap.add_argument("--sampled-only", action="store_true",
                     help="time only sampled rounds at depth 1 (profiling case)")
+    ap.add_argument("--batched-only", action="store_true",
+                    help="time only the 8-row batched draft + verify (profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -639,6 +641,15 @@ def main():
         tensors = {n: to(a) for n, a in model.tensors.items()}
         out = measure_sampled(tensors, to(model.embed), s, dev, rounds=max(args.steps, 1), depths=(1,))
         print(json.dumps({"sampled": out}), flush=True)
+        return
+    if args.batched_only:
+        import torch as _t
+        s, model, K, V, base, thid, tok0 = build_workload(args.seed, rank, args.vocab)
+        dev = _t.device("cuda", local_rank)
+        to = lambda a: (_t.from_numpy(a).view(_t.bfloat16) if a.dtype == np.uint16 else _t.from_numpy(a)).to(dev)
+        tensors = {n: to(a) for n, a in model.tensors.items()}
+        out = measure_batched(tensors, to(model.embed), s, dev, reps=max(args.steps, 1))
+        print(json.dumps({"batched_8_rows": out}), flush=True)
         return
     if args.flush_only:
         import torch as _t

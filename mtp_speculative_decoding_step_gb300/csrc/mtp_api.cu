@@ -132,12 +132,25 @@ GemvPlan plan_gemv(int N, int K, int M, bool dual, int sms) {
   p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   const int rows = gemv_rows_per_group(p.mt);
   p.ngroups = N / rows;
-  // at least one block per SM: every block keeps enough loads in flight to
-  // draw its share of HBM, so long blocks in one wave beat many short ones
-  // with split-K tails
-  p.S = dual ? 2 : 1;
-  while (p.S < 8 && (long long)p.ngroups * p.S < (long long)sms) p.S *= 2;
-  while (p.S < 8 && (long long)p.mt * (K / p.S) * 4 > 96 * 1024) p.S *= 2;
+  // Split K so that the blocks spread evenly over the SMs: every block streams
+  // the same bytes and an SM holding one block more than the others sets the
+  // kernel's time, so pick the split whose block count wastes the least of the
+  // last wave (ceil(B / sms) * sms / B), preferring fewer, longer splits unless
+  // a finer one is clearly better. A split is a multiple of 8 elements, at
+  // least 512 long, stages within 96 KB and (dual prologue) stays inside one
+  // half of x.
+  p.S = 0;
+  double best = 1e30;
+  for (int S = 1; S <= 64; ++S) {
+    if (K % S != 0) continue;
+    const int KS = K / S;
+    if (KS % 8 != 0 || (S > 1 && KS < 512) || (long long)p.mt * KS * 4 > 96 * 1024) continue;
+    if (dual && (S < 2 || (K / 2) % KS != 0)) continue;
+    const long long B = (long long)p.ngroups * S;
+    const double waste = (double)((B + sms - 1) / sms) * sms / (double)B;
+    if (waste < best * 0.97) { best = waste; p.S = S; }
+  }
+  if (p.S == 0) p.S = dual ? 2 : 1;
   p.smem = p.mt * (K / p.S) * 4;
   return p;
 }
