@@ -245,8 +245,12 @@ struct VerifyArgs {
   int32_t* n_acc;
   int32_t* out_tok;
   int32_t* stats;
+  int32_t* status;
   RowParams p[kMaxRows];
 };
 void launch_verify(const VerifyArgs& a, cudaStream_t s);
+// All rows greedy without a repetition penalty: argmax matches in one launch
+// (depth <= 16; desc, q, hist and u unused).
+void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
 
 }  // namespace mtp

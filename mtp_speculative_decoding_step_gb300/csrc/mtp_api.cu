@@ -930,20 +930,30 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
   for (int r = 0; r < rows; ++r) any_sampled |= !row_params(h_params[r]).greedy;
   if (any_sampled && !d_q) return MTP_ERR_BAD_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  TDesc* desc = static_cast<TDesc*>(d_workspace);
-  SampleArgs sa;
-  std::memset(&sa, 0, sizeof(sa));
-  sa.mode = 1; sa.rows = rows; sa.V = vocab; sa.W = hist_w; sa.depth = depth;
-  sa.logits = d_logits; sa.hist = d_hist; sa.drafts = d_draft; sa.desc = desc;
-  for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
-  launch_sample(sa, s);
-  VerifyArgs va;
-  std::memset(&va, 0, sizeof(va));
-  va.rows = rows; va.V = vocab; va.W = hist_w; va.depth = depth;
-  va.logits = d_logits; va.drafts = d_draft; va.q = d_q; va.hist = d_hist; va.u = d_u; va.desc = desc;
-  va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
-  for (int r = 0; r < rows; ++r) va.p[r] = sa.p[r];
-  launch_verify(va, s);
+  bool all_fast_greedy = true;
+  for (int r = 0; r < rows; ++r) all_fast_greedy &= fast_greedy(h_params[r]);
+  if (all_fast_greedy) {
+    VerifyArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.rows = rows; va.V = vocab; va.depth = depth;
+    va.logits = d_logits; va.drafts = d_draft; va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
+    launch_verify_greedy(va, s);
+  } else {
+    TDesc* desc = static_cast<TDesc*>(d_workspace);
+    SampleArgs sa;
+    std::memset(&sa, 0, sizeof(sa));
+    sa.mode = 1; sa.rows = rows; sa.V = vocab; sa.W = hist_w; sa.depth = depth;
+    sa.logits = d_logits; sa.hist = d_hist; sa.drafts = d_draft; sa.desc = desc;
+    for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
+    launch_sample(sa, s);
+    VerifyArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.rows = rows; va.V = vocab; va.W = hist_w; va.depth = depth;
+    va.logits = d_logits; va.drafts = d_draft; va.q = d_q; va.hist = d_hist; va.u = d_u; va.desc = desc;
+    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
+    for (int r = 0; r < rows; ++r) va.p[r] = sa.p[r];
+    launch_verify(va, s);
+  }
   st = cuda_ok(cudaGetLastError());
   if (st != MTP_OK) return st;
   if (h_out) {

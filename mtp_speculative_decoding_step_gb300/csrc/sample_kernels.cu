@@ -1265,6 +1265,105 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
   c.cl.sync();
 }
 
+// Verify of greedy rows without a repetition penalty, in one launch. With
+// point-mass p and q the Leviathan/Chen rule accepts x_i exactly when x_i is
+// the argmax of target row i-1, and the correction or bonus token is the
+// argmax of the first unmatched row. One 8-CTA cluster per row: each CTA
+// takes the argmax (value desc, id asc) of its vocabulary slice for every
+// position, the cluster combines the slices through DSMEM, and rank 0 walks
+// the accept chain and writes the outputs.
+constexpr int kGreedyMaxPos = 17;
+
+__global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
+  __shared__ float s_v[kGreedyMaxPos];
+  __shared__ int s_i[kGreedyMaxPos];
+  __shared__ float sv[kST / 32];
+  __shared__ int si[kST / 32];
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int r = blockIdx.x / kClusterCTAs;
+  const int d = a.depth;
+  int v0, n;
+  slice_of(a.V, rank, v0, n);
+  pdl_wait();
+  pdl_trigger();
+  const float* lg = a.logits + (size_t)r * (d + 1) * a.V;
+  bool bad = false;
+  for (int i = 0; i <= d; ++i) {
+    const float* row = lg + (size_t)i * a.V + v0;
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    auto one = [&](int j, float z) {
+      if (!isfinite(z)) bad = true;
+      if (better(z, v0 + j, bv, bi)) { bv = z; bi = v0 + j; }
+    };
+    if (((v0 + (size_t)i * a.V) & 3) == 0 && (n & 3) == 0) {
+      const float4* l4 = reinterpret_cast<const float4*>(row);
+      const int n4 = n / 4;
+      for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+        float4 xb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j4 = b0 + u * kST + threadIdx.x;
+          if (j4 < n4) xb[u] = __ldg(l4 + j4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j4 = b0 + u * kST + threadIdx.x;
+          if (j4 < n4) {
+            one(4 * j4, xb[u].x);
+            one(4 * j4 + 1, xb[u].y);
+            one(4 * j4 + 2, xb[u].z);
+            one(4 * j4 + 3, xb[u].w);
+          }
+        }
+      }
+    } else {
+      for (int j = threadIdx.x; j < n; j += kST) one(j, __ldg(row + j));
+    }
+    block_argmax(bv, bi, sv, si);
+    if (threadIdx.x == 0) { s_v[i] = bv; s_i[i] = bi; }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
+  cl.sync();
+  if (rank == 0 && threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // lane i < d+1 combines position i over the cluster
+    int am = 0x7FFFFFFF;
+    if (lane <= d) {
+      float gv = -INFINITY;
+      for (int q = 0; q < kClusterCTAs; ++q) {
+        const float v = *cl.map_shared_rank(&s_v[lane], q);
+        const int id = *cl.map_shared_rank(&s_i[lane], q);
+        if (better(v, id, gv, am)) { gv = v; am = id; }
+      }
+    }
+    // the chain needs every position's argmax in one lane: gather them
+    int amax[kGreedyMaxPos];
+#pragma unroll
+    for (int i = 0; i < kGreedyMaxPos; ++i) amax[i] = __shfl_sync(0xFFFFFFFFu, am, i);
+    if (lane == 0) {
+      const int32_t* dr = a.drafts + (size_t)r * d;
+      int nacc = 0;
+      for (int i = 1; i <= d; ++i) {
+        const int x = dr[i - 1];
+        if (x < 0 || x >= a.V || x != amax[i - 1]) break;
+        nacc = i;
+      }
+      a.n_acc[r] = nacc;
+      int32_t* o = a.out_tok + (size_t)r * (d + 1);
+      for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? amax[nacc] : -1);
+      if (a.stats) {
+        int32_t* st = a.stats + (size_t)r * (d + 2);
+        st[0] += 1;
+        if (nacc < d) st[1] += 1;
+        for (int i = 1; i <= nacc; ++i) st[1 + i] += 1;
+      }
+    }
+  }
+  cl.sync();  // keep shared memory alive until rank 0 has read it
+}
+
 static int sample_smem(int V, int C = 0, int P = 0) {
   const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
   const size_t cand = 16 + (size_t)C * 8 + (size_t)P * 8 + (size_t)C * 4 + 4 + (size_t)C * 8;
@@ -1311,5 +1410,23 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
 }
 
 void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verify, a, a.rows, a.V, s); }
+
+void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.rows * kClusterCTAs);
+  cfg.blockDim = dim3(kST);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCTAs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, k_verify_greedy, a);
+  count_launch();
+}
 
 }  // namespace mtp
