@@ -340,83 +340,75 @@ bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s) {
 
 // ------------------------------------------------------------ epilogue
 
-// grid ceil(nout / 1024), block 256: each thread owns outputs
-// blockIdx.x * 1024 + u * 256 + tid (u < 4) for every item.
+// grid (ceil(nout / 256), M), block 256: thread t of block (x, m) owns output
+// o = 256 x + t of item m. Logits: block argmax per (x, m), and the last block
+// to finish reduces every item's blocks into its token.
 __global__ void __launch_bounds__(256) k_tcv_finish(const __grid_constant__ TcFinishArgs a) {
   __shared__ float sv[8];
   __shared__ int si[8];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m = blockIdx.y, o = blockIdx.x * 256 + tid;
   pdl_wait();
   pdl_trigger();
   const bool logits = a.epi == EPI_LOGITS;
-  for (int m = 0; m < a.M; ++m) {
-    const float* p = a.part + (size_t)m * a.ld_item;
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int o = blockIdx.x * 1024 + u * 256 + tid;
-      if (o >= a.nout) continue;
-      float v;
-      if (a.epi == EPI_SWIGLU) {
-        const int t = o >> 6, j = o & 63;
-        float g = 0.f, up = 0.f;
-        for (int sp = 0; sp < a.ksplit; ++sp) {
-          g += __ldcg(p + (size_t)sp * a.ld_split + (size_t)t * 128 + j);
-          up += __ldcg(p + (size_t)sp * a.ld_split + (size_t)t * 128 + 64 + j);
-        }
-        v = g / (1.f + expf(-g)) * up;
-      } else {
-        v = 0.f;
-        for (int sp = 0; sp < a.ksplit; ++sp) v += __ldcg(p + (size_t)sp * a.ld_split + o);
-        if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + o];
+  const float* p = a.part + (size_t)m * a.ld_item;
+  float v = -INFINITY;
+  if (o < a.nout) {
+    if (a.epi == EPI_SWIGLU) {
+      const size_t r = (size_t)(o >> 6) * 128 + (o & 63);
+      float g = 0.f, up = 0.f;
+      for (int sp = 0; sp < a.ksplit; ++sp) {
+        g += __ldcg(p + (size_t)sp * a.ld_split + r);
+        up += __ldcg(p + (size_t)sp * a.ld_split + r + 64);
       }
-      if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
-      if (logits) {
-        if (!isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
-        if (better(v, o, bv, bi)) { bv = v; bi = o; }
-      }
+      v = g / (1.f + expf(-g)) * up;
+    } else {
+      v = 0.f;
+      for (int sp = 0; sp < a.ksplit; ++sp) v += __ldcg(p + (size_t)sp * a.ld_split + o);
+      if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + o];
     }
-    if (logits) {
-      warp_argmax(bv, bi);
-      if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
-      __syncthreads();
-      if (warp == 0) {
-        bv = lane < 8 ? sv[lane] : -INFINITY;
-        bi = lane < 8 ? si[lane] : 0x7FFFFFFF;
-        warp_argmax(bv, bi);
-        if (lane == 0) {
-          a.gmax[(size_t)m * gridDim.x + blockIdx.x] = bv;
-          a.gidx[(size_t)m * gridDim.x + blockIdx.x] = bi;
-        }
-      }
-      __syncthreads();
-    }
+    if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
   }
   if (!logits) return;
+  if (o < a.nout && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
+  float bv = o < a.nout ? v : -INFINITY;
+  int bi = o < a.nout ? o : 0x7FFFFFFF;
+  warp_argmax(bv, bi);
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  const int ng = (int)gridDim.x;
+  if (warp == 0) {
+    bv = lane < 8 ? sv[lane] : -INFINITY;
+    bi = lane < 8 ? si[lane] : 0x7FFFFFFF;
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      a.gmax[(size_t)m * ng + blockIdx.x] = bv;
+      a.gidx[(size_t)m * ng + blockIdx.x] = bi;
+    }
+  }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.done, 1) == (int)gridDim.x - 1;
+  if (tid == 0) s_last = atomicAdd(a.done, 1) == ng * (int)gridDim.y - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int m = warp; m < a.M; m += 8) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int g = lane; g < (int)gridDim.x; g += 32) {
-      const float v = __ldcg(&a.gmax[(size_t)m * gridDim.x + g]);
-      const int i = __ldcg(&a.gidx[(size_t)m * gridDim.x + g]);
-      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+  for (int mm = warp; mm < (int)gridDim.y; mm += 8) {
+    float cv = -INFINITY;
+    int ci = 0x7FFFFFFF;
+    for (int g = lane; g < ng; g += 32) {
+      const float x = __ldcg(&a.gmax[(size_t)mm * ng + g]);
+      const int i = __ldcg(&a.gidx[(size_t)mm * ng + g]);
+      if (better(x, i, cv, ci)) { cv = x; ci = i; }
     }
-    warp_argmax(bv, bi);
-    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[m]] = bi;
+    warp_argmax(cv, ci);
+    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[mm]] = ci;
   }
   if (tid == 0) *a.done = 0;
 }
 
 void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s) {
-  launch_pdl(k_tcv_finish, dim3((a.nout + 1023) / 1024), dim3(256), 0, s, a);
+  launch_pdl(k_tcv_finish, dim3((a.nout + 255) / 256, a.M), dim3(256), 0, s, a);
   count_launch();
 }
 

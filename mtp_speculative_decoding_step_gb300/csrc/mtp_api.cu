@@ -132,25 +132,13 @@ GemvPlan plan_gemv(int N, int K, int M, bool dual, int sms) {
   p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   const int rows = gemv_rows_per_group(p.mt);
   p.ngroups = N / rows;
-  // Split K so that the blocks spread evenly over the SMs: every block streams
-  // the same bytes and an SM holding one block more than the others sets the
-  // kernel's time, so pick the split whose block count wastes the least of the
-  // last wave (ceil(B / sms) * sms / B), preferring fewer, longer splits unless
-  // a finer one is clearly better. A split is a multiple of 8 elements, at
-  // least 512 long, stages within 96 KB and (dual prologue) stays inside one
-  // half of x.
-  p.S = 0;
-  double best = 1e30;
-  for (int S = 1; S <= 64; ++S) {
-    if (K % S != 0) continue;
-    const int KS = K / S;
-    if (KS % 8 != 0 || (S > 1 && KS < 512) || (long long)p.mt * KS * 4 > 96 * 1024) continue;
-    if (dual && (S < 2 || (K / 2) % KS != 0)) continue;
-    const long long B = (long long)p.ngroups * S;
-    const double waste = (double)((B + sms - 1) / sms) * sms / (double)B;
-    if (waste < best * 0.97) { best = waste; p.S = S; }
-  }
-  if (p.S == 0) p.S = dual ? 2 : 1;
+  // at least one block per SM: every block keeps enough loads in flight to
+  // draw its share of HBM, so long blocks in one wave beat many short ones
+  // with split-K tails (block counts balanced over the SMs measured slower:
+  // a lone block per SM cannot keep enough loads in flight)
+  p.S = dual ? 2 : 1;
+  while (p.S < 8 && (long long)p.ngroups * p.S < (long long)sms) p.S *= 2;
+  while (p.S < 8 && (long long)p.mt * (K / p.S) * 4 > 96 * 1024) p.S *= 2;
   p.smem = p.mt * (K / p.S) * 4;
   return p;
 }
@@ -704,7 +692,7 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
     h->tc_gemv = st == MTP_OK;
   }
-  const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 1023) / 1024));
+  const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 255) / 256));
   if (st == MTP_OK) st = alloc(h, &h->gmax, gslots);
   if (st == MTP_OK) st = alloc(h, &h->gidx, gslots);
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);

@@ -603,6 +603,45 @@ __device__ void rank_sort(uint32_t* key, int* id, int L) {
   __syncthreads();
 }
 
+// Merge kClusterCTAs sorted runs held back to back in key/id (run r at
+// [off[r], off[r+1]), L <= kMergePer * kST in total) into one ascending (key,
+// id) list: an entry's final position is its index in its own run plus, for
+// every other run, the count of entries below it there (a binary search).
+constexpr int kMergePer = 8;
+
+__device__ void merge_runs(uint32_t* key, int* id, const int* off, int L) {
+  uint32_t rk[kMergePer];
+  int ri[kMergePer], pos[kMergePer];
+#pragma unroll
+  for (int u = 0; u < kMergePer; ++u) {
+    const int t = threadIdx.x + u * kST;
+    pos[u] = -1;
+    if (t < L) {
+      rk[u] = key[t];
+      ri[u] = id[t];
+      int own = 0;
+      while (t >= off[own + 1]) ++own;
+      int p = t - off[own];
+      for (int q = 0; q < kClusterCTAs; ++q) {
+        if (q == own) continue;
+        int lo = off[q], hi = off[q + 1];
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (pair_gt(rk[u], ri[u], key[mid], id[mid])) lo = mid + 1;
+          else hi = mid;
+        }
+        p += lo - off[q];
+      }
+      pos[u] = p;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kMergePer; ++u)
+    if (pos[u] >= 0) { key[pos[u]] = rk[u]; id[pos[u]] = ri[u]; }
+  __syncthreads();
+}
+
 // Warp 0: first index j < L at which the running sum of w(j) reaches target
 // (L if never). w must be cheap and deterministic.
 template <class W>
@@ -659,6 +698,8 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
     __syncthreads();
   }
+  // sort this CTA's run (short runs only; the merge below needs every run sorted)
+  if (sm->ccount <= 2 * kST) rank_sort(cb.ckey, cb.cid, sm->ccount);
   unsigned long long sall = 0;
   if (k == 0)
     for (int j = threadIdx.x; j < n; j += kST) sall += to_fix(expf(zs[j] - mx));
@@ -672,12 +713,13 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
   int off[kClusterCTAs + 1];
   off[0] = 0;
   unsigned long long S_all = 0;
-  bool truncated = false;
+  bool truncated = false, runs_sorted = true;
   for (int r = 0; r < kClusterCTAs; ++r) {
     Mail* x = c.remote(m, r);
     off[r + 1] = off[r] + (int)x->u[0];
     S_all += x->u[1];
     truncated |= x->i[0] != 0;
+    runs_sorted &= (int)x->u[0] <= 2 * kST;
   }
   const int L = off[kClusterCTAs];
   int Pd = 1;
@@ -694,7 +736,7 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
   }
   __syncthreads();
-  if (L <= 1024) rank_sort(cb.mkey, cb.mid, L);
+  if (runs_sorted && L <= kMergePer * kST) merge_runs(cb.mkey, cb.mid, off, L);
   else bitonic_sort(cb.mkey, cb.mid, Pd);
   if (threadIdx.x < 32) {
     auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
@@ -791,7 +833,7 @@ __device__ int candidate_draw(const TDesc& d, CandBufs& cb, float u, SampleSmem*
 // find the exact crossing element. Elements beyond the span weigh 0 and follow
 // every binned element, so they never hold the crossing. Sets the top-p fields
 // of d and returns true, or returns false (nothing decided) when the crossing
-// bin holds more than 2 * kST elements.
+// bin holds more than kMergePer * kST elements (or 2 * kST in one CTA).
 constexpr int kFlatBins = 256 * kClusterCTAs;
 constexpr float kFlatSpan = 30.f;  // exp(-30) * 2^40 rounds to 0
 
@@ -889,18 +931,20 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = (unsigned long long)sm->ccount;
+  const int mine = sm->ccount;
+  if (mine <= cb.C && mine <= 2 * kST) rank_sort(cb.ckey, cb.cid, mine);
+  if (threadIdx.x == 0) sm->mail[c.ph].u[0] = (unsigned long long)mine;
   m = c.publish();
   int off[kClusterCTAs + 1];
   off[0] = 0;
   bool over = false;
   for (int r = 0; r < kClusterCTAs; ++r) {
     const int cnt = (int)c.remote(m, r)->u[0];
-    over |= cnt > cb.C;
+    over |= cnt > cb.C || cnt > 2 * kST;
     off[r + 1] = off[r] + cnt;
   }
   const int L = off[kClusterCTAs];
-  if (over || L == 0 || L > 2 * kST) return false;
+  if (over || L == 0 || L > kMergePer * kST || L > cb.P) return false;
   for (int t = threadIdx.x; t < L; t += kST) {
     int r = 0;
     while (t >= off[r + 1]) ++r;
@@ -908,7 +952,7 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
     cb.mid[t] = c.cl.map_shared_rank(cb.cid, r)[t - off[r]];
   }
   __syncthreads();
-  rank_sort(cb.mkey, cb.mid, L);
+  merge_runs(cb.mkey, cb.mid, off, L);
   if (threadIdx.x < 32) {
     const int j = warp_find_cross(L, rem, [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); }, nullptr);
     if (threadIdx.x == 0) sm->found = j < L ? j : L - 1;
