@@ -82,10 +82,15 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // TMA producer. The weight tiles come from HBM: they are prefetched into
+    // L2 kPrefetch steps ahead of their shared-memory load, so the loads the
+    // pipeline waits on hit L2.
+    constexpr int kPrefetch = STAGES;
+    for (int i = STAGES; i < min(nk, STAGES + kPrefetch); ++i) tma_prefetch_2d(tb, (kb + i) * kTileK, nb);
     for (int i = 0; i < nk; ++i) {
       const int s = i % STAGES, r = i / STAGES;
       if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1)) { *s_fail = 1; break; }
+      if (r > 0 && i + kPrefetch < nk) tma_prefetch_2d(tb, (kb + i + kPrefetch) * kTileK, nb);
       uint8_t* as = base + s * kStage;
       mbar_expect_tx(smem_u32(&full[s]), kStage);
       tma_load_2d(smem_u32(as), &ta, (kb + i) * kTileK, m0, smem_u32(&full[s]));

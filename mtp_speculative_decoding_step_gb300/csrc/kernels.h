@@ -246,6 +246,7 @@ struct VerifyArgs {
   int32_t* out_tok;
   int32_t* stats;
   int32_t* status;
+  int vec_ok;  // logits rows 16-byte aligned (set by the greedy launcher)
   RowParams p[kMaxRows];
 };
 void launch_verify(const VerifyArgs& a, cudaStream_t s);

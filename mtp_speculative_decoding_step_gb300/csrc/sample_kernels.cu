@@ -1312,91 +1312,124 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
 // Verify of greedy rows without a repetition penalty, in one launch. With
 // point-mass p and q the Leviathan/Chen rule accepts x_i exactly when x_i is
 // the argmax of target row i-1, and the correction or bonus token is the
-// argmax of the first unmatched row. One 8-CTA cluster per row: each CTA
-// takes the argmax (value desc, id asc) of its vocabulary slice for every
-// position, the cluster combines the slices through DSMEM, and rank 0 walks
-// the accept chain and writes the outputs.
+// argmax of the first unmatched row. One cluster per row (16 CTAs where the
+// device schedules them, else 8): each CTA takes the argmax (value desc, id
+// asc) of its vocabulary slice for every position, with the loads of several
+// positions in flight together, the cluster combines the slices through DSMEM,
+// and rank 0 walks the accept chain and writes the outputs.
 constexpr int kGreedyMaxPos = 17;
+constexpr int kGreedyBuf = 16;  // float4 loads in flight per thread
+constexpr int kGreedyGroup = 4;  // positions reduced together
 
 __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
   __shared__ float s_v[kGreedyMaxPos];
   __shared__ int s_i[kGreedyMaxPos];
-  __shared__ float sv[kST / 32];
-  __shared__ int si[kST / 32];
+  __shared__ float wv[kGreedyGroup][kST / 32];
+  __shared__ int wi[kGreedyGroup][kST / 32];
   cg::cluster_group cl = cg::this_cluster();
+  const int nc = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
-  const int r = blockIdx.x / kClusterCTAs;
+  const int r = blockIdx.x / nc;
   const int d = a.depth;
-  int v0, n;
-  slice_of(a.V, rank, v0, n);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = ((a.V + nc - 1) / nc + 3) & ~3;
+  const int v0 = min(rank * per, a.V);
+  const int n = min(per, a.V - v0);
   pdl_wait();
   pdl_trigger();
   const float* lg = a.logits + (size_t)r * (d + 1) * a.V;
   bool bad = false;
-  for (int i = 0; i <= d; ++i) {
-    const float* row = lg + (size_t)i * a.V + v0;
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    auto one = [&](int j, float z) {
-      if (!isfinite(z)) bad = true;
-      if (better(z, v0 + j, bv, bi)) { bv = z; bi = v0 + j; }
-    };
-    if (((v0 + (size_t)i * a.V) & 3) == 0 && (n & 3) == 0) {
-      const float4* l4 = reinterpret_cast<const float4*>(row);
-      const int n4 = n / 4;
-      for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
-        float4 xb[4];
+  const bool vec = a.vec_ok != 0;
+  const int n4 = vec ? n / 4 : 0;
+  const int U = max(1, (n4 + kST - 1) / kST);
+  const int G = vec ? max(1, min(kGreedyGroup, kGreedyBuf / U)) : 1;
+  for (int i0 = 0; i0 <= d; i0 += G) {
+    const int gi = min(G, d + 1 - i0);
+    float bv[kGreedyGroup];
+    int bi[kGreedyGroup];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j4 = b0 + u * kST + threadIdx.x;
-          if (j4 < n4) xb[u] = __ldg(l4 + j4);
-        }
+    for (int e = 0; e < kGreedyGroup; ++e) { bv[e] = -INFINITY; bi[e] = 0x7FFFFFFF; }
+    if (vec) {
+      float4 buf[kGreedyBuf];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j4 = b0 + u * kST + threadIdx.x;
-          if (j4 < n4) {
-            one(4 * j4, xb[u].x);
-            one(4 * j4 + 1, xb[u].y);
-            one(4 * j4 + 2, xb[u].z);
-            one(4 * j4 + 3, xb[u].w);
+      for (int e = 0; e < kGreedyBuf; ++e) {
+        const int pi = e / U, j4 = (e - pi * U) * kST + threadIdx.x;
+        if (pi < gi && j4 < n4)
+          buf[e] = __ldg(reinterpret_cast<const float4*>(lg + (size_t)(i0 + pi) * a.V + v0) + j4);
+      }
+#pragma unroll
+      for (int e = 0; e < kGreedyBuf; ++e) {
+        const int pi = e / U, j4 = (e - pi * U) * kST + threadIdx.x;
+        if (pi < gi && j4 < n4) {
+          const float x[4] = {buf[e].x, buf[e].y, buf[e].z, buf[e].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (!isfinite(x[q])) bad = true;
+            // slot pi of bv/bi holds position i0 + pi (e is ascending in pi)
+#pragma unroll
+            for (int t = 0; t < kGreedyGroup; ++t)
+              if (t == pi && better(x[q], v0 + 4 * j4 + q, bv[t], bi[t])) { bv[t] = x[q]; bi[t] = v0 + 4 * j4 + q; }
           }
         }
       }
+      // the tail that does not fill a float4
+      for (int j = 4 * n4 + threadIdx.x; j < n; j += kST)
+        for (int pi = 0; pi < gi; ++pi) {
+          const float x = __ldg(lg + (size_t)(i0 + pi) * a.V + v0 + j);
+          if (!isfinite(x)) bad = true;
+#pragma unroll
+          for (int t = 0; t < kGreedyGroup; ++t)
+            if (t == pi && better(x, v0 + j, bv[t], bi[t])) { bv[t] = x; bi[t] = v0 + j; }
+        }
     } else {
-      for (int j = threadIdx.x; j < n; j += kST) one(j, __ldg(row + j));
+      for (int j = threadIdx.x; j < n; j += kST) {
+        const float x = __ldg(lg + (size_t)i0 * a.V + v0 + j);
+        if (!isfinite(x)) bad = true;
+        if (better(x, v0 + j, bv[0], bi[0])) { bv[0] = x; bi[0] = v0 + j; }
+      }
     }
-    block_argmax(bv, bi, sv, si);
-    if (threadIdx.x == 0) { s_v[i] = bv; s_i[i] = bi; }
+    // block argmax of every position of the group: warps, then one warp each
+#pragma unroll
+    for (int t = 0; t < kGreedyGroup; ++t) {
+      if (t < gi) {
+        float v = bv[t];
+        int i = bi[t];
+        warp_argmax(v, i);
+        if (lane == 0) { wv[t][warp] = v; wi[t][warp] = i; }
+      }
+    }
+    __syncthreads();
+    if (warp < gi) {
+      float v = lane < kST / 32 ? wv[warp][lane] : -INFINITY;
+      int i = lane < kST / 32 ? wi[warp][lane] : 0x7FFFFFFF;
+      warp_argmax(v, i);
+      if (lane == 0) { s_v[i0 + warp] = v; s_i[i0 + warp] = i; }
+    }
+    __syncthreads();
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
   cl.sync();
-  if (rank == 0 && threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    // lane i < d+1 combines position i over the cluster
+  if (rank == 0 && warp == 0) {
+    // lane i <= d combines position i over the cluster
     int am = 0x7FFFFFFF;
     if (lane <= d) {
       float gv = -INFINITY;
-      for (int q = 0; q < kClusterCTAs; ++q) {
+      for (int q = 0; q < nc; ++q) {
         const float v = *cl.map_shared_rank(&s_v[lane], q);
         const int id = *cl.map_shared_rank(&s_i[lane], q);
         if (better(v, id, gv, am)) { gv = v; am = id; }
       }
     }
-    // the chain needs every position's argmax in one lane: gather them
-    int amax[kGreedyMaxPos];
-#pragma unroll
-    for (int i = 0; i < kGreedyMaxPos; ++i) amax[i] = __shfl_sync(0xFFFFFFFFu, am, i);
+    const int32_t* dr = a.drafts + (size_t)r * d;
+    // accepted prefix: drafts x_i (i = 1..d) equal to the argmax of row i-1
+    const int x = lane < d ? dr[lane] : -1;
+    const bool match = lane < d && x >= 0 && x < a.V && x == am;
+    const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < d && !match);
+    const int nacc = miss ? __ffs(miss) - 1 : d;
+    const int y = __shfl_sync(0xFFFFFFFFu, am, nacc);
+    if (lane <= d) a.out_tok[(size_t)r * (d + 1) + lane] = lane < nacc ? x : (lane == nacc ? y : -1);
     if (lane == 0) {
-      const int32_t* dr = a.drafts + (size_t)r * d;
-      int nacc = 0;
-      for (int i = 1; i <= d; ++i) {
-        const int x = dr[i - 1];
-        if (x < 0 || x >= a.V || x != amax[i - 1]) break;
-        nacc = i;
-      }
       a.n_acc[r] = nacc;
-      int32_t* o = a.out_tok + (size_t)r * (d + 1);
-      for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? amax[nacc] : -1);
       if (a.stats) {
         int32_t* st = a.stats + (size_t)r * (d + 2);
         st[0] += 1;
@@ -1455,20 +1488,34 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
 
 void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verify, a, a.rows, a.V, s); }
 
-void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s) {
+void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
+  VerifyArgs a = a0;
+  a.vec_ok = (a.V % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0) ? 1 : 0;
+  static int wide = -1;  // 16-CTA clusters schedulable on this device (checked once)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.rows * kClusterCTAs);
   cfg.blockDim = dim3(kST);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterCTAs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  if (wide < 0) {
+    wide = 0;
+    if (cudaFuncSetAttribute(k_verify_greedy, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      int nclusters = 0;
+      cfg.gridDim = dim3(16);
+      attr[0].val.clusterDim.x = 16;
+      if (cudaOccupancyMaxActiveClusters(&nclusters, k_verify_greedy, &cfg) == cudaSuccess && nclusters > 0) wide = 1;
+    }
+    cudaGetLastError();
+  }
+  const int nc = wide ? 16 : kClusterCTAs;
+  cfg.gridDim = dim3(a.rows * nc);
+  attr[0].val.clusterDim.x = nc;
   cudaLaunchKernelEx(&cfg, k_verify_greedy, a);
   count_launch();
 }

@@ -21,6 +21,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Prefetch a 2-D tile into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand in 128B-swizzled 8-row x
 // 128-byte atoms (stride between 8-row groups 1024 bytes).
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
