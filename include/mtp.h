@@ -203,8 +203,11 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth,
  *   d_n_acc [rows] out, d_out_tok [rows][depth+1] out (accepted drafts, then y,
  *   then -1), d_stats [rows][depth+2] int32 accumulated (NULL to skip):
  *   [0] rounds, [1] rounds with a rejection (rollbacks), [1+i] accepts at i.
- *   h_out (optional, pinned host, [rows][depth+2]): copy of n_acc then out_tok
- *   per row, enqueued after the kernel: the round's one device->host read.
+ *   h_out (optional, pinned host, [rows][depth+2]): n_acc then out_tok per row,
+ *   the round's one device->host read. Page-locked memory the device can
+ *   address (cudaHostAlloc / cudaMallocHost) is written by the verify kernel
+ *   itself; other host memory gets a copy enqueued after the kernel. Either
+ *   way it is complete once the stream has reached the end of this call.
  *   d_workspace: spec_verify_workspace_bytes(rows, depth, vocab) bytes.
  * Errors: BAD_ARG.
  */

@@ -14,8 +14,11 @@
 // activations (fp32) in shared memory and accumulates in fp32.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace mtp {
 
@@ -99,22 +102,22 @@ __device__ __forceinline__ void gemv_fma(float (&acc)[RPW][MT], const uint4 (&w)
   }
 }
 
-// Block-reduce MT partial sums at once (one barrier round; 256 threads);
+// Block-reduce MT partial sums at once (one barrier round);
 // every thread gets all MT totals, each summed in a fixed order.
 template <int MT>
-__device__ __forceinline__ void block_sum_n(float (&v)[MT], float* red /* >= 8 * MT */) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ void block_sum_n(float (&v)[MT], float* red /* >= 32 * MT */) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
   for (int m = 0; m < MT; ++m) v[m] = warp_sum(v[m]);
   __syncthreads();
   if (lane == 0)
 #pragma unroll
-    for (int m = 0; m < MT; ++m) red[m * 8 + w] = v[m];
+    for (int m = 0; m < MT; ++m) red[m * 32 + w] = v[m];
   __syncthreads();
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     float t = 0.f;
-    for (int k = 0; k < 8; ++k) t += red[m * 8 + k];
+    for (int k = 0; k < nw; ++k) t += red[m * 32 + k];
     v[m] = t;
   }
   __syncthreads();
@@ -205,6 +208,91 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
     for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
 }
 
+// Split-K combine and epilogue of one block group, shared by the GEMV
+// kernels. s_out[m][l] holds this block's partial of row group*ROWS + l for
+// item m; every thread of the block calls it.
+template <int MT, int ROWS>
+__device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, int split, int* s_last_p) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int& s_last = *s_last_p;
+  // Deterministic split-K: every split stores its partial; the last block of
+  // the group sums them in split order.
+  if (a.S > 1) {
+    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+      const int m = t / ROWS, l = t - m * ROWS;
+      a.part[((size_t)split * MT + m) * a.N + (size_t)group * ROWS + l] = s_out[m][l];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&a.counters[group], 1) == a.S - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+      const int m = t / ROWS, l = t - m * ROWS;
+      float sum = 0.f;
+      for (int s = 0; s < a.S; ++s) sum += __ldcg(&a.part[((size_t)s * MT + m) * a.N + (size_t)group * ROWS + l]);
+      s_out[m][l] = sum;
+    }
+    if (tid == 0) a.counters[group] = 0;
+    __syncthreads();
+  }
+
+  if (a.epi == EPI_SWIGLU) {
+    constexpr int HALF = ROWS / 2;
+    for (int t = tid; t < a.M * HALF; t += blockDim.x) {
+      const int m = t / HALF, l = t - m * HALF;
+      const float g = s_out[m][l], u = s_out[m][l + HALF];
+      a.y[(size_t)m * a.ldy + (size_t)group * HALF + l] = g / (1.f + expf(-g)) * u;
+    }
+    return;
+  }
+  for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+    const int m = t / ROWS, l = t - m * ROWS;
+    const size_t n = (size_t)group * ROWS + l;
+    float v = s_out[m][l];
+    if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + n];
+    a.y[(size_t)m * a.ldy + n] = v;
+    if (a.epi == EPI_LOGITS && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
+  }
+  if (a.epi != EPI_LOGITS) return;
+
+  // Group argmax (value desc, id asc) per item, then the last group block
+  // reduces all groups into the token.
+  if (warp < a.M) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int l = lane; l < ROWS; l += 32) {
+      const float v = s_out[warp][l];
+      const int i = group * ROWS + l;
+      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      a.gmax[(size_t)warp * a.ngroups + group] = bv;
+      a.gidx[(size_t)warp * a.ngroups + group] = bi;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.done, 1) == a.ngroups - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < a.M) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int g = lane; g < a.ngroups; g += 32) {
+      const float v = __ldcg(&a.gmax[(size_t)warp * a.ngroups + g]);
+      const int i = __ldcg(&a.gidx[(size_t)warp * a.ngroups + g]);
+      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[warp]] = bi;
+  }
+  if (tid == 0) *a.done = 0;
+}
+
 template <typename WT, int MT>
 __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArgs a) {
   constexpr int VN = Vec<WT>::N;
@@ -212,7 +300,7 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   constexpr int ROWS = 8 * RPW;
   extern __shared__ __align__(16) float xs[];
   __shared__ float s_out[MT][ROWS];
-  __shared__ float s_red[8 * MT > 32 ? 8 * MT : 32];
+  __shared__ float s_red[32 * MT];
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -301,82 +389,7 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   }
   __syncthreads();
 
-  // Deterministic split-K: every split stores its partial; the last block of
-  // the group sums them in split order.
-  if (a.S > 1) {
-    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
-      const int m = t / ROWS, l = t - m * ROWS;
-      a.part[((size_t)split * MT + m) * a.N + (size_t)group * ROWS + l] = s_out[m][l];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&a.counters[group], 1) == a.S - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
-      const int m = t / ROWS, l = t - m * ROWS;
-      float sum = 0.f;
-      for (int s = 0; s < a.S; ++s) sum += __ldcg(&a.part[((size_t)s * MT + m) * a.N + (size_t)group * ROWS + l]);
-      s_out[m][l] = sum;
-    }
-    if (tid == 0) a.counters[group] = 0;
-    __syncthreads();
-  }
-
-  if (a.epi == EPI_SWIGLU) {
-    constexpr int HALF = ROWS / 2;
-    for (int t = tid; t < a.M * HALF; t += blockDim.x) {
-      const int m = t / HALF, l = t - m * HALF;
-      const float g = s_out[m][l], u = s_out[m][l + HALF];
-      a.y[(size_t)m * a.ldy + (size_t)group * HALF + l] = g / (1.f + expf(-g)) * u;
-    }
-    return;
-  }
-  for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
-    const int m = t / ROWS, l = t - m * ROWS;
-    const size_t n = (size_t)group * ROWS + l;
-    float v = s_out[m][l];
-    if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + n];
-    a.y[(size_t)m * a.ldy + n] = v;
-    if (a.epi == EPI_LOGITS && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
-  }
-  if (a.epi != EPI_LOGITS) return;
-
-  // Group argmax (value desc, id asc) per item, then the last group block
-  // reduces all groups into the token.
-  if (warp < a.M) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int l = lane; l < ROWS; l += 32) {
-      const float v = s_out[warp][l];
-      const int i = group * ROWS + l;
-      if (better(v, i, bv, bi)) { bv = v; bi = i; }
-    }
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      a.gmax[(size_t)warp * a.ngroups + group] = bv;
-      a.gidx[(size_t)warp * a.ngroups + group] = bi;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.done, 1) == a.ngroups - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (warp < a.M) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int g = lane; g < a.ngroups; g += 32) {
-      const float v = __ldcg(&a.gmax[(size_t)warp * a.ngroups + g]);
-      const int i = __ldcg(&a.gidx[(size_t)warp * a.ngroups + g]);
-      if (better(v, i, bv, bi)) { bv = v; bi = i; }
-    }
-    warp_argmax(bv, bi);
-    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[warp]] = bi;
-  }
-  if (tid == 0) *a.done = 0;
+  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last);
 }
 
 template <typename WT, int MT>
@@ -394,6 +407,171 @@ void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
     case 2: bf ? launch_gemv_t<uint16_t, 2>(a, smem, s) : launch_gemv_t<float, 2>(a, smem, s); break;
     case 4: bf ? launch_gemv_t<uint16_t, 4>(a, smem, s) : launch_gemv_t<float, 4>(a, smem, s); break;
     default: bf ? launch_gemv_t<uint16_t, 8>(a, smem, s) : launch_gemv_t<float, 8>(a, smem, s); break;
+  }
+}
+
+// --------------------------------------------- GEMV fed by TMA (bf16 weights)
+//
+// Same contraction, prologue and epilogue as k_gemv, but the weight rows come
+// through a ring of shared-memory stages that a producer warp fills with 2-D
+// TMA copies (64 rows x 256 columns, 32 KB per stage), so each SM keeps up to
+// six stages (192 KB) of the weight stream in flight without holding them in
+// registers. The first stages are requested before the previous kernel has
+// finished (the weights do not depend on it). Warps 0-7 compute: warp w owns
+// rows 8w..8w+7 of the block's 64, lane l the columns 8l..8l+7 of a stage.
+constexpr int kTmaCols = 256;
+constexpr int kTmaRows = 64;
+constexpr uint32_t kTmaStageBytes = kTmaRows * kTmaCols * 2;
+
+template <int MT>
+__global__ void __launch_bounds__(288, 1)
+    k_gemv_tma(const __grid_constant__ CUtensorMap t0, const __grid_constant__ CUtensorMap t1,
+               const __grid_constant__ CUtensorMap t2, const __grid_constant__ GemvArgs a, int stages) {
+  constexpr int ROWS = kTmaRows;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int KS = a.K / a.S;
+  float* xs = reinterpret_cast<float*>(ring + (size_t)stages * kTmaStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xs + MT * KS);
+  uint64_t* empty = full + stages;
+  __shared__ float s_out[MT][ROWS];
+  __shared__ float s_red[32 * MT];
+  __shared__ int s_last, s_fail;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = blockIdx.x / a.S, split = blockIdx.x - group * a.S;
+  const int k0 = split * KS, nst = KS / kTmaCols;
+  const CUtensorMap* tm = &t0;
+  int row0 = group * ROWS;
+  if (a.epi == EPI_SWIGLU) {
+    row0 = group * (ROWS / 2);  // 32 gate rows (t0) then the matching 32 up rows (t1)
+  } else {
+    int sg = 0, start = 0;
+    while (sg < 2 && group * ROWS >= a.seg_end[sg]) { start = a.seg_end[sg]; ++sg; }
+    tm = sg == 0 ? &t0 : (sg == 1 ? &t1 : &t2);
+    row0 = group * ROWS - start;
+  }
+  auto load = [&](int slot, int i) {
+    uint8_t* dst = ring + (size_t)slot * kTmaStageBytes;
+    const int x = k0 + i * kTmaCols;
+    if (a.epi == EPI_SWIGLU) {
+      tc::tma_load_2d(smem_u32(dst), &t0, x, row0, smem_u32(&full[slot]));
+      tc::tma_load_2d(smem_u32(dst + kTmaStageBytes / 2), &t1, x, row0, smem_u32(&full[slot]));
+    } else {
+      tc::tma_load_2d(smem_u32(dst), tm, x, row0, smem_u32(&full[slot]));
+    }
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 8);
+    }
+    s_fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool producer = warp == 8;
+  if (producer && lane == 0) {
+    for (int i = 0; i < min(nst, stages); ++i) {
+      mbar_expect_tx(smem_u32(&full[i]), kTmaStageBytes);
+      load(i, i);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  gemv_prologue<MT>(a, xs, k0, KS, s_red);
+  __syncthreads();
+
+  if (!producer) {
+    float acc[8][MT];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+    for (int i = 0; i < nst; ++i) {
+      const int slot = i % stages;
+      if (!mbar_wait(smem_u32(&full[slot]), (i / stages) & 1)) { s_fail = 1; break; }
+      const uint8_t* st = ring + (size_t)slot * kTmaStageBytes;
+      float xv[MT][8];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float4* xp = reinterpret_cast<const float4*>(xs + m * KS + i * kTmaCols + 8 * lane);
+        const float4 u0 = xp[0], u1 = xp[1];
+        xv[m][0] = u0.x; xv[m][1] = u0.y; xv[m][2] = u0.z; xv[m][3] = u0.w;
+        xv[m][4] = u1.x; xv[m][5] = u1.y; xv[m][6] = u1.z; xv[m][7] = u1.w;
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)(warp * 8 + r) * (kTmaCols * 2) + 16 * lane);
+        const float wf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                             bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          float t = acc[r][m];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t = fmaf(wf[j], xv[m][j], t);
+          acc[r][m] = t;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const float t = warp_sum(acc[r][m]);
+        if (lane == 0) s_out[m][warp * 8 + r] = t;
+      }
+  } else if (lane == 0) {
+    // refill slot i % stages with stage i once the 8 compute warps released it
+    for (int i = stages; i < nst; ++i) {
+      const int slot = i % stages;
+      if (!mbar_wait(smem_u32(&empty[slot]), ((i / stages) - 1) & 1)) { s_fail = 1; break; }
+      mbar_expect_tx(smem_u32(&full[slot]), kTmaStageBytes);
+      load(slot, i);
+    }
+  }
+  __syncthreads();
+  if (s_fail) {
+    if (tid == 0) {
+      flag_status(a.status, MTP_ERR_TIMEOUT);
+      for (int i = 0; i < stages; ++i) mbar_wait(smem_u32(&full[i]), 0);  // let copies land before exit
+    }
+    return;
+  }
+  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last);
+}
+
+template <int MT>
+static bool launch_gemv_tma_t(const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s) {
+  const CUtensorMap* tm = static_cast<const CUtensorMap*>(maps);
+  auto k = k_gemv_tma<MT>;
+  static int set_smem = 0;
+  if (smem > set_smem) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+    set_smem = smem;
+  }
+  const cudaError_t e = launch_pdl(k, dim3(a.ngroups * a.S), dim3(288), (size_t)smem, s, tm[0], tm[1], tm[2], a, stages);
+  count_launch();
+  return e == cudaSuccess;
+}
+
+int gemv_tma_smem(int mt, int K, int S, int* stages) {
+  const int ks = K / S;
+  const int fixed = mt * ks * 4 + 1024 + 2 * 6 * 8;
+  const int st = std::min(6, (227 * 1024 - fixed) / (int)kTmaStageBytes);
+  *stages = st;
+  return st >= 2 ? fixed + st * (int)kTmaStageBytes : -1;
+}
+
+bool launch_gemv_tma(int mt, const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s) {
+  switch (mt) {
+    case 1: return launch_gemv_tma_t<1>(a, maps, stages, smem, s);
+    case 2: return launch_gemv_tma_t<2>(a, maps, stages, smem, s);
+    case 4: return launch_gemv_tma_t<4>(a, maps, stages, smem, s);
+    default: return false;
   }
 }
 

@@ -54,6 +54,12 @@ struct GemvArgs {
 // rows per block group for a batch width MT
 inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
+// The same GEMV with the weights streamed by TMA (bf16, mt <= 4, K/S a multiple
+// of 256 columns). maps: three CUtensorMap (64-row boxes; 32-row boxes of gate
+// and up for SwiGLU). gemv_tma_smem: dynamic shared memory (-1: does not fit)
+// and the ring depth.
+int gemv_tma_smem(int mt, int K, int S, int* stages);
+bool launch_gemv_tma(int mt, const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.
 struct QkvPostArgs {
@@ -247,6 +253,7 @@ struct VerifyArgs {
   int32_t* stats;
   int32_t* status;
   int vec_ok;  // logits rows 16-byte aligned (set by the greedy launcher)
+  int32_t* h_rec;  // device-visible [rows][depth+2] host record (n_acc, out_tok), or null
   RowParams p[kMaxRows];
 };
 void launch_verify(const VerifyArgs& a, cudaStream_t s);

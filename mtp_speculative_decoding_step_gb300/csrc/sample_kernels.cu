@@ -1299,6 +1299,11 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
     a.n_acc[r] = nacc;
     int32_t* o = a.out_tok + (size_t)r * (d + 1);
     for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
+    if (a.h_rec) {
+      int32_t* hr = a.h_rec + (size_t)r * (d + 2);
+      hr[0] = nacc;
+      for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+    }
     if (a.stats) {
       int32_t* s = a.stats + (size_t)r * (d + 2);
       s[0] += 1;
@@ -1427,9 +1432,14 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
     const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < d && !match);
     const int nacc = miss ? __ffs(miss) - 1 : d;
     const int y = __shfl_sync(0xFFFFFFFFu, am, nacc);
-    if (lane <= d) a.out_tok[(size_t)r * (d + 1) + lane] = lane < nacc ? x : (lane == nacc ? y : -1);
+    const int ov = lane < nacc ? x : (lane == nacc ? y : -1);
+    if (lane <= d) {
+      a.out_tok[(size_t)r * (d + 1) + lane] = ov;
+      if (a.h_rec) a.h_rec[(size_t)r * (d + 2) + 1 + lane] = ov;
+    }
     if (lane == 0) {
       a.n_acc[r] = nacc;
+      if (a.h_rec) a.h_rec[(size_t)r * (d + 2)] = nacc;
       if (a.stats) {
         int32_t* st = a.stats + (size_t)r * (d + 2);
         st[0] += 1;
