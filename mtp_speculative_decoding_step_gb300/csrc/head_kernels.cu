@@ -764,52 +764,61 @@ void launch_qkv_post(const QkvPostArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------- decode attention
 
-// One block per (chunk of kAttnChunk slots, kv head, head item). Thread 0
-// copies the chunk's K and V rows (contiguous in the cache) into shared memory
-// as 64-slot tiles with bulk asynchronous copies; the block then computes the
-// scores of the G query heads of the group against each tile, keeps an online
-// softmax, and accumulates P.V with one thread per head dimension. Partials
-// (o, running max, running sum) are merged by k_attn_merge.
+// One block per (chunk of a.chunk slots, kv head, head item). Thread 0 streams
+// the chunk's K and V rows (contiguous in the cache) through a ring of NS
+// shared-memory stages of 64 slots with bulk asynchronous copies, so the next
+// tiles load while the block computes the scores of the G query heads of the
+// group against the current one, keeps an online softmax, and accumulates P.V
+// with one thread per head dimension. Partials (o, running max, running sum)
+// are merged by k_attn_merge.
+template <int DH, typename KT>
+struct AttnRing {
+  static constexpr int TS = 64;
+  static constexpr int kTileBytes = 2 * TS * DH * (int)sizeof(KT);
+  static constexpr int NS = (200 * 1024) / kTileBytes >= 3 ? 3 : ((200 * 1024) / kTileBytes >= 2 ? 2 : 1);
+};
+
 template <int DH, int G, typename KT>
 __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ AttnArgs a) {
-  constexpr int TS = 64;
-  constexpr int NT = kAttnChunk / TS;
+  constexpr int TS = AttnRing<DH, KT>::TS;
+  constexpr int NS = AttnRing<DH, KT>::NS;
   constexpr int EPL = DH / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   KT* ks = reinterpret_cast<KT*>(smem);
-  KT* vs = ks + NT * TS * DH;
-  float* qs = reinterpret_cast<float*>(vs + NT * TS * DH);
+  KT* vs = ks + NS * TS * DH;
+  float* qs = reinterpret_cast<float*>(vs + NS * TS * DH);
   float* ps = qs + G * DH;          // [G][TS]
   float* st = ps + G * TS;          // [G][4]: running max, alpha, running sum
   uint64_t* bar = reinterpret_cast<uint64_t*>(st + 4 * 8);
 
   const int c = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
   const int L = a.slot[m] + 1;
-  const int t0 = c * kAttnChunk;
+  const int t0 = c * a.chunk;
   if (t0 >= L) return;
-  const int n = min(kAttnChunk, L - t0);
+  const int n = min(a.chunk, L - t0);
   const int nt = (n + TS - 1) / TS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int i = 0; i < NT; ++i) mbar_init(smem_u32(&bar[i]), 1);
+    for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&bar[i]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < G) { st[4 * tid] = -INFINITY; st[4 * tid + 1] = 0.f; st[4 * tid + 2] = 0.f; }
   __syncthreads();
   pdl_wait();  // the cache rows of this call's new slots come from k_qkv_post
   const size_t base = (((size_t)a.row[m] * a.nkv + g) * a.cap + t0) * DH;
-  if (tid == 0) {
-    for (int i = 0; i < nt; ++i) {
-      const int rows = min(TS, n - i * TS);
-      const uint32_t bytes = (uint32_t)(rows * DH * sizeof(KT));
-      mbar_expect_tx(smem_u32(&bar[i]), 2 * bytes);
-      bulk_g2s(smem_u32(ks + i * TS * DH), reinterpret_cast<const KT*>(a.kc) + base + (size_t)i * TS * DH, bytes,
-               smem_u32(&bar[i]));
-      bulk_g2s(smem_u32(vs + i * TS * DH), reinterpret_cast<const KT*>(a.vc) + base + (size_t)i * TS * DH, bytes,
-               smem_u32(&bar[i]));
-    }
-  }
+  auto issue = [&](int i) {  // tile i into ring slot i % NS
+    const int slot = i % NS;
+    const int rows = min(TS, n - i * TS);
+    const uint32_t bytes = (uint32_t)(rows * DH * sizeof(KT));
+    mbar_expect_tx(smem_u32(&bar[slot]), 2 * bytes);
+    bulk_g2s(smem_u32(ks + slot * TS * DH), reinterpret_cast<const KT*>(a.kc) + base + (size_t)i * TS * DH, bytes,
+             smem_u32(&bar[slot]));
+    bulk_g2s(smem_u32(vs + slot * TS * DH), reinterpret_cast<const KT*>(a.vc) + base + (size_t)i * TS * DH, bytes,
+             smem_u32(&bar[slot]));
+  };
+  if (tid == 0)
+    for (int i = 0; i < min(nt, NS); ++i) issue(i);
   pdl_trigger();
   const float* qg = a.q + (size_t)m * a.nq * DH + (size_t)g * G * DH;
   float qr[G][EPL];
@@ -822,10 +831,14 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
 #pragma unroll
   for (int h = 0; h < G; ++h) o[h] = 0.f;
   bool ok = true;
+  int issued = min(nt, NS);
   for (int i = 0; i < nt; ++i) {
     const int rows = min(TS, n - i * TS);
-    const bool got = mbar_wait(smem_u32(&bar[i]), 0);
+    const int slot = i % NS;
+    const bool got = mbar_wait(smem_u32(&bar[slot]), (i / NS) & 1);
     if (__syncthreads_or(!got)) { ok = false; break; }
+    const KT* kt = ks + slot * TS * DH;
+    const KT* vt = vs + slot * TS * DH;
     // scores: warp w takes keys 8w..8w+7 of the tile; lane owns EPL dims of
     // every key; the 8 keys x 8 head slots of partial dots are reduced across
     // the warp by a halving butterfly (62 shuffles), leaving lane l with the
@@ -837,7 +850,7 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
       for (int kk = 0; kk < 8; ++kk) {
         float kv[EPL];
         const int j = kb + kk < rows ? kb + kk : rows - 1;
-        const KT* kr = ks + (size_t)(i * TS + j) * DH + lane * EPL;
+        const KT* kr = kt + (size_t)j * DH + lane * EPL;
 #pragma unroll
         for (int e = 0; e < EPL; ++e)
           kv[e] = sizeof(KT) == 2 ? bf16_to_f(((const uint16_t*)kr)[e]) : ((const float*)kr)[e];
@@ -895,7 +908,7 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
       float acc[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[h] = o[h] * st[4 * h + 1];
-      const KT* vr = vs + (size_t)i * TS * DH + d;
+      const KT* vr = vt + d;
       int j = 0;
       for (; j + 4 <= rows; j += 4) {
         float vv[4];
@@ -917,12 +930,15 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
 #pragma unroll
       for (int h = 0; h < G; ++h) o[h] = acc[h];
     }
-    __syncthreads();
+    __syncthreads();  // every thread is done with this slot: refill it
+    if (tid == 0 && issued < nt) issue(issued);
+    issued = min(nt, issued + 1);
   }
   if (!ok) {
     if (tid == 0) {
       flag_status(a.status, MTP_ERR_TIMEOUT);
-      for (int i = 0; i < nt; ++i) mbar_wait(smem_u32(&bar[i]), 0);  // let copies land before exit
+      // let the copies in flight land before exit: the last tile issued into each slot
+      for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(smem_u32(&bar[j % NS]), (j / NS) & 1);
     }
     return;
   }
@@ -949,7 +965,7 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
   pdl_wait();
   pdl_trigger();
   const int L = a.slot[m] + 1;
-  const int nch = (L + kAttnChunk - 1) / kAttnChunk;
+  const int nch = (L + a.chunk - 1) / a.chunk;
   const size_t hq = (size_t)m * a.nq + h;
   const float* ml = a.pml + hq * a.max_chunks * 2;
   float mx = -INFINITY;
@@ -984,19 +1000,34 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
 
 template <int DH, int G, typename KT>
 static void attn_t(const AttnArgs& a, int nch, cudaStream_t s) {
-  constexpr int TS = 64, NT = kAttnChunk / TS;
-  const size_t smem = 2 * (size_t)NT * TS * DH * sizeof(KT) + (size_t)(G * DH + G * TS + 32) * sizeof(float) + 64;
+  constexpr int TS = AttnRing<DH, KT>::TS, NS = AttnRing<DH, KT>::NS;
+  const size_t smem = 2 * (size_t)NS * TS * DH * sizeof(KT) + (size_t)(G * DH + G * TS + 32) * sizeof(float) + 64;
   auto k = k_attn_chunk<DH, G, KT>;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set = true;
+  }
   launch_pdl(k, dim3(nch, a.nkv, a.Mh), dim3(256), smem, s, a);
   launch_pdl(k_attn_merge<DH>, dim3(a.nq, a.Mh), dim3(DH), (size_t)a.max_chunks * sizeof(float), s, a);
   count_launch(2);
 }
 
-void launch_attention(const AttnArgs& a, cudaStream_t s) {
+void launch_attention(const AttnArgs& a0, int sms, cudaStream_t s) {
+  AttnArgs a = a0;
   int maxL = 0;
-  for (int m = 0; m < a.Mh; ++m) maxL = a.slot[m] + 1 > maxL ? a.slot[m] + 1 : maxL;
-  const int nch = (maxL + kAttnChunk - 1) / kAttnChunk;
+  long long total = 0;
+  for (int m = 0; m < a.Mh; ++m) {
+    maxL = a.slot[m] + 1 > maxL ? a.slot[m] + 1 : maxL;
+    total += a.slot[m] + 1;
+  }
+  // slots per block: the whole job spread over about two blocks per SM, in
+  // whole 64-slot tiles, never below kAttnChunk (the partial buffers' unit)
+  const long long per = (total * a.nkv + 2LL * sms - 1) / (2LL * sms);
+  int chunk = (int)((per + 63) / 64 * 64);
+  if (chunk < kAttnChunk) chunk = kAttnChunk;
+  a.chunk = chunk;
+  const int nch = (maxL + chunk - 1) / chunk;
   const int G = a.nq / a.nkv;
   const bool bf = a.wdt == MTP_DTYPE_BF16;
 #define MTP_ATTN_CASE(DHV, GV)                                                \

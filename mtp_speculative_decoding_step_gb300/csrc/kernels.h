@@ -12,7 +12,7 @@ void count_launch(int n = 1);
 
 constexpr int kMaxItems = 256;   // pairs per head call (the pages' flush cap)
 constexpr int kMaxRows = 64;
-constexpr int kAttnChunk = 128;  // KV slots per decode-attention block
+constexpr int kAttnChunk = 128;  // smallest KV slot range of a decode-attention block
 constexpr int kClusterCTAs = 8;  // CTAs per sampling cluster
 
 enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_DUAL = 2 };
@@ -173,6 +173,7 @@ struct AttnArgs {
   const void* vc;
   long long cap;
   int Mh, nq, nkv, dh, wdt, max_chunks;
+  int chunk;             // slots per block (a multiple of 64, >= kAttnChunk; set by the launcher)
   float scale;
   float* po;             // [Mh][nq][max_chunks][dh]
   float* pml;            // [Mh][nq][max_chunks][2]
@@ -181,7 +182,7 @@ struct AttnArgs {
   int row[kMaxRows];
   int slot[kMaxRows];
 };
-void launch_attention(const AttnArgs& a, cudaStream_t s);
+void launch_attention(const AttnArgs& a, int sms, cudaStream_t s);
 
 // Copy a norm vector to fp32 adding `shift`.
 void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, cudaStream_t s);

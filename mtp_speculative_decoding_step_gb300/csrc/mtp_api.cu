@@ -446,7 +446,7 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
       a.scale = 1.0f / std::sqrt((float)c.head_dim);
       a.po = h->po; a.pml = h->pml; a.o = h->o + (size_t)m0 * qw; a.status = h->status;
       for (int m = 0; m < mp; ++m) { a.row[m] = it.row[m0 + m]; a.slot[m] = it.slot[m0 + m]; }
-      launch_attention(a, s);
+      launch_attention(a, h->sms, s);
     }
   }
   GemvJob j;
