@@ -414,17 +414,18 @@ void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
 //
 // Same contraction, prologue and epilogue as k_gemv, but the weight rows come
 // through a ring of shared-memory stages that a producer warp fills with 2-D
-// TMA copies (64 rows x 256 columns, 32 KB per stage), so each SM keeps up to
-// six stages (192 KB) of the weight stream in flight without holding them in
+// TMA copies (64 rows x 128 columns, 16 KB per stage); two blocks fit on an SM,
+// so one block's start-up and drain overlap the other's stream, and each SM
+// keeps up to ten stages (160 KB) of weights in flight without holding them in
 // registers. The first stages are requested before the previous kernel has
 // finished (the weights do not depend on it). Warps 0-7 compute: warp w owns
-// rows 8w..8w+7 of the block's 64, lane l the columns 8l..8l+7 of a stage.
-constexpr int kTmaCols = 256;
+// rows 8w..8w+7 of the block's 64, lane l the columns 4l..4l+3 of a stage.
+constexpr int kTmaCols = 128;
 constexpr int kTmaRows = 64;
 constexpr uint32_t kTmaStageBytes = kTmaRows * kTmaCols * 2;
 
 template <int MT>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(288, 2)
     k_gemv_tma(const __grid_constant__ CUtensorMap t0, const __grid_constant__ CUtensorMap t1,
                const __grid_constant__ CUtensorMap t2, const __grid_constant__ GemvArgs a, int stages) {
   constexpr int ROWS = kTmaRows;
@@ -493,24 +494,21 @@ __global__ void __launch_bounds__(288, 1)
       const int slot = i % stages;
       if (!mbar_wait(smem_u32(&full[slot]), (i / stages) & 1)) { s_fail = 1; break; }
       const uint8_t* st = ring + (size_t)slot * kTmaStageBytes;
-      float xv[MT][8];
+      float xv[MT][4];
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
-        const float4* xp = reinterpret_cast<const float4*>(xs + m * KS + i * kTmaCols + 8 * lane);
-        const float4 u0 = xp[0], u1 = xp[1];
+        const float4 u0 = *reinterpret_cast<const float4*>(xs + m * KS + i * kTmaCols + 4 * lane);
         xv[m][0] = u0.x; xv[m][1] = u0.y; xv[m][2] = u0.z; xv[m][3] = u0.w;
-        xv[m][4] = u1.x; xv[m][5] = u1.y; xv[m][6] = u1.z; xv[m][7] = u1.w;
       }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)(warp * 8 + r) * (kTmaCols * 2) + 16 * lane);
-        const float wf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                             bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+        const uint2 w = *reinterpret_cast<const uint2*>(st + (size_t)(warp * 8 + r) * (kTmaCols * 2) + 8 * lane);
+        const float wf[4] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y)};
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           float t = acc[r][m];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) t = fmaf(wf[j], xv[m][j], t);
+          for (int j = 0; j < 4; ++j) t = fmaf(wf[j], xv[m][j], t);
           acc[r][m] = t;
         }
       }
@@ -559,11 +557,12 @@ static bool launch_gemv_tma_t(const GemvArgs& a, const void* maps, int stages, i
 }
 
 int gemv_tma_smem(int mt, int K, int S, int* stages) {
+  // two blocks per SM: each within half of the SM's 228 KB, less static use
   const int ks = K / S;
-  const int fixed = mt * ks * 4 + 1024 + 2 * 6 * 8;
-  const int st = std::min(6, (227 * 1024 - fixed) / (int)kTmaStageBytes);
+  const int fixed = mt * ks * 4 + 1024 + 2 * 8 * 8;
+  const int st = std::min(8, (110 * 1024 - fixed) / (int)kTmaStageBytes);
   *stages = st;
-  return st >= 2 ? fixed + st * (int)kTmaStageBytes : -1;
+  return st >= 3 ? fixed + st * (int)kTmaStageBytes : -1;
 }
 
 bool launch_gemv_tma(int mt, const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s) {

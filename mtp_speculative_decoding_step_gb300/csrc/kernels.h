@@ -55,7 +55,7 @@ struct GemvArgs {
 inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
 // The same GEMV with the weights streamed by TMA (bf16, mt <= 4, K/S a multiple
-// of 256 columns). maps: three CUtensorMap (64-row boxes; 32-row boxes of gate
+// of 128 columns). maps: three CUtensorMap (64-row boxes; 32-row boxes of gate
 // and up for SwiGLU). gemv_tma_smem: dynamic shared memory (-1: does not fit)
 // and the ring depth.
 int gemv_tma_smem(int mt, int K, int S, int* stages);

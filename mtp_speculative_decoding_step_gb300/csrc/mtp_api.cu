@@ -320,7 +320,7 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     a.amax_out = j.amax_out;
     a.status = h->status;
     int stages = 0;
-    const int tsmem = (j.tm && h->tma_gemv && pl.mt <= 4 && (j.K / pl.S) % 256 == 0)
+    const int tsmem = (j.tm && h->tma_gemv && pl.mt <= 4 && (j.K / pl.S) % 128 == 0)
                           ? gemv_tma_smem(pl.mt, j.K, pl.S, &stages) : -1;
     if (tsmem > 0 && launch_gemv_tma(pl.mt, a, j.tm, stages, tsmem, s)) continue;
     launch_gemv(pl.mt, a, pl.smem, s);
@@ -709,9 +709,9 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
     h->tc_gemv = st == MTP_OK;
     // TMA maps for the TMA-fed GEMV: 64-row boxes (32-row boxes of gate / up)
-    // of 256 columns, one per weight segment
+    // of 128 columns, one per weight segment
     auto mk = [&](CUtensorMap* m, const void* w, int rows, int cols, int box_rows) {
-      return tc::make_map_box(m, w, rows, cols, 256, box_rows);
+      return tc::make_map_box(m, w, rows, cols, 128, box_rows);
     };
     bool ok = true;
     auto three = [&](int id, const void* w0, int r0, const void* w1, int r1, const void* w2, int r2, int cols) {
