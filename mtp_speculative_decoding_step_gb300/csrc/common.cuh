@@ -175,10 +175,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 // Bounded wait on an mbarrier phase; false when the poll budget runs out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (unsigned i = 0; i < kWaitLimit; ++i)

@@ -174,11 +174,12 @@ static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, c
   return cudaGetLastError() == cudaSuccess;
 }
 
-// mh: 128-row halves per CTA (1 or 2); bn: 128, 160 (mh 1) or 256 (mh 2).
+// mh: 128-row halves per CTA (1 or 2); bn: 128, 160, 256 (mh 1) or 128, 256 (mh 2).
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
                     int ksplit, float* D, int32_t* status, cudaStream_t s, int mh) {
   if (mh == 2 && bn == 256) return tc_gemm_t<256, 3, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
   if (mh == 2) return tc_gemm_t<128, 4, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+  if (bn == 256) return tc_gemm_t<256, 4, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
   if (bn == 160) return tc_gemm_t<160, 5, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
   return tc_gemm_t<128, 6, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
 }

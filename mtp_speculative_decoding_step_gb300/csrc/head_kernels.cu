@@ -18,7 +18,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "tc_common.cuh"
 
 namespace mtp {
 
@@ -407,170 +406,6 @@ void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
     case 2: bf ? launch_gemv_t<uint16_t, 2>(a, smem, s) : launch_gemv_t<float, 2>(a, smem, s); break;
     case 4: bf ? launch_gemv_t<uint16_t, 4>(a, smem, s) : launch_gemv_t<float, 4>(a, smem, s); break;
     default: bf ? launch_gemv_t<uint16_t, 8>(a, smem, s) : launch_gemv_t<float, 8>(a, smem, s); break;
-  }
-}
-
-// --------------------------------------------- GEMV fed by TMA (bf16 weights)
-//
-// Same contraction, prologue and epilogue as k_gemv, but the weight rows come
-// through a ring of shared-memory stages that a producer warp fills with 2-D
-// TMA copies (64 rows x 128 columns, 16 KB per stage); two blocks fit on an SM,
-// so one block's start-up and drain overlap the other's stream, and each SM
-// keeps up to ten stages (160 KB) of weights in flight without holding them in
-// registers. The first stages are requested before the previous kernel has
-// finished (the weights do not depend on it). Warps 0-7 compute: warp w owns
-// rows 8w..8w+7 of the block's 64, lane l the columns 4l..4l+3 of a stage.
-constexpr int kTmaCols = 128;
-constexpr int kTmaRows = 64;
-constexpr uint32_t kTmaStageBytes = kTmaRows * kTmaCols * 2;
-
-template <int MT>
-__global__ void __launch_bounds__(288, 2)
-    k_gemv_tma(const __grid_constant__ CUtensorMap t0, const __grid_constant__ CUtensorMap t1,
-               const __grid_constant__ CUtensorMap t2, const __grid_constant__ GemvArgs a, int stages) {
-  constexpr int ROWS = kTmaRows;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int KS = a.K / a.S;
-  float* xs = reinterpret_cast<float*>(ring + (size_t)stages * kTmaStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(xs + MT * KS);
-  uint64_t* empty = full + stages;
-  __shared__ float s_out[MT][ROWS];
-  __shared__ float s_red[32 * MT];
-  __shared__ int s_last, s_fail;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int group = blockIdx.x / a.S, split = blockIdx.x - group * a.S;
-  const int k0 = split * KS, nst = KS / kTmaCols;
-  const CUtensorMap* tm = &t0;
-  int row0 = group * ROWS;
-  if (a.epi == EPI_SWIGLU) {
-    row0 = group * (ROWS / 2);  // 32 gate rows (t0) then the matching 32 up rows (t1)
-  } else {
-    int sg = 0, start = 0;
-    while (sg < 2 && group * ROWS >= a.seg_end[sg]) { start = a.seg_end[sg]; ++sg; }
-    tm = sg == 0 ? &t0 : (sg == 1 ? &t1 : &t2);
-    row0 = group * ROWS - start;
-  }
-  auto load = [&](int slot, int i) {
-    uint8_t* dst = ring + (size_t)slot * kTmaStageBytes;
-    const int x = k0 + i * kTmaCols;
-    if (a.epi == EPI_SWIGLU) {
-      tc::tma_load_2d(smem_u32(dst), &t0, x, row0, smem_u32(&full[slot]));
-      tc::tma_load_2d(smem_u32(dst + kTmaStageBytes / 2), &t1, x, row0, smem_u32(&full[slot]));
-    } else {
-      tc::tma_load_2d(smem_u32(dst), tm, x, row0, smem_u32(&full[slot]));
-    }
-  };
-
-  if (tid == 0) {
-    for (int i = 0; i < stages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), 8);
-    }
-    s_fail = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  const bool producer = warp == 8;
-  if (producer && lane == 0) {
-    for (int i = 0; i < min(nst, stages); ++i) {
-      mbar_expect_tx(smem_u32(&full[i]), kTmaStageBytes);
-      load(i, i);
-    }
-  }
-  pdl_wait();
-  pdl_trigger();
-  gemv_prologue<MT>(a, xs, k0, KS, s_red);
-  __syncthreads();
-
-  if (!producer) {
-    float acc[8][MT];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
-    for (int i = 0; i < nst; ++i) {
-      const int slot = i % stages;
-      if (!mbar_wait(smem_u32(&full[slot]), (i / stages) & 1)) { s_fail = 1; break; }
-      const uint8_t* st = ring + (size_t)slot * kTmaStageBytes;
-      float xv[MT][4];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const float4 u0 = *reinterpret_cast<const float4*>(xs + m * KS + i * kTmaCols + 4 * lane);
-        xv[m][0] = u0.x; xv[m][1] = u0.y; xv[m][2] = u0.z; xv[m][3] = u0.w;
-      }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint2 w = *reinterpret_cast<const uint2*>(st + (size_t)(warp * 8 + r) * (kTmaCols * 2) + 8 * lane);
-        const float wf[4] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y)};
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          float t = acc[r][m];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) t = fmaf(wf[j], xv[m][j], t);
-          acc[r][m] = t;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const float t = warp_sum(acc[r][m]);
-        if (lane == 0) s_out[m][warp * 8 + r] = t;
-      }
-  } else if (lane == 0) {
-    // refill slot i % stages with stage i once the 8 compute warps released it
-    for (int i = stages; i < nst; ++i) {
-      const int slot = i % stages;
-      if (!mbar_wait(smem_u32(&empty[slot]), ((i / stages) - 1) & 1)) { s_fail = 1; break; }
-      mbar_expect_tx(smem_u32(&full[slot]), kTmaStageBytes);
-      load(slot, i);
-    }
-  }
-  __syncthreads();
-  if (s_fail) {
-    if (tid == 0) {
-      flag_status(a.status, MTP_ERR_TIMEOUT);
-      for (int i = 0; i < stages; ++i) mbar_wait(smem_u32(&full[i]), 0);  // let copies land before exit
-    }
-    return;
-  }
-  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last);
-}
-
-template <int MT>
-static bool launch_gemv_tma_t(const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s) {
-  const CUtensorMap* tm = static_cast<const CUtensorMap*>(maps);
-  auto k = k_gemv_tma<MT>;
-  static int set_smem = 0;
-  if (smem > set_smem) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
-    set_smem = smem;
-  }
-  const cudaError_t e = launch_pdl(k, dim3(a.ngroups * a.S), dim3(288), (size_t)smem, s, tm[0], tm[1], tm[2], a, stages);
-  count_launch();
-  return e == cudaSuccess;
-}
-
-int gemv_tma_smem(int mt, int K, int S, int* stages) {
-  // two blocks per SM: each within half of the SM's 228 KB, less static use
-  const int ks = K / S;
-  const int fixed = mt * ks * 4 + 1024 + 2 * 8 * 8;
-  const int st = std::min(8, (110 * 1024 - fixed) / (int)kTmaStageBytes);
-  *stages = st;
-  return st >= 3 ? fixed + st * (int)kTmaStageBytes : -1;
-}
-
-bool launch_gemv_tma(int mt, const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s) {
-  switch (mt) {
-    case 1: return launch_gemv_tma_t<1>(a, maps, stages, smem, s);
-    case 2: return launch_gemv_tma_t<2>(a, maps, stages, smem, s);
-    case 4: return launch_gemv_tma_t<4>(a, maps, stages, smem, s);
-    default: return false;
   }
 }
 

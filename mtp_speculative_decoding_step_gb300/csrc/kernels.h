@@ -54,12 +54,6 @@ struct GemvArgs {
 // rows per block group for a batch width MT
 inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
-// The same GEMV with the weights streamed by TMA (bf16, mt <= 4, K/S a multiple
-// of 128 columns). maps: three CUtensorMap (64-row boxes; 32-row boxes of gate
-// and up for SwiGLU). gemv_tma_smem: dynamic shared memory (-1: does not fit)
-// and the ring depth.
-int gemv_tma_smem(int mt, int K, int S, int* stages);
-bool launch_gemv_tma(int mt, const GemvArgs& a, const void* maps, int stages, int smem, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.
 struct QkvPostArgs {

@@ -11,7 +11,6 @@
 
 #include "../../include/mtp.h"
 #include "kernels.h"
-#include "tc_common.cuh"
 
 using namespace mtp;
 
@@ -91,10 +90,6 @@ struct mtp_handle {
   uint16_t* x2 = nullptr;                 // hi/lo bf16 activations of the tensor-core GEMV
   float* tvpart = nullptr;                // its split-K partials
   bool tc_gemv = false;                   // batched GEMVs on tcgen05 (bf16 weights)
-  // TMA maps of every weight matrix for the TMA-fed GEMV (bf16), three per job
-  enum { TM_FC, TM_QKV, TM_KV, TM_O, TM_GU, TM_DOWN, TM_LM, TM_COUNT };
-  CUtensorMap tm[TM_COUNT][3];
-  bool tma_gemv = false;
   int32_t* status = nullptr;
   size_t part_floats = 0;
   int max_chunks = 0, lm_groups_max = 0, counters_n = 0;
@@ -197,7 +192,6 @@ struct GemvJob {
   int hid_dt;
   int32_t* amax_out;
   const int* amax_idx;
-  const CUtensorMap* tm;  // three maps for the TMA-fed GEMV, or null
 };
 
 // Batches of at least this many items run their GEMVs on the tensor cores:
@@ -319,10 +313,6 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     a.done = h->done;
     a.amax_out = j.amax_out;
     a.status = h->status;
-    int stages = 0;
-    const int tsmem = (j.tm && h->tma_gemv && pl.mt <= 4 && (j.K / pl.S) % 128 == 0)
-                          ? gemv_tma_smem(pl.mt, j.K, pl.S, &stages) : -1;
-    if (tsmem > 0 && launch_gemv_tma(pl.mt, a, j.tm, stages, tsmem, s)) continue;
     launch_gemv(pl.mt, a, pl.smem, s);
   }
 }
@@ -371,7 +361,6 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
     GemvJob j;
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->w[T_FC];
-    j.tm = h->tm[mtp_handle::TM_FC];
     j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
     j.N = H; j.K = 2 * H; j.pro = PRO_DUAL; j.epi = EPI_STORE; j.dual = true;
     j.nw = h->nrm[T_PRE_E]; j.nw2 = h->nrm[T_PRE_H];
@@ -386,14 +375,12 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
     std::memset(&j, 0, sizeof(j));
     if (need_q) {
       j.w[0] = h->w[T_Q]; j.w[1] = h->w[T_K]; j.w[2] = h->w[T_V];
-      j.tm = h->tm[mtp_handle::TM_QKV];
-      j.seg_end[0] = qw; j.seg_end[1] = qw + kw; j.seg_end[2] = qw + 2 * kw;
+        j.seg_end[0] = qw; j.seg_end[1] = qw + kw; j.seg_end[2] = qw + 2 * kw;
       j.N = qw + 2 * kw;
       j.y = h->qkv;
     } else {
       j.w[0] = h->w[T_K]; j.w[1] = h->w[T_V]; j.w[2] = h->w[T_V];
-      j.tm = h->tm[mtp_handle::TM_KV];
-      j.seg_end[0] = kw; j.seg_end[1] = 2 * kw; j.seg_end[2] = 2 * kw;
+        j.seg_end[0] = kw; j.seg_end[1] = 2 * kw; j.seg_end[2] = 2 * kw;
       j.N = 2 * kw;
       j.y = h->qkv + qw;
     }
@@ -454,7 +441,6 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     ProfScope ps(h, s, PK_O);
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->w[T_O]; j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
-    j.tm = h->tm[mtp_handle::TM_O];
     j.N = H; j.K = qw; j.pro = PRO_PLAIN; j.epi = EPI_RESID;
     j.x = h->o; j.ldx = qw; j.y = h->h1; j.ldy = H; j.resid = h->h0; j.ldr = H;
     run_gemv(h, j, R, s);
@@ -463,7 +449,6 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     ProfScope ps(h, s, PK_GATEUP);
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->w[T_GATE]; j.w[1] = h->w[T_UP];
-    j.tm = h->tm[mtp_handle::TM_GU];
     j.N = 2 * I; j.K = H; j.pro = PRO_NORM; j.epi = EPI_SWIGLU;
     j.x = h->h1; j.ldx = H; j.nw = h->nrm[T_POST]; j.y = h->mlp; j.ldy = I;
     run_gemv(h, j, R, s);
@@ -472,7 +457,6 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     ProfScope ps(h, s, PK_DOWN);
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->w[T_DOWN]; j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
-    j.tm = h->tm[mtp_handle::TM_DOWN];
     j.N = H; j.K = I; j.pro = PRO_PLAIN; j.epi = EPI_RESID;
     j.x = h->mlp; j.ldx = I; j.y = h->h2; j.ldy = H; j.resid = h->h1; j.ldr = H;
     run_gemv(h, j, R, s);
@@ -481,7 +465,6 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     ProfScope ps(h, s, PK_LMHEAD);
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->lm; j.seg_end[0] = c.vocab; j.seg_end[1] = c.vocab; j.seg_end[2] = c.vocab;
-    j.tm = h->tm[mtp_handle::TM_LM];
     j.N = c.vocab; j.K = H; j.pro = PRO_NORM; j.epi = EPI_LOGITS;
     j.x = h->h2; j.ldx = H; j.nw = h->nrm[T_NORM]; j.y = logits; j.ldy = ld_logits;
     j.amax_out = amax_out; j.amax_idx = amax_out ? amax_idx.data() : nullptr;
@@ -708,26 +691,6 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     if (st == MTP_OK) st = alloc(h, &h->x2, (size_t)2 * kTcGemvMaxItems * kmax);
     if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
     h->tc_gemv = st == MTP_OK;
-    // TMA maps for the TMA-fed GEMV: 64-row boxes (32-row boxes of gate / up)
-    // of 128 columns, one per weight segment
-    auto mk = [&](CUtensorMap* m, const void* w, int rows, int cols, int box_rows) {
-      return tc::make_map_box(m, w, rows, cols, 128, box_rows);
-    };
-    bool ok = true;
-    auto three = [&](int id, const void* w0, int r0, const void* w1, int r1, const void* w2, int r2, int cols) {
-      ok = ok && mk(&h->tm[id][0], w0, r0, cols, 64) && mk(&h->tm[id][1], w1, r1, cols, 64) &&
-           mk(&h->tm[id][2], w2, r2, cols, 64);
-    };
-    three(mtp_handle::TM_FC, h->w[T_FC], H, h->w[T_FC], H, h->w[T_FC], H, 2 * H);
-    three(mtp_handle::TM_QKV, h->w[T_Q], qw, h->w[T_K], kw, h->w[T_V], kw, H);
-    three(mtp_handle::TM_KV, h->w[T_K], kw, h->w[T_V], kw, h->w[T_V], kw, H);
-    three(mtp_handle::TM_O, h->w[T_O], H, h->w[T_O], H, h->w[T_O], H, qw);
-    three(mtp_handle::TM_DOWN, h->w[T_DOWN], H, h->w[T_DOWN], H, h->w[T_DOWN], H, I);
-    three(mtp_handle::TM_LM, h->lm, c.vocab, h->lm, c.vocab, h->lm, c.vocab, H);
-    ok = ok && mk(&h->tm[mtp_handle::TM_GU][0], h->w[T_GATE], I, H, 32) &&
-         mk(&h->tm[mtp_handle::TM_GU][1], h->w[T_UP], I, H, 32) &&
-         mk(&h->tm[mtp_handle::TM_GU][2], h->w[T_UP], I, H, 32);
-    h->tma_gemv = ok && qw % 64 == 0 && kw % 64 == 0 && I % 32 == 0;
   }
   const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 255) / 256));
   if (st == MTP_OK) st = alloc(h, &h->gmax, gslots);

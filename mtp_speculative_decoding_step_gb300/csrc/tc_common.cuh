@@ -108,20 +108,5 @@ inline bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
   return r == CUDA_SUCCESS;
 }
 
-// Row-major bf16 matrix [rows][cols] as a 2-D map with a box_cols x box_rows
-// box and no swizzle (rows land in shared memory as plain 2*box_cols-byte rows).
-inline bool make_map_box(CUtensorMap* m, const void* ptr, int rows, int cols, int box_cols, int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace tc
 }  // namespace mtp
