@@ -672,6 +672,109 @@ __device__ int warp_find_cross(int L, unsigned long long target, W w, unsigned l
   return found;
 }
 
+// Weighted selection in a shared-memory list, by one CTA: among the n entries
+// (key[i], id[i]) taken in (key asc, id asc) order, find the entry at which the
+// running weight first reaches target (1 <= target <= the total). The weight
+// is a function of the key (equal keys weigh the same), so digit passes over
+// the key settle K*, and the n-th tie at K* (n = ceil(remaining / weight)) is
+// the one with n-1 smaller ids. Returns false (nothing decided) when more than
+// 2 * kST entries tie at K*.
+template <class Wk>
+__device__ bool list_select(SampleSmem* sm, const uint32_t* key, const int* id, int n, unsigned long long target,
+                            Wk wk, uint32_t& Kout, int& idout) {
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int i = threadIdx.x; i < n; i += kST) {
+    kmin = min(kmin, key[i]);
+    kmax = max(kmax, key[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+  __syncthreads();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int w = 0; w < kST / 32; ++w) {
+    kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
+    kmax = max(kmax, (uint32_t)sm->wsum[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
+  uint32_t prefix = kmin & mask;
+  unsigned long long* h = sm->hist[0];
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0ull;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kST) {
+      const uint32_t k = key[i];
+      if ((k & mask) == prefix) atomicAdd(&h[(k >> lo) & dmask], wk(k));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      unsigned long long s8 = 0;
+      for (int b = 0; b < 8; ++b) s8 += h[lane * 8 + b];
+      unsigned long long incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned long long cum = incl - s8;
+      const bool mine = cum < target && target <= incl;
+      if (mine) {
+        for (int b = 0; b < 8; ++b) {
+          const unsigned long long t = h[lane * 8 + b];
+          if (cum < target && target <= cum + t) {
+            sm->sel_bin = lane * 8 + b;
+            sm->sel_rem = target - cum;
+            break;
+          }
+          cum += t;
+        }
+      }
+      if (!__ballot_sync(0xFFFFFFFFu, mine) && lane == 0) {  // target above the total: the last bin
+        sm->sel_bin = (int)dmask;
+        sm->sel_rem = target;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm->sel_bin << lo;
+    mask |= dmask << lo;
+    target = sm->sel_rem;
+    hi = lo - 1;
+  }
+  const uint32_t K = prefix;
+  const unsigned long long ew = wk(K);
+  const unsigned long long need = ew > 0 ? (target + ew - 1) / ew : 1ull;
+  // ties at K and the need-th of them in id order
+  if (threadIdx.x == 0) { sm->found = -1; sm->ccount = 0; }
+  __syncthreads();
+  int ties = 0;
+  for (int i = threadIdx.x; i < n; i += kST) ties += key[i] == K;
+  ties = (int)block_sum_u64((unsigned long long)ties, sm->wsum);
+  if (ties > 2 * kST) return false;
+  for (int i = threadIdx.x; i < n; i += kST) {
+    if (key[i] != K) continue;
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += key[j] == K && id[j] < id[i];
+    if ((unsigned long long)rank == (need < (unsigned long long)ties ? need : (unsigned long long)ties) - 1)
+      sm->found = id[i];
+  }
+  __syncthreads();
+  Kout = K;
+  idout = sm->found;
+  __syncthreads();
+  return idout >= 0;
+}
+
 // Candidate path for a sampled row whose zs holds transformed logits and
 // whose global max is mx. Returns false (nothing decided) when the cut is not
 // guaranteed to lie inside the exact part of the union.
@@ -698,8 +801,8 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
     __syncthreads();
   }
-  // sort this CTA's run (short runs only; the merge below needs every run sorted)
-  if (sm->ccount <= 2 * kST) rank_sort(cb.ckey, cb.cid, sm->ccount);
+  // without top-k the union is merged from sorted runs: sort this CTA's run
+  if (k == 0 && sm->ccount <= 2 * kST) rank_sort(cb.ckey, cb.cid, sm->ccount);
   unsigned long long sall = 0;
   if (k == 0)
     for (int j = threadIdx.x; j < n; j += kST) sall += to_fix(expf(zs[j] - mx));
@@ -736,11 +839,39 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     }
   }
   __syncthreads();
-  if (runs_sorted && L <= kMergePer * kST) merge_runs(cb.mkey, cb.mid, off, L);
-  else bitonic_sort(cb.mkey, cb.mid, Pd);
+  int Ls = L;  // length of the sorted prefix of mkey / mid
+  bool sorted = false;
+  if (k > 0 && k <= 2 * kST) {
+    // only the top-k of the union matters: select them, then sort just those
+    uint32_t Kk = 0xFFFFFFFFu;
+    int ck = 0x7FFFFFFF;
+    bool sel = L <= k || list_select(sm, cb.mkey, cb.mid, L, (unsigned long long)k,
+                                     [](uint32_t) { return 1ull; }, Kk, ck);
+    if (sel) {
+      uint32_t* skey = reinterpret_cast<uint32_t*>(cb.sw);
+      if (threadIdx.x == 0) sm->ccount = 0;
+      __syncthreads();
+      for (int t = threadIdx.x; t < L; t += kST)
+        if (in_prefix(cb.mkey[t], cb.mid[t], Kk, ck)) {
+          const int pos = atomicAdd(&sm->ccount, 1);
+          skey[pos] = cb.mkey[t];
+          cb.sid[pos] = cb.mid[t];
+        }
+      __syncthreads();
+      Ls = sm->ccount;
+      rank_sort(skey, cb.sid, Ls);
+      for (int t = threadIdx.x; t < Ls; t += kST) { cb.mkey[t] = skey[t]; cb.mid[t] = cb.sid[t]; }
+      __syncthreads();
+      sorted = true;
+    }
+  }
+  if (!sorted) {
+    if (k == 0 && runs_sorted && L <= kMergePer * kST) merge_runs(cb.mkey, cb.mid, off, L);
+    else bitonic_sort(cb.mkey, cb.mid, Pd);
+  }
   if (threadIdx.x < 32) {
     auto fx = [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); };
-    const int Kk = k > 0 ? min(k, L) : L;
+    const int Kk = k > 0 ? min(k, Ls) : Ls;
     unsigned long long SE = 0;
     if (k > 0) {
       warp_find_cross(Kk, ~0ull, fx, &SE);
@@ -782,7 +913,7 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
   const int Kf = sm->fin_kf;
   d.k_key = 0xFFFFFFFFu;
   d.k_cut = 0x7FFFFFFF;
-  if (Kf >= L && !truncated) {  // nothing cut
+  if (Kf >= Ls && !truncated) {  // nothing cut
     d.p_key = 0xFFFFFFFFu;
     d.p_cut = 0x7FFFFFFF;
   } else {
@@ -833,12 +964,13 @@ __device__ int candidate_draw(const TDesc& d, CandBufs& cb, float u, SampleSmem*
 // find the exact crossing element. Elements beyond the span weigh 0 and follow
 // every binned element, so they never hold the crossing. Sets the top-p fields
 // of d and returns true, or returns false (nothing decided) when the crossing
-// bin holds more than kMergePer * kST elements (or 2 * kST in one CTA).
+// bin holds more than kMergePer * kST elements (or 2 * kST in one CTA). Without
+// min-p the kept set's fixed-point mass is returned in *S_exact (else 0).
 constexpr int kFlatBins = 256 * kClusterCTAs;
 constexpr float kFlatSpan = 30.f;  // exp(-30) * 2^40 rounds to 0
 
 __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowParams& p, float mx, float zmin,
-                           CandBufs& cb, TDesc& d) {
+                           CandBufs& cb, TDesc& d, unsigned long long* S_exact) {
   SampleSmem* sm = c.sm;
   float span = mx - zmin;
   if (!(span > 0.f)) return false;  // one distinct value, or non-finite input
@@ -932,7 +1064,6 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
   }
   __syncthreads();
   const int mine = sm->ccount;
-  if (mine <= cb.C && mine <= 2 * kST) rank_sort(cb.ckey, cb.cid, mine);
   if (threadIdx.x == 0) sm->mail[c.ph].u[0] = (unsigned long long)mine;
   m = c.publish();
   int off[kClusterCTAs + 1];
@@ -952,15 +1083,22 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
     cb.mid[t] = c.cl.map_shared_rank(cb.cid, r)[t - off[r]];
   }
   __syncthreads();
-  merge_runs(cb.mkey, cb.mid, off, L);
-  if (threadIdx.x < 32) {
-    const int j = warp_find_cross(L, rem, [&](int j) { return to_fix(expf(key_to_z(cb.mkey[j]) - mx)); }, nullptr);
-    if (threadIdx.x == 0) sm->found = j < L ? j : L - 1;
+  auto wk = [&](uint32_t k) { return to_fix(expf(key_to_z(k) - mx)); };
+  uint32_t K;
+  int cut;
+  if (!list_select(sm, cb.mkey, cb.mid, L, rem, wk, K, cut)) return false;
+  d.p_key = K;
+  d.p_cut = cut;
+  d.kept = -1;
+  *S_exact = 0ull;
+  if (!(p.min_p > 0.f)) {
+    // the kept mass, exactly: every bin before the crossing bin (target - rem)
+    // plus that bin's entries up to the crossing
+    unsigned long long loc = 0;
+    for (int t = threadIdx.x; t < L; t += kST)
+      if (in_prefix(cb.mkey[t], cb.mid[t], K, cut)) loc += wk(cb.mkey[t]);
+    *S_exact = (target - rem) + block_sum_u64(loc, sm->wsum);
   }
-  __syncthreads();
-  d.p_key = cb.mkey[sm->found];
-  d.p_cut = cb.mid[sm->found];
-  __syncthreads();
   return true;
 }
 
@@ -968,7 +1106,7 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
 // transformed logits (penalised, then / T) and `d` the descriptor; greedy rows
 // only get d.argmax.
 __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, int V, const float* lg,
-                              const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb, bool flat_first) {
+                              const RowParams& p, TDesc& d, int32_t* status, CandBufs& cb) {
   SampleSmem* sm = c.sm;
   build_bitmap(sm, bits, v0, n);
   // one pass: stage, repetition penalty, argmax of the penalised logits,
@@ -1060,12 +1198,16 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
 
   d.m = gv / p.temperature + 0.0f;
   const float mx = d.m;
-  // verify descriptors try the binned top-p cut first (no draw follows);
-  // the draft step tries the candidate union first (its draw reuses the list)
+  // rows without top-k try the binned top-p cut first; top-k rows (and rows
+  // the binned cut cannot settle) take the candidate union, then the radix path
   const bool flat_ok = !(p.top_k > 0 && p.top_k < V) && p.top_p > 0.f && p.top_p < 1.f;
-  bool flat_done = flat_first && flat_ok && flat_top_p(c, zs, v0, n, p, mx, zmin, cb, d);
+  unsigned long long S_exact = 0;
+  const bool flat_done = flat_ok && flat_top_p(c, zs, v0, n, p, mx, zmin, cb, d, &S_exact);
+  if (flat_done && S_exact > 0) {
+    d.S = (float)((double)S_exact / kFix);
+    return false;
+  }
   if (!flat_done && candidate_transform(c, zs, v0, n, V, p, mx, kmin, kmax, cb, d)) return true;
-  if (!flat_done && !flat_first && flat_ok) flat_done = flat_top_p(c, zs, v0, n, p, mx, zmin, cb, d);
 
   if (p.top_k > 0 && p.top_k < V) {
     uint32_t K;
@@ -1182,7 +1324,7 @@ __global__ void __launch_bounds__(kST, 1) k_sample(const __grid_constant__ Sampl
   const RowParams p = a.p[r];
   load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, i);
   TDesc d;
-  const bool fast = transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status, cb, a.mode == 1);
+  const bool fast = transform_row(c, zs, bits, v0, n, a.V, lg, p, d, a.status, cb);
 
   if (a.mode == 1) {
     if (c.rank == 0 && threadIdx.x == 0) a.desc[task] = d;

@@ -6,7 +6,7 @@ tied logits (a few distinct values), which push the cut into a crowded
 stretch of equal keys.  The transform descriptors that spec_verify leaves in
 its workspace (one 32-byte record per row and position: max transformed logit
 m, normaliser S, top-k bound (key, id), top-p bound (key, id), argmax, kept
-count) are decoded on the host, the kept set they define is rebuilt from the
+count or -1) are decoded on the host, the kept set they define is rebuilt from the
 logits, and both are compared with the oracle's transform: the kept set
 exactly (unless the oracle's cumulative mass lies within 1e-6 of the top-p
 threshold at the cut, a counted near-tie) and S to 1e-5."""
@@ -104,5 +104,6 @@ def test_wide_top_p_descriptors():
             z = _transformed(lg[r, i], rows[r], window)
             ez = np.exp(z[want].astype(np.float64) - np.float64(desc[r, i]["m"]))
             assert abs(float(desc[r, i]["S"]) - ez.sum()) <= 1e-5 * ez.sum(), (r, i)
-            assert desc[r, i]["kept"] == want.sum(), (r, i)
+            # the support size is recorded where the path counts it (-1: not needed)
+            assert desc[r, i]["kept"] in (-1, want.sum()), (r, i)
     assert near <= 1
