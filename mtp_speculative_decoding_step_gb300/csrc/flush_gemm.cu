@@ -31,7 +31,13 @@ struct TcGemmArgs {
   float* D;          // [ksplit][M][ldd]
   long long ldd;
   int32_t* status;
+  const uint8_t* pf[2];  // ranges the next kernel streams, prefetched into L2 (or null)
+  long long pf_bytes[2];
 };
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 template <int BN, int STAGES, int MH>
 __global__ void __launch_bounds__(128, 1)
@@ -82,19 +88,38 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer. The weight tiles come from HBM: they are prefetched into
-    // L2 kPrefetch steps ahead of their shared-memory load, so the loads the
+    // TMA producer. The weight tiles (B) do not depend on the previous kernel:
+    // the first ring of them is requested before waiting for it, the
+    // activations (A) after. Weight tiles further ahead are prefetched into L2
+    // kPrefetch steps before their shared-memory load, so the loads the
     // pipeline waits on hit L2.
     constexpr int kPrefetch = STAGES;
+    const int pre = min(nk, STAGES);
+    for (int i = 0; i < pre; ++i) {
+      mbar_expect_tx(smem_u32(&full[i]), kStage);
+      tma_load_2d(smem_u32(base + i * kStage + kABytes), tb, (kb + i) * kTileK, nb, smem_u32(&full[i]));
+    }
     for (int i = STAGES; i < min(nk, STAGES + kPrefetch); ++i) tma_prefetch_2d(tb, (kb + i) * kTileK, nb);
-    for (int i = 0; i < nk; ++i) {
+    pdl_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(smem_u32(base + i * kStage), &ta, (kb + i) * kTileK, m0, smem_u32(&full[i]));
+    for (int i = pre; i < nk; ++i) {
       const int s = i % STAGES, r = i / STAGES;
-      if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1)) { *s_fail = 1; break; }
-      if (r > 0 && i + kPrefetch < nk) tma_prefetch_2d(tb, (kb + i + kPrefetch) * kTileK, nb);
+      if (!mbar_wait(smem_u32(&empty[s]), (r - 1) & 1)) { *s_fail = 1; break; }
+      if (i + kPrefetch < nk) tma_prefetch_2d(tb, (kb + i + kPrefetch) * kTileK, nb);
       uint8_t* as = base + s * kStage;
       mbar_expect_tx(smem_u32(&full[s]), kStage);
       tma_load_2d(smem_u32(as), &ta, (kb + i) * kTileK, m0, smem_u32(&full[s]));
       tma_load_2d(smem_u32(as + kABytes), tb, (kb + i) * kTileK, nb, smem_u32(&full[s]));
+    }
+    // the next kernel's weights: this CTA's share of each range, into L2
+    const long long nb_cta = (long long)gridDim.x * gridDim.y * gridDim.z;
+    const long long cta = ((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    for (int q = 0; q < 2; ++q) {
+      if (!a.pf[q]) continue;
+      const long long share = ((a.pf_bytes[q] + nb_cta - 1) / nb_cta + 15) & ~15LL;
+      const long long lo = cta * share, hi = min(a.pf_bytes[q], lo + share) & ~15LL;
+      for (long long o = lo; o < hi; o += 65536) prefetch_l2(a.pf[q] + o, (uint32_t)min(65536LL, hi - o));
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
@@ -118,7 +143,10 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // epilogue: TMEM lanes 32w..32w+31 hold rows m0 + 32w + lane
+  // epilogue: TMEM lanes 32w..32w+31 hold rows m0 + 32w + lane; the partials
+  // are written only once the previous kernel (a reader of D) has finished
+  pdl_wait();
+  pdl_trigger();
   const bool got = mbar_wait(smem_u32(accf), 0);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (got) {
@@ -157,7 +185,7 @@ __global__ void __launch_bounds__(128, 1)
 // D[split][M][N] = A[M][K] . [B0; B1]^T  (B0 rows [0, n0rows), B1 the rest).
 template <int BN, int STAGES, int MH>
 static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int ksplit,
-                      float* D, int32_t* status, cudaStream_t s) {
+                      float* D, int32_t* status, cudaStream_t s, const void* const* pf, const long long* pf_bytes) {
   if (M < 1 || K % kTileK != 0 || N % BN != 0 || n0rows % BN != 0 || ksplit < 1) return false;
   CUtensorMap ta, tb0, tb1;
   if (!make_map(&ta, A, M, K, kTileM * MH)) return false;
@@ -165,23 +193,32 @@ static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, c
   if (!make_map(&tb1, B1 ? B1 : B0, B1 ? N - n0rows : n0rows, K, BN)) return false;
   TcGemmArgs a;
   a.M = M; a.N = N; a.K = K; a.n_split_b = n0rows; a.ksplit = ksplit; a.D = D; a.ldd = N; a.status = status;
+  for (int q = 0; q < 2; ++q) {
+    a.pf[q] = pf ? static_cast<const uint8_t*>(pf[q]) : nullptr;
+    a.pf_bytes[q] = pf && pf[q] ? pf_bytes[q] : 0;
+  }
   const int smem = STAGES * (kTileM * MH + BN) * kTileK * 2 + 1024 + 256;
   auto k = k_tc_gemm<BN, STAGES, MH>;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set = true;
+  }
   dim3 grid((M + kTileM * MH - 1) / (kTileM * MH), N / BN, ksplit);
-  k<<<grid, 128, smem, s>>>(ta, tb0, tb1, a);
+  const cudaError_t e = launch_pdl(k, grid, dim3(128), (size_t)smem, s, ta, tb0, tb1, a);
   count_launch();
-  return cudaGetLastError() == cudaSuccess;
+  return e == cudaSuccess;
 }
 
 // mh: 128-row halves per CTA (1 or 2); bn: 128, 160, 256 (mh 1) or 128, 256 (mh 2).
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
-                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh) {
-  if (mh == 2 && bn == 256) return tc_gemm_t<256, 3, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
-  if (mh == 2) return tc_gemm_t<128, 4, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
-  if (bn == 256) return tc_gemm_t<256, 4, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
-  if (bn == 160) return tc_gemm_t<160, 5, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
-  return tc_gemm_t<128, 6, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s);
+                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh, const void* const* pf,
+                    const long long* pf_bytes) {
+  if (mh == 2 && bn == 256) return tc_gemm_t<256, 3, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s, pf, pf_bytes);
+  if (mh == 2) return tc_gemm_t<128, 4, 2>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s, pf, pf_bytes);
+  if (bn == 256) return tc_gemm_t<256, 4, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s, pf, pf_bytes);
+  if (bn == 160) return tc_gemm_t<160, 5, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s, pf, pf_bytes);
+  return tc_gemm_t<128, 6, 1>(A, M, K, B0, n0rows, B1, N, ksplit, D, status, s, pf, pf_bytes);
 }
 
 }  // namespace mtp

@@ -97,8 +97,11 @@ void launch_flush_x(const FlushXArgs& a, int M, cudaStream_t s);
 void launch_flush_norm(const float* part, int nsplit, long long split_stride, int M, int H, const float* w,
                        float eps, uint16_t* b, cudaStream_t s);
 // D[split][M][N] = A[M][K] . [B0; B1]^T on tcgen05 (bf16 in, fp32 out).
+// pf[2] / pf_bytes[2]: two ranges the next kernel streams (prefetched into L2
+// once this kernel's own loads are issued), or null.
 bool launch_tc_gemm(const void* A, int M, int K, const void* B0, int n0rows, const void* B1, int N, int bn,
-                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh = 1);
+                    int ksplit, float* D, int32_t* status, cudaStream_t s, int mh = 1,
+                    const void* const* pf = nullptr, const long long* pf_bytes = nullptr);
 
 // Batched GEMV on tcgen05 (bf16 weights, kTcGemvMaxItems items per pass).
 constexpr int kTcGemvMaxItems = 64;

@@ -504,7 +504,10 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
     const int mh = 1;
     const int bn = H % 160 == 0 ? 160 : 128;
     const int ks = tc_splits((mp + 128 * mh - 1) / (128 * mh), H / bn, 2 * H / 64, h->sms, 8);
-    if (!launch_tc_gemm(h->xb, mp, 2 * H, h->w[T_FC], H, nullptr, H, bn, ks, h->tcpart, h->status, s, mh))
+    // the k/v weights of the next contraction go to L2 while fc streams its own
+    const void* pf[2] = {h->w[T_K], h->w[T_V]};
+    const long long pfb[2] = {2LL * kw * H, 2LL * kw * H};
+    if (!launch_tc_gemm(h->xb, mp, 2 * H, h->w[T_FC], H, nullptr, H, bn, ks, h->tcpart, h->status, s, mh, pf, pfb))
       return MTP_ERR_CUDA;
     launch_flush_norm(h->tcpart, ks, (long long)mp * H, mp, H, h->nrm[T_IN], c.eps, h->bb, s);
   }

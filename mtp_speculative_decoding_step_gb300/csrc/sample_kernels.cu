@@ -119,6 +119,7 @@ __device__ unsigned long long cluster_sum_u64(Clu& c, unsigned long long local) 
   if (threadIdx.x == 0) c.sm->mail[c.ph].u[0] = local;
   Mail* m = c.publish();
   unsigned long long t = 0;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) t += c.remote(m, r)->u[0];
   return t;
 }
@@ -162,6 +163,7 @@ __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, W
   Mail* mm = c.publish();
   kmin = 0xFFFFFFFFu;
   kmax = 0u;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
     kmin = min(kmin, (uint32_t)c.remote(mm, r)->u[0]);
     kmax = max(kmax, (uint32_t)c.remote(mm, r)->u[1]);
@@ -194,6 +196,7 @@ __device__ void radix_select(Clu& c, const float* zs, int n_local, Act active, W
     c.cl.sync();
     for (int b = threadIdx.x; b < 256; b += kST) {
       unsigned long long t = 0;
+#pragma unroll
       for (int r = 0; r < kClusterCTAs; ++r) t += c.cl.map_shared_rank(h, r)[b];
       sm->tot[b] = t;
     }
@@ -253,6 +256,7 @@ __device__ int tie_cut(Clu& c, const float* zs, int n_local, int v0, Act active,
   Mail* m = c.publish();
   unsigned long long before = 0, total = 0;
   int owner = -1;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
     const unsigned long long t = c.remote(m, r)->u[0];
     if (owner < 0 && before + t >= n) owner = r;
@@ -304,15 +308,19 @@ __device__ int cluster_draw(Clu& c, int n_local, int v0, Wt weight, float u) {
   if (threadIdx.x == 0) sm->mail[c.ph].u[0] = loc;
   Mail* m = c.publish();
   unsigned long long tot = 0;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) tot += c.remote(m, r)->u[0];
   if (tot == 0) return -1;
   const unsigned long long target = (unsigned long long)floor((double)u * (double)tot) + 1ull;
+  unsigned long long tv[kClusterCTAs];
+#pragma unroll
+  for (int r = 0; r < kClusterCTAs; ++r) tv[r] = c.remote(m, r)->u[0];
   unsigned long long before = 0;
   int owner = kClusterCTAs - 1;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
-    const unsigned long long t = c.remote(m, r)->u[0];
-    if (before + t >= target) { owner = r; break; }
-    before += t;
+    if (before + tv[r] >= target) { owner = r; break; }
+    before += tv[r];
   }
   int pick = -1;
   if (c.rank == owner) {
@@ -817,6 +825,7 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
   off[0] = 0;
   unsigned long long S_all = 0;
   bool truncated = false, runs_sorted = true;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
     Mail* x = c.remote(m, r);
     off[r + 1] = off[r] + (int)x->u[0];
@@ -995,6 +1004,7 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
   unsigned long long own = 0;
   if (threadIdx.x < 256) {
     const int b = c.rank * 256 + threadIdx.x;
+#pragma unroll
     for (int r = 0; r < kClusterCTAs; ++r) own += c.cl.map_shared_rank(hw, r)[b];
     sm->tot[threadIdx.x] = own;
   }
@@ -1002,15 +1012,19 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
   if (threadIdx.x == 0) sm->mail[c.ph].u[0] = own;
   Mail* m = c.publish();  // also ends every remote read of hw
   unsigned long long SE = 0;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) SE += c.remote(m, r)->u[0];
   if (SE == 0) return false;
   const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+  unsigned long long tv[kClusterCTAs];
+#pragma unroll
+  for (int r = 0; r < kClusterCTAs; ++r) tv[r] = c.remote(m, r)->u[0];
   unsigned long long before = 0;
   int owner = kClusterCTAs - 1;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
-    const unsigned long long t = c.remote(m, r)->u[0];
-    if (before + t >= target) { owner = r; break; }
-    before += t;
+    if (before + tv[r] >= target) { owner = r; break; }
+    before += tv[r];
   }
   if (c.rank == owner && threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -1069,6 +1083,7 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
   int off[kClusterCTAs + 1];
   off[0] = 0;
   bool over = false;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
     const int cnt = (int)c.remote(m, r)->u[0];
     over |= cnt > cb.C || cnt > 2 * kST;
@@ -1181,6 +1196,7 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   Mail* m = c.publish();
   float gv = -INFINITY, zmin = INFINITY;
   int gi = 0x7FFFFFFF;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) {
     Mail* x = c.remote(m, r);
     if (better(x->f[0], x->i[0], gv, gi)) { gv = x->f[0]; gi = x->i[0]; }
@@ -1260,6 +1276,7 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
   if (threadIdx.x == 0) { sm->mail[c.ph].u[0] = loc; sm->mail[c.ph].u[1] = cnt; }
   m = c.publish();
   unsigned long long S = 0, K = 0;
+#pragma unroll
   for (int r = 0; r < kClusterCTAs; ++r) { S += c.remote(m, r)->u[0]; K += c.remote(m, r)->u[1]; }
   d.S = (float)((double)S / kFix);
   d.kept = (int)K;
@@ -1471,6 +1488,7 @@ constexpr int kGreedyGroup = 4;  // positions reduced together
 __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
   __shared__ float s_v[kGreedyMaxPos];
   __shared__ int s_i[kGreedyMaxPos];
+  __shared__ int s_am[kGreedyMaxPos];
   __shared__ float wv[kGreedyGroup][kST / 32];
   __shared__ int wi[kGreedyGroup][kST / 32];
   cg::cluster_group cl = cg::this_cluster();
@@ -1556,17 +1574,20 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
   cl.sync();
-  if (rank == 0 && warp == 0) {
-    // lane i <= d combines position i over the cluster
-    int am = 0x7FFFFFFF;
-    if (lane <= d) {
-      float gv = -INFINITY;
-      for (int q = 0; q < nc; ++q) {
-        const float v = *cl.map_shared_rank(&s_v[lane], q);
-        const int id = *cl.map_shared_rank(&s_i[lane], q);
-        if (better(v, id, gv, am)) { gv = v; am = id; }
-      }
+  if (rank == 0 && warp <= d) {
+    // warp i combines position i: lane q reads CTA q's slice argmax
+    float v = -INFINITY;
+    int id = 0x7FFFFFFF;
+    if (lane < nc) {
+      v = *cl.map_shared_rank(&s_v[warp], lane);
+      id = *cl.map_shared_rank(&s_i[warp], lane);
     }
+    warp_argmax(v, id);
+    if (lane == 0) s_am[warp] = id;
+  }
+  __syncthreads();
+  if (rank == 0 && warp == 0) {
+    const int am = lane <= d ? s_am[lane] : 0x7FFFFFFF;
     const int32_t* dr = a.drafts + (size_t)r * d;
     // accepted prefix: drafts x_i (i = 1..d) equal to the argmax of row i-1
     const int x = lane < d ? dr[lane] : -1;
