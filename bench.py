@@ -45,7 +45,7 @@ POOL = 16
 # of the same kernel at V=32768 (profiles/lm_head_gemv_H5120_V32768.md),
 # scaled by the rows processed (152064 / 32768). Set to None when the kernel
 # changes until it is captured again.
-LM_TRAFFIC_BYTES = round((335.650048e6 + 5.9648e6) * 152064 / 32768)
+LM_TRAFFIC_BYTES = round((335.637760e6 + 3.358464e6) * 152064 / 32768)
 WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064), bf16 weights, "
             "batch 1, greedy, depth 2 (block 3), draft KV 4096")
 
