@@ -685,11 +685,12 @@ __device__ int warp_find_cross(int L, unsigned long long target, W w, unsigned l
 // running weight first reaches target (1 <= target <= the total). The weight
 // is a function of the key (equal keys weigh the same), so digit passes over
 // the key settle K*, and the n-th tie at K* (n = ceil(remaining / weight)) is
-// the one with n-1 smaller ids. Returns false (nothing decided) when more than
-// 2 * kST entries tie at K*.
+// the one with n-1 smaller ids (the ties are gathered into tie_buf, which holds
+// tie_cap ids). Returns false (nothing decided) when more than tie_cap entries
+// tie at K*.
 template <class Wk>
 __device__ bool list_select(SampleSmem* sm, const uint32_t* key, const int* id, int n, unsigned long long target,
-                            Wk wk, uint32_t& Kout, int& idout) {
+                            Wk wk, int* tie_buf, int tie_cap, uint32_t& Kout, int& idout) {
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int i = threadIdx.x; i < n; i += kST) {
     kmin = min(kmin, key[i]);
@@ -762,19 +763,24 @@ __device__ bool list_select(SampleSmem* sm, const uint32_t* key, const int* id, 
   const uint32_t K = prefix;
   const unsigned long long ew = wk(K);
   const unsigned long long need = ew > 0 ? (target + ew - 1) / ew : 1ull;
-  // ties at K and the need-th of them in id order
+  // ties at K, gathered, and the need-th of them in id order (each tie's rank
+  // is its count of smaller tie ids)
   if (threadIdx.x == 0) { sm->found = -1; sm->ccount = 0; }
   __syncthreads();
-  int ties = 0;
-  for (int i = threadIdx.x; i < n; i += kST) ties += key[i] == K;
-  ties = (int)block_sum_u64((unsigned long long)ties, sm->wsum);
-  if (ties > 2 * kST) return false;
-  for (int i = threadIdx.x; i < n; i += kST) {
-    if (key[i] != K) continue;
+  for (int i = threadIdx.x; i < n; i += kST)
+    if (key[i] == K) {
+      const int pos = atomicAdd(&sm->ccount, 1);
+      if (pos < tie_cap) tie_buf[pos] = id[i];
+    }
+  __syncthreads();
+  const int ties = sm->ccount;
+  if (ties > tie_cap) return false;
+  const unsigned long long want = need < (unsigned long long)ties ? need : (unsigned long long)ties;
+  for (int t = threadIdx.x; t < ties; t += kST) {
+    const int me = tie_buf[t];
     int rank = 0;
-    for (int j = 0; j < n; ++j) rank += key[j] == K && id[j] < id[i];
-    if ((unsigned long long)rank == (need < (unsigned long long)ties ? need : (unsigned long long)ties) - 1)
-      sm->found = id[i];
+    for (int q = 0; q < ties; ++q) rank += tie_buf[q] < me;
+    if ((unsigned long long)rank == want - 1) sm->found = me;
   }
   __syncthreads();
   Kout = K;
@@ -855,7 +861,7 @@ __device__ bool candidate_transform(Clu& c, const float* zs, int v0, int n, int 
     uint32_t Kk = 0xFFFFFFFFu;
     int ck = 0x7FFFFFFF;
     bool sel = L <= k || list_select(sm, cb.mkey, cb.mid, L, (unsigned long long)k,
-                                     [](uint32_t) { return 1ull; }, Kk, ck);
+                                     [](uint32_t) { return 1ull; }, cb.sid, min(cb.C, 2 * kST), Kk, ck);
     if (sel) {
       uint32_t* skey = reinterpret_cast<uint32_t*>(cb.sw);
       if (threadIdx.x == 0) sm->ccount = 0;
@@ -1101,7 +1107,7 @@ __device__ bool flat_top_p(Clu& c, const float* zs, int v0, int n, const RowPara
   auto wk = [&](uint32_t k) { return to_fix(expf(key_to_z(k) - mx)); };
   uint32_t K;
   int cut;
-  if (!list_select(sm, cb.mkey, cb.mid, L, rem, wk, K, cut)) return false;
+  if (!list_select(sm, cb.mkey, cb.mid, L, rem, wk, cb.sid, min(cb.C, 2 * kST), K, cut)) return false;
   d.p_key = K;
   d.p_cut = cut;
   d.kept = -1;
@@ -1387,27 +1393,36 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
   const float* lg = a.logits + (size_t)r * (d + 1) * a.V;
   const float* uu = a.u + (size_t)r * (d + 1);
 
-  // accept chain (every CTA evaluates it identically)
-  int nacc = 0;
-  for (int i = 1; i <= d; ++i) {
-    const int x = dr[i - 1];
-    bool acc;
-    if (x < 0 || x >= a.V) {  // an out-of-range draft is rejected, never dereferenced
-      acc = false;
-    } else if (p.greedy) {
-      acc = x == desc[i - 1].argmax;
-    } else {
-      load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, i - 1);
-      bool pen = false;
-      for (int t = 0; t < sm->nwin; ++t) pen |= sm->wtok[t] == x;
-      const float pv = eval_p(desc[i - 1], p, lg[(size_t)(i - 1) * a.V + x], pen, x);
-      const float qv = a.q[((size_t)r * d + (i - 1)) * a.V + x];
-      acc = qv > 0.f && uu[i - 1] < pv / qv;
-      __syncthreads();
+  // accept chain, every position at once (every CTA evaluates it identically):
+  // lane j of warp 0 tests draft x_{j+1} against target row j. The penalty
+  // window of row j is the W tokens starting at j of (history ++ drafts).
+  {
+    const int32_t* hist = a.hist + (size_t)r * a.W;
+    for (int t = threadIdx.x; t < a.W + d; t += kST) sm->wtok[t] = t < a.W ? hist[t] : dr[t - a.W];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int j = threadIdx.x;
+      bool acc = false;
+      if (j < d) {
+        const int x = dr[j];
+        if (x >= 0 && x < a.V) {  // an out-of-range draft is rejected, never dereferenced
+          if (p.greedy) {
+            acc = x == desc[j].argmax;
+          } else {
+            bool pen = false;
+            for (int t = j; t < j + a.W; ++t) pen |= sm->wtok[t] == x;
+            const float pv = eval_p(desc[j], p, __ldg(lg + (size_t)j * a.V + x), pen, x);
+            const float qv = __ldg(a.q + ((size_t)r * d + j) * a.V + x);
+            acc = qv > 0.f && uu[j] < pv / qv;
+          }
+        }
+      }
+      const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc) & (d >= 32 ? 0xFFFFFFFFu : ((1u << d) - 1u));
+      if (j == 0) sm->fin_kf = rej ? __ffs(rej) - 1 : d;
     }
-    if (!acc) break;
-    nacc = i;
+    __syncthreads();
   }
+  const int nacc = sm->fin_kf;
   int y;
   if (p.greedy) {
     y = desc[nacc].argmax;
@@ -1421,6 +1436,41 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
     // draw weights of this slice, computed once: the residual max(p - q, 0)
     // after a rejection, else p (the bonus row)
     auto stage = [&](bool residual) {
+      const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(ln + v0) & 15) == 0 &&
+                       (!residual || (reinterpret_cast<uintptr_t>(qn + v0) & 15) == 0);
+      if (vec) {
+        const float4* l4 = reinterpret_cast<const float4*>(ln + v0);
+        const float4* q4 = residual ? reinterpret_cast<const float4*>(qn + v0) : nullptr;
+        const int n4 = n / 4;
+        for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+          float4 lv[4], qv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j4 = b0 + u * kST + threadIdx.x;
+            if (j4 < n4) {
+              lv[u] = __ldg(l4 + j4);
+              qv[u] = residual ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j4 = b0 + u * kST + threadIdx.x;
+            if (j4 < n4) {
+              const float lx[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+              const float qx[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                const float pv = eval_p(dn, p, lx[e], bit(bits, j), v0 + j);
+                const float rv = residual ? pv - qx[e] : pv;
+                ws[j] = rv > 0.f ? rv : 0.f;
+              }
+            }
+          }
+        }
+        __syncthreads();
+        return;
+      }
       for (int b0 = 0; b0 < n; b0 += 8 * kST) {
         float lv[8], qv[8];
 #pragma unroll
