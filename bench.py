@@ -556,9 +556,11 @@ def cpu_rounds(work, budget_s: float, max_rounds: int):
     hids = [thid[0, 0]]
     t0 = time.perf_counter()
     done = 0
+    # the draft KV holds 1024 slots beyond the prefill: at most DEPTH + 1 new per round
+    max_rounds = min(max_rounds, 1000 // (DEPTH + 1))
     while done < max_rounds:
         d = head.draft(Kc[0], Vc[0], slot, toks, hids, DEPTH, p, np.zeros(0, np.int32), np.zeros(DEPTH, np.float32))
-        lg = synth.plant_logits(base[done % POOL], d["drafts"], coins[done])
+        lg = synth.plant_logits(base[done % POOL], d["drafts"], coins[done % len(coins)])
         n, out, _ = oracle.verify_row(lg, d["drafts"], None, p, np.zeros(0, np.int32),
                                       np.zeros(DEPTH + 1, np.float32))
         slot += len(toks)
@@ -663,7 +665,7 @@ def main():
     result, work = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.quick:
-            n, sec, thr = cpu_rounds(work, args.cpu_budget, 8)
+            n, sec, thr = cpu_rounds(work, args.cpu_budget, 100000)
             result["cpu_baseline"] = {"value": round(n * DEPTH / sec, 3), "unit": "draft tok/s", "cores": thr,
                                       "kind": "oracle",
                                       "sample": f"{n} whole rounds (2 draft steps + verify) of the same workload"}
