@@ -36,21 +36,8 @@ __device__ __forceinline__ uint32_t desc_key(float z) {
   return ~u;                                        // ascending in -z
 }
 
-// round(w * 2^40) to the nearest integer, ties to even, for 0 <= w < 2^23,
-// built from the float's bits (mantissa shifted by the exponent): no float to
-// 64-bit integer conversion, which is slow on this path.
 __device__ __forceinline__ uint64_t to_fix(float w) {
-  if (!(w > 0.f)) return 0ull;
-  const uint32_t u = __float_as_uint(w);
-  const int e = (int)(u >> 23);  // biased exponent (w > 0: no sign bit)
-  if (e == 0) return 0ull;       // subnormal: below 2^-126, far under 2^-41
-  const uint32_t m = (u & 0x7FFFFFu) | 0x800000u;
-  int sh = e - 127 - 23 + 40;    // w * 2^40 = m * 2^sh
-  if (sh >= 0) return (uint64_t)m << (sh < 39 ? sh : 39);
-  if (sh < -24) return 0ull;     // m * 2^sh < 2^-1: rounds to 0
-  const int rs = -sh;
-  const uint32_t q = m >> rs, rem = m & ((1u << rs) - 1u), half = 1u << (rs - 1);
-  return (uint64_t)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
+  return w > 0.f ? (uint64_t)__float2ull_rn(w * 1099511627776.0f) : 0ull;
 }
 
 __device__ __forceinline__ float penalize(float z, float r) { return z > 0.f ? z / r : z * r; }
