@@ -92,14 +92,25 @@ typedef struct {
 /* Per-row sampling parameters. temperature 0 (or top_k 1) is greedy: the
  * point mass at the argmax ("greedy is a special case of sampled decoding",
  * Ollama MLX-runner commit log). rep_penalty 1, top_k 0, top_p 1, min_p 0
- * disable their transforms. */
+ * disable their transforms.
+ *
+ * flags: 0, or MTP_SAMPLE_ARGMAX_DRAFT on a sampled row: the drafter proposes
+ * the argmax of its (penalised) logits instead of a sample, and spec_verify
+ * treats that draft as a point mass q (q(x) = 1): x is accepted with
+ * probability p(x) and a rejection draws from p with x removed, so the
+ * committed tokens still follow p. This is the drafter flag
+ * supports_greedy_draft_argmax ("feat(inference): support the qwen3_5_mtp
+ * drafter" issue, Upstream contract to port); mtp_draft then needs neither
+ * d_q nor d_u for the row, and spec_verify reads no q for it. */
+#define MTP_SAMPLE_ARGMAX_DRAFT 1
 typedef struct {
   float temperature;  /* >= 0 */
   float rep_penalty;  /* > 0 */
   float top_p;        /* (0, 1] */
   float min_p;        /* [0, 1) */
   int32_t top_k;      /* 0 = off, else 1..1024 */
-  int32_t reserved;   /* must be 0 (frequency penalty is not implemented) */
+  int32_t flags;      /* 0 or MTP_SAMPLE_ARGMAX_DRAFT; other bits are rejected
+                         (frequency penalty is not implemented) */
 } mtp_sampling;
 
 /* Draft KV cache buffers, caller-owned device memory, borrowed by mtp_load.

@@ -56,7 +56,7 @@ class Tensor(ctypes.Structure):
 
 class Sampling(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("rep_penalty", ctypes.c_float), ("top_p", ctypes.c_float),
-                ("min_p", ctypes.c_float), ("top_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("min_p", ctypes.c_float), ("top_k", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class KV(ctypes.Structure):
@@ -134,15 +134,21 @@ def _dtype_code(t) -> int:
     return MTP_DTYPE_BF16 if t.dtype == torch.bfloat16 else MTP_DTYPE_F32
 
 
+MTP_SAMPLE_ARGMAX_DRAFT = 1
+
+
 def sampling_array(params) -> ctypes.Array:
-    """params: list of dicts/tuples (temperature, rep_penalty, top_k, top_p, min_p)."""
+    """params: list of dicts (temperature, rep_penalty, top_k, top_p, min_p,
+    argmax_draft) or tuples (temperature, rep_penalty, top_k, top_p, min_p)."""
     arr = (Sampling * len(params))()
     for i, p in enumerate(params):
+        flags = 0
         if isinstance(p, dict):
+            flags = MTP_SAMPLE_ARGMAX_DRAFT if p.get("argmax_draft", False) else 0
             p = (p.get("temperature", 0.0), p.get("rep_penalty", 1.0), p.get("top_k", 0),
                  p.get("top_p", 1.0), p.get("min_p", 0.0))
         t, r, k, tp, mp = p
-        arr[i] = Sampling(float(t), float(r), float(tp), float(mp), int(k), 0)
+        arr[i] = Sampling(float(t), float(r), float(tp), float(mp), int(k), flags)
     return arr
 
 

@@ -206,6 +206,7 @@ void launch_set_len(int32_t* len, int rows, const int* h_len, cudaStream_t s);
 struct RowParams {
   float temperature, rep_penalty, top_p, min_p;
   int top_k, greedy;
+  int argmax_draft;  // the draft was the argmax: q is the point mass at it
 };
 
 // Transform descriptor of one (row, position): enough to evaluate p(v) at any v.

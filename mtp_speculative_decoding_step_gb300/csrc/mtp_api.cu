@@ -324,7 +324,7 @@ mtp_status check_params(const mtp_sampling* hp, int rows) {
   for (int r = 0; r < rows; ++r) {
     const mtp_sampling& p = hp[r];
     if (!(p.temperature >= 0.f) || !(p.rep_penalty > 0.f) || !(p.top_p > 0.f && p.top_p <= 1.f) ||
-        !(p.min_p >= 0.f && p.min_p < 1.f) || p.top_k < 0 || p.top_k > 1024 || p.reserved != 0)
+        !(p.min_p >= 0.f && p.min_p < 1.f) || p.top_k < 0 || p.top_k > 1024 || (p.flags & ~MTP_SAMPLE_ARGMAX_DRAFT) != 0)
       return MTP_ERR_BAD_ARG;
   }
   return MTP_OK;
@@ -338,7 +338,17 @@ RowParams row_params(const mtp_sampling& p) {
   r.min_p = p.min_p;
   r.top_k = p.top_k;
   r.greedy = (p.temperature <= 0.f || p.top_k == 1) ? 1 : 0;
+  r.argmax_draft = (p.flags & MTP_SAMPLE_ARGMAX_DRAFT) && !r.greedy ? 1 : 0;
   return r;
+}
+
+// The parameters the draft step samples with: an argmax-drafted row drafts
+// greedily (after its repetition penalty); the verify keeps the row's own.
+mtp_sampling draft_params(const mtp_sampling& p) {
+  mtp_sampling d = p;
+  if (p.flags & MTP_SAMPLE_ARGMAX_DRAFT) d.temperature = 0.f;
+  d.flags = 0;
+  return d;
 }
 
 // Items of one head call. Head items (one per row, the row's newest pair)
@@ -812,8 +822,9 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
   const mtp_config& c = h->cfg;
   bool all_fast = true, any_sampled = false;
   for (int r = 0; r < rows; ++r) {
-    all_fast &= fast_greedy(h_params[r]);
-    any_sampled |= !row_params(h_params[r]).greedy;
+    const mtp_sampling dp = draft_params(h_params[r]);
+    all_fast &= fast_greedy(dp);
+    any_sampled |= !row_params(dp).greedy;
   }
   if (any_sampled && (!d_q || !d_u)) return MTP_ERR_BAD_ARG;
   int total = 0;
@@ -851,7 +862,7 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
   sa.mode = 0; sa.rows = rows; sa.V = V; sa.W = hist_w; sa.depth = depth;
   sa.hist = d_hist; sa.drafts = d_draft; sa.u = d_u; sa.q = d_q; sa.draft_out = d_draft;
   sa.status = h->status;
-  for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
+  for (int r = 0; r < rows; ++r) sa.p[r] = row_params(draft_params(h_params[r]));
 
   for (int k = 1; k <= depth; ++k) {
     Items itk;
@@ -917,9 +928,12 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
     return MTP_ERR_BAD_ARG;
   mtp_status st = check_params(h_params, rows);
   if (st != MTP_OK) return st;
-  bool any_sampled = false;
-  for (int r = 0; r < rows; ++r) any_sampled |= !row_params(h_params[r]).greedy;
-  if (any_sampled && !d_q) return MTP_ERR_BAD_ARG;
+  bool dense_q = false;  // some row's draft distribution is a dense q (sampled, not argmax-drafted)
+  for (int r = 0; r < rows; ++r) {
+    const RowParams rp = row_params(h_params[r]);
+    dense_q |= !rp.greedy && !rp.argmax_draft;
+  }
+  if (dense_q && !d_q) return MTP_ERR_BAD_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the host record: written by the verify kernel itself when the device can
   // address the caller's page-locked buffer, else copied after it

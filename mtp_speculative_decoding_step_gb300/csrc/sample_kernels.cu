@@ -1412,7 +1412,8 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
             bool pen = false;
             for (int t = j; t < j + a.W; ++t) pen |= sm->wtok[t] == x;
             const float pv = eval_p(desc[j], p, __ldg(lg + (size_t)j * a.V + x), pen, x);
-            const float qv = __ldg(a.q + ((size_t)r * d + j) * a.V + x);
+            // an argmax draft is a point mass: q(x) = 1
+            const float qv = p.argmax_draft ? 1.f : __ldg(a.q + ((size_t)r * d + j) * a.V + x);
             acc = qv > 0.f && uu[j] < pv / qv;
           }
         }
@@ -1431,16 +1432,19 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
     build_bitmap(sm, bits, v0, n);
     const TDesc dn = desc[nacc];
     const float* ln = lg + (size_t)nacc * a.V;
-    const float* qn = nacc < d ? a.q + ((size_t)r * d + nacc) * a.V : nullptr;
+    const float* qn = nacc < d && !p.argmax_draft ? a.q + ((size_t)r * d + nacc) * a.V : nullptr;
+    // the rejected draft of an argmax-drafted row: its q is 1 there, 0 elsewhere
+    const int xr = nacc < d && p.argmax_draft ? dr[nacc] : -1;
     float* ws = reinterpret_cast<float*>(dyn + sizeof(SampleSmem));
     // draw weights of this slice, computed once: the residual max(p - q, 0)
     // after a rejection, else p (the bonus row)
     auto stage = [&](bool residual) {
+      const bool dense_q = residual && qn != nullptr;
       const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(ln + v0) & 15) == 0 &&
-                       (!residual || (reinterpret_cast<uintptr_t>(qn + v0) & 15) == 0);
+                       (!dense_q || (reinterpret_cast<uintptr_t>(qn + v0) & 15) == 0);
       if (vec) {
         const float4* l4 = reinterpret_cast<const float4*>(ln + v0);
-        const float4* q4 = residual ? reinterpret_cast<const float4*>(qn + v0) : nullptr;
+        const float4* q4 = dense_q ? reinterpret_cast<const float4*>(qn + v0) : nullptr;
         const int n4 = n / 4;
         for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
           float4 lv[4], qv[4];
@@ -1449,7 +1453,7 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
             const int j4 = b0 + u * kST + threadIdx.x;
             if (j4 < n4) {
               lv[u] = __ldg(l4 + j4);
-              qv[u] = residual ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              qv[u] = dense_q ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
 #pragma unroll
@@ -1462,7 +1466,7 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
               for (int e = 0; e < 4; ++e) {
                 const int j = 4 * j4 + e;
                 const float pv = eval_p(dn, p, lx[e], bit(bits, j), v0 + j);
-                const float rv = residual ? pv - qx[e] : pv;
+                const float rv = residual ? pv - (v0 + j == xr ? 1.f : qx[e]) : pv;
                 ws[j] = rv > 0.f ? rv : 0.f;
               }
             }
@@ -1478,7 +1482,7 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
           const int j = b0 + u * kST + threadIdx.x;
           if (j < n) {
             lv[u] = __ldg(ln + v0 + j);
-            qv[u] = residual ? __ldg(qn + v0 + j) : 0.f;
+            qv[u] = dense_q ? __ldg(qn + v0 + j) : 0.f;
           }
         }
 #pragma unroll
@@ -1486,7 +1490,7 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
           const int j = b0 + u * kST + threadIdx.x;
           if (j < n) {
             const float pv = eval_p(dn, p, lv[u], bit(bits, j), v0 + j);
-            const float rv = residual ? pv - qv[u] : pv;
+            const float rv = residual ? pv - (v0 + j == xr ? 1.f : qv[u]) : pv;
             ws[j] = rv > 0.f ? rv : 0.f;
           }
         }
