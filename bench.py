@@ -275,6 +275,7 @@ def run_ours(args, rank, world, local_rank):
     h.close()
     flush, flush_flops, flush_bytes = ({}, 0.0, 0.0) if args.quick else measure_flush(tensors, embed, s, dev)
     sampled = None if args.quick else measure_sampled(tensors, embed, s, dev)
+    sampled_am = None if args.quick else measure_sampled(tensors, embed, s, dev, depths=(2,), argmax_draft=True)
     batched = None if args.quick else measure_batched(tensors, embed, s, dev)
 
     H, Vocab = s.hidden, s.vocab
@@ -321,6 +322,7 @@ def run_ours(args, rank, world, local_rank):
                      "bytes_per_launch": lm_bytes},
         "gpu_launches": int(launches),
         "sampled_depth_sweep": sampled,
+        "sampled_argmax_draft_depth2": sampled_am,
         "batched_8_rows": batched,
         "flush_256_pairs": {"by_offset": flush, "flops": flush_flops, "weight_bytes": flush_bytes,
                             "bf16_peak_tflops": peak_bf16(), "bound": "tensor/hbm ridge"} if flush else None,
@@ -395,12 +397,14 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
 SAMPLED = dict(temperature=0.8, rep_penalty=1.1, top_k=40, top_p=0.95, min_p=0.05)
 
 
-def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 4, 5, 6)):
+def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 4, 5, 6), argmax_draft=False):
     """Sampled decoding on the 27B-shaped head: T 0.8, repetition penalty 1.1
     over a 64-token history, top-k 40, top-p 0.95, min-p 0.05, depth 1..6.
     Target row i = the drafter's logits at step i+1 plus N(0,1) noise (the
     bonus row N(0,4)), so acceptance is partial. Reports per-position
-    acceptance, rollbacks, drafted tok/s and the verify / sampler times."""
+    acceptance, rollbacks, drafted tok/s and the verify / sampler times.
+    argmax_draft: the rows draft the argmax and the verify takes q as the
+    point mass at it (no draft sampler, no q)."""
     import torch
 
     import mtp_speculative_decoding_step_gb300 as m
@@ -408,7 +412,7 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 
     V, H, W = s.vocab, s.hidden, 64
     cap = KV_LEN + 1024
     out = {}
-    params = m.sampling_array([SAMPLED])
+    params = m.sampling_array([dict(SAMPLED, argmax_draft=argmax_draft)])
     stream = torch.cuda.current_stream()
     noise = torch.from_numpy(synth.normal(7, "smp:noise", (8, 6, V), std=1.0)).to(dev)
     bonus = torch.from_numpy(synth.normal(7, "smp:bonus", (8, V), std=4.0)).to(dev)
@@ -443,11 +447,12 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 
                 ev[0].record(stream)
                 vt, committed = 0.0, 0
             m.mtp_draft(h, depth, [P], out_tok, thid[r % 8].view(1, 7, H)[:, :depth + 1], params, draft,
-                        hist=hist, u=ud[r], q=q, logits=dl)
+                        hist=hist, u=None if argmax_draft else ud[r], q=None if argmax_draft else q, logits=dl)
             tl[0, :depth] = dl[0] + noise[r % 8, :depth]
             tl[0, depth] = bonus[r % 8]
             ev[1].record(stream)
-            m.spec_verify(tl, draft, params, uv[r], n_acc, out_tok, ws, q=q, hist=hist, stats=stats, h_out=h_out)
+            m.spec_verify(tl, draft, params, uv[r], n_acc, out_tok, ws, q=None if argmax_draft else q, hist=hist,
+                          stats=stats, h_out=h_out)
             ev[2].record(stream)
             m.kv_rollback(h, 1, depth)
             if r % 64 == 63:
@@ -471,7 +476,8 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 
                            "draft_tok_per_s": round(rounds * depth / (ms / 1e3), 1),
                            "committed_tok_per_s": round(committed / (ms / 1e3), 1),
                            "verify_us": round(1e3 * vt / rounds, 2),
-                           "draft_sampler_us": round(1e3 * prof["sample"][0] / max(prof["sample"][1], 1), 2)}
+                           "draft_sampler_us": round(1e3 * prof["sample"][0] / max(prof["sample"][1], 1), 2)
+                           if prof["sample"][1] else 0.0}
         h.close()
     return out
 
