@@ -231,6 +231,33 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
                        int32_t* d_stats, int32_t* h_out, void* d_workspace);
 
 /*
+ * Draft-depth controller (host-side; "Ollama qwen3_5 MTP loader and SelfDraft
+ * path", Facts: depth control; Ollama MLX-runner commit "choose the
+ * speculative draft length to maximize throughput"). It picks the depth N in
+ * [0, max_depth] that maximises committed(N) / cost(N): committed(N) =
+ * 1 + sum_{i<=N} prod_{j<=i} a_j from per-position acceptance a_j (Laplace-
+ * smoothed counts of rounds that reached position j), cost(N) = the mean
+ * measured seconds of a round at depth N (an unmeasured depth extends its
+ * measured neighbours linearly). N never exceeds one past the deepest position
+ * with data. Every 4th round it returns one past its choice (a probe); while
+ * the choice is plain decode each probe doubles that interval, up to 512
+ * rounds. Before any other choice it runs one round of plain decode (depth 0)
+ * to measure the base cost.
+ * State persists for the object's lifetime. No GPU work; not thread-safe.
+ *   mtp_depth_ctl_next: depth to draft this round (0 = plain decode).
+ *   mtp_depth_ctl_observe: feed back the round actually run (depth, accepted
+ *     drafts n_acc <= depth, wall-clock seconds > 0); BAD_ARG otherwise.
+ *   mtp_depth_ctl_state: optional host outputs a[max_depth] (acceptance
+ *     estimates), cost[max_depth+1] (seconds per round), the probe interval.
+ */
+typedef struct mtp_depth_ctl* mtp_depth_ctl_t;
+mtp_status mtp_depth_ctl_create(int32_t max_depth, mtp_depth_ctl_t* out);
+void mtp_depth_ctl_free(mtp_depth_ctl_t c);
+int32_t mtp_depth_ctl_next(mtp_depth_ctl_t c);
+mtp_status mtp_depth_ctl_observe(mtp_depth_ctl_t c, int32_t depth, int32_t n_acc, double round_seconds);
+mtp_status mtp_depth_ctl_state(mtp_depth_ctl_t c, double* h_accept, double* h_cost, int32_t* h_interval);
+
+/*
  * spec_verify_noalloc — spec_verify without a caller-provided workspace, for
  * callers that cannot allocate device memory (a host whose own pool owns all
  * device memory, or code running where a cudaMalloc would stall the device or

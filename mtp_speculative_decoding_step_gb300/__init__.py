@@ -32,6 +32,8 @@ EXPORTS = (
     "mtp_set_lengths", "mtp_device_status", "mtp_flush", "mtp_draft", "spec_verify_workspace_bytes",
     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_kinds", "mtp_profile_kind_name",
     "mtp_profile_read", "mtp_kernel_launches", "spec_verify_noalloc",
+    "mtp_depth_ctl_create", "mtp_depth_ctl_free", "mtp_depth_ctl_next", "mtp_depth_ctl_observe",
+    "mtp_depth_ctl_state",
 )
 
 
@@ -309,3 +311,45 @@ def mtp_profile_read(h: Handle) -> dict:
 
 def mtp_kernel_launches() -> int:
     return int(lib().mtp_kernel_launches())
+
+
+class DepthController:
+    """Draft-depth controller (host-side, in libmtp): next() is the depth to
+    draft this round, observe(depth, n_acc, seconds) feeds back the round run."""
+
+    def __init__(self, max_depth: int):
+        L = lib()
+        L.mtp_depth_ctl_create.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p)]
+        L.mtp_depth_ctl_next.argtypes = [ctypes.c_void_p]
+        L.mtp_depth_ctl_next.restype = ctypes.c_int32
+        L.mtp_depth_ctl_observe.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double]
+        L.mtp_depth_ctl_state.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.mtp_depth_ctl_free.argtypes = [ctypes.c_void_p]
+        self.max_depth = max_depth
+        self.ptr = ctypes.c_void_p()
+        _check(L.mtp_depth_ctl_create(max_depth, ctypes.byref(self.ptr)), "mtp_depth_ctl_create")
+
+    def next(self) -> int:
+        return int(lib().mtp_depth_ctl_next(self.ptr))
+
+    def observe(self, depth: int, n_acc: int, seconds: float) -> None:
+        _check(lib().mtp_depth_ctl_observe(self.ptr, depth, n_acc, float(seconds)), "mtp_depth_ctl_observe")
+
+    def state(self):
+        a = np.zeros(max(self.max_depth, 1), np.float64)
+        c = np.zeros(self.max_depth + 1, np.float64)
+        iv = ctypes.c_int32(0)
+        _check(lib().mtp_depth_ctl_state(self.ptr, a.ctypes.data, c.ctypes.data, ctypes.byref(iv)),
+               "mtp_depth_ctl_state")
+        return a[: self.max_depth], c, int(iv.value)
+
+    def close(self):
+        if self.ptr:
+            lib().mtp_depth_ctl_free(self.ptr)
+            self.ptr = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
