@@ -71,7 +71,8 @@ class _Model(ctypes.Structure):
                 ("dh", ctypes.c_int), ("I", ctypes.c_int), ("V", ctypes.c_int),
                 ("eps", ctypes.c_double), ("theta", ctypes.c_double), ("wdt", ctypes.c_int)] + \
                [(n, ctypes.c_void_p) for n in ("E", "lm", "fc", "wq", "wk", "wv", "wo", "wg", "wu", "wd")] + \
-               [(n, ctypes.c_void_p) for n in ("n_emb", "n_hid", "n_in", "n_post", "n_qn", "n_kn", "n_fin")]
+               [(n, ctypes.c_void_p) for n in ("n_emb", "n_hid", "n_in", "n_post", "n_qn", "n_kn", "n_fin")] + \
+               [("lmq", ctypes.c_void_p), ("lmq_scale", ctypes.c_void_p)]
 
 
 class Params(ctypes.Structure):
@@ -97,8 +98,38 @@ def _load():
         lib.orc_draw.argtypes = [vp, ci, ctypes.c_float, vp]
         lib.orc_draw.restype = ci
         lib.orc_verify_row.argtypes = [ci, ci, vp, vp, vp, vp, vp, ci, vp, vp, vp, vp]
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_decode.restype = ctypes.c_float
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_quantize_rows_e4m3.argtypes = [vp, ci, ci, vp, vp]
         _lib = lib
     return _lib
+
+
+def e4m3_encode(x: float) -> int:
+    """fp8 e4m3 code of x: round to nearest even, finite values beyond 448
+    saturate to 448."""
+    return int(_load().orc_e4m3_encode(float(x)))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(_load().orc_e4m3_decode(int(c)))
+
+
+def quantize_rows_e4m3(w: np.ndarray):
+    """Per-row fp8 e4m3 quantisation of a [rows, cols] matrix (bf16 bit
+    patterns or fp32): scale = max|w| / 448 per row, code = e4m3(w / scale),
+    in fp32. Returns (codes uint8 [rows, cols], scales fp32 [rows])."""
+    a = np.ascontiguousarray(w)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << 16).view(np.float32)
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    rows, cols = a.shape
+    q = np.zeros((rows, cols), np.uint8)
+    sc = np.zeros(rows, np.float32)
+    _load().orc_quantize_rows_e4m3(_c(a), rows, cols, _c(q), _c(sc))
+    return q, sc
 
 
 def make_params(temperature=0.0, rep_penalty=1.0, top_k=0, top_p=1.0, min_p=0.0) -> Params:
@@ -154,7 +185,10 @@ def load_norms(tensors: dict) -> tuple[dict, bool]:
 class Head:
     """The MTP head with its borrowed tied lm_head, on host arrays."""
 
-    def __init__(self, shape, tensors: dict, embed: np.ndarray, lm_head: np.ndarray | None = None):
+    def __init__(self, shape, tensors: dict, embed: np.ndarray, lm_head: np.ndarray | None = None,
+                 lm_fp8: tuple | None = None):
+        """lm_fp8: (codes [V, H] uint8, scales [V] fp32) of a quantised draft
+        head; the logits then use it (the embedding gather keeps `embed`)."""
         self.s = shape
         self.norms, self.raw_hf = load_norms(tensors)
         w = {(n[4:] if self.raw_hf else n): np.ascontiguousarray(a) for n, a in tensors.items()}
@@ -180,6 +214,10 @@ class Head:
         m.n_qn = _c(nm[L + "self_attn.q_norm.weight"])
         m.n_kn = _c(nm[L + "self_attn.k_norm.weight"])
         m.n_fin = _c(nm["norm.weight"])
+        if lm_fp8 is not None:
+            self._q = np.ascontiguousarray(lm_fp8[0], dtype=np.uint8)
+            self._qs = np.ascontiguousarray(lm_fp8[1], dtype=np.float32)
+            m.lmq, m.lmq_scale = _c(self._q), _c(self._qs)
         self.m = m
 
     # ------------------------------------------------------------------

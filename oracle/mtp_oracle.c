@@ -69,6 +69,10 @@ typedef struct {
   const void *E, *lm, *fc, *wq, *wk, *wv, *wo, *wg, *wu, *wd;
   /* the seven RMSNorm weights, already carrying the layout's +1.0 shift */
   const double *n_emb, *n_hid, *n_in, *n_post, *n_qn, *n_kn, *n_fin;
+  /* optional fp8 draft head: e4m3 codes [V][H] and one scale per row; when
+   * set, the logits use them instead of lm (the embedding gather keeps E) */
+  const uint8_t* lmq;
+  const float* lmq_scale;
 } orc_model;
 
 /* y[n] = sum_k W[n,k] x[k];  W row-major [N,K] (a Linear's weight). */
@@ -79,6 +83,57 @@ static void matvec(const void* W, int dt, int N, int K, const double* x, double*
     size_t base = (size_t)n * (size_t)K;
     for (int k = 0; k < K; ++k) acc += get(W, dt, base + k) * x[k];
     y[n] = acc;
+  }
+}
+
+/* ---------------------------------------------------------- fp8 e4m3
+ * The 8-bit float with 1 sign bit, 4 exponent bits (bias 7) and 3 mantissa
+ * bits, no infinities, the all-ones magnitude pattern NaN, largest finite 448.
+ * A draft-only quantised copy of the tied output head ("Ollama qwen3_5 MTP
+ * loader and SelfDraft path", Facts: the draft's tied output head quantized;
+ * format unstated, read as e4m3 with one fp32 scale per row). */
+float orc_e4m3_decode(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 15, mant = c & 7;
+  double v;
+  if (e == 15 && mant == 7) return NAN;
+  if (e == 0) v = ldexp((double)mant, -9);          /* subnormal: m/8 * 2^-6 */
+  else v = ldexp(1.0 + mant / 8.0, e - 7);
+  return (float)(s ? -v : v);
+}
+
+/* Round to nearest (ties to even), saturating finite values beyond 448 to
+ * 448; NaN -> the NaN code. */
+uint8_t orc_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const int s = signbit(x) ? 1 : 0;
+  double a = fabs((double)x);
+  if (a > 448.0) a = 448.0;
+  uint8_t c;
+  if (a < ldexp(1.0, -6)) {                 /* subnormal range: steps of 2^-9 */
+    const double m = rint(a * 512.0);       /* m == 8 lands on the smallest normal */
+    c = (uint8_t)(m >= 8.0 ? (1 << 3) : (int)m);
+  } else {
+    int e;
+    frexp(a, &e);
+    e -= 1;                                 /* 2^e <= a < 2^(e+1) */
+    double m = rint((ldexp(a, -e) - 1.0) * 8.0);
+    if (m >= 8.0) { m = 0.0; e += 1; }
+    if (e > 8 || (e == 8 && m > 6.0)) { e = 8; m = 6.0; }   /* 448 */
+    c = (uint8_t)(((e + 7) << 3) | (int)m);
+  }
+  return (uint8_t)((s << 7) | c);
+}
+
+/* Per-row quantisation, the decisions in fp32: scale = max|w| / 448 (1 for an
+ * all-zero row), code = e4m3(w / scale). */
+void orc_quantize_rows_e4m3(const float* w, int rows, int cols, uint8_t* q, float* scale) {
+  for (int r = 0; r < rows; ++r) {
+    const float* row = w + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int k = 0; k < cols; ++k) amax = fabsf(row[k]) > amax ? fabsf(row[k]) : amax;
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scale[r] = sc;
+    for (int k = 0; k < cols; ++k) q[(size_t)r * cols + k] = orc_e4m3_encode(row[k] / sc);
   }
 }
 
@@ -219,7 +274,18 @@ int orc_step(const orc_model* m, int tok, const void* hid, int hid_dt, void* Kc,
     for (int i = 0; i < H; ++i) h2[i] = (double)(float)h2[i];
     rmsnorm(h2, H, m->n_fin, m->eps, c);
     double* lg = malloc(sizeof(double) * m->V);
-    matvec(m->lm, m->wdt, m->V, H, c, lg);
+    if (m->lmq) {
+      /* logits[v] = scale[v] * sum_k e4m3(q[v,k]) * x[k] */
+#pragma omp parallel for schedule(static)
+      for (int n = 0; n < m->V; ++n) {
+        double acc = 0.0;
+        const uint8_t* row = m->lmq + (size_t)n * H;
+        for (int k = 0; k < H; ++k) acc += (double)orc_e4m3_decode(row[k]) * c[k];
+        lg[n] = (double)m->lmq_scale[n] * acc;
+      }
+    } else {
+      matvec(m->lm, m->wdt, m->V, H, c, lg);
+    }
     for (int i = 0; i < m->V; ++i) logits_out[i] = (float)lg[i];
     free(lg);
   }

@@ -467,3 +467,64 @@ def test_verify_bonus_comes_from_last_row_when_all_accepted():
     n, out, _ = oracle.verify_row(lg, drafts, p[:d], P(1.0), np.zeros(0, np.int32), u)
     assert n == 2
     assert out[2] == int(np.searchsorted(np.cumsum(p[2].astype(np.float64)), 0.37 * p[2].astype(np.float64).sum(), side="right"))
+
+
+# ------------------------------------------------------------ fp8 draft head
+def test_e4m3_codes_match_torch_float8():
+    """The oracle's e4m3 encoder against torch's float8_e4m3fn conversion
+    (round to nearest even) on normals, subnormals, ties and the top of the
+    range, below the point where torch turns to NaN; and every code decodes
+    to torch's value."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([
+        rng.standard_normal(4000) * 30, rng.standard_normal(2000) * 0.01, rng.uniform(-463.9, 463.9, 2000),
+        # exact ties between neighbouring codes: the midpoints of 1.0/1.125, 1.125/1.25, of two subnormals
+        np.array([1.0625, 1.1875, 3 * 2.0 ** -10, 2.0 ** -10, 448.0, -448.0, 0.0, -0.0, 2.0 ** -6, 2.0 ** -9]),
+    ]).astype(np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x)) for x in xs], np.uint8)
+    np.testing.assert_array_equal(got, want)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    dec = np.array([oracle.e4m3_decode(int(c)) for c in codes], np.float32)
+    np.testing.assert_array_equal(dec, ref)
+
+
+def test_e4m3_saturates_and_row_quantisation_bounds():
+    assert oracle.e4m3_encode(500.0) == 0x7E and oracle.e4m3_encode(-1e9) == 0xFE  # +-448
+    rng = np.random.default_rng(6)
+    w = (rng.standard_normal((16, 300)) * rng.uniform(0.01, 3.0, (16, 1))).astype(np.float32)
+    q, sc = oracle.quantize_rows_e4m3(w)
+    for r in range(16):
+        amax = float(np.max(np.abs(w[r])))
+        assert sc[r] == np.float32(amax) / np.float32(448.0)
+        # the largest magnitude takes the largest code
+        assert np.max(q[r] & 0x7F) == 0x7E
+        dq = np.array([oracle.e4m3_decode(int(c)) for c in q[r]], np.float64) * sc[r]
+        err = np.abs(dq - w[r])
+        # half a step of a 3-bit mantissa (1/16 relative) for normals, half the
+        # smallest subnormal step (2^-10 * scale) below 2^-6 * scale
+        bound = np.maximum(np.abs(w[r]) / 16.0, 2.0 ** -10 * sc[r]) * (1 + 1e-6)
+        assert np.all(err <= bound)
+
+
+def test_fp8_head_equals_the_bf16_head_on_exactly_representable_rows():
+    """A head whose rows are e4m3 values scaled by max 448 quantises without
+    loss, so the fp8 logits reduce to the bf16 head's."""
+    s = synth.TINY
+    model = synth.make_model(s, 44)
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 0x7E, (s.vocab, s.hidden)).astype(np.uint8) | (rng.integers(0, 2, (s.vocab, s.hidden)) << 7).astype(np.uint8)
+    codes[:, 0] = 0x7E  # each row's largest magnitude is 448: scale 1
+    lm = np.array([[oracle.e4m3_decode(int(c)) for c in row] for row in codes], np.float32)
+    q, sc = oracle.quantize_rows_e4m3(lm)
+    np.testing.assert_array_equal(q, codes)
+    np.testing.assert_array_equal(sc, np.ones(s.vocab, np.float32))
+    h_ref = oracle.Head(s, model.tensors, model.embed, lm_head=lm)
+    h_q = oracle.Head(s, model.tensors, model.embed, lm_head=lm, lm_fp8=(q, sc))
+    K, V = synth.kv_prefill(s, 44, 1, 64, [10])
+    hid = synth.normal(44, "h", (s.hidden,))
+    _, l1 = h_ref.step(5, hid, K[0].copy(), V[0].copy(), 10)
+    _, l2 = h_q.step(5, hid, K[0].copy(), V[0].copy(), 10)
+    np.testing.assert_allclose(l2, l1, rtol=1e-6, atol=1e-6 * np.max(np.abs(l1)))
