@@ -231,6 +231,25 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
                        int32_t* d_stats, int32_t* h_out, void* d_workspace);
 
 /*
+ * mtp_set_draft_head — which copy of the tied output head the drafter reads.
+ * MTP_HEAD_BF16 (the default): the borrowed head itself. MTP_HEAD_FP8: an fp8
+ * e4m3 copy with one fp32 scale per row (scale = max|row| / 448, codes =
+ * e4m3(w / scale), round to nearest even, saturating), made from the borrowed
+ * head by this call and owned by the handle (vocab * hidden bytes + vocab
+ * floats, allocated on the first request). The draft logits become
+ * scale[v] * sum_k e4m3(code[v,k]) * x[k]: half the head's bytes per draft
+ * step, a draft-only change ("Ollama qwen3_5 MTP loader and SelfDraft path",
+ * Facts: quantizing the draft's tied output head; the format is not stated
+ * there). spec_verify is untouched: it reads the target's logits. Call again
+ * after the borrowed head's contents change. bf16 heads only; asynchronous on
+ * the stream. Errors: BAD_ARG, CONFIG_BOUNDS (fp32 head or hidden % 16),
+ * CUDA.
+ */
+#define MTP_HEAD_BF16 0
+#define MTP_HEAD_FP8 1
+mtp_status mtp_set_draft_head(mtp_t h, mtp_stream stream, int32_t format);
+
+/*
  * Draft-depth controller (host-side; "Ollama qwen3_5 MTP loader and SelfDraft
  * path", Facts: depth control; Ollama MLX-runner commit "choose the
  * speculative draft length to maximize throughput"). It picks the depth N in

@@ -33,7 +33,7 @@ EXPORTS = (
     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_kinds", "mtp_profile_kind_name",
     "mtp_profile_read", "mtp_kernel_launches", "spec_verify_noalloc",
     "mtp_depth_ctl_create", "mtp_depth_ctl_free", "mtp_depth_ctl_next", "mtp_depth_ctl_observe",
-    "mtp_depth_ctl_state",
+    "mtp_depth_ctl_state", "mtp_set_draft_head",
 )
 
 
@@ -311,6 +311,17 @@ def mtp_profile_read(h: Handle) -> dict:
 
 def mtp_kernel_launches() -> int:
     return int(lib().mtp_kernel_launches())
+
+
+MTP_HEAD_BF16, MTP_HEAD_FP8 = 0, 1
+
+
+def mtp_set_draft_head(h: Handle, fmt: int, stream=None) -> None:
+    """MTP_HEAD_FP8: the drafter reads an e4m3 copy of the tied head (per-row
+    scales); MTP_HEAD_BF16: the borrowed head itself."""
+    L = lib()
+    L.mtp_set_draft_head.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    _check(L.mtp_set_draft_head(h.ptr, _stream(stream), int(fmt)), "mtp_set_draft_head")
 
 
 class DepthController:

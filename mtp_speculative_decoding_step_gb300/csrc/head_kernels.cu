@@ -13,6 +13,7 @@
 // weight matrix exactly once with 16-byte L1-bypassing loads, keeps the
 // activations (fp32) in shared memory and accumulates in fp32.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -45,6 +46,29 @@ struct Vec<float> {  // 4 fp32 per 16-byte vector
   __device__ __forceinline__ static void unpack(const uint4& w, float* f) {
     f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
     f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+  }
+};
+
+// fp8 e4m3 weights (the quantised draft head): 16 per 16-byte vector, widened
+// exactly through f16 pairs.
+struct fp8e4m3 {
+  uint8_t v;
+};
+template <>
+struct Vec<fp8e4m3> {
+  static constexpr int N = 16;
+  __device__ __forceinline__ static void unpack(const uint4& w, float* f) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t h0, h1;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((unsigned short)(wd[i] & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((unsigned short)(wd[i] >> 16)));
+      f[4 * i + 0] = __half2float(__ushort_as_half((unsigned short)(h0 & 0xFFFFu)));
+      f[4 * i + 1] = __half2float(__ushort_as_half((unsigned short)(h0 >> 16)));
+      f[4 * i + 2] = __half2float(__ushort_as_half((unsigned short)(h1 & 0xFFFFu)));
+      f[4 * i + 3] = __half2float(__ushort_as_half((unsigned short)(h1 >> 16)));
+    }
   }
 };
 
@@ -246,6 +270,14 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
     }
     return;
   }
+  if (a.wscale) {  // per-row scales of quantised weights
+    __syncthreads();
+    for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
+      const int m = t / ROWS, l = t - m * ROWS;
+      s_out[m][l] *= a.wscale[(size_t)group * ROWS + l];
+    }
+    __syncthreads();
+  }
   for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
     const int m = t / ROWS, l = t - m * ROWS;
     const size_t n = (size_t)group * ROWS + l;
@@ -400,6 +432,15 @@ static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
 }
 
 void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
+  if (a.wdt == kDtypeFp8) {
+    switch (mt) {
+      case 1: launch_gemv_t<fp8e4m3, 1>(a, smem, s); break;
+      case 2: launch_gemv_t<fp8e4m3, 2>(a, smem, s); break;
+      case 4: launch_gemv_t<fp8e4m3, 4>(a, smem, s); break;
+      default: launch_gemv_t<fp8e4m3, 8>(a, smem, s); break;
+    }
+    return;
+  }
   const bool bf = a.wdt == MTP_DTYPE_BF16;
   switch (mt) {
     case 1: bf ? launch_gemv_t<uint16_t, 1>(a, smem, s) : launch_gemv_t<float, 1>(a, smem, s); break;
@@ -407,6 +448,35 @@ void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
     case 4: bf ? launch_gemv_t<uint16_t, 4>(a, smem, s) : launch_gemv_t<float, 4>(a, smem, s); break;
     default: bf ? launch_gemv_t<uint16_t, 8>(a, smem, s) : launch_gemv_t<float, 8>(a, smem, s); break;
   }
+}
+
+// One block per row of a bf16 matrix: scale = max|w| / 448 (1 for an all-zero
+// row), codes = e4m3(w / scale), round to nearest even, saturating.
+__global__ void k_quant_e4m3(const uint16_t* w, int cols, uint8_t* q, float* scale) {
+  __shared__ float red[32];
+  const uint16_t* row = w + (size_t)blockIdx.x * cols;
+  float amax = 0.f;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x) amax = fmaxf(amax, fabsf(bf16_to_f(row[k])));
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+  const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+  if (threadIdx.x == 0) scale[blockIdx.x] = sc;
+  uint16_t* qr = reinterpret_cast<uint16_t*>(q + (size_t)blockIdx.x * cols);
+  for (int k = threadIdx.x; k < cols / 2; k += blockDim.x) {
+    const float x0 = bf16_to_f(row[2 * k]) / sc, x1 = bf16_to_f(row[2 * k + 1]) / sc;
+    unsigned short c;
+    // the second operand lands in the low byte: element 2k first in memory
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(x1), "f"(x0));
+    qr[k] = c;
+  }
+}
+
+void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s) {
+  k_quant_e4m3<<<rows, 256, 0, s>>>(w, cols, q, scale);
+  count_launch();
 }
 
 // ------------------------------------------------- q/k norm, RoPE, KV append

@@ -49,7 +49,12 @@ struct GemvArgs {
   int32_t* amax_out;
   int amax_idx[8];
   int32_t* status;
+  const float* wscale;  // per-row scales of quantised weights (fp8), or null
 };
+// weight dtype code of the quantised (fp8 e4m3) draft head, beside MTP_DTYPE_*
+constexpr int kDtypeFp8 = 8;
+// Per-row e4m3 quantisation of a bf16 [rows][cols] matrix (cols even).
+void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s);
 
 // rows per block group for a batch width MT
 inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }

@@ -90,6 +90,9 @@ struct mtp_handle {
   uint16_t* x2 = nullptr;                 // hi/lo bf16 activations of the tensor-core GEMV
   float* tvpart = nullptr;                // its split-K partials
   bool tc_gemv = false;                   // batched GEMVs on tcgen05 (bf16 weights)
+  uint8_t* lmq = nullptr;                 // fp8 e4m3 copy of the draft head (mtp_set_draft_head)
+  float* lmq_scale = nullptr;             // its per-row scales
+  bool lm_fp8 = false;
   int32_t* status = nullptr;
   size_t part_floats = 0;
   int max_chunks = 0, lm_groups_max = 0, counters_n = 0;
@@ -192,6 +195,8 @@ struct GemvJob {
   int hid_dt;
   int32_t* amax_out;
   const int* amax_idx;
+  bool fp8;               // w[0] holds e4m3 codes with per-row scales wscale
+  const float* wscale;
 };
 
 // Batches of at least this many items run their GEMVs on the tensor cores:
@@ -280,7 +285,7 @@ bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
 }
 
 void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
-  if (h->tc_gemv && M >= kTcGemvMinItems && run_gemv_tc(h, j, M, s)) return;
+  if (!j.fp8 && h->tc_gemv && M >= kTcGemvMinItems && run_gemv_tc(h, j, M, s)) return;
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mp = std::min(8, M - m0);
     const GemvPlan pl = plan_gemv(j.N, j.K, mp, j.dual, h->sms);
@@ -288,7 +293,8 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     std::memset(&a, 0, sizeof(a));
     for (int i = 0; i < 3; ++i) { a.w[i] = j.w[i]; a.seg_end[i] = j.seg_end[i]; }
     a.N = j.N; a.K = j.K; a.S = pl.S; a.ngroups = pl.ngroups;
-    a.pro = j.pro; a.epi = j.epi; a.M = mp; a.wdt = h->cfg.dtype;
+    a.pro = j.pro; a.epi = j.epi; a.M = mp; a.wdt = j.fp8 ? kDtypeFp8 : h->cfg.dtype;
+    a.wscale = j.fp8 ? j.wscale : nullptr;
     a.x = j.x ? j.x + (size_t)m0 * j.ldx : nullptr;
     a.ldx = j.ldx;
     a.nw = j.nw; a.nw2 = j.nw2; a.eps = h->cfg.eps;
@@ -474,7 +480,10 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
   {
     ProfScope ps(h, s, PK_LMHEAD);
     std::memset(&j, 0, sizeof(j));
-    j.w[0] = h->lm; j.seg_end[0] = c.vocab; j.seg_end[1] = c.vocab; j.seg_end[2] = c.vocab;
+    j.w[0] = h->lm_fp8 ? static_cast<const void*>(h->lmq) : h->lm;
+    j.fp8 = h->lm_fp8;
+    j.wscale = h->lmq_scale;
+    j.seg_end[0] = c.vocab; j.seg_end[1] = c.vocab; j.seg_end[2] = c.vocab;
     j.N = c.vocab; j.K = H; j.pro = PRO_NORM; j.epi = EPI_LOGITS;
     j.x = h->h2; j.ldx = H; j.nw = h->nrm[T_NORM]; j.y = logits; j.ldy = ld_logits;
     j.amax_out = amax_out; j.amax_idx = amax_out ? amax_idx.data() : nullptr;
@@ -550,6 +559,22 @@ mtp_status flush_tensor_cores(mtp_handle* h, const Items& all, int m0, int mp, c
 extern "C" {
 
 int32_t mtp_default_block_size(const mtp_config* cfg) { return cfg ? cfg->mtp_layers + 2 : -1; }
+
+mtp_status mtp_set_draft_head(mtp_t h, mtp_stream stream, int32_t format) {
+  if (!h || (format != MTP_HEAD_BF16 && format != MTP_HEAD_FP8)) return MTP_ERR_BAD_ARG;
+  const mtp_config& c = h->cfg;
+  if (format == MTP_HEAD_FP8) {
+    if (c.dtype != MTP_DTYPE_BF16 || c.hidden % 16 != 0) return MTP_ERR_CONFIG_BOUNDS;
+    mtp_status st = MTP_OK;
+    if (!h->lmq) st = alloc(h, &h->lmq, (size_t)c.vocab * c.hidden);
+    if (st == MTP_OK && !h->lmq_scale) st = alloc(h, &h->lmq_scale, (size_t)c.vocab);
+    if (st != MTP_OK) return st;
+    launch_quant_e4m3(static_cast<const uint16_t*>(h->lm), c.vocab, c.hidden, h->lmq, h->lmq_scale,
+                      reinterpret_cast<cudaStream_t>(stream));
+  }
+  h->lm_fp8 = format == MTP_HEAD_FP8;
+  return cuda_ok(cudaGetLastError());
+}
 
 const char* mtp_status_str(mtp_status s) {
   switch (s) {
