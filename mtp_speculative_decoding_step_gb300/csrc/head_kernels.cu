@@ -743,15 +743,16 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
     if (__syncthreads_or(!got)) { ok = false; break; }
     const KT* kt = ks + slot * TS * DH;
     const KT* vt = vs + slot * TS * DH;
-    // scores: warp w takes keys 8w..8w+7 of the tile; lane owns EPL dims of
-    // every key; the 8 keys x 8 head slots of partial dots are reduced across
-    // the warp by a halving butterfly (62 shuffles), leaving lane l with the
-    // sums of key l/4, head slots 2(l%4) and 2(l%4)+1.
+    // scores: warp w takes keys KPW*w .. KPW*w + KPW-1 of the tile; lane owns
+    // EPL dims of every key; the KPW keys x 8 head slots of partial dots are
+    // reduced across the warp by a halving butterfly, leaving lane l with the
+    // NF sums t = l*NF + u (u < NF) of key t/8, head slot t%8.
     {
-      float v[64];
-      const int kb = warp * 8;
+      constexpr int KPW = TS / 8, NV = KPW * 8, NF = NV / 32;
+      float v[NV];
+      const int kb = warp * KPW;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < KPW; ++kk) {
         float kv[EPL];
         const int j = kb + kk < rows ? kb + kk : rows - 1;
         const KT* kr = kt + (size_t)j * DH + lane * EPL;
@@ -769,7 +770,7 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
         }
       }
 #pragma unroll
-      for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
+      for (int o = 16, n = NV; o >= 1; o >>= 1, n >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int t = 0; t < n / 2; ++t) {
@@ -778,10 +779,10 @@ __global__ void __launch_bounds__(256) k_attn_chunk(const __grid_constant__ Attn
           v[t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
         }
       }
-      const int key = kb + lane / 4, h0 = 2 * (lane % 4);
-      if (key < rows) {
-        if (h0 < G) ps[h0 * TS + key] = v[0] * a.scale;
-        if (h0 + 1 < G) ps[(h0 + 1) * TS + key] = v[1] * a.scale;
+#pragma unroll
+      for (int u = 0; u < NF; ++u) {
+        const int t = lane * NF + u, key = kb + t / 8, h = t % 8;
+        if (key < rows && h < G) ps[h * TS + key] = v[u] * a.scale;
       }
     }
     __syncthreads();
