@@ -170,6 +170,8 @@ def run_ours(args, rank, world, local_rank):
     klen = torch.tensor([KV_LEN], dtype=torch.int32, device=dev)
     cfg = m.make_config(s, 1, KV_LEN + 1024, DEPTH)
     h = m.mtp_load(cfg, tensors, embed, None, kk, vv, klen, lengths=[KV_LEN])
+    if args.fp8_head:
+        m.mtp_set_draft_head(h, m.MTP_HEAD_FP8)
     params = m.sampling_array([dict(temperature=0.0)])
     base_d = to(base)
     thid_d = to(thid)
@@ -627,6 +629,8 @@ def main():
                     help="time only sampled rounds at depth 1 (profiling case)")
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the 8-row batched draft + verify (profiling case)")
+    ap.add_argument("--fp8-head", action="store_true",
+                    help="draft with the fp8 copy of the tied head throughout (profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
