@@ -153,57 +153,73 @@ template <int MT>
 __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, float* red) {
   const int tid = threadIdx.x;
   if (a.pro == PRO_DUAL) {
-    // x = [norm_e(E[tok]) ; norm_h(hidden)]; this block's slice lies in one half.
+    // x = [norm_e(E[tok]) ; norm_h(hidden)]; this block's slice may take a
+    // part of each half, and each part needs its half's norm.
     const int H = a.K / 2;
-    const bool emb = k0 < H;
-    const float* nw = emb ? a.nw : a.nw2;
-    const int kk0 = emb ? k0 : k0 - H;
-    const void* src = emb ? a.E : a.hid;
-    const int dt = emb ? a.wdt : a.hid_dt;
-    size_t base[MT];
+    const int ke1 = min(k0 + KS, H), kh0 = max(k0, H);
+    const bool use_e = k0 < ke1, use_h = kh0 < k0 + KS;
+    size_t be[MT], bh[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      base[m] = 0;
+      be[m] = 0;
+      bh[m] = 0;
       if (m < a.M) {
-        int t = emb ? a.tok[a.tok_idx[m]] : 0;
+        int t = a.tok[a.tok_idx[m]];
         if (t < 0 || t >= a.vocab) {  // a bad token id reads row 0 and raises the status word
-          if (tid == 0) flag_status(a.status, MTP_ERR_BAD_ARG);
+          if (tid == 0 && use_e) flag_status(a.status, MTP_ERR_BAD_ARG);
           t = 0;
         }
-        base[m] = emb ? (size_t)t * (size_t)H : (size_t)a.hid_off[m];
+        be[m] = (size_t)t * (size_t)H;
+        bh[m] = (size_t)a.hid_off[m];
       }
     }
-    float ss[MT];
+    float ss[2 * MT];  // [0, MT): embedding rows, [MT, 2 MT): hidden rows
 #pragma unroll
-    for (int m = 0; m < MT; ++m) ss[m] = 0.f;
-    if (dt == MTP_DTYPE_BF16) {
-      for (int i = tid; i < H / 8; i += blockDim.x) {
+    for (int m = 0; m < 2 * MT; ++m) ss[m] = 0.f;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < a.M) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + base[m]) + i);
-            const float f[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                                bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+    for (int half = 0; half < 2; ++half) {
+      if (half == 0 ? !use_e : !use_h) continue;
+      const void* src = half == 0 ? a.E : a.hid;
+      const int dt = half == 0 ? a.wdt : a.hid_dt;
+      if (dt == MTP_DTYPE_BF16) {
+        for (int i = tid; i < H / 8; i += blockDim.x) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ss[m] = fmaf(f[j], f[j], ss[m]);
+          for (int m = 0; m < MT; ++m) {
+            if (m < a.M) {
+              const size_t b = half == 0 ? be[m] : bh[m];
+              const uint4 w = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(src) + b) + i);
+              const float f[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                                  bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+              float& acc = ss[half * MT + m];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc = fmaf(f[j], f[j], acc);
+            }
+          }
+        }
+      } else {
+        for (int i = tid; i < H / 4; i += blockDim.x) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m < a.M) {
+              const size_t b = half == 0 ? be[m] : bh[m];
+              const float4 v = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + b) + i);
+              float& acc = ss[half * MT + m];
+              acc = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, acc))));
+            }
           }
         }
       }
-    } else {
-      for (int i = tid; i < H / 4; i += blockDim.x) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < a.M) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + base[m]) + i);
-            ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
-          }
-        }
-      }
     }
-    block_sum_n<MT>(ss, red);
+    block_sum_n<2 * MT>(ss, red);
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-      if (m < a.M) row_stage(xs + m * KS, src, dt, base[m] + kk0, KS, rsqrtf(ss[m] / (float)H + a.eps), nw + kk0);
+    for (int m = 0; m < MT; ++m) {
+      if (m >= a.M) continue;
+      if (use_e)
+        row_stage(xs + m * KS, a.E, a.wdt, be[m] + k0, ke1 - k0, rsqrtf(ss[m] / (float)H + a.eps), a.nw + k0);
+      if (use_h)
+        row_stage(xs + m * KS + (kh0 - k0), a.hid, a.hid_dt, bh[m] + (kh0 - H), k0 + KS - kh0,
+                  rsqrtf(ss[MT + m] / (float)H + a.eps), a.nw2 + (kh0 - H));
+    }
   } else if (a.pro == PRO_NORM) {
     float ss[MT];
 #pragma unroll
@@ -331,12 +347,12 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   constexpr int ROWS = 8 * RPW;
   extern __shared__ __align__(16) float xs[];
   __shared__ float s_out[MT][ROWS];
-  __shared__ float s_red[32 * MT];
+  __shared__ float s_red[64 * MT];
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int group = blockIdx.x / a.S, split = blockIdx.x - group * a.S;
-  const int KS = a.K / a.S, k0 = split * KS;
+  const int k0 = gemv_slice_start(a.K, a.S, split), KS = gemv_slice_start(a.K, a.S, split + 1) - k0;
 
   // This warp's RPW consecutive physical rows.
   const int l0 = warp * RPW;

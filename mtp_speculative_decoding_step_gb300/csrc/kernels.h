@@ -58,6 +58,12 @@ void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float*
 
 // rows per block group for a batch width MT
 inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
+// K-slices of a GEMV: split `sp` of S covers [start(sp), start(sp + 1)), cut
+// on 16-element boundaries (K a multiple of 16); lengths differ by at most 16.
+__host__ __device__ inline int gemv_slice_start(int K, int S, int sp) {
+  return (int)((long long)sp * (K / 16) / S) * 16;
+}
+inline int gemv_slice_max(int K, int S) { return ((K / 16 + S - 1) / S) * 16; }
 void launch_gemv(int mt, const GemvArgs& a, int smem_bytes, cudaStream_t s);
 
 // Per-item per-head q_norm / k_norm + RoPE + KV append.

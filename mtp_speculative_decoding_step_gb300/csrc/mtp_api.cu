@@ -130,19 +130,20 @@ void free_all(mtp_handle* h) {
 
 int esize(int dt) { return dt == MTP_DTYPE_BF16 ? 2 : 4; }
 
-GemvPlan plan_gemv(int N, int K, int M, bool dual, int sms) {
+GemvPlan plan_gemv(int N, int K, int M, int sms) {
   GemvPlan p;
   p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   const int rows = gemv_rows_per_group(p.mt);
   p.ngroups = N / rows;
-  // at least one block per SM: every block keeps enough loads in flight to
-  // draw its share of HBM, so long blocks in one wave beat many short ones
-  // with split-K tails (block counts balanced over the SMs measured slower:
-  // a lone block per SM cannot keep enough loads in flight)
-  p.S = dual ? 2 : 1;
-  while (p.S < 8 && (long long)p.ngroups * p.S < (long long)sms) p.S *= 2;
-  while (p.S < 8 && (long long)p.mt * (K / p.S) * 4 > 96 * 1024) p.S *= 2;
-  p.smem = p.mt * (K / p.S) * 4;
+  // A block streams one K-slice of its group's rows with a fixed number of
+  // loads in flight per lane, so its time follows the slice length. K is cut
+  // so that the grid comes as close as it can to the two blocks per SM that
+  // stay resident together (slices of at least 64 columns); grids wider than
+  // that run in waves and keep whole rows.
+  const int units = K / 16;
+  p.S = std::max(1, std::min({16, 2 * sms / std::max(p.ngroups, 1), std::max(1, units / 4)}));
+  while (p.S < units && (long long)p.mt * gemv_slice_max(K, p.S) * 4 > 96 * 1024) ++p.S;
+  p.smem = p.mt * gemv_slice_max(K, p.S) * 4;
   return p;
 }
 
@@ -177,7 +178,6 @@ struct GemvJob {
   const void* w[3];
   int seg_end[3];
   int N, K, pro, epi;
-  bool dual;
   // item-indexed operands (row stride in elements)
   const float* x;
   long long ldx;
@@ -288,7 +288,7 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
   if (!j.fp8 && h->tc_gemv && M >= kTcGemvMinItems && run_gemv_tc(h, j, M, s)) return;
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mp = std::min(8, M - m0);
-    const GemvPlan pl = plan_gemv(j.N, j.K, mp, j.dual, h->sms);
+    const GemvPlan pl = plan_gemv(j.N, j.K, mp, h->sms);
     GemvArgs a;
     std::memset(&a, 0, sizeof(a));
     for (int i = 0; i < 3; ++i) { a.w[i] = j.w[i]; a.seg_end[i] = j.seg_end[i]; }
@@ -378,7 +378,7 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
     std::memset(&j, 0, sizeof(j));
     j.w[0] = h->w[T_FC];
     j.seg_end[0] = H; j.seg_end[1] = H; j.seg_end[2] = H;
-    j.N = H; j.K = 2 * H; j.pro = PRO_DUAL; j.epi = EPI_STORE; j.dual = true;
+    j.N = H; j.K = 2 * H; j.pro = PRO_DUAL; j.epi = EPI_STORE;
     j.nw = h->nrm[T_PRE_E]; j.nw2 = h->nrm[T_PRE_H];
     j.y = h->h0; j.ldy = H;
     j.tok = tok; j.tok_idx = it.tok_idx.data();
@@ -701,11 +701,10 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   // split-K partials and counters: worst case over every GEMV shape and width
   size_t part = 0;
   int groups = 0;
-  const int shapes[7][3] = {{H, 2 * H, 1}, {qw + 2 * kw, H, 0}, {2 * kw, H, 0}, {H, qw, 0},
-                            {2 * I, H, 0}, {H, I, 0},          {c.vocab, H, 0}};
+  const int shapes[7][2] = {{H, 2 * H}, {qw + 2 * kw, H}, {2 * kw, H}, {H, qw}, {2 * I, H}, {H, I}, {c.vocab, H}};
   for (int mt : {1, 2, 4, 8})
     for (auto& sh : shapes) {
-      GemvPlan pl = plan_gemv(sh[0], sh[1], mt, sh[2] != 0, h->sms);
+      GemvPlan pl = plan_gemv(sh[0], sh[1], mt, h->sms);
       if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * sh[0]);
       groups = std::max(groups, pl.ngroups);
     }
