@@ -45,7 +45,10 @@ POOL = 16
 # of the same kernel at V=32768 (profiles/lm_head_gemv_H5120_V32768.md),
 # scaled by the rows processed (152064 / 32768). Set to None when the kernel
 # changes until it is captured again.
-LM_TRAFFIC_BYTES = round((335.637760e6 + 3.358464e6) * 152064 / 32768)
+LM_TRAFFIC_BYTES = round((335.669248e6 + 3.021312e6) * 152064 / 32768)
+# In the timed region, every BRACKET_EVERY-th round has its lm_head launches
+# and its verify bracketed with CUDA events (the live per-kernel durations).
+BRACKET_EVERY = 4
 WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064), bf16 weights, "
             "batch 1, greedy, depth 2 (block 3), draft KV 4096")
 
@@ -141,17 +144,14 @@ def pool_top2(base):
     return v[..., 0].astype(np.float32), v[..., 1].astype(np.float32), o[..., 0].astype(np.int64)
 
 
-def plant_device(lg, draft, coins, top1, top2, arg1):
-    """Device-side planting (torch ops, no host sync), same rule as
+def plant_device(lg, draft, coins, top1, top2, arg1, stream_ptr):
+    """Device-side planting (one kernel, no host sync), same rule as
     synth.plant_logits: row i gets logit[x_{i+1}] = max + 1 when coins[i],
     else logit[x_{i+1}] = second - 1 if x_{i+1} was the argmax.
     coins/top1/top2/arg1: [DEPTH] device tensors for this round / pool row."""
-    import torch
-    x = draft[0].long()
-    rows = torch.arange(x.numel(), device=x.device)
-    cur = lg[0, rows, x]
-    new = torch.where(coins, top1 + 1.0, torch.where(arg1 == x, top2 - 1.0, cur))
-    lg[0].index_put_((rows, x), new)
+    import synth
+    synth.plant_device(stream_ptr, lg.data_ptr(), lg.shape[-1], draft.data_ptr(), draft.shape[1],
+                       coins.data_ptr(), top1.data_ptr(), top2.data_ptr(), arg1.data_ptr())
 
 
 def run_ours(args, rank, world, local_rank):
@@ -191,8 +191,16 @@ def run_ours(args, rank, world, local_rank):
     first_tok[0, 0] = tok0
     ws = torch.zeros(m.spec_verify_workspace_bytes(1, DEPTH, s.vocab), dtype=torch.uint8, device=dev)
     h_out = torch.zeros(DEPTH + 2, dtype=torch.int32).pin_memory()
+    h_out_np = h_out.numpy()  # the verify writes the round's record here
     hid_in = torch.zeros((1, DEPTH + 1, s.hidden), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    # per-pool views, made once so that the host path between rounds stays short
+    hid_pool = [thid_d[i].view(1, DEPTH + 1, s.hidden) for i in range(POOL)]
+    lg_pool = [base_d[i].view(1, DEPTH + 1, s.vocab) for i in range(POOL)]
+    thid_h_pool = [thid_h[i].view(1, DEPTH + 1, s.hidden) for i in range(POOL)]
+    base_h_pool = [base_h[i].view(1, DEPTH + 1, s.vocab) for i in range(POOL)]
+    synth.build_device()
     ev_v0 = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
     ev_v1 = [torch.cuda.Event(enable_timing=True) for _ in range(rounds)]
 
@@ -200,27 +208,25 @@ def run_ours(args, rank, world, local_rank):
 
     def one_round(i, e2e=False, timed_verify=False):
         P = state["P"]
+        j = i % POOL
         if e2e:
-            hid_in.view(torch.int16).copy_(thid_h[i % POOL].view(1, DEPTH + 1, s.hidden), non_blocking=True)
+            hid_in.view(torch.int16).copy_(thid_h_pool[j], non_blocking=True)
             hid = hid_in
         else:
-            hid = thid_d[i % POOL].view(1, DEPTH + 1, s.hidden)
-        m.mtp_draft(h, DEPTH, [P], state["tok"], hid, params, draft)
-        if e2e:
-            lg.copy_(base_h[i % POOL].view(1, DEPTH + 1, s.vocab), non_blocking=True)
-        else:
-            lg.copy_(base_d[i % POOL].view(1, DEPTH + 1, s.vocab))
-        plant_device(lg, draft, coins_d[i], top1_d[i % POOL], top2_d[i % POOL], arg1_d[i % POOL])
+            hid = hid_pool[j]
+        m.mtp_draft(h, DEPTH, [P], state["tok"], hid, params, draft, stream=sp)
+        lg.copy_(base_h_pool[j] if e2e else lg_pool[j], non_blocking=e2e)
+        plant_device(lg, draft, coins_d[i], top1_d[j], top2_d[j], arg1_d[j], sp)
         if timed_verify:
             ev_v0[i].record(stream)
-        m.spec_verify(lg, draft, params, u, n_acc, out_tok, ws, h_out=h_out)
+        m.spec_verify(lg, draft, params, u, n_acc, out_tok, ws, h_out=h_out, stream=sp)
         if timed_verify:
             ev_v1[i].record(stream)
-        m.kv_rollback(h, 1, DEPTH)
+        m.kv_rollback(h, 1, DEPTH, stream=sp)
         if i % 64 == 63:  # keep the draft KV near 4096 positions over long runs
-            m.mtp_set_lengths(h, [KV_LEN])
+            m.mtp_set_lengths(h, [KV_LEN], stream=sp)
         stream.synchronize()
-        n = int(h_out[0])
+        n = int(h_out_np[0])
         state["P"] = n + 1
         state["tok"] = out_tok
         state["ncommit"] += n + 1
@@ -239,9 +245,25 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.warmup, min(rounds, args.warmup + 20)):
         one_round(i)
     prof_all = m.mtp_profile_read(h)
-    # timed region: only the lm_head launches are bracketed (roofline of the dominant kernel)
+    # the draft step alone: back-to-back draft calls with no brackets, no
+    # verify and no host sync between them (the KV length is put back after
+    # each call)
+    m.mtp_profile_enable(h, False)
+    n_alone = 50
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for i in range(n_alone):
+        m.mtp_draft(h, DEPTH, [1], first_tok, hid_pool[i % POOL], params, draft, stream=sp)
+        m.mtp_set_lengths(h, [KV_LEN], stream=sp)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    step_alone_ms = a0.elapsed_time(a1) / (n_alone * DEPTH)
+    # timed region: the lm_head launches (roofline of the dominant kernel) and
+    # the verify are bracketed with events on every BRACKET_EVERY-th round.
+    # An event between two launches ends their programmatic overlap, so the
+    # other rounds run unbracketed.
     clocks = Clocks(local_rank)
-    m.mtp_profile_enable(h, ["lm_head"])
     launches0 = m.mtp_kernel_launches()
     state["ncommit"] = state["nacc"] = 0
     t0 = torch.cuda.Event(enable_timing=True)
@@ -249,7 +271,10 @@ def run_ours(args, rank, world, local_rank):
     t0.record(stream)
     wall0 = time.perf_counter()
     for i in range(args.warmup, rounds):
-        one_round(i, timed_verify=True)
+        bracket = (i - args.warmup) % BRACKET_EVERY == 0
+        if bracket or BRACKET_EVERY == 1 or (i - args.warmup) % BRACKET_EVERY == 1:
+            m.mtp_profile_enable(h, ["lm_head"] if bracket else False)
+        one_round(i, timed_verify=bracket)
     t1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -259,7 +284,8 @@ def run_ours(args, rank, world, local_rank):
     m.mtp_profile_enable(h, False)
     ms = t0.elapsed_time(t1)
     ncommit, nacc = state["ncommit"], state["nacc"]
-    verify_ms = [ev_v0[i].elapsed_time(ev_v1[i]) for i in range(args.warmup, rounds)]
+    verify_ms = [ev_v0[i].elapsed_time(ev_v1[i]) for i in range(args.warmup, rounds)
+                 if (i - args.warmup) % BRACKET_EVERY == 0]
     ms, drafted = combine_ranks(ms, args.steps * DEPTH, dev)
 
     # end to end: target outputs copied from pinned host memory, result read back
@@ -346,8 +372,9 @@ def run_ours(args, rank, world, local_rank):
         "committed_tok_per_s": round(world * ncommit / (ms / 1e3), 2),
         "acceptance_per_draft": round(nacc / (args.steps * DEPTH), 4),
         "verify_us_per_round": round(1e3 * float(np.mean(verify_ms)), 2),
-        "draft_step_us": round(1e3 * draft_ms / DEPTH, 1),
-        "draft_step_hbm_frac": round(step_bytes / (draft_ms / DEPTH / 1e3) / 1e9 / peak, 4),
+        "draft_step_us": round(1e3 * step_alone_ms, 1),
+        "draft_step_hbm_frac": round(step_bytes / (step_alone_ms / 1e3) / 1e9 / peak, 4),
+        "bracketed_step_us": round(1e3 * draft_ms / DEPTH, 1),
         "kernel_avg_us": breakdown,
         "roofline": {"bound": "hbm", "kernel": "lm_head GEMV (tied head, fused final norm + argmax)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": src, "unit": "GB/s",

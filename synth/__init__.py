@@ -37,6 +37,38 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+_PLANT_SO = os.path.join(_HERE, "libsynth_plant.so")
+_plant = None
+
+
+def build_device(force: bool = False) -> str:
+    """Compile plant.cu (the benchmark's device-side target planting) for sm_103a."""
+    src = os.path.join(_HERE, "plant.cu")
+    if force or not os.path.exists(_PLANT_SO) or os.path.getmtime(_PLANT_SO) < os.path.getmtime(src):
+        nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+        tmp = _PLANT_SO + f".{os.getpid()}.tmp"
+        subprocess.check_call([nvcc if os.path.exists(nvcc) else "nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
+                               "-O2", "-Xcompiler", "-fPIC", "-shared", src, "-o", tmp])
+        os.replace(tmp, _PLANT_SO)
+    return _PLANT_SO
+
+
+def plant_device(stream: int, lg, vocab: int, draft, depth: int, coins, top1, top2, arg1) -> None:
+    """plant_logits() on the device, in place, for one verify block (device
+    pointers: lg f32 [depth+1][vocab], draft i32, coins u8, top1/top2 f32,
+    arg1 i64, each [depth])."""
+    global _plant
+    if _plant is None:
+        lib = ctypes.CDLL(build_device())
+        vp = ctypes.c_void_p
+        lib.synth_plant.argtypes = [vp, vp, ctypes.c_longlong, vp, ctypes.c_int, vp, vp, vp, vp]
+        lib.synth_plant.restype = ctypes.c_int
+        _plant = lib
+    rc = _plant.synth_plant(stream, lg, vocab, draft, depth, coins, top1, top2, arg1)
+    if rc != 0:
+        raise RuntimeError(f"synth_plant: CUDA error {rc}")
+
+
 def _load():
     global _lib
     if _lib is None:
