@@ -338,6 +338,7 @@ def run_ours(args, rank, world, local_rank):
     sampled = None if args.quick else measure_sampled(tensors, embed, s, dev)
     sampled_am = None if args.quick else measure_sampled(tensors, embed, s, dev, depths=(2,), argmax_draft=True)
     batched = None if args.quick else measure_batched(tensors, embed, s, dev)
+    stress = None if args.quick else measure_verify_stress(s, dev)
 
     H, Vocab = s.hidden, s.vocab
     lm_bytes = Vocab * H * 2 + Vocab * 4 + H * 4
@@ -387,6 +388,7 @@ def run_ours(args, rank, world, local_rank):
         "sampled_argmax_draft_depth2": sampled_am,
         "fp8_draft_head": fp8,
         "batched_8_rows": batched,
+        "verify_stress": stress,
         "flush_256_pairs": {"by_offset": flush, "flops": flush_flops, "weight_bytes": flush_bytes,
                             "bf16_peak_tflops": peak_bf16(), "bound": "tensor/hbm ridge"} if flush else None,
         "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
@@ -420,7 +422,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
         torch.bfloat16).to(dev)
     stream = torch.cuda.current_stream()
     # the flush reads 126 MB of weights, less than L2: overwrite L2 before each timed flush
-    l2 = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    l2 = L2Flush(dev)
     out = {}
     for off in (0, 8192, 32768):
         for i in range(3):
@@ -429,7 +431,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
         ms = 0.0
         for i in range(reps):
             m.mtp_set_lengths(h, [off])
-            l2.add_(1)
+            l2()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -442,7 +444,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
         m.mtp_profile_read(h)
         for i in range(min(reps, 10)):
             m.mtp_set_lengths(h, [off])
-            l2.add_(1)
+            l2()
             m.mtp_flush(h, [npairs], tok, hid)
         torch.cuda.synchronize()
         prof = m.mtp_profile_read(h)
@@ -452,7 +454,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
                          "tflops": round(flops / t / 1e12, 2), "weight_gbs": round(wbytes / t / 1e9, 1),
                          "fc_us": round(1e3 * prof["flush_fc"][0] / max(prof["flush_fc"][1], 1), 2),
                          "kv_us": round(1e3 * prof["flush_kv"][0] / max(prof["flush_kv"][1], 1), 2),
-                         "l2": "flushed (256 MiB write) before each timed flush"}
+                         "l2": L2Flush.WHAT}
     h.close()
     return out, flops, wbytes
 
@@ -578,7 +580,7 @@ def measure_batched(tensors, embed, s, dev, reps: int = 20):
     n_acc = torch.zeros(R, dtype=torch.int32, device=dev)
     out_tok = torch.zeros((R, depth + 1), dtype=torch.int32, device=dev)
     ws = torch.zeros(m.spec_verify_workspace_bytes(R, depth, V), dtype=torch.uint8, device=dev)
-    flush = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)  # > L2: flush between timed verifies
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     dt = vt = 0.0
     for i in range(reps + 2):
@@ -588,8 +590,7 @@ def measure_batched(tensors, embed, s, dev, reps: int = 20):
         m.mtp_draft(h, depth, [1] * R, tok, hid, params, draft, hist=hist, u=ud, q=q, logits=dl)
         e[1].record(stream)
         tl[:, :depth] = dl + 0.5
-        flush.add_(1)
-        flush.add_(1)
+        flush()
         e[2].record(stream)
         m.spec_verify(tl, draft, params, uv, n_acc, out_tok, ws, q=q, hist=hist)
         e[3].record(stream)
@@ -608,7 +609,75 @@ def measure_batched(tensors, embed, s, dev, reps: int = 20):
             "draft_tok_per_s": round(R * depth / dt, 1), "draft_step_us": round(1e6 * dt / depth, 1),
             "draft_step_hbm_gbs": round((wbytes + kvbytes) / (dt / depth) / 1e9, 1),
             "verify_us": round(1e6 * vt, 2), "verify_bytes": vbytes,
-            "verify_gbs": round(vbytes / vt / 1e9, 1), "verify_l2": "flushed (128 MiB write) before each verify"}
+            "verify_gbs": round(vbytes / vt / 1e9, 1), "verify_l2": L2Flush.WHAT}
+
+
+class L2Flush:
+    """Before a timed launch: write a 256 MiB scratch buffer (twice the L2),
+    then read another one, so that the L2 holds only clean lines of the
+    second and the write-back of the first is over before timing starts."""
+    WHAT = "flushed before each timed launch (256 MiB write, then a 256 MiB read)"
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        self.sink = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.add_(1.0)
+        self.sink.copy_(self.r.sum())
+
+
+def measure_verify_stress(s, dev, R: int = 64, depth: int = 3, reps: int = 10):
+    """The verify alone over many independent rows in one launch: R rows of
+    depth `depth`, once all greedy and once with the sampled parameters
+    (T 0.8, penalty 1.1 over a 64-token ring, top-k 40, top-p 0.95, min-p
+    0.05) with argmax drafts (point-mass q). Target logits N(0,4); each draft
+    is the argmax of its target row with probability 0.7. Bytes: every target
+    row read once, R (depth+1) V 4; L2 overwritten before each timed verify."""
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+    V = s.vocab
+    base = synth.normal(41, "stress:tl", (R, depth + 1, V), std=4.0)
+    am = base[:, :depth].argmax(-1).astype(np.int32)
+    other = synth.randint(41, "stress:x", (R, depth), V).astype(np.int32)
+    hit = synth.uniform(41, "stress:coins", (R, depth)) < 0.7
+    drafts = np.where(hit, am, other).astype(np.int32)
+    tl = torch.from_numpy(base).to(dev)
+    draft = torch.from_numpy(drafts).to(dev)
+    hist = torch.from_numpy(synth.randint(41, "stress:hist", (R, 64), V)).to(dev)
+    uv = torch.from_numpy(synth.uniform(41, "stress:u", (R, depth + 1))).to(dev)
+    n_acc = torch.zeros(R, dtype=torch.int32, device=dev)
+    out_tok = torch.zeros((R, depth + 1), dtype=torch.int32, device=dev)
+    ws = torch.zeros(m.spec_verify_workspace_bytes(R, depth, V), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    vbytes = R * (depth + 1) * V * 4
+    out = {"rows": R, "depth": depth, "bytes": vbytes, "l2": L2Flush.WHAT}
+    for name, prm in (("greedy", dict(temperature=0.0)),
+                      ("sampled_argmax_drafts", dict(temperature=0.8, rep_penalty=1.1, top_k=40, top_p=0.95,
+                                                     min_p=0.05, argmax_draft=True))):
+        params = m.sampling_array([prm] * R)
+        hs = hist if name != "greedy" else None
+        t = 0.0
+        for i in range(reps + 2):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            m.spec_verify(tl, draft, params, uv, n_acc, out_tok, ws, hist=hs)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                t += e0.elapsed_time(e1) / 1e3
+        t /= reps
+        peak, _ = peaks()
+        out[name] = {"verify_us": round(1e6 * t, 2), "gbs": round(vbytes / t / 1e9, 1),
+                     "hbm_frac": round(vbytes / t / 1e9 / peak, 4)}
+    return out
 
 
 def cpu_rounds(work, budget_s: float, max_rounds: int):
@@ -656,6 +725,8 @@ def main():
                     help="time only sampled rounds at depth 1 (profiling case)")
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the 8-row batched draft + verify (profiling case)")
+    ap.add_argument("--stress-only", action="store_true",
+                    help="time only the many-row verify stress case (profiling case)")
     ap.add_argument("--fp8-head", action="store_true",
                     help="draft with the fp8 copy of the tied head throughout (profiling case)")
     args = ap.parse_args()
@@ -723,6 +794,13 @@ def main():
         tensors = {n: to(a) for n, a in model.tensors.items()}
         out = measure_batched(tensors, to(model.embed), s, dev, reps=max(args.steps, 1))
         print(json.dumps({"batched_8_rows": out}), flush=True)
+        return
+    if args.stress_only:
+        import dataclasses
+        import torch as _t
+        s = synth.QWEN27B if not args.vocab else dataclasses.replace(synth.QWEN27B, vocab=args.vocab)
+        out = measure_verify_stress(s, _t.device("cuda", local_rank), reps=max(args.steps, 1))
+        print(json.dumps({"verify_stress": out}), flush=True)
         return
     if args.flush_only:
         import torch as _t

@@ -1531,7 +1531,8 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
 // point-mass p and q the Leviathan/Chen rule accepts x_i exactly when x_i is
 // the argmax of target row i-1, and the correction or bonus token is the
 // argmax of the first unmatched row. One cluster per row (16 CTAs where the
-// device schedules them, else 8): each CTA takes the argmax (value desc, id
+// device schedules them, else 8, halved while rows x CTAs exceeds the SM
+// count): each CTA takes the argmax (value desc, id
 // asc) of its vocabulary slice for every position, with the loads of several
 // positions in flight together, the cluster combines the slices through DSMEM,
 // and rank 0 walks the accept chain and writes the outputs.
@@ -1539,6 +1540,7 @@ constexpr int kGreedyMaxPos = 17;
 constexpr int kGreedyBuf = 16;  // float4 loads in flight per thread
 constexpr int kGreedyGroup = 4;  // positions reduced together
 
+template <bool WIDE>
 __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
   __shared__ float s_v[kGreedyMaxPos];
   __shared__ int s_i[kGreedyMaxPos];
@@ -1561,14 +1563,62 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
   const bool vec = a.vec_ok != 0;
   const int n4 = vec ? n / 4 : 0;
   const int U = max(1, (n4 + kST - 1) / kST);
-  const int G = vec ? max(1, min(kGreedyGroup, kGreedyBuf / U)) : 1;
+  const int G = (vec && !WIDE) ? max(1, min(kGreedyGroup, kGreedyBuf / U)) : 1;
   for (int i0 = 0; i0 <= d; i0 += G) {
     const int gi = min(G, d + 1 - i0);
     float bv[kGreedyGroup];
     int bi[kGreedyGroup];
 #pragma unroll
     for (int e = 0; e < kGreedyGroup; ++e) { bv[e] = -INFINITY; bi[e] = 0x7FFFFFFF; }
-    if (vec) {
+    if constexpr (WIDE) {
+      // wide slices (many rows per launch, or a large vocabulary): one
+      // position at a time (G = 1), two sets of B loads per thread, the next
+      // set in flight while the current one is reduced
+      constexpr int B = 8;
+      const float4* src = reinterpret_cast<const float4*>(lg + (size_t)i0 * a.V + v0);
+      // four independent (value, id) chains, one per vector lane, merged at
+      // the end: the compares of one set do not wait on each other
+      float v[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      int id[4] = {0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF};
+      float4 b0[B], b1[B];
+      auto load = [&](float4 (&b)[B], int base) {
+#pragma unroll
+        for (int e = 0; e < B; ++e) {
+          const int j4 = base + e * kST + threadIdx.x;
+          if (j4 < n4) b[e] = __ldg(src + j4);
+        }
+      };
+      auto reduce = [&](const float4 (&b)[B], int base) {
+#pragma unroll
+        for (int e = 0; e < B; ++e) {
+          const int j4 = base + e * kST + threadIdx.x;
+          if (j4 < n4) {
+            const float x[4] = {b[e].x, b[e].y, b[e].z, b[e].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (!isfinite(x[q])) bad = true;
+              if (better(x[q], v0 + 4 * j4 + q, v[q], id[q])) { v[q] = x[q]; id[q] = v0 + 4 * j4 + q; }
+            }
+          }
+        }
+      };
+      constexpr int step = B * kST;
+      load(b0, 0);
+      for (int base = 0; base < n4; base += 2 * step) {
+        load(b1, base + step);
+        reduce(b0, base);
+        load(b0, base + 2 * step);
+        reduce(b1, base + step);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (better(v[q], id[q], bv[0], bi[0])) { bv[0] = v[q]; bi[0] = id[q]; }
+      for (int j = 4 * n4 + threadIdx.x; j < n; j += kST) {
+        const float x = __ldg(lg + (size_t)i0 * a.V + v0 + j);
+        if (!isfinite(x)) bad = true;
+        if (better(x, v0 + j, bv[0], bi[0])) { bv[0] = x; bi[0] = v0 + j; }
+      }
+    } else if (vec) {
       float4 buf[kGreedyBuf];
 #pragma unroll
       for (int e = 0; e < kGreedyBuf; ++e) {
@@ -1718,7 +1768,9 @@ void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verif
 void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   VerifyArgs a = a0;
   a.vec_ok = (a.V % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0) ? 1 : 0;
-  static int wide = -1;  // 16-CTA clusters schedulable on this device (checked once)
+  // 16-CTA clusters schedulable on this device, per kernel instance (checked once)
+  static int wide16[2] = {-1, -1};
+  static int sms = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kST);
   cfg.stream = s;
@@ -1730,20 +1782,34 @@ void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (wide < 0) {
-    wide = 0;
-    if (cudaFuncSetAttribute(k_verify_greedy, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-      int nclusters = 0;
-      cfg.gridDim = dim3(16);
-      attr[0].val.clusterDim.x = 16;
-      if (cudaOccupancyMaxActiveClusters(&nclusters, k_verify_greedy, &cfg) == cudaSuccess && nclusters > 0) wide = 1;
+  void (*kern[2])(VerifyArgs) = {k_verify_greedy<false>, k_verify_greedy<true>};
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+    for (int w = 0; w < 2; ++w) {
+      wide16[w] = 0;
+      if (cudaFuncSetAttribute(kern[w], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        int nclusters = 0;
+        cfg.gridDim = dim3(16);
+        attr[0].val.clusterDim.x = 16;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, kern[w], &cfg) == cudaSuccess && nclusters > 0) wide16[w] = 1;
+      }
     }
     cudaGetLastError();
   }
-  const int nc = wide ? 16 : kClusterCTAs;
+  // one row per cluster; many rows take narrower clusters so that rows x CTAs
+  // fits one wave (each CTA then streams a wider slice). Slices wider than one
+  // round of the grouped loads take the double-buffered instance.
+  int nc = (wide16[0] && wide16[1]) ? 16 : kClusterCTAs;
+  while (nc > 1 && a.rows * nc > sms) nc /= 2;
+  const int per = ((a.V + nc - 1) / nc + 3) & ~3;
+  const int U = (per / 4 + kST - 1) / kST;
+  const int w = (a.vec_ok && U > kGreedyBuf) ? 1 : 0;
   cfg.gridDim = dim3(a.rows * nc);
   attr[0].val.clusterDim.x = nc;
-  cudaLaunchKernelEx(&cfg, k_verify_greedy, a);
+  cudaLaunchKernelEx(&cfg, kern[w], a);
   count_launch();
 }
 
