@@ -264,11 +264,33 @@ struct VerifyArgs {
   int32_t* status;
   int vec_ok;  // logits rows 16-byte aligned (set by the greedy launcher)
   int32_t* h_rec;  // device-visible [rows][depth+2] host record (n_acc, out_tok), or null
+  // streaming path only: per (row, position) descriptors (written here, the
+  // same array as desc), accept flags and kept lists
+  TDesc* wdesc;      // [rows][depth+1]
+  int32_t* acc;      // [rows][depth+1]
+  int32_t* kid;      // [rows][depth+1][kStreamTopK] kept ids, in (key, id) order
+  uint32_t* kkey;    // [rows][depth+1][kStreamTopK] their keys
+  int ring_ns;       // stages of the shared-memory ring the target rows stream through
   RowParams p[kMaxRows];
 };
 void launch_verify(const VerifyArgs& a, cudaStream_t s);
+// Streaming verify for many (row, position) tasks whose sampled rows all have
+// 1 <= top_k <= kStreamTopK < V: one CTA per task reads its target row once
+// and keeps the exact top-k in shared memory; a second launch walks each
+// row's accept chain and draws over the stopping position's kept list.
+constexpr int kStreamTopK = 256;
+void launch_verify_stream(const VerifyArgs& a, cudaStream_t s);
+size_t verify_stream_smem(int V, int* ring_ns = nullptr);
 // All rows greedy without a repetition penalty: argmax matches in one launch
 // (depth <= 16; desc, q, hist and u unused).
 void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
+
+// spec_verify with the streaming path allowed or not (the workspace of
+// spec_verify_workspace_bytes holds its lists; a descriptors-only scratch does not).
+mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
+                            const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
+                            const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
+                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace,
+                            bool allow_stream);
 
 }  // namespace mtp

@@ -492,6 +492,30 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
   return cuda_ok(cudaGetLastError());
 }
 
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// The streaming verify takes calls with more (row, position) tasks than one
+// wave of 8-CTA clusters holds (two CTAs per SM), where every sampled row cuts
+// to a top-k of at most kStreamTopK below the vocabulary.
+bool stream_verify_fits(int rows, int depth, int vocab, const mtp_sampling* hp) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  // the streaming kernel's shared memory (with the penalty bitmap) must fit
+  if (vocab > (1 << 20) || verify_stream_smem(vocab) > 226 * 1024 ||
+      (long long)rows * (depth + 1) * kClusterCTAs <= 2LL * sms)
+    return false;
+  for (int r = 0; r < rows; ++r) {
+    const RowParams rp = row_params(hp[r]);
+    if (!rp.greedy && !(rp.top_k >= 1 && rp.top_k <= kStreamTopK && rp.top_k < vocab)) return false;
+  }
+  return true;
+}
+
 // K splits so that (M tiles) x (N tiles) x splits fills at most one wave.
 int tc_splits(int mtiles, int ntiles, int ktiles, int sms, int max_splits) {
   int best = 1;
@@ -940,13 +964,21 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
 size_t spec_verify_workspace_bytes(int32_t rows, int32_t depth, int32_t vocab) {
   (void)vocab;
   if (rows < 1 || depth < 1) return 0;
-  return sizeof(TDesc) * (size_t)rows * (depth + 1);
+  const size_t tasks = (size_t)rows * (depth + 1);
+  // descriptors, then (streaming path) accept flags and kept lists
+  return align256(sizeof(TDesc) * tasks) + align256(sizeof(int32_t) * tasks) +
+         2 * align256(sizeof(int32_t) * tasks * kStreamTopK);
 }
 
-mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
-                       const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
-                       const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
-                       int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace) {
+}  // extern "C"
+
+namespace mtp {
+
+mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
+                            const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
+                            const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
+                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace,
+                            bool allow_stream) {
   if (rows < 1 || rows > kMaxRows || depth < 1 || depth > 16 || vocab < 1 || !d_logits || !d_draft ||
       hist_w < 0 || hist_w > 128 || (hist_w > 0 && !d_hist) || !d_u || !d_n_acc || !d_out_tok || !d_workspace)
     return MTP_ERR_BAD_ARG;
@@ -977,6 +1009,24 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
     va.logits = d_logits; va.drafts = d_draft; va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
     va.h_rec = h_rec;
     launch_verify_greedy(va, s);
+  } else if (allow_stream && stream_verify_fits(rows, depth, vocab, h_params)) {
+    const size_t tasks = (size_t)rows * (depth + 1);
+    uint8_t* w = static_cast<uint8_t*>(d_workspace);
+    VerifyArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.rows = rows; va.V = vocab; va.W = hist_w; va.depth = depth;
+    va.logits = d_logits; va.drafts = d_draft; va.q = d_q; va.hist = d_hist; va.u = d_u;
+    va.wdesc = reinterpret_cast<TDesc*>(w);
+    va.desc = va.wdesc;
+    w += align256(sizeof(TDesc) * tasks);
+    va.acc = reinterpret_cast<int32_t*>(w);
+    w += align256(sizeof(int32_t) * tasks);
+    va.kid = reinterpret_cast<int32_t*>(w);
+    w += align256(sizeof(int32_t) * tasks * kStreamTopK);
+    va.kkey = reinterpret_cast<uint32_t*>(w);
+    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec; va.status = nullptr;
+    for (int r = 0; r < rows; ++r) va.p[r] = row_params(h_params[r]);
+    launch_verify_stream(va, s);
   } else {
     TDesc* desc = static_cast<TDesc*>(d_workspace);
     SampleArgs sa;
@@ -1004,6 +1054,18 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
                                      sizeof(int32_t) * (depth + 1), rows, cudaMemcpyDeviceToHost, s));
   }
   return st;
+}
+
+}  // namespace mtp
+
+extern "C" {
+
+mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
+                       const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
+                       const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
+                       int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace) {
+  return mtp::spec_verify_impl(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u,
+                               d_n_acc, d_out_tok, d_stats, h_out, d_workspace, true);
 }
 
 mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* d_n_acc, int32_t* d_target_len,

@@ -1563,62 +1563,87 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
   const bool vec = a.vec_ok != 0;
   const int n4 = vec ? n / 4 : 0;
   const int U = max(1, (n4 + kST - 1) / kST);
-  const int G = (vec && !WIDE) ? max(1, min(kGreedyGroup, kGreedyBuf / U)) : 1;
+  const int G = vec ? max(1, min(kGreedyGroup, kGreedyBuf / U)) : 1;
+  if constexpr (WIDE) {
+    // Wide slices (many rows per launch, or a large vocabulary; 16-byte
+    // loads): every position's slice streamed back to back in chunks of B
+    // loads per thread, the next chunk in flight while the current one is
+    // reduced, across position boundaries too. Four independent (value, id)
+    // chains per thread, one per vector lane; the block argmax of a position
+    // is taken when its last chunk has been reduced.
+    // (The launcher takes this instance only where the 16-byte loads apply.)
+    constexpr int B = 8;
+    constexpr int step = B * kST;
+    if (threadIdx.x <= d) { s_v[threadIdx.x] = -INFINITY; s_i[threadIdx.x] = 0x7FFFFFFF; }  // an empty slice
+    __syncthreads();
+    const int nch = (n4 + step - 1) / step;
+    const int total = (d + 1) * nch;
+    float v[4];
+    int id[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { v[q] = -INFINITY; id[q] = 0x7FFFFFFF; }
+    float4 b0[B], b1[B];
+    auto load = [&](float4 (&b)[B], int c) {
+      if (c >= total) return;
+      const int pi = c / nch, base = (c - pi * nch) * step;
+      const float4* src = reinterpret_cast<const float4*>(lg + (size_t)pi * a.V + v0);
+#pragma unroll
+      for (int e = 0; e < B; ++e) {
+        const int j4 = base + e * kST + threadIdx.x;
+        if (j4 < n4) { const uint4 t = ldg_stream(src + j4); b[e] = make_float4(__uint_as_float(t.x), __uint_as_float(t.y), __uint_as_float(t.z), __uint_as_float(t.w)); }
+      }
+    };
+    auto reduce = [&](const float4 (&b)[B], int c) {
+      if (c >= total) return;  // uniform over the block, like the test below
+      const int pi = c / nch, base = (c - pi * nch) * step;
+#pragma unroll
+      for (int e = 0; e < B; ++e) {
+        const int j4 = base + e * kST + threadIdx.x;
+        if (j4 < n4) {
+          const float x[4] = {b[e].x, b[e].y, b[e].z, b[e].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (!isfinite(x[q])) bad = true;
+            if (better(x[q], v0 + 4 * j4 + q, v[q], id[q])) { v[q] = x[q]; id[q] = v0 + 4 * j4 + q; }
+          }
+        }
+      }
+      if (c - pi * nch == nch - 1) {  // the position's last chunk: its block argmax
+        float bvv = -INFINITY;
+        int bii = 0x7FFFFFFF;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (better(v[q], id[q], bvv, bii)) { bvv = v[q]; bii = id[q]; }
+          v[q] = -INFINITY;
+          id[q] = 0x7FFFFFFF;
+        }
+        warp_argmax(bvv, bii);
+        if (lane == 0) { wv[0][warp] = bvv; wi[0][warp] = bii; }
+        __syncthreads();
+        if (warp == 0) {
+          float x = lane < kST / 32 ? wv[0][lane] : -INFINITY;
+          int i = lane < kST / 32 ? wi[0][lane] : 0x7FFFFFFF;
+          warp_argmax(x, i);
+          if (lane == 0) { s_v[pi] = x; s_i[pi] = i; }
+        }
+        __syncthreads();
+      }
+    };
+    load(b0, 0);
+    for (int c = 0; c < total; c += 2) {
+      load(b1, c + 1);
+      reduce(b0, c);
+      load(b0, c + 2);
+      reduce(b1, c + 1);
+    }
+  } else  // grouped positions, all loads of a group in flight together
   for (int i0 = 0; i0 <= d; i0 += G) {
     const int gi = min(G, d + 1 - i0);
     float bv[kGreedyGroup];
     int bi[kGreedyGroup];
 #pragma unroll
     for (int e = 0; e < kGreedyGroup; ++e) { bv[e] = -INFINITY; bi[e] = 0x7FFFFFFF; }
-    if constexpr (WIDE) {
-      // wide slices (many rows per launch, or a large vocabulary): one
-      // position at a time (G = 1), two sets of B loads per thread, the next
-      // set in flight while the current one is reduced
-      constexpr int B = 8;
-      const float4* src = reinterpret_cast<const float4*>(lg + (size_t)i0 * a.V + v0);
-      // four independent (value, id) chains, one per vector lane, merged at
-      // the end: the compares of one set do not wait on each other
-      float v[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      int id[4] = {0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF};
-      float4 b0[B], b1[B];
-      auto load = [&](float4 (&b)[B], int base) {
-#pragma unroll
-        for (int e = 0; e < B; ++e) {
-          const int j4 = base + e * kST + threadIdx.x;
-          if (j4 < n4) b[e] = __ldg(src + j4);
-        }
-      };
-      auto reduce = [&](const float4 (&b)[B], int base) {
-#pragma unroll
-        for (int e = 0; e < B; ++e) {
-          const int j4 = base + e * kST + threadIdx.x;
-          if (j4 < n4) {
-            const float x[4] = {b[e].x, b[e].y, b[e].z, b[e].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (!isfinite(x[q])) bad = true;
-              if (better(x[q], v0 + 4 * j4 + q, v[q], id[q])) { v[q] = x[q]; id[q] = v0 + 4 * j4 + q; }
-            }
-          }
-        }
-      };
-      constexpr int step = B * kST;
-      load(b0, 0);
-      for (int base = 0; base < n4; base += 2 * step) {
-        load(b1, base + step);
-        reduce(b0, base);
-        load(b0, base + 2 * step);
-        reduce(b1, base + step);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (better(v[q], id[q], bv[0], bi[0])) { bv[0] = v[q]; bi[0] = id[q]; }
-      for (int j = 4 * n4 + threadIdx.x; j < n; j += kST) {
-        const float x = __ldg(lg + (size_t)i0 * a.V + v0 + j);
-        if (!isfinite(x)) bad = true;
-        if (better(x, v0 + j, bv[0], bi[0])) { bv[0] = x; bi[0] = v0 + j; }
-      }
-    } else if (vec) {
+    if (vec) {
       float4 buf[kGreedyBuf];
 #pragma unroll
       for (int e = 0; e < kGreedyBuf; ++e) {
@@ -1718,6 +1743,581 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
   cl.sync();  // keep shared memory alive until rank 0 has read it
 }
 
+// ------------------------------------------------------------ streaming verify
+// Throughput form of the sampled verify for many tasks (rows x positions) whose
+// sampled rows all cut to a top-k of at most kStreamTopK. With top-k set, the
+// kept set and every probability the verify needs come from the k largest
+// transformed logits, so one CTA per task reads its target row once: it
+// penalises, tracks the argmax, and keeps the (key, id)-smallest candidates in
+// shared memory under a threshold that tightens to the exact k-th each time the
+// buffer fills. The descriptor it writes is the one the cluster path
+// computes (same keys, same fixed-point sums, same cut rules); the task also
+// evaluates the accept test of the draft its row judges and stores its kept
+// list. k_verify_finish then walks each row's accept chain and draws the
+// correction or bonus token over the stopping position's kept list, in id
+// order, with the cluster path's inverse-CDF rule.
+constexpr int kStreamCap = 4096;  // candidate entries (a power of two, >= 4 kStreamTopK)
+constexpr int kStreamChunk = 32 * kST;  // elements per thread round (8 float4 per thread)
+
+constexpr int kRingChunk = 8192;            // floats per ring stage (32 KB)
+constexpr size_t kStreamSmemMax = 226 * 1024;  // dynamic shared memory the streaming kernel may take
+
+// Dynamic shared memory of the streaming kernel: sampler scratch, candidate
+// buffers, the penalty bitmap, then (16-byte rows) a ring of ns stages of
+// kRingChunk floats and their mbarriers. The ring takes up to 4 stages of
+// what is left; *ring_ns = 0 when fewer than 2 fit.
+struct StreamLayout {
+  size_t ckey, bits, ring, bar, total;
+  int ns;
+  __host__ __device__ StreamLayout(int V, int ns_want) {
+    ckey = (sizeof(SampleSmem) + 15) & ~size_t(15);
+    bits = ckey + 3 * sizeof(uint32_t) * kStreamCap;
+    ring = (bits + sizeof(uint32_t) * ((V + 31) / 32 + 1) + 127) & ~size_t(127);
+    ns = ns_want;
+    bar = ring + (size_t)ns * kRingChunk * sizeof(float);
+    total = bar + 8 * (size_t)(ns > 0 ? ns : 1) + 16;
+  }
+};
+
+size_t verify_stream_smem(int V, int* ring_ns) {
+  const StreamLayout base(V, 0);
+  int ns = (int)((kStreamSmemMax - base.ring - 64) / (kRingChunk * sizeof(float)));
+  ns = ns > 4 ? 4 : ns;
+  if (ns < 2) ns = 0;
+  if (ring_ns) *ring_ns = ns;
+  return StreamLayout(V, ns).total;
+}
+
+// Keep exactly the k (key, id)-smallest of the buffered candidates; the
+// threshold becomes the k-th. Out of line: it runs rarely, and the streaming
+// loop keeps its registers.
+// Smallest penalised logit z whose transformed value z / T + 0 reaches the
+// transformed value of key K (division rounds monotonically, so every z below
+// it transforms below): the streaming loop skips the division for them. -inf
+// (no skipping) when K admits everything or the search does not settle.
+__device__ float stream_z_cut(uint32_t K, float T) {
+  if (K == 0xFFFFFFFFu) return -INFINITY;
+  const float tt = key_to_z(K);
+  if (!isfinite(tt)) return -INFINITY;
+  auto reaches = [&](float z) { return z / T + 0.0f >= tt; };
+  float z = tt * T;
+  if (!isfinite(z)) return -INFINITY;
+  for (int it = 0; it < 64; ++it) {
+    if (reaches(z)) {
+      const float lo = nextafterf(z, -INFINITY);
+      if (!reaches(lo)) return z;
+      z = lo;
+    } else {
+      z = nextafterf(z, INFINITY);
+    }
+  }
+  return -INFINITY;
+}
+
+// The k-th entry (1 <= k <= n) of n shared-memory (key, id) pairs with
+// distinct ids, in (key asc, id asc) order: digit passes of up to 8 bits from
+// the highest bit where the keys differ, counting into 32-bit bins with one
+// atomic per group of lanes that share a digit; then the ties at the settled
+// key are gathered (tie holds n ids) and the wanted one is the tie with the
+// right count of smaller ids.
+__device__ void stream_select(SampleSmem* sm, const uint32_t* key, const int* id, int n, int k, int* tie,
+                              uint32_t& Kout, int& idout) {
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int i = threadIdx.x; i < n; i += kST) {
+    kmin = min(kmin, key[i]);
+    kmax = max(kmax, key[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+  __syncthreads();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int w = 0; w < kST / 32; ++w) {
+    kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
+    kmax = max(kmax, (uint32_t)sm->wsum[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
+  uint32_t prefix = kmin & mask;
+  uint32_t target = (uint32_t)k;
+  uint32_t* h = reinterpret_cast<uint32_t*>(sm->hist[0]);
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kST) {
+      const uint32_t kk = key[i];
+      if ((kk & mask) == prefix) {
+        const uint32_t dg = (kk >> lo) & dmask;
+        const unsigned peers = __match_any_sync(__activemask(), dg);
+        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[dg], (uint32_t)__popc(peers));
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint32_t s8 = 0;
+      for (int b = 0; b < 8; ++b) s8 += h[lane * 8 + b];
+      uint32_t incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      uint32_t cum = incl - s8;
+      if (cum < target && target <= incl) {
+        for (int b = 0; b < 8; ++b) {
+          const uint32_t t = h[lane * 8 + b];
+          if (cum < target && target <= cum + t) {
+            sm->sel_bin = lane * 8 + b;
+            sm->sel_rem = target - cum;
+            break;
+          }
+          cum += t;
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm->sel_bin << lo;
+    mask |= dmask << lo;
+    target = (uint32_t)sm->sel_rem;
+    hi = lo - 1;
+  }
+  const uint32_t K = prefix;
+  if (threadIdx.x == 0) { sm->found = -1; sm->ccount = 0; }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kST)
+    if (key[i] == K) tie[atomicAdd(&sm->ccount, 1)] = id[i];
+  __syncthreads();
+  const int ties = sm->ccount;
+  for (int t = threadIdx.x; t < ties; t += kST) {
+    const int me = tie[t];
+    int rank = 0;
+    for (int q = 0; q < ties; ++q) rank += tie[q] < me;
+    if ((uint32_t)rank == target - 1) sm->found = me;
+  }
+  __syncthreads();
+  Kout = K;
+  idout = sm->found;
+  __syncthreads();
+}
+
+__device__ __noinline__ void stream_compact(SampleSmem* sm, uint32_t* ckey, int* cid, int* tie, int k, int* cnt,
+                                            int* kept_n, uint32_t* thrK, int* thrI, float* zcut, float T) {
+  const int n = min(*cnt, kStreamCap);
+  uint32_t K;
+  int cut;
+  stream_select(sm, ckey, cid, n, k, tie, K, cut);
+  if (threadIdx.x == 0) *kept_n = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < n; t += kST)
+    if (in_prefix(ckey[t], cid[t], K, cut)) {
+      const int pos = atomicAdd(kept_n, 1);
+      tie[pos] = (int)ckey[t];
+      tie[kStreamTopK + pos] = cid[t];
+    }
+  __syncthreads();
+  const int kept = *kept_n;
+  for (int t = threadIdx.x; t < kept; t += kST) { ckey[t] = (uint32_t)tie[t]; cid[t] = tie[kStreamTopK + t]; }
+  if (threadIdx.x == 0) { *cnt = kept; *thrK = K; *thrI = cut; *zcut = stream_z_cut(K, T); }
+  __syncthreads();
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kST, 1) k_verify_stream(const __grid_constant__ VerifyArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  const StreamLayout lay(a.V, VEC ? a.ring_ns : 0);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(dyn + lay.ckey);
+  int* cid = reinterpret_cast<int*>(ckey + kStreamCap);
+  int* tie = cid + kStreamCap;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + lay.bits);
+  float* ring = reinterpret_cast<float*>(dyn + lay.ring);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dyn + lay.bar);
+  __shared__ int s_cnt, s_kept;
+  __shared__ uint32_t s_thrK;
+  __shared__ int s_thrI;
+  __shared__ float s_zc;
+  __shared__ float s_bv[kST / 32];
+  __shared__ int s_bi[kST / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int d = a.depth, V = a.V;
+  const int task = blockIdx.x, r = task / (d + 1), i = task - r * (d + 1);
+  const RowParams p = a.p[r];
+  const float* lg = a.logits + ((size_t)r * (d + 1) + i) * V;
+  const int32_t* dr = a.drafts + (size_t)r * d;
+  // 16-byte rows stream through the ring: its first stages are requested
+  // before the rest of the setup
+  const int NS = lay.ns;
+  const int nch = (V + kRingChunk - 1) / kRingChunk;
+  auto issue = [&](int c) {
+    const int slot = c % NS;
+    const uint32_t bytes = (uint32_t)min(kRingChunk, V - c * kRingChunk) * 4u;
+    mbar_expect_tx(smem_u32(&bar[slot]), bytes);
+    bulk_g2s(smem_u32(ring + (size_t)slot * kRingChunk), lg + (size_t)c * kRingChunk, bytes, smem_u32(&bar[slot]));
+  };
+  if constexpr (VEC) {
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&bar[s]), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int c = 0; c < min(nch, NS); ++c) issue(c);
+  }
+  load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, i);
+  const bool pen = p.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, 0, V);
+  const bool smp = !p.greedy;
+  // Every row keeps candidates: a sampled row its top-k of the transformed
+  // logits z / T, a greedy row its top-1 of z (T = 1).
+  const int kk = smp ? p.top_k : 1;  // 1 <= top_k <= kStreamTopK < V (checked by the host)
+  const float TT = smp ? p.temperature : 1.f;
+  if (threadIdx.x == 0) { s_cnt = 0; s_thrK = 0xFFFFFFFFu; s_thrI = 0x7FFFFFFF; s_zc = -INFINITY; }
+  __syncthreads();
+
+  auto pen_z = [&](float raw, int j) { return pen && bit(bits, j) ? penalize(raw, p.rep_penalty) : raw; };
+  auto key_of = [&](float raw, int j) { return desc_key(pen_z(raw, j) / TT + 0.0f); };
+  auto append = [&](uint32_t key, int j) {
+    const int pos = atomicAdd(&s_cnt, 1);
+    if (pos < kStreamCap) { ckey[pos] = key; cid[pos] = j; return true; }
+    return false;
+  };
+  auto compact = [&]() { stream_compact(sm, ckey, cid, tie, kk, &s_cnt, &s_kept, &s_thrK, &s_thrI, &s_zc, TT); };
+  // A first threshold before anything is kept, from the first span of the
+  // row: the kk-th smallest of the threads' smallest keys there. At least kk
+  // elements lie at or below it, so the top kk all do (kept inclusively).
+  auto first_threshold = [&](uint32_t mk) {
+    ckey[threadIdx.x] = mk;
+    cid[threadIdx.x] = threadIdx.x;
+    __syncthreads();
+    uint32_t K0;
+    int i0;
+    stream_select(sm, ckey, cid, kST, kk, tie, K0, i0);
+    if (threadIdx.x == 0) { s_thrK = K0; s_thrI = 0x7FFFFFFF; s_zc = stream_z_cut(K0, TT); }
+    __syncthreads();
+  };
+  // One element of the stream (window tokens arrive as NaN and fail every
+  // test: they are offered after the stream with their penalised logits).
+  // An append that finds the buffer full raises `overflow`; the rescan below
+  // then recovers it.
+  // The argmax of the penalised logits is tracked on the elements that reach
+  // zc: the largest z has the smallest key, so it always does.
+  bool overflow = false;
+  float gv = -INFINITY;
+  int gi = 0x7FFFFFFF;
+  auto offer = [&](float z, int j, uint32_t thrK, int thrI, float zc) {
+    if (z >= zc) {  // below zc an element cannot pass: no division
+      if (better(z, j, gv, gi)) { gv = z; gi = j; }
+      const uint32_t key = desc_key(z / TT + 0.0f);
+      if (in_prefix(key, j, thrK, thrI) && !append(key, j)) overflow = true;
+    }
+  };
+  const float kNaN = __int_as_float(0x7FC00000);
+  auto comp = [](const float4& v, int q) { return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w)); };
+  if constexpr (VEC) {
+    // thread t takes float4 u kST + t (u < 4) of each 8192-float stage;
+    // no barriers between elements, one per stage
+    uint32_t thrK = 0xFFFFFFFFu;
+    int thrI = 0x7FFFFFFF;
+    float zc = -INFINITY;
+    bool ok = true;
+    int issued = min(nch, NS);
+    for (int c = 0; c < nch; ++c) {
+      const int slot = c % NS;
+      // one warp polls the stage's barrier; the others wait at the block
+      // barrier, which takes no issue slots
+      const bool got = threadIdx.x >= 32 || mbar_wait(smem_u32(&bar[slot]), (c / NS) & 1);
+      if (__syncthreads_or(!got)) { ok = false; break; }
+      const float4* src = reinterpret_cast<const float4*>(ring + (size_t)slot * kRingChunk);
+      const int n4 = min(kRingChunk, V - c * kRingChunk) / 4;
+      if (c == 0) {
+        uint32_t mk = 0xFFFFFFFFu;
+        for (int u = 0; u < kRingChunk / 4 / kST; ++u) {
+          const int j4 = u * kST + threadIdx.x;
+          if (j4 < n4) {
+            const float4 v = src[j4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mk = min(mk, key_of(comp(v, q), 4 * j4 + q));
+          }
+        }
+        first_threshold(mk);
+        thrK = s_thrK;
+        thrI = s_thrI;
+        zc = s_zc;
+      }
+      // one compare per element into a mask (bit 4u + q); the few elements
+      // at or above zc are then taken one by one from the stage
+      uint32_t hit = 0;
+#pragma unroll
+      for (int u = 0; u < kRingChunk / 4 / kST; ++u) {
+        const int j4 = u * kST + threadIdx.x;
+        if (j4 < n4) {
+          const float4 v = src[j4];
+          const int j0 = c * kRingChunk + 4 * j4;
+          const uint32_t skip = pen ? bits[j0 >> 5] >> (j0 & 31) : 0u;  // window tokens: offered after
+          const uint32_t h = (v.x >= zc ? 1u : 0u) | (v.y >= zc ? 2u : 0u) | (v.z >= zc ? 4u : 0u) |
+                             (v.w >= zc ? 8u : 0u);
+          hit |= (h & ~skip & 0xFu) << (4 * u);
+        }
+      }
+      while (hit) {
+        const int bq = __ffs(hit) - 1;
+        hit &= hit - 1;
+        const int j4 = (bq >> 2) * kST + threadIdx.x;
+        offer(reinterpret_cast<const float*>(src)[4 * j4 + (bq & 3)], c * kRingChunk + 4 * j4 + (bq & 3), thrK, thrI,
+              zc);
+      }
+      __syncthreads();  // every thread is done with this stage: refill it
+      if (threadIdx.x == 0 && issued < nch) issue(issued);
+      issued = min(nch, issued + 1);
+    }
+    if (!ok) {
+      // a stage never arrived: raise the status word and let the copies in
+      // flight land before the shared memory is released
+      if (threadIdx.x == 0) {
+        flag_status(a.status, MTP_ERR_TIMEOUT);
+        for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(smem_u32(&bar[j % NS]), (j / NS) & 1);
+      }
+      __syncthreads();
+    }
+  } else {
+    // 4-byte loads: thread t takes element e kST + t (e < 32) of each span of
+    // kStreamChunk, the next span's loads in flight while one is processed
+    const int nround = (V + kStreamChunk - 1) / kStreamChunk;
+    auto load = [&](float (&b)[32], int c) {
+      if (c >= nround) return;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = c * kStreamChunk + e * kST + threadIdx.x;
+        b[e] = j < V ? __ldg(lg + j) : kNaN;
+      }
+    };
+    float nb[32];
+    load(nb, 0);
+    {
+      uint32_t mk = 0xFFFFFFFFu;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = e * kST + threadIdx.x;
+        if (j < V) mk = min(mk, key_of(nb[e], j));
+      }
+      first_threshold(mk);
+    }
+    const uint32_t thrK = s_thrK;
+    const int thrI = s_thrI;
+    const float zc = s_zc;
+    for (int c = 0; c < nround; ++c) {
+      float b[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) b[e] = nb[e];
+      load(nb, c + 1);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = c * kStreamChunk + e * kST + threadIdx.x;
+        offer(j < V && !(pen && bit(bits, j)) ? b[e] : kNaN, j, thrK, thrI, zc);
+      }
+    }
+  }
+  if (pen) {
+    // the window tokens the stream skipped, each once, with their penalised
+    // logits, under the final threshold
+    __syncthreads();
+    const uint32_t thrK = s_thrK;
+    const int thrI = s_thrI;
+    for (int t = threadIdx.x; t < sm->nwin; t += kST) {
+      const int v = sm->wtok[t];
+      bool first = v >= 0 && v < V;
+      for (int u = 0; u < t && first; ++u) first = sm->wtok[u] != v;
+      if (!first) continue;
+      const float z = pen_z(__ldg(lg + v), v);
+      if (better(z, v, gv, gi)) { gv = z; gi = v; }
+      const uint32_t key = desc_key(z / TT + 0.0f);
+      if (in_prefix(key, v, thrK, thrI) && !append(key, v)) overflow = true;
+    }
+    __syncthreads();
+  }
+  // Overflow (rare: the first threshold admitted more than the buffer holds):
+  // the held entries' exact top kk bound the row's kk-th, so keep that bound,
+  // empty the buffer and offer the whole row again under it; repeat until
+  // everything that passes fits. Each pass tightens the bound.
+  while (__syncthreads_or(overflow)) {
+    if (threadIdx.x == 0 && s_cnt > kStreamCap) s_cnt = kStreamCap;
+    __syncthreads();
+    compact();
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    const uint32_t thrK = s_thrK;
+    const int thrI = s_thrI;
+    const float zc = s_zc;
+    overflow = false;
+    for (int j = threadIdx.x; j < V; j += kST) offer(pen_z(__ldg(lg + j), j), j, thrK, thrI, zc);
+  }
+  __syncthreads();
+  if (s_cnt > kk) compact();
+  const int L = s_cnt;  // == kk: V > kk elements were all offered
+  rank_sort(ckey, cid, L);
+  block_argmax(gv, gi, s_bv, s_bi);
+  if (gi == 0x7FFFFFFF) gi = 0;  // nothing comparable (non-finite input): id 0
+
+  TDesc dd;
+  dd.argmax = gi;
+  dd.k_key = 0xFFFFFFFFu;
+  dd.k_cut = 0x7FFFFFFF;
+  dd.p_key = 0xFFFFFFFFu;
+  dd.p_cut = 0x7FFFFFFF;
+  dd.m = 0.f;
+  dd.S = 1.f;
+  dd.kept = 1;
+  if (smp) {
+    // the largest transformed logit: z / T rounds monotonically in z
+    const float mx = key_to_z(ckey[0]);
+    // the cut rules of the cluster path's candidate list (top-k list sorted by
+    // (key, id)): top-p on its fixed-point mass, then min-p, at least one kept
+    if (threadIdx.x < 32) {
+      auto fx = [&](int j) { return to_fix(expf(key_to_z(ckey[j]) - mx)); };
+      unsigned long long SE = 0;
+      warp_find_cross(L, ~0ull, fx, &SE);
+      int Kf = L;
+      if (p.top_p > 0.f && p.top_p < 1.f) {
+        const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+        const int j = warp_find_cross(L, target, fx, nullptr);
+        if (j < L) Kf = min(Kf, j + 1);
+      }
+      if (p.min_p > 0.f) {
+        int first = L;
+        for (int j = threadIdx.x; j < L; j += 32)
+          if (!(expf(key_to_z(ckey[j]) - mx) >= p.min_p)) { first = j; break; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
+        if (first < Kf) Kf = first;
+      }
+      if (Kf < 1) Kf = 1;
+      unsigned long long Sf = 0;
+      warp_find_cross(Kf, ~0ull, fx, &Sf);
+      if (threadIdx.x == 0) { sm->fin_kf = Kf; sm->fin_sf = Sf; }
+    }
+    __syncthreads();
+    const int Kf = sm->fin_kf;
+    dd.p_key = ckey[Kf - 1];
+    dd.p_cut = cid[Kf - 1];
+    dd.m = mx;
+    dd.S = (float)((double)sm->fin_sf / kFix);
+    dd.kept = Kf;
+    int32_t* kid = a.kid + (size_t)task * kStreamTopK;
+    uint32_t* kkey = a.kkey + (size_t)task * kStreamTopK;
+    for (int t = threadIdx.x; t < Kf; t += kST) { kid[t] = cid[t]; kkey[t] = ckey[t]; }
+  }
+  if (threadIdx.x == 0) {
+    a.wdesc[task] = dd;
+    // the accept test of draft x_{i+1} against this target row
+    int acc = 0;
+    if (i < d) {
+      const int x = dr[i];
+      if (x >= 0 && x < V) {  // an out-of-range draft is rejected, never dereferenced
+        if (p.greedy) {
+          acc = x == dd.argmax;
+        } else {
+          const float pv = eval_p(dd, p, __ldg(lg + x), pen && bit(bits, x), x);
+          // an argmax draft is a point mass: q(x) = 1
+          const float qv = p.argmax_draft ? 1.f : __ldg(a.q + ((size_t)r * d + i) * V + x);
+          acc = qv > 0.f && a.u[(size_t)r * (d + 1) + i] < pv / qv;
+        }
+      }
+    }
+    a.acc[task] = acc;
+  }
+}
+
+// Per row: the accept chain from the tasks' flags, then the correction (after
+// a rejection: norm(max(p - q, 0)) at the stopping position) or the bonus
+// token (p_d), drawn over that position's kept list in id order.
+__global__ void __launch_bounds__(kStreamTopK) k_verify_finish(const __grid_constant__ VerifyArgs a) {
+  __shared__ int s_id[kStreamTopK];
+  __shared__ unsigned long long s_w[kStreamTopK];
+  __shared__ int s_nacc, s_pick;
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x, d = a.depth;
+  const RowParams p = a.p[r];
+  const int32_t* dr = a.drafts + (size_t)r * d;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const bool ok = lane < d && a.acc[(size_t)r * (d + 1) + lane] != 0;
+    const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, ok) & (d >= 32 ? 0xFFFFFFFFu : ((1u << d) - 1u));
+    if (lane == 0) s_nacc = rej ? __ffs(rej) - 1 : d;
+  }
+  __syncthreads();
+  const int nacc = s_nacc;
+  const int tn = r * (d + 1) + nacc;
+  const TDesc dn = a.wdesc[tn];
+  int y = dn.argmax;
+  if (!p.greedy) {
+    const int Kf = dn.kept;
+    const int32_t* kid = a.kid + (size_t)tn * kStreamTopK;
+    const uint32_t* kkey = a.kkey + (size_t)tn * kStreamTopK;
+    const float* qn = nacc < d && !p.argmax_draft ? a.q + ((size_t)r * d + nacc) * a.V : nullptr;
+    const int xr = nacc < d && p.argmax_draft ? dr[nacc] : -1;
+    const float uu = a.u[(size_t)r * (d + 1) + d];
+    // place entry t at its rank in id order with its weight
+    auto draw = [&](bool residual) {
+      for (int t = threadIdx.x; t < Kf; t += blockDim.x) {
+        const int id = kid[t];
+        int rank = 0;
+        for (int q = 0; q < Kf; ++q) rank += kid[q] < id;
+        const float pv = expf(key_to_z(kkey[t]) - dn.m) / dn.S;
+        float w = pv;
+        if (residual) w = pv - (id == xr ? 1.f : (qn ? __ldg(qn + id) : 0.f));
+        s_id[rank] = id;
+        s_w[rank] = to_fix(w > 0.f ? w : 0.f);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        unsigned long long tot = 0;
+        warp_find_cross(Kf, ~0ull, [&](int j) { return s_w[j]; }, &tot);
+        int pick = -1;
+        if (tot > 0) {
+          const unsigned long long target = (unsigned long long)floor((double)uu * (double)tot) + 1ull;
+          const int j = warp_find_cross(Kf, target, [&](int j) { return s_w[j]; }, nullptr);
+          pick = j < Kf ? s_id[j] : s_id[Kf - 1];
+        }
+        if (threadIdx.x == 0) s_pick = pick;
+      }
+      __syncthreads();
+      return s_pick;
+    };
+    int yy = -1;
+    if (nacc < d) yy = draw(true);
+    if (yy < 0) yy = draw(false);
+    if (yy >= 0) y = yy;
+  }
+  if (threadIdx.x == 0) {
+    a.n_acc[r] = nacc;
+    int32_t* o = a.out_tok + (size_t)r * (d + 1);
+    for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
+    if (a.h_rec) {
+      int32_t* hr = a.h_rec + (size_t)r * (d + 2);
+      hr[0] = nacc;
+      for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+    }
+    if (a.stats) {
+      int32_t* st = a.stats + (size_t)r * (d + 2);
+      st[0] += 1;
+      if (nacc < d) st[1] += 1;
+      for (int i = 1; i <= nacc; ++i) st[1 + i] += 1;
+    }
+  }
+}
+
 static int sample_smem(int V, int C = 0, int P = 0) {
   const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
   const size_t cand = 16 + (size_t)C * 8 + (size_t)P * 8 + (size_t)C * 4 + 4 + (size_t)C * 8;
@@ -1764,6 +2364,23 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
 }
 
 void launch_verify(const VerifyArgs& a, cudaStream_t s) { launch_cluster(k_verify, a, a.rows, a.V, s); }
+
+void launch_verify_stream(const VerifyArgs& a0, cudaStream_t s) {
+  VerifyArgs a = a0;
+  int ns = 0;
+  size_t smem = verify_stream_smem(a.V, &ns);
+  // rows starting on 16-byte boundaries stream through the shared-memory ring
+  // (bulk copies); others take 4-byte loads into registers
+  const bool vec = (a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0 && ns >= 2;
+  a.ring_ns = vec ? ns : 0;
+  if (!vec) smem = StreamLayout(a.V, 0).total;
+  auto k = vec ? k_verify_stream<true> : k_verify_stream<false>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_pdl(k, dim3(a.rows * (a.depth + 1)), dim3(kST), smem, s, a);
+  count_launch();
+  launch_pdl(k_verify_finish, dim3(a.rows), dim3(kStreamTopK), 0, s, a);
+  count_launch();
+}
 
 void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   VerifyArgs a = a0;

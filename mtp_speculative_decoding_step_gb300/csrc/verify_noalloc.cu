@@ -55,6 +55,8 @@ extern "C" mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32
   void* scratch = nullptr;
   const mtp_status st = scratch_address(&scratch);
   if (st != MTP_OK) return st;
-  return spec_verify(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u, d_n_acc,
-                     d_out_tok, d_stats, h_out, scratch);
+  // the scratch holds descriptors only: the streaming path (which also needs
+  // per-task kept lists) stays off
+  return mtp::spec_verify_impl(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u,
+                               d_n_acc, d_out_tok, d_stats, h_out, scratch, false);
 }

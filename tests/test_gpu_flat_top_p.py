@@ -86,7 +86,8 @@ def test_wide_top_p_descriptors():
     m.spec_verify(g.to_dev(lg), g.to_dev(drafts), rows, g.to_dev(u), n_acc, out, ws, q=g.to_dev(q),
                   hist=g.to_dev(hist))
     torch.cuda.synchronize()
-    desc = ws.cpu().numpy().view(DESC).reshape(R, depth + 1)
+    # the descriptors lead the workspace
+    desc = ws.cpu().numpy()[: R * (depth + 1) * DESC.itemsize].view(DESC).reshape(R, depth + 1)
     near = 0
     for r in range(R):
         p = oracle.make_params(**rows[r])
