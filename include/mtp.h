@@ -219,7 +219,12 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth,
  *   address (cudaHostAlloc / cudaMallocHost) is written by the verify kernel
  *   itself; other host memory gets a copy enqueued after the kernel. Either
  *   way it is complete once the stream has reached the end of this call.
- *   d_workspace: spec_verify_workspace_bytes(rows, depth, vocab) bytes.
+ *   d_workspace: spec_verify_workspace_bytes(rows, depth, vocab) bytes (the
+ *   transform descriptors, then the streaming path's accept flags and kept lists).
+ * Calls with more (row, position) tasks than one wave of 8-CTA clusters holds,
+ * whose sampled rows all cut to a top-k of at most 256 below the vocabulary,
+ * take a streaming path: one CTA per task reads its target row once. Its
+ * results are identical.
  * Errors: BAD_ARG.
  */
 size_t spec_verify_workspace_bytes(int32_t rows, int32_t depth, int32_t vocab);
