@@ -219,13 +219,20 @@ def run_ours(args, rank, world, local_rank):
         plant_device(lg, draft, coins_d[i], top1_d[j], top2_d[j], arg1_d[j], sp)
         if timed_verify:
             ev_v0[i].record(stream)
+        h_out_np[0] = -1  # the verify overwrites it with the accepted count, its tokens first
         m.spec_verify(lg, draft, params, u, n_acc, out_tok, ws, h_out=h_out, stream=sp)
         if timed_verify:
             ev_v1[i].record(stream)
         m.kv_rollback(h, 1, DEPTH, stream=sp)
         if i % 64 == 63:  # keep the draft KV near 4096 positions over long runs
             m.mtp_set_lengths(h, [KV_LEN], stream=sp)
-        stream.synchronize()
+        # the round's one host read: poll the record the verify writes (the
+        # rollback may still run; the next round's launches queue behind it)
+        t_poll = time.perf_counter()
+        while h_out_np[0] < 0:
+            if time.perf_counter() - t_poll > 2.0:
+                stream.synchronize()
+                break
         n = int(h_out_np[0])
         state["P"] = n + 1
         state["tok"] = out_tok

@@ -218,7 +218,10 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth,
  *   the round's one device->host read. Page-locked memory the device can
  *   address (cudaHostAlloc / cudaMallocHost) is written by the verify kernel
  *   itself; other host memory gets a copy enqueued after the kernel. Either
- *   way it is complete once the stream has reached the end of this call.
+ *   way it is complete once the stream has reached the end of this call. In
+ *   device-addressable memory each row's n_acc is stored after its out_tok
+ *   with release semantics at system scope: a host that set n_acc negative
+ *   beforehand may poll it instead of waiting for the stream.
  *   d_workspace: spec_verify_workspace_bytes(rows, depth, vocab) bytes (the
  *   transform descriptors, then the streaming path's accept flags and kept lists).
  * Calls with more (row, position) tasks than one wave of 8-CTA clusters holds,

@@ -1513,9 +1513,10 @@ __global__ void __launch_bounds__(kST, 1) k_verify(const __grid_constant__ Verif
     int32_t* o = a.out_tok + (size_t)r * (d + 1);
     for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
     if (a.h_rec) {
+      // the record's tokens are visible to the host before its count
       int32_t* hr = a.h_rec + (size_t)r * (d + 2);
-      hr[0] = nacc;
       for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+      st_release_sys(hr, nacc);
     }
     if (a.stats) {
       int32_t* s = a.stats + (size_t)r * (d + 2);
@@ -1729,9 +1730,11 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
       a.out_tok[(size_t)r * (d + 1) + lane] = ov;
       if (a.h_rec) a.h_rec[(size_t)r * (d + 2) + 1 + lane] = ov;
     }
+    __syncwarp();
     if (lane == 0) {
       a.n_acc[r] = nacc;
-      if (a.h_rec) a.h_rec[(size_t)r * (d + 2)] = nacc;
+      // the record's tokens are visible to the host before its count
+      if (a.h_rec) st_release_sys(a.h_rec + (size_t)r * (d + 2), nacc);
       if (a.stats) {
         int32_t* st = a.stats + (size_t)r * (d + 2);
         st[0] += 1;
@@ -2305,9 +2308,10 @@ __global__ void __launch_bounds__(kStreamTopK) k_verify_finish(const __grid_cons
     int32_t* o = a.out_tok + (size_t)r * (d + 1);
     for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
     if (a.h_rec) {
+      // the record's tokens are visible to the host before its count
       int32_t* hr = a.h_rec + (size_t)r * (d + 2);
-      hr[0] = nacc;
       for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+      st_release_sys(hr, nacc);
     }
     if (a.stats) {
       int32_t* st = a.stats + (size_t)r * (d + 2);
