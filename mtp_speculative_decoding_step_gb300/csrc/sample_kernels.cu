@@ -1759,7 +1759,7 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
 // list. k_verify_finish then walks each row's accept chain and draws the
 // correction or bonus token over the stopping position's kept list, in id
 // order, with the cluster path's inverse-CDF rule.
-constexpr int kStreamCap = 4096;  // candidate entries (a power of two, >= 4 kStreamTopK)
+constexpr int kStreamCap = 1536;  // candidate entries (>= 2 kStreamTopK), small enough for two CTAs per SM
 constexpr int kStreamChunk = 32 * kST;  // elements per thread round (8 float4 per thread)
 
 constexpr int kRingChunk = 8192;            // floats per ring stage (32 KB)
@@ -1767,8 +1767,9 @@ constexpr size_t kStreamSmemMax = 226 * 1024;  // dynamic shared memory the stre
 
 // Dynamic shared memory of the streaming kernel: sampler scratch, candidate
 // buffers, the penalty bitmap, then (16-byte rows) a ring of ns stages of
-// kRingChunk floats and their mbarriers. The ring takes up to 4 stages of
-// what is left; *ring_ns = 0 when fewer than 2 fit.
+// kRingChunk floats and their mbarriers. The ring takes 2 stages where they
+// fit (*ring_ns = 0 otherwise); at V = 152064 the whole is about 108 KB, so
+// two CTAs share an SM.
 struct StreamLayout {
   size_t ckey, bits, ring, bar, total;
   int ns;
@@ -1785,7 +1786,7 @@ struct StreamLayout {
 size_t verify_stream_smem(int V, int* ring_ns) {
   const StreamLayout base(V, 0);
   int ns = (int)((kStreamSmemMax - base.ring - 64) / (kRingChunk * sizeof(float)));
-  ns = ns > 4 ? 4 : ns;
+  ns = ns > 2 ? 2 : ns;  // two stages: at the full vocabulary two CTAs fit on an SM
   if (ns < 2) ns = 0;
   if (ring_ns) *ring_ns = ns;
   return StreamLayout(V, ns).total;
@@ -1935,7 +1936,7 @@ __device__ __noinline__ void stream_compact(SampleSmem* sm, uint32_t* ckey, int*
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(kST, 1) k_verify_stream(const __grid_constant__ VerifyArgs a) {
+__global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant__ VerifyArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   const StreamLayout lay(a.V, VEC ? a.ring_ns : 0);
