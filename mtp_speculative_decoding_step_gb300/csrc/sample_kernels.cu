@@ -1542,7 +1542,7 @@ constexpr int kGreedyBuf = 16;  // float4 loads in flight per thread
 constexpr int kGreedyGroup = 4;  // positions reduced together
 
 template <bool WIDE>
-__global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
+__global__ void __launch_bounds__(kST, WIDE ? 2 : 1) k_verify_greedy(const __grid_constant__ VerifyArgs a) {
   __shared__ float s_v[kGreedyMaxPos];
   __shared__ int s_i[kGreedyMaxPos];
   __shared__ int s_am[kGreedyMaxPos];
@@ -1572,8 +1572,9 @@ __global__ void __launch_bounds__(kST, 1) k_verify_greedy(const __grid_constant_
     // reduced, across position boundaries too. Four independent (value, id)
     // chains per thread, one per vector lane; the block argmax of a position
     // is taken when its last chunk has been reduced.
-    // (The launcher takes this instance only where the 16-byte loads apply.)
-    constexpr int B = 8;
+    // (The launcher takes this instance only where the 16-byte loads apply.
+    // Two CTAs share an SM: B = 4 keeps a thread within 64 registers.)
+    constexpr int B = 4;
     constexpr int step = B * kST;
     if (threadIdx.x <= d) { s_v[threadIdx.x] = -INFINITY; s_i[threadIdx.x] = 0x7FFFFFFF; }  // an empty slice
     __syncthreads();
@@ -2424,11 +2425,15 @@ void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   // one row per cluster; many rows take narrower clusters so that rows x CTAs
   // fits one wave (each CTA then streams a wider slice). Slices wider than one
   // round of the grouped loads take the double-buffered instance.
-  int nc = (wide16[0] && wide16[1]) ? 16 : kClusterCTAs;
+  const int nc0 = (wide16[0] && wide16[1]) ? 16 : kClusterCTAs;
+  int nc = nc0;
   while (nc > 1 && a.rows * nc > sms) nc /= 2;
-  const int per = ((a.V + nc - 1) / nc + 3) & ~3;
-  const int U = (per / 4 + kST - 1) / kST;
-  const int w = (a.vec_ok && U > kGreedyBuf) ? 1 : 0;
+  int per = ((a.V + nc - 1) / nc + 3) & ~3;
+  const int w = (a.vec_ok && (per / 4 + kST - 1) / kST > kGreedyBuf) ? 1 : 0;
+  if (w) {  // the wide instance fits two CTAs per SM: twice the CTAs per row
+    nc = nc0;
+    while (nc > 1 && a.rows * nc > 2 * sms) nc /= 2;
+  }
   cfg.gridDim = dim3(a.rows * nc);
   attr[0].val.clusterDim.x = nc;
   cudaLaunchKernelEx(&cfg, kern[w], a);
