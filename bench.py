@@ -48,7 +48,7 @@ POOL = 16
 LM_TRAFFIC_BYTES = round((335.669248e6 + 3.021312e6) * 152064 / 32768)
 # In the timed region, every BRACKET_EVERY-th round has its lm_head launches
 # and its verify bracketed with CUDA events (the live per-kernel durations).
-BRACKET_EVERY = 4
+BRACKET_EVERY = 8
 WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064), bf16 weights, "
             "batch 1, greedy, depth 2 (block 3), draft KV 4096")
 
