@@ -131,9 +131,22 @@ def _stream(stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+_BF16 = None
+
+
 def _dtype_code(t) -> int:
-    import torch
-    return MTP_DTYPE_BF16 if t.dtype == torch.bfloat16 else MTP_DTYPE_F32
+    global _BF16
+    if _BF16 is None:
+        import torch
+        _BF16 = torch.bfloat16
+    return MTP_DTYPE_BF16 if t.dtype is _BF16 else MTP_DTYPE_F32
+
+
+def _i32_array(values):
+    """Host int32 array for a C pointer argument (a list/tuple or a numpy array)."""
+    if isinstance(values, np.ndarray):
+        values = values.astype(np.int32, copy=False).ravel().tolist()
+    return (ctypes.c_int32 * len(values))(*values)
 
 
 MTP_SAMPLE_ARGMAX_DRAFT = 1
@@ -221,8 +234,7 @@ def mtp_get_lengths(h: Handle) -> np.ndarray:
 
 
 def mtp_set_lengths(h: Handle, lengths, stream=None):
-    hl = np.ascontiguousarray(lengths, dtype=np.int32)
-    _check(lib().mtp_set_lengths(h.ptr, _stream(stream), hl.ctypes.data), "mtp_set_lengths")
+    _check(lib().mtp_set_lengths(h.ptr, _stream(stream), _i32_array(lengths)), "mtp_set_lengths")
 
 
 def mtp_device_status(h: Handle) -> int:
@@ -239,12 +251,13 @@ def mtp_flush(h: Handle, pairs, tok, hid, stream=None):
 
 def mtp_draft(h: Handle, depth: int, pairs, tok, hid, params, draft, hist=None, u=None, q=None, logits=None,
               hidden=None, stream=None):
-    hp = np.ascontiguousarray(pairs, dtype=np.int32)
+    # (on the host path between two rounds: argument marshalling kept lean)
+    hp = _i32_array(pairs)
     sp = params if isinstance(params, ctypes.Array) else sampling_array(params)
     hist_w = 0 if hist is None else hist.shape[1]
-    rc = lib().mtp_draft(h.ptr, _stream(stream), len(hp), depth, hp.ctypes.data, tok.shape[1], _ptr(tok),
-                         _ptr(hid), _dtype_code(hid), sp, _ptr(hist), hist_w, _ptr(u), _ptr(draft), _ptr(q),
-                         _ptr(logits), _ptr(hidden))
+    rc = lib().mtp_draft(h.ptr, stream if type(stream) is int else _stream(stream), len(hp), depth, hp,
+                         tok.shape[1], _ptr(tok), _ptr(hid), _dtype_code(hid), sp, _ptr(hist), hist_w, _ptr(u),
+                         _ptr(draft), _ptr(q), _ptr(logits), _ptr(hidden))
     _check(rc, "mtp_draft")
 
 
