@@ -1761,7 +1761,7 @@ __global__ void __launch_bounds__(kST, WIDE ? 2 : 1) k_verify_greedy(const __gri
 // correction or bonus token over the stopping position's kept list, in id
 // order, with the cluster path's inverse-CDF rule.
 constexpr int kStreamCap = 1536;  // candidate entries (>= 2 kStreamTopK), small enough for two CTAs per SM
-constexpr int kStreamChunk = 32 * kST;  // elements per thread round (8 float4 per thread)
+constexpr int kStreamChunk = 32 * kST;  // elements per round of the 4-byte-load path (32 per thread)
 
 constexpr int kRingChunk = 8192;            // floats per ring stage (32 KB)
 constexpr size_t kStreamSmemMax = 226 * 1024;  // dynamic shared memory the streaming kernel may take
