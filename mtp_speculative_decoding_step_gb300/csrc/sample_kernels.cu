@@ -1780,7 +1780,7 @@ struct StreamLayout {
     ring = (bits + sizeof(uint32_t) * ((V + 31) / 32 + 1) + 127) & ~size_t(127);
     ns = ns_want;
     bar = ring + (size_t)ns * kRingChunk * sizeof(float);
-    total = bar + 8 * (size_t)(ns > 0 ? ns : 1) + 16;
+    total = bar + 16 * (size_t)(ns > 0 ? ns : 1) + 16;  // full and empty mbarriers
   }
 };
 
@@ -1970,9 +1970,13 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
     mbar_expect_tx(smem_u32(&bar[slot]), bytes);
     bulk_g2s(smem_u32(ring + (size_t)slot * kRingChunk), lg + (size_t)c * kRingChunk, bytes, smem_u32(&bar[slot]));
   };
+  uint64_t* empty = bar + NS;  // a stage is free again once every warp has arrived on it
   if constexpr (VEC) {
     if (threadIdx.x == 0) {
-      for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&bar[s]), 1);
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(smem_u32(&bar[s]), 1);
+        mbar_init(smem_u32(&empty[s]), kST / 32);
+      }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -2037,12 +2041,12 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
     float zc = -INFINITY;
     bool ok = true;
     int issued = min(nch, NS);
+    // No block barrier per stage: each warp waits for a stage to land, and
+    // releases it on the stage's empty barrier when done; thread 0 refills a
+    // stage once all warps have released it.
     for (int c = 0; c < nch; ++c) {
       const int slot = c % NS;
-      // one warp polls the stage's barrier; the others wait at the block
-      // barrier, which takes no issue slots
-      const bool got = threadIdx.x >= 32 || mbar_wait(smem_u32(&bar[slot]), (c / NS) & 1);
-      if (__syncthreads_or(!got)) { ok = false; break; }
+      if (!mbar_wait(smem_u32(&bar[slot]), (c / NS) & 1)) { ok = false; break; }
       const float4* src = reinterpret_cast<const float4*>(ring + (size_t)slot * kRingChunk);
       const int n4 = min(kRingChunk, V - c * kRingChunk) / 4;
       if (c == 0) {
@@ -2082,11 +2086,16 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
         offer(reinterpret_cast<const float*>(src)[4 * j4 + (bq & 3)], c * kRingChunk + 4 * j4 + (bq & 3), thrK, thrI,
               zc);
       }
-      __syncthreads();  // every thread is done with this stage: refill it
-      if (threadIdx.x == 0 && issued < nch) issue(issued);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&empty[slot]));
+      if (threadIdx.x == 0 && issued < nch) {
+        // every warp has released this stage: refill it
+        if (!mbar_wait(smem_u32(&empty[slot]), (c / NS) & 1)) { ok = false; break; }
+        issue(issued);
+      }
       issued = min(nch, issued + 1);
     }
-    if (!ok) {
+    if (__syncthreads_or(!ok)) {
       // a stage never arrived: raise the status word and let the copies in
       // flight land before the shared memory is released
       if (threadIdx.x == 0) {
