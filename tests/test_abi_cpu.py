@@ -128,3 +128,36 @@ def test_spec_verify_rejects_bad_arguments_without_launching(L):
     bad[6] = FAKE
     assert L.spec_verify(*bad) == 9
     assert m.spec_verify_workspace_bytes(8, 3, 152064) >= 8 * 4 * 32
+
+
+def test_workspace_holds_descriptors_and_streaming_lists():
+    # descriptors (32 bytes each), accept flags, and two kept-list arrays of 256
+    # entries per (row, position), each region 256-byte aligned
+    rows, depth = 64, 3
+    tasks = rows * (depth + 1)
+    al = lambda b: (b + 255) // 256 * 256
+    want = al(32 * tasks) + al(4 * tasks) + 2 * al(4 * tasks * 256)
+    assert m.spec_verify_workspace_bytes(rows, depth, 152064) == want
+    assert m.spec_verify_workspace_bytes(0, 3, 64) == 0
+
+
+def test_binding_marshals_host_int_arrays_and_dtypes():
+    import numpy as np
+    import torch
+    assert list(m._i32_array([3, 5])) == [3, 5]
+    assert list(m._i32_array(np.array([[7], [9]], dtype=np.int64))) == [7, 9]
+    assert m._dtype_code(torch.zeros(1, dtype=torch.bfloat16)) == m.MTP_DTYPE_BF16
+    assert m._dtype_code(torch.zeros(1, dtype=torch.float32)) == m.MTP_DTYPE_F32
+
+
+def test_draft_rejects_a_null_handle_before_any_launch(L):
+    import torch
+
+    class NullHandle:
+        ptr = None
+
+    tok = torch.zeros((1, 3), dtype=torch.int32)
+    hid = torch.zeros((1, 3, 256), dtype=torch.bfloat16)
+    draft = torch.zeros((1, 2), dtype=torch.int32)
+    with pytest.raises(m.MTPError):
+        m.mtp_draft(NullHandle(), 2, [1], tok, hid, [dict(temperature=0.0)], draft, stream=0)
