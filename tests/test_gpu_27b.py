@@ -34,21 +34,23 @@ def test_greedy_round_parity(model):
     for slot in range(4096, 4099):
         assert g.max_rel(K[0, :, slot], g.to_f32(rig.oK[0, :, slot])) < TOL
         assert g.max_rel(V[0, :, slot], g.to_f32(rig.oV[0, :, slot])) < TOL
-    if ref["margins"][0] > 1e-2:
-        assert out["draft"][0, 0] == ref["drafts"][0]
-        assert g.max_rel(out["logits"][0, 1], ref["logits"][1]) < TOL
-        if ref["margins"][1] > 1e-2:
-            assert out["draft"][0, 1] == ref["drafts"][1]
+    # the seeded case has clear argmaxes (top-2 gaps about 0.33 on both steps),
+    # so both drafts must match exactly and the step-2 logits are comparable
+    assert ref["margins"][0] > 1e-2 and ref["margins"][1] > 1e-2, ref["margins"]
+    assert out["draft"][0, 0] == ref["drafts"][0]
+    assert g.max_rel(out["logits"][0, 1], ref["logits"][1]) < TOL
+    assert g.max_rel(out["hidden"][0, 1], ref["h2"][1]) < TOL
+    assert out["draft"][0, 1] == ref["drafts"][1]
     # verify of planted target logits (argmax moved onto each draft w.p. 0.7)
     base = synth.normal(2, "t27:logits", (1, 3, S.vocab), std=4.0)
     coins = synth.uniform(2, "t27:coins", (2,)) < 0.7
     lg_g = synth.plant_logits(base[0], out["draft"][0], coins)[None]
     lg_o = synth.plant_logits(base[0], ref["drafts"], coins)
     got = rig.verify(lg_g, out["draft"], None, [dict(temperature=0.0)], np.zeros((1, 3), np.float32))
-    n, toks_ref, _ = oracle.verify_row(lg_o, ref["drafts"], None, oracle.make_params(0.0),
-                                       np.zeros(0, np.int32), np.zeros(3, np.float32))
-    if np.array_equal(out["draft"][0], ref["drafts"]):
-        assert got["n_acc"][0] == n and np.array_equal(got["out_tok"][0], toks_ref)
+    n, toks_ref, mg = oracle.verify_row(lg_o, ref["drafts"], None, oracle.make_params(0.0),
+                                        np.zeros(0, np.int32), np.zeros(3, np.float32))
+    assert np.min(mg[np.isfinite(mg)]) > 1e-2, mg
+    assert got["n_acc"][0] == n and np.array_equal(got["out_tok"][0], toks_ref)
     m.kv_rollback(rig.h, 1, 2)
     assert list(m.mtp_get_lengths(rig.h)) == [4099]
     rig.close()
