@@ -13,8 +13,13 @@
  *    allocate and free (the handle's scratch and norm copies) and may block.
  *  - Arguments are validated on the host before any launch; a bad argument
  *    returns a status and launches nothing. Faults seen on the device (a
- *    non-finite logit) are OR-ed into the handle's device status word, which
- *    the caller reads at its one per-round synchronisation.
+ *    non-finite logit, a bounded wait that ran out) are OR-ed, as
+ *    1 << MTP_ERR_*, into a device status word that the caller reads at its
+ *    one per-round synchronisation: the handle's word (mtp_device_status) for
+ *    the head calls, the caller's d_status for spec_verify, which takes no
+ *    handle. The outputs of a call whose status word gained a bit carry no
+ *    meaning; spec_verify's still stay in range (token ids in [0, V), counts
+ *    in [0, depth]).
  *  - The caller owns every buffer it passes. Large weights, the borrowed
  *    embedding / lm_head and the KV buffers are borrowed by mtp_load and must
  *    outlive the handle.
@@ -47,7 +52,7 @@ typedef enum {
   MTP_ERR_KV_CAPACITY = 8,      /* a write would pass the KV capacity */
   MTP_ERR_BAD_ARG = 9,          /* null pointer, bad count, bad sampling parameter */
   MTP_ERR_NONFINITE = 10,       /* device status bit: a non-finite logit was seen */
-  MTP_ERR_TIMEOUT = 11,         /* reserved: no entry point waits on another block */
+  MTP_ERR_TIMEOUT = 11,         /* device status bit: a bounded wait on an asynchronous copy ran out */
   MTP_ERR_CUDA = 12,            /* a CUDA runtime call failed */
   MTP_ERR_LAYOUT = 13           /* tensor names mix the raw-HF "mtp." and split layouts */
 } mtp_status;
@@ -222,6 +227,11 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth,
  *   device-addressable memory each row's n_acc is stored after its out_tok
  *   with release semantics at system scope: a host that set n_acc negative
  *   beforehand may poll it instead of waiting for the stream.
+ *   d_status (optional, device int32): OR-ed with 1 << MTP_ERR_NONFINITE when
+ *   a target logit the verify reads is NaN or infinite, and with
+ *   1 << MTP_ERR_TIMEOUT when a bounded wait of the streaming path ran out
+ *   (fail-closed errors, "Ollama qwen3_5 MTP loader and SelfDraft path",
+ *   Facts). The caller clears it; NULL drops these reports.
  *   d_workspace: spec_verify_workspace_bytes(rows, depth, vocab) bytes (the
  *   transform descriptors, then the streaming path's accept flags and kept lists).
  * Calls with more (row, position) tasks than one wave of 8-CTA clusters holds,
@@ -236,7 +246,7 @@ mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t v
                        const float* d_logits, const int32_t* d_draft, const float* d_q,
                        const mtp_sampling* h_params, const int32_t* d_hist, int32_t hist_w,
                        const float* d_u, int32_t* d_n_acc, int32_t* d_out_tok,
-                       int32_t* d_stats, int32_t* h_out, void* d_workspace);
+                       int32_t* d_stats, int32_t* h_out, int32_t* d_status, void* d_workspace);
 
 /*
  * mtp_set_draft_head — which copy of the tied output head the drafter reads.
@@ -289,7 +299,8 @@ mtp_status mtp_depth_ctl_state(mtp_depth_ctl_t c, double* h_accept, double* h_co
  * callers that cannot allocate device memory (a host whose own pool owns all
  * device memory, or code running where a cudaMalloc would stall the device or
  * is forbidden). The pages have no counterpart; it exists for such hosts.
- * Same arguments and results as spec_verify minus d_workspace. The scratch
+ * Same arguments and results as spec_verify minus d_workspace (d_status
+ * included). The scratch
  * (one 32-byte descriptor per verified row and position) is a fixed array
  * inside the library, 1088 descriptors (34,816 bytes) per device, held for
  * the life of the process: rows * (depth + 1) above 1088 returns
@@ -302,7 +313,7 @@ mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32_t depth, i
                                const float* d_logits, const int32_t* d_draft, const float* d_q,
                                const mtp_sampling* h_params, const int32_t* d_hist, int32_t hist_w,
                                const float* d_u, int32_t* d_n_acc, int32_t* d_out_tok,
-                               int32_t* d_stats, int32_t* h_out);
+                               int32_t* d_stats, int32_t* h_out, int32_t* d_status);
 
 /*
  * kv_rollback — drop speculative cache slots after a verify.
@@ -310,12 +321,22 @@ mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32_t depth, i
  * (its length becomes the length before that call + h_pairs[r]); with
  * zero_tail the dropped slots are zeroed. Target KV (optional): each
  * d_target_len[r] is trimmed by block - (d_n_acc[r] + 1), block = depth + 1
- * verified positions ("trims by block_size - (max(accepted) + 1)", comment on
- * qualifying the qwen3_5 path). Rows never drafted are left as they are.
+ * verified positions: the positions past the accepted drafts and the one
+ * committed correction or bonus token are dropped ("support the qwen3_5_mtp
+ * drafter" issue, comment on qualifying the qwen3_5 path). Rows never drafted
+ * are left as they are.
  * Errors: BAD_ARG.
  */
 mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* d_n_acc,
                        int32_t* d_target_len, int32_t depth, int32_t zero_tail);
+
+/* Test hook of the streaming verify's bounded waits: the next spec_verify
+ * call that takes the streaming path leaves ring stage `stage` of every task
+ * unfilled (a copy that never lands) and gives each wait `wait_polls` polls,
+ * so its waits run out; it then reports MTP_ERR_TIMEOUT in d_status, writes
+ * in-range outputs and leaves the context usable. One-shot, process-wide, not
+ * for production use. Errors: BAD_ARG (stage < 0 or wait_polls < 1). */
+mtp_status mtp_test_verify_stall(int32_t stage, int32_t wait_polls);
 
 /* Number of kernels this library has launched in the process so far. */
 int64_t mtp_kernel_launches(void);

@@ -33,7 +33,7 @@ EXPORTS = (
     "spec_verify", "kv_rollback", "mtp_profile_enable", "mtp_profile_kinds", "mtp_profile_kind_name",
     "mtp_profile_read", "mtp_kernel_launches", "spec_verify_noalloc",
     "mtp_depth_ctl_create", "mtp_depth_ctl_free", "mtp_depth_ctl_next", "mtp_depth_ctl_observe",
-    "mtp_depth_ctl_state", "mtp_set_draft_head",
+    "mtp_depth_ctl_state", "mtp_set_draft_head", "mtp_test_verify_stall",
 )
 
 
@@ -93,9 +93,10 @@ def lib():
         L.spec_verify_workspace_bytes.argtypes = [i32, i32, i32]
         L.spec_verify_workspace_bytes.restype = sz
         L.spec_verify.argtypes = [vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(Sampling), vp, i32, vp, vp,
-                                  vp, vp, vp, vp]
+                                  vp, vp, vp, vp, vp]
         L.spec_verify_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, ctypes.POINTER(Sampling), vp, i32,
-                                          vp, vp, vp, vp, vp]
+                                          vp, vp, vp, vp, vp, vp]
+        L.mtp_test_verify_stall.argtypes = [i32, i32]
         L.kv_rollback.argtypes = [vp, vp, i32, vp, vp, i32, i32]
         L.mtp_profile_enable.argtypes = [vp, i32]
         L.mtp_profile_kinds.restype = i32
@@ -105,7 +106,7 @@ def lib():
         L.mtp_kernel_launches.restype = ctypes.c_int64
         for name in ("mtp_load", "mtp_free", "mtp_get_lengths", "mtp_set_lengths", "mtp_flush", "mtp_draft",
                      "spec_verify", "spec_verify_noalloc", "kv_rollback", "mtp_profile_enable",
-                     "mtp_profile_read"):
+                     "mtp_profile_read", "mtp_test_verify_stall"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -266,19 +267,20 @@ def spec_verify_workspace_bytes(rows: int, depth: int, vocab: int) -> int:
 
 
 def spec_verify(logits, draft, params, u, n_acc, out_tok, workspace, q=None, hist=None, stats=None,
-                h_out=None, stream=None):
-    """logits [rows, depth+1, V] f32; draft [rows, depth] i32; u [rows, depth+1] f32."""
+                h_out=None, status=None, stream=None):
+    """logits [rows, depth+1, V] f32; draft [rows, depth] i32; u [rows, depth+1] f32;
+    status: optional device int32 word (OR of 1 << MTP_ERR_* seen on the device)."""
     rows, dp1, V = logits.shape
     sp = params if isinstance(params, ctypes.Array) else sampling_array(params)
     hist_w = 0 if hist is None else hist.shape[1]
     rc = lib().spec_verify(_stream(stream), rows, dp1 - 1, V, _ptr(logits), _ptr(draft), _ptr(q), sp,
                            _ptr(hist), hist_w, _ptr(u), _ptr(n_acc), _ptr(out_tok), _ptr(stats), _ptr(h_out),
-                           _ptr(workspace))
+                           _ptr(status), _ptr(workspace))
     _check(rc, "spec_verify")
 
 
 def spec_verify_noalloc(logits, draft, params, u, n_acc, out_tok, q=None, hist=None, stats=None, h_out=None,
-                        stream=None):
+                        status=None, stream=None):
     """spec_verify with the library's fixed scratch instead of a workspace
     (for callers that cannot allocate device memory)."""
     rows, dp1, V = logits.shape
@@ -286,8 +288,15 @@ def spec_verify_noalloc(logits, draft, params, u, n_acc, out_tok, q=None, hist=N
     hist_w = 0 if hist is None else hist.shape[1]
     rc = lib().spec_verify_noalloc(_stream(stream), rows, dp1 - 1, V, _ptr(logits), _ptr(draft), _ptr(q), sp,
                                    _ptr(hist), hist_w, _ptr(u), _ptr(n_acc), _ptr(out_tok), _ptr(stats),
-                                   _ptr(h_out))
+                                   _ptr(h_out), _ptr(status))
     _check(rc, "spec_verify_noalloc")
+
+
+def mtp_test_verify_stall(stage: int, wait_polls: int) -> None:
+    """Test hook: the next streaming-path spec_verify leaves ring stage
+    `stage` unfilled and gives each wait `wait_polls` polls (its waits run out
+    and it reports MTP_ERR_TIMEOUT)."""
+    _check(lib().mtp_test_verify_stall(int(stage), int(wait_polls)), "mtp_test_verify_stall")
 
 
 def kv_rollback(h: Handle, rows: int, depth: int, n_acc=None, target_len=None, zero_tail: bool = False,

@@ -187,8 +187,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait on an mbarrier phase; false when the poll budget runs out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (unsigned i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned limit = kWaitLimit) {
+  for (unsigned i = 0; i < limit; ++i)
     if (mbar_try(bar, parity)) return true;
   return false;
 }

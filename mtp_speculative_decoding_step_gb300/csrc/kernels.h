@@ -271,6 +271,11 @@ struct VerifyArgs {
   int32_t* kid;      // [rows][depth+1][kStreamTopK] kept ids, in (key, id) order
   uint32_t* kkey;    // [rows][depth+1][kStreamTopK] their keys
   int ring_ns;       // stages of the shared-memory ring the target rows stream through
+  // bounded waits of the streaming path: polls before a wait gives up (0 =
+  // the default), and a ring stage left unfilled (-1 = none) so that a test
+  // can make its waits run out (mtp_test_verify_stall)
+  unsigned wait_limit;
+  int stall_stage;
   RowParams p[kMaxRows];
 };
 void launch_verify(const VerifyArgs& a, cudaStream_t s);
@@ -285,12 +290,16 @@ size_t verify_stream_smem(int V, int* ring_ns = nullptr);
 // (depth <= 16; desc, q, hist and u unused).
 void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
 
+// Multiprocessor count of the current device (looked up once per device).
+constexpr int kMaxDevices = 64;
+int device_sm_count();
+
 // spec_verify with the streaming path allowed or not (the workspace of
 // spec_verify_workspace_bytes holds its lists; a descriptors-only scratch does not).
 mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
                             const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
                             const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
-                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace,
-                            bool allow_stream);
+                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, int32_t* d_status,
+                            void* d_workspace, bool allow_stream);
 
 }  // namespace mtp

@@ -4,8 +4,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -18,7 +20,33 @@ constexpr int kTcFlushMinItems = 16;  // below this the flush stays on the GEMV 
 
 namespace mtp {
 unsigned long long launches_so_far();
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 1;
+    }
+    sms[dev] = n;
+  }
+  return sms[dev];
 }
+}  // namespace mtp
+
+namespace {
+// One-shot test hook of the streaming verify's bounded waits
+// (mtp_test_verify_stall): the ring stage to leave unfilled and the polls
+// before a wait gives up.
+std::atomic<int> g_stall_stage{-1};
+std::atomic<unsigned> g_stall_polls{0};
+}  // namespace
 
 namespace {
 
@@ -498,13 +526,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 // wave of 8-CTA clusters holds (two CTAs per SM), where every sampled row cuts
 // to a top-k of at most kStreamTopK below the vocabulary.
 bool stream_verify_fits(int rows, int depth, int vocab, const mtp_sampling* hp) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-  }
+  const int sms = device_sm_count();
   // the streaming kernel's shared memory (with the penalty bitmap) must fit
   if (vocab > (1 << 20) || verify_stream_smem(vocab) > 226 * 1024 ||
       (long long)rows * (depth + 1) * kClusterCTAs <= 2LL * sms)
@@ -977,8 +999,8 @@ namespace mtp {
 mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
                             const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
                             const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
-                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace,
-                            bool allow_stream) {
+                            int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, int32_t* d_status,
+                            void* d_workspace, bool allow_stream) {
   if (rows < 1 || rows > kMaxRows || depth < 1 || depth > 16 || vocab < 1 || !d_logits || !d_draft ||
       hist_w < 0 || hist_w > 128 || (hist_w > 0 && !d_hist) || !d_u || !d_n_acc || !d_out_tok || !d_workspace)
     return MTP_ERR_BAD_ARG;
@@ -1007,7 +1029,7 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
     std::memset(&va, 0, sizeof(va));
     va.rows = rows; va.V = vocab; va.depth = depth;
     va.logits = d_logits; va.drafts = d_draft; va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats;
-    va.h_rec = h_rec;
+    va.h_rec = h_rec; va.status = d_status;
     launch_verify_greedy(va, s);
   } else if (allow_stream && stream_verify_fits(rows, depth, vocab, h_params)) {
     const size_t tasks = (size_t)rows * (depth + 1);
@@ -1024,7 +1046,9 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
     va.kid = reinterpret_cast<int32_t*>(w);
     w += align256(sizeof(int32_t) * tasks * kStreamTopK);
     va.kkey = reinterpret_cast<uint32_t*>(w);
-    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec; va.status = nullptr;
+    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec; va.status = d_status;
+    va.stall_stage = g_stall_stage.exchange(-1);
+    va.wait_limit = va.stall_stage >= 0 ? g_stall_polls.load() : 0u;
     for (int r = 0; r < rows; ++r) va.p[r] = row_params(h_params[r]);
     launch_verify_stream(va, s);
   } else {
@@ -1032,14 +1056,14 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
     SampleArgs sa;
     std::memset(&sa, 0, sizeof(sa));
     sa.mode = 1; sa.rows = rows; sa.V = vocab; sa.W = hist_w; sa.depth = depth;
-    sa.logits = d_logits; sa.hist = d_hist; sa.drafts = d_draft; sa.desc = desc;
+    sa.logits = d_logits; sa.hist = d_hist; sa.drafts = d_draft; sa.desc = desc; sa.status = d_status;
     for (int r = 0; r < rows; ++r) sa.p[r] = row_params(h_params[r]);
     launch_sample(sa, s);
     VerifyArgs va;
     std::memset(&va, 0, sizeof(va));
     va.rows = rows; va.V = vocab; va.W = hist_w; va.depth = depth;
     va.logits = d_logits; va.drafts = d_draft; va.q = d_q; va.hist = d_hist; va.u = d_u; va.desc = desc;
-    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec;
+    va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec; va.status = d_status;
     for (int r = 0; r < rows; ++r) va.p[r] = sa.p[r];
     launch_verify(va, s);
   }
@@ -1063,9 +1087,17 @@ extern "C" {
 mtp_status spec_verify(mtp_stream stream, int32_t rows, int32_t depth, int32_t vocab, const float* d_logits,
                        const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
                        const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
-                       int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, void* d_workspace) {
+                       int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, int32_t* d_status,
+                       void* d_workspace) {
   return mtp::spec_verify_impl(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u,
-                               d_n_acc, d_out_tok, d_stats, h_out, d_workspace, true);
+                               d_n_acc, d_out_tok, d_stats, h_out, d_status, d_workspace, true);
+}
+
+mtp_status mtp_test_verify_stall(int32_t stage, int32_t wait_polls) {
+  if (stage < 0 || wait_polls < 1) return MTP_ERR_BAD_ARG;
+  g_stall_polls.store((unsigned)wait_polls);
+  g_stall_stage.store(stage);
+  return MTP_OK;
 }
 
 mtp_status kv_rollback(mtp_t h, mtp_stream stream, int32_t rows, const int32_t* d_n_acc, int32_t* d_target_len,

@@ -20,6 +20,8 @@
 // every result is independent of thread scheduling.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -1208,7 +1210,7 @@ __device__ bool transform_row(Clu& c, float* zs, uint32_t* bits, int v0, int n, 
     if (better(x->f[0], x->i[0], gv, gi)) { gv = x->f[0]; gi = x->i[0]; }
     zmin = fminf(zmin, x->f[1]);
   }
-  d.argmax = gi;
+  d.argmax = gi < V ? gi : 0;  // nothing comparable (every logit NaN): id 0
   d.k_key = 0xFFFFFFFFu;
   d.k_cut = 0x7FFFFFFF;
   d.p_key = 0xFFFFFFFFu;
@@ -1714,7 +1716,7 @@ __global__ void __launch_bounds__(kST, WIDE ? 2 : 1) k_verify_greedy(const __gri
       id = *cl.map_shared_rank(&s_i[warp], lane);
     }
     warp_argmax(v, id);
-    if (lane == 0) s_am[warp] = id;
+    if (lane == 0) s_am[warp] = id < a.V ? id : 0;  // nothing comparable (every logit NaN): id 0
   }
   __syncthreads();
   if (rank == 0 && warp == 0) {
@@ -1964,7 +1966,9 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
   // before the rest of the setup
   const int NS = lay.ns;
   const int nch = (V + kRingChunk - 1) / kRingChunk;
+  const unsigned lim = a.wait_limit ? a.wait_limit : kWaitLimit;
   auto issue = [&](int c) {
+    if (c == a.stall_stage) return;  // test hook: this stage never lands, its waits run out
     const int slot = c % NS;
     const uint32_t bytes = (uint32_t)min(kRingChunk, V - c * kRingChunk) * 4u;
     mbar_expect_tx(smem_u32(&bar[slot]), bytes);
@@ -2024,6 +2028,9 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
   bool overflow = false;
   float gv = -INFINITY;
   int gi = 0x7FFFFFFF;
+  // x * 0 is 0 for every finite x and NaN for NaN or an infinity: one
+  // dependent FMA per element finds a non-finite logit anywhere in the row
+  float nf = 0.f;
   auto offer = [&](float z, int j, uint32_t thrK, int thrI, float zc) {
     if (z >= zc) {  // below zc an element cannot pass: no division
       if (better(z, j, gv, gi)) { gv = z; gi = j; }
@@ -2043,10 +2050,13 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
     int issued = min(nch, NS);
     // No block barrier per stage: each warp waits for a stage to land, and
     // releases it on the stage's empty barrier when done; thread 0 refills a
-    // stage once all warps have released it.
+    // stage once all warps have released it. A wait that runs out ends the
+    // loop for its whole warp (at the first stage, before the block-wide
+    // threshold, for the whole block), so no barrier is left half-reached.
     for (int c = 0; c < nch; ++c) {
       const int slot = c % NS;
-      if (!mbar_wait(smem_u32(&bar[slot]), (c / NS) & 1)) { ok = false; break; }
+      const bool got = mbar_wait(smem_u32(&bar[slot]), (c / NS) & 1, lim);
+      if (c == 0 ? !__syncthreads_and(got) : !__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
       const float4* src = reinterpret_cast<const float4*>(ring + (size_t)slot * kRingChunk);
       const int n4 = min(kRingChunk, V - c * kRingChunk) / 4;
       if (c == 0) {
@@ -2077,6 +2087,7 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
           const uint32_t h = (v.x >= zc ? 1u : 0u) | (v.y >= zc ? 2u : 0u) | (v.z >= zc ? 4u : 0u) |
                              (v.w >= zc ? 8u : 0u);
           hit |= (h & ~skip & 0xFu) << (4 * u);
+          nf = fmaf(v.w, 0.f, fmaf(v.z, 0.f, fmaf(v.y, 0.f, fmaf(v.x, 0.f, nf))));
         }
       }
       while (hit) {
@@ -2088,21 +2099,38 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
       }
       __syncwarp();
       if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&empty[slot]));
+      bool refilled = true;
       if (threadIdx.x == 0 && issued < nch) {
         // every warp has released this stage: refill it
-        if (!mbar_wait(smem_u32(&empty[slot]), (c / NS) & 1)) { ok = false; break; }
-        issue(issued);
+        refilled = mbar_wait(smem_u32(&empty[slot]), (c / NS) & 1, lim);
+        if (refilled) issue(issued);
       }
+      if (threadIdx.x < 32 && !__all_sync(0xFFFFFFFFu, refilled)) { ok = false; break; }
       issued = min(nch, issued + 1);
     }
     if (__syncthreads_or(!ok)) {
-      // a stage never arrived: raise the status word and let the copies in
-      // flight land before the shared memory is released
+      // a stage never arrived: raise the status word, let the copies in
+      // flight land before the shared memory is released, and leave a task
+      // result that stays in range (no accept, the kept list {0}); the row's
+      // outputs are not meaningful and the status word says so
       if (threadIdx.x == 0) {
         flag_status(a.status, MTP_ERR_TIMEOUT);
-        for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(smem_u32(&bar[j % NS]), (j / NS) & 1);
+        for (int j = max(0, issued - NS); j < issued; ++j) mbar_wait(smem_u32(&bar[j % NS]), (j / NS) & 1, lim);
+        TDesc dd;
+        dd.argmax = 0;
+        dd.k_key = 0xFFFFFFFFu;
+        dd.k_cut = 0x7FFFFFFF;
+        dd.p_key = desc_key(0.f);
+        dd.p_cut = 0;
+        dd.m = 0.f;
+        dd.S = 1.f;
+        dd.kept = 1;
+        a.wdesc[task] = dd;
+        a.acc[task] = 0;
+        a.kid[(size_t)task * kStreamTopK] = 0;
+        a.kkey[(size_t)task * kStreamTopK] = dd.p_key;
       }
-      __syncthreads();
+      return;  // block-uniform: every thread saw the same vote
     }
   } else {
     // 4-byte loads: thread t takes element e kST + t (e < 32) of each span of
@@ -2138,10 +2166,12 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int j = c * kStreamChunk + e * kST + threadIdx.x;
+        if (j < V) nf = fmaf(b[e], 0.f, nf);
         offer(j < V && !(pen && bit(bits, j)) ? b[e] : kNaN, j, thrK, thrI, zc);
       }
     }
   }
+  if (__syncthreads_or(isnan(nf)) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
   if (pen) {
     // the window tokens the stream skipped, each once, with their penalised
     // logits, under the final threshold
@@ -2397,12 +2427,22 @@ void launch_verify_stream(const VerifyArgs& a0, cudaStream_t s) {
   count_launch();
 }
 
+// Per device: whether each greedy-verify instance can be launched in 16-CTA
+// clusters (checked once per device, under a lock).
+struct GreedyDevInfo {
+  bool ready = false;
+  int wide16[2] = {0, 0};
+};
+
 void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   VerifyArgs a = a0;
   a.vec_ok = (a.V % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0) ? 1 : 0;
-  // 16-CTA clusters schedulable on this device, per kernel instance (checked once)
-  static int wide16[2] = {-1, -1};
-  static int sms = 0;
+  static std::mutex mu;
+  static GreedyDevInfo info[kMaxDevices];
+  const int sms = device_sm_count();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kST);
   cfg.stream = s;
@@ -2415,21 +2455,26 @@ void launch_verify_greedy(const VerifyArgs& a0, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   void (*kern[2])(VerifyArgs) = {k_verify_greedy<false>, k_verify_greedy<true>};
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
-    for (int w = 0; w < 2; ++w) {
-      wide16[w] = 0;
-      if (cudaFuncSetAttribute(kern[w], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-        int nclusters = 0;
-        cfg.gridDim = dim3(16);
-        attr[0].val.clusterDim.x = 16;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, kern[w], &cfg) == cudaSuccess && nclusters > 0) wide16[w] = 1;
+  int wide16[2];
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    GreedyDevInfo& in = info[dev];
+    if (!in.ready) {
+      for (int w = 0; w < 2; ++w) {
+        in.wide16[w] = 0;
+        if (cudaFuncSetAttribute(kern[w], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+          int nclusters = 0;
+          cfg.gridDim = dim3(16);
+          attr[0].val.clusterDim.x = 16;
+          if (cudaOccupancyMaxActiveClusters(&nclusters, kern[w], &cfg) == cudaSuccess && nclusters > 0)
+            in.wide16[w] = 1;
+        }
       }
+      cudaGetLastError();
+      in.ready = true;
     }
-    cudaGetLastError();
+    wide16[0] = in.wide16[0];
+    wide16[1] = in.wide16[1];
   }
   // one row per cluster; many rows take narrower clusters so that rows x CTAs
   // fits one wave (each CTA then streams a wider slice). Slices wider than one

@@ -50,7 +50,7 @@ extern "C" mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32
                                           const float* d_logits, const int32_t* d_draft, const float* d_q,
                                           const mtp_sampling* h_params, const int32_t* d_hist, int32_t hist_w,
                                           const float* d_u, int32_t* d_n_acc, int32_t* d_out_tok,
-                                          int32_t* d_stats, int32_t* h_out) {
+                                          int32_t* d_stats, int32_t* h_out, int32_t* d_status) {
   if (rows < 1 || depth < 1 || (long long)rows * (depth + 1) > kNoAllocDescs) return MTP_ERR_BAD_ARG;
   void* scratch = nullptr;
   const mtp_status st = scratch_address(&scratch);
@@ -58,5 +58,5 @@ extern "C" mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32
   // the scratch holds descriptors only: the streaming path (which also needs
   // per-task kept lists) stays off
   return mtp::spec_verify_impl(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u,
-                               d_n_acc, d_out_tok, d_stats, h_out, scratch, false);
+                               d_n_acc, d_out_tok, d_stats, h_out, d_status, scratch, false);
 }

@@ -335,7 +335,8 @@ def rollback_lengths(draft_len_before: int, n_acc: int, target_len: int, depth: 
     Draft KV: only the slot of the first head call (the genuine pair) survives,
     so its length becomes draft_len_before + P (P = pairs of that call).  Here
     returned for P = 1.  Target KV: trimmed by block - (n_acc + 1) with
-    block = depth + 1 positions verified ("trims by block_size - (max(accepted)
-    + 1)", qualify-on-the-qwen3_5-path comment)."""
+    block = depth + 1 positions verified, i.e. every verified position past the
+    accepted drafts and the one committed correction or bonus token ("support
+    the qwen3_5_mtp drafter" issue, comment on qualifying the qwen3_5 path)."""
     block = depth + 1
     return draft_len_before + 1, target_len - (block - (n_acc + 1))

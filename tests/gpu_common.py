@@ -129,3 +129,21 @@ def verify_near_tie(mg, n, d, greedy, gap=0.0):
 
 def draft_near_tie(margin, greedy, gap):
     return margin <= gap if greedy else margin < DRAW_BAND
+
+
+class _DevPtr:
+    """A raw device pointer presented through the CUDA array interface, so
+    that torch can view library-owned device memory without copying it."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (int(ptr), False),
+                                         "version": 3}
+
+
+def device_i32(ptr: int, n: int = 1):
+    """torch int32 view of n words at a device address owned by the library."""
+    return torch.as_tensor(_DevPtr(ptr, n), device="cuda")
+
+
+NONFINITE = 1 << 10   # 1 << MTP_ERR_NONFINITE
+TIMEOUT = 1 << 11     # 1 << MTP_ERR_TIMEOUT

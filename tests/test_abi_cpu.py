@@ -111,12 +111,12 @@ def test_config_layer_count_does_not_stand_in_for_tensors(L):
 
 def test_spec_verify_rejects_bad_arguments_without_launching(L):
     sp = m.sampling_array([dict(temperature=0.0)])
-    args = [None, 1, 2, 64, FAKE, FAKE, None, sp, None, 0, FAKE, FAKE, FAKE, None, None, FAKE]
+    args = [None, 1, 2, 64, FAKE, FAKE, None, sp, None, 0, FAKE, FAKE, FAKE, None, None, None, FAKE]
     bad = list(args)
     bad[1] = 0
     assert L.spec_verify(*bad) == 9
     bad = list(args)
-    bad[15] = None                      # no workspace
+    bad[16] = None                      # no workspace
     assert L.spec_verify(*bad) == 9
     sp2 = m.sampling_array([dict(temperature=0.7, top_p=0.9)])
     bad = list(args)
@@ -161,3 +161,8 @@ def test_draft_rejects_a_null_handle_before_any_launch(L):
     draft = torch.zeros((1, 2), dtype=torch.int32)
     with pytest.raises(m.MTPError):
         m.mtp_draft(NullHandle(), 2, [1], tok, hid, [dict(temperature=0.0)], draft, stream=0)
+
+
+def test_verify_stall_hook_rejects_bad_arguments(L):
+    assert L.mtp_test_verify_stall(-1, 100) == 9
+    assert L.mtp_test_verify_stall(1, 0) == 9
