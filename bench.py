@@ -344,6 +344,7 @@ def run_ours(args, rank, world, local_rank):
     flush, flush_flops, flush_bytes = ({}, 0.0, 0.0) if args.quick else measure_flush(tensors, embed, s, dev)
     sampled = None if args.quick else measure_sampled(tensors, embed, s, dev)
     sampled_am = None if args.quick else measure_sampled(tensors, embed, s, dev, depths=(2,), argmax_draft=True)
+    depth_ctl = None if args.quick else measure_depth_controller(tensors, embed, s, dev, sampled)
     batched = None if args.quick else measure_batched(tensors, embed, s, dev)
     stress = None if args.quick else measure_verify_stress(s, dev)
 
@@ -393,6 +394,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "sampled_depth_sweep": sampled,
         "sampled_argmax_draft_depth2": sampled_am,
+        "depth_controller": depth_ctl,
         "fp8_draft_head": fp8,
         "batched_8_rows": batched,
         "verify_stress": stress,
@@ -469,7 +471,7 @@ def measure_flush(tensors, embed, s, dev, reps: int = 20):
 SAMPLED = dict(temperature=0.8, rep_penalty=1.1, top_k=40, top_p=0.95, min_p=0.05)
 
 
-def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 4, 5, 6), argmax_draft=False):
+def measure_sampled(tensors, embed, s, dev, rounds: int = 1000, depths=(1, 2, 3, 4, 5, 6), argmax_draft=False):
     """Sampled decoding on the 27B-shaped head: T 0.8, repetition penalty 1.1
     over a 64-token history, top-k 40, top-p 0.95, min-p 0.05, depth 1..6.
     Target row i = the drafter's logits at step i+1 plus N(0,1) noise (the
@@ -544,7 +546,10 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 
         prof = m.mtp_profile_read(h)
         m.mtp_profile_enable(h, False)
         out[str(depth)] = {"rounds": int(st[0]), "rollbacks": int(st[1]),
+                           "accepts_per_position": [int(x) for x in st[2:]],
                            "accept_per_position": [round(int(x) / max(int(st[0]), 1), 4) for x in st[2:]],
+                           "round_ms": round(ms / rounds, 4),
+                           "committed_per_round": round(committed / rounds, 4),
                            "draft_tok_per_s": round(rounds * depth / (ms / 1e3), 1),
                            "committed_tok_per_s": round(committed / (ms / 1e3), 1),
                            "verify_us": round(1e3 * vt / rounds, 2),
@@ -552,6 +557,120 @@ def measure_sampled(tensors, embed, s, dev, rounds: int = 100, depths=(1, 2, 3, 
                            if prof["sample"][1] else 0.0}
         h.close()
     return out
+
+
+# A 27B-parameter bf16 target streams its 54 GB of weights once per forward;
+# at batch 1 and a handful of verified positions that read, not the position
+# count, sets its time. The depth-controller leg models the target this way.
+TARGET_BYTES = 27e9 * 2
+
+
+def measure_depth_controller(tensors, embed, s, dev, sweep, rounds: int = 400, max_depth: int = 6):
+    """The draft-depth controller choosing the depth of every round of the
+    sampled workload (the sweep's parameters, target rows, noise and history)
+    from live per-position acceptance and measured round times.  The target
+    model is not part of this benchmark: each round's measured time gets the
+    modelled target forward added (TARGET_BYTES at the measured HBM peak), and
+    a plain-decode round (depth 0) costs that alone and commits one token.
+    Reported beside the depth that maximises committed tokens per second in
+    the measured sweep under the same model."""
+    import torch
+
+    import mtp_speculative_decoding_step_gb300 as m
+    import synth
+    V, H, W = s.vocab, s.hidden, 64
+    cap = KV_LEN + 1024
+    peak, _ = peaks()
+    t_target = TARGET_BYTES / (peak * 1e9)
+    params = m.sampling_array([SAMPLED])
+    stream = torch.cuda.current_stream()
+    noise = torch.from_numpy(synth.normal(7, "smp:noise", (8, 6, V), std=1.0)).to(dev)
+    bonus = torch.from_numpy(synth.normal(7, "smp:bonus", (8, V), std=4.0)).to(dev)
+    thid = torch.from_numpy(synth.normal(7, "smp:hid", (8, 264, H), dtype="bf16")).view(torch.bfloat16).to(dev)
+    plain_tok = synth.randint(7, "ctl:plain", (rounds + 4,), V)
+    K, Vc = synth.kv_prefill(s, 7, 1, cap, [KV_LEN])
+    kk = torch.from_numpy(K).view(torch.bfloat16).to(dev)
+    vv = torch.from_numpy(Vc).view(torch.bfloat16).to(dev)
+    klen = torch.tensor([KV_LEN], dtype=torch.int32, device=dev)
+    h = m.mtp_load(m.make_config(s, 1, cap, max_depth), tensors, embed, None, kk, vv, klen, lengths=[KV_LEN])
+    ctl = m.DepthController(max_depth)
+    hist = torch.from_numpy(synth.randint(7, "smp:hist", (1, W), V)).to(dev)
+    ud = torch.from_numpy(synth.uniform(7, "ctl:ud", (rounds + 4, 1, max_depth))).to(dev)
+    uv = torch.from_numpy(synth.uniform(7, "ctl:uv", (rounds + 4, 1, max_depth + 1))).to(dev)
+    draft = torch.zeros((1, max_depth), dtype=torch.int32, device=dev)
+    q = torch.zeros((1, max_depth, V), dtype=torch.float32, device=dev)
+    dl = torch.zeros((1, max_depth, V), dtype=torch.float32, device=dev)
+    tl = torch.zeros((1, max_depth + 1, V), dtype=torch.float32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    pend = torch.zeros((1, 256), dtype=torch.int32, device=dev)  # pending pairs' tokens (newest last)
+    pend[0, 0] = 11
+    h_out = torch.zeros(max_depth + 2, dtype=torch.int32).pin_memory()
+    P, chosen, committed, model_s = 1, [], 0, 0.0
+    for r in range(rounds):
+        d = ctl.next()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if d == 0 and P < 250:
+            # plain decode: the target alone commits one token; its pair joins the pending ones
+            pend[0, P] = int(plain_tok[r])
+            P += 1
+            n = 0
+        else:
+            d = max(d, 1)  # (a long run of plain rounds is flushed by a drafting round)
+            if m.mtp_get_lengths(h)[0] + P + d > cap:
+                m.mtp_set_lengths(h, [KV_LEN])
+            dr, qq, dd = draft[:, :d], q[:, :d], dl[:, :d]
+            out_tok = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+            tlv = tl[:, :d + 1]
+            m.mtp_draft(h, d, [P], pend[:, :P].contiguous(), thid[r % 8].view(1, 264, H)[:, :P], params, dr,
+                        hist=hist, u=ud[r, :, :d].contiguous(), q=qq, logits=dd)
+            tlv[0, :d] = dd[0] + noise[r % 8, :d]
+            tlv[0, d] = bonus[r % 8]
+            h_out[0] = -1
+            m.spec_verify(tlv, dr, params, uv[r, :, :d + 1].contiguous(), n_acc, out_tok, ws_for(dev, d, V, m),
+                          q=qq, hist=hist, h_out=h_out)
+            m.kv_rollback(h, 1, d)
+            stream.synchronize()
+            n = int(h_out[0])
+            hist = torch.cat([hist[:, n + 1:], out_tok[:, :n + 1]], dim=1)
+            pend[0, :n + 1] = out_tok[0, :n + 1]
+            P = n + 1
+        dt = time.perf_counter() - t0 + t_target
+        ctl.observe(d, n, dt)
+        model_s += dt
+        committed += n + 1
+        chosen.append(d)
+    a, cost, interval = ctl.state()
+    h.close()
+    ctl.close()
+    tail = chosen[rounds // 2:]
+    settled = max(set(tail), key=tail.count)
+    # the sweep's best depth under the same target model (depth 0 = plain decode)
+    rate = {"0": 1.0 / t_target}
+    for k, v in (sweep or {}).items():
+        rate[k] = v["committed_per_round"] / (v["round_ms"] / 1e3 + t_target)
+    best = max(rate, key=rate.get)
+    return {"rounds": rounds, "max_depth": max_depth, "target_model_ms": round(t_target * 1e3, 3),
+            "target_model": "27e9 bf16 weights read once per round at the measured HBM peak",
+            "settled_depth": int(settled),
+            "depth_histogram_second_half": {str(k): tail.count(k) for k in sorted(set(tail))},
+            "committed_tok_per_s_modelled": round(committed / model_s, 1),
+            "accept_estimate": [round(float(x), 4) for x in a],
+            "round_cost_ms_estimate": [round(float(x) * 1e3, 4) for x in cost],
+            "probe_interval": interval,
+            "sweep_best_depth": int(best),
+            "sweep_committed_tok_per_s_modelled": {k: round(v, 1) for k, v in rate.items()}}
+
+
+_WS = {}
+
+
+def ws_for(dev, depth, V, m):
+    """One verify workspace per depth (made once, outside the timed rounds' hot path)."""
+    import torch
+    if depth not in _WS:
+        _WS[depth] = torch.zeros(m.spec_verify_workspace_bytes(1, depth, V), dtype=torch.uint8, device=dev)
+    return _WS[depth]
 
 
 def measure_batched(tensors, embed, s, dev, reps: int = 20):
@@ -714,7 +833,7 @@ def cpu_rounds(work, budget_s: float, max_rounds: int):
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    return done, time.perf_counter() - t0, int(os.environ.get("OMP_NUM_THREADS", os.cpu_count()))
+    return done, time.perf_counter() - t0, oracle.threads()
 
 
 def main():
@@ -825,6 +944,13 @@ def main():
             result["cpu_baseline"] = {"value": round(n * DEPTH / sec, 3), "unit": "draft tok/s", "cores": thr,
                                       "kind": "oracle",
                                       "sample": f"{n} whole rounds (2 draft steps + verify) of the same workload"}
+            # the same oracle on one host core
+            oracle.set_threads(1)
+            n1, sec1, thr1 = cpu_rounds(work, args.cpu_budget, 100000)
+            oracle.set_threads(thr)
+            result["cpu_baseline"]["one_core"] = {
+                "value": round(n1 * DEPTH / sec1, 3), "unit": "draft tok/s", "cores": thr1,
+                "sample": f"{n1} whole rounds (2 draft steps + verify) of the same workload"}
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -103,8 +103,19 @@ def _load():
         lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_quantize_rows_e4m3.argtypes = [vp, ci, ci, vp, vp]
+        lib.orc_set_threads.argtypes = [ci]
+        lib.orc_threads.restype = ci
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (results do not depend on it)."""
+    _load().orc_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(_load().orc_threads())
 
 
 def e4m3_encode(x: float) -> int:

@@ -29,9 +29,16 @@
  * Where the pages are silent the readings are stated beside the code.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads of the parallel loops below (the CPU baseline runs on all host
+ * cores, then on one). No arithmetic depends on it: every reduction is a
+ * sequential loop inside one thread. */
+void orc_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int orc_threads(void) { return omp_get_max_threads(); }
 
 /* ---------------------------------------------------------------- storage */
 
