@@ -289,6 +289,12 @@ size_t verify_stream_smem(int V, int* ring_ns = nullptr);
 // All rows greedy without a repetition penalty: argmax matches in one launch
 // (depth <= 16; desc, q, hist and u unused).
 void launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
+// The same for many rows as one balanced stream over [rows][depth+1][V]
+// (equal ranges per CTA, one key per touched segment in d_part, then a
+// per-row finish). False, launching nothing, where it does not apply (V % 4,
+// alignment, or more than kFlatMaxCTAs ranges or part_bytes of keys needed).
+constexpr int kFlatMaxCTAs = 2048;
+bool launch_verify_greedy_flat(const VerifyArgs& a, void* d_part, size_t part_bytes, cudaStream_t s);
 
 // Multiprocessor count of the current device (looked up once per device).
 constexpr int kMaxDevices = 64;
@@ -300,6 +306,6 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
                             const int32_t* d_draft, const float* d_q, const mtp_sampling* h_params,
                             const int32_t* d_hist, int32_t hist_w, const float* d_u, int32_t* d_n_acc,
                             int32_t* d_out_tok, int32_t* d_stats, int32_t* h_out, int32_t* d_status,
-                            void* d_workspace, bool allow_stream);
+                            void* d_workspace, size_t workspace_bytes, bool allow_stream);
 
 }  // namespace mtp

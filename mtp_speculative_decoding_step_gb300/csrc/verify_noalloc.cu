@@ -58,5 +58,6 @@ extern "C" mtp_status spec_verify_noalloc(mtp_stream stream, int32_t rows, int32
   // the scratch holds descriptors only: the streaming path (which also needs
   // per-task kept lists) stays off
   return mtp::spec_verify_impl(stream, rows, depth, vocab, d_logits, d_draft, d_q, h_params, d_hist, hist_w, d_u,
-                               d_n_acc, d_out_tok, d_stats, h_out, d_status, scratch, false);
+                               d_n_acc, d_out_tok, d_stats, h_out, d_status, scratch, sizeof(g_verify_scratch),
+                               false);
 }

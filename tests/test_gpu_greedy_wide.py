@@ -1,9 +1,7 @@
-"""The one-launch greedy verify where each CTA's vocabulary slice is wider
-than one round of its loads: many rows (the cluster narrows so that rows x
-CTAs fits one wave, each CTA then streams V/2 or V of every position), and a
-vocabulary of 2^20 (16-CTA clusters, 65536 logits per slice). Greedy decisions
-are argmax matches (value desc, id asc), so they are compared exactly with
-the oracle."""
+"""The greedy verify at wide shapes: many rows at the full vocabulary, and a
+vocabulary of 2^20 with maxima deep inside it and an exact tie. Greedy
+decisions are argmax matches (value desc, id asc), so they are compared
+exactly with the oracle."""
 import numpy as np
 import pytest
 import torch
