@@ -285,6 +285,32 @@ void launch_verify(const VerifyArgs& a, cudaStream_t s);
 // row's accept chain and draws over the stopping position's kept list.
 constexpr int kStreamTopK = 256;
 void launch_verify_stream(const VerifyArgs& a, cudaStream_t s);
+// The per-row accept chain and draw over the kept lists (wdesc, acc, kid, kkey).
+void launch_verify_finish(const VerifyArgs& a, cudaStream_t s);
+
+// Exact top-k transform of rows that cut to a top-k of at most kStreamTopK
+// (or are greedy), one 8-CTA cluster per task: draft steps (mode 0: q and the
+// draw) or verify tasks (mode 1: descriptor, accept test and kept list for
+// launch_verify_finish).
+struct TopkArgs {
+  int mode;
+  int rows, V, W, depth, pos;
+  const float* logits;   // mode 0: [rows][ld]; mode 1: [rows][depth+1][V]
+  long long ld;
+  const int32_t* hist;   // [rows][W]
+  const int32_t* drafts; // [rows][depth]
+  const float* u;        // mode 0: [rows][depth]; mode 1: [rows][depth+1]
+  float* q;              // mode 0: out [rows][depth][V]; mode 1: the drafts' q (in)
+  int32_t* draft_out;    // mode 0
+  TDesc* wdesc;          // mode 1: [rows][depth+1]
+  int32_t* acc;
+  int32_t* kid;
+  uint32_t* kkey;
+  int32_t* status;
+  RowParams p[kMaxRows];
+};
+bool topk_fits(const RowParams* p, int rows, int V, const float* logits, long long ld);
+void launch_topk(const TopkArgs& a, cudaStream_t s);
 size_t verify_stream_smem(int V, int* ring_ns = nullptr);
 // All rows greedy without a repetition penalty: argmax matches in one launch
 // (depth <= 16; desc, q, hist and u unused).

@@ -538,6 +538,14 @@ bool stream_verify_fits(int rows, int depth, int vocab, const mtp_sampling* hp) 
   return true;
 }
 
+// Every sampled row cuts to a top-k of at most kStreamTopK and the rows fit
+// the one-cluster-per-task top-k transform.
+bool topk_rows(int rows, int vocab, const float* logits, const mtp_sampling* hp) {
+  RowParams rp[kMaxRows];
+  for (int r = 0; r < rows; ++r) rp[r] = row_params(hp[r]);
+  return topk_fits(rp, rows, vocab, logits, vocab);
+}
+
 // K splits so that (M tiles) x (N tiles) x splits fills at most one wave.
 int tc_splits(int mtiles, int ntiles, int ktiles, int sms, int max_splits) {
   int best = 1;
@@ -1037,7 +1045,11 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
     // batch 1, V = 152064); the single cluster launch takes what it cannot
     // (rows not 16-byte aligned, V % 4 != 0)
     if (!launch_verify_greedy_flat(va, d_workspace, workspace_bytes, s)) launch_verify_greedy(va, s);
-  } else if (allow_stream && stream_verify_fits(rows, depth, vocab, h_params)) {
+  } else if (allow_stream && (stream_verify_fits(rows, depth, vocab, h_params) || topk_rows(rows, vocab, d_logits, h_params))) {
+    // rows that cut to a small top-k: many tasks stream (one CTA per task),
+    // fewer take one cluster per task; both write the descriptors, accept
+    // flags and kept lists that the per-row finish draws from
+    const bool streaming = stream_verify_fits(rows, depth, vocab, h_params);
     const size_t tasks = (size_t)rows * (depth + 1);
     uint8_t* w = static_cast<uint8_t*>(d_workspace);
     VerifyArgs va;
@@ -1053,10 +1065,22 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
     w += align256(sizeof(int32_t) * tasks * kStreamTopK);
     va.kkey = reinterpret_cast<uint32_t*>(w);
     va.n_acc = d_n_acc; va.out_tok = d_out_tok; va.stats = d_stats; va.h_rec = h_rec; va.status = d_status;
-    va.stall_stage = g_stall_stage.exchange(-1);
-    va.wait_limit = va.stall_stage >= 0 ? g_stall_polls.load() : 0u;
     for (int r = 0; r < rows; ++r) va.p[r] = row_params(h_params[r]);
-    launch_verify_stream(va, s);
+    if (streaming) {
+      va.stall_stage = g_stall_stage.exchange(-1);
+      va.wait_limit = va.stall_stage >= 0 ? g_stall_polls.load() : 0u;
+      launch_verify_stream(va, s);
+    } else {
+      TopkArgs t;
+      std::memset(&t, 0, sizeof(t));
+      t.mode = 1; t.rows = rows; t.V = vocab; t.W = hist_w; t.depth = depth;
+      t.logits = d_logits; t.ld = vocab; t.hist = d_hist; t.drafts = d_draft; t.u = d_u;
+      t.q = const_cast<float*>(d_q);
+      t.wdesc = va.wdesc; t.acc = va.acc; t.kid = va.kid; t.kkey = va.kkey; t.status = d_status;
+      for (int r = 0; r < rows; ++r) t.p[r] = va.p[r];
+      launch_topk(t, s);
+      launch_verify_finish(va, s);
+    }
   } else {
     TDesc* desc = static_cast<TDesc*>(d_workspace);
     SampleArgs sa;

@@ -20,6 +20,7 @@
 // every result is independent of thread scheduling.
 #include <cooperative_groups.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -2363,6 +2364,428 @@ __global__ void __launch_bounds__(kStreamTopK) k_verify_finish(const __grid_cons
   }
 }
 
+// ------------------------------------------------------------ top-k transform
+// Low-latency exact transform of one (row, position) whose row cuts to a
+// top-k of at most kStreamTopK (or is greedy), one 8-CTA cluster per task:
+//  1. each CTA stages its vocabulary slice (repetition penalty, the argmax of
+//     the penalised logits, z / T and its key), and every thread keeps the
+//     smallest (key, id) it saw;
+//  2. every CTA copies the cluster's 4096 thread minima and selects their
+//     k-th smallest: k distinct elements lie at or below it, so the row's
+//     top-k does too;
+//  3. each CTA gathers its elements at or below that bound (typically a little
+//     over k in all), the cluster exchanges them once, and every CTA selects
+//     and sorts the exact top-k of the union;
+//  4. the candidate path's cut rules on that sorted list (top-p on the
+//     fixed-point mass of the top-k, min-p, at least one token) give the
+//     descriptor, so every decision equals the cluster path's.
+// If the bound admits more elements than the buffers hold (heavy ties), the
+// exact k-th comes from the cluster radix selection and the gather is redone.
+// Draft steps (mode 0) write q and draw; verify tasks (mode 1) write the
+// descriptor, the accept test of the draft their row judges and the kept list
+// that k_verify_finish draws from.
+constexpr int kTkLocCap = 512;     // candidates one CTA may gather
+constexpr int kTkMergeCap = 1024;  // candidates of the whole cluster
+constexpr int kTkLocalK = 64;      // top-k up to this bound from each CTA's own thread minima
+
+__host__ __device__ inline int tk_per(int V) { return (((V + kClusterCTAs - 1) / kClusterCTAs) + 3) & ~3; }
+
+struct TkLayout {
+  size_t zs, bits, tmk, tmi, allk, alli, tie, lk, li, mk, mi, sk, si, sw, sid, total;
+  __host__ __device__ explicit TkLayout(int V) {
+    const int per = tk_per(V);
+    size_t o = (sizeof(SampleSmem) + 15) & ~size_t(15);
+    zs = o;
+    o += 4 * (size_t)per;
+    bits = o;
+    o += 4 * (size_t)((per + 31) / 32 + 1);
+    o = (o + 15) & ~size_t(15);
+    tmk = o; o += 4 * kST;
+    tmi = o; o += 4 * kST;
+    allk = o; o += 4 * kST * kClusterCTAs;
+    alli = o; o += 4 * kST * kClusterCTAs;
+    tie = o; o += 4 * kST * kClusterCTAs;
+    lk = o; o += 4 * kTkLocCap;
+    li = o; o += 4 * kTkLocCap;
+    mk = o; o += 4 * kTkMergeCap;
+    mi = o; o += 4 * kTkMergeCap;
+    sk = o; o += 4 * kStreamTopK;
+    si = o; o += 4 * kStreamTopK;
+    o = (o + 7) & ~size_t(7);
+    sw = o; o += 8 * kStreamTopK;
+    sid = o; o += 4 * kStreamTopK;
+    total = o;
+  }
+};
+
+__global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  const TkLayout lay(a.V);
+  float* zs = reinterpret_cast<float*>(dyn + lay.zs);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + lay.bits);
+  uint32_t* tmk = reinterpret_cast<uint32_t*>(dyn + lay.tmk);
+  int* tmi = reinterpret_cast<int*>(dyn + lay.tmi);
+  uint32_t* allk = reinterpret_cast<uint32_t*>(dyn + lay.allk);
+  int* alli = reinterpret_cast<int*>(dyn + lay.alli);
+  int* tie = reinterpret_cast<int*>(dyn + lay.tie);
+  uint32_t* lk = reinterpret_cast<uint32_t*>(dyn + lay.lk);
+  int* li = reinterpret_cast<int*>(dyn + lay.li);
+  uint32_t* mk = reinterpret_cast<uint32_t*>(dyn + lay.mk);
+  int* mi = reinterpret_cast<int*>(dyn + lay.mi);
+  uint32_t* sk = reinterpret_cast<uint32_t*>(dyn + lay.sk);
+  int* si = reinterpret_cast<int*>(dyn + lay.si);
+  unsigned long long* sw = reinterpret_cast<unsigned long long*>(dyn + lay.sw);
+  int* sid = reinterpret_cast<int*>(dyn + lay.sid);
+  __shared__ float s_bv[kST / 32];
+  __shared__ int s_bi[kST / 32];
+  Clu c(sm);
+  pdl_wait();
+  pdl_trigger();
+  const int task = blockIdx.x / kClusterCTAs;
+  int r, i;
+  const float* lg;
+  if (a.mode == 0) {
+    r = task;
+    i = a.pos;
+    lg = a.logits + (size_t)r * a.ld;
+  } else {
+    r = task / (a.depth + 1);
+    i = task - r * (a.depth + 1);
+    lg = a.logits + ((size_t)r * (a.depth + 1) + i) * a.V;
+  }
+  const RowParams p = a.p[r];
+  const int per = tk_per(a.V);
+  const int v0 = min(c.rank * per, a.V);
+  const int n = min(per, a.V - v0);
+  const int32_t* dr = a.drafts + (size_t)r * a.depth;
+  load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, i);
+  const bool pen = p.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, v0, n);
+  const bool smp = !p.greedy;
+  const float T = smp ? p.temperature : 1.f;
+
+  // 1. stage the slice: penalty, argmax of the penalised logits, z / T, keys,
+  //    and each thread's smallest (key, id). A thread keeps four independent
+  //    chains, one per vector lane, merged at the end; ids ascend within a
+  //    chain, so strict comparisons keep the lowest id on ties.
+  float bz[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  int bzi[4] = {0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF};
+  uint32_t tk[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+  int ti[4] = {0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF};
+  float nf = 0.f;  // x * 0: NaN once a NaN or an infinity has been read
+  {
+    const float4* l4 = reinterpret_cast<const float4*>(lg + v0);
+    const int n4 = n / 4;
+    for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+      float4 xb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j4 = b0 + u * kST + threadIdx.x;
+        if (j4 < n4) xb[u] = __ldg(l4 + j4);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j4 = b0 + u * kST + threadIdx.x;
+        if (j4 < n4) {
+          const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+          const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
+          float zt4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            nf = fmaf(xs[e], 0.f, nf);
+            const float z = ((wb >> e) & 1u) ? penalize(xs[e], p.rep_penalty) : xs[e];
+            if (z > bz[e]) { bz[e] = z; bzi[e] = v0 + j; }
+            zt4[e] = z / T + 0.0f;
+            const uint32_t key = desc_key(zt4[e]);
+            if (key < tk[e]) { tk[e] = key; ti[e] = v0 + j; }
+          }
+          reinterpret_cast<float4*>(zs)[j4] = make_float4(zt4[0], zt4[1], zt4[2], zt4[3]);
+        }
+      }
+    }
+  }
+  float bzv = bz[0];
+  int bzid = bzi[0];
+  uint32_t tkk = tk[0];
+  int tid_ = ti[0];
+#pragma unroll
+  for (int e = 1; e < 4; ++e) {
+    if (better(bz[e], bzi[e], bzv, bzid)) { bzv = bz[e]; bzid = bzi[e]; }
+    if (tk[e] < tkk || (tk[e] == tkk && ti[e] < tid_)) { tkk = tk[e]; tid_ = ti[e]; }
+  }
+  if (tkk == 0xFFFFFFFFu && tid_ == 0x7FFFFFFF) tid_ = 0x7FFFFFFF - (c.rank * kST + (int)threadIdx.x);  // distinct placeholder
+  if (__syncthreads_or(isnan(nf)) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
+  tmk[threadIdx.x] = tkk;
+  tmi[threadIdx.x] = tid_;
+  block_argmax(bzv, bzid, s_bv, s_bi);
+  // small k: this CTA's k-th smallest thread minimum (k distinct elements of
+  // the slice lie at or below it); the cluster's smallest such bound is
+  // published with the argmax
+  const int k = p.top_k;  // 2 <= k <= kStreamTopK < V for sampled rows (checked by the host)
+  const bool local_bound = !p.greedy && k <= kTkLocalK;
+  uint32_t Kc = 0xFFFFFFFFu;
+  int Ic = 0x7FFFFFFF;
+  if (local_bound) stream_select(sm, tmk, tmi, kST, k, tie, Kc, Ic);
+  if (threadIdx.x == 0) {
+    sm->mail[c.ph].f[0] = bzv;
+    sm->mail[c.ph].i[0] = bzid;
+    sm->mail[c.ph].u[0] = ((unsigned long long)Kc << 32) | (uint32_t)Ic;
+  }
+  Mail* m = c.publish();
+  float gv = -INFINITY;
+  int gi = 0x7FFFFFFF;
+#pragma unroll
+  for (int q = 0; q < kClusterCTAs; ++q) {
+    Mail* x = c.remote(m, q);
+    if (better(x->f[0], x->i[0], gv, gi)) { gv = x->f[0]; gi = x->i[0]; }
+  }
+  const int argmax = gi < a.V ? gi : 0;  // nothing comparable (every logit NaN): id 0
+  unsigned long long kb = ~0ull;
+#pragma unroll
+  for (int q = 0; q < kClusterCTAs; ++q) kb = min(kb, c.remote(m, q)->u[0]);
+
+  if (!smp) {  // greedy: the point mass at the argmax
+    if (c.rank == 0 && threadIdx.x == 0) {
+      if (a.mode == 0) {
+        a.draft_out[(size_t)r * a.depth + i] = argmax;
+      } else {
+        TDesc dd;
+        dd.argmax = argmax;
+        dd.k_key = 0xFFFFFFFFu;
+        dd.k_cut = 0x7FFFFFFF;
+        dd.p_key = 0xFFFFFFFFu;
+        dd.p_cut = 0x7FFFFFFF;
+        dd.m = 0.f;
+        dd.S = 1.f;
+        dd.kept = 1;
+        a.wdesc[task] = dd;
+        a.acc[task] = (i < a.depth && dr[i] == argmax) ? 1 : 0;
+      }
+    }
+    c.cl.sync();  // every CTA has read this one's mail
+    return;
+  }
+
+  // 2. the bound: for small k the smallest of the CTAs' own k-th thread
+  //    minima; else the k-th smallest of the cluster's thread minima (either
+  //    way k distinct elements lie at or below it, so the top-k does too)
+  uint32_t K0 = (uint32_t)(kb >> 32);
+  int I0 = (int)(uint32_t)kb;
+  if (!local_bound) {
+    for (int t = threadIdx.x; t < kST * kClusterCTAs; t += kST) {
+      const int rr = t / kST, q = t - rr * kST;
+      allk[t] = c.cl.map_shared_rank(tmk, rr)[q];
+      alli[t] = c.cl.map_shared_rank(tmi, rr)[q];
+    }
+    __syncthreads();
+    stream_select(sm, allk, alli, kST * kClusterCTAs, k, tie, K0, I0);
+  }
+
+  // 3. gather the elements at or below the bound, exchange them once
+  auto gather = [&](uint32_t K, int cut) {
+    if (threadIdx.x == 0) sm->ccount = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += kST) {
+      const uint32_t key = desc_key(zs[j]);
+      if (in_prefix(key, v0 + j, K, cut)) {
+        const int pos = atomicAdd(&sm->ccount, 1);
+        if (pos < kTkLocCap) {
+          lk[pos] = key;
+          li[pos] = v0 + j;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sm->mail[c.ph].i[0] = sm->ccount;
+    return c.publish();
+  };
+  int off[kClusterCTAs + 1];
+  auto offsets = [&](Mail* mm) {
+    bool over = false;
+    off[0] = 0;
+#pragma unroll
+    for (int q = 0; q < kClusterCTAs; ++q) {
+      const int cq = c.remote(mm, q)->i[0];
+      over |= cq > kTkLocCap;
+      off[q + 1] = off[q] + min(cq, kTkLocCap);
+    }
+    return over || off[kClusterCTAs] > kTkMergeCap;
+  };
+  if (offsets(gather(K0, I0))) {
+    // too many at the bound: the exact k-th by cluster radix selection
+    uint32_t Kx;
+    unsigned long long rem;
+    radix_select(c, zs, n, [](int) { return true; }, [](int) { return 1ull; }, (unsigned long long)k, Kx, rem);
+    const int cut = tie_cut(c, zs, n, v0, [](int) { return true; }, Kx, rem);
+    offsets(gather(Kx, cut));
+  }
+  const int M = min(off[kClusterCTAs], kTkMergeCap);
+  for (int t = threadIdx.x; t < M; t += kST) {
+    int q = 0;
+    while (t >= off[q + 1]) ++q;
+    mk[t] = c.cl.map_shared_rank(lk, q)[t - off[q]];
+    mi[t] = c.cl.map_shared_rank(li, q)[t - off[q]];
+  }
+  __syncthreads();
+  // the exact top-k of the union (it holds at least k), sorted by (key, id)
+  uint32_t Kk = 0xFFFFFFFFu;
+  int Ik = 0x7FFFFFFF;
+  if (M > k) stream_select(sm, mk, mi, M, k, tie, Kk, Ik);
+  if (threadIdx.x == 0) sm->ccount = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < M; t += kST)
+    if (in_prefix(mk[t], mi[t], Kk, Ik)) {
+      const int pos = atomicAdd(&sm->ccount, 1);
+      if (pos < kStreamTopK) {
+        sk[pos] = mk[t];
+        si[pos] = mi[t];
+      }
+    }
+  __syncthreads();
+  const int L = min(sm->ccount, kStreamTopK);  // == k
+  rank_sort(sk, si, L);
+
+  // 4. cut rules on the sorted top-k: top-p on its fixed-point mass, then
+  //    min-p, at least one token kept
+  const float mx = key_to_z(sk[0]);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    auto fx = [&](int j) { return to_fix(expf(key_to_z(sk[j]) - mx)); };
+    unsigned long long SE = 0;
+    warp_find_cross(L, ~0ull, fx, &SE);
+    int Kf = L;
+    if (p.top_p > 0.f && p.top_p < 1.f) {
+      const unsigned long long target = (unsigned long long)ceil((double)p.top_p * (double)SE);
+      const int j = warp_find_cross(L, target, fx, nullptr);
+      if (j < L) Kf = min(Kf, j + 1);
+    }
+    if (p.min_p > 0.f) {
+      int first = L;
+      for (int j = lane; j < L; j += 32)
+        if (!(expf(key_to_z(sk[j]) - mx) >= p.min_p)) { first = j; break; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
+      if (first < Kf) Kf = first;
+    }
+    if (Kf < 1) Kf = 1;
+    unsigned long long Sf = 0;
+    warp_find_cross(Kf, ~0ull, fx, &Sf);
+    if (lane == 0) {
+      sm->fin_kf = Kf;
+      sm->fin_sf = Sf;
+    }
+  }
+  __syncthreads();
+  TDesc dd;
+  dd.argmax = argmax;
+  dd.k_key = 0xFFFFFFFFu;
+  dd.k_cut = 0x7FFFFFFF;
+  dd.kept = sm->fin_kf;
+  dd.p_key = sk[dd.kept - 1];
+  dd.p_cut = si[dd.kept - 1];
+  dd.m = mx;
+  dd.S = (float)((double)sm->fin_sf / kFix);
+  const int Kf = dd.kept;
+
+  if (a.mode == 1) {
+    if (c.rank == 0) {
+      int32_t* kid = a.kid + (size_t)task * kStreamTopK;
+      uint32_t* kkey = a.kkey + (size_t)task * kStreamTopK;
+      for (int t = threadIdx.x; t < Kf; t += kST) { kid[t] = si[t]; kkey[t] = sk[t]; }
+      if (threadIdx.x == 0) {
+        a.wdesc[task] = dd;
+        // the accept test of draft x_{i+1} against this target row
+        int acc = 0;
+        if (i < a.depth) {
+          const int x = dr[i];
+          if (x >= 0 && x < a.V) {  // an out-of-range draft is rejected, never dereferenced
+            bool px = false;
+            for (int t = 0; t < sm->nwin; ++t) px |= sm->wtok[t] == x;
+            const float pv = eval_p(dd, p, __ldg(lg + x), pen && px, x);
+            // an argmax draft is a point mass: q(x) = 1
+            const float qv = p.argmax_draft ? 1.f : __ldg(a.q + ((size_t)r * a.depth + i) * a.V + x);
+            acc = qv > 0.f && a.u[(size_t)r * (a.depth + 1) + i] < pv / qv;
+          }
+        }
+        a.acc[task] = acc;
+      }
+    }
+  } else {
+    // q over the slice: the kept prefix of the (key, id) order, renormalised
+    float4* q4 = reinterpret_cast<float4*>(a.q + ((size_t)r * a.depth + i) * a.V + v0);
+    for (int j4 = threadIdx.x; j4 < n / 4; j4 += kST) {
+      float o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * j4 + e;
+        o[e] = 0.f;
+        if (in_prefix(desc_key(zs[j]), v0 + j, dd.p_key, dd.p_cut)) {
+          const float ev = expf(zs[j] - mx);
+          if (!(p.min_p > 0.f) || ev >= p.min_p) o[e] = ev / dd.S;
+        }
+      }
+      q4[j4] = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    if (c.rank == 0) {
+      // the draw: the kept entries in id order, weights to_fix(q)
+      for (int t = threadIdx.x; t < Kf; t += kST) {
+        const int id = si[t];
+        int rank = 0;
+        for (int q = 0; q < Kf; ++q) rank += si[q] < id;
+        sid[rank] = id;
+        sw[rank] = to_fix(expf(key_to_z(sk[t]) - dd.m) / dd.S);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        unsigned long long tot = 0;
+        warp_find_cross(Kf, ~0ull, [&](int j) { return sw[j]; }, &tot);
+        int pick = -1;
+        if (tot > 0) {
+          const float u = a.u[(size_t)r * a.depth + i];
+          const unsigned long long target = (unsigned long long)floor((double)u * (double)tot) + 1ull;
+          const int j = warp_find_cross(Kf, target, [&](int j) { return sw[j]; }, nullptr);
+          pick = j < Kf ? sid[j] : sid[Kf - 1];
+        }
+        if (threadIdx.x == 0) a.draft_out[(size_t)r * a.depth + i] = pick >= 0 ? pick : argmax;
+      }
+    }
+  }
+  c.cl.sync();  // keep shared memory alive until every remote read is done
+}
+
+bool topk_fits(const RowParams* p, int rows, int V, const float* logits, long long ld) {
+  if (V % 4 != 0 || (reinterpret_cast<uintptr_t>(logits) & 15) != 0 || ld % 4 != 0 ||
+      TkLayout(V).total > 226 * 1024)
+    return false;
+  for (int r = 0; r < rows; ++r)
+    if (!p[r].greedy && !(p[r].top_k >= 1 && p[r].top_k <= kStreamTopK && p[r].top_k < V)) return false;
+  return true;
+}
+
+void launch_topk(const TopkArgs& a, cudaStream_t s) {
+  const int smem = (int)TkLayout(a.V).total;
+  cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaLaunchConfig_t cfg = {};
+  const int tasks = a.mode == 0 ? a.rows : a.rows * (a.depth + 1);
+  cfg.gridDim = dim3(tasks * kClusterCTAs);
+  cfg.blockDim = dim3(kST);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCTAs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, k_topk, a);
+  count_launch();
+}
+
 static int sample_smem(int V, int C = 0, int P = 0) {
   const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
   const size_t cand = 16 + (size_t)C * 8 + (size_t)P * 8 + (size_t)C * 4 + 4 + (size_t)C * 8;
@@ -2392,6 +2815,16 @@ static void launch_cluster(void (*k)(Args), const Args& a, int tasks, int V, cud
 }
 
 void launch_sample(const SampleArgs& a0, cudaStream_t s) {
+  if (a0.mode == 0 && topk_fits(a0.p, a0.rows, a0.V, a0.logits, a0.ld)) {
+    TopkArgs t;
+    memset(&t, 0, sizeof(t));
+    t.mode = 0; t.rows = a0.rows; t.V = a0.V; t.W = a0.W; t.depth = a0.depth; t.pos = a0.pos;
+    t.logits = a0.logits; t.ld = a0.ld; t.hist = a0.hist; t.drafts = a0.drafts; t.u = a0.u; t.q = a0.q;
+    t.draft_out = a0.draft_out; t.status = a0.status;
+    for (int r = 0; r < a0.rows; ++r) t.p[r] = a0.p[r];
+    launch_topk(t, s);
+    return;
+  }
   SampleArgs a = a0;
   int C = 1;
   for (int r = 0; r < a.rows; ++r) {
@@ -2423,6 +2856,10 @@ void launch_verify_stream(const VerifyArgs& a0, cudaStream_t s) {
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   launch_pdl(k, dim3(a.rows * (a.depth + 1)), dim3(kST), smem, s, a);
   count_launch();
+  launch_verify_finish(a, s);
+}
+
+void launch_verify_finish(const VerifyArgs& a, cudaStream_t s) {
   launch_pdl(k_verify_finish, dim3(a.rows), dim3(kStreamTopK), 0, s, a);
   count_launch();
 }
