@@ -17,6 +17,8 @@
 
 #include <algorithm>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -920,40 +922,60 @@ __global__ void k_attn_merge(const __grid_constant__ AttnArgs a) {
 }
 
 template <int DH, int G, typename KT>
-static void attn_t(const AttnArgs& a, int nch, cudaStream_t s) {
+static void attn_t(const AttnArgs& a0, int sms, cudaStream_t s) {
   constexpr int TS = AttnRing<DH, KT>::TS, NS = AttnRing<DH, KT>::NS;
   const size_t smem = 2 * (size_t)NS * TS * DH * sizeof(KT) + (size_t)(G * DH + G * TS + 32) * sizeof(float) + 64;
   auto k = k_attn_chunk<DH, G, KT>;
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    set = true;
+  // blocks of this instance resident on one SM, looked up once per device
+  static std::mutex mu;
+  static int resident[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  int per_sm;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident[dev] <= 0) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      int nb = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, 256, smem) != cudaSuccess || nb < 1) nb = 1;
+      cudaGetLastError();
+      resident[dev] = nb;
+    }
+    per_sm = resident[dev];
   }
+  // slots per block: the smallest whole number of 64-slot units (never below
+  // kAttnChunk, the partial buffers' unit) whose blocks all fit one wave of
+  // the resident blocks; a wave more would cost a whole block's time for a few
+  AttnArgs a = a0;
+  long long total = 0;
+  int maxL = 0;
+  for (int m = 0; m < a.Mh; ++m) {
+    total += a.slot[m] + 1;
+    maxL = max(maxL, a.slot[m] + 1);
+  }
+  const long long slots = (long long)per_sm * sms;
+  auto blocks = [&](int chunk) {
+    long long b = 0;
+    for (int m = 0; m < a.Mh; ++m) b += (a.slot[m] + chunk) / chunk;
+    return b * a.nkv;
+  };
+  int chunk = (int)(((total * a.nkv + slots - 1) / slots + 63) / 64 * 64);
+  if (chunk < kAttnChunk) chunk = kAttnChunk;
+  while (chunk < maxL && blocks(chunk) > slots) chunk += 64;
+  a.chunk = chunk;
+  const int nch = (maxL + chunk - 1) / chunk;
   launch_pdl(k, dim3(nch, a.nkv, a.Mh), dim3(256), smem, s, a);
   launch_pdl(k_attn_merge<DH>, dim3(a.nq, a.Mh), dim3(DH), (size_t)a.max_chunks * sizeof(float), s, a);
   count_launch(2);
 }
 
-void launch_attention(const AttnArgs& a0, int sms, cudaStream_t s) {
-  AttnArgs a = a0;
-  int maxL = 0;
-  long long total = 0;
-  for (int m = 0; m < a.Mh; ++m) {
-    maxL = a.slot[m] + 1 > maxL ? a.slot[m] + 1 : maxL;
-    total += a.slot[m] + 1;
-  }
-  // slots per block: the whole job spread over about two blocks per SM, in
-  // whole 64-slot tiles, never below kAttnChunk (the partial buffers' unit)
-  const long long per = (total * a.nkv + 2LL * sms - 1) / (2LL * sms);
-  int chunk = (int)((per + 63) / 64 * 64);
-  if (chunk < kAttnChunk) chunk = kAttnChunk;
-  a.chunk = chunk;
-  const int nch = (maxL + chunk - 1) / chunk;
+void launch_attention(const AttnArgs& a, int sms, cudaStream_t s) {
   const int G = a.nq / a.nkv;
   const bool bf = a.wdt == MTP_DTYPE_BF16;
 #define MTP_ATTN_CASE(DHV, GV)                                                \
   if (a.dh == DHV && G == GV) {                                               \
-    if (bf) attn_t<DHV, GV, uint16_t>(a, nch, s); else attn_t<DHV, GV, float>(a, nch, s); \
+    if (bf) attn_t<DHV, GV, uint16_t>(a, sms, s); else attn_t<DHV, GV, float>(a, sms, s); \
     return;                                                                   \
   }
   MTP_ATTN_CASE(256, 6)
