@@ -734,6 +734,17 @@ def measure_batched(tensors, embed, s, dev, reps: int = 20):
         if i >= 2:
             dt += e[0].elapsed_time(e[1])
             vt += e[2].elapsed_time(e[3])
+    # per-kind times of the draft call from a separate pass with every kind
+    # bracketed by events (the brackets end the programmatic overlap)
+    m.mtp_profile_enable(h, True)
+    m.mtp_profile_read(h)
+    for i in range(5):
+        m.mtp_set_lengths(h, lens)
+        m.mtp_draft(h, depth, [1] * R, tok, hid, params, draft, hist=hist, u=ud, q=q, logits=dl)
+    torch.cuda.synchronize()
+    prof = m.mtp_profile_read(h)
+    m.mtp_profile_enable(h, False)
+    kinds = {k: round(v[0] / max(v[1], 1) * 1e3, 2) for k, v in prof.items() if v[1]}
     h.close()
     dt, vt = dt / reps / 1e3, vt / reps / 1e3
     sampled_rows = sum(1 for r in rows if r["temperature"] > 0)
@@ -744,7 +755,8 @@ def measure_batched(tensors, embed, s, dev, reps: int = 20):
             "draft_tok_per_s": round(R * depth / dt, 1), "draft_step_us": round(1e6 * dt / depth, 1),
             "draft_step_hbm_gbs": round((wbytes + kvbytes) / (dt / depth) / 1e9, 1),
             "verify_us": round(1e6 * vt, 2), "verify_bytes": vbytes,
-            "verify_gbs": round(vbytes / vt / 1e9, 1), "verify_l2": L2Flush.WHAT}
+            "verify_gbs": round(vbytes / vt / 1e9, 1), "verify_l2": L2Flush.WHAT,
+            "kernel_avg_us_bracketed": kinds}
 
 
 class L2Flush:
