@@ -286,7 +286,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = m.mtp_kernel_launches() - launches0
-    clk = clocks.stop()
+    clk_timed = clocks.stop()
+    # a second sampler over the GPU legs that follow (under load throughout),
+    # so that a short timed region still comes with a population of samples
+    clocks_after = Clocks(local_rank)
     prof = m.mtp_profile_read(h)
     m.mtp_profile_enable(h, False)
     ms = t0.elapsed_time(t1)
@@ -347,6 +350,14 @@ def run_ours(args, rank, world, local_rank):
     depth_ctl = None if args.quick else measure_depth_controller(tensors, embed, s, dev, sampled)
     batched = None if args.quick else measure_batched(tensors, embed, s, dev)
     stress = None if args.quick else measure_verify_stress(s, dev)
+    clk_after = clocks_after.stop()
+    clk = dict(clk_timed)
+    clk["timed_region_samples"] = clk_timed.get("samples", 0)
+    if clk_after.get("samples"):
+        clk["after_timed_region"] = clk_after
+        clk["reasons"] = sorted(set(clk_timed.get("reasons", [])) | set(clk_after.get("reasons", [])))
+        if not clk_timed.get("samples"):
+            clk["sm_mhz"], clk["sm_max_mhz"] = clk_after["sm_mhz"], clk_after["sm_max_mhz"]
 
     H, Vocab = s.hidden, s.vocab
     lm_bytes = Vocab * H * 2 + Vocab * 4 + H * 4
@@ -390,7 +401,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4),
                      "traffic": LM_TRAFFIC_BYTES if not args.vocab else None,
                      "traffic_source": "ncu capture at V=32768 scaled by rows to V=152064",
-                     "bytes_per_launch": lm_bytes},
+                     "bytes_per_launch": lm_bytes, "launches_timed": int(lm_n)},
         "gpu_launches": int(launches),
         "sampled_depth_sweep": sampled,
         "sampled_argmax_draft_depth2": sampled_am,

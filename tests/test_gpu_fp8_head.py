@@ -6,7 +6,8 @@ CUDA cores) are compared with the oracle quantising the same head the same
 way. Logits must agree within 1e-2 of the largest magnitude, as for every
 bf16 head, and drafts exactly unless the oracle reports a near-tie. The fp8
 logits must also differ from the bf16 head's, which shows that the copy is in
-use, and switching back must restore the bf16 head."""
+use, and switching back must restore the bf16 head. The same comparison runs
+at the 27B shape the benchmark times (H 5120, vocab 152064, KV 4096)."""
 import numpy as np
 import pytest
 
@@ -56,4 +57,24 @@ def test_switching_back_restores_the_bf16_head():
     out = rig.draft(depth, [1], tok, hid, [dict(temperature=0.0)])
     ref = rig.oracle_draft(0, depth, [17], list(g.to_f32(hid)[0, :1]), oracle.make_params(0.0))
     assert g.max_rel(out["logits"][0, 0], ref["logits"][0]) < TOL
+    rig.close()
+
+
+def test_fp8_head_at_the_27b_shape(model27):
+    # the shape the benchmark times: H 5120, vocab 152064, KV 4096, depth 2;
+    # the seeded case has clear argmaxes under the quantised head (top-2 gaps
+    # about 0.30 on both steps), so both drafts must match exactly
+    S27 = synth.QWEN27B
+    rig = g.Rig(S27, seed=2, rows=1, capacity=4096 + 256, prefill=[4096], max_depth=2, model=model27)
+    q, sc = oracle.quantize_rows_e4m3(rig.model.embed)
+    rig.orc = oracle.Head(S27, rig.model.tensors, rig.model.embed, lm_fp8=(q, sc))
+    m.mtp_set_draft_head(rig.h, m.MTP_HEAD_FP8)
+    toks = [1234, 77, 150000]
+    tok, hid = rig.pairs([toks])
+    out = rig.draft(2, [3], tok, hid, [dict(temperature=0.0)])
+    ref = rig.oracle_draft(0, 2, toks, g.to_f32(hid)[0], oracle.make_params(0.0))
+    assert g.max_rel(out["logits"][0, 0], ref["logits"][0]) < TOL
+    assert ref["margins"][0] > 1e-2 and out["draft"][0, 0] == ref["drafts"][0]
+    assert g.max_rel(out["logits"][0, 1], ref["logits"][1]) < TOL
+    assert ref["margins"][1] > 1e-2 and out["draft"][0, 1] == ref["drafts"][1]
     rig.close()
