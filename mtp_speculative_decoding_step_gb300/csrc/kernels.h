@@ -246,9 +246,57 @@ struct SampleArgs {
   int32_t* status;
   int cand;                  // local candidates per CTA (set by launch_sample)
   int merge;                 // merged candidate buffer (power of two)
+  void* flat_ws;             // draft: scratch of the flat transform (flat_workspace_bytes), or null
+  size_t flat_ws_bytes;
   RowParams p[kMaxRows];
 };
 void launch_sample(const SampleArgs& a, cudaStream_t s);
+
+// Flat transform of rows with a wide support (no top-k below V: top-p, min-p
+// or plain temperature over the whole vocabulary) as a chain of short kernels
+// that spread every (row, position) over many CTAs: statistics (penalised
+// argmax and minimum), a weighted value histogram, the gather of the top-p
+// crossing bin (its last CTA resolves the descriptor), then the draw's sums
+// (their last CTA draws: q and the draft token of a draft step; the accept
+// chain and the correction or bonus token of a verify).
+struct FlatArgs {
+  int mode;                  // 0 draft step, 1 verify
+  int rows, V, W, depth, pos, tasks, P;
+  const float* logits;       // mode 0: row r at logits + r * ld; mode 1: [rows][depth+1][V]
+  long long ld;
+  const int32_t* hist;       // [rows][W]
+  const int32_t* drafts;     // [rows][depth]
+  const float* u;            // mode 0: [rows][depth]; mode 1: [rows][depth+1]
+  float* q;                  // mode 0: out [rows][depth][V]; mode 1: the drafts' q (null if unused)
+  int32_t* draft_out;        // mode 0
+  int32_t* n_acc;            // mode 1 outputs
+  int32_t* out_tok;
+  int32_t* stats;
+  int32_t* h_rec;
+  int32_t* status;
+  // scratch (flat_workspace_bytes), descriptors first
+  TDesc* desc;               // [tasks]
+  unsigned long long* amax;  // [tasks][P]
+  float* zmin;               // [tasks][P]
+  unsigned long long* hist_w;  // [tasks][kFlatHistBins]
+  unsigned long long* sminp;   // [tasks]
+  int32_t* ccnt;             // [tasks]
+  uint32_t* ckey;            // [tasks][kFlatCandCap]
+  int32_t* cid;
+  unsigned long long* wsum;  // [rows][P][2]
+  int32_t* nstop;            // [rows]
+  int32_t* gcnt;             // [tasks] gathering CTAs done (the last resolves)
+  int32_t* scnt;             // [rows] summing CTAs done (the last draws)
+  RowParams p[kMaxRows];
+};
+constexpr int kFlatHistBins = 2048;
+constexpr int kFlatCandCap = 1024;
+constexpr int kFlatMaxParts = 64;
+size_t flat_workspace_bytes(int rows, int tasks);
+bool flat_fits(const RowParams* p, int rows, int V, const float* logits, long long ld);
+// Lays the scratch out in ws (desc at offset 0), picks the parts per task and
+// launches the chain; false (nothing launched) if ws_bytes is too small.
+bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s);
 
 struct VerifyArgs {
   int rows, V, W, depth;

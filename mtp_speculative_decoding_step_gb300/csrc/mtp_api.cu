@@ -117,6 +117,8 @@ struct mtp_handle {
   float* tcpart = nullptr;                // split-K partial tiles of the tensor-core flush
   uint16_t* x2 = nullptr;                 // hi/lo bf16 activations of the tensor-core GEMV
   float* tvpart = nullptr;                // its split-K partials
+  uint8_t* flat_ws = nullptr;             // scratch of the draft-side flat transform
+  size_t flat_ws_bytes = 0;
   bool tc_gemv = false;                   // batched GEMVs on tcgen05 (bf16 weights)
   uint8_t* lmq = nullptr;                 // fp8 e4m3 copy of the draft head (mtp_set_draft_head)
   float* lmq_scale = nullptr;             // its per-row scales
@@ -538,6 +540,23 @@ bool stream_verify_fits(int rows, int depth, int vocab, const mtp_sampling* hp) 
   return true;
 }
 
+// Rows without a top-k below V (and greedy rows beside them): the flat
+// transform chain over many CTAs per task. False, launching nothing, where it
+// does not apply.
+bool flat_rows(int rows, int depth, int vocab, int hist_w, const float* d_logits, const int32_t* d_draft,
+               const float* d_q, const mtp_sampling* hp, const int32_t* d_hist, const float* d_u, int32_t* d_n_acc,
+               int32_t* d_out_tok, int32_t* d_stats, int32_t* h_rec, int32_t* d_status, void* ws, size_t ws_bytes,
+               cudaStream_t s) {
+  FlatArgs f;
+  std::memset(&f, 0, sizeof(f));
+  for (int r = 0; r < rows; ++r) f.p[r] = row_params(hp[r]);
+  if (!flat_fits(f.p, rows, vocab, d_logits, vocab)) return false;
+  f.mode = 1; f.rows = rows; f.V = vocab; f.W = hist_w; f.depth = depth; f.tasks = rows * (depth + 1);
+  f.logits = d_logits; f.ld = vocab; f.hist = d_hist; f.drafts = d_draft; f.u = d_u; f.q = const_cast<float*>(d_q);
+  f.n_acc = d_n_acc; f.out_tok = d_out_tok; f.stats = d_stats; f.h_rec = h_rec; f.status = d_status;
+  return launch_flat(f, ws, ws_bytes, s);
+}
+
 // Every sampled row cuts to a top-k of at most kStreamTopK and the rows fit
 // the one-cluster-per-task top-k transform.
 bool topk_rows(int rows, int vocab, const float* logits, const mtp_sampling* hp) {
@@ -789,6 +808,8 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
   if (st == MTP_OK) st = alloc(h, &h->done, 1);
   if (st == MTP_OK) st = alloc(h, &h->status, 1);
+  h->flat_ws_bytes = flat_workspace_bytes(R, R);
+  if (st == MTP_OK) st = alloc(h, &h->flat_ws, h->flat_ws_bytes);
   if (st == MTP_OK) st = alloc(h, &h->inv_freq, (size_t)dh / 2);
   if (st == MTP_OK) {
     std::vector<double> f(dh / 2);
@@ -940,6 +961,7 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
   sa.mode = 0; sa.rows = rows; sa.V = V; sa.W = hist_w; sa.depth = depth;
   sa.hist = d_hist; sa.drafts = d_draft; sa.u = d_u; sa.q = d_q; sa.draft_out = d_draft;
   sa.status = h->status;
+  sa.flat_ws = h->flat_ws; sa.flat_ws_bytes = h->flat_ws_bytes;
   for (int r = 0; r < rows; ++r) sa.p[r] = row_params(draft_params(h_params[r]));
 
   for (int k = 1; k <= depth; ++k) {
@@ -999,7 +1021,8 @@ size_t spec_verify_workspace_bytes(int32_t rows, int32_t depth, int32_t vocab) {
   // greedy stream over many rows) one 64-bit key per range and segment
   const size_t lists = align256(sizeof(TDesc) * tasks) + align256(sizeof(int32_t) * tasks) +
                        2 * align256(sizeof(int32_t) * tasks * kStreamTopK);
-  return std::max(lists, align256(sizeof(unsigned long long) * (tasks + kFlatMaxCTAs)));
+  return std::max({lists, align256(sizeof(unsigned long long) * (tasks + kFlatMaxCTAs)),
+                   flat_workspace_bytes(rows, (int)tasks)});
 }
 
 }  // extern "C"
@@ -1081,7 +1104,11 @@ mtp_status spec_verify_impl(mtp_stream stream, int32_t rows, int32_t depth, int3
       launch_topk(t, s);
       launch_verify_finish(va, s);
     }
-  } else {
+  } else if (!(allow_stream && flat_rows(rows, depth, vocab, hist_w, d_logits, d_draft, d_q, h_params, d_hist, d_u,
+                                         d_n_acc, d_out_tok, d_stats, h_rec, d_status, d_workspace, workspace_bytes,
+                                         s))) {
+    // every other mix: one 8-CTA cluster per task for the descriptors, then
+    // one per row for the accept chain and the draw
     TDesc* desc = static_cast<TDesc*>(d_workspace);
     SampleArgs sa;
     std::memset(&sa, 0, sizeof(sa));

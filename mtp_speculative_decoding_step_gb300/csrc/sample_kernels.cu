@@ -20,6 +20,8 @@
 // every result is independent of thread scheduling.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include <cstring>
 #include <mutex>
 
@@ -2786,6 +2788,865 @@ void launch_topk(const TopkArgs& a, cudaStream_t s) {
   count_launch();
 }
 
+// ------------------------------------------------------------ flat transform
+// Rows with a wide support (no top-k below V) spread every (row, position)
+// over P parts of its vocabulary, one CTA per part, through a chain of four
+// short kernels (each waits for the previous one at griddepcontrol.wait):
+//   k_fl_stats    argmax of the penalised logits and their minimum, per part;
+//                 zeroes the task's histogram and counters
+//   k_fl_hist     fixed-point weights exp(z' - m) (z' = z / T + 0) added into
+//                 kFlatBins equal value slices of [m - span, m] (the cluster
+//                 path's binning), and the min-p mass
+//   k_fl_gather   the bin in which the running mass reaches ceil(top_p * SE),
+//                 and its elements, into a per-task list; the task's last CTA
+//                 then takes the exact crossing element of that list in
+//                 (key, id) order (a weighted selection), the kept mass S and
+//                 the descriptor (if the bin holds more than the list: an
+//                 exact block-level radix selection over the row)
+//   k_fl_sums     per part of the drawn row: the accept chain (verify), the
+//                 part's sums of the draw weights (and, for a draft step, q);
+//                 the row's last CTA finds the part and then the element where
+//                 the running weight reaches the draw's target, and writes the
+//                 outputs.
+// The keys, weights, cut rules and draws are those of the cluster path.
+__device__ __forceinline__ unsigned long long fl_amax_key(float v, int id) {
+  uint32_t u = __float_as_uint(v + 0.0f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ float fl_key_value(unsigned long long k) {
+  uint32_t u = (uint32_t)(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+
+struct FlTask {
+  int r, i;
+  const float* lg;
+};
+__device__ __forceinline__ FlTask fl_task(const FlatArgs& a, int t) {
+  FlTask x;
+  if (a.mode == 0) {
+    x.r = t;
+    x.i = a.pos;
+    x.lg = a.logits + (size_t)t * a.ld;
+  } else {
+    x.r = t / (a.depth + 1);
+    x.i = t - x.r * (a.depth + 1);
+    x.lg = a.logits + (size_t)t * a.V;
+  }
+  return x;
+}
+__host__ __device__ __forceinline__ int fl_per(int V, int P) { return ((V + P - 1) / P + 3) & ~3; }
+
+// The task's transform scale: maximum transformed logit m, the argmax of the
+// penalised logits, and the bin scale of [m - span, m].
+struct FlScale {
+  float mx, scale;
+  int amax;
+};
+__device__ FlScale fl_scale(const FlatArgs& a, int t, const RowParams& rp) {
+  // every warp combines the P (<= 64) part slots, two per lane
+  const int lane = threadIdx.x & 31;
+  unsigned long long best = 0ull;
+  float zm = INFINITY;
+  for (int q = lane; q < a.P; q += 32) {
+    best = max(best, __ldcg(&a.amax[(size_t)t * a.P + q]));
+    zm = fminf(zm, __ldcg(&a.zmin[(size_t)t * a.P + q]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    zm = fminf(zm, __shfl_xor_sync(0xFFFFFFFFu, zm, o));
+  }
+  FlScale s;
+  s.amax = best ? (int)(0xFFFFFFFFu - (uint32_t)best) : 0;
+  const float zmax = best ? fl_key_value(best) : -INFINITY;
+  const float T = rp.greedy ? 1.f : rp.temperature;
+  s.mx = zmax / T + 0.0f;
+  const float zlo = zm / T + 0.0f;
+  float span = s.mx - zlo;
+  if (!(span > 0.f)) span = 0.f;
+  if (span > kFlatSpan) span = kFlatSpan;
+  s.scale = span > 0.f ? ((float)kFlatBins - 0.01f) / span : 0.f;
+  return s;
+}
+__device__ __forceinline__ int fl_bin(const FlScale& s, float z) {
+  const float t = (s.mx - z) * s.scale;
+  return t < (float)kFlatBins ? (int)t : kFlatBins;  // beyond the span (and NaN): no bin
+}
+
+// Every thread of the block: total mass SE of the task's histogram, the bin
+// b in which the running mass reaches target = ceil(top_p SE) and the mass
+// still needed there (b = -1 when SE is 0), into shared memory. Four bins per
+// thread, one block scan.
+__device__ void fl_cross(SampleSmem* sm, const unsigned long long* h, float top_p, unsigned long long* SE_out,
+                         int* b_out, unsigned long long* need_out, unsigned long long* target_out) {
+  constexpr int PER = kFlatBins / kST;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned long long v[PER];
+  unsigned long long s = 0;
+#pragma unroll
+  for (int b = 0; b < PER; ++b) {
+    v[b] = __ldcg(&h[threadIdx.x * PER + b]);
+    s += v[b];
+  }
+  unsigned long long incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) sm->wsum[w] = incl;
+  if (threadIdx.x == 0) *b_out = -1;
+  __syncthreads();
+  unsigned long long before = 0, SE = 0;
+  for (int q = 0; q < kST / 32; ++q) {
+    if (q < w) before += sm->wsum[q];
+    SE += sm->wsum[q];
+  }
+  const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)SE);
+  unsigned long long cum = before + incl - s;
+  if (SE > 0 && cum < target && target <= cum + s) {
+#pragma unroll
+    for (int b = 0; b < PER; ++b) {
+      if (cum < target && target <= cum + v[b]) {
+        *b_out = threadIdx.x * PER + b;
+        *need_out = target - cum;
+        break;
+      }
+      cum += v[b];
+    }
+  }
+  if (threadIdx.x == 0) {
+    *SE_out = SE;
+    *target_out = target;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ size_t fl_bits_off() { return (sizeof(SampleSmem) + 15) & ~size_t(15); }
+
+__global__ void __launch_bounds__(kST) k_fl_stats(const __grid_constant__ FlatArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  __shared__ float s_bv[kST / 32];
+  __shared__ int s_bi[kST / 32];
+  __shared__ float s_mn[kST / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y, p = blockIdx.x;
+  const FlTask k = fl_task(a, t);
+  const RowParams rp = a.p[k.r];
+  // this task's share of the scratch the next kernels accumulate into
+  for (int b = p * kST + threadIdx.x; b < kFlatBins; b += a.P * kST) a.hist_w[(size_t)t * kFlatBins + b] = 0ull;
+  if (p == 0 && threadIdx.x == 0) {
+    a.sminp[t] = 0ull;
+    a.ccnt[t] = 0;
+    a.gcnt[t] = 0;
+    if (k.i == 0 || a.mode == 0) a.scnt[k.r] = 0;
+  }
+  const int per = fl_per(a.V, a.P);
+  const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
+  load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
+  const bool pen = rp.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, v0, n);
+  // four independent chains per thread (one per vector lane): ids ascend
+  // within a chain, so strict > keeps the lowest id on ties
+  float bz[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  int bzi[4] = {0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF, 0x7FFFFFFF};
+  float mn = INFINITY, nf = 0.f;
+  const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
+  const int n4 = n / 4;
+  for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+    float4 xb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * kST + threadIdx.x;
+      if (j4 < n4) xb[u] = __ldg(l4 + j4);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * kST + threadIdx.x;
+      if (j4 < n4) {
+        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+        const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          nf = fmaf(xs[e], 0.f, nf);
+          const float z = ((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e];
+          if (z > bz[e]) { bz[e] = z; bzi[e] = v0 + 4 * j4 + e; }
+          mn = fminf(mn, z);
+        }
+      }
+    }
+  }
+  float bv = bz[0];
+  int bi = bzi[0];
+#pragma unroll
+  for (int e = 1; e < 4; ++e)
+    if (better(bz[e], bzi[e], bv, bi)) { bv = bz[e]; bi = bzi[e]; }
+  if (__syncthreads_or(isnan(nf)) && threadIdx.x == 0) flag_status(a.status, MTP_ERR_NONFINITE);
+  block_argmax(bv, bi, s_bv, s_bi);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+  if ((threadIdx.x & 31) == 0) s_mn[threadIdx.x >> 5] = mn;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m2 = INFINITY;
+    for (int w = 0; w < kST / 32; ++w) m2 = fminf(m2, s_mn[w]);
+    a.amax[(size_t)t * a.P + p] = (bi >= 0 && bi < a.V) ? fl_amax_key(bv, bi) : 0ull;
+    a.zmin[(size_t)t * a.P + p] = m2;
+  }
+}
+
+__global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  const int per = fl_per(a.V, a.P);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  unsigned long long* hh =
+      reinterpret_cast<unsigned long long*>(dyn + ((fl_bits_off() + 4 * (size_t)((per + 31) / 32 + 1) + 15) & ~size_t(15)));
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y, p = blockIdx.x;
+  const FlTask k = fl_task(a, t);
+  const RowParams rp = a.p[k.r];
+  if (rp.greedy) return;
+  const FlScale sc = fl_scale(a, t, rp);
+  const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
+  for (int b = threadIdx.x; b < kFlatBins; b += kST) hh[b] = 0ull;
+  load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
+  const bool pen = rp.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, v0, n);
+  __syncthreads();
+  const bool minp = rp.min_p > 0.f;
+  unsigned long long smp = 0ull;
+  const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
+  const int n4 = n / 4;
+  for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+    float4 xb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * kST + threadIdx.x;
+      if (j4 < n4) xb[u] = __ldg(l4 + j4);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * kST + threadIdx.x;
+      if (j4 < n4) {
+        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+        const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float z = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
+          const int b = fl_bin(sc, z);
+          if (b < kFlatBins) {
+            const float ev = expf(z - sc.mx);
+            const unsigned long long w = to_fix(ev);
+            if (w) {
+              atomicAdd(&hh[b], w);
+              if (minp && ev >= rp.min_p) smp += w;
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kFlatBins; b += kST)
+    if (hh[b]) atomicAdd(&a.hist_w[(size_t)t * kFlatBins + b], hh[b]);
+  if (minp) {
+    const unsigned long long tot = block_sum_u64(smp, sm->wsum);
+    if (threadIdx.x == 0 && tot) atomicAdd(&a.sminp[t], tot);
+  }
+}
+
+__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn);
+__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn);
+
+__global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  __shared__ unsigned long long s_SE, s_need, s_target;
+  __shared__ int s_b;
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y, p = blockIdx.x;
+  const FlTask k = fl_task(a, t);
+  const RowParams rp = a.p[k.r];
+  if (rp.greedy || !(rp.top_p > 0.f && rp.top_p < 1.f)) {
+    // nothing to gather: one CTA writes the descriptor
+    if (p == 0) fl_resolve_task(a, t, dyn);
+    return;
+  }
+  const FlScale sc = fl_scale(a, t, rp);
+  fl_cross(sm, a.hist_w + (size_t)t * kFlatBins, rp.top_p, &s_SE, &s_b, &s_need, &s_target);
+  const int bstar = s_b;
+  const int per = fl_per(a.V, a.P);
+  const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
+  load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
+  const bool pen = rp.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, v0, n);
+  for (int j = threadIdx.x; j < n; j += kST) {
+    float z = __ldg(k.lg + v0 + j);
+    if (pen && bit(bits, j)) z = penalize(z, rp.rep_penalty);
+    z = z / rp.temperature + 0.0f;
+    if (bstar >= 0 && fl_bin(sc, z) == bstar) {
+      const int pos = atomicAdd(&a.ccnt[t], 1);
+      if (pos < kFlatCandCap) {
+        a.ckey[(size_t)t * kFlatCandCap + pos] = desc_key(z);
+        a.cid[(size_t)t * kFlatCandCap + pos] = v0 + j;
+      }
+    }
+  }
+  // the last of the task's CTAs to finish resolves its descriptor
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.gcnt[t], 1) == a.P - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  fl_resolve_task(a, t, dyn);
+}
+
+// Exact crossing inside bin bstar of one row by one CTA, when the gathered
+// list overflowed (heavily tied logits): radix selection over the keys of the
+// bin's elements with their fixed-point weights (digit passes over the row),
+// then the right tie in id order. Returns the (key, id) bound, and in *in_bin
+// the weight of the bin's elements up to and including it.
+template <class Z>
+__device__ void fl_exact_cut(SampleSmem* sm, int V, Z zof, const FlScale& sc, int bstar, unsigned long long need,
+                             uint32_t& Kout, int& cutout, unsigned long long* in_bin) {
+  auto wk = [&](uint32_t key) { return to_fix(expf(key_to_z(key) - sc.mx)); };
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int j = threadIdx.x; j < V; j += kST) {
+    const float z = zof(j);
+    if (fl_bin(sc, z) == bstar) {
+      const uint32_t key = desc_key(z);
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm->wsum[threadIdx.x >> 5] = ((unsigned long long)kmin << 32) | kmax;
+  __syncthreads();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int w = 0; w < kST / 32; ++w) {
+    kmin = min(kmin, (uint32_t)(sm->wsum[w] >> 32));
+    kmax = max(kmax, (uint32_t)sm->wsum[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int hi = diff ? 31 - __clz(diff) : -1;
+  uint32_t mask = hi >= 0 ? ~((hi == 31) ? 0xFFFFFFFFu : ((2u << hi) - 1u)) : 0xFFFFFFFFu;
+  uint32_t prefix = kmin & mask;
+  unsigned long long target = need;
+  unsigned long long* h = sm->hist[0];
+  while (hi >= 0) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += kST) h[b] = 0ull;
+    __syncthreads();
+    for (int j = threadIdx.x; j < V; j += kST) {
+      const float z = zof(j);
+      if (fl_bin(sc, z) != bstar) continue;
+      const uint32_t key = desc_key(z);
+      if ((key & mask) == prefix) atomicAdd(&h[(key >> lo) & dmask], wk(key));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      unsigned long long s8 = 0;
+      for (int b = 0; b < 8; ++b) s8 += h[lane * 8 + b];
+      unsigned long long incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned long long cum = incl - s8;
+      const bool mine = cum < target && target <= incl;
+      if (mine) {
+        for (int b = 0; b < 8; ++b) {
+          const unsigned long long t = h[lane * 8 + b];
+          if (cum < target && target <= cum + t) {
+            sm->sel_bin = lane * 8 + b;
+            sm->sel_rem = target - cum;
+            break;
+          }
+          cum += t;
+        }
+      }
+      if (!__ballot_sync(0xFFFFFFFFu, mine) && lane == 0) {  // target above the total: the last digit
+        sm->sel_bin = (int)dmask;
+        sm->sel_rem = target;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm->sel_bin << lo;
+    mask |= dmask << lo;
+    target = sm->sel_rem;
+    hi = lo - 1;
+  }
+  const uint32_t K = prefix;
+  const unsigned long long ew = wk(K);
+  const unsigned long long want = ew > 0 ? (target + ew - 1) / ew : 1ull;  // the want-th tie in id order
+  // ties at K in id order: per-thread contiguous ranges, block exclusive scan of their counts
+  const int chunk = (V + kST - 1) / kST;
+  const int a0 = min((int)threadIdx.x * chunk, V), a1 = min(a0 + chunk, V);
+  unsigned long long c = 0;
+  for (int j = a0; j < a1; ++j) {
+    const float z = zof(j);
+    if (fl_bin(sc, z) == bstar && desc_key(z) == K) ++c;
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned long long incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (threadIdx.x == 0) sm->found = 0x7FFFFFFF;
+  __syncthreads();
+  if (lane == 31) sm->wsum[w] = incl;
+  __syncthreads();
+  unsigned long long before = 0;
+  for (int q = 0; q < w; ++q) before += sm->wsum[q];
+  unsigned long long cum = before + incl - c;
+  if (cum < want && want <= cum + c) {
+    for (int j = a0; j < a1; ++j) {
+      const float z = zof(j);
+      if (fl_bin(sc, z) == bstar && desc_key(z) == K && ++cum == want) {
+        sm->found = j;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const int cut = sm->found;  // 0x7FFFFFFF: every tie (the target lies past them)
+  // the bin's weight up to and including the bound
+  unsigned long long loc = 0;
+  for (int j = threadIdx.x; j < V; j += kST) {
+    const float z = zof(j);
+    if (fl_bin(sc, z) == bstar) {
+      const uint32_t key = desc_key(z);
+      if (in_prefix(key, j, K, cut)) loc += wk(key);
+    }
+  }
+  *in_bin = block_sum_u64(loc, sm->wsum);
+  Kout = K;
+  cutout = cut;
+}
+
+// One CTA: the descriptor of task t (shared memory laid out as SampleSmem,
+// then the candidate list, its tie buffer and a bitmap of the whole row).
+__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn) {
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  uint32_t* mk = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  int* mi = reinterpret_cast<int*>(mk + kFlatCandCap);
+  int* tie = mi + kFlatCandCap;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(tie + kFlatCandCap);
+  __shared__ unsigned long long s_SE, s_need, s_target;
+  __shared__ int s_b;
+  const FlTask k = fl_task(a, t);
+  const RowParams rp = a.p[k.r];
+  const FlScale sc = fl_scale(a, t, rp);
+  TDesc d;
+  d.argmax = sc.amax;
+  d.k_key = 0xFFFFFFFFu;
+  d.k_cut = 0x7FFFFFFF;
+  d.p_key = 0xFFFFFFFFu;
+  d.p_cut = 0x7FFFFFFF;
+  d.m = 0.f;
+  d.S = 1.f;
+  d.kept = rp.greedy ? 1 : -1;
+  if (rp.greedy) {
+    if (threadIdx.x == 0) a.desc[t] = d;
+    return;
+  }
+  const bool topp = rp.top_p > 0.f && rp.top_p < 1.f;
+  fl_cross(sm, a.hist_w + (size_t)t * kFlatBins, topp ? rp.top_p : 1.f, &s_SE, &s_b, &s_need, &s_target);
+  unsigned long long S = s_SE;
+  const int bstar = s_b;
+  if (topp && bstar >= 0) {
+    auto wk = [&](uint32_t key) { return to_fix(expf(key_to_z(key) - sc.mx)); };
+    const int cnt = __ldcg(&a.ccnt[t]);
+    uint32_t K = 0xFFFFFFFFu;
+    int cut = 0x7FFFFFFF;
+    unsigned long long in_bin = 0;
+    bool ok = cnt <= kFlatCandCap;
+    if (ok) {
+      for (int q = threadIdx.x; q < cnt; q += kST) {
+        mk[q] = __ldcg(&a.ckey[(size_t)t * kFlatCandCap + q]);
+        mi[q] = __ldcg(&a.cid[(size_t)t * kFlatCandCap + q]);
+      }
+      __syncthreads();
+      ok = cnt > 0 && list_select(sm, mk, mi, cnt, s_need, wk, tie, kFlatCandCap, K, cut);
+      if (ok) {
+        unsigned long long loc = 0;
+        for (int q = threadIdx.x; q < cnt; q += kST)
+          if (in_prefix(mk[q], mi[q], K, cut)) loc += wk(mk[q]);
+        in_bin = block_sum_u64(loc, sm->wsum);
+      }
+    }
+    if (!ok) {
+      load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
+      const bool pen = rp.rep_penalty != 1.f;
+      if (pen) build_bitmap(sm, bits, 0, a.V);
+      auto zof = [&](int j) {
+        float z = __ldg(k.lg + j);
+        if (pen && bit(bits, j)) z = penalize(z, rp.rep_penalty);
+        return z / rp.temperature + 0.0f;
+      };
+      fl_exact_cut(sm, a.V, zof, sc, bstar, s_need, K, cut, &in_bin);
+    }
+    d.p_key = K;
+    d.p_cut = cut;
+    // the kept mass: every bin before the crossing one, then that bin's
+    // elements up to the bound; with min-p the shorter of the two prefixes
+    S = (s_target - s_need) + in_bin;
+    if (rp.min_p > 0.f && !(expf(key_to_z(K) - sc.mx) >= rp.min_p)) S = __ldcg(&a.sminp[t]);
+  } else if (rp.min_p > 0.f) {
+    S = __ldcg(&a.sminp[t]);
+  }
+  d.m = sc.mx;
+  d.S = (float)((double)S / kFix);
+  if (threadIdx.x == 0) a.desc[t] = d;
+}
+
+// Warp 0 (every lane): the row's accept chain over its d drafts, from the
+// descriptors, the raw target logits at the drafts and q. Lane i evaluates
+// draft x_{i+1} against target row i under row i's penalty window; hw holds
+// the row's history (W) then its drafts (d), staged by the block.
+__device__ int fl_chain(const FlatArgs& a, int r, const RowParams& rp, const int* hw) {
+  const int lane = threadIdx.x & 31, d = a.depth;
+  bool acc = false;
+  if (lane < d) {
+    const int x = hw[a.W + lane];
+    if (x >= 0 && x < a.V) {  // an out-of-range draft is rejected, never dereferenced
+      const int t = r * (d + 1) + lane;
+      const TDesc dd = a.desc[t];
+      const float raw = __ldg(a.logits + (size_t)t * a.V + x);
+      const float qv = rp.argmax_draft ? 1.f : __ldg(a.q + ((size_t)r * d + lane) * a.V + x);
+      bool px = false;
+      const int drop = lane < a.W ? lane : a.W;
+      for (int q = drop; q < a.W; ++q) px |= hw[q] == x;
+      for (int q = lane > a.W ? lane - a.W : 0; q < lane; ++q) px |= hw[a.W + q] == x;
+      const float pv = eval_p(dd, rp, raw, px, x);
+      acc = qv > 0.f && a.u[(size_t)r * (d + 1) + lane] < pv / qv;
+    }
+  }
+  const unsigned rej = ~__ballot_sync(0xFFFFFFFFu, acc) & (d >= 32 ? 0xFFFFFFFFu : ((1u << d) - 1u));
+  return rej ? __ffs(rej) - 1 : d;
+}
+
+// The draw's row: its task, descriptor, weights of element v.
+struct FlDraw {
+  int n, tn;
+  bool residual;
+  const float* lg;
+  const float* qn;
+  int xr;
+  TDesc dn;
+};
+__device__ FlDraw fl_draw_row(const FlatArgs& a, int r, int n, const RowParams& rp) {
+  FlDraw w;
+  w.n = n;
+  w.tn = a.mode == 0 ? r : r * (a.depth + 1) + n;
+  w.lg = a.mode == 0 ? a.logits + (size_t)r * a.ld : a.logits + (size_t)w.tn * a.V;
+  w.residual = a.mode == 1 && n < a.depth;
+  w.qn = (w.residual && !rp.argmax_draft) ? a.q + ((size_t)r * a.depth + n) * a.V : nullptr;
+  w.xr = (w.residual && rp.argmax_draft) ? a.drafts[(size_t)r * a.depth + n] : -1;
+  w.dn = a.desc[w.tn];
+  return w;
+}
+
+__global__ void __launch_bounds__(kST) k_fl_sums(const __grid_constant__ FlatArgs a) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  __shared__ int s_n, s_last;
+  __shared__ int s_hw[128 + 16];
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.y, p = blockIdx.x;
+  const RowParams rp = a.p[r];
+  if (rp.greedy) {
+    if (p == 0) fl_pick_row(a, r, dyn);
+    return;
+  }
+  if (a.mode == 1) {
+    for (int q = threadIdx.x; q < a.W + a.depth; q += kST)
+      s_hw[q] = q < a.W ? a.hist[(size_t)r * a.W + q] : a.drafts[(size_t)r * a.depth + q - a.W];
+    __syncthreads();
+  }
+  if (threadIdx.x < 32) {
+    const int n = a.mode == 0 ? a.pos : fl_chain(a, r, rp, s_hw);
+    if (threadIdx.x == 0) s_n = n;
+  }
+  __syncthreads();
+  const FlDraw w = fl_draw_row(a, r, s_n, rp);
+  const int per = fl_per(a.V, a.P);
+  const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
+  load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, w.n);
+  const bool pen = rp.rep_penalty != 1.f;
+  if (pen) build_bitmap(sm, bits, v0, n);
+  float* qout = a.mode == 0 ? a.q + ((size_t)r * a.depth + a.pos) * a.V : nullptr;
+  unsigned long long wp = 0, wr = 0;
+  for (int j = threadIdx.x; j < n; j += kST) {
+    const int v = v0 + j;
+    const float pv = eval_p(w.dn, rp, __ldg(w.lg + v), pen && bit(bits, j), v);
+    if (qout) qout[v] = pv;
+    wp += to_fix(pv);
+    if (w.residual) {
+      const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : __ldg(w.qn + v);
+      const float rv = pv - qv;
+      wr += to_fix(rv > 0.f ? rv : 0.f);
+    }
+  }
+  wp = block_sum_u64(wp, sm->wsum);
+  wr = block_sum_u64(wr, sm->wsum);
+  if (threadIdx.x == 0) {
+    a.wsum[((size_t)r * a.P + p) * 2 + 0] = wr;
+    a.wsum[((size_t)r * a.P + p) * 2 + 1] = wp;
+    if (p == 0) a.nstop[r] = w.n;
+  }
+  // the last of the row's CTAs to finish draws
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.scnt[r], 1) == a.P - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  fl_pick_row(a, r, dyn);
+}
+
+// One CTA: the row's draw and outputs (greedy rows: the argmax chain).
+__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn) {
+  SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
+  __shared__ int s_part, s_y;
+  __shared__ unsigned long long s_need;
+  const int d = a.depth;
+  const RowParams rp = a.p[r];
+  const int32_t* dr = a.drafts + (size_t)r * d;
+  int nacc, y;
+  if (rp.greedy) {
+    // point masses: accept while the draft is the argmax of the row before it
+    if (a.mode == 0) {
+      nacc = 0;
+      y = a.desc[r].argmax;
+    } else {
+      int am = 0, x = -1;
+      const int lane = threadIdx.x & 31;
+      if (threadIdx.x < 32) {
+        am = lane <= d ? a.desc[r * (d + 1) + lane].argmax : 0;
+        x = lane < d ? dr[lane] : -1;
+      }
+      const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < d && !(x >= 0 && x < a.V && x == am));
+      nacc = miss ? __ffs(miss) - 1 : d;
+      y = __shfl_sync(0xFFFFFFFFu, am, nacc);
+    }
+  } else {
+    nacc = a.mode == 0 ? 0 : __ldcg(&a.nstop[r]);
+    const FlDraw w = fl_draw_row(a, r, a.mode == 0 ? a.pos : nacc, rp);
+    // every warp: the row's two totals over its parts (lane l holds parts 2l, 2l+1)
+    const int lane = threadIdx.x & 31;
+    unsigned long long pr[2] = {0ull, 0ull}, pp[2] = {0ull, 0ull};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int p = 2 * lane + e;
+      if (p < a.P) {
+        pr[e] = __ldcg(&a.wsum[((size_t)r * a.P + p) * 2 + 0]);
+        pp[e] = __ldcg(&a.wsum[((size_t)r * a.P + p) * 2 + 1]);
+      }
+    }
+    unsigned long long tr = pr[0] + pr[1], tp = pp[0] + pp[1];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tr += __shfl_xor_sync(0xFFFFFFFFu, tr, o);
+      tp += __shfl_xor_sync(0xFFFFFFFFu, tp, o);
+    }
+    const bool use_r = w.residual && tr > 0;
+    const unsigned long long tot = use_r ? tr : tp;
+    y = -1;
+    if (tot > 0) {
+      const float uu = a.mode == 0 ? a.u[(size_t)r * d + a.pos] : a.u[(size_t)r * (d + 1) + d];
+      const unsigned long long target = (unsigned long long)floor((double)uu * (double)tot) + 1ull;
+      if (threadIdx.x < 32) {
+        // the part where the running weight reaches the target: lane scan
+        const unsigned long long* pw = use_r ? pr : pp;
+        const unsigned long long mine = pw[0] + pw[1];
+        unsigned long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const unsigned long long excl = incl - mine;
+        const bool here = excl < target && target <= incl;
+        const unsigned who = __ballot_sync(0xFFFFFFFFu, here);
+        if (here && lane == __ffs(who) - 1) {
+          const bool first = target <= excl + pw[0] && 2 * lane < a.P;
+          s_part = first ? 2 * lane : 2 * lane + 1;
+          s_need = first ? target - excl : target - excl - pw[0];
+        }
+        if (!who && lane == 0) {  // rounding left the target past the total: the last part
+          s_part = a.P - 1;
+          s_need = 1ull;
+        }
+        if (lane == 0) s_y = -1;
+      }
+      __syncthreads();
+      const int per = fl_per(a.V, a.P);
+      const int v0 = min(s_part * per, a.V), n = min(per, a.V - v0);
+      load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, w.n);
+      const bool pen = rp.rep_penalty != 1.f;
+      if (pen) build_bitmap(sm, bits, v0, n);
+      auto weight = [&](int j) {
+        const int v = v0 + j;
+        const float pv = eval_p(w.dn, rp, __ldg(w.lg + v), pen && bit(bits, j), v);
+        if (!use_r) return to_fix(pv);
+        const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : __ldg(w.qn + v);
+        const float rv = pv - qv;
+        return to_fix(rv > 0.f ? rv : 0.f);
+      };
+      // smallest id whose running weight reaches the target: per-thread
+      // contiguous ranges of the part, block exclusive scan of their sums
+      const int chunk = (n + kST - 1) / kST;
+      const int a0 = min((int)threadIdx.x * chunk, n), a1 = min(a0 + chunk, n);
+      unsigned long long c = 0;
+      for (int j = a0; j < a1; ++j) c += weight(j);
+      const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+      unsigned long long incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) sm->wsum[wp] = incl;
+      __syncthreads();
+      unsigned long long before = 0;
+      for (int q = 0; q < wp; ++q) before += sm->wsum[q];
+      unsigned long long cum = before + incl - c;
+      const unsigned long long need = s_need;
+      if (cum < need && need <= cum + c) {
+        for (int j = a0; j < a1; ++j) {
+          const unsigned long long x = weight(j);
+          cum += x;
+          if (x > 0 && cum >= need) { s_y = v0 + j; break; }
+        }
+      }
+      __syncthreads();
+      y = s_y;
+    }
+    if (y < 0) y = w.dn.argmax;
+  }
+  if (threadIdx.x == 0) {
+    if (a.mode == 0) {
+      a.draft_out[(size_t)r * d + a.pos] = y;
+    } else {
+      a.n_acc[r] = nacc;
+      int32_t* o = a.out_tok + (size_t)r * (d + 1);
+      for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
+      if (a.h_rec) {
+        // the record's tokens are visible to the host before its count
+        int32_t* hr = a.h_rec + (size_t)r * (d + 2);
+        for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+        st_release_sys(hr, nacc);
+      }
+      if (a.stats) {
+        int32_t* st = a.stats + (size_t)r * (d + 2);
+        st[0] += 1;
+        if (nacc < d) st[1] += 1;
+        for (int i = 1; i <= nacc; ++i) st[1 + i] += 1;
+      }
+    }
+  }
+}
+
+static size_t fl_align(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t flat_workspace_bytes(int rows, int tasks) {
+  const size_t T = (size_t)tasks, R = (size_t)rows, P = kFlatMaxParts;
+  return fl_align(sizeof(TDesc) * T) + fl_align(8 * T * P) + fl_align(4 * T * P) + fl_align(8 * T * kFlatHistBins) +
+         fl_align(8 * T) + fl_align(4 * T) + 2 * fl_align(4 * T * kFlatCandCap) + fl_align(16 * R * P) +
+         fl_align(4 * R) + fl_align(4 * T) + fl_align(4 * R);
+}
+
+bool flat_fits(const RowParams* p, int rows, int V, const float* logits, long long ld) {
+  if (V % 4 != 0 || V < 2048 || (reinterpret_cast<uintptr_t>(logits) & 15) != 0 || ld % 4 != 0) return false;
+  for (int r = 0; r < rows; ++r)
+    if (!p[r].greedy && p[r].top_k > 0 && p[r].top_k < V) return false;
+  return true;
+}
+
+bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!ws || ws_bytes < flat_workspace_bytes(a.rows, a.tasks) || a.depth + 1 > 32) return false;
+  const int sms = device_sm_count();
+  int P = 2 * sms / a.tasks;
+  P = std::max(1, std::min({P, kFlatMaxParts, a.V / 2048}));
+  a.P = P;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t T = (size_t)a.tasks, R = (size_t)a.rows, PM = kFlatMaxParts;
+  auto take = [&](size_t bytes) {
+    uint8_t* q = w;
+    w += fl_align(bytes);
+    return q;
+  };
+  a.desc = reinterpret_cast<TDesc*>(take(sizeof(TDesc) * T));
+  a.amax = reinterpret_cast<unsigned long long*>(take(8 * T * PM));
+  a.zmin = reinterpret_cast<float*>(take(4 * T * PM));
+  a.hist_w = reinterpret_cast<unsigned long long*>(take(8 * T * kFlatHistBins));
+  a.sminp = reinterpret_cast<unsigned long long*>(take(8 * T));
+  a.ccnt = reinterpret_cast<int32_t*>(take(4 * T));
+  a.ckey = reinterpret_cast<uint32_t*>(take(4 * T * kFlatCandCap));
+  a.cid = reinterpret_cast<int32_t*>(take(4 * T * kFlatCandCap));
+  a.wsum = reinterpret_cast<unsigned long long*>(take(16 * R * PM));
+  a.nstop = reinterpret_cast<int32_t*>(take(4 * R));
+  a.gcnt = reinterpret_cast<int32_t*>(take(4 * T));
+  a.scnt = reinterpret_cast<int32_t*>(take(4 * R));
+  const int per = fl_per(a.V, P);
+  const size_t base = (sizeof(SampleSmem) + 15) & ~size_t(15);
+  const size_t bits_part = 4 * (size_t)((per + 31) / 32 + 1);
+  const size_t sm_part = base + bits_part;
+  const size_t sm_hist = ((base + bits_part + 15) & ~size_t(15)) + 8 * (size_t)kFlatBins;
+  const size_t sm_res = base + 12 * (size_t)kFlatCandCap + 4 * (size_t)((a.V + 31) / 32 + 1);
+  if (sm_res > 226 * 1024 || sm_hist > 226 * 1024) return false;
+  {
+    // the kernels' dynamic shared memory limit, raised once per device
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      for (auto k : {k_fl_stats, k_fl_hist, k_fl_gather, k_fl_sums})
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 226 * 1024);
+      done[dev] = true;
+    }
+  }
+  const dim3 parts(P, a.tasks), rowsP(P, a.rows);
+  launch_pdl(k_fl_stats, parts, dim3(kST), sm_part, s, a);
+  launch_pdl(k_fl_hist, parts, dim3(kST), sm_hist, s, a);
+  launch_pdl(k_fl_gather, parts, dim3(kST), std::max(sm_part, sm_res), s, a);
+  launch_pdl(k_fl_sums, rowsP, dim3(kST), sm_part, s, a);
+  count_launch(4);
+  return true;
+}
+
 static int sample_smem(int V, int C = 0, int P = 0) {
   const int per = (V + kClusterCTAs - 1) / kClusterCTAs;
   const size_t cand = 16 + (size_t)C * 8 + (size_t)P * 8 + (size_t)C * 4 + 4 + (size_t)C * 8;
@@ -2824,6 +3685,15 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
     for (int r = 0; r < a0.rows; ++r) t.p[r] = a0.p[r];
     launch_topk(t, s);
     return;
+  }
+  if (a0.mode == 0 && a0.flat_ws && flat_fits(a0.p, a0.rows, a0.V, a0.logits, a0.ld)) {
+    FlatArgs f;
+    memset(&f, 0, sizeof(f));
+    f.mode = 0; f.rows = a0.rows; f.V = a0.V; f.W = a0.W; f.depth = a0.depth; f.pos = a0.pos; f.tasks = a0.rows;
+    f.logits = a0.logits; f.ld = a0.ld; f.hist = a0.hist; f.drafts = a0.drafts; f.u = a0.u; f.q = a0.q;
+    f.draft_out = a0.draft_out; f.status = a0.status;
+    for (int r = 0; r < a0.rows; ++r) f.p[r] = a0.p[r];
+    if (launch_flat(f, a0.flat_ws, a0.flat_ws_bytes, s)) return;
   }
   SampleArgs a = a0;
   int C = 1;

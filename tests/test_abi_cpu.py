@@ -130,14 +130,24 @@ def test_spec_verify_rejects_bad_arguments_without_launching(L):
     assert m.spec_verify_workspace_bytes(8, 3, 152064) >= 8 * 4 * 32
 
 
-def test_workspace_holds_descriptors_and_streaming_lists():
-    # descriptors (32 bytes each), accept flags, and two kept-list arrays of 256
-    # entries per (row, position), each region 256-byte aligned
-    rows, depth = 64, 3
-    tasks = rows * (depth + 1)
+def test_workspace_holds_the_largest_path_layout():
+    # the largest of three layouts, each region 256-byte aligned:
+    #  - streaming / top-k lists: descriptors (32 bytes each), accept flags and
+    #    two kept-list arrays of 256 entries per (row, position);
+    #  - greedy stream: one 64-bit key per (range, segment), ranges <= 2048;
+    #  - flat transform: descriptors, 64 part slots (8 + 4 bytes) per task, a
+    #    2048-bin fixed-point histogram, the min-p mass and two counters per
+    #    task, a 1024-entry crossing-bin list (key, id), 64 part sums (2 x 8
+    #    bytes) and two counters per row
     al = lambda b: (b + 255) // 256 * 256
-    want = al(32 * tasks) + al(4 * tasks) + 2 * al(4 * tasks * 256)
-    assert m.spec_verify_workspace_bytes(rows, depth, 152064) == want
+    for rows, depth in ((64, 3), (8, 3), (1, 2)):
+        tasks = rows * (depth + 1)
+        lists = al(32 * tasks) + al(4 * tasks) + 2 * al(4 * tasks * 256)
+        keys = al(8 * (tasks + 2048))
+        flat = (al(32 * tasks) + al(8 * tasks * 64) + al(4 * tasks * 64) + al(8 * tasks * 2048) + al(8 * tasks)
+                + al(4 * tasks) + 2 * al(4 * tasks * 1024) + al(16 * rows * 64) + al(4 * rows) + al(4 * tasks)
+                + al(4 * rows))
+        assert m.spec_verify_workspace_bytes(rows, depth, 152064) == max(lists, keys, flat), (rows, depth)
     assert m.spec_verify_workspace_bytes(0, 3, 64) == 0
 
 
