@@ -261,7 +261,11 @@ void launch_sample(const SampleArgs& a, cudaStream_t s);
 // chain and the correction or bonus token of a verify).
 struct FlatArgs {
   int mode;                  // 0 draft step, 1 verify
-  int rows, V, W, depth, pos, tasks, P;
+  int rows, V, W, depth, pos, tasks;
+  int P;                     // parts per task of the argmax/minimum pass (every task)
+  int Ps;                    // parts per task of the histogram and gather passes (sampled tasks)
+  int P2;                    // parts per row of the sums pass
+  int nsr;                   // sampled rows, listed in srow
   const float* logits;       // mode 0: row r at logits + r * ld; mode 1: [rows][depth+1][V]
   long long ld;
   const int32_t* hist;       // [rows][W]
@@ -283,11 +287,12 @@ struct FlatArgs {
   int32_t* ccnt;             // [tasks]
   uint32_t* ckey;            // [tasks][kFlatCandCap]
   int32_t* cid;
-  unsigned long long* wsum;  // [rows][P][2]
+  unsigned long long* wsum;  // [rows][P2][16 warp slices][2]
   int32_t* nstop;            // [rows]
   int32_t* gcnt;             // [tasks] gathering CTAs done (the last resolves)
   int32_t* scnt;             // [rows] summing CTAs done (the last draws)
   RowParams p[kMaxRows];
+  int srow[kMaxRows];        // the rows that are not greedy, in order
 };
 constexpr int kFlatHistBins = 2048;
 constexpr int kFlatCandCap = 1024;
@@ -295,7 +300,8 @@ constexpr int kFlatMaxParts = 64;
 size_t flat_workspace_bytes(int rows, int tasks);
 bool flat_fits(const RowParams* p, int rows, int V, const float* logits, long long ld);
 // Lays the scratch out in ws (desc at offset 0), picks the parts per task and
-// launches the chain; false (nothing launched) if ws_bytes is too small.
+// launches the chain; false (nothing launched) if ws_bytes is too small or q
+// does not start on a 16-byte boundary.
 bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s);
 
 struct VerifyArgs {

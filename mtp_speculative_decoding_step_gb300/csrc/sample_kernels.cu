@@ -2790,24 +2790,27 @@ void launch_topk(const TopkArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------ flat transform
 // Rows with a wide support (no top-k below V) spread every (row, position)
-// over P parts of its vocabulary, one CTA per part, through a chain of four
+// over parts of its vocabulary, one CTA per part, through a chain of four
 // short kernels (each waits for the previous one at griddepcontrol.wait):
-//   k_fl_stats    argmax of the penalised logits and their minimum, per part;
-//                 zeroes the task's histogram and counters
-//   k_fl_hist     fixed-point weights exp(z' - m) (z' = z / T + 0) added into
-//                 kFlatBins equal value slices of [m - span, m] (the cluster
-//                 path's binning), and the min-p mass
-//   k_fl_gather   the bin in which the running mass reaches ceil(top_p * SE),
-//                 and its elements, into a per-task list; the task's last CTA
-//                 then takes the exact crossing element of that list in
-//                 (key, id) order (a weighted selection), the kept mass S and
-//                 the descriptor (if the bin holds more than the list: an
-//                 exact block-level radix selection over the row)
-//   k_fl_sums     per part of the drawn row: the accept chain (verify), the
-//                 part's sums of the draw weights (and, for a draft step, q);
-//                 the row's last CTA finds the part and then the element where
-//                 the running weight reaches the draw's target, and writes the
-//                 outputs.
+//   k_fl_stats    every task, P parts: argmax of the penalised logits and
+//                 their minimum; zeroes the task's histogram and counters
+//   k_fl_hist     sampled tasks, Ps parts: fixed-point weights exp(z' - m)
+//                 (z' = z / T + 0) added into kFlatBins equal value slices of
+//                 [m - span, m] (the cluster path's binning), and the min-p
+//                 mass
+//   k_fl_gather   sampled tasks, Ps parts: the bin in which the running mass
+//                 reaches ceil(top_p * SE), and its elements, into a per-task
+//                 list; the task's last CTA then takes the exact crossing
+//                 element of that list in (key, id) order (a weighted
+//                 selection), the kept mass S and the descriptor (if the bin
+//                 holds more than the list: an exact block-level radix
+//                 selection over the row)
+//   k_fl_sums     every row, P2 parts of 16 warp slices each: the accept
+//                 chain (verify), each slice's sums of the draw weights (and,
+//                 for a draft step, q); the row's last CTA finds the slice and
+//                 then the element where the running weight reaches the
+//                 draw's target, and writes the outputs. Greedy rows take the
+//                 argmax chain from the first kernel's part maxima.
 // The keys, weights, cut rules and draws are those of the cluster path.
 __device__ __forceinline__ unsigned long long fl_amax_key(float v, int id) {
   uint32_t u = __float_as_uint(v + 0.0f);
@@ -2839,21 +2842,40 @@ __device__ __forceinline__ FlTask fl_task(const FlatArgs& a, int t) {
 }
 __host__ __device__ __forceinline__ int fl_per(int V, int P) { return ((V + P - 1) / P + 3) & ~3; }
 
+// The j-th sampled task (grid row of the histogram and gather kernels).
+__device__ __forceinline__ int fl_sampled_task(const FlatArgs& a, int j) {
+  if (a.mode == 0) return a.srow[j];
+  const int tpr = a.depth + 1, s = j / tpr;
+  return a.srow[s] * tpr + (j - s * tpr);
+}
+
 // The task's transform scale: maximum transformed logit m, the argmax of the
 // penalised logits, and the bin scale of [m - span, m].
 struct FlScale {
   float mx, scale;
   int amax;
 };
-__device__ FlScale fl_scale(const FlatArgs& a, int t, const RowParams& rp) {
-  // every warp combines the P (<= 64) part slots, two per lane
+// Every warp: the task's P (<= 64) part slots, two per lane (loads only).
+struct FlSlots {
+  unsigned long long best;
+  float zm;
+};
+__device__ __forceinline__ FlSlots fl_slots(const FlatArgs& a, int t) {
   const int lane = threadIdx.x & 31;
-  unsigned long long best = 0ull;
-  float zm = INFINITY;
-  for (int q = lane; q < a.P; q += 32) {
-    best = max(best, __ldcg(&a.amax[(size_t)t * a.P + q]));
-    zm = fminf(zm, __ldcg(&a.zmin[(size_t)t * a.P + q]));
+  const unsigned long long* am = a.amax + (size_t)t * a.P;
+  const float* zn = a.zmin + (size_t)t * a.P;
+  FlSlots s;
+  s.best = lane < a.P ? __ldcg(am + lane) : 0ull;
+  s.zm = lane < a.P ? __ldcg(zn + lane) : INFINITY;
+  if (lane + 32 < a.P) {
+    s.best = max(s.best, __ldcg(am + lane + 32));
+    s.zm = fminf(s.zm, __ldcg(zn + lane + 32));
   }
+  return s;
+}
+__device__ FlScale fl_scale_of(FlSlots sl, const RowParams& rp) {
+  unsigned long long best = sl.best;
+  float zm = sl.zm;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
@@ -2871,26 +2893,33 @@ __device__ FlScale fl_scale(const FlatArgs& a, int t, const RowParams& rp) {
   s.scale = span > 0.f ? ((float)kFlatBins - 0.01f) / span : 0.f;
   return s;
 }
+__device__ __forceinline__ FlScale fl_scale(const FlatArgs& a, int t, const RowParams& rp) {
+  return fl_scale_of(fl_slots(a, t), rp);
+}
 __device__ __forceinline__ int fl_bin(const FlScale& s, float z) {
   const float t = (s.mx - z) * s.scale;
   return t < (float)kFlatBins ? (int)t : kFlatBins;  // beyond the span (and NaN): no bin
 }
 
-// Every thread of the block: total mass SE of the task's histogram, the bin
-// b in which the running mass reaches target = ceil(top_p SE) and the mass
-// still needed there (b = -1 when SE is 0), into shared memory. Four bins per
-// thread, one block scan.
-__device__ void fl_cross(SampleSmem* sm, const unsigned long long* h, float top_p, unsigned long long* SE_out,
-                         int* b_out, unsigned long long* need_out, unsigned long long* target_out) {
-  constexpr int PER = kFlatBins / kST;
+// The crossing of a task's histogram: total mass SE, the bin b in which the
+// running mass reaches target = ceil(top_p SE) (b = -1 when SE is 0) and the
+// mass still needed there.
+struct FlCross {
+  unsigned long long SE, need, target;
+  int b;
+};
+constexpr int kFlPer = kFlatBins / kST;  // histogram bins per thread
+__device__ __forceinline__ void fl_bins_load(const unsigned long long* h, unsigned long long (&v)[kFlPer]) {
+#pragma unroll
+  for (int b = 0; b < kFlPer; ++b) v[b] = __ldcg(&h[threadIdx.x * kFlPer + b]);
+}
+// Every thread of the block, from its kFlPer bins: the crossing, into *out
+// (shared memory). One block scan.
+__device__ void fl_cross(SampleSmem* sm, const unsigned long long (&v)[kFlPer], float top_p, FlCross* out) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  unsigned long long v[PER];
   unsigned long long s = 0;
 #pragma unroll
-  for (int b = 0; b < PER; ++b) {
-    v[b] = __ldcg(&h[threadIdx.x * PER + b]);
-    s += v[b];
-  }
+  for (int b = 0; b < kFlPer; ++b) s += v[b];
   unsigned long long incl = s;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -2899,7 +2928,7 @@ __device__ void fl_cross(SampleSmem* sm, const unsigned long long* h, float top_
   }
   __syncthreads();
   if (lane == 31) sm->wsum[w] = incl;
-  if (threadIdx.x == 0) *b_out = -1;
+  if (threadIdx.x == 0) out->b = -1;
   __syncthreads();
   unsigned long long before = 0, SE = 0;
   for (int q = 0; q < kST / 32; ++q) {
@@ -2910,20 +2939,29 @@ __device__ void fl_cross(SampleSmem* sm, const unsigned long long* h, float top_
   unsigned long long cum = before + incl - s;
   if (SE > 0 && cum < target && target <= cum + s) {
 #pragma unroll
-    for (int b = 0; b < PER; ++b) {
+    for (int b = 0; b < kFlPer; ++b) {
       if (cum < target && target <= cum + v[b]) {
-        *b_out = threadIdx.x * PER + b;
-        *need_out = target - cum;
+        out->b = threadIdx.x * kFlPer + b;
+        out->need = target - cum;
         break;
       }
       cum += v[b];
     }
   }
   if (threadIdx.x == 0) {
-    *SE_out = SE;
-    *target_out = target;
+    out->SE = SE;
+    out->target = target;
   }
   __syncthreads();
+}
+
+// Loads of batch b0 of a part: four 16-byte vectors per thread, kST apart.
+__device__ __forceinline__ void fl_load4(const float4* l4, int b0, int n4, float4 (&xb)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int j4 = b0 + u * kST + threadIdx.x;
+    if (j4 < n4) xb[u] = __ldg(l4 + j4);
+  }
 }
 
 __device__ __forceinline__ size_t fl_bits_off() { return (sizeof(SampleSmem) + 15) & ~size_t(15); }
@@ -3002,37 +3040,49 @@ __global__ void __launch_bounds__(kST) k_fl_stats(const __grid_constant__ FlatAr
   }
 }
 
+// Adds w to a 64-bit bin held as two 32-bit words, with native 32-bit shared
+// atomics: the low word wraps modulo 2^32 and the thread whose add wrapped it
+// carries one into the high word, so hi * 2^32 + lo stays the exact sum.
+__device__ __forceinline__ void fl_bin_add(uint32_t* lo, uint32_t* hi, int b, unsigned long long w) {
+  const uint32_t wl = (uint32_t)w, wh = (uint32_t)(w >> 32);
+  const uint32_t old = atomicAdd(&lo[b], wl);
+  const uint32_t c = old + wl < old ? 1u : 0u;
+  if (wh + c) atomicAdd(&hi[b], wh + c);
+}
+__host__ __device__ __forceinline__ size_t fl_hist_off(int per) {
+  return (((sizeof(SampleSmem) + 15) & ~size_t(15)) + 4 * (size_t)((per + 31) / 32 + 1) + 15) & ~size_t(15);
+}
+
+// The target logits are inputs of the whole chain (the kernel before the
+// first one of the chain has finished once any later one starts), so the
+// histogram, gather and sums kernels load their first batch of them before
+// waiting for the kernel before them.
 __global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
-  const int per = fl_per(a.V, a.P);
+  const int per = fl_per(a.V, a.Ps);
   uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
-  unsigned long long* hh =
-      reinterpret_cast<unsigned long long*>(dyn + ((fl_bits_off() + 4 * (size_t)((per + 31) / 32 + 1) + 15) & ~size_t(15)));
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.y, p = blockIdx.x;
+  uint32_t* lo = reinterpret_cast<uint32_t*>(dyn + fl_hist_off(per));
+  uint32_t* hi = lo + kFlatBins;
+  const int t = fl_sampled_task(a, blockIdx.y), p = blockIdx.x;
   const FlTask k = fl_task(a, t);
   const RowParams rp = a.p[k.r];
-  if (rp.greedy) return;
-  const FlScale sc = fl_scale(a, t, rp);
   const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
-  for (int b = threadIdx.x; b < kFlatBins; b += kST) hh[b] = 0ull;
+  const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
+  const int n4 = n / 4;
+  float4 xb[4];
+  fl_load4(l4, 0, n4, xb);
+  for (int b = threadIdx.x; b < 2 * kFlatBins; b += kST) lo[b] = 0u;
   load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
   const bool pen = rp.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
-  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const FlScale sc = fl_scale(a, t, rp);
   const bool minp = rp.min_p > 0.f;
   unsigned long long smp = 0ull;
-  const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
-  const int n4 = n / 4;
   for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
-    float4 xb[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * kST + threadIdx.x;
-      if (j4 < n4) xb[u] = __ldg(l4 + j4);
-    }
+    if (b0 > 0) fl_load4(l4, b0, n4, xb);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j4 = b0 + u * kST + threadIdx.x;
@@ -3047,7 +3097,7 @@ __global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArg
             const float ev = expf(z - sc.mx);
             const unsigned long long w = to_fix(ev);
             if (w) {
-              atomicAdd(&hh[b], w);
+              fl_bin_add(lo, hi, b, w);
               if (minp && ev >= rp.min_p) smp += w;
             }
           }
@@ -3056,62 +3106,105 @@ __global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArg
     }
   }
   __syncthreads();
-  for (int b = threadIdx.x; b < kFlatBins; b += kST)
-    if (hh[b]) atomicAdd(&a.hist_w[(size_t)t * kFlatBins + b], hh[b]);
+  for (int b = threadIdx.x; b < kFlatBins; b += kST) {
+    const unsigned long long v = ((unsigned long long)hi[b] << 32) + lo[b];
+    if (v) atomicAdd(&a.hist_w[(size_t)t * kFlatBins + b], v);
+  }
   if (minp) {
     const unsigned long long tot = block_sum_u64(smp, sm->wsum);
     if (threadIdx.x == 0 && tot) atomicAdd(&a.sminp[t], tot);
   }
 }
 
-__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn);
-__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn);
+__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn, const FlScale* sc_in,
+                                const FlCross* cr_in);
 
 __global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
-  __shared__ unsigned long long s_SE, s_need, s_target;
-  __shared__ int s_b;
+  __shared__ FlCross s_cr;
   __shared__ int s_last;
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.y, p = blockIdx.x;
+  const int t = fl_sampled_task(a, blockIdx.y), p = blockIdx.x;
   const FlTask k = fl_task(a, t);
   const RowParams rp = a.p[k.r];
-  if (rp.greedy || !(rp.top_p > 0.f && rp.top_p < 1.f)) {
+  if (!(rp.top_p > 0.f && rp.top_p < 1.f)) {
     // nothing to gather: one CTA writes the descriptor
-    if (p == 0) fl_resolve_task(a, t, dyn);
+    pdl_wait();
+    pdl_trigger();
+    if (p == 0) fl_resolve_task(a, t, dyn, nullptr, nullptr);
     return;
   }
-  const FlScale sc = fl_scale(a, t, rp);
-  fl_cross(sm, a.hist_w + (size_t)t * kFlatBins, rp.top_p, &s_SE, &s_b, &s_need, &s_target);
-  const int bstar = s_b;
-  const int per = fl_per(a.V, a.P);
+  const int per = fl_per(a.V, a.Ps);
   const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
+  const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
+  const int n4 = n / 4;
+  float4 xb[4];
+  fl_load4(l4, 0, n4, xb);
   load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
   const bool pen = rp.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
-  for (int j = threadIdx.x; j < n; j += kST) {
-    float z = __ldg(k.lg + v0 + j);
-    if (pen && bit(bits, j)) z = penalize(z, rp.rep_penalty);
-    z = z / rp.temperature + 0.0f;
-    if (bstar >= 0 && fl_bin(sc, z) == bstar) {
-      const int pos = atomicAdd(&a.ccnt[t], 1);
-      if (pos < kFlatCandCap) {
-        a.ckey[(size_t)t * kFlatCandCap + pos] = desc_key(z);
-        a.cid[(size_t)t * kFlatCandCap + pos] = v0 + j;
+  pdl_wait();
+  pdl_trigger();
+  // one round trip: the histogram bins and the part slots
+  unsigned long long hv[kFlPer];
+  fl_bins_load(a.hist_w + (size_t)t * kFlatBins, hv);
+  const FlScale sc = fl_scale(a, t, rp);
+  fl_cross(sm, hv, rp.top_p, &s_cr);
+  const int bstar = s_cr.b;
+  if (bstar >= 0) {
+    const int lane = threadIdx.x & 31;
+    uint32_t* ckey = a.ckey + (size_t)t * kFlatCandCap;
+    int32_t* cid = a.cid + (size_t)t * kFlatCandCap;
+    for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
+      if (b0 > 0) fl_load4(l4, b0, n4, xb);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j4 = b0 + u * kST + threadIdx.x;
+        float zz[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t mm = 0u;  // elements of this vector in the crossing bin
+        if (j4 < n4) {
+          const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+          const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            zz[e] = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
+            if (fl_bin(sc, zz[e]) == bstar) mm |= 1u << e;
+          }
+        }
+        if (__any_sync(0xFFFFFFFFu, mm != 0u)) {
+          // one list append per warp: exclusive scan of the lanes' counts
+          const int c = __popc(mm);
+          int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += x;
+          }
+          int base = 0;
+          if (lane == 31) base = atomicAdd(&a.ccnt[t], incl);
+          int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if ((mm >> e) & 1u) {
+              if (pos < kFlatCandCap) {
+                ckey[pos] = desc_key(zz[e]);
+                cid[pos] = v0 + 4 * j4 + e;
+              }
+              ++pos;
+            }
+        }
       }
     }
   }
   // the last of the task's CTAs to finish resolves its descriptor
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&a.gcnt[t], 1) == a.P - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.gcnt[t], 1) == a.Ps - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  fl_resolve_task(a, t, dyn);
+  fl_resolve_task(a, t, dyn, &sc, &s_cr);
 }
 
 // Exact crossing inside bin bstar of one row by one CTA, when the gathered
@@ -3249,50 +3342,98 @@ __device__ void fl_exact_cut(SampleSmem* sm, int V, Z zof, const FlScale& sc, in
   cutout = cut;
 }
 
-// One CTA: the descriptor of task t (shared memory laid out as SampleSmem,
-// then the candidate list, its tie buffer and a bitmap of the whole row).
-__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn) {
+// One CTA: the descriptor of a sampled task t (shared memory laid out as
+// SampleSmem, then the candidate list, its tie buffer and a bitmap of the
+// whole row). sc_in and cr_in: the scale and crossing the calling CTA already
+// holds (null: computed here).
+__device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn, const FlScale* sc_in,
+                                const FlCross* cr_in) {
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   uint32_t* mk = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
   int* mi = reinterpret_cast<int*>(mk + kFlatCandCap);
   int* tie = mi + kFlatCandCap;
   uint32_t* bits = reinterpret_cast<uint32_t*>(tie + kFlatCandCap);
-  __shared__ unsigned long long s_SE, s_need, s_target;
-  __shared__ int s_b;
+  __shared__ FlCross s_cr;
+  __shared__ uint32_t s_K;
+  __shared__ int s_cut, s_ok;
+  __shared__ unsigned long long s_in;
   const FlTask k = fl_task(a, t);
   const RowParams rp = a.p[k.r];
-  const FlScale sc = fl_scale(a, t, rp);
+  const bool topp = rp.top_p > 0.f && rp.top_p < 1.f;
+  FlScale sc;
+  const FlCross* cr = cr_in;
+  if (sc_in) {
+    sc = *sc_in;
+  } else {
+    unsigned long long hv[kFlPer];
+    fl_bins_load(a.hist_w + (size_t)t * kFlatBins, hv);
+    sc = fl_scale(a, t, rp);
+    fl_cross(sm, hv, topp ? rp.top_p : 1.f, &s_cr);
+    cr = &s_cr;
+  }
   TDesc d;
   d.argmax = sc.amax;
   d.k_key = 0xFFFFFFFFu;
   d.k_cut = 0x7FFFFFFF;
   d.p_key = 0xFFFFFFFFu;
   d.p_cut = 0x7FFFFFFF;
-  d.m = 0.f;
-  d.S = 1.f;
-  d.kept = rp.greedy ? 1 : -1;
-  if (rp.greedy) {
-    if (threadIdx.x == 0) a.desc[t] = d;
-    return;
-  }
-  const bool topp = rp.top_p > 0.f && rp.top_p < 1.f;
-  fl_cross(sm, a.hist_w + (size_t)t * kFlatBins, topp ? rp.top_p : 1.f, &s_SE, &s_b, &s_need, &s_target);
-  unsigned long long S = s_SE;
-  const int bstar = s_b;
+  d.kept = -1;
+  unsigned long long S = cr->SE;
+  const int bstar = cr->b;
   if (topp && bstar >= 0) {
     auto wk = [&](uint32_t key) { return to_fix(expf(key_to_z(key) - sc.mx)); };
-    const int cnt = __ldcg(&a.ccnt[t]);
+    const unsigned long long need = cr->need;
     uint32_t K = 0xFFFFFFFFu;
     int cut = 0x7FFFFFFF;
     unsigned long long in_bin = 0;
-    bool ok = cnt <= kFlatCandCap;
-    if (ok) {
+    // one round trip: the list's length and its first 32 entries
+    const int lane = threadIdx.x & 31;
+    const int cnt = __ldcg(&a.ccnt[t]);
+    uint32_t k0 = 0xFFFFFFFFu;
+    int i0 = 0x7FFFFFFF;
+    if (threadIdx.x < 32) {
+      k0 = __ldcg(&a.ckey[(size_t)t * kFlatCandCap + lane]);
+      i0 = __ldcg(&a.cid[(size_t)t * kFlatCandCap + lane]);
+    }
+    bool ok = false;
+    if (cnt >= 1 && cnt <= 32) {
+      // a short list: warp 0, one entry per lane; the weight of the entries
+      // before each one in (key, id) order, and the entry where it crosses
+      if (threadIdx.x == 0) s_ok = 0;
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        const bool have = lane < cnt;
+        const uint32_t kk = have ? k0 : 0xFFFFFFFFu;
+        const int ii = have ? i0 : 0x7FFFFFFF;
+        const unsigned long long ww = have ? wk(kk) : 0ull;
+        unsigned long long before = 0;
+        for (int j = 0; j < cnt; ++j) {
+          const uint32_t kj = __shfl_sync(0xFFFFFFFFu, kk, j);
+          const int ij = __shfl_sync(0xFFFFFFFFu, ii, j);
+          const unsigned long long wj = __shfl_sync(0xFFFFFFFFu, ww, j);
+          if (kj < kk || (kj == kk && ij < ii)) before += wj;
+        }
+        if (have && before < need && need <= before + ww) {  // exactly one entry
+          s_K = kk;
+          s_cut = ii;
+          s_in = before + ww;
+          s_ok = 1;
+        }
+      }
+      __syncthreads();
+      ok = s_ok != 0;
+      if (ok) {
+        K = s_K;
+        cut = s_cut;
+        in_bin = s_in;
+      }
+    } else if (cnt > 32 && cnt <= kFlatCandCap) {
       for (int q = threadIdx.x; q < cnt; q += kST) {
         mk[q] = __ldcg(&a.ckey[(size_t)t * kFlatCandCap + q]);
         mi[q] = __ldcg(&a.cid[(size_t)t * kFlatCandCap + q]);
       }
       __syncthreads();
-      ok = cnt > 0 && list_select(sm, mk, mi, cnt, s_need, wk, tie, kFlatCandCap, K, cut);
+      ok = list_select(sm, mk, mi, cnt, need, wk, tie, kFlatCandCap, K, cut);
       if (ok) {
         unsigned long long loc = 0;
         for (int q = threadIdx.x; q < cnt; q += kST)
@@ -3309,13 +3450,13 @@ __device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn) {
         if (pen && bit(bits, j)) z = penalize(z, rp.rep_penalty);
         return z / rp.temperature + 0.0f;
       };
-      fl_exact_cut(sm, a.V, zof, sc, bstar, s_need, K, cut, &in_bin);
+      fl_exact_cut(sm, a.V, zof, sc, bstar, need, K, cut, &in_bin);
     }
     d.p_key = K;
     d.p_cut = cut;
     // the kept mass: every bin before the crossing one, then that bin's
     // elements up to the bound; with min-p the shorter of the two prefixes
-    S = (s_target - s_need) + in_bin;
+    S = (cr->target - need) + in_bin;
     if (rp.min_p > 0.f && !(expf(key_to_z(K) - sc.mx) >= rp.min_p)) S = __ldcg(&a.sminp[t]);
   } else if (rp.min_p > 0.f) {
     S = __ldcg(&a.sminp[t]);
@@ -3372,208 +3513,324 @@ __device__ FlDraw fl_draw_row(const FlatArgs& a, int r, int n, const RowParams& 
   return w;
 }
 
-__global__ void __launch_bounds__(kST) k_fl_sums(const __grid_constant__ FlatArgs a) {
+// Warp slice wi of part p (of P2) of a row: [*s0, *s0 + *sn) within the
+// part, which starts at *v0. Every bound is a multiple of 4.
+__device__ __forceinline__ void fl_slice(const FlatArgs& a, int p, int wi, int* v0, int* s0, int* sn) {
+  const int per = fl_per(a.V, a.P2);
+  *v0 = min(p * per, a.V);
+  const int n = min(per, a.V - *v0);
+  const int wsz = fl_per(n, kST / 32);
+  *s0 = min(wi * wsz, n);
+  *sn = min(wsz, n - *s0);
+}
+
+// The penalty window of position i from hw = history (W) then drafts: the W
+// tokens hw[i, i + W).
+__device__ void window_from(SampleSmem* sm, const int* hw, int W, int i) {
+  for (int q = threadIdx.x; q < W; q += kST) sm->wtok[q] = hw[i + q];
+  if (threadIdx.x == 0) sm->nwin = W;
+  __syncthreads();
+}
+
+__device__ void fl_pick_greedy(const FlatArgs& a, int r);
+__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn, const FlDraw& w, const RowParams& rp);
+
+__global__ void __launch_bounds__(kST, 2) k_fl_sums(const __grid_constant__ FlatArgs a) {
   extern __shared__ __align__(16) unsigned char dyn[];
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
   __shared__ int s_n, s_last;
-  __shared__ int s_hw[128 + 16];
-  pdl_wait();
-  pdl_trigger();
+  __shared__ int s_hw[128 + 32];
   const int r = blockIdx.y, p = blockIdx.x;
   const RowParams rp = a.p[r];
   if (rp.greedy) {
-    if (p == 0) fl_pick_row(a, r, dyn);
+    pdl_wait();
+    pdl_trigger();
+    if (p == 0) fl_pick_greedy(a, r);
     return;
   }
-  if (a.mode == 1) {
-    for (int q = threadIdx.x; q < a.W + a.depth; q += kST)
-      s_hw[q] = q < a.W ? a.hist[(size_t)r * a.W + q] : a.drafts[(size_t)r * a.depth + q - a.W];
-    __syncthreads();
-  }
+  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int v0, s0, sn;
+  fl_slice(a, p, wi, &v0, &s0, &sn);
+  const int n = min(fl_per(a.V, a.P2), a.V - v0);
+  // history then drafts: inputs of the chain, staged before the wait
+  for (int q = threadIdx.x; q < a.W + a.depth; q += kST)
+    s_hw[q] = q < a.W ? a.hist[(size_t)r * a.W + q] : a.drafts[(size_t)r * a.depth + q - a.W];
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < 32) {
-    const int n = a.mode == 0 ? a.pos : fl_chain(a, r, rp, s_hw);
-    if (threadIdx.x == 0) s_n = n;
+    const int nn = a.mode == 0 ? a.pos : fl_chain(a, r, rp, s_hw);
+    if (threadIdx.x == 0) s_n = nn;
   }
   __syncthreads();
+  // one round trip: the drawn row's descriptor and this warp's slice of it
   const FlDraw w = fl_draw_row(a, r, s_n, rp);
-  const int per = fl_per(a.V, a.P);
-  const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
-  load_window(sm, a.hist + (size_t)r * a.W, a.W, a.drafts + (size_t)r * a.depth, w.n);
+  const float4* l4 = reinterpret_cast<const float4*>(w.lg + v0 + s0);
+  const float4* q4 = w.qn ? reinterpret_cast<const float4*>(w.qn + v0 + s0) : nullptr;
+  const int n4 = sn / 4;
+  float4 xb[4], qb[4];
+  auto load = [&](int b0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * 32 + lane;
+      if (j4 < n4) {
+        xb[u] = __ldg(l4 + j4);
+        qb[u] = q4 ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  load(0);
+  window_from(sm, s_hw, a.W, w.n);
   const bool pen = rp.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
-  float* qout = a.mode == 0 ? a.q + ((size_t)r * a.depth + a.pos) * a.V : nullptr;
+  // each warp sums its own slice (lanes read consecutive 16-byte vectors)
+  float4* o4 = a.mode == 0 ? reinterpret_cast<float4*>(a.q + ((size_t)r * a.depth + a.pos) * a.V + v0 + s0) : nullptr;
   unsigned long long wp = 0, wr = 0;
-  for (int j = threadIdx.x; j < n; j += kST) {
-    const int v = v0 + j;
-    const float pv = eval_p(w.dn, rp, __ldg(w.lg + v), pen && bit(bits, j), v);
-    if (qout) qout[v] = pv;
-    wp += to_fix(pv);
-    if (w.residual) {
-      const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : __ldg(w.qn + v);
-      const float rv = pv - qv;
-      wr += to_fix(rv > 0.f ? rv : 0.f);
+  for (int b0 = 0; b0 < n4; b0 += 4 * 32) {
+    if (b0 > 0) load(b0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j4 = b0 + u * 32 + lane;
+      if (j4 < n4) {
+        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+        const float qs[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+        const int jj = s0 + 4 * j4;  // index within the part
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = v0 + jj + e;
+          pv[e] = eval_p(w.dn, rp, xs[e], pen && bit(bits, jj + e), v);
+          wp += to_fix(pv[e]);
+          if (w.residual) {
+            const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qs[e];
+            const float rv = pv[e] - qv;
+            wr += to_fix(rv > 0.f ? rv : 0.f);
+          }
+        }
+        if (o4) o4[j4] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+      }
     }
   }
-  wp = block_sum_u64(wp, sm->wsum);
-  wr = block_sum_u64(wr, sm->wsum);
-  if (threadIdx.x == 0) {
-    a.wsum[((size_t)r * a.P + p) * 2 + 0] = wr;
-    a.wsum[((size_t)r * a.P + p) * 2 + 1] = wp;
-    if (p == 0) a.nstop[r] = w.n;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    wp += __shfl_xor_sync(0xFFFFFFFFu, wp, o);
+    wr += __shfl_xor_sync(0xFFFFFFFFu, wr, o);
+  }
+  if (lane == 0) {
+    unsigned long long* ws = a.wsum + ((((size_t)r * a.P2 + p) * (kST / 32)) + wi) * 2;
+    ws[0] = wr;
+    ws[1] = wp;
   }
   // the last of the row's CTAs to finish draws
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&a.scnt[r], 1) == a.P - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.scnt[r], 1) == a.P2 - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  fl_pick_row(a, r, dyn);
+  fl_pick_row(a, r, dyn, w, rp);
 }
 
-// One CTA: the row's draw and outputs (greedy rows: the argmax chain).
-__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn) {
+// The row's outputs: accepted count nacc (verify) and the drawn token y.
+__device__ void fl_write_row(const FlatArgs& a, int r, int nacc, int y) {
+  const int d = a.depth;
+  const int32_t* dr = a.drafts + (size_t)r * d;
+  if (a.mode == 0) {
+    a.draft_out[(size_t)r * d + a.pos] = y;
+    return;
+  }
+  a.n_acc[r] = nacc;
+  int32_t* o = a.out_tok + (size_t)r * (d + 1);
+  for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
+  if (a.h_rec) {
+    // the record's tokens are visible to the host before its count
+    int32_t* hr = a.h_rec + (size_t)r * (d + 2);
+    for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
+    st_release_sys(hr, nacc);
+  }
+  if (a.stats) {
+    int32_t* st = a.stats + (size_t)r * (d + 2);
+    st[0] += 1;
+    if (nacc < d) st[1] += 1;
+    for (int i = 1; i <= nacc; ++i) st[1 + i] += 1;
+  }
+}
+
+// Warp 0 of one CTA, greedy row: point masses at the argmax of each position
+// (the first kernel's part maxima); accept while the draft is the argmax of
+// the row before it.
+__device__ void fl_pick_greedy(const FlatArgs& a, int r) {
+  if (threadIdx.x >= 32) return;
+  const int d = a.depth, lane = threadIdx.x;
+  const int np = a.mode == 0 ? 1 : d + 1;
+  int am = 0;
+  for (int i = 0; i < np; ++i) {
+    const int t = a.mode == 0 ? r : r * (d + 1) + i;
+    const unsigned long long* slot = a.amax + (size_t)t * a.P;
+    unsigned long long best = lane < a.P ? __ldcg(slot + lane) : 0ull;
+    if (lane + 32 < a.P) best = max(best, __ldcg(slot + lane + 32));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    if (lane == i) am = best ? (int)(0xFFFFFFFFu - (uint32_t)best) : 0;
+  }
+  int nacc = 0, y;
+  if (a.mode == 0) {
+    y = __shfl_sync(0xFFFFFFFFu, am, 0);
+  } else {
+    const int x = lane < d ? a.drafts[(size_t)r * d + lane] : -1;
+    const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < d && !(x >= 0 && x < a.V && x == am));
+    nacc = miss ? __ffs(miss) - 1 : d;
+    y = __shfl_sync(0xFFFFFFFFu, am, nacc);
+  }
+  if (lane == 0) fl_write_row(a, r, nacc, y);
+}
+
+// One CTA (the row's last to finish its sums), sampled row: the draw from
+// the slices' sums, then the element inside the chosen slice.
+__device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn, const FlDraw& w, const RowParams& rp) {
   SampleSmem* sm = reinterpret_cast<SampleSmem*>(dyn);
   uint32_t* bits = reinterpret_cast<uint32_t*>(dyn + fl_bits_off());
-  __shared__ int s_part, s_y;
+  __shared__ int s_slice, s_y;
   __shared__ unsigned long long s_need;
-  const int d = a.depth;
-  const RowParams rp = a.p[r];
-  const int32_t* dr = a.drafts + (size_t)r * d;
-  int nacc, y;
-  if (rp.greedy) {
-    // point masses: accept while the draft is the argmax of the row before it
-    if (a.mode == 0) {
-      nacc = 0;
-      y = a.desc[r].argmax;
-    } else {
-      int am = 0, x = -1;
-      const int lane = threadIdx.x & 31;
-      if (threadIdx.x < 32) {
-        am = lane <= d ? a.desc[r * (d + 1) + lane].argmax : 0;
-        x = lane < d ? dr[lane] : -1;
-      }
-      const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < d && !(x >= 0 && x < a.V && x == am));
-      nacc = miss ? __ffs(miss) - 1 : d;
-      y = __shfl_sync(0xFFFFFFFFu, am, nacc);
-    }
-  } else {
-    nacc = a.mode == 0 ? 0 : __ldcg(&a.nstop[r]);
-    const FlDraw w = fl_draw_row(a, r, a.mode == 0 ? a.pos : nacc, rp);
-    // every warp: the row's two totals over its parts (lane l holds parts 2l, 2l+1)
-    const int lane = threadIdx.x & 31;
-    unsigned long long pr[2] = {0ull, 0ull}, pp[2] = {0ull, 0ull};
+  __shared__ unsigned long long s_wr[kST / 32], s_wp[kST / 32];
+  const int d = a.depth, lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int NS = a.P2 * (kST / 32);
+  // the row's slices in order, two per thread: one round trip
+  const unsigned long long* ws = a.wsum + (size_t)r * NS * 2;
+  unsigned long long pr0 = 0, pr1 = 0, pp0 = 0, pp1 = 0;
+  if (2 * (int)threadIdx.x < NS) {
+    pr0 = __ldcg(ws + 4 * threadIdx.x + 0);
+    pp0 = __ldcg(ws + 4 * threadIdx.x + 1);
+  }
+  if (2 * (int)threadIdx.x + 1 < NS) {
+    pr1 = __ldcg(ws + 4 * threadIdx.x + 2);
+    pp1 = __ldcg(ws + 4 * threadIdx.x + 3);
+  }
+  // block scans of both sums at once
+  const unsigned long long mr = pr0 + pr1, mp = pp0 + pp1;
+  unsigned long long ir = mr, ip = mp;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int p = 2 * lane + e;
-      if (p < a.P) {
-        pr[e] = __ldcg(&a.wsum[((size_t)r * a.P + p) * 2 + 0]);
-        pp[e] = __ldcg(&a.wsum[((size_t)r * a.P + p) * 2 + 1]);
-      }
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long xr = __shfl_up_sync(0xFFFFFFFFu, ir, o);
+    const unsigned long long xp = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+    if (lane >= o) {
+      ir += xr;
+      ip += xp;
     }
-    unsigned long long tr = pr[0] + pr[1], tp = pp[0] + pp[1];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tr += __shfl_xor_sync(0xFFFFFFFFu, tr, o);
-      tp += __shfl_xor_sync(0xFFFFFFFFu, tp, o);
-    }
-    const bool use_r = w.residual && tr > 0;
-    const unsigned long long tot = use_r ? tr : tp;
-    y = -1;
-    if (tot > 0) {
-      const float uu = a.mode == 0 ? a.u[(size_t)r * d + a.pos] : a.u[(size_t)r * (d + 1) + d];
-      const unsigned long long target = (unsigned long long)floor((double)uu * (double)tot) + 1ull;
-      if (threadIdx.x < 32) {
-        // the part where the running weight reaches the target: lane scan
-        const unsigned long long* pw = use_r ? pr : pp;
-        const unsigned long long mine = pw[0] + pw[1];
-        unsigned long long incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const unsigned long long excl = incl - mine;
-        const bool here = excl < target && target <= incl;
-        const unsigned who = __ballot_sync(0xFFFFFFFFu, here);
-        if (here && lane == __ffs(who) - 1) {
-          const bool first = target <= excl + pw[0] && 2 * lane < a.P;
-          s_part = first ? 2 * lane : 2 * lane + 1;
-          s_need = first ? target - excl : target - excl - pw[0];
-        }
-        if (!who && lane == 0) {  // rounding left the target past the total: the last part
-          s_part = a.P - 1;
-          s_need = 1ull;
-        }
-        if (lane == 0) s_y = -1;
-      }
-      __syncthreads();
-      const int per = fl_per(a.V, a.P);
-      const int v0 = min(s_part * per, a.V), n = min(per, a.V - v0);
-      load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, w.n);
-      const bool pen = rp.rep_penalty != 1.f;
-      if (pen) build_bitmap(sm, bits, v0, n);
-      auto weight = [&](int j) {
-        const int v = v0 + j;
-        const float pv = eval_p(w.dn, rp, __ldg(w.lg + v), pen && bit(bits, j), v);
-        if (!use_r) return to_fix(pv);
-        const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : __ldg(w.qn + v);
-        const float rv = pv - qv;
-        return to_fix(rv > 0.f ? rv : 0.f);
-      };
-      // smallest id whose running weight reaches the target: per-thread
-      // contiguous ranges of the part, block exclusive scan of their sums
-      const int chunk = (n + kST - 1) / kST;
-      const int a0 = min((int)threadIdx.x * chunk, n), a1 = min(a0 + chunk, n);
-      unsigned long long c = 0;
-      for (int j = a0; j < a1; ++j) c += weight(j);
-      const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
-      unsigned long long incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (lane == 31) sm->wsum[wp] = incl;
-      __syncthreads();
-      unsigned long long before = 0;
-      for (int q = 0; q < wp; ++q) before += sm->wsum[q];
-      unsigned long long cum = before + incl - c;
-      const unsigned long long need = s_need;
-      if (cum < need && need <= cum + c) {
-        for (int j = a0; j < a1; ++j) {
-          const unsigned long long x = weight(j);
-          cum += x;
-          if (x > 0 && cum >= need) { s_y = v0 + j; break; }
-        }
-      }
-      __syncthreads();
-      y = s_y;
-    }
-    if (y < 0) y = w.dn.argmax;
+  }
+  __syncthreads();
+  if (lane == 31) {
+    s_wr[wi] = ir;
+    s_wp[wi] = ip;
   }
   if (threadIdx.x == 0) {
-    if (a.mode == 0) {
-      a.draft_out[(size_t)r * d + a.pos] = y;
-    } else {
-      a.n_acc[r] = nacc;
-      int32_t* o = a.out_tok + (size_t)r * (d + 1);
-      for (int i = 0; i <= d; ++i) o[i] = i < nacc ? dr[i] : (i == nacc ? y : -1);
-      if (a.h_rec) {
-        // the record's tokens are visible to the host before its count
-        int32_t* hr = a.h_rec + (size_t)r * (d + 2);
-        for (int i = 0; i <= d; ++i) hr[1 + i] = o[i];
-        st_release_sys(hr, nacc);
-      }
-      if (a.stats) {
-        int32_t* st = a.stats + (size_t)r * (d + 2);
-        st[0] += 1;
-        if (nacc < d) st[1] += 1;
-        for (int i = 1; i <= nacc; ++i) st[1 + i] += 1;
+    // rounding left the target past the total: the last slice
+    s_slice = NS - 1;
+    s_need = 1ull;
+    s_y = -1;
+  }
+  __syncthreads();
+  unsigned long long tr = 0, tp = 0, br = 0, bp = 0;
+  for (int q = 0; q < kST / 32; ++q) {
+    if (q < wi) {
+      br += s_wr[q];
+      bp += s_wp[q];
+    }
+    tr += s_wr[q];
+    tp += s_wp[q];
+  }
+  const bool use_r = w.residual && tr > 0;
+  const unsigned long long tot = use_r ? tr : tp;
+  int y = -1;
+  if (tot > 0) {
+    const float uu = a.mode == 0 ? a.u[(size_t)r * d + a.pos] : a.u[(size_t)r * (d + 1) + d];
+    const unsigned long long target = (unsigned long long)floor((double)uu * (double)tot) + 1ull;
+    const unsigned long long w0 = use_r ? pr0 : pp0, mine = use_r ? mr : mp;
+    const unsigned long long excl = use_r ? br + ir - mr : bp + ip - mp;
+    if (excl < target && target <= excl + mine) {
+      const bool first = target <= excl + w0;
+      s_slice = first ? 2 * threadIdx.x : 2 * threadIdx.x + 1;
+      s_need = first ? target - excl : target - excl - w0;
+    }
+    __syncthreads();
+    int v0, s0, sn;
+    fl_slice(a, s_slice / (kST / 32), s_slice % (kST / 32), &v0, &s0, &sn);
+    // the window of the drawn row is in shared memory already
+    const bool pen = rp.rep_penalty != 1.f;
+    if (pen) build_bitmap(sm, bits, v0 + s0, sn);
+    if (threadIdx.x < 32) {
+      // warp 0 walks the slice in chunks of 128 elements (four chunks'
+      // loads in flight): smallest id whose running weight reaches need
+      unsigned long long need = s_need;
+      const float4* l4 = reinterpret_cast<const float4*>(w.lg + v0 + s0);
+      const float4* q4 = w.qn ? reinterpret_cast<const float4*>(w.qn + v0 + s0) : nullptr;
+      const int n4 = sn / 4;
+      bool done = false;
+      for (int b0 = 0; b0 < n4 && !done; b0 += 4 * 32) {
+        float4 xb[4], qb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j4 = b0 + u * 32 + lane;
+          if (j4 < n4) {
+            xb[u] = __ldg(l4 + j4);
+            qb[u] = q4 ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (done) break;
+          const int j4 = b0 + u * 32 + lane;
+          unsigned long long wt[4] = {0ull, 0ull, 0ull, 0ull};
+          if (j4 < n4) {
+            const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+            const float qs[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int v = v0 + s0 + 4 * j4 + e;
+              const float pv = eval_p(w.dn, rp, xs[e], pen && bit(bits, 4 * j4 + e), v);
+              if (!use_r) {
+                wt[e] = to_fix(pv);
+              } else {
+                const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qs[e];
+                const float rv = pv - qv;
+                wt[e] = to_fix(rv > 0.f ? rv : 0.f);
+              }
+            }
+          }
+          const unsigned long long ls = wt[0] + wt[1] + wt[2] + wt[3];
+          unsigned long long li = ls;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long x = __shfl_up_sync(0xFFFFFFFFu, li, o);
+            if (lane >= o) li += x;
+          }
+          const unsigned long long ct = __shfl_sync(0xFFFFFFFFu, li, 31);
+          if (need <= ct) {
+            const unsigned long long ex = li - ls;
+            if (ex < need && need <= li) {
+              unsigned long long cum = ex;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                cum += wt[e];
+                if (wt[e] > 0 && cum >= need) {
+                  s_y = v0 + s0 + 4 * j4 + e;
+                  break;
+                }
+              }
+            }
+            done = true;
+          } else {
+            need -= ct;
+          }
+        }
       }
     }
+    __syncthreads();
+    y = s_y;
   }
+  if (y < 0) y = w.dn.argmax;
+  if (threadIdx.x == 0) fl_write_row(a, r, a.mode == 0 ? 0 : w.n, y);
 }
 
 static size_t fl_align(size_t b) { return (b + 255) & ~size_t(255); }
@@ -3581,7 +3838,7 @@ static size_t fl_align(size_t b) { return (b + 255) & ~size_t(255); }
 size_t flat_workspace_bytes(int rows, int tasks) {
   const size_t T = (size_t)tasks, R = (size_t)rows, P = kFlatMaxParts;
   return fl_align(sizeof(TDesc) * T) + fl_align(8 * T * P) + fl_align(4 * T * P) + fl_align(8 * T * kFlatHistBins) +
-         fl_align(8 * T) + fl_align(4 * T) + 2 * fl_align(4 * T * kFlatCandCap) + fl_align(16 * R * P) +
+         fl_align(8 * T) + fl_align(4 * T) + 2 * fl_align(4 * T * kFlatCandCap) + fl_align(16 * R * P * (kST / 32)) +
          fl_align(4 * R) + fl_align(4 * T) + fl_align(4 * R);
 }
 
@@ -3594,10 +3851,17 @@ bool flat_fits(const RowParams* p, int rows, int V, const float* logits, long lo
 
 bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!ws || ws_bytes < flat_workspace_bytes(a.rows, a.tasks) || a.depth + 1 > 32) return false;
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15) != 0) return false;
   const int sms = device_sm_count();
-  int P = 2 * sms / a.tasks;
-  P = std::max(1, std::min({P, kFlatMaxParts, a.V / 2048}));
-  a.P = P;
+  a.nsr = 0;
+  for (int r = 0; r < a.rows; ++r)
+    if (!a.p[r].greedy) a.srow[a.nsr++] = r;
+  const int nst = a.nsr * (a.mode == 0 ? 1 : a.depth + 1);
+  // parts per unit: about two CTAs per SM over the units that do the work
+  auto parts = [&](int units) { return std::max(1, std::min({2 * sms / std::max(units, 1), kFlatMaxParts, a.V / 2048})); };
+  a.P = parts(a.tasks);
+  a.Ps = parts(nst);
+  a.P2 = a.nsr ? parts(a.nsr) : 1;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t T = (size_t)a.tasks, R = (size_t)a.rows, PM = kFlatMaxParts;
   auto take = [&](size_t bytes) {
@@ -3613,15 +3877,13 @@ bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
   a.ccnt = reinterpret_cast<int32_t*>(take(4 * T));
   a.ckey = reinterpret_cast<uint32_t*>(take(4 * T * kFlatCandCap));
   a.cid = reinterpret_cast<int32_t*>(take(4 * T * kFlatCandCap));
-  a.wsum = reinterpret_cast<unsigned long long*>(take(16 * R * PM));
+  a.wsum = reinterpret_cast<unsigned long long*>(take(16 * R * PM * (kST / 32)));
   a.nstop = reinterpret_cast<int32_t*>(take(4 * R));
   a.gcnt = reinterpret_cast<int32_t*>(take(4 * T));
   a.scnt = reinterpret_cast<int32_t*>(take(4 * R));
-  const int per = fl_per(a.V, P);
   const size_t base = (sizeof(SampleSmem) + 15) & ~size_t(15);
-  const size_t bits_part = 4 * (size_t)((per + 31) / 32 + 1);
-  const size_t sm_part = base + bits_part;
-  const size_t sm_hist = ((base + bits_part + 15) & ~size_t(15)) + 8 * (size_t)kFlatBins;
+  auto sm_part = [&](int P) { return base + 4 * (size_t)((fl_per(a.V, P) + 31) / 32 + 1); };
+  const size_t sm_hist = fl_hist_off(fl_per(a.V, a.Ps)) + 8 * (size_t)kFlatBins;
   const size_t sm_res = base + 12 * (size_t)kFlatCandCap + 4 * (size_t)((a.V + 31) / 32 + 1);
   if (sm_res > 226 * 1024 || sm_hist > 226 * 1024) return false;
   {
@@ -3638,12 +3900,15 @@ bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
       done[dev] = true;
     }
   }
-  const dim3 parts(P, a.tasks), rowsP(P, a.rows);
-  launch_pdl(k_fl_stats, parts, dim3(kST), sm_part, s, a);
-  launch_pdl(k_fl_hist, parts, dim3(kST), sm_hist, s, a);
-  launch_pdl(k_fl_gather, parts, dim3(kST), std::max(sm_part, sm_res), s, a);
-  launch_pdl(k_fl_sums, rowsP, dim3(kST), sm_part, s, a);
-  count_launch(4);
+  launch_pdl(k_fl_stats, dim3(a.P, a.tasks), dim3(kST), sm_part(a.P), s, a);
+  int n = 1;
+  if (nst > 0) {
+    launch_pdl(k_fl_hist, dim3(a.Ps, nst), dim3(kST), sm_hist, s, a);
+    launch_pdl(k_fl_gather, dim3(a.Ps, nst), dim3(kST), std::max(sm_part(a.Ps), sm_res), s, a);
+    n += 2;
+  }
+  launch_pdl(k_fl_sums, dim3(a.P2, a.rows), dim3(kST), sm_part(a.P2), s, a);
+  count_launch(n + 1);
   return true;
 }
 
