@@ -283,6 +283,7 @@ struct FlatArgs {
   unsigned long long* amax;  // [tasks][P]
   float* zmin;               // [tasks][P]
   unsigned long long* hist_w;  // [tasks][kFlatHistBins]
+  unsigned long long* sub_w;   // [tasks][kFlatHistBins] mass per sub-bin of the crossing bin
   unsigned long long* sminp;   // [tasks]
   int32_t* ccnt;             // [tasks]
   uint32_t* ckey;            // [tasks][kFlatCandCap]

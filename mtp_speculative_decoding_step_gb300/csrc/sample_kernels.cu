@@ -2901,6 +2901,31 @@ __device__ __forceinline__ int fl_bin(const FlScale& s, float z) {
   return t < (float)kFlatBins ? (int)t : kFlatBins;  // beyond the span (and NaN): no bin
 }
 
+// Sub-bins of bin b: its order keys (from a little above its top value to a
+// little below its bottom one) cut into kFlatBins equal ranges of 2^sh keys.
+// sub_of is monotone in the key (clamped at both ends), so the sub-bins keep
+// the (key asc) order whatever the rounding of the bin edges.
+struct FlSub {
+  uint32_t k0;
+  int sh;
+};
+__device__ __forceinline__ FlSub fl_sub(const FlScale& s, int b) {
+  const float zt = s.mx - (float)b / s.scale, zb = s.mx - (float)(b + 1) / s.scale;
+  const float top = zt + fabsf(zt) * 1e-6f + 1e-30f, bot = zb - fabsf(zb) * 1e-6f - 1e-30f;
+  FlSub u;
+  u.k0 = desc_key(top);
+  const uint32_t k1 = desc_key(bot);
+  const uint32_t span = k1 > u.k0 ? k1 - u.k0 : 1u;
+  const int nb = 32 - __clz(span);
+  u.sh = nb > 11 ? nb - 11 : 0;
+  return u;
+}
+__device__ __forceinline__ int fl_sub_of(const FlSub& u, uint32_t key) {
+  if (key <= u.k0) return 0;
+  const uint32_t q = (key - u.k0) >> u.sh;
+  return q < (uint32_t)kFlatBins ? (int)q : kFlatBins - 1;
+}
+
 // The crossing of a task's histogram: total mass SE, the bin b in which the
 // running mass reaches target = ceil(top_p SE) (b = -1 when SE is 0) and the
 // mass still needed there.
@@ -2979,7 +3004,10 @@ __global__ void __launch_bounds__(kST) k_fl_stats(const __grid_constant__ FlatAr
   const FlTask k = fl_task(a, t);
   const RowParams rp = a.p[k.r];
   // this task's share of the scratch the next kernels accumulate into
-  for (int b = p * kST + threadIdx.x; b < kFlatBins; b += a.P * kST) a.hist_w[(size_t)t * kFlatBins + b] = 0ull;
+  for (int b = p * kST + threadIdx.x; b < kFlatBins; b += a.P * kST) {
+    a.hist_w[(size_t)t * kFlatBins + b] = 0ull;
+    a.sub_w[(size_t)t * kFlatBins + b] = 0ull;
+  }
   if (p == 0 && threadIdx.x == 0) {
     a.sminp[t] = 0ull;
     a.ccnt[t] = 0;
@@ -3048,6 +3076,15 @@ __device__ __forceinline__ void fl_bin_add(uint32_t* lo, uint32_t* hi, int b, un
   const uint32_t old = atomicAdd(&lo[b], wl);
   const uint32_t c = old + wl < old ? 1u : 0u;
   if (wh + c) atomicAdd(&hi[b], wh + c);
+}
+// The gather's sub-bin histogram: after the resolve's layout (SampleSmem, the
+// candidate list, its tie buffer and a bitmap of the whole row) and after the
+// part's bitmap.
+__host__ __device__ __forceinline__ size_t fl_sub_off(int V, int per) {
+  const size_t base = (sizeof(SampleSmem) + 15) & ~size_t(15);
+  const size_t res = base + 12 * (size_t)kFlatCandCap + 4 * (size_t)((V + 31) / 32 + 1);
+  const size_t part = base + 4 * (size_t)((per + 31) / 32 + 1);
+  return ((res > part ? res : part) + 15) & ~size_t(15);
 }
 __host__ __device__ __forceinline__ size_t fl_hist_off(int per) {
   return (((sizeof(SampleSmem) + 15) & ~size_t(15)) + 4 * (size_t)((per + 31) / 32 + 1) + 15) & ~size_t(15);
@@ -3156,6 +3193,13 @@ __global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatA
     const int lane = threadIdx.x & 31;
     uint32_t* ckey = a.ckey + (size_t)t * kFlatCandCap;
     int32_t* cid = a.cid + (size_t)t * kFlatCandCap;
+    // the crossing bin's mass per sub-bin (its elements are few: a sparse
+    // shared histogram, flushed where non-zero)
+    const FlSub su = fl_sub(sc, bstar);
+    uint32_t* slo = reinterpret_cast<uint32_t*>(dyn + fl_sub_off(a.V, per));
+    uint32_t* shi = slo + kFlatBins;
+    for (int b = threadIdx.x; b < 2 * kFlatBins; b += kST) slo[b] = 0u;
+    __syncthreads();
     for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
       if (b0 > 0) fl_load4(l4, b0, n4, xb);
 #pragma unroll
@@ -3187,14 +3231,22 @@ __global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatA
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if ((mm >> e) & 1u) {
+              const uint32_t key = desc_key(zz[e]);
               if (pos < kFlatCandCap) {
-                ckey[pos] = desc_key(zz[e]);
+                ckey[pos] = key;
                 cid[pos] = v0 + 4 * j4 + e;
               }
               ++pos;
+              const unsigned long long w = to_fix(expf(zz[e] - sc.mx));
+              if (w) fl_bin_add(slo, shi, fl_sub_of(su, key), w);
             }
         }
       }
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < kFlatBins; b += kST) {
+      const unsigned long long v = ((unsigned long long)shi[b] << 32) + slo[b];
+      if (v) atomicAdd(&a.sub_w[(size_t)t * kFlatBins + b], v);
     }
   }
   // the last of the task's CTAs to finish resolves its descriptor
@@ -3342,6 +3394,186 @@ __device__ void fl_exact_cut(SampleSmem* sm, int V, Z zof, const FlScale& sc, in
   cutout = cut;
 }
 
+// Every thread of the block (warp 0 holds the entries): of n <= 32 entries
+// with distinct ids, one per lane of warp 0 (have), the one where the running
+// weight in (key asc, id asc) order first reaches need. Returns false when no
+// entry is found; else *K, *cut and *in_w (the weight of the entries up to
+// and including it).
+template <class Wk>
+__device__ bool fl_warp_cross(bool have, uint32_t kk, int ii, int n, unsigned long long need, Wk wk, uint32_t* K,
+                              int* cut, unsigned long long* in_w, int* s_ok, uint32_t* s_K, int* s_cut,
+                              unsigned long long* s_in) {
+  if (threadIdx.x == 0) *s_ok = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (!have) {
+      kk = 0xFFFFFFFFu;
+      ii = 0x7FFFFFFF;
+    }
+    const unsigned long long ww = have ? wk(kk) : 0ull;
+    unsigned long long before = 0;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t kj = __shfl_sync(0xFFFFFFFFu, kk, j);
+      const int ij = __shfl_sync(0xFFFFFFFFu, ii, j);
+      const unsigned long long wj = __shfl_sync(0xFFFFFFFFu, ww, j);
+      if (kj < kk || (kj == kk && ij < ii)) before += wj;
+    }
+    if (have && ww > 0 && before < need && need <= before + ww) {  // exactly one entry
+      *s_K = kk;
+      *s_cut = ii;
+      *s_in = before + ww;
+      *s_ok = 1;
+    }
+  }
+  __syncthreads();
+  const bool ok = *s_ok != 0;
+  if (ok) {
+    *K = *s_K;
+    *cut = *s_cut;
+    *in_w = *s_in;
+  }
+  __syncthreads();
+  return ok;
+}
+
+// Every thread of the block, from its kFlPer bins of a histogram: the bin b
+// where the running mass reaches need (out->b = -1 when it does not) and the
+// mass still needed there, into *out (shared memory). One block scan.
+__device__ __forceinline__ void fl_reach(SampleSmem* sm, const unsigned long long (&v)[kFlPer],
+                                         unsigned long long need, FlCross* out) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned long long s = 0;
+#pragma unroll
+  for (int b = 0; b < kFlPer; ++b) s += v[b];
+  unsigned long long incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) sm->wsum[w] = incl;
+  if (threadIdx.x == 0) out->b = -1;
+  __syncthreads();
+  unsigned long long cum = incl - s;
+  for (int q = 0; q < w; ++q) cum += sm->wsum[q];
+  if (cum < need && need <= cum + s) {
+#pragma unroll
+    for (int b = 0; b < kFlPer; ++b) {
+      if (cum < need && need <= cum + v[b]) {
+        out->b = threadIdx.x * kFlPer + b;
+        out->need = need - cum;
+        break;
+      }
+      cum += v[b];
+    }
+  }
+  __syncthreads();
+}
+
+// One CTA: of up to 2 kST (key, id) entries with distinct ids (cnt of them
+// in key[], id[] of global memory), the entry where the running weight in
+// (key asc, id asc) order first reaches need, weight(key) being each entry's
+// fixed-point weight. A bitonic sort over the block (two entries per thread;
+// shuffles below a warp's span, shared memory above), then a block scan of
+// the weights. Returns false when no entry is found; else *K, *cut (the
+// entry) and *in_w (the weight of the entries up to and including it).
+template <class Wk>
+__device__ bool fl_sorted_cross(const uint32_t* gkey, const int32_t* gid, int cnt, unsigned long long need, Wk wk,
+                                uint32_t* sk, int* si, unsigned long long* wsum, uint32_t* K, int* cut,
+                                unsigned long long* in_w, int* s_ok, uint32_t* s_K, int* s_cut,
+                                unsigned long long* s_in) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  uint32_t k[2];
+  int id[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int i = 2 * t + e;
+    const bool real = i < cnt;
+    k[e] = real ? __ldcg(gkey + i) : 0xFFFFFFFFu;
+    id[e] = real ? __ldcg(gid + i) : 0x7FFFFFFF - (2 * kST - 1) + i;  // distinct, above every vocabulary id
+  }
+#pragma unroll
+  for (int size = 2; size <= 2 * kST; size <<= 1) {
+    const bool asc = ((2 * t) & size) == 0;
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride == 1) {
+        if (pair_gt(k[0], id[0], k[1], id[1]) == asc) {
+          const uint32_t tk = k[0]; k[0] = k[1]; k[1] = tk;
+          const int ti = id[0]; id[0] = id[1]; id[1] = ti;
+        }
+        continue;
+      }
+      uint32_t ok[2];
+      int oi[2];
+      if (stride < 64) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          ok[e] = __shfl_xor_sync(0xFFFFFFFFu, k[e], stride >> 1);
+          oi[e] = __shfl_xor_sync(0xFFFFFFFFu, id[e], stride >> 1);
+        }
+      } else {
+        __syncthreads();
+        sk[2 * t] = k[0]; sk[2 * t + 1] = k[1];
+        si[2 * t] = id[0]; si[2 * t + 1] = id[1];
+        __syncthreads();
+        const int pt = t ^ (stride >> 1);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          ok[e] = sk[2 * pt + e];
+          oi[e] = si[2 * pt + e];
+        }
+      }
+      const bool low = ((2 * t) & stride) == 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool other_less = pair_gt(k[e], id[e], ok[e], oi[e]);
+        if (low == asc ? other_less : !other_less) {
+          k[e] = ok[e];
+          id[e] = oi[e];
+        }
+      }
+    }
+  }
+  // entries 2t, 2t+1 in order: their weights and the block's running weight
+  unsigned long long wt[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) wt[e] = 2 * t + e < cnt ? wk(k[e]) : 0ull;
+  const unsigned long long mine = wt[0] + wt[1];
+  unsigned long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  __syncthreads();
+  if (lane == 31) wsum[w] = incl;
+  if (t == 0) *s_ok = 0;
+  __syncthreads();
+  unsigned long long before = incl - mine;
+  for (int q = 0; q < w; ++q) before += wsum[q];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    if (wt[e] > 0 && before < need && need <= before + wt[e]) {  // exactly one entry
+      *s_K = k[e];
+      *s_cut = id[e];
+      *s_in = before + wt[e];
+      *s_ok = 1;
+    }
+    before += wt[e];
+  }
+  __syncthreads();
+  const bool ok = *s_ok != 0;
+  if (ok) {
+    *K = *s_K;
+    *cut = *s_cut;
+    *in_w = *s_in;
+  }
+  __syncthreads();
+  return ok;
+}
+
 // One CTA: the descriptor of a sampled task t (shared memory laid out as
 // SampleSmem, then the candidate list, its tie buffer and a bitmap of the
 // whole row). sc_in and cr_in: the scale and crossing the calling CTA already
@@ -3397,49 +3629,55 @@ __device__ void fl_resolve_task(const FlatArgs& a, int t, unsigned char* dyn, co
     }
     bool ok = false;
     if (cnt >= 1 && cnt <= 32) {
-      // a short list: warp 0, one entry per lane; the weight of the entries
-      // before each one in (key, id) order, and the entry where it crosses
-      if (threadIdx.x == 0) s_ok = 0;
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const bool have = lane < cnt;
-        const uint32_t kk = have ? k0 : 0xFFFFFFFFu;
-        const int ii = have ? i0 : 0x7FFFFFFF;
-        const unsigned long long ww = have ? wk(kk) : 0ull;
-        unsigned long long before = 0;
-        for (int j = 0; j < cnt; ++j) {
-          const uint32_t kj = __shfl_sync(0xFFFFFFFFu, kk, j);
-          const int ij = __shfl_sync(0xFFFFFFFFu, ii, j);
-          const unsigned long long wj = __shfl_sync(0xFFFFFFFFu, ww, j);
-          if (kj < kk || (kj == kk && ij < ii)) before += wj;
-        }
-        if (have && before < need && need <= before + ww) {  // exactly one entry
-          s_K = kk;
-          s_cut = ii;
-          s_in = before + ww;
-          s_ok = 1;
-        }
-      }
-      __syncthreads();
-      ok = s_ok != 0;
-      if (ok) {
-        K = s_K;
-        cut = s_cut;
-        in_bin = s_in;
-      }
+      // a short list: warp 0, one entry per lane
+      ok = fl_warp_cross(threadIdx.x < 32 && lane < cnt, k0, i0, cnt, need, wk, &K, &cut, &in_bin, &s_ok, &s_K,
+                         &s_cut, &s_in);
     } else if (cnt > 32 && cnt <= kFlatCandCap) {
-      for (int q = threadIdx.x; q < cnt; q += kST) {
-        mk[q] = __ldcg(&a.ckey[(size_t)t * kFlatCandCap + q]);
-        mi[q] = __ldcg(&a.cid[(size_t)t * kFlatCandCap + q]);
+      // the crossing sub-bin of the gather's sub-histogram, then that
+      // sub-bin's entries of the list (typically a few) on warp 0
+      static_assert(kFlatCandCap <= 2 * kST, "two list entries per thread");
+      unsigned long long sv[kFlPer];
+      fl_bins_load(a.sub_w + (size_t)t * kFlatBins, sv);
+      uint32_t ek[2];
+      int ei[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int q = 2 * threadIdx.x + e;
+        ek[e] = q < cnt ? __ldcg(&a.ckey[(size_t)t * kFlatCandCap + q]) : 0xFFFFFFFFu;
+        ei[e] = q < cnt ? __ldcg(&a.cid[(size_t)t * kFlatCandCap + q]) : -1;
       }
+      FlCross& sc2 = s_cr;  // reused: the calling CTA's crossing was read above
       __syncthreads();
-      ok = list_select(sm, mk, mi, cnt, need, wk, tie, kFlatCandCap, K, cut);
-      if (ok) {
-        unsigned long long loc = 0;
-        for (int q = threadIdx.x; q < cnt; q += kST)
-          if (in_prefix(mk[q], mi[q], K, cut)) loc += wk(mk[q]);
-        in_bin = block_sum_u64(loc, sm->wsum);
+      fl_reach(sm, sv, need, &sc2);
+      const int sstar = sc2.b;
+      if (sstar >= 0) {
+        const unsigned long long need2 = sc2.need;
+        const FlSub su = fl_sub(sc, bstar);
+        if (threadIdx.x == 0) sm->ccount = 0;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (ei[e] >= 0 && fl_sub_of(su, ek[e]) == sstar) {
+            const int pos = atomicAdd(&sm->ccount, 1);
+            if (pos < 32) {
+              mk[pos] = ek[e];
+              mi[pos] = ei[e];
+            }
+          }
+        __syncthreads();
+        const int c2 = sm->ccount;
+        if (c2 >= 1 && c2 <= 32) {
+          const bool have = threadIdx.x < 32 && lane < c2;
+          const uint32_t kk = have ? mk[lane] : 0xFFFFFFFFu;
+          const int ii = have ? mi[lane] : 0x7FFFFFFF;
+          unsigned long long in2 = 0;
+          ok = fl_warp_cross(have, kk, ii, c2, need2, wk, &K, &cut, &in2, &s_ok, &s_K, &s_cut, &s_in);
+          if (ok) in_bin = (need - need2) + in2;
+        }
       }
+      if (!ok)
+        ok = fl_sorted_cross(a.ckey + (size_t)t * kFlatCandCap, a.cid + (size_t)t * kFlatCandCap, cnt, need, wk, mk,
+                             mi, sm->wsum, &K, &cut, &in_bin, &s_ok, &s_K, &s_cut, &s_in);
     }
     if (!ok) {
       load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
@@ -3837,7 +4075,7 @@ static size_t fl_align(size_t b) { return (b + 255) & ~size_t(255); }
 
 size_t flat_workspace_bytes(int rows, int tasks) {
   const size_t T = (size_t)tasks, R = (size_t)rows, P = kFlatMaxParts;
-  return fl_align(sizeof(TDesc) * T) + fl_align(8 * T * P) + fl_align(4 * T * P) + fl_align(8 * T * kFlatHistBins) +
+  return fl_align(sizeof(TDesc) * T) + fl_align(8 * T * P) + fl_align(4 * T * P) + 2 * fl_align(8 * T * kFlatHistBins) +
          fl_align(8 * T) + fl_align(4 * T) + 2 * fl_align(4 * T * kFlatCandCap) + fl_align(16 * R * P * (kST / 32)) +
          fl_align(4 * R) + fl_align(4 * T) + fl_align(4 * R);
 }
@@ -3873,6 +4111,7 @@ bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
   a.amax = reinterpret_cast<unsigned long long*>(take(8 * T * PM));
   a.zmin = reinterpret_cast<float*>(take(4 * T * PM));
   a.hist_w = reinterpret_cast<unsigned long long*>(take(8 * T * kFlatHistBins));
+  a.sub_w = reinterpret_cast<unsigned long long*>(take(8 * T * kFlatHistBins));
   a.sminp = reinterpret_cast<unsigned long long*>(take(8 * T));
   a.ccnt = reinterpret_cast<int32_t*>(take(4 * T));
   a.ckey = reinterpret_cast<uint32_t*>(take(4 * T * kFlatCandCap));
@@ -3884,8 +4123,7 @@ bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
   const size_t base = (sizeof(SampleSmem) + 15) & ~size_t(15);
   auto sm_part = [&](int P) { return base + 4 * (size_t)((fl_per(a.V, P) + 31) / 32 + 1); };
   const size_t sm_hist = fl_hist_off(fl_per(a.V, a.Ps)) + 8 * (size_t)kFlatBins;
-  const size_t sm_res = base + 12 * (size_t)kFlatCandCap + 4 * (size_t)((a.V + 31) / 32 + 1);
-  if (sm_res > 226 * 1024 || sm_hist > 226 * 1024) return false;
+  if (fl_sub_off(a.V, fl_per(a.V, a.Ps)) + 8 * (size_t)kFlatBins > 226 * 1024 || sm_hist > 226 * 1024) return false;
   {
     // the kernels' dynamic shared memory limit, raised once per device
     static std::mutex mu;
@@ -3904,7 +4142,8 @@ bool launch_flat(FlatArgs a, void* ws, size_t ws_bytes, cudaStream_t s) {
   int n = 1;
   if (nst > 0) {
     launch_pdl(k_fl_hist, dim3(a.Ps, nst), dim3(kST), sm_hist, s, a);
-    launch_pdl(k_fl_gather, dim3(a.Ps, nst), dim3(kST), std::max(sm_part(a.Ps), sm_res), s, a);
+    launch_pdl(k_fl_gather, dim3(a.Ps, nst), dim3(kST), fl_sub_off(a.V, fl_per(a.V, a.Ps)) + 8 * (size_t)kFlatBins,
+               s, a);
     n += 2;
   }
   launch_pdl(k_fl_sums, dim3(a.P2, a.rows), dim3(kST), sm_part(a.P2), s, a);

@@ -136,7 +136,8 @@ def test_workspace_holds_the_largest_path_layout():
     #    two kept-list arrays of 256 entries per (row, position);
     #  - greedy stream: one 64-bit key per (range, segment), ranges <= 2048;
     #  - flat transform: descriptors, 64 part slots (8 + 4 bytes) per task, a
-    #    2048-bin fixed-point histogram, the min-p mass and two counters per
+    #    2048-bin fixed-point histogram and a 2048-bin one of the crossing bin's
+    #    sub-bins, the min-p mass and two counters per
     #    task, a 1024-entry crossing-bin list (key, id), 64 parts x 16 warp
     #    slices of sums (2 x 8 bytes) and two counters per row
     al = lambda b: (b + 255) // 256 * 256
@@ -144,7 +145,7 @@ def test_workspace_holds_the_largest_path_layout():
         tasks = rows * (depth + 1)
         lists = al(32 * tasks) + al(4 * tasks) + 2 * al(4 * tasks * 256)
         keys = al(8 * (tasks + 2048))
-        flat = (al(32 * tasks) + al(8 * tasks * 64) + al(4 * tasks * 64) + al(8 * tasks * 2048) + al(8 * tasks)
+        flat = (al(32 * tasks) + al(8 * tasks * 64) + al(4 * tasks * 64) + 2 * al(8 * tasks * 2048) + al(8 * tasks)
                 + al(4 * tasks) + 2 * al(4 * tasks * 1024) + al(16 * rows * 64 * 16) + al(4 * rows) + al(4 * tasks)
                 + al(4 * rows))
         assert m.spec_verify_workspace_bytes(rows, depth, 152064) == max(lists, keys, flat), (rows, depth)
