@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmtp.so")
 SOURCES = ("mtp_api.cu", "head_kernels.cu", "sample_kernels.cu", "flush_gemm.cu", "gemv_tc.cu", "depth_ctl.cu", "verify_noalloc.cu",
-           "verify_flat.cu")
+           "verify_flat.cu", "attn_mma.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "--extended-lambda"]

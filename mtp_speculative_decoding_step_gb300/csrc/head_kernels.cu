@@ -944,17 +944,26 @@ static void attn_t(const AttnArgs& a0, int sms, cudaStream_t s) {
     }
     per_sm = resident[dev];
   }
-  // slots per block: the smallest whole number of 64-slot units (never below
-  // kAttnChunk, the partial buffers' unit) whose blocks all fit one wave of
-  // the resident blocks; a wave more would cost a whole block's time for a few
   AttnArgs a = a0;
+  a.chunk = attn_chunk_slots(a, (long long)per_sm * sms);
+  int maxL = 0;
+  for (int m = 0; m < a.Mh; ++m) maxL = max(maxL, a.slot[m] + 1);
+  const int nch = (maxL + a.chunk - 1) / a.chunk;
+  launch_pdl(k, dim3(nch, a.nkv, a.Mh), dim3(256), smem, s, a);
+  count_launch();
+  launch_attn_merge(a, s);
+}
+
+// Slots per block: the smallest whole number of 64-slot units (never below
+// kAttnChunk, the partial buffers' unit) whose blocks all fit one wave of the
+// resident blocks; a wave more would cost a whole block's time for a few.
+int attn_chunk_slots(const AttnArgs& a, long long slots) {
   long long total = 0;
   int maxL = 0;
   for (int m = 0; m < a.Mh; ++m) {
     total += a.slot[m] + 1;
     maxL = max(maxL, a.slot[m] + 1);
   }
-  const long long slots = (long long)per_sm * sms;
   auto blocks = [&](int chunk) {
     long long b = 0;
     for (int m = 0; m < a.Mh; ++m) b += (a.slot[m] + chunk) / chunk;
@@ -963,14 +972,19 @@ static void attn_t(const AttnArgs& a0, int sms, cudaStream_t s) {
   int chunk = (int)(((total * a.nkv + slots - 1) / slots + 63) / 64 * 64);
   if (chunk < kAttnChunk) chunk = kAttnChunk;
   while (chunk < maxL && blocks(chunk) > slots) chunk += 64;
-  a.chunk = chunk;
-  const int nch = (maxL + chunk - 1) / chunk;
-  launch_pdl(k, dim3(nch, a.nkv, a.Mh), dim3(256), smem, s, a);
-  launch_pdl(k_attn_merge<DH>, dim3(a.nq, a.Mh), dim3(DH), (size_t)a.max_chunks * sizeof(float), s, a);
-  count_launch(2);
+  return chunk;
+}
+
+void launch_attn_merge(const AttnArgs& a, cudaStream_t s) {
+  const size_t smem = (size_t)a.max_chunks * sizeof(float);
+  if (a.dh == 256) launch_pdl(k_attn_merge<256>, dim3(a.nq, a.Mh), dim3(256), smem, s, a);
+  else if (a.dh == 128) launch_pdl(k_attn_merge<128>, dim3(a.nq, a.Mh), dim3(128), smem, s, a);
+  else launch_pdl(k_attn_merge<64>, dim3(a.nq, a.Mh), dim3(64), smem, s, a);
+  count_launch();
 }
 
 void launch_attention(const AttnArgs& a, int sms, cudaStream_t s) {
+  if (launch_attention_mma(a, sms, s)) return;
   const int G = a.nq / a.nkv;
   const bool bf = a.wdt == MTP_DTYPE_BF16;
 #define MTP_ATTN_CASE(DHV, GV)                                                \

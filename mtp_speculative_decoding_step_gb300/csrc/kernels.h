@@ -191,6 +191,13 @@ struct AttnArgs {
   int slot[kMaxRows];
 };
 void launch_attention(const AttnArgs& a, int sms, cudaStream_t s);
+// The tensor-core instance (bf16 cache, head dim 128 or 256, at most 8 query
+// heads per KV head); false, with nothing launched, for any other shape.
+bool launch_attention_mma(const AttnArgs& a, int sms, cudaStream_t s);
+// Slots per attention block for `slots` resident blocks, and the merge of the
+// blocks' partial outputs.
+int attn_chunk_slots(const AttnArgs& a, long long slots);
+void launch_attn_merge(const AttnArgs& a, cudaStream_t s);
 
 // Copy a norm vector to fp32 adding `shift`.
 void launch_norm_copy(const void* src, int dt, int n, float shift, float* dst, cudaStream_t s);
