@@ -2980,13 +2980,29 @@ __device__ void fl_cross(SampleSmem* sm, const unsigned long long (&v)[kFlPer], 
   __syncthreads();
 }
 
-// Loads of batch b0 of a part: four 16-byte vectors per thread, kST apart.
-__device__ __forceinline__ void fl_load4(const float4* l4, int b0, int n4, float4 (&xb)[4]) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int j4 = b0 + u * kST + threadIdx.x;
-    if (j4 < n4) xb[u] = __ldg(l4 + j4);
+// A rolled pass over one thread's 16-byte items j4 = t0 + u * stride, u < nu
+// (nu the same for every thread that takes part, so the body may hold warp
+// collectives), with the next two items' loads in flight. The body is one
+// copy of the per-item code, which stays in the instruction cache across
+// iterations; the kernels here run it a few times per launch, where an
+// unrolled copy per item would be fetched cold each time. first: item u = 0.
+template <class F>
+__device__ __forceinline__ void fl_rolled(const float4* p, int t0, int stride, int n4, int nu, float4 first,
+                                          F&& body) {
+  float4 a = first, b = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (t0 + stride < n4) b = __ldg(p + t0 + stride);
+#pragma unroll 1
+  for (int u = 0; u < nu; ++u) {
+    const int j4 = t0 + u * stride;
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j4 + 2 * stride < n4) c = __ldg(p + j4 + 2 * stride);
+    body(a, j4, j4 < n4);
+    a = b;
+    b = c;
   }
+}
+__device__ __forceinline__ float4 fl_first(const float4* p, int j4, int n4) {
+  return j4 < n4 ? __ldg(p + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __device__ __forceinline__ size_t fl_bits_off() { return (sizeof(SampleSmem) + 15) & ~size_t(15); }
@@ -3026,29 +3042,18 @@ __global__ void __launch_bounds__(kST) k_fl_stats(const __grid_constant__ FlatAr
   float mn = INFINITY, nf = 0.f;
   const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
   const int n4 = n / 4;
-  for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
-    float4 xb[4];
+  fl_rolled(l4, threadIdx.x, kST, n4, (n4 - (int)threadIdx.x + kST - 1) / kST, fl_first(l4, threadIdx.x, n4),
+            [&](const float4& x, int j4, bool valid) {
+              const float xs[4] = {x.x, x.y, x.z, x.w};
+              const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * kST + threadIdx.x;
-      if (j4 < n4) xb[u] = __ldg(l4 + j4);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * kST + threadIdx.x;
-      if (j4 < n4) {
-        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-        const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          nf = fmaf(xs[e], 0.f, nf);
-          const float z = ((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e];
-          if (z > bz[e]) { bz[e] = z; bzi[e] = v0 + 4 * j4 + e; }
-          mn = fminf(mn, z);
-        }
-      }
-    }
-  }
+              for (int e = 0; e < 4; ++e) {
+                nf = fmaf(xs[e], 0.f, nf);
+                const float z = ((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e];
+                if (z > bz[e]) { bz[e] = z; bzi[e] = v0 + 4 * j4 + e; }
+                mn = fminf(mn, z);
+              }
+            });
   float bv = bz[0];
   int bi = bzi[0];
 #pragma unroll
@@ -3107,8 +3112,7 @@ __global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArg
   const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
   const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
   const int n4 = n / 4;
-  float4 xb[4];
-  fl_load4(l4, 0, n4, xb);
+  const float4 x0 = fl_first(l4, threadIdx.x, n4);
   for (int b = threadIdx.x; b < 2 * kFlatBins; b += kST) lo[b] = 0u;
   load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
   const bool pen = rp.rep_penalty != 1.f;
@@ -3118,30 +3122,24 @@ __global__ void __launch_bounds__(kST) k_fl_hist(const __grid_constant__ FlatArg
   const FlScale sc = fl_scale(a, t, rp);
   const bool minp = rp.min_p > 0.f;
   unsigned long long smp = 0ull;
-  for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
-    if (b0 > 0) fl_load4(l4, b0, n4, xb);
+  fl_rolled(l4, threadIdx.x, kST, n4, (n4 - (int)threadIdx.x + kST - 1) / kST, x0,
+            [&](const float4& x, int j4, bool valid) {
+              const float xs[4] = {x.x, x.y, x.z, x.w};
+              const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * kST + threadIdx.x;
-      if (j4 < n4) {
-        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-        const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float z = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
-          const int b = fl_bin(sc, z);
-          if (b < kFlatBins) {
-            const float ev = expf(z - sc.mx);
-            const unsigned long long w = to_fix(ev);
-            if (w) {
-              fl_bin_add(lo, hi, b, w);
-              if (minp && ev >= rp.min_p) smp += w;
-            }
-          }
-        }
-      }
-    }
-  }
+              for (int e = 0; e < 4; ++e) {
+                const float z = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
+                const int b = fl_bin(sc, z);
+                if (b < kFlatBins) {
+                  const float ev = expf(z - sc.mx);
+                  const unsigned long long w = to_fix(ev);
+                  if (w) {
+                    fl_bin_add(lo, hi, b, w);
+                    if (minp && ev >= rp.min_p) smp += w;
+                  }
+                }
+              }
+            });
   __syncthreads();
   for (int b = threadIdx.x; b < kFlatBins; b += kST) {
     const unsigned long long v = ((unsigned long long)hi[b] << 32) + lo[b];
@@ -3176,8 +3174,7 @@ __global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatA
   const int v0 = min(p * per, a.V), n = min(per, a.V - v0);
   const float4* l4 = reinterpret_cast<const float4*>(k.lg + v0);
   const int n4 = n / 4;
-  float4 xb[4];
-  fl_load4(l4, 0, n4, xb);
+  const float4 x0 = fl_first(l4, threadIdx.x, n4);
   load_window(sm, a.hist + (size_t)k.r * a.W, a.W, a.drafts + (size_t)k.r * a.depth, k.i);
   const bool pen = rp.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
@@ -3200,49 +3197,45 @@ __global__ void __launch_bounds__(kST) k_fl_gather(const __grid_constant__ FlatA
     uint32_t* shi = slo + kFlatBins;
     for (int b = threadIdx.x; b < 2 * kFlatBins; b += kST) slo[b] = 0u;
     __syncthreads();
-    for (int b0 = 0; b0 < n4; b0 += 4 * kST) {
-      if (b0 > 0) fl_load4(l4, b0, n4, xb);
+    // every thread runs the block's largest item count (warp-uniform appends)
+    fl_rolled(l4, threadIdx.x, kST, n4, (n4 + kST - 1) / kST, x0, [&](const float4& x, int j4, bool valid) {
+      float zz[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t mm = 0u;  // elements of this vector in the crossing bin
+      if (valid) {
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j4 = b0 + u * kST + threadIdx.x;
-        float zz[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t mm = 0u;  // elements of this vector in the crossing bin
-        if (j4 < n4) {
-          const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-          const uint32_t wb = pen ? bits[j4 >> 3] >> ((4 * j4) & 31) : 0u;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            zz[e] = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
-            if (fl_bin(sc, zz[e]) == bstar) mm |= 1u << e;
-          }
-        }
-        if (__any_sync(0xFFFFFFFFu, mm != 0u)) {
-          // one list append per warp: exclusive scan of the lanes' counts
-          const int c = __popc(mm);
-          int incl = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += x;
-          }
-          int base = 0;
-          if (lane == 31) base = atomicAdd(&a.ccnt[t], incl);
-          int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if ((mm >> e) & 1u) {
-              const uint32_t key = desc_key(zz[e]);
-              if (pos < kFlatCandCap) {
-                ckey[pos] = key;
-                cid[pos] = v0 + 4 * j4 + e;
-              }
-              ++pos;
-              const unsigned long long w = to_fix(expf(zz[e] - sc.mx));
-              if (w) fl_bin_add(slo, shi, fl_sub_of(su, key), w);
-            }
+        for (int e = 0; e < 4; ++e) {
+          zz[e] = (((wb >> e) & 1u) ? penalize(xs[e], rp.rep_penalty) : xs[e]) / rp.temperature + 0.0f;
+          if (fl_bin(sc, zz[e]) == bstar) mm |= 1u << e;
         }
       }
-    }
+      if (__any_sync(0xFFFFFFFFu, mm != 0u)) {
+        // one list append per warp: exclusive scan of the lanes' counts
+        const int c = __popc(mm);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        int base = 0;
+        if (lane == 31) base = atomicAdd(&a.ccnt[t], incl);
+        int pos = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((mm >> e) & 1u) {
+            const uint32_t key = desc_key(zz[e]);
+            if (pos < kFlatCandCap) {
+              ckey[pos] = key;
+              cid[pos] = v0 + 4 * j4 + e;
+            }
+            ++pos;
+            const unsigned long long w = to_fix(expf(zz[e] - sc.mx));
+            if (w) fl_bin_add(slo, shi, fl_sub_of(su, key), w);
+          }
+      }
+    });
     __syncthreads();
     for (int b = threadIdx.x; b < kFlatBins; b += kST) {
       const unsigned long long v = ((unsigned long long)shi[b] << 32) + slo[b];
@@ -3807,48 +3800,50 @@ __global__ void __launch_bounds__(kST, 2) k_fl_sums(const __grid_constant__ Flat
   const float4* l4 = reinterpret_cast<const float4*>(w.lg + v0 + s0);
   const float4* q4 = w.qn ? reinterpret_cast<const float4*>(w.qn + v0 + s0) : nullptr;
   const int n4 = sn / 4;
-  float4 xb[4], qb[4];
-  auto load = [&](int b0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * 32 + lane;
-      if (j4 < n4) {
-        xb[u] = __ldg(l4 + j4);
-        qb[u] = q4 ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-  };
-  load(0);
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 xa = zero4, qa = zero4;
+  if (lane < n4) {
+    xa = __ldg(l4 + lane);
+    if (q4) qa = __ldg(q4 + lane);
+  }
   window_from(sm, s_hw, a.W, w.n);
   const bool pen = rp.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
-  // each warp sums its own slice (lanes read consecutive 16-byte vectors)
+  // each warp sums its own slice (lanes read consecutive 16-byte vectors); a
+  // rolled loop with the next vector in flight, one copy of the element code
   float4* o4 = a.mode == 0 ? reinterpret_cast<float4*>(a.q + ((size_t)r * a.depth + a.pos) * a.V + v0 + s0) : nullptr;
   unsigned long long wp = 0, wr = 0;
-  for (int b0 = 0; b0 < n4; b0 += 4 * 32) {
-    if (b0 > 0) load(b0);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j4 = b0 + u * 32 + lane;
-      if (j4 < n4) {
-        const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-        const float qs[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
-        const int jj = s0 + 4 * j4;  // index within the part
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int v = v0 + jj + e;
-          pv[e] = eval_p(w.dn, rp, xs[e], pen && bit(bits, jj + e), v);
-          wp += to_fix(pv[e]);
-          if (w.residual) {
-            const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qs[e];
-            const float rv = pv[e] - qv;
-            wr += to_fix(rv > 0.f ? rv : 0.f);
-          }
-        }
-        if (o4) o4[j4] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-      }
+  const int nu = (n4 - lane + 31) / 32;
+#pragma unroll 1
+  for (int u = 0; u < nu; ++u) {
+    const int j4 = lane + 32 * u;
+    float4 xn = zero4, qn = zero4;
+    if (j4 + 32 < n4) {
+      xn = __ldg(l4 + j4 + 32);
+      if (q4) qn = __ldg(q4 + j4 + 32);
     }
+    const int jj = s0 + 4 * j4;  // index within the part
+    float4 pv4 = zero4;
+#pragma unroll 1
+    for (int e = 0; e < 4; ++e) {
+      const float x = e == 0 ? xa.x : (e == 1 ? xa.y : (e == 2 ? xa.z : xa.w));
+      const float qx = e == 0 ? qa.x : (e == 1 ? qa.y : (e == 2 ? qa.z : qa.w));
+      const int v = v0 + jj + e;
+      const float pv = eval_p(w.dn, rp, x, pen && bit(bits, jj + e), v);
+      wp += to_fix(pv);
+      if (w.residual) {
+        const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qx;
+        const float rv = pv - qv;
+        wr += to_fix(rv > 0.f ? rv : 0.f);
+      }
+      if (e == 0) pv4.x = pv;
+      else if (e == 1) pv4.y = pv;
+      else if (e == 2) pv4.z = pv;
+      else pv4.w = pv;
+    }
+    if (o4) o4[j4] = pv4;
+    xa = xn;
+    qa = qn;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -3998,70 +3993,75 @@ __device__ void fl_pick_row(const FlatArgs& a, int r, unsigned char* dyn, const 
     const bool pen = rp.rep_penalty != 1.f;
     if (pen) build_bitmap(sm, bits, v0 + s0, sn);
     if (threadIdx.x < 32) {
-      // warp 0 walks the slice in chunks of 128 elements (four chunks'
-      // loads in flight): smallest id whose running weight reaches need
+      // warp 0 walks the slice in chunks of 128 elements (a rolled loop, the
+      // next chunk's loads in flight): smallest id whose running weight
+      // reaches need
       unsigned long long need = s_need;
       const float4* l4 = reinterpret_cast<const float4*>(w.lg + v0 + s0);
       const float4* q4 = w.qn ? reinterpret_cast<const float4*>(w.qn + v0 + s0) : nullptr;
       const int n4 = sn / 4;
-      bool done = false;
-      for (int b0 = 0; b0 < n4 && !done; b0 += 4 * 32) {
-        float4 xb[4], qb[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j4 = b0 + u * 32 + lane;
-          if (j4 < n4) {
-            xb[u] = __ldg(l4 + j4);
-            qb[u] = q4 ? __ldg(q4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 xa = zero4, qa = zero4;
+      if (lane < n4) {
+        xa = __ldg(l4 + lane);
+        if (q4) qa = __ldg(q4 + lane);
+      }
+#pragma unroll 1
+      for (int b0 = 0; b0 < n4; b0 += 32) {
+        const int j4 = b0 + lane;
+        float4 xn = zero4, qn = zero4;
+        if (j4 + 32 < n4) {
+          xn = __ldg(l4 + j4 + 32);
+          if (q4) qn = __ldg(q4 + j4 + 32);
+        }
+        unsigned long long wt[4] = {0ull, 0ull, 0ull, 0ull};
+        if (j4 < n4) {
+#pragma unroll 1
+          for (int e = 0; e < 4; ++e) {
+            const float x = e == 0 ? xa.x : (e == 1 ? xa.y : (e == 2 ? xa.z : xa.w));
+            const float qx = e == 0 ? qa.x : (e == 1 ? qa.y : (e == 2 ? qa.z : qa.w));
+            const int v = v0 + s0 + 4 * j4 + e;
+            const float pv = eval_p(w.dn, rp, x, pen && bit(bits, 4 * j4 + e), v);
+            unsigned long long wgt;
+            if (!use_r) {
+              wgt = to_fix(pv);
+            } else {
+              const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qx;
+              const float rv = pv - qv;
+              wgt = to_fix(rv > 0.f ? rv : 0.f);
+            }
+            if (e == 0) wt[0] = wgt;
+            else if (e == 1) wt[1] = wgt;
+            else if (e == 2) wt[2] = wgt;
+            else wt[3] = wgt;
           }
         }
+        const unsigned long long ls = wt[0] + wt[1] + wt[2] + wt[3];
+        unsigned long long li = ls;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (done) break;
-          const int j4 = b0 + u * 32 + lane;
-          unsigned long long wt[4] = {0ull, 0ull, 0ull, 0ull};
-          if (j4 < n4) {
-            const float xs[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-            const float qs[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long x = __shfl_up_sync(0xFFFFFFFFu, li, o);
+          if (lane >= o) li += x;
+        }
+        const unsigned long long ct = __shfl_sync(0xFFFFFFFFu, li, 31);
+        if (need <= ct) {
+          const unsigned long long ex = li - ls;
+          if (ex < need && need <= li) {
+            unsigned long long cum = ex;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int v = v0 + s0 + 4 * j4 + e;
-              const float pv = eval_p(w.dn, rp, xs[e], pen && bit(bits, 4 * j4 + e), v);
-              if (!use_r) {
-                wt[e] = to_fix(pv);
-              } else {
-                const float qv = w.xr >= 0 ? (v == w.xr ? 1.f : 0.f) : qs[e];
-                const float rv = pv - qv;
-                wt[e] = to_fix(rv > 0.f ? rv : 0.f);
+              cum += wt[e];
+              if (wt[e] > 0 && cum >= need) {
+                s_y = v0 + s0 + 4 * j4 + e;
+                break;
               }
             }
           }
-          const unsigned long long ls = wt[0] + wt[1] + wt[2] + wt[3];
-          unsigned long long li = ls;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long x = __shfl_up_sync(0xFFFFFFFFu, li, o);
-            if (lane >= o) li += x;
-          }
-          const unsigned long long ct = __shfl_sync(0xFFFFFFFFu, li, 31);
-          if (need <= ct) {
-            const unsigned long long ex = li - ls;
-            if (ex < need && need <= li) {
-              unsigned long long cum = ex;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                cum += wt[e];
-                if (wt[e] > 0 && cum >= need) {
-                  s_y = v0 + s0 + 4 * j4 + e;
-                  break;
-                }
-              }
-            }
-            done = true;
-          } else {
-            need -= ct;
-          }
+          break;  // warp-uniform: every lane saw the same chunk total
         }
+        need -= ct;
+        xa = xn;
+        qa = qn;
       }
     }
     __syncthreads();
