@@ -65,6 +65,21 @@ __device__ __forceinline__ void load8(const void* src, int dt, size_t base, int 
 __global__ void k_tcx_prep(const __grid_constant__ TcxPrepArgs a) {
   __shared__ float red[32];
   const int m = blockIdx.x, part = blockIdx.y;
+  // the norm weights are constants of the head: this thread's two vectors of
+  // them are loaded before waiting for the previous kernel
+  const float* wpre = a.pro == PRO_DUAL ? (part == 0 ? a.nw : a.nw2) : (a.pro == PRO_NORM ? a.nw : nullptr);
+  float4 wv[2][2];
+  if (wpre && m < a.M) {
+    const int nv0 = (a.pro == PRO_DUAL ? a.K / 2 : a.K) / 8;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = threadIdx.x + u * blockDim.x;
+      if (i < nv0) {
+        wv[u][0] = __ldg(reinterpret_cast<const float4*>(wpre) + 2 * i);
+        wv[u][1] = __ldg(reinterpret_cast<const float4*>(wpre) + 2 * i + 1);
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
   const int L = a.pro == PRO_DUAL ? a.K / 2 : a.K;
@@ -122,7 +137,7 @@ __global__ void k_tcx_prep(const __grid_constant__ TcxPrepArgs a) {
   for (int u = 0; u < 2; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
     if (i < nv) {
-      const float4 w0 = reinterpret_cast<const float4*>(w)[2 * i], w1 = reinterpret_cast<const float4*>(w)[2 * i + 1];
+      const float4 w0 = wv[u][0], w1 = wv[u][1];
       const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       float v[8];
 #pragma unroll
