@@ -364,6 +364,8 @@ __global__ void __launch_bounds__(256) k_tcv_finish(const __grid_constant__ TcFi
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m = blockIdx.y, o = blockIdx.x * 256 + tid;
+  // the residual stream was written several kernels back: read it before the wait
+  const float rv = (a.epi == EPI_RESID && o < a.nout) ? a.resid[(size_t)m * a.ldr + o] : 0.f;
   pdl_wait();
   pdl_trigger();
   const bool logits = a.epi == EPI_LOGITS;
@@ -372,16 +374,28 @@ __global__ void __launch_bounds__(256) k_tcv_finish(const __grid_constant__ TcFi
   if (o < a.nout) {
     if (a.epi == EPI_SWIGLU) {
       const size_t r = (size_t)(o >> 6) * 128 + (o & 63);
+      // every split's partial in flight at once (tcv_splits makes at most 8), summed in split order
+      float gs[8], us[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) {
+        gs[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r) : 0.f;
+        us[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r + 64) : 0.f;
+      }
       float g = 0.f, up = 0.f;
-      for (int sp = 0; sp < a.ksplit; ++sp) {
-        g += __ldcg(p + (size_t)sp * a.ld_split + r);
-        up += __ldcg(p + (size_t)sp * a.ld_split + r + 64);
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) {
+        g += gs[sp];
+        up += us[sp];
       }
       v = g / (1.f + expf(-g)) * up;
     } else {
+      float ps[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) ps[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + o) : 0.f;
       v = 0.f;
-      for (int sp = 0; sp < a.ksplit; ++sp) v += __ldcg(p + (size_t)sp * a.ld_split + o);
-      if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + o];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) v += ps[sp];
+      v += rv;
     }
     if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
   }
