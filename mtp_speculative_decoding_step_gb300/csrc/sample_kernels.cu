@@ -570,6 +570,58 @@ __device__ __forceinline__ bool pair_gt(uint32_t ka, int ia, uint32_t kb, int ib
   return ka > kb || (ka == kb && ia > ib);
 }
 
+// Ascending (key, id) sort of kST pairs, one per thread, with distinct ids:
+// a bitonic network, its compare-exchanges over shuffles below a warp's span
+// and through shared memory (sk, si: kST entries each) above it. On return
+// thread t holds the t-th smallest pair. For one pair per thread this takes
+// fewer block barriers than a digit-by-digit radix selection.
+__device__ void block_sort(uint32_t& key, int& id, uint32_t* sk, int* si) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int size = 2; size <= kST; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint32_t ok;
+      int oi;
+      if (stride >= 32) {
+        __syncthreads();
+        sk[t] = key;
+        si[t] = id;
+        __syncthreads();
+        ok = sk[t ^ stride];
+        oi = si[t ^ stride];
+      } else {
+        ok = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
+        oi = __shfl_xor_sync(0xFFFFFFFFu, id, stride);
+      }
+      const bool asc = (t & size) == 0;
+      const bool low = (t & stride) == 0;
+      const bool other_less = ok < key || (ok == key && oi < id);
+      if (low == asc ? other_less : !other_less) {
+        key = ok;
+        id = oi;
+      }
+    }
+  }
+  __syncthreads();
+}
+// The k-th smallest (1 <= k <= kST) of kST pairs, one per thread with
+// distinct ids, to every thread (sorts them with block_sort).
+__device__ void block_kth_pair(uint32_t key, int id, int k, uint32_t* sk, int* si, SampleSmem* sm, uint32_t& K,
+                               int& I) {
+  block_sort(key, id, sk, si);
+  if ((int)threadIdx.x == k - 1) {
+    sm->sel_rem = key;
+    sm->found = id;
+  }
+  __syncthreads();
+  K = (uint32_t)sm->sel_rem;
+  I = sm->found;
+  __syncthreads();
+}
+// Sentinel id of thread t for block_sort (above every vocabulary id).
+__device__ __forceinline__ int sort_sentinel() { return 0x7FFFFFFF - (kST - 1) + (int)threadIdx.x; }
+
 // Ascending (key, id) bitonic sort of P (power of two) entries in shared memory.
 __device__ void bitonic_sort(uint32_t* key, int* id, int P) {
   for (int k = 2; k <= P; k <<= 1) {
@@ -2013,12 +2065,9 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
   // row: the kk-th smallest of the threads' smallest keys there. At least kk
   // elements lie at or below it, so the top kk all do (kept inclusively).
   auto first_threshold = [&](uint32_t mk) {
-    ckey[threadIdx.x] = mk;
-    cid[threadIdx.x] = threadIdx.x;
-    __syncthreads();
     uint32_t K0;
     int i0;
-    stream_select(sm, ckey, cid, kST, kk, tie, K0, i0);
+    block_kth_pair(mk, threadIdx.x, kk, reinterpret_cast<uint32_t*>(tie), tie + kST, sm, K0, i0);
     if (threadIdx.x == 0) { s_thrK = K0; s_thrI = 0x7FFFFFFF; s_zc = stream_z_cut(K0, TT); }
     __syncthreads();
   };
@@ -2210,9 +2259,23 @@ __global__ void __launch_bounds__(kST, 2) k_verify_stream(const __grid_constant_
     for (int j = threadIdx.x; j < V; j += kST) offer(pen_z(__ldg(lg + j), j), j, thrK, thrI, zc);
   }
   __syncthreads();
-  if (s_cnt > kk) compact();
+  const int nheld = s_cnt;
+  if (nheld <= kST) {
+    // the held entries sorted at once: their first kk are the row's top kk, in order
+    uint32_t x = threadIdx.x < nheld ? ckey[threadIdx.x] : 0xFFFFFFFFu;
+    int xi = threadIdx.x < nheld ? cid[threadIdx.x] : sort_sentinel();
+    block_sort(x, xi, reinterpret_cast<uint32_t*>(tie), tie + kST);
+    if ((int)threadIdx.x < kk) {
+      ckey[threadIdx.x] = x;
+      cid[threadIdx.x] = xi;
+    }
+    if (threadIdx.x == 0) s_cnt = min(nheld, kk);
+    __syncthreads();
+  } else {
+    compact();
+    rank_sort(ckey, cid, s_cnt);
+  }
   const int L = s_cnt;  // == kk: V > kk elements were all offered
-  rank_sort(ckey, cid, L);
   block_argmax(gv, gi, s_bv, s_bi);
   if (gi == 0x7FFFFFFF) gi = 0;  // nothing comparable (non-finite input): id 0
 
@@ -2529,7 +2592,7 @@ __global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArg
   const bool local_bound = !p.greedy && k <= kTkLocalK;
   uint32_t Kc = 0xFFFFFFFFu;
   int Ic = 0x7FFFFFFF;
-  if (local_bound) stream_select(sm, tmk, tmi, kST, k, tie, Kc, Ic);
+  if (local_bound) block_kth_pair(tkk, tid_, k, reinterpret_cast<uint32_t*>(tie), tie + kST, sm, Kc, Ic);
   if (threadIdx.x == 0) {
     sm->mail[c.ph].f[0] = bzv;
     sm->mail[c.ph].i[0] = bzid;
@@ -2632,22 +2695,36 @@ __global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArg
   }
   __syncthreads();
   // the exact top-k of the union (it holds at least k), sorted by (key, id)
-  uint32_t Kk = 0xFFFFFFFFu;
-  int Ik = 0x7FFFFFFF;
-  if (M > k) stream_select(sm, mk, mi, M, k, tie, Kk, Ik);
-  if (threadIdx.x == 0) sm->ccount = 0;
-  __syncthreads();
-  for (int t = threadIdx.x; t < M; t += kST)
-    if (in_prefix(mk[t], mi[t], Kk, Ik)) {
-      const int pos = atomicAdd(&sm->ccount, 1);
-      if (pos < kStreamTopK) {
-        sk[pos] = mk[t];
-        si[pos] = mi[t];
-      }
+  int L;
+  if (M <= kST) {
+    // one entry per thread, sorted at once: the first k are the top-k in order
+    uint32_t x = threadIdx.x < M ? mk[threadIdx.x] : 0xFFFFFFFFu;
+    int xi = threadIdx.x < M ? mi[threadIdx.x] : sort_sentinel();
+    block_sort(x, xi, reinterpret_cast<uint32_t*>(tie), tie + kST);
+    if ((int)threadIdx.x < k) {
+      sk[threadIdx.x] = x;
+      si[threadIdx.x] = xi;
     }
-  __syncthreads();
-  const int L = min(sm->ccount, kStreamTopK);  // == k
-  rank_sort(sk, si, L);
+    __syncthreads();
+    L = min(M, k);
+  } else {
+    uint32_t Kk = 0xFFFFFFFFu;
+    int Ik = 0x7FFFFFFF;
+    stream_select(sm, mk, mi, M, k, tie, Kk, Ik);
+    if (threadIdx.x == 0) sm->ccount = 0;
+    __syncthreads();
+    for (int t = threadIdx.x; t < M; t += kST)
+      if (in_prefix(mk[t], mi[t], Kk, Ik)) {
+        const int pos = atomicAdd(&sm->ccount, 1);
+        if (pos < kStreamTopK) {
+          sk[pos] = mk[t];
+          si[pos] = mi[t];
+        }
+      }
+    __syncthreads();
+    L = min(sm->ccount, kStreamTopK);  // == k
+    rank_sort(sk, si, L);
+  }
 
   // 4. cut rules on the sorted top-k: top-p on its fixed-point mass, then
   //    min-p, at least one token kept
