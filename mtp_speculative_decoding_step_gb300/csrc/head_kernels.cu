@@ -504,9 +504,12 @@ void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float*
 // the host at load); the angle is formed and reduced modulo 2*pi in double and
 // its sine/cosine taken in fp32 (error ~2^-24 rad after reduction).
 __device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int pos, const double* inv_freq) {
+  // the angle and its reduction to [0, 2 pi) in double (a multiply by 1 / (2 pi)
+  // instead of a divide: this part's double-precision rate is low)
   const double two_pi = 6.283185307179586476925286766559;
+  const double inv_two_pi = 0.15915494309189533576888376337251;
   double ang = (double)pos * inv_freq[i];
-  ang -= two_pi * floor(ang / two_pi);
+  ang -= two_pi * floor(ang * inv_two_pi);
   float s, c;
   sincosf((float)ang, &s, &c);
   const float y0 = x0 * c - x1 * s;
