@@ -441,6 +441,301 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last);
 }
 
+// ------------------------------------------ fp8 head GEMV on the tensor cores
+//
+// The e4m3 head streamed through mma.sync m16n8k16 (f16 inputs, fp32
+// accumulators) instead of widened element by element: one cvt.e4m3x2 per two
+// codes and one MMA per 256 codes, where the CUDA-core loop spends about two
+// and a half instructions per code. Every e4m3 value is exact in f16. Each
+// activation x is split into three f16 parts after scaling by a power of two
+// 2^e (per item and block, chosen so that max|x| 2^e lies in [2^14, 2^15)):
+// hi = f16(x'), mid = f16(x' - hi), lo = f16(x' - hi - mid), together 33
+// significant bits. The products of a code and a part are exact in fp32, the
+// sums accumulate in fp32, and the result is scaled back by 2^-e.
+//
+// A warp owns 16 rows: lane (g, t) loads 16-byte chunks of rows g and g + 8,
+// the A operand. The k order inside one MMA is a permutation of the chunk's
+// columns, the same for A and for the parts (the B operand, one column per
+// part), so it cancels in the sum. 128 rows per block of 8 warps.
+constexpr int kFp8MmaRows = 128;
+
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^e such that v 2^e lies in [2^14, 2^15) (v = f 2^E, f in [0.5, 1)); 0 for
+// a zero or non-finite v
+__device__ __forceinline__ int fp8_part_exp(float v) {
+  int E = 0;
+  frexpf(v, &E);
+  return (v > 0.f && isfinite(v)) ? min(max(15 - E, -126), 126) : 0;
+}
+
+// hi, mid and lo f16 parts of four scaled activations, stored at columns
+// k..k+3 of three consecutive part rows PS halves apart
+__device__ __forceinline__ void fp8_parts4(uint16_t* dst, int PS, float4 v) {
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  uint16_t p[3][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const __half hi = __float2half_rn(x[c]);
+    const float r1 = x[c] - __half2float(hi);
+    const __half mid = __float2half_rn(r1);
+    const __half lo = __float2half_rn(r1 - __half2float(mid));
+    p[0][c] = __half_as_ushort(hi);
+    p[1][c] = __half_as_ushort(mid);
+    p[2][c] = __half_as_ushort(lo);
+  }
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+    *reinterpret_cast<uint2*>(dst + q * PS) =
+        make_uint2((uint32_t)p[q][0] | ((uint32_t)p[q][1] << 16), (uint32_t)p[q][2] | ((uint32_t)p[q][3] << 16));
+}
+
+template <int MT>
+__global__ void __launch_bounds__(256, 2) k_gemv_fp8_mma(const __grid_constant__ GemvArgs a) {
+  constexpr int NP = 3 * MT;        // parts: hi, mid, lo of each item
+  constexpr int NT = (NP + 7) / 8;  // n-tiles of 8 parts
+  extern __shared__ __align__(16) float xs[];
+  __shared__ float s_out[MT][kFp8MmaRows];
+  __shared__ float s_red[64 * MT];
+  __shared__ int s_e[MT];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  // Without a K split the grid may be narrower than the group count: a block
+  // then walks groups blockIdx.x, + gridDim.x, ..., with one prologue, and the
+  // next group's first codes in flight during this group's epilogue.
+  const bool walk = a.S == 1;
+  int group = walk ? blockIdx.x : blockIdx.x / a.S;
+  const int split = walk ? 0 : blockIdx.x - group * a.S;
+  const int k0 = gemv_slice_start(a.K, a.S, split), KS = gemv_slice_start(a.K, a.S, split + 1) - k0;
+  const int PS = KS + 4;  // halves between parts (8 bytes of padding against bank conflicts)
+  uint16_t* xp = reinterpret_cast<uint16_t*>(xs + MT * KS);
+
+  // rows l0 + g and l0 + g + 8 of the group, in the virtual row space
+  const int l0 = warp * 16;
+  const uint8_t* WA;
+  const uint8_t* WB;
+  auto set_rows = [&](int grp) {
+    const int v = grp * kFp8MmaRows + l0 + g;
+    int sg = 0, start = 0;
+    while (v >= a.seg_end[sg]) { start = a.seg_end[sg]; ++sg; }
+    WA = reinterpret_cast<const uint8_t*>(a.w[sg]) + (size_t)(v - start) * a.K + k0;
+    const int v8 = v + 8;
+    sg = 0; start = 0;
+    while (v8 >= a.seg_end[sg]) { start = a.seg_end[sg]; ++sg; }
+    WB = reinterpret_cast<const uint8_t*>(a.w[sg]) + (size_t)(v8 - start) * a.K + k0;
+  };
+  set_rows(group);
+
+  // A set is 256 columns: four steps of 64, lane t taking the 16-column chunk
+  // 4 u + t of step u, of both its rows.
+  const int nchunk = KS / 16, nset = (nchunk + 15) / 16;
+  auto load_set = [&](uint4 (&w)[8], int j) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = 16 * j + 4 * u + t;
+      if (q < nchunk) {
+        w[2 * u] = ldg_stream(WA + 16 * q);
+        w[2 * u + 1] = ldg_stream(WB + 16 * q);
+      } else {
+        w[2 * u] = w[2 * u + 1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  // the codes do not depend on the previous kernel: the first set (both sets
+  // for one item, where the registers allow) in flight before waiting for it
+  uint4 w0[8], w1[8];
+  load_set(w0, 0);
+  if (MT == 1 && nset > 1) load_set(w1, 1);
+  pdl_wait();
+  pdl_trigger();
+
+  if (a.pro == PRO_NORM) {
+    // x = RMSNorm(row) * nw: one pass for the sums of squares and the largest
+    // |row * nw| of this slice (which, times the norm's scale, bounds max |x|),
+    // then the parts straight from the normalised row
+    float ss[MT], mx[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) ss[m] = mx[m] = 0.f;
+    for (int i = tid; i < a.K / 4; i += blockDim.x) {
+      const int k = 4 * i;
+      const bool mine = k >= k0 && k < k0 + KS;
+      const float4 ww = mine ? reinterpret_cast<const float4*>(a.nw)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < a.M) {
+          const float4 v = reinterpret_cast<const float4*>(a.x + (size_t)m * a.ldx)[i];
+          ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+          mx[m] = fmaxf(mx[m], fmaxf(fmaxf(fabsf(v.x * ww.x), fabsf(v.y * ww.y)),
+                                     fmaxf(fabsf(v.z * ww.z), fabsf(v.w * ww.w))));
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      ss[m] = warp_sum(ss[m]);
+      mx[m] = warp_max(mx[m]);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        s_red[m * 32 + warp] = ss[m];
+        s_red[(MT + m) * 32 + warp] = mx[m];
+      }
+    __syncthreads();
+    float inv[MT], up[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float t2 = 0.f, mm = 0.f;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+        t2 += s_red[m * 32 + i];
+        mm = fmaxf(mm, s_red[(MT + m) * 32 + i]);
+      }
+      inv[m] = rsqrtf(t2 / (float)a.K + a.eps);
+      const int e = fp8_part_exp(inv[m] * mm);
+      up[m] = __int_as_float((127 + e) << 23);
+      if (tid == 0) s_e[m] = e;
+    }
+    for (int i = tid; i < MT * (KS / 4); i += blockDim.x) {
+      const int m = i / (KS / 4), k = 4 * (i - m * (KS / 4));
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m < a.M) {
+        const float4 x4 = *reinterpret_cast<const float4*>(a.x + (size_t)m * a.ldx + k0 + k);
+        const float4 ww = *reinterpret_cast<const float4*>(a.nw + k0 + k);
+        // the normalised element as the CUDA-core path forms it, then 2^e
+        v = make_float4(x4.x * inv[m] * ww.x * up[m], x4.y * inv[m] * ww.y * up[m], x4.z * inv[m] * ww.z * up[m],
+                        x4.w * inv[m] * ww.w * up[m]);
+      }
+      fp8_parts4(xp + 3 * m * PS + k, PS, v);
+    }
+  } else {
+    gemv_prologue<MT>(a, xs, k0, KS, s_red);
+    __syncthreads();
+    // the power of two of each item: max |x| over this block's slice
+    float mx[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      mx[m] = 0.f;
+      for (int k = tid; k < KS; k += blockDim.x) mx[m] = fmaxf(mx[m], fabsf(xs[m * KS + k]));
+      mx[m] = warp_max(mx[m]);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) s_red[m * 32 + warp] = mx[m];
+    __syncthreads();
+    if (tid < MT) {
+      float v = 0.f;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) v = fmaxf(v, s_red[tid * 32 + i]);
+      s_e[tid] = fp8_part_exp(v);
+    }
+    __syncthreads();
+    for (int i = tid; i < MT * (KS / 4); i += blockDim.x) {
+      const int m = i / (KS / 4), k = 4 * (i - m * (KS / 4));
+      const float up = __int_as_float((127 + s_e[m]) << 23);
+      const float4 x4 = *reinterpret_cast<const float4*>(xs + m * KS + k);
+      fp8_parts4(xp + 3 * m * PS + k, PS, make_float4(x4.x * up, x4.y * up, x4.z * up, x4.w * up));
+    }
+  }
+  __syncthreads();
+  if (MT > 1 && nset > 1) load_set(w1, 1);
+
+  // lane (g, t) reads part 8 n + g: the B operand's column g
+  const uint16_t* xb = xp + g * PS + 16 * t;
+  for (;;) {
+    float d[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.f;
+    auto compute_set = [&](const uint4 (&w)[8], int j) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = 16 * j + 4 * u + t;
+        const bool ok = q < nchunk;
+        const uint32_t wa[4] = {w[2 * u].x, w[2 * u].y, w[2 * u].z, w[2 * u].w};
+        const uint32_t wb[4] = {w[2 * u + 1].x, w[2 * u + 1].y, w[2 * u + 1].z, w[2 * u + 1].w};
+#pragma unroll
+        for (int sw = 0; sw < 4; ++sw) {
+          // columns 16 q + 4 sw + {0, 1} are k = 2t, 2t+1; + {2, 3} are k = 2t+8, 2t+9
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2(wa[sw], a0, a2);
+          e4m3x4_to_f16x2(wb[sw], a1, a3);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            uint2 b = make_uint2(0u, 0u);
+            if (ok && 8 * n + g < 3 * a.M)
+              b = *reinterpret_cast<const uint2*>(xb + 8 * n * PS + 256 * j + 64 * u + 4 * sw);
+            mma_f16(d[n], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+      }
+    };
+    for (int j = 0; j < nset; j += 2) {
+      compute_set(w0, j);
+      if (j + 2 < nset) load_set(w0, j + 2);
+      if (j + 1 >= nset) break;
+      compute_set(w1, j + 1);
+      if (j + 3 < nset) load_set(w1, j + 3);
+    }
+
+    // d[n] = D[row g | g + 8][part 8 n + 2 t | + 1]: item m sums parts 3m..3m+2
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float r0 = 0.f, r8 = 0.f;
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int p = 8 * n + 2 * t + c;
+          if (p >= 3 * m && p < 3 * m + 3) {
+            r0 += d[n][c];
+            r8 += d[n][2 + c];
+          }
+        }
+      r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 1);
+      r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, 2);
+      r8 += __shfl_xor_sync(0xFFFFFFFFu, r8, 1);
+      r8 += __shfl_xor_sync(0xFFFFFFFFu, r8, 2);
+      if (t == 0) {
+        const float back = __int_as_float((127 - s_e[m]) << 23);
+        s_out[m][l0 + g] = r0 * back;
+        s_out[m][l0 + g + 8] = r8 * back;
+      }
+    }
+    __syncthreads();
+    const int next = walk ? group + (int)gridDim.x : a.ngroups;
+    if (next < a.ngroups) {
+      set_rows(next);
+      load_set(w0, 0);
+      if (nset > 1) load_set(w1, 1);
+    }
+    gemv_finish<MT, kFp8MmaRows>(a, s_out, group, split, &s_last);
+    if (next >= a.ngroups) break;
+    group = next;
+    __syncthreads();  // s_out and s_last are reused
+  }
+}
+
+template <int MT>
+static void launch_gemv_fp8_mma_t(const GemvArgs& a, int smem, cudaStream_t s) {
+  auto k = k_gemv_fp8_mma<MT>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // without a K split, at most the two blocks per SM that stay resident
+  const int grid = a.S == 1 ? std::min(a.ngroups, 2 * device_sm_count()) : a.ngroups * a.S;
+  launch_pdl(k, dim3(grid), dim3(256), smem, s, a);
+  count_launch();
+}
+
 template <typename WT, int MT>
 static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
   auto k = k_gemv<WT, MT>;
@@ -450,6 +745,15 @@ static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
 }
 
 void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
+  if (a.wdt == kDtypeFp8 && gemv_fp8_mma(a.N)) {
+    switch (mt) {
+      case 1: launch_gemv_fp8_mma_t<1>(a, smem, s); break;
+      case 2: launch_gemv_fp8_mma_t<2>(a, smem, s); break;
+      case 4: launch_gemv_fp8_mma_t<4>(a, smem, s); break;
+      default: launch_gemv_fp8_mma_t<8>(a, smem, s); break;
+    }
+    return;
+  }
   if (a.wdt == kDtypeFp8) {
     switch (mt) {
       case 1: launch_gemv_t<fp8e4m3, 1>(a, smem, s); break;
@@ -500,15 +804,15 @@ void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float*
 // ------------------------------------------------- q/k norm, RoPE, KV append
 
 // Rotate the pair (x0 at i, x1 at i + dh/2) to position `pos`: angle =
-// pos * theta^(-2i/dh). inv_freq[i] is that frequency in double (computed on
-// the host at load); the angle is formed and reduced modulo 2*pi in double and
+// pos * theta^(-2i/dh). `freq` is that frequency in double (computed on the
+// host at load); the angle is formed and reduced modulo 2*pi in double and
 // its sine/cosine taken in fp32 (error ~2^-24 rad after reduction).
-__device__ __forceinline__ void rope_pair(float& x0, float& x1, int i, int pos, const double* inv_freq) {
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, int pos, double freq) {
   // the angle and its reduction to [0, 2 pi) in double (a multiply by 1 / (2 pi)
   // instead of a divide: this part's double-precision rate is low)
   const double two_pi = 6.283185307179586476925286766559;
   const double inv_two_pi = 0.15915494309189533576888376337251;
-  double ang = (double)pos * inv_freq[i];
+  double ang = (double)pos * freq;
   ang -= two_pi * floor(ang * inv_two_pi);
   float s, c;
   sincosf((float)ang, &s, &c);
@@ -533,9 +837,14 @@ __device__ __forceinline__ float qkv_at(const QkvPostArgs& a, int m, int col) {
 
 __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
   __shared__ float red[32];
+  const int m = blockIdx.x, h = blockIdx.y + (a.q_off < 0 ? a.nq : 0), i = threadIdx.x, half = a.dh / 2;
+  // the norm weights and the RoPE frequency are constants of the model: read
+  // them before waiting for the GEMM that produced qkv
+  const float* nw = h < a.nq ? a.wq : a.wk;
+  const float w0 = nw[i], w1 = nw[i + half];
+  const double freq = a.inv_freq[i];
   pdl_wait();
   pdl_trigger();
-  const int m = blockIdx.x, h = blockIdx.y + (a.q_off < 0 ? a.nq : 0), i = threadIdx.x, half = a.dh / 2;
   const int slot = a.slot[m], row = a.row[m];
   if (h < a.nq) {
     const int qd = a.qdst[m];
@@ -543,9 +852,9 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
     float x0 = qkv_at(a, m, a.q_off + h * a.dh + i), x1 = qkv_at(a, m, a.q_off + h * a.dh + i + half);
     const float ss = block_sum(x0 * x0 + x1 * x1, red);
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
-    x0 = x0 * inv * a.wq[i];
-    x1 = x1 * inv * a.wq[i + half];
-    rope_pair(x0, x1, i, slot, a.inv_freq);
+    x0 = x0 * inv * w0;
+    x1 = x1 * inv * w1;
+    rope_pair(x0, x1, slot, freq);
     float* dst = a.q_out + (size_t)qd * a.nq * a.dh + h * a.dh;
     dst[i] = x0;
     dst[i + half] = x1;
@@ -554,9 +863,9 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
     float x0 = qkv_at(a, m, a.k_off + g * a.dh + i), x1 = qkv_at(a, m, a.k_off + g * a.dh + i + half);
     const float ss = block_sum(x0 * x0 + x1 * x1, red);
     const float inv = rsqrtf(ss / (float)a.dh + a.eps);
-    x0 = x0 * inv * a.wk[i];
-    x1 = x1 * inv * a.wk[i + half];
-    rope_pair(x0, x1, i, slot, a.inv_freq);
+    x0 = x0 * inv * w0;
+    x1 = x1 * inv * w1;
+    rope_pair(x0, x1, slot, freq);
     const size_t off = (((size_t)row * a.nkv + g) * a.cap + slot) * a.dh;
     store_elem(a.kc, a.wdt, off + i, x0);
     store_elem(a.kc, a.wdt, off + i + half, x1);
@@ -572,6 +881,17 @@ __global__ void k_qkv_post(const __grid_constant__ QkvPostArgs a) {
 __global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
   __shared__ float red[32];
   const int m = blockIdx.x, half = blockIdx.y, H = a.H, nv = H / 8;
+  const float* w = half == 0 ? a.nw_e : a.nw_h;
+  float4 wv[2][2];  // this thread's norm weights, read before the wait (constants of the model)
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    wv[u][0] = wv[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < nv) {
+      wv[u][0] = reinterpret_cast<const float4*>(w)[2 * i];
+      wv[u][1] = reinterpret_cast<const float4*>(w)[2 * i + 1];
+    }
+  }
   pdl_wait();
   pdl_trigger();
   size_t base;
@@ -587,7 +907,6 @@ __global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
   }
   const void* src = half == 0 ? a.E : a.hid;
   const int dt = half == 0 ? a.wdt : a.hid_dt;
-  const float* w = half == 0 ? a.nw_e : a.nw_h;
   float f[2][8];
   float ss = 0.f;
 #pragma unroll
@@ -614,7 +933,7 @@ __global__ void k_flush_x(const __grid_constant__ FlushXArgs a) {
   for (int u = 0; u < 2; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
     if (i < nv) {
-      const float4 w0 = reinterpret_cast<const float4*>(w)[2 * i], w1 = reinterpret_cast<const float4*>(w)[2 * i + 1];
+      const float4 w0 = wv[u][0], w1 = wv[u][1];
       const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
       uint32_t o[4];
 #pragma unroll
@@ -644,6 +963,12 @@ __global__ void k_flush_norm(const float* part, int nsplit, long long split_stri
                              float eps, uint16_t* b) {
   __shared__ float red[32];
   const int m = blockIdx.x, n4 = H / 4;
+  float4 wv[4];  // this thread's norm weights, read before the wait (constants of the model)
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = threadIdx.x + u * blockDim.x;
+    wv[u] = i < n4 ? reinterpret_cast<const float4*>(w)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   pdl_wait();
   pdl_trigger();
   const float* p = part + (size_t)m * H;
@@ -668,7 +993,7 @@ __global__ void k_flush_norm(const float* part, int nsplit, long long split_stri
   for (int u = 0; u < 4; ++u) {
     const int i = threadIdx.x + u * blockDim.x;
     if (i < n4) {
-      const float4 ww = reinterpret_cast<const float4*>(w)[i];
+      const float4 ww = wv[u];
       out[i] = make_uint2((uint32_t)f_to_bf16(v[u].x * inv * ww.x) | ((uint32_t)f_to_bf16(v[u].y * inv * ww.y) << 16),
                           (uint32_t)f_to_bf16(v[u].z * inv * ww.z) | ((uint32_t)f_to_bf16(v[u].w * inv * ww.w) << 16));
     }

@@ -56,8 +56,11 @@ constexpr int kDtypeFp8 = 8;
 // Per-row e4m3 quantisation of a bf16 [rows][cols] matrix (cols even).
 void launch_quant_e4m3(const uint16_t* w, int rows, int cols, uint8_t* q, float* scale, cudaStream_t s);
 
+// The fp8 head runs on the tensor cores (128 rows per block group) when its
+// row count allows; otherwise on the CUDA cores.
+inline bool gemv_fp8_mma(int N) { return N % 128 == 0; }
 // rows per block group for a batch width MT
-inline int gemv_rows_per_group(int mt) { return 8 * (mt <= 4 ? 8 : 4); }
+inline int gemv_rows_per_group(int mt, bool fp8_mma = false) { return fp8_mma ? 128 : 8 * (mt <= 4 ? 8 : 4); }
 // K-slices of a GEMV: split `sp` of S covers [start(sp), start(sp + 1)), cut
 // on 16-element boundaries (K a multiple of 16); lengths differ by at most 16.
 __host__ __device__ inline int gemv_slice_start(int K, int S, int sp) {

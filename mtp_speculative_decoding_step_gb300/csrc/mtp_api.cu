@@ -160,10 +160,11 @@ void free_all(mtp_handle* h) {
 
 int esize(int dt) { return dt == MTP_DTYPE_BF16 ? 2 : 4; }
 
-GemvPlan plan_gemv(int N, int K, int M, int sms) {
+GemvPlan plan_gemv(int N, int K, int M, int sms, bool fp8 = false) {
   GemvPlan p;
   p.mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
-  const int rows = gemv_rows_per_group(p.mt);
+  const bool mma = fp8 && gemv_fp8_mma(N);
+  const int rows = gemv_rows_per_group(p.mt, mma);
   p.ngroups = N / rows;
   // A block streams one K-slice of its group's rows with a fixed number of
   // loads in flight per lane, so its time follows the slice length. K is cut
@@ -172,8 +173,14 @@ GemvPlan plan_gemv(int N, int K, int M, int sms) {
   // that run in waves and keep whole rows.
   const int units = K / 16;
   p.S = std::max(1, std::min({16, 2 * sms / std::max(p.ngroups, 1), std::max(1, units / 4)}));
-  while (p.S < units && (long long)p.mt * gemv_slice_max(K, p.S) * 4 > 96 * 1024) ++p.S;
-  p.smem = p.mt * gemv_slice_max(K, p.S) * 4;
+  // the staged activations (fp32), and on the tensor-core fp8 path their
+  // three f16 parts besides
+  auto smem = [&](int S) {
+    const long long ks = gemv_slice_max(K, S);
+    return p.mt * ks * 4 + (mma ? 3LL * p.mt * (ks + 4) * 2 : 0LL);
+  };
+  while (p.S < units && smem(p.S) > 96 * 1024) ++p.S;
+  p.smem = (int)smem(p.S);
   return p;
 }
 
@@ -318,7 +325,7 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
   if (!j.fp8 && h->tc_gemv && M >= kTcGemvMinItems && run_gemv_tc(h, j, M, s)) return;
   for (int m0 = 0; m0 < M; m0 += 8) {
     const int mp = std::min(8, M - m0);
-    const GemvPlan pl = plan_gemv(j.N, j.K, mp, h->sms);
+    const GemvPlan pl = plan_gemv(j.N, j.K, mp, h->sms, j.fp8);
     GemvArgs a;
     std::memset(&a, 0, sizeof(a));
     for (int i = 0; i < 3; ++i) { a.w[i] = j.w[i]; a.seg_end[i] = j.seg_end[i]; }
@@ -775,12 +782,17 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   size_t part = 0;
   int groups = 0;
   const int shapes[7][2] = {{H, 2 * H}, {qw + 2 * kw, H}, {2 * kw, H}, {H, qw}, {2 * I, H}, {H, I}, {c.vocab, H}};
-  for (int mt : {1, 2, 4, 8})
+  for (int mt : {1, 2, 4, 8}) {
     for (auto& sh : shapes) {
       GemvPlan pl = plan_gemv(sh[0], sh[1], mt, h->sms);
       if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * sh[0]);
       groups = std::max(groups, pl.ngroups);
     }
+    // the fp8 draft head (mtp_set_draft_head)
+    GemvPlan pl = plan_gemv(c.vocab, H, mt, h->sms, true);
+    if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * c.vocab);
+    groups = std::max(groups, pl.ngroups);
+  }
   h->part_floats = part;
   h->lm_groups_max = c.vocab / gemv_rows_per_group(8);
   h->lm_groups_max = std::max(h->lm_groups_max, c.vocab / gemv_rows_per_group(1));
