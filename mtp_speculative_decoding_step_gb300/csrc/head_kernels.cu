@@ -249,11 +249,38 @@ __device__ void gemv_prologue(const GemvArgs& a, float* xs, int k0, int KS, floa
     for (int k = tid; k < KS; k += blockDim.x) xs[m * KS + k] = 0.f;
 }
 
+// PRO_NORM with the norm's scale left for the epilogue: RMSNorm(x) * nw =
+// r (x * nw) with r = rsqrt(mean(x^2) + eps) one scalar per item, so
+// W RMSNorm(x) nw = r W (x * nw). Stage x * nw over the slice in one pass and
+// keep each thread's sum of squares of x over the slice; the block's sums meet
+// at the epilogue (across the K splits in the split combine), which applies r.
+// No pass over the whole row and no barrier round stand before the weights.
+template <int MT>
+__device__ void gemv_stage_deferred(const GemvArgs& a, float* xs, int k0, int KS, float (&ss)[MT]) {
+  const float4* w4 = reinterpret_cast<const float4*>(a.nw + k0);
+#pragma unroll
+  for (int m = 0; m < MT; ++m) ss[m] = 0.f;
+  for (int i = threadIdx.x; i < KS / 4; i += blockDim.x) {
+    const float4 ww = w4[i];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m < a.M) {
+        v = reinterpret_cast<const float4*>(a.x + (size_t)m * a.ldx + k0)[i];
+        ss[m] = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss[m]))));
+        v = make_float4(v.x * ww.x, v.y * ww.y, v.z * ww.z, v.w * ww.w);
+      }
+      reinterpret_cast<float4*>(xs + m * KS)[i] = v;
+    }
+  }
+}
+
 // Split-K combine and epilogue of one block group, shared by the GEMV
 // kernels. s_out[m][l] holds this block's partial of row group*ROWS + l for
 // item m; every thread of the block calls it.
 template <int MT, int ROWS>
-__device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, int split, int* s_last_p) {
+__device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, int split, int* s_last_p,
+                            bool defer = false) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int& s_last = *s_last_p;
   // Deterministic split-K: every split stores its partial; the last block of
@@ -273,6 +300,11 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
       const int m = t / ROWS, l = t - m * ROWS;
       float sum = 0.f;
       for (int s = 0; s < a.S; ++s) sum += __ldcg(&a.part[((size_t)s * MT + m) * a.N + (size_t)group * ROWS + l]);
+      if (defer) {  // the deferred norm scale: the splits' sums of squares, in split order
+        float q = 0.f;
+        for (int s = 0; s < a.S; ++s) q += __ldcg(&a.ssq[s * MT + m]);
+        sum *= rsqrtf(q / (float)a.K + a.eps);
+      }
       s_out[m][l] = sum;
     }
     if (tid == 0) a.counters[group] = 0;
@@ -386,7 +418,12 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   pdl_wait();
   pdl_trigger();
 
-  gemv_prologue<MT>(a, xs, k0, KS, s_red);
+  const bool defer = a.pro == PRO_NORM;
+  float ssq[MT];
+  if (defer)
+    gemv_stage_deferred<MT>(a, xs, k0, KS, ssq);
+  else
+    gemv_prologue<MT>(a, xs, k0, KS, s_red);
   __syncthreads();
 
   float acc[RPW][MT];
@@ -436,9 +473,36 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
 #pragma unroll
       for (int m = 0; m < MT; ++m) s_out[m][l0 + i] = acc[i][m];
   }
+  if (defer) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float v = warp_sum(ssq[m]);
+      if (lane == 0) s_red[m * 32 + warp] = v;
+    }
+  }
   __syncthreads();
+  if (defer) {
+    // the block's sums of squares over its slice, in warp order
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      float q = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) q += s_red[m * 32 + w];
+      ssq[m] = q;
+    }
+    if (a.S == 1) {
+      for (int t = tid; t < MT * ROWS; t += blockDim.x) {
+        const int m = t / ROWS, l = t - m * ROWS;
+        s_out[m][l] *= rsqrtf(ssq[m] / (float)a.K + a.eps);
+      }
+      __syncthreads();
+    } else if (tid == 0) {
+      // every block of this split has the same sums (same slice, same order)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) a.ssq[split * MT + m] = ssq[m];
+    }
+  }
 
-  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last);
+  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last, defer);
 }
 
 // ------------------------------------------ fp8 head GEMV on the tensor cores

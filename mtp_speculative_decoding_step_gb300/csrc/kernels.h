@@ -50,6 +50,7 @@ struct GemvArgs {
   int amax_idx[8];
   int32_t* status;
   const float* wscale;  // per-row scales of quantised weights (fp8), or null
+  float* ssq;           // [S][MT] sums of squares of x per K split (deferred RMSNorm scale)
 };
 // weight dtype code of the quantised (fp8 e4m3) draft head, beside MTP_DTYPE_*
 constexpr int kDtypeFp8 = 8;

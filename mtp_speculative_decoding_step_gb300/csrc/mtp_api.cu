@@ -112,6 +112,7 @@ struct mtp_handle {
   float *h0 = nullptr, *qkv = nullptr, *qrot = nullptr, *o = nullptr, *h1 = nullptr, *mlp = nullptr,
         *h2 = nullptr, *logits = nullptr, *po = nullptr, *pml = nullptr, *part = nullptr, *gmax = nullptr;
   int *gidx = nullptr, *counters = nullptr, *done = nullptr;
+  float* ssq = nullptr;                   // per-split sums of squares of a GEMV's x, [S][8]
   uint16_t *xb = nullptr, *bb = nullptr;  // bf16 activations of the tensor-core flush
   double* inv_freq = nullptr;             // RoPE frequencies theta^(-2i/dh), [dh/2]
   float* tcpart = nullptr;                // split-K partial tiles of the tensor-core flush
@@ -350,6 +351,7 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     a.resid = j.resid ? j.resid + (size_t)m0 * j.ldr : nullptr;
     a.ldr = j.ldr;
     a.part = h->part;
+    a.ssq = h->ssq;
     a.counters = h->counters;
     a.gmax = h->gmax;
     a.gidx = h->gidx;
@@ -780,24 +782,27 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   if (st == MTP_OK) st = alloc(h, &h->pml, (size_t)std::min(R, kMaxRows) * c.n_q * h->max_chunks * 2);
   // split-K partials and counters: worst case over every GEMV shape and width
   size_t part = 0;
-  int groups = 0;
+  int groups = 0, smax = 1;
   const int shapes[7][2] = {{H, 2 * H}, {qw + 2 * kw, H}, {2 * kw, H}, {H, qw}, {2 * I, H}, {H, I}, {c.vocab, H}};
   for (int mt : {1, 2, 4, 8}) {
     for (auto& sh : shapes) {
       GemvPlan pl = plan_gemv(sh[0], sh[1], mt, h->sms);
       if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * sh[0]);
       groups = std::max(groups, pl.ngroups);
+      smax = std::max(smax, pl.S);
     }
     // the fp8 draft head (mtp_set_draft_head)
     GemvPlan pl = plan_gemv(c.vocab, H, mt, h->sms, true);
     if (pl.S > 1) part = std::max(part, (size_t)pl.S * pl.mt * c.vocab);
     groups = std::max(groups, pl.ngroups);
+    smax = std::max(smax, pl.S);
   }
   h->part_floats = part;
   h->lm_groups_max = c.vocab / gemv_rows_per_group(8);
   h->lm_groups_max = std::max(h->lm_groups_max, c.vocab / gemv_rows_per_group(1));
   h->counters_n = groups;
   if (st == MTP_OK) st = alloc(h, &h->part, part);
+  if (st == MTP_OK) st = alloc(h, &h->ssq, (size_t)smax * 8);
   if (c.dtype == MTP_DTYPE_BF16) {
     if (st == MTP_OK) st = alloc(h, &h->xb, (size_t)kMaxItems * 2 * H);
     if (st == MTP_OK) st = alloc(h, &h->bb, (size_t)kMaxItems * H);
