@@ -311,6 +311,19 @@ __global__ void __launch_bounds__(128) k_tc_gemv(const __grid_constant__ CUtenso
 }
 
 template <int NI, int STAGES>
+constexpr int tc_gemv_smem() { return STAGES * (kTileM + NI) * kTileK * 2 + 1024 + 256; }
+// the stage counts of launch_tc_gemv's instances
+constexpr int kTcvSmem16 = tc_gemv_smem<16, 6>(), kTcvSmem32 = tc_gemv_smem<32, 6>(),
+              kTcvSmem64 = tc_gemv_smem<64, 5>(), kTcvSmem128 = tc_gemv_smem<128, 4>();
+
+int tc_gemv_blocks_per_sm(int NI) {
+  const int smem = NI <= 16 ? kTcvSmem16 : (NI <= 32 ? kTcvSmem32 : (NI <= 64 ? kTcvSmem64 : kTcvSmem128));
+  // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+  const int n = (228 * 1024) / (smem + 1024);
+  return n > 1 ? n : 1;
+}
+
+template <int NI, int STAGES>
 static bool tc_gemv_t(const TcGemvLaunch& L, const TcGemvArgs& a, cudaStream_t s) {
   CUtensorMap wm[3], xm;
   const int box_rows = L.swiglu ? kTileM / 2 : kTileM;
@@ -319,7 +332,7 @@ static bool tc_gemv_t(const TcGemvLaunch& L, const TcGemvArgs& a, cudaStream_t s
     if (!make_map(&wm[i], L.w[i2], L.rows[i2], L.K, box_rows)) return false;
   }
   if (!make_map(&xm, L.X2, NI, L.K, NI)) return false;
-  const int smem = STAGES * (kTileM + NI) * kTileK * 2 + 1024 + 256;
+  const int smem = tc_gemv_smem<NI, STAGES>();
   auto k = k_tc_gemv<NI, STAGES>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   cudaLaunchConfig_t cfg = {};

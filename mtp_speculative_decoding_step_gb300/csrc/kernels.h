@@ -158,6 +158,9 @@ struct TcGemvLaunch {
   int32_t* status;
 };
 bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s);
+// CTAs of the tensor-core GEMV with NI activation columns resident per SM
+// (by its shared memory)
+int tc_gemv_blocks_per_sm(int NI);
 
 // Sum the split partials (split order) and apply the epilogue; outputs
 // o < nout (nout = N, or N/2 for SwiGLU).

@@ -242,10 +242,22 @@ struct GemvJob {
 constexpr int kTcGemvMinItems = 5;
 
 // K splits for the tensor-core GEMV: about two CTAs per SM, at least 8 K tiles each.
-int tcv_splits(int tiles, int ktiles, int sms) {
-  int ks = 1;
-  while (ks < 8 && tiles * ks < 2 * sms && ktiles / (2 * ks) >= 8) ks *= 2;
-  return ks;
+// K splits of a tensor-core GEMV: the count (at most 8, at least 8 K tiles
+// each) whose CTAs best fill whole waves of the `slots` resident CTAs, i.e.
+// the largest C / (slots * ceil(C / slots)) for C = tiles * ks; ties keep the
+// fewer splits. (Doubling the splits until the grid passed the slots, as
+// before, gave 320 CTAs for 304 slots: a second wave of 16.)
+int tcv_splits(int tiles, int ktiles, int slots) {
+  int best = 1;
+  double best_e = 0.0;
+  for (int ks = 1; ks <= 8; ++ks) {
+    if (ks > 1 && ktiles / ks < 8) break;
+    const long long C = (long long)tiles * ks;
+    const long long waves = (C + slots - 1) / slots;
+    const double e = (double)C / (double)(waves * slots);
+    if (e > best_e + 1e-9) { best_e = e; best = ks; }
+  }
+  return best;
 }
 
 // Weight maps of a GEMV job on the tensor-core path; false if the job's row
@@ -283,10 +295,10 @@ bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
   TcGemvLaunch L;
   if (!tc_layout(j, L)) return false;
   const int tiles = (j.N + 127) / 128;
-  const int ks = tcv_splits(tiles, j.K / 64, h->sms);
   for (int m0 = 0; m0 < M; m0 += kTcGemvMaxItems) {
     const int mp = std::min(kTcGemvMaxItems, M - m0);
     const int NI = mp <= 8 ? 16 : (mp <= 16 ? 32 : (mp <= 32 ? 64 : 128));
+    const int ks = tcv_splits(tiles, j.K / 64, h->sms * tc_gemv_blocks_per_sm(NI));
     TcxPrepArgs p;
     std::memset(&p, 0, sizeof(p));
     p.pro = j.pro; p.K = j.K; p.M = mp; p.MI = NI / 2;
@@ -811,10 +823,11 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     // split partials of the widest shape
     const int kmax = std::max(std::max(2 * H, I), qw);
     size_t tvp = 0;
-    for (auto& sh : shapes) {
-      const int ks = tcv_splits((sh[0] + 127) / 128, sh[1] / 64, h->sms);
-      tvp = std::max(tvp, (size_t)ks * kTcGemvMaxItems * sh[0]);
-    }
+    for (auto& sh : shapes)
+      for (int NI : {16, 32, 64, 128}) {
+        const int ks = tcv_splits((sh[0] + 127) / 128, sh[1] / 64, h->sms * tc_gemv_blocks_per_sm(NI));
+        tvp = std::max(tvp, (size_t)ks * kTcGemvMaxItems * sh[0]);
+      }
     if (st == MTP_OK) st = alloc(h, &h->x2, (size_t)2 * kTcGemvMaxItems * kmax);
     if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
     h->tc_gemv = st == MTP_OK;
