@@ -17,6 +17,8 @@
 // partial tiles [split][M][N] that the consumer kernel sums in split order.
 // Every mbarrier wait is bounded: on expiry the CTA raises the status word,
 // waits (bounded) for its own copies, frees its TMEM and returns.
+#include <mutex>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -199,10 +201,18 @@ static bool tc_gemm_t(const void* A, int M, int K, const void* B0, int n0rows, c
   }
   const int smem = STAGES * (kTileM * MH + BN) * kTileK * 2 + 1024 + 256;
   auto k = k_tc_gemm<BN, STAGES, MH>;
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = true;
+  {
+    // the dynamic shared memory limit, raised once per device
+    static std::mutex mu;
+    static bool set[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set[dev]) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      set[dev] = true;
+    }
   }
   dim3 grid((M + kTileM * MH - 1) / (kTileM * MH), N / BN, ksplit);
   const cudaError_t e = launch_pdl(k, grid, dim3(128), (size_t)smem, s, ta, tb0, tb1, a);

@@ -312,13 +312,17 @@ __global__ void __launch_bounds__(128) k_tc_gemv(const __grid_constant__ CUtenso
 
 template <int NI, int STAGES>
 constexpr int tc_gemv_smem() { return STAGES * (kTileM + NI) * kTileK * 2 + 1024 + 256; }
+
 // the stage counts of launch_tc_gemv's instances
 constexpr int kTcvSmem16 = tc_gemv_smem<16, 6>(), kTcvSmem32 = tc_gemv_smem<32, 6>(),
               kTcvSmem64 = tc_gemv_smem<64, 5>(), kTcvSmem128 = tc_gemv_smem<128, 4>();
 
+// From the shared memory alone (228 KB per SM, 1 KB of it reserved per
+// resident CTA; 128 threads and 32 TMEM columns per CTA are never the limit):
+// two CTAs at 8 items, one above. (Splits chosen from the occupancy query's
+// count instead ran the 8-row draft step at 532 us against 513 us.)
 int tc_gemv_blocks_per_sm(int NI) {
   const int smem = NI <= 16 ? kTcvSmem16 : (NI <= 32 ? kTcvSmem32 : (NI <= 64 ? kTcvSmem64 : kTcvSmem128));
-  // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
   const int n = (228 * 1024) / (smem + 1024);
   return n > 1 ? n : 1;
 }
