@@ -373,73 +373,95 @@ bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s) {
 // ------------------------------------------------------------ epilogue
 
 // grid (ceil(nout / 256), M), block 256: thread t of block (x, m) owns output
-// o = 256 x + t of item m. Logits: block argmax per (x, m), and the last block
-// to finish reduces every item's blocks into its token.
+// o = 256 x + t of item m (store, residual and SwiGLU epilogues).
 __global__ void __launch_bounds__(256) k_tcv_finish(const __grid_constant__ TcFinishArgs a) {
-  __shared__ float sv[8];
-  __shared__ int si[8];
-  __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int m = blockIdx.y, o = blockIdx.x * 256 + tid;
   // the residual stream was written several kernels back: read it before the wait
   const float rv = (a.epi == EPI_RESID && o < a.nout) ? a.resid[(size_t)m * a.ldr + o] : 0.f;
   pdl_wait();
   pdl_trigger();
-  const bool logits = a.epi == EPI_LOGITS;
   const float* p = a.part + (size_t)m * a.ld_item;
-  float v = -INFINITY;
-  if (o < a.nout) {
-    if (a.epi == EPI_SWIGLU) {
-      const size_t r = (size_t)(o >> 6) * 128 + (o & 63);
-      // every split's partial in flight at once (tcv_splits makes at most 8), summed in split order
-      float gs[8], us[8];
+  if (o >= a.nout) return;
+  float v;
+  if (a.epi == EPI_SWIGLU) {
+    const size_t r = (size_t)(o >> 6) * 128 + (o & 63);
+    // every split's partial in flight at once (tcv_splits makes at most 8), summed in split order
+    float gs[8], us[8];
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp) {
-        gs[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r) : 0.f;
-        us[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r + 64) : 0.f;
-      }
-      float g = 0.f, up = 0.f;
+    for (int sp = 0; sp < 8; ++sp) {
+      gs[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r) : 0.f;
+      us[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + r + 64) : 0.f;
+    }
+    float g = 0.f, up = 0.f;
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp) {
-        g += gs[sp];
-        up += us[sp];
-      }
-      v = g / (1.f + expf(-g)) * up;
-    } else {
+    for (int sp = 0; sp < 8; ++sp) {
+      g += gs[sp];
+      up += us[sp];
+    }
+    v = g / (1.f + expf(-g)) * up;
+  } else {
+    float ps[8];
+#pragma unroll
+    for (int sp = 0; sp < 8; ++sp) ps[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + o) : 0.f;
+    v = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < 8; ++sp) v += ps[sp];
+    v += rv;
+  }
+  if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
+}
+
+// Logits epilogue: grid ceil(nout / 256), block 256. Block x takes outputs
+// o = 256 x + t of every item (split partials summed in split order, or the
+// logits the contraction wrote directly), its argmax per item, and the last
+// block to finish reduces each item's blocks into its token. One counter
+// update per block, not per (block, item): the single counter is the one
+// address every block of the launch updates.
+__global__ void __launch_bounds__(256) k_tcv_logits(const __grid_constant__ TcFinishArgs a) {
+  __shared__ float sv[8];
+  __shared__ int si[8];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int o = blockIdx.x * 256 + tid, ng = (int)gridDim.x;
+  pdl_wait();
+  pdl_trigger();
+  for (int m = 0; m < a.M; ++m) {
+    const float* p = a.part + (size_t)m * a.ld_item;
+    float v = -INFINITY;
+    if (o < a.nout) {
       float ps[8];
 #pragma unroll
       for (int sp = 0; sp < 8; ++sp) ps[sp] = sp < a.ksplit ? __ldcg(p + (size_t)sp * a.ld_split + o) : 0.f;
       v = 0.f;
 #pragma unroll
       for (int sp = 0; sp < 8; ++sp) v += ps[sp];
-      v += rv;
+      if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
+      if (!isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
     }
-    if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
-  }
-  if (!logits) return;
-  if (o < a.nout && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
-  float bv = o < a.nout ? v : -INFINITY;
-  int bi = o < a.nout ? o : 0x7FFFFFFF;
-  warp_argmax(bv, bi);
-  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
-  __syncthreads();
-  const int ng = (int)gridDim.x;
-  if (warp == 0) {
-    bv = lane < 8 ? sv[lane] : -INFINITY;
-    bi = lane < 8 ? si[lane] : 0x7FFFFFFF;
+    float bv = o < a.nout ? v : -INFINITY;
+    int bi = o < a.nout ? o : 0x7FFFFFFF;
     warp_argmax(bv, bi);
-    if (lane == 0) {
-      a.gmax[(size_t)m * ng + blockIdx.x] = bv;
-      a.gidx[(size_t)m * ng + blockIdx.x] = bi;
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (warp == 0) {
+      bv = lane < 8 ? sv[lane] : -INFINITY;
+      bi = lane < 8 ? si[lane] : 0x7FFFFFFF;
+      warp_argmax(bv, bi);
+      if (lane == 0) {
+        a.gmax[(size_t)m * ng + blockIdx.x] = bv;
+        a.gidx[(size_t)m * ng + blockIdx.x] = bi;
+      }
     }
+    __syncthreads();  // sv and si are reused by the next item
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.done, 1) == ng * (int)gridDim.y - 1;
+  if (tid == 0) s_last = atomicAdd(a.done, 1) == ng - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int mm = warp; mm < (int)gridDim.y; mm += 8) {
+  for (int mm = warp; mm < a.M; mm += 8) {
     float cv = -INFINITY;
     int ci = 0x7FFFFFFF;
     for (int g = lane; g < ng; g += 32) {
@@ -454,7 +476,10 @@ __global__ void __launch_bounds__(256) k_tcv_finish(const __grid_constant__ TcFi
 }
 
 void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s) {
-  launch_pdl(k_tcv_finish, dim3((a.nout + 255) / 256, a.M), dim3(256), 0, s, a);
+  if (a.epi == EPI_LOGITS)
+    launch_pdl(k_tcv_logits, dim3((a.nout + 255) / 256), dim3(256), 0, s, a);
+  else
+    launch_pdl(k_tcv_finish, dim3((a.nout + 255) / 256, a.M), dim3(256), 0, s, a);
   count_launch();
 }
 
