@@ -1,10 +1,11 @@
 """The fp8 draft head (mtp_set_draft_head with MTP_HEAD_FP8): an e4m3 copy
 of the tied output head, one fp32 scale per row, read by the drafter's logits
-only. On a reduced bf16 head of the same family (H=512, vocab 4096), a batch
-of 1 (CUDA-core GEMV) and a batch of 8 (tensor-core layers, fp8 head on the
-CUDA cores) are compared with the oracle quantising the same head the same
-way. Logits must agree within 1e-2 of the largest magnitude, as for every
-bf16 head, and drafts exactly unless the oracle reports a near-tie. The fp8
+only. On a reduced bf16 head of the same family (H=512, vocab 4096 or 4032),
+a batch of 1 and a batch of 8 are compared with the oracle quantising the
+same head the same way; vocab 4096 runs the fp8 head on the tensor cores,
+4032 (not a multiple of 128 rows) on the CUDA cores. Logits must agree within
+1e-2 of the largest magnitude, as for every bf16 head, and drafts exactly
+unless the oracle reports a near-tie. The fp8
 logits must also differ from the bf16 head's, which shows that the copy is in
 use, and switching back must restore the bf16 head. The same comparison runs
 at the 27B shape the benchmark times (H 5120, vocab 152064, KV 4096)."""
@@ -21,10 +22,14 @@ S = synth.small_shape("bf16", vocab=4096)
 TOL = 1e-2
 
 
+# vocab 4096 takes the tensor-core fp8 GEMV (row groups of 128); 4032 (a
+# multiple of 64 only) takes the CUDA-core one
+@pytest.mark.parametrize("vocab", [4096, 4032])
 @pytest.mark.parametrize("R", [1, 8])
-def test_fp8_head_matches_the_oracle(R):
+def test_fp8_head_matches_the_oracle(R, vocab):
     depth = 2
     prefill = [40 + 7 * r for r in range(R)]
+    S = synth.small_shape("bf16", vocab=vocab)
     rig = g.Rig(S, seed=61, rows=R, capacity=256, prefill=prefill, max_depth=depth)
     q, sc = oracle.quantize_rows_e4m3(rig.model.embed)
     orc_bf16 = rig.orc
