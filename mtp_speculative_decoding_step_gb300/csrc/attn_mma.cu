@@ -120,8 +120,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_attn_mma(const __grid_consta
     st[4 * tid + 1] = 0.f;
     st[4 * tid + 2] = 0.f;
   }
-  pdl_wait();  // the cache rows of this call's new slots come from k_qkv_post
-  pdl_trigger();
   const size_t base = ((size_t)a.row[m] * a.nkv + g) * a.cap + t0;  // first slot row of the chunk
   const uint16_t* kc = reinterpret_cast<const uint16_t*>(a.kc);
   const uint16_t* vc = reinterpret_cast<const uint16_t*>(a.vc);
@@ -143,8 +141,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k_attn_mma(const __grid_consta
     }
     cp_async_commit();  // one group per tile index, empty past the end
   };
-#pragma unroll
-  for (int i = 0; i < kMmaNS; ++i) issue(i);
+  // Tiles whose slots all lie below this call's first new slot hold cache rows
+  // written by earlier calls: they are requested before waiting for k_qkv_post,
+  // which writes the new ones; the rest after it.
+  int pre = 0;
+  while (pre < kMmaNS && (pre >= nt || t0 + (pre + 1) * kMmaTS <= a.first_new[m])) issue(pre++);
+  pdl_wait();
+  pdl_trigger();
+  for (int i = pre; i < kMmaNS; ++i) issue(i);
 
   // this warp's A fragments of Q: rows 0-7 the heads rounded to bf16, rows
   // 8-15 what that left over (heads >= G are zero)

@@ -196,6 +196,9 @@ struct AttnArgs {
   int32_t* status;
   int row[kMaxRows];
   int slot[kMaxRows];
+  // the first cache slot of item m's row that this call's k_qkv_post writes
+  // (slots below it are final before the attention starts; 0: none known)
+  int first_new[kMaxRows];
 };
 void launch_attention(const AttnArgs& a, int sms, cudaStream_t s);
 // The tensor-core instance (bf16 cache, head dim 128 or 256, at most 8 query

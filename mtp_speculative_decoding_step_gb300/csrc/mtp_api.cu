@@ -499,7 +499,15 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
       a.max_chunks = h->max_chunks;
       a.scale = 1.0f / std::sqrt((float)c.head_dim);
       a.po = h->po; a.pml = h->pml; a.o = h->o + (size_t)m0 * qw; a.status = h->status;
-      for (int m = 0; m < mp; ++m) { a.row[m] = it.row[m0 + m]; a.slot[m] = it.slot[m0 + m]; }
+      for (int m = 0; m < mp; ++m) {
+        a.row[m] = it.row[m0 + m];
+        a.slot[m] = it.slot[m0 + m];
+        // every item of this call on the same row gets its K/V slot written now
+        int fn = a.slot[m];
+        for (int q = 0; q < it.n; ++q)
+          if (it.row[q] == a.row[m]) fn = std::min(fn, it.slot[q]);
+        a.first_new[m] = fn;
+      }
       launch_attention(a, h->sms, s);
     }
   }
