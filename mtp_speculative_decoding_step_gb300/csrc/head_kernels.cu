@@ -360,16 +360,44 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (warp < a.M) {
+  // The groups' maxima of each item, reduced by the whole block (this runs
+  // once per launch, at its very end, so it is on the path to the next
+  // kernel): thread t takes groups t, t + blockDim, ... with four loads in
+  // flight, then warp and block reductions. s_out is free again: the block's
+  // own outputs are stored.
+  float* sv = &s_out[0][0];
+  const int nw = (int)(blockDim.x >> 5);
+  for (int m = 0; m < a.M; ++m) {
+    const float* gm = a.gmax + (size_t)m * a.ngroups;
+    const int* gx = a.gidx + (size_t)m * a.ngroups;
     float bv = -INFINITY;
     int bi = 0x7FFFFFFF;
-    for (int g = lane; g < a.ngroups; g += 32) {
-      const float v = __ldcg(&a.gmax[(size_t)warp * a.ngroups + g]);
-      const int i = __ldcg(&a.gidx[(size_t)warp * a.ngroups + g]);
-      if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    for (int g0 = tid; g0 < a.ngroups; g0 += 4 * (int)blockDim.x) {
+      float v[4];
+      int ix[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * (int)blockDim.x;
+        v[u] = g < a.ngroups ? __ldcg(gm + g) : -INFINITY;
+        ix[u] = g < a.ngroups ? __ldcg(gx + g) : 0x7FFFFFFF;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (better(v[u], ix[u], bv, bi)) { bv = v[u]; bi = ix[u]; }
     }
     warp_argmax(bv, bi);
-    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[warp]] = bi;
+    __syncthreads();  // the previous item's block reduction has read sv
+    if (lane == 0) {
+      sv[2 * warp] = bv;
+      sv[2 * warp + 1] = __int_as_float(bi);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      bv = lane < nw ? sv[2 * lane] : -INFINITY;
+      bi = lane < nw ? __float_as_int(sv[2 * lane + 1]) : 0x7FFFFFFF;
+      warp_argmax(bv, bi);
+      if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[m]] = bi;
+    }
   }
   if (tid == 0) *a.done = 0;
 }
