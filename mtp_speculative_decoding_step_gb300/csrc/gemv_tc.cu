@@ -461,13 +461,23 @@ __global__ void __launch_bounds__(256) k_tcv_logits(const __grid_constant__ TcFi
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // one warp per item, eight loads in flight per lane: this runs once per
+  // launch, at its end, on the path to the next kernel
   for (int mm = warp; mm < a.M; mm += 8) {
     float cv = -INFINITY;
     int ci = 0x7FFFFFFF;
-    for (int g = lane; g < ng; g += 32) {
-      const float x = __ldcg(&a.gmax[(size_t)mm * ng + g]);
-      const int i = __ldcg(&a.gidx[(size_t)mm * ng + g]);
-      if (better(x, i, cv, ci)) { cv = x; ci = i; }
+    for (int g0 = lane; g0 < ng; g0 += 8 * 32) {
+      float x[8];
+      int ix[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int g = g0 + 32 * u;
+        x[u] = g < ng ? __ldcg(&a.gmax[(size_t)mm * ng + g]) : -INFINITY;
+        ix[u] = g < ng ? __ldcg(&a.gidx[(size_t)mm * ng + g]) : 0x7FFFFFFF;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (better(x[u], ix[u], cv, ci)) { cv = x[u]; ci = ix[u]; }
     }
     warp_argmax(cv, ci);
     if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[mm]] = ci;
