@@ -280,7 +280,7 @@ __device__ void gemv_stage_deferred(const GemvArgs& a, float* xs, int k0, int KS
 // item m; every thread of the block calls it.
 template <int MT, int ROWS>
 __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, int split, int* s_last_p,
-                            bool defer = false) {
+                            bool defer = false, const float* rv_pre = nullptr) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int& s_last = *s_last_p;
   // Deterministic split-K: every split stores its partial; the last block of
@@ -298,13 +298,25 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
     __threadfence();
     for (int t = tid; t < a.M * ROWS; t += blockDim.x) {
       const int m = t / ROWS, l = t - m * ROWS;
-      float sum = 0.f;
-      for (int s = 0; s < a.S; ++s) sum += __ldcg(&a.part[((size_t)s * MT + m) * a.N + (size_t)group * ROWS + l]);
-      if (defer) {  // the deferred norm scale: the splits' sums of squares, in split order
-        float q = 0.f;
-        for (int s = 0; s < a.S; ++s) q += __ldcg(&a.ssq[s * MT + m]);
-        sum *= rsqrtf(q / (float)a.K + a.eps);
+      // the splits' partials (and sums of squares) eight at a time in flight,
+      // summed in split order: the group's last block is on the kernel's tail
+      float sum = 0.f, q = 0.f;
+      for (int s0 = 0; s0 < a.S; s0 += 8) {
+        float ps[8], qs[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int sp = s0 + u;
+          ps[u] = sp < a.S ? __ldcg(&a.part[((size_t)sp * MT + m) * a.N + (size_t)group * ROWS + l]) : 0.f;
+          qs[u] = (defer && sp < a.S) ? __ldcg(&a.ssq[sp * MT + m]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sum += ps[u];
+          q += qs[u];
+        }
       }
+      // the deferred norm scale from the splits' sums of squares
+      if (defer) sum *= rsqrtf(q / (float)a.K + a.eps);
       s_out[m][l] = sum;
     }
     if (tid == 0) a.counters[group] = 0;
@@ -332,7 +344,7 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
     const int m = t / ROWS, l = t - m * ROWS;
     const size_t n = (size_t)group * ROWS + l;
     float v = s_out[m][l];
-    if (a.epi == EPI_RESID) v += a.resid[(size_t)m * a.ldr + n];
+    if (a.epi == EPI_RESID) v += (rv_pre && t == tid) ? *rv_pre : a.resid[(size_t)m * a.ldr + n];
     a.y[(size_t)m * a.ldy + n] = v;
     if (a.epi == EPI_LOGITS && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
   }
@@ -435,6 +447,13 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
   // loads before waiting for it. Each lane keeps one 16-byte vector of each
   // of its RPW rows in flight; with one item the next vector set is issued
   // before the current one is consumed (two sets in flight).
+  // the residual (written several kernels back) of the output this thread
+  // stores in the epilogue, read before the wait
+  float rv = 0.f;
+  if (a.epi == EPI_RESID && tid < a.M * ROWS) {
+    const int m = tid / ROWS, l = tid - m * ROWS;
+    rv = a.resid[(size_t)m * a.ldr + (size_t)group * ROWS + l];
+  }
   const int nvec = KS / VN;
   int v0 = lane;
   bool has0 = v0 < nvec;
@@ -530,7 +549,7 @@ __global__ void __launch_bounds__(256, 2) k_gemv(const __grid_constant__ GemvArg
     }
   }
 
-  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last, defer);
+  gemv_finish<MT, ROWS>(a, s_out, group, split, &s_last, defer, &rv);
 }
 
 // ------------------------------------------ fp8 head GEMV on the tensor cores
