@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(256) k_tcv_logits(const __grid_constant__ TcFi
       for (int sp = 0; sp < 8; ++sp) v += ps[sp];
       if (a.write_y) a.y[(size_t)m * a.ldy + o] = v;
       if (!isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
+      if (a.qzero) a.qzero[(size_t)m * a.ldqz + o] = 0.f;
     }
     float bv = o < a.nout ? v : -INFINITY;
     int bi = o < a.nout ? o : 0x7FFFFFFF;

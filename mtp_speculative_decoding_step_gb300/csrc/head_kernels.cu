@@ -347,6 +347,7 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
     if (a.epi == EPI_RESID) v += (rv_pre && t == tid) ? *rv_pre : a.resid[(size_t)m * a.ldr + n];
     a.y[(size_t)m * a.ldy + n] = v;
     if (a.epi == EPI_LOGITS && !isfinite(v)) flag_status(a.status, MTP_ERR_NONFINITE);
+    if (a.qzero) a.qzero[(size_t)m * a.ldqz + n] = 0.f;
   }
   if (a.epi != EPI_LOGITS) return;
 

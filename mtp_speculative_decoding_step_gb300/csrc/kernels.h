@@ -51,6 +51,8 @@ struct GemvArgs {
   int32_t* status;
   const float* wscale;  // per-row scales of quantised weights (fp8), or null
   float* ssq;           // [S][MT] sums of squares of x per K split (deferred RMSNorm scale)
+  float* qzero;         // logits epilogue: item m's draft distribution row (stride ldqz), zeroed
+  long long ldqz;       // where the logits go (the sampler then writes its kept entries only)
 };
 // weight dtype code of the quantised (fp8 e4m3) draft head, beside MTP_DTYPE_*
 constexpr int kDtypeFp8 = 8;
@@ -178,6 +180,8 @@ struct TcFinishArgs {
   int32_t* amax_out;
   int32_t* status;
   int amax_idx[kTcGemvMaxItems];
+  float* qzero;         // logits: item m's draft distribution row (stride ldqz) zeroed beside them
+  long long ldqz;
 };
 void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s);
 
@@ -265,6 +269,7 @@ struct SampleArgs {
   int merge;                 // merged candidate buffer (power of two)
   void* flat_ws;             // draft: scratch of the flat transform (flat_workspace_bytes), or null
   size_t flat_ws_bytes;
+  int q_zeroed;              // draft: the logits epilogue cleared this step's q rows (the top-k path writes its kept entries only)
   RowParams p[kMaxRows];
 };
 void launch_sample(const SampleArgs& a, cudaStream_t s);
@@ -379,6 +384,7 @@ struct TopkArgs {
   int32_t* kid;
   uint32_t* kkey;
   int32_t* status;
+  int q_zeroed;          // mode 0: q already holds zeros; write the kept entries only
   RowParams p[kMaxRows];
 };
 bool topk_fits(const RowParams* p, int rows, int V, const float* logits, long long ld);

@@ -235,6 +235,8 @@ struct GemvJob {
   const int* amax_idx;
   bool fp8;               // w[0] holds e4m3 codes with per-row scales wscale
   const float* wscale;
+  float* qzero;           // logits jobs: item m's draft distribution row (stride ldqz) zeroed
+  long long ldqz;
 };
 
 // Batches of at least this many items run their GEMVs on the tensor cores:
@@ -329,6 +331,8 @@ bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     f.ldr = j.ldr;
     f.gmax = h->gmax; f.gidx = h->gidx; f.done = h->done; f.amax_out = j.amax_out; f.status = h->status;
     for (int m = 0; m < mp; ++m) f.amax_idx[m] = j.amax_idx ? j.amax_idx[m0 + m] : 0;
+    f.qzero = j.qzero ? j.qzero + (size_t)m0 * j.ldqz : nullptr;
+    f.ldqz = j.ldqz;
     launch_tcv_finish(f, s);
   }
   return true;
@@ -370,6 +374,8 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     a.done = h->done;
     a.amax_out = j.amax_out;
     a.status = h->status;
+    a.qzero = j.qzero ? j.qzero + (size_t)m0 * j.ldqz : nullptr;
+    a.ldqz = j.ldqz;
     launch_gemv(pl.mt, a, pl.smem, s);
   }
 }
@@ -483,7 +489,7 @@ mtp_status run_front(mtp_handle* h, const Items& it, const int32_t* tok, const v
 // attention -> o_proj + residual -> post norm -> gate/up SwiGLU -> down +
 // residual -> final norm -> lm_head (+ argmax) for the head items.
 mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_logits, int32_t* amax_out,
-                    const std::vector<int>& amax_idx, cudaStream_t s) {
+                    const std::vector<int>& amax_idx, cudaStream_t s, float* qzero = nullptr, long long ldqz = 0) {
   const mtp_config& c = h->cfg;
   const int H = c.hidden, qw = c.n_q * c.head_dim, I = c.inter;
   const int R = it.n_head;
@@ -546,6 +552,7 @@ mtp_status run_back(mtp_handle* h, const Items& it, float* logits, long long ld_
     j.N = c.vocab; j.K = H; j.pro = PRO_NORM; j.epi = EPI_LOGITS;
     j.x = h->h2; j.ldx = H; j.nw = h->nrm[T_NORM]; j.y = logits; j.ldy = ld_logits;
     j.amax_out = amax_out; j.amax_idx = amax_out ? amax_idx.data() : nullptr;
+    j.qzero = qzero; j.ldqz = ldqz;
     run_gemv(h, j, R, s);
   }
   return cuda_ok(cudaGetLastError());
@@ -1001,6 +1008,10 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
   sa.status = h->status;
   sa.flat_ws = h->flat_ws; sa.flat_ws_bytes = h->flat_ws_bytes;
   for (int r = 0; r < rows; ++r) sa.p[r] = row_params(draft_params(h_params[r]));
+  // with the top-k sampler, each step's logits epilogue clears that step's q
+  // rows and the sampler writes their kept entries only
+  if (!all_fast && d_q && topk_fits(sa.p, rows, V, d_logits ? d_logits : h->logits, d_logits ? (long long)depth * V : V))
+    sa.q_zeroed = 1;
 
   for (int k = 1; k <= depth; ++k) {
     Items itk;
@@ -1027,7 +1038,8 @@ mtp_status mtp_draft(mtp_t h, mtp_stream stream, int32_t rows, int32_t depth, co
     float* lg = d_logits ? d_logits + (size_t)(k - 1) * V : h->logits;
     const long long ldl = d_logits ? (long long)depth * V : V;
     for (int r = 0; r < rows; ++r) amax_idx[r] = r * depth + (k - 1);
-    st = run_back(h, *it, lg, ldl, all_fast ? d_draft : nullptr, amax_idx, s);
+    st = run_back(h, *it, lg, ldl, all_fast ? d_draft : nullptr, amax_idx, s,
+                  sa.q_zeroed ? d_q + (size_t)(k - 1) * V : nullptr, (long long)depth * V);
     if (st != MTP_OK) return st;
     if (!all_fast) {
       ProfScope ps(h, s, PK_SAMPLE);

@@ -2505,8 +2505,6 @@ __global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArg
   __shared__ float s_bv[kST / 32];
   __shared__ int s_bi[kST / 32];
   Clu c(sm);
-  pdl_wait();
-  pdl_trigger();
   const int task = blockIdx.x / kClusterCTAs;
   int r, i;
   const float* lg;
@@ -2524,9 +2522,14 @@ __global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArg
   const int v0 = min(c.rank * per, a.V);
   const int n = min(per, a.V - v0);
   const int32_t* dr = a.drafts + (size_t)r * a.depth;
+  // The penalty window (history, then this call's earlier drafts) and its
+  // bitmap before the wait: the drafts of earlier positions come from kernels
+  // that had finished before the previous one could start.
   load_window(sm, a.hist + (size_t)r * a.W, a.W, dr, i);
   const bool pen = p.rep_penalty != 1.f;
   if (pen) build_bitmap(sm, bits, v0, n);
+  pdl_wait();
+  pdl_trigger();
   const bool smp = !p.greedy;
   const float T = smp ? p.temperature : 1.f;
 
@@ -2792,20 +2795,36 @@ __global__ void __launch_bounds__(kST, 1) k_topk(const __grid_constant__ TopkArg
       }
     }
   } else {
-    // q over the slice: the kept prefix of the (key, id) order, renormalised
-    float4* q4 = reinterpret_cast<float4*>(a.q + ((size_t)r * a.depth + i) * a.V + v0);
-    for (int j4 = threadIdx.x; j4 < n / 4; j4 += kST) {
-      float o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * j4 + e;
-        o[e] = 0.f;
-        if (in_prefix(desc_key(zs[j]), v0 + j, dd.p_key, dd.p_cut)) {
-          const float ev = expf(zs[j] - mx);
-          if (!(p.min_p > 0.f) || ev >= p.min_p) o[e] = ev / dd.S;
+    // q is optional when no row is sampled (greedy rows with a penalty come here)
+    float* qr = a.q ? a.q + ((size_t)r * a.depth + i) * a.V : nullptr;
+    if (!qr) {
+    } else if (a.q_zeroed) {
+      // q is zero but for the kept prefix of the (key, id) order, renormalised:
+      // the kept entries that fall in this CTA's slice, with the values the
+      // full write below gives them
+      for (int t = threadIdx.x; t < Kf; t += kST) {
+        const int id = si[t];
+        if (id >= v0 && id < v0 + n) {
+          const float ev = expf(key_to_z(sk[t]) - mx);
+          qr[id] = (!(p.min_p > 0.f) || ev >= p.min_p) ? ev / dd.S : 0.f;
         }
       }
-      q4[j4] = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      // q over the slice: the kept prefix of the (key, id) order, renormalised
+      float4* q4 = reinterpret_cast<float4*>(qr + v0);
+      for (int j4 = threadIdx.x; j4 < n / 4; j4 += kST) {
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * j4 + e;
+          o[e] = 0.f;
+          if (in_prefix(desc_key(zs[j]), v0 + j, dd.p_key, dd.p_cut)) {
+            const float ev = expf(zs[j] - mx);
+            if (!(p.min_p > 0.f) || ev >= p.min_p) o[e] = ev / dd.S;
+          }
+        }
+        q4[j4] = make_float4(o[0], o[1], o[2], o[3]);
+      }
     }
     if (c.rank == 0) {
       // the draw: the kept entries in id order, weights to_fix(q)
@@ -4262,7 +4281,7 @@ void launch_sample(const SampleArgs& a0, cudaStream_t s) {
     memset(&t, 0, sizeof(t));
     t.mode = 0; t.rows = a0.rows; t.V = a0.V; t.W = a0.W; t.depth = a0.depth; t.pos = a0.pos;
     t.logits = a0.logits; t.ld = a0.ld; t.hist = a0.hist; t.drafts = a0.drafts; t.u = a0.u; t.q = a0.q;
-    t.draft_out = a0.draft_out; t.status = a0.status;
+    t.draft_out = a0.draft_out; t.status = a0.status; t.q_zeroed = a0.q_zeroed;
     for (int r = 0; r < a0.rows; ++r) t.p[r] = a0.p[r];
     launch_topk(t, s);
     return;

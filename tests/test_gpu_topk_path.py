@@ -95,3 +95,23 @@ def test_topk_draft_step_q_and_token(k):
     if not g.draft_near_tie(ref["margins"][0], False, 1e-3):
         assert out["draft"][0, 0] == ref["drafts"][0]
     rig.close()
+
+
+def test_greedy_penalty_draft_without_q():
+    # greedy rows with a repetition penalty take the top-k sampler as well; with
+    # no sampled row the caller may pass no q, which must then stay unwritten
+    S = synth.small_shape("bf16", vocab=32768)
+    prm = dict(temperature=0.0, rep_penalty=1.3)
+    rig = g.Rig(S, seed=97, rows=1, capacity=256, prefill=[77], max_depth=2,
+                model=synth.make_model(S, 97, weight_std=0.1))
+    hist = synth.randint(97, "tkg:hist", (1, 24), S.vocab)
+    tok, hid = rig.pairs([[321]])
+    out = rig.draft(2, [1], tok, hid, [prm], hist=hist)
+    assert out["q"] is None
+    ref = rig.oracle_draft(0, 2, [321], g.to_f32(hid)[0, :1], oracle.make_params(**prm), hist=hist[0])
+    for k in range(2):
+        assert g.max_rel(out["logits"][0, k], ref["logits"][k]) < 1e-2, k
+        if ref["margins"][k] <= 1e-3:
+            break
+        assert out["draft"][0, k] == ref["drafts"][k], k
+    rig.close()
