@@ -243,12 +243,11 @@ struct GemvJob {
 // below it the CUDA-core GEMV keeps up with HBM.
 constexpr int kTcGemvMinItems = 5;
 
-// K splits for the tensor-core GEMV: about two CTAs per SM, at least 8 K tiles each.
 // K splits of a tensor-core GEMV: the count (at most 8, at least 8 K tiles
 // each) whose CTAs best fill whole waves of the `slots` resident CTAs, i.e.
 // the largest C / (slots * ceil(C / slots)) for C = tiles * ks; ties keep the
-// fewer splits. (Doubling the splits until the grid passed the slots, as
-// before, gave 320 CTAs for 304 slots: a second wave of 16.)
+// fewer splits. (Doubling the splits while the grid stays under the slots
+// gives 320 CTAs for 304 slots at 40 row tiles: a second wave of 16.)
 int tcv_splits(int tiles, int ktiles, int slots) {
   int best = 1;
   double best_e = 0.0;
