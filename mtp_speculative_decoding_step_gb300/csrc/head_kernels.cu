@@ -412,7 +412,10 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
       if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[m]] = bi;
     }
   }
-  if (tid == 0) *a.done = 0;
+  if (tid == 0) {
+    *a.done = 0;
+    if (a.walk) *a.walk = 0;  // every group has been taken and finished
+  }
 }
 
 template <typename WT, int MT>
@@ -848,6 +851,128 @@ static void launch_gemv_fp8_mma_t(const GemvArgs& a, int smem, cudaStream_t s) {
   count_launch();
 }
 
+// ------------------------------------------------ walking GEMV, one item
+//
+// The one-item logits GEMV over several waves of whole row groups (no K
+// split: the tied lm_head) with resident blocks that walk groups: x is staged
+// once per block, the next group is taken from a counter one group ahead and
+// its first weight vectors are in flight during the current group's
+// epilogue. Groups are taken in order as blocks free up, so the balance is
+// that of launching one block per group, without a block's launch, staging
+// and cold first loads per group.
+template <typename WT>
+__global__ void __launch_bounds__(256, 2) k_gemv_walk(const __grid_constant__ GemvArgs a) {
+  constexpr int MT = 1, RPW = 8, ROWS = 8 * RPW, VN = Vec<WT>::N;
+  extern __shared__ __align__(16) float xs[];  // x over the whole row
+  __shared__ float s_out[MT][ROWS];
+  __shared__ float s_red[64];
+  __shared__ int s_last, s_next;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nvec = a.K / VN, l0 = warp * RPW;
+  auto rows_of = [&](int g) -> const WT* {
+    if (a.epi == EPI_SWIGLU) {
+      constexpr int HALF = ROWS / 2;
+      const int prow = g * HALF + (l0 % HALF);
+      return reinterpret_cast<const WT*>(a.w[l0 < HALF ? 0 : 1]) + (size_t)prow * a.K;
+    }
+    const int v = g * ROWS + l0;
+    int sg = 0, start = 0;
+    while (v >= a.seg_end[sg]) { start = a.seg_end[sg]; ++sg; }
+    return reinterpret_cast<const WT*>(a.w[sg]) + (size_t)(v - start) * a.K;
+  };
+  int group = blockIdx.x;
+  const WT* W = rows_of(group);
+  uint4 w0[RPW], w1[RPW];
+  if (lane < nvec) {
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)lane * VN);
+  }
+  pdl_wait();
+  pdl_trigger();
+  // the block's second group (the counter starts at zero for every launch)
+  if (tid == 0) s_next = (int)gridDim.x + atomicAdd(a.walk, 1);
+  const bool defer = a.pro == PRO_NORM;
+  float ssq[MT];
+  if (defer)
+    gemv_stage_deferred<MT>(a, xs, 0, a.K, ssq);
+  else
+    gemv_prologue<MT>(a, xs, 0, a.K, s_red);
+  float r = 1.f;
+  if (defer) {  // the RMSNorm scale of the whole row, once for all groups
+    const float v = warp_sum(ssq[0]);
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    float q = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) q += s_red[w];
+    r = rsqrtf(q / (float)a.K + a.eps);
+  }
+  __syncthreads();
+
+  for (;;) {
+    float acc[RPW][MT];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) acc[i][0] = 0.f;
+    int v0 = lane;
+    bool has0 = v0 < nvec;
+    while (has0) {
+      const bool has1 = v0 + 32 < nvec;
+      if (has1) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) w1[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
+      }
+      gemv_fma<WT, MT, RPW>(acc, w0, xs, a.K, v0 * VN);
+      if (!has1) break;
+      v0 += 32;
+      has0 = v0 + 32 < nvec;
+      if (has0) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)(v0 + 32) * VN);
+      }
+      gemv_fma<WT, MT, RPW>(acc, w1, xs, a.K, v0 * VN);
+      v0 += 32;
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) acc[i][0] = warp_sum(acc[i][0]);
+    if (lane == 0)
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) s_out[0][l0 + i] = acc[i][0] * r;
+    __syncthreads();
+    // the next group's first vectors in flight during this group's epilogue,
+    // and the group after it taken now
+    const int next = s_next;
+    if (next < a.ngroups) {
+      W = rows_of(next);
+      if (lane < nvec) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) w0[i] = ldg_stream(W + (size_t)i * a.K + (size_t)lane * VN);
+      }
+    }
+    __syncthreads();  // every thread has read s_next
+    if (tid == 0 && next < a.ngroups) s_next = (int)gridDim.x + atomicAdd(a.walk, 1);
+    gemv_finish<MT, ROWS>(a, s_out, group, 0, &s_last);
+    if (next >= a.ngroups) break;
+    group = next;
+    __syncthreads();  // s_out, s_last and s_next are reused
+  }
+}
+
+template <typename WT>
+static void launch_gemv_walk_t(const GemvArgs& a, int smem, cudaStream_t s) {
+  auto k = k_gemv_walk<WT>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int grid = std::min(a.ngroups, 2 * device_sm_count());
+  launch_pdl(k, dim3(grid), dim3(256), smem, s, a);
+  count_launch();
+}
+
+// The walking GEMV takes one-item logits jobs (the lm_head: their last block,
+// which reduces the group maxima, also clears the group counter) without a K
+// split and with more groups than two waves of resident blocks.
+bool gemv_walks(int mt, const GemvArgs& a) {
+  return mt == 1 && a.S == 1 && a.walk && a.epi == EPI_LOGITS && a.wdt != kDtypeFp8 &&
+         a.ngroups > 2 * device_sm_count();
+}
+
 template <typename WT, int MT>
 static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
   auto k = k_gemv<WT, MT>;
@@ -857,6 +982,13 @@ static void launch_gemv_t(const GemvArgs& a, int smem, cudaStream_t s) {
 }
 
 void launch_gemv(int mt, const GemvArgs& a, int smem, cudaStream_t s) {
+  if (gemv_walks(mt, a)) {
+    if (a.wdt == MTP_DTYPE_BF16)
+      launch_gemv_walk_t<uint16_t>(a, smem, s);
+    else
+      launch_gemv_walk_t<float>(a, smem, s);
+    return;
+  }
   if (a.wdt == kDtypeFp8 && gemv_fp8_mma(a.N)) {
     switch (mt) {
       case 1: launch_gemv_fp8_mma_t<1>(a, smem, s); break;

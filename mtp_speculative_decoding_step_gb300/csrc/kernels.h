@@ -53,6 +53,7 @@ struct GemvArgs {
   float* ssq;           // [S][MT] sums of squares of x per K split (deferred RMSNorm scale)
   float* qzero;         // logits epilogue: item m's draft distribution row (stride ldqz), zeroed
   long long ldqz;       // where the logits go (the sampler then writes its kept entries only)
+  int* walk;            // group counter of the walking GEMV (zero between launches), or null
 };
 // weight dtype code of the quantised (fp8 e4m3) draft head, beside MTP_DTYPE_*
 constexpr int kDtypeFp8 = 8;

@@ -111,7 +111,7 @@ struct mtp_handle {
   // scratch
   float *h0 = nullptr, *qkv = nullptr, *qrot = nullptr, *o = nullptr, *h1 = nullptr, *mlp = nullptr,
         *h2 = nullptr, *logits = nullptr, *po = nullptr, *pml = nullptr, *part = nullptr, *gmax = nullptr;
-  int *gidx = nullptr, *counters = nullptr, *done = nullptr;
+  int *gidx = nullptr, *counters = nullptr, *done = nullptr, *walk = nullptr;
   float* ssq = nullptr;                   // per-split sums of squares of a GEMV's x, [S][8]
   uint16_t *xb = nullptr, *bb = nullptr;  // bf16 activations of the tensor-core flush
   double* inv_freq = nullptr;             // RoPE frequencies theta^(-2i/dh), [dh/2]
@@ -371,6 +371,7 @@ void run_gemv(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     a.gmax = h->gmax;
     a.gidx = h->gidx;
     a.done = h->done;
+    a.walk = h->walk;
     a.amax_out = j.amax_out;
     a.status = h->status;
     a.qzero = j.qzero ? j.qzero + (size_t)m0 * j.ldqz : nullptr;
@@ -851,6 +852,7 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   if (st == MTP_OK) st = alloc(h, &h->gidx, gslots);
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);
   if (st == MTP_OK) st = alloc(h, &h->done, 1);
+  if (st == MTP_OK) st = alloc(h, &h->walk, 1);
   if (st == MTP_OK) st = alloc(h, &h->status, 1);
   h->flat_ws_bytes = flat_workspace_bytes(R, R);
   if (st == MTP_OK) st = alloc(h, &h->flat_ws, h->flat_ws_bytes);
@@ -862,6 +864,7 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
   }
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->counters, 0, sizeof(int) * groups, s));
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->done, 0, sizeof(int), s));
+  if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->walk, 0, sizeof(int), s));
   if (st == MTP_OK) st = cuda_ok(cudaMemsetAsync(h->status, 0, sizeof(int32_t), s));
   h->len.assign(R, 0);
   h->keep.assign(R, -1);
