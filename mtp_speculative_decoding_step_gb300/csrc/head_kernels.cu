@@ -330,6 +330,15 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
       const float g = s_out[m][l], u = s_out[m][l + HALF];
       a.y[(size_t)m * a.ldy + (size_t)group * HALF + l] = g / (1.f + expf(-g)) * u;
     }
+    if (a.walk) {
+      // walking blocks: the last group to finish clears the group counter
+      // (every group has been taken by then) and this count
+      __syncthreads();
+      if (tid == 0 && atomicAdd(a.done, 1) == a.ngroups - 1) {
+        *a.walk = 0;
+        *a.done = 0;
+      }
+    }
     return;
   }
   if (a.wscale) {  // per-row scales of quantised weights
@@ -853,8 +862,8 @@ static void launch_gemv_fp8_mma_t(const GemvArgs& a, int smem, cudaStream_t s) {
 
 // ------------------------------------------------ walking GEMV, one item
 //
-// The one-item logits GEMV over several waves of whole row groups (no K
-// split: the tied lm_head) with resident blocks that walk groups: x is staged
+// The one-item logits or SwiGLU GEMV over more than a wave of whole row groups
+// (no K split: the tied lm_head, gate/up) with resident blocks that walk groups: x is staged
 // once per block, the next group is taken from a counter one group ahead and
 // its first weight vectors are in flight during the current group's
 // epilogue. Groups are taken in order as blocks free up, so the balance is
@@ -965,12 +974,12 @@ static void launch_gemv_walk_t(const GemvArgs& a, int smem, cudaStream_t s) {
   count_launch();
 }
 
-// The walking GEMV takes one-item logits jobs (the lm_head: their last block,
-// which reduces the group maxima, also clears the group counter) without a K
-// split and with more groups than two waves of resident blocks.
+// The walking GEMV takes one-item logits and SwiGLU jobs (the lm_head and
+// gate/up: their last group to finish clears the group counter) without a K
+// split and with more groups than one wave of resident blocks.
 bool gemv_walks(int mt, const GemvArgs& a) {
-  return mt == 1 && a.S == 1 && a.walk && a.epi == EPI_LOGITS && a.wdt != kDtypeFp8 &&
-         a.ngroups > 2 * device_sm_count();
+  return mt == 1 && a.S == 1 && a.walk && (a.epi == EPI_LOGITS || a.epi == EPI_SWIGLU) &&
+         a.wdt != kDtypeFp8 && a.ngroups > 2 * device_sm_count();
 }
 
 template <typename WT, int MT>
