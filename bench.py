@@ -45,7 +45,7 @@ POOL = 16
 # of the same kernel at V=32768 (profiles/lm_head_gemv_H5120_V32768.md),
 # scaled by the rows processed (152064 / 32768). Set to None when the kernel
 # changes until it is captured again.
-LM_TRAFFIC_BYTES = round((335.662848e6 + 2.771456e6) * 152064 / 32768)
+LM_TRAFFIC_BYTES = round((335.662848e6 + 3.067904e6) * 152064 / 32768)
 # In the timed region, every BRACKET_EVERY-th round has its lm_head launches
 # and its verify bracketed with CUDA events (the live per-kernel durations).
 BRACKET_EVERY = 8
