@@ -2,7 +2,8 @@
 run their GEMVs on the tensor cores: the weights stream through TMA into
 tcgen05 MMAs and every activation row travels as a bf16 pair (x_hi = bf16(x),
 x_lo = bf16(x - x_hi)).  On a reduced bf16 head of the same family (H=512,
-8/2 heads x 128, SwiGLU 1536, vocab 4096), batches of 8 and 20 rows with
+8/2 heads x 128, SwiGLU 1536, vocab 4096, and 65536 for a head of more row
+tiles than resident CTAs), batches of 8 and 20 rows with
 ragged pending pairs (one pass of up to 64 items, and two passes) are compared
 with the oracle: logits, the drafter's hidden state and the new KV slots
 within 1e-2 of the largest magnitude (bf16 weights and cache), drafted tokens
@@ -20,7 +21,7 @@ S = synth.small_shape("bf16", vocab=4096)
 TOL = 1e-2
 
 
-def _run(R, pend, depth, params, seed):
+def _run(R, pend, depth, params, seed, S=S):
     prefill = [int(x) for x in 100 + synth.randint(seed, "pre", (R,), 400)]
     rig = g.Rig(S, seed=seed, rows=R, capacity=640, prefill=prefill, max_depth=depth)
     toks = [[int(t) for t in synth.randint(seed, f"tok{r}", (pend[r],), S.vocab)] for r in range(R)]
@@ -60,6 +61,14 @@ def test_batch_of_8_rows_mixed_sampling():
     R = 8
     params = [dict(temperature=0.0) if r % 2 == 0 else dict(temperature=0.7, top_p=0.9) for r in range(R)]
     _run(R, [1] * R, 3, params, seed=71)
+
+
+def test_batch_of_8_rows_wide_vocabulary():
+    # vocab 65536: 512 row tiles of the tied head, more than one wave of
+    # resident CTAs
+    R = 8
+    params = [dict(temperature=0.0) if r % 2 == 0 else dict(temperature=0.9, top_k=40) for r in range(R)]
+    _run(R, [1, 2, 1, 3, 1, 2, 1, 1], 2, params, seed=73, S=synth.small_shape("bf16", vocab=65536))
 
 
 def test_batch_of_20_rows_two_passes():
