@@ -19,9 +19,12 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// fp32 -> bf16 bits, round to nearest even (finite inputs; NaN stays NaN-ish).
+// fp32 -> bf16 bits, round to nearest even; infinities stay infinite, NaN stays NaN.
 __device__ __forceinline__ uint16_t f_to_bf16(float f) {
   uint32_t u = __float_as_uint(f);
+  // a NaN stays a (quiet) NaN with its sign: the rounding add below would
+  // carry the all-ones NaN into the sign bit and leave -0
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }

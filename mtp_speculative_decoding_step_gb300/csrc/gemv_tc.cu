@@ -168,6 +168,14 @@ struct TcGemvArgs {
   float* out;  // out[split * ld_split + item * ld_item + row]
   long long ld_item, ld_split;
   int32_t* status;
+  // fused logits epilogue (one split, out = the logits): item m's draft
+  // distribution row cleared (or null) and the tile's (max, index) of each
+  // item at gmax / gidx[m * tiles + tile]
+  int fuse_logits;
+  float* qzero;
+  long long ldqz;
+  float* gmax;
+  int* gidx;
 };
 
 template <int NI, int STAGES>
@@ -277,10 +285,14 @@ __global__ void __launch_bounds__(128) k_tc_gemv(const __grid_constant__ CUtenso
 
   // epilogue: TMEM lane 32w + l holds virtual row v0 + 32w + l; column c < MI
   // is item c's x_hi product, column MI + c its x_lo product
+  __shared__ float s_bv[4][MI];
+  __shared__ int s_bi[4][MI];
   pdl_wait();
-  const bool got = mbar_wait(smem_u32(accf), 0);
+  // warp-uniform: the TMEM loads and the argmax shuffles are warp-wide
+  const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(accf), 0));
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   pdl_trigger();
+  bool bad = false;
   if (got) {
     const int row = v0 + warp * 32 + lane;
     float* o = a.out + (size_t)split * a.ld_split + row;
@@ -290,15 +302,49 @@ __global__ void __launch_bounds__(128) k_tc_gemv(const __grid_constant__ CUtenso
       float hv[8], lv[8];
       tmem_ld8(tl + (uint32_t)c, hv);
       tmem_ld8(tl + (uint32_t)(MI + c), lv);
-      if (row < a.N) {
+      if (a.fuse_logits) {
+        // the logit (+0: a lone split's sum, as the split combine forms it),
+        // the cleared q entry, and the warp's (max, lowest index) per item
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int m = c + j;
+          if (m < a.M) {
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF;
+            if (row < a.N) {
+              const float x = hv[j] + lv[j] + 0.f;
+              o[(size_t)m * a.ld_item] = x;
+              if (a.qzero) a.qzero[(size_t)m * a.ldqz + row] = 0.f;
+              bad |= !isfinite(x);
+              bv = x;
+              bi = row;
+            }
+            warp_argmax(bv, bi);
+            if (lane == 0) { s_bv[warp][m] = bv; s_bi[warp][m] = bi; }
+          }
+        }
+      } else if (row < a.N) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (c + j < a.M) o[(size_t)(c + j) * a.ld_item] = hv[j] + lv[j];
       }
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0 && (!got || *s_fail)) {
+  if (bad) flag_status(a.status, MTP_ERR_NONFINITE);
+  const bool all_got = __syncthreads_and(got);
+  if (a.fuse_logits && threadIdx.x < a.M) {
+    // the tile's pair per item; an index in range even when nothing compares
+    const int m = threadIdx.x;
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    if (all_got)
+      for (int w = 0; w < 4; ++w)
+        if (better(s_bv[w][m], s_bi[w][m], bv, bi)) { bv = s_bv[w][m]; bi = s_bi[w][m]; }
+    if (bi == 0x7FFFFFFF) bi = min(v0, a.N - 1);
+    a.gmax[(size_t)m * gridDim.x + tile] = bv;
+    a.gidx[(size_t)m * gridDim.x + tile] = bi;
+  }
+  if (threadIdx.x == 0 && (!all_got || *s_fail)) {
     flag_status(a.status, MTP_ERR_TIMEOUT);
     for (int s = 0; s < STAGES; ++s) mbar_wait(smem_u32(&full[s]), 0);
   }
@@ -361,6 +407,9 @@ bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s) {
   a.N = L.N; a.K = L.K; a.ksplit = L.ksplit; a.M = L.M; a.swiglu = L.swiglu;
   for (int i = 0; i < 3; ++i) a.seg_end[i] = L.seg_end[i];
   a.out = L.out; a.ld_item = L.ld_item; a.ld_split = L.ld_split; a.status = L.status;
+  a.fuse_logits = L.fuse_logits && L.ksplit == 1 && !L.swiglu ? 1 : 0;
+  a.qzero = L.qzero; a.ldqz = L.ldqz; a.gmax = L.gmax; a.gidx = L.gidx;
+  if (a.fuse_logits && (!a.gmax || !a.gidx)) return false;
   switch (L.NI) {
     case 16: return tc_gemv_t<16, 6>(L, a, s);
     case 32: return tc_gemv_t<32, 6>(L, a, s);
@@ -481,9 +530,43 @@ __global__ void __launch_bounds__(256) k_tcv_logits(const __grid_constant__ TcFi
         if (better(x[u], ix[u], cv, ci)) { cv = x[u]; ci = ix[u]; }
     }
     warp_argmax(cv, ci);
-    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[mm]] = ci;
+    // an item whose logits are all NaN (flagged above) still gets a token in range
+    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[mm]] = ci == 0x7FFFFFFF ? 0 : ci;
   }
   if (tid == 0) *a.done = 0;
+}
+
+// The launch-wide argmax after the fused logits epilogue: one warp per item
+// over its per-tile (max, index) pairs (a.nout of them), eight loads in
+// flight per lane; a launch of one block.
+__global__ void __launch_bounds__(256) k_tcv_argmax(const __grid_constant__ TcFinishArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ng = a.nout;
+  for (int mm = warp; mm < a.M; mm += 8) {
+    float cv = -INFINITY;
+    int ci = 0x7FFFFFFF;
+    for (int g0 = lane; g0 < ng; g0 += 8 * 32) {
+      float x[8];
+      int ix[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int g = g0 + 32 * u;
+        x[u] = g < ng ? __ldcg(&a.gmax[(size_t)mm * ng + g]) : -INFINITY;
+        ix[u] = g < ng ? __ldcg(&a.gidx[(size_t)mm * ng + g]) : 0x7FFFFFFF;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (better(x[u], ix[u], cv, ci)) { cv = x[u]; ci = ix[u]; }
+    }
+    warp_argmax(cv, ci);
+    if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[mm]] = ci == 0x7FFFFFFF ? 0 : ci;
+  }
+}
+
+void launch_tcv_argmax(const TcFinishArgs& a, cudaStream_t s) {
+  launch_pdl(k_tcv_argmax, dim3(1), dim3(256), 0, s, a);
+  count_launch();
 }
 
 void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s) {

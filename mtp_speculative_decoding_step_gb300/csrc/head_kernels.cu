@@ -418,7 +418,8 @@ __device__ void gemv_finish(const GemvArgs& a, float (*s_out)[ROWS], int group, 
       bv = lane < nw ? sv[2 * lane] : -INFINITY;
       bi = lane < nw ? __float_as_int(sv[2 * lane + 1]) : 0x7FFFFFFF;
       warp_argmax(bv, bi);
-      if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[m]] = bi;
+      // an item whose logits are all NaN (flagged) still gets a token in range
+      if (lane == 0 && a.amax_out) a.amax_out[a.amax_idx[m]] = bi == 0x7FFFFFFF ? 0 : bi;
     }
   }
   if (tid == 0) {

@@ -159,6 +159,14 @@ struct TcGemvLaunch {
   float* out;
   long long ld_item, ld_split;
   int32_t* status;
+  // one split, out = the logits: the epilogue also clears item m's row of
+  // qzero (stride ldqz; or null) and leaves each tile's (max, index) per item
+  // in gmax / gidx[m * tiles + tile] for launch_tcv_argmax
+  int fuse_logits;
+  float* qzero;
+  long long ldqz;
+  float* gmax;
+  int* gidx;
 };
 bool launch_tc_gemv(const TcGemvLaunch& L, cudaStream_t s);
 // CTAs of the tensor-core GEMV with NI activation columns resident per SM
@@ -185,6 +193,9 @@ struct TcFinishArgs {
   long long ldqz;
 };
 void launch_tcv_finish(const TcFinishArgs& a, cudaStream_t s);
+// After a fused logits epilogue: amax_out[amax_idx[m]] = the argmax of item m
+// over its a.nout tile pairs in gmax / gidx (lowest index on ties).
+void launch_tcv_argmax(const TcFinishArgs& a, cudaStream_t s);
 
 // Decode attention of the head items over slots 0..slot (split over chunks).
 struct AttnArgs {

@@ -293,7 +293,7 @@ bool tc_layout(const GemvJob& j, TcGemvLaunch& L) {
 // prologue + hi/lo split, tcgen05 contraction, split sum + epilogue; passes of
 // at most kTcGemvMaxItems items.
 bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
-  TcGemvLaunch L;
+  TcGemvLaunch L = {};
   if (!tc_layout(j, L)) return false;
   const int tiles = (j.N + 127) / 128;
   for (int m0 = 0; m0 < M; m0 += kTcGemvMaxItems) {
@@ -313,11 +313,20 @@ bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     }
     launch_tcx_prep(p, s);
     const bool direct = ks == 1 && (j.epi == EPI_STORE || j.epi == EPI_LOGITS);
+    // one split of the logits: the contraction's own epilogue writes them,
+    // clears q and takes each tile's argmax (no pass that reads them back)
+    const bool fuse = direct && j.epi == EPI_LOGITS;
     float* y = j.y + (size_t)m0 * j.ldy;
+    float* qz = j.qzero ? j.qzero + (size_t)m0 * j.ldqz : nullptr;
     L.M = mp; L.NI = NI; L.ksplit = ks; L.X2 = h->x2; L.status = h->status;
     L.out = direct ? y : h->tvpart;
     L.ld_item = direct ? j.ldy : j.N;
     L.ld_split = (long long)mp * j.N;
+    L.fuse_logits = fuse ? 1 : 0;
+    L.qzero = fuse ? qz : nullptr;
+    L.ldqz = j.ldqz;
+    L.gmax = h->gmax;
+    L.gidx = h->gidx;
     if (!launch_tc_gemv(L, s)) return false;
     if (direct && j.epi == EPI_STORE) continue;
     TcFinishArgs f;
@@ -330,9 +339,14 @@ bool run_gemv_tc(mtp_handle* h, const GemvJob& j, int M, cudaStream_t s) {
     f.ldr = j.ldr;
     f.gmax = h->gmax; f.gidx = h->gidx; f.done = h->done; f.amax_out = j.amax_out; f.status = h->status;
     for (int m = 0; m < mp; ++m) f.amax_idx[m] = j.amax_idx ? j.amax_idx[m0 + m] : 0;
-    f.qzero = j.qzero ? j.qzero + (size_t)m0 * j.ldqz : nullptr;
+    f.qzero = qz;
     f.ldqz = j.ldqz;
-    launch_tcv_finish(f, s);
+    if (fuse) {
+      f.nout = tiles;  // the per-tile pairs
+      launch_tcv_argmax(f, s);
+    } else {
+      launch_tcv_finish(f, s);
+    }
   }
   return true;
 }
@@ -847,7 +861,9 @@ mtp_status mtp_load(const mtp_config* cfg, const mtp_tensor* tensors, int32_t n_
     if (st == MTP_OK) st = alloc(h, &h->tvpart, tvp);
     h->tc_gemv = st == MTP_OK;
   }
-  const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 255) / 256));
+  // per-group argmax pairs: 8 items of the CUDA-core head, or up to
+  // kTcGemvMaxItems items of the tensor-core head per 128-row tile
+  const size_t gslots = std::max((size_t)8 * h->lm_groups_max, (size_t)kTcGemvMaxItems * ((c.vocab + 127) / 128));
   if (st == MTP_OK) st = alloc(h, &h->gmax, gslots);
   if (st == MTP_OK) st = alloc(h, &h->gidx, gslots);
   if (st == MTP_OK) st = alloc(h, &h->counters, (size_t)groups);

@@ -148,3 +148,27 @@ def test_draft_reports_nonfinite_logits_in_the_handle_word():
     rig.draft(2, [1], tok, hid, [dict(temperature=0.0)])
     assert int(word.item()) & g.NONFINITE
     rig.close()
+
+
+def test_batched_draft_nonfinite_row_is_reported_and_others_unchanged():
+    # eight rows take the tensor-core head, whose lone-split logits epilogue
+    # takes each tile's argmax; a NaN in one row's newest hidden makes that
+    # row's logits NaN: the word reports it, its tokens stay in the
+    # vocabulary, and the other rows draft what they draft without it
+    s = synth.small_shape("bf16", vocab=4096)
+    R = 8
+    rig = g.Rig(s, seed=67, rows=R, capacity=256, prefill=[64] * R, max_depth=2)
+    word = g.device_i32(m.mtp_device_status(rig.h))
+    word.zero_()
+    tok, hid = rig.pairs([[5 + r] for r in range(R)], seed_tag="st:bdraft")
+    greedy = [dict(temperature=0.0)] * R
+    clean = np.array(rig.draft(2, [1] * R, tok, hid, greedy)["draft"])
+    assert int(word.item()) == 0
+    m.mtp_set_lengths(rig.h, [64] * R)
+    hid[3, 0, 17] = float("nan")
+    bad = np.array(rig.draft(2, [1] * R, tok, hid, greedy)["draft"])
+    assert int(word.item()) & g.NONFINITE
+    assert bad.min() >= 0 and bad.max() < s.vocab
+    keep = [r for r in range(R) if r != 3]
+    assert np.array_equal(bad[keep], clean[keep])
+    rig.close()
