@@ -21,9 +21,14 @@
 //                 the hi/lo split into X2[NI][K] (bf16, K-major)
 //   k_tc_gemv   : warp 0 lane 0 = TMA producer, warp 1 lane 0 = MMA issuer,
 //                 4 warps = epilogue (TMEM -> registers -> fp32 partials);
-//                 split-K CTAs write partials [split][item][row]
-//   k_tcv_finish: sums the splits in split order and applies the epilogue
-//                 (store, residual, SwiGLU, logits + two-level argmax)
+//                 split-K CTAs write partials [split][item][row]; with one
+//                 split a store or logits job is written in place, and the
+//                 logits epilogue (q cleared, each tile's argmax) runs here
+//   k_tcv_finish / k_tcv_logits: sum the splits in split order and apply
+//                 the epilogue (store, residual, SwiGLU, logits + two-level
+//                 argmax)
+//   k_tcv_argmax: after the in-place logits epilogue, the per-item argmax
+//                 over the tiles' pairs
 // Every mbarrier wait is bounded; on expiry the CTA raises the status word,
 // waits (bounded) for its own copies, frees its TMEM and returns.
 #include "kernels.h"
