@@ -2,8 +2,8 @@
 run their GEMVs on the tensor cores: the weights stream through TMA into
 tcgen05 MMAs and every activation row travels as a bf16 pair (x_hi = bf16(x),
 x_lo = bf16(x - x_hi)).  On a reduced bf16 head of the same family (H=512,
-8/2 heads x 128, SwiGLU 1536, vocab 4096, and 65536 for a head of more row
-tiles than resident CTAs), batches of 8 and 20 rows with
+8/2 heads x 128, SwiGLU 1536, vocab 4096; 65536 for a head of more row
+tiles than resident CTAs, 4032 for a partial last tile), batches of 8 and 20 rows with
 ragged pending pairs (one pass of up to 64 items, and two passes) are compared
 with the oracle: logits, the drafter's hidden state and the new KV slots
 within 1e-2 of the largest magnitude (bf16 weights and cache), drafted tokens
@@ -69,6 +69,14 @@ def test_batch_of_8_rows_wide_vocabulary():
     R = 8
     params = [dict(temperature=0.0) if r % 2 == 0 else dict(temperature=0.9, top_k=40) for r in range(R)]
     _run(R, [1, 2, 1, 3, 1, 2, 1, 1], 2, params, seed=73, S=synth.small_shape("bf16", vocab=65536))
+
+
+def test_batch_of_8_rows_partial_last_tile():
+    # vocab 4032: the head's last 128-row tile holds 64 rows, so the in-place
+    # logits epilogue's writes and per-tile argmax meet rows past the vocabulary
+    R = 8
+    params = [dict(temperature=0.0) if r % 2 == 0 else dict(temperature=0.9, top_k=40) for r in range(R)]
+    _run(R, [1, 2, 1, 3, 1, 2, 1, 1], 2, params, seed=79, S=synth.small_shape("bf16", vocab=4032))
 
 
 def test_batch_of_20_rows_two_passes():
