@@ -143,6 +143,39 @@ def test_fc_concat_order_norms_and_tied_head():
         np.testing.assert_allclose(lg, E.astype(np.float64) @ f, rtol=1e-5, atol=1e-5)
 
 
+def _hidden_only_head(s):
+    """fc = [0 | I], every other block zero, unit norm weights: h2 = h0 =
+    RMSNorm_h(hidden), so the step exposes the oracle's RMSNorm alone."""
+    t = _structured(s)
+    fc = np.zeros((s.hidden, 2 * s.hidden), np.float32)
+    fc[:, s.hidden:] = np.eye(s.hidden)
+    t["mtp.fc.weight"] = fc
+    return oracle.Head(s, t, np.zeros((s.vocab, s.hidden), np.float32))
+
+
+def test_rmsnorm_closed_forms():
+    # "Upstream contract to port", module shape: nn.RMSNorm(hidden_size, eps).
+    # With every |x_i| = 1 the mean square is 1, so with eps = 1 the norm is
+    # x / sqrt(2) exactly; eps outside the root would give x / 2 and a sum in
+    # place of the mean x / sqrt(H + 1).
+    s = _tiny_shape(eps=1.0)
+    h = _hidden_only_head(s)
+    sign = np.where(np.arange(s.hidden) % 3 == 0, -1.0, 1.0).astype(np.float32)
+    K, V = _cache(s, 2)
+    h2, _ = h.step(0, sign, K, V, 0)
+    np.testing.assert_allclose(h2, sign / math.sqrt(2.0), rtol=1e-7, atol=0)
+    # with a negligible eps the output has unit root mean square whatever the
+    # input's scale, and scaling the input leaves it unchanged
+    s = _tiny_shape(H=16, dh=8, I=16, eps=1e-12)
+    h = _hidden_only_head(s)
+    x = np.random.default_rng(5).normal(0, 3.0, s.hidden).astype(np.float32)
+    K, V = _cache(s, 2)
+    a, _ = h.step(0, x, K, V, 0)
+    b, _ = h.step(0, (40.0 * x).astype(np.float32), K, V, 0)
+    assert abs(math.sqrt(float(np.mean(np.asarray(a, np.float64) ** 2))) - 1.0) < 1e-6
+    np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-6)
+
+
 def _qk_probe(s, slot, which):
     """Head whose k (pre-norm) is sqrt(H) * e_which: hid one-hot -> h0 = sqrt(H) e_0."""
     t = _structured(s)
