@@ -7,7 +7,7 @@ import math
 
 import numpy as np
 import pytest
-from scipy.special import softmax
+from scipy.special import expit, softmax
 
 import oracle
 import synth
@@ -288,7 +288,13 @@ def test_swiglu_mlp_closed_form():
     h1 = _rms(hid, 1.0, s.eps)
     c = _rms(h1, 1.0, s.eps)
     g = 1.5 * c
-    np.testing.assert_allclose(h2, h1 + (g / (1 + np.exp(-g))) * (-0.5 * c), rtol=1e-5, atol=1e-6)
+    # silu from scipy's logistic function (the oracle has its own exp)
+    np.testing.assert_allclose(h2, h1 + (g * expit(g)) * (-0.5 * c), rtol=1e-5, atol=1e-6)
+    # and the gate's sign matters: silu is not odd (silu(-g) = silu(g) - g)
+    t["mtp.layers.0.mlp.gate_proj.weight"] = -1.5 * np.eye(8, dtype=np.float32)
+    h = oracle.Head(s, t, np.zeros((s.vocab, 8), np.float32))
+    h2n, _ = h.step(0, hid, K, V, 0)
+    np.testing.assert_allclose(h2n - h1, ((g * expit(g)) - g) * (-0.5 * c), rtol=1e-5, atol=1e-6)
 
 
 def test_flush_is_batch_order_independent_and_matches_full_steps():
