@@ -103,6 +103,7 @@ def _load():
         lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_quantize_rows_e4m3.argtypes = [vp, ci, ci, vp, vp]
+        lib.orc_bf16_round.argtypes = [vp, ctypes.c_long, vp]
         lib.orc_set_threads.argtypes = [ci]
         lib.orc_threads.restype = ci
         _lib = lib
@@ -116,6 +117,15 @@ def set_threads(n: int) -> None:
 
 def threads() -> int:
     return int(_load().orc_threads())
+
+
+def bf16_round_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp32 values under the oracle's rounding:
+    nearest even, NaN kept a NaN."""
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    out = np.zeros(x.shape, np.uint16)
+    _load().orc_bf16_round(x.ctypes.data, x.size, out.ctypes.data)
+    return out
 
 
 def e4m3_encode(x: float) -> int:

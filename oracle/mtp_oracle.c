@@ -49,11 +49,20 @@ static inline double bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
+/* fp32 -> bf16 bits, round to nearest even; a NaN stays a quiet NaN (the
+   rounding add would carry an all-ones payload into the sign bit) */
 static inline uint16_t float_to_bf16(float f) {
   uint32_t u;
   memcpy(&u, &f, 4);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+
+/* the oracle's bf16 rounding over n values (the rounding the bf16 KV cache
+   stores with), exposed so that it can be pinned */
+void orc_bf16_round(const float* x, long n, uint16_t* out) {
+  for (long i = 0; i < n; ++i) out[i] = float_to_bf16(x[i]);
 }
 
 /* element i of a weight/KV/hidden array stored as fp32 (dt=0) or bf16 (dt=1) */

@@ -509,6 +509,27 @@ def test_verify_bonus_comes_from_last_row_when_all_accepted():
 
 
 # ------------------------------------------------------------ fp8 draft head
+def test_bf16_rounding_matches_torch():
+    # bf16 weights and KV cache (the drafter is published in bf16, "Where the
+    # MTP weights actually live"): the oracle's fp32 -> bf16 rounding against
+    # PyTorch's conversion: random values, exact ties (both directions of
+    # round-half-even), overflow to infinity, subnormals, signed zeros and
+    # infinities; NaN inputs (with any payload) must stay NaN
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    base = [rng.normal(0, 1, 4000), rng.normal(0, 1e-3, 1000), rng.normal(0, 1e30, 1000)]
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 2 + 2.0 ** -7, 1 + 2.0 ** -8 + 2.0 ** -20])
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 3.4028235e38, -3.4028235e38, 1e-40, -1e-40, 1.17549435e-38,
+                        3.3895314e38, 3.3961775e38])
+    x = np.concatenate(base + [ties, special]).astype(np.float32)
+    got = oracle.bf16_round_bits(x)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, want)
+    nans = np.array([0x7FC00000, 0x7FFFFFFF, 0xFFFFFFFF, 0x7F800001, 0xFFC00000], np.uint32).view(np.float32)
+    b = oracle.bf16_round_bits(nans)
+    assert np.all((b & 0x7F80) == 0x7F80) and np.all((b & 0x007F) != 0)
+
+
 def test_e4m3_codes_match_torch_float8():
     """The oracle's e4m3 encoder against torch's float8_e4m3fn conversion
     (round to nearest even) on normals, subnormals, ties and the top of the
