@@ -53,6 +53,17 @@ WORKLOAD = ("27B-shaped MTP head (H=5120, 24q/4kv x 256, SwiGLU 17408, V=152064)
             "batch 1, greedy, depth 2 (block 3), draft KV 4096")
 
 
+def step_bytes_of(s, kv_len: int):
+    """Algorithmic bytes of one batch-1 draft step of a bf16 head, read once:
+    (layer weights: fc, q/k/v, o, gate/up/down; the tied lm_head with its
+    fp32 logits row and the final norm row; K and V at kv_len positions)."""
+    H, qw, kw, inter = s.hidden, s.n_q * s.head_dim, s.n_kv * s.head_dim, s.inter
+    layer = 2 * (H * 2 * H + (qw + 2 * kw) * H + H * qw + 3 * inter * H)
+    lm = s.vocab * H * 2 + s.vocab * 4 + H * 4
+    kv = 2 * kw * 2 * kv_len
+    return layer, lm, kv
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -359,15 +370,12 @@ def run_ours(args, rank, world, local_rank):
         if not clk_timed.get("samples"):
             clk["sm_mhz"], clk["sm_max_mhz"] = clk_after["sm_mhz"], clk_after["sm_max_mhz"]
 
-    H, Vocab = s.hidden, s.vocab
-    lm_bytes = Vocab * H * 2 + Vocab * 4 + H * 4
+    layer_bytes, lm_bytes, kv_bytes = step_bytes_of(s, KV_LEN)
     lm_ms, lm_n = prof["lm_head"]
     lm_avg_s = lm_ms / max(lm_n, 1) / 1e3
     peak, src = peaks()
     achieved = lm_bytes / lm_avg_s / 1e9
     breakdown = {k: round(v[0] / max(v[1], 1) * 1e3, 2) for k, v in prof_all.items() if v[1]}
-    layer_bytes = 2 * (H * 2 * H + (24 * 256 + 2 * 4 * 256) * H + H * 24 * 256 + 3 * 17408 * H)
-    kv_bytes = 2 * 4 * 256 * 2 * KV_LEN
     step_bytes = layer_bytes + lm_bytes + kv_bytes
     n_prof = max(prof_all["lm_head"][1] // DEPTH, 1)
     draft_ms = sum(v[0] for k, v in prof_all.items() if k not in ("rollback",)) / n_prof
@@ -412,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
         "flush_256_pairs": {"by_offset": flush, "flops": flush_flops, "weight_bytes": flush_bytes,
                             "bf16_peak_tflops": peak_bf16(), "bound": "tensor/hbm ridge"} if flush else None,
         "e2e": {"value": round(e2e_units / e2e_s, 2), "unit": "draft tok/s",
-                "h2d_bytes_per_step": (DEPTH + 1) * Vocab * 4 + (DEPTH + 1) * H * 2,
+                "h2d_bytes_per_step": (DEPTH + 1) * s.vocab * 4 + (DEPTH + 1) * s.hidden * 2,
                 "d2h_bytes_per_step": 4 * (DEPTH + 2)},
         "clocks": clk,
         "wall_s": round(wall, 3),
